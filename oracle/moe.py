@@ -1,0 +1,254 @@
+"""Plain fp64 statement of the sparse top-k MoE FFN forward pass (test infrastructure only).
+
+Pages cited (no page has a title of its own; each is named by its address):
+  csdn/6a919c0d  = devpress.csdn.net/awstech/6a919c0d2b83d06f0ec6f601.html
+  csdn/6a462027  = devpress.csdn.net/awstech/6a46202710ee7a33f285c5a4.html
+  csdn/6a462500  = devpress.csdn.net/awstech/6a46250010ee7a33f285d330.html
+  aicoding/6a320eef = aicoding.csdn.net/6a320eef10ee7a33f27e52b3.html
+
+Inputs are taken as their exact stored values (bf16 or fp32) upcast to fp64;
+nothing is rounded in between. Library primitives used as single steps: numpy
+matmul, numpy argmax, scipy's erf.
+
+Readings where the pages are silent or disagree (each listed in the design notes):
+  * inference routing is deterministic: no noise, temperature 1, no bias unless
+    the workload adds one (csdn/6a462027 §3.1 says Gumbel noise is training-only);
+  * top-k picks the k largest logits, the lower expert index winning a tie, and
+    records them in descending order (slot 0 = largest);
+  * the gate is the softmax probability itself, not renormalised over the k
+    chosen experts (csdn/6a919c0d §2.2 step 4; aicoding/6a320eef §3.2);
+  * the expert is d -> d_ff -> d with the erf form of GeLU and no biases
+    (csdn/6a462027 §3.2);
+  * within one expert, routed rows keep the row-major order of the (token, slot)
+    assignments (the pages only ask for "a scatter").
+"""
+from __future__ import annotations
+
+import math
+from typing import Mapping, Optional, Sequence, Union
+
+import numpy as np
+from scipy.special import erf
+
+ArrayLike = Union[np.ndarray, Sequence]
+
+
+def router_logits(x: np.ndarray, w_r: np.ndarray, b_r: Optional[np.ndarray] = None) -> np.ndarray:
+    """l[t, e] = sum_i x[t, i] * W_r[i, e] (+ b_r[e]).
+
+    The router is one linear layer over the token's hidden state with one output
+    per expert: csdn/6a919c0d §2.2 steps 1-2; aicoding/6a320eef §3.2 ("h x W_router",
+    W_router is d x E).
+    """
+    logits = np.asarray(x, np.float64) @ np.asarray(w_r, np.float64)
+    if b_r is not None:
+        logits = logits + np.asarray(b_r, np.float64)[None, :]
+    return logits
+
+
+def softmax(logits: np.ndarray) -> np.ndarray:
+    """p[t, e] = exp(l[t, e] - m_t) / sum_e' exp(l[t, e'] - m_t), m_t = max_e l[t, e].
+
+    Softmax over all E router outputs (aicoding/6a320eef §3.2 "Softmax(logits)"),
+    with the maximum subtracted first as csdn/6a919c0d §4.2 advises.
+    """
+    logits = np.asarray(logits, np.float64)
+    m = logits.max(axis=1, keepdims=True)
+    ex = np.exp(logits - m)
+    return ex / ex.sum(axis=1, keepdims=True)
+
+
+def topk_select(logits: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest logits per token, largest first, lower index first on ties.
+
+    Deterministic top-k (csdn/6a919c0d §2.2 step 3: take the two experts with the
+    highest confidence; csdn/6a462027 §3.1: deterministic at inference). Selecting
+    on logits equals selecting on softmax probabilities because softmax is
+    strictly increasing in each logit. Done as k rounds of "take the maximum and
+    strike it out"; numpy's argmax returns the first (lowest) index among equal
+    maxima, which is the tie rule.
+    """
+    work = np.array(logits, np.float64, copy=True)
+    T, E = work.shape
+    if not (1 <= k <= E):
+        raise ValueError("topk_select: need 1 <= k <= E")
+    idx = np.empty((T, k), np.int64)
+    rows = np.arange(T)
+    for j in range(k):
+        e = np.argmax(work, axis=1)
+        idx[:, j] = e
+        work[rows, e] = -np.inf
+    return idx
+
+
+def gates_of(p: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """gate[t, j] = p[t, idx[t, j]]: the chosen experts' softmax probabilities, not renormalised.
+
+    csdn/6a919c0d §2.2 step 4 (weights = each expert's confidence);
+    aicoding/6a320eef §3.2 (weights = the corresponding p values) and its §3.1
+    worked example (0.42 + 0.38 = 0.80).
+    """
+    return np.take_along_axis(np.asarray(p, np.float64), np.asarray(idx), axis=1)
+
+
+def gelu(z: np.ndarray) -> np.ndarray:
+    """GeLU(z) = z * Phi(z) = 0.5 * z * (1 + erf(z / sqrt(2))), the exact (erf) form.
+
+    csdn/6a462027 §3.2 (GELU experts) and §4.2 (F.gelu, whose default is the erf form).
+    """
+    z = np.asarray(z, np.float64)
+    return 0.5 * z * (1.0 + erf(z / math.sqrt(2.0)))
+
+
+def expert_ffn(x_rows: np.ndarray, w1_e: np.ndarray, w2_e: np.ndarray) -> np.ndarray:
+    """FFN_e(x) = GeLU(x W1_e) W2_e for a stack of token rows.
+
+    Each expert is the same d -> d_ff -> d two-layer MLP with its own W1 [d, d_ff]
+    and W2 [d_ff, d] (csdn/6a462027 §3.2; the stacked layout experts[E, d, d_ff]
+    is its §4.2 sketch). Row r of the result depends on row r of x_rows only.
+    """
+    h = gelu(np.asarray(x_rows, np.float64) @ np.asarray(w1_e, np.float64))
+    return h @ np.asarray(w2_e, np.float64)
+
+
+def forward(x: np.ndarray, w_r: np.ndarray, w1: Union[np.ndarray, Mapping], w2: Union[np.ndarray, Mapping],
+            k: int, b_r: Optional[np.ndarray] = None) -> dict:
+    """Forward pass of the layer for the tokens in x.
+
+    out[t] = sum_{j=0..k-1} gate[t, j] * FFN_{idx[t, j]}(x[t]), summed in slot order.
+
+    The routed tokens go only to their k experts (csdn/6a919c0d §2.2 steps 3-4;
+    csdn/6a462027 §4.2 steps 4-7: route, run only the selected experts, sum the
+    outputs weighted by the probabilities). ``w1[e]`` / ``w2[e]`` may be arrays
+    or any mapping that yields expert e's matrices; only routed experts are read.
+    Returns the output and every routing intermediate.
+    """
+    x = np.asarray(x, np.float64)
+    T, d = x.shape
+    logits = router_logits(x, w_r, b_r)
+    p = softmax(logits)
+    idx = topk_select(logits, k)
+    gate = gates_of(p, idx)
+    y = np.zeros((k, T, d), np.float64)
+    for j in range(k):
+        for e in np.unique(idx[:, j]):
+            rows = np.nonzero(idx[:, j] == e)[0]
+            y[j, rows] = expert_ffn(x[rows], w1[int(e)], w2[int(e)])
+    out = np.zeros((T, d), np.float64)
+    for j in range(k):
+        out = out + gate[:, j:j + 1] * y[j]
+    return {"out": out, "idx": idx, "gate": gate, "p": p, "logits": logits, "y": y}
+
+
+def dense_forward(x: np.ndarray, w_r: np.ndarray, w1, w2, k: int, b_r: Optional[np.ndarray] = None) -> np.ndarray:
+    """Brute force: evaluate all E experts on every token and weight them by mask_topk * p.
+
+    The mask is the rank definition of top-k, independent of ``topk_select``:
+    expert e is kept for token t when fewer than k experts beat it, where e' beats
+    e if l[t, e'] > l[t, e], or l[t, e'] == l[t, e] and e' < e. Experts are summed
+    in ascending index order.
+    """
+    x = np.asarray(x, np.float64)
+    logits = router_logits(x, w_r, b_r)
+    p = softmax(logits)
+    T, E = logits.shape
+    out = np.zeros_like(x)
+    for e in range(E):
+        le = logits[:, e:e + 1]
+        beats = (logits > le) | ((logits == le) & (np.arange(E)[None, :] < e))
+        keep = (beats.sum(axis=1) < k).astype(np.float64)
+        out = out + (keep * p[:, e])[:, None] * expert_ffn(x, w1[e], w2[e])
+    return out
+
+
+def dispatch(idx: np.ndarray, E: int, gate: Optional[np.ndarray] = None) -> dict:
+    """Per-expert histogram, exclusive scan and stable permutation of the T*k assignments.
+
+    counts[e] = #{(t, j) : idx[t, j] == e}; offsets = exclusive scan of counts
+    (offsets[E] = T*k); the row of assignment (t, j) is offsets[e] plus the number
+    of earlier assignments, in row-major (t, j) order, routed to the same e.
+    perm_token[row] = t and row_gate[row] = gate[t, j] invert that map. This is
+    the "scatter" of csdn/6a462027 §4.2 step 5 (group each expert's tokens), done
+    as a counting sort.
+    """
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    counts = np.zeros(E, np.int64)
+    for t in range(T):
+        for j in range(k):
+            counts[idx[t, j]] += 1
+    offsets = np.zeros(E + 1, np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + counts[e]
+    seen = np.zeros(E, np.int64)
+    row_of = np.empty((T, k), np.int64)
+    perm_token = np.empty(T * k, np.int64)
+    row_gate = np.zeros(T * k, np.float64)
+    for t in range(T):
+        for j in range(k):
+            e = idx[t, j]
+            r = offsets[e] + seen[e]
+            seen[e] += 1
+            row_of[t, j] = r
+            perm_token[r] = t
+            if gate is not None:
+                row_gate[r] = gate[t, j]
+    return {"counts": counts, "offsets": offsets, "row_of": row_of, "perm_token": perm_token,
+            "row_gate": row_gate}
+
+
+def expert_rows_ffn(x_perm: np.ndarray, offsets: np.ndarray, row_gate: np.ndarray, w1, w2,
+                    rows: Optional[np.ndarray] = None) -> np.ndarray:
+    """y_perm[r] = row_gate[r] * FFN_e(x_perm[r]) for the expert e whose range [offsets[e], offsets[e+1]) holds r.
+
+    The per-expert FFN over only the routed rows (csdn/6a462027 §4.2 step 6, "in
+    practice a grouped GEMM") with the gate applied to the expert's output
+    (csdn/6a919c0d §2.2 step 4). ``rows`` restricts the evaluation to some rows.
+    """
+    x_perm = np.asarray(x_perm, np.float64)
+    offsets = np.asarray(offsets)
+    A = x_perm.shape[0]
+    rows = np.arange(A) if rows is None else np.asarray(rows)
+    expert_of_row = np.searchsorted(offsets, rows, side="right") - 1
+    y = np.zeros((len(rows), x_perm.shape[1]), np.float64)
+    for e in np.unique(expert_of_row):
+        sel = np.nonzero(expert_of_row == e)[0]
+        y[sel] = np.asarray(row_gate, np.float64)[rows[sel], None] * expert_ffn(x_perm[rows[sel]], w1[int(e)], w2[int(e)])
+    return y
+
+
+def combine(y_perm: np.ndarray, row_of: np.ndarray) -> np.ndarray:
+    """out[t] = sum_{j=0..k-1} y_perm[row_of[t, j]], summed in slot order.
+
+    The weighted sum of the k expert outputs (csdn/6a462027 §4.2 step 7,
+    "scatter_add"); the weights were already applied per row.
+    """
+    y_perm = np.asarray(y_perm, np.float64)
+    row_of = np.asarray(row_of)
+    T, k = row_of.shape
+    out = np.zeros((T, y_perm.shape[1]), np.float64)
+    for j in range(k):
+        out = out + y_perm[row_of[:, j]]
+    return out
+
+
+def ambiguous_tokens(logits: np.ndarray, k: int, min_gap: float) -> np.ndarray:
+    """Tokens whose top-(k+1) logits (top-k when E == k) have an adjacent gap below min_gap.
+
+    Used by the input recipe to re-draw such tokens so that every routing index
+    is decided by a margin far above fp32 rounding of the logits.
+    """
+    logits = np.asarray(logits, np.float64)
+    T, E = logits.shape
+    m = min(k + 1, E)
+    top = -np.sort(-logits, axis=1)[:, :m]
+    if m < 2:
+        return np.zeros(0, np.int64)
+    gaps = top[:, :-1] - top[:, 1:]
+    return np.nonzero((gaps < min_gap).any(axis=1))[0]
+
+
+def top_share(counts: np.ndarray, n: int) -> float:
+    """Fraction of all assignments taken by the n most-loaded experts."""
+    c = np.sort(np.asarray(counts, np.int64))[::-1]
+    return float(c[:n].sum()) / float(c.sum())

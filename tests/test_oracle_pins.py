@@ -1,0 +1,343 @@
+"""Pins of the fp64 oracle against facts fixed outside it.
+
+Each pin ties one oracle function to something other than itself: a worked
+example printed on the pages, a closed form, a library routine for a special
+case that reduces to it, or brute force on tiny inputs. ``test_planted_mistakes``
+shows that a plausible mistake planted anywhere in the oracle fails at least one
+pin.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from oracle import moe as om
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rand_layer(rng, T, d, F, E, scale_r=1.0):
+    x = rng.standard_normal((T, d))
+    w_r = rng.standard_normal((d, E)) * scale_r / math.sqrt(d)
+    w1 = rng.standard_normal((E, d, F)) / math.sqrt(d)
+    w2 = rng.standard_normal((E, F, d)) / math.sqrt(F)
+    return x, w_r, w1, w2
+
+
+# ----------------------------------------------------------------------------- pin checks
+# Each check raises AssertionError on failure. They look oracle functions up on the
+# module at call time, so test_planted_mistakes can swap one out.
+
+def check_worked_example():
+    """aicoding/6a320eef §3.1: probabilities 0.42/0.38/0.12/0.05/(<0.01) -> experts 3 and 17, gates sum 0.80."""
+    g = _load("router_worked_example.json")
+    E = g["E"]
+    named = {int(e): p for e, p in g["named_probs"].items()}
+    rest = (1.0 - sum(named.values())) / (E - len(named))
+    assert rest < g["others_below"]
+    p_true = np.full(E, rest)
+    for e, p in named.items():
+        p_true[e] = p
+    # One token whose hidden state is the first unit vector: its logits are row 0 of W_r.
+    d = 4
+    x = np.zeros((1, d)); x[0, 0] = 1.0
+    w_r = np.zeros((d, E)); w_r[0] = np.log(p_true) + 3.0   # any common shift
+    logits = om.router_logits(x, w_r)
+    p = om.softmax(logits)
+    idx = om.topk_select(logits, 2)
+    gate = om.gates_of(p, idx)
+    assert list(idx[0]) == g["expected_top2"]
+    assert np.allclose(gate[0], g["expected_gates"], rtol=0, atol=1e-12)
+    assert abs(gate[0].sum() - g["expected_gate_sum"]) < 1e-12
+    assert np.allclose(p[0], p_true, rtol=1e-12, atol=0)
+
+
+def check_router_closed_form():
+    """Zero hidden state gives logits = bias; a unit vector e_i gives row i of W_r plus bias."""
+    rng = np.random.default_rng(1)
+    d, E = 6, 5
+    w_r = rng.standard_normal((d, E))
+    b_r = rng.standard_normal(E)
+    x = np.zeros((d + 1, d))
+    for i in range(d):
+        x[i + 1, i] = 1.0
+    logits = om.router_logits(x, w_r, b_r)
+    assert np.array_equal(logits[0], b_r)
+    for i in range(d):
+        assert np.allclose(logits[i + 1], w_r[i] + b_r, rtol=0, atol=1e-15)
+
+
+def check_softmax_library():
+    """Softmax equals scipy's, sums to one, and is shift invariant."""
+    rng = np.random.default_rng(2)
+    l = rng.standard_normal((7, 13)) * 5
+    p = om.softmax(l)
+    assert np.allclose(p, scipy.special.softmax(l, axis=1), rtol=1e-13, atol=0)
+    assert np.allclose(p.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    assert np.allclose(om.softmax(l + 1000.0), p, rtol=1e-12, atol=0)
+
+
+def check_topk_ties_and_order():
+    """Largest first; equal logits go to the lower index; matches torch.topk where there are no ties."""
+    l = np.array([[1.0, 3.0, 3.0, 2.0],
+                  [5.0, 5.0, 5.0, 5.0],
+                  [0.0, -1.0, 2.0, 2.0]])
+    assert om.topk_select(l, 2).tolist() == [[1, 2], [0, 1], [2, 3]]
+    assert om.topk_select(l, 3).tolist() == [[1, 2, 3], [0, 1, 2], [2, 3, 0]]
+    rng = np.random.default_rng(3)
+    l = rng.standard_normal((50, 9))
+    ref = torch.topk(torch.from_numpy(l), 3, dim=1).indices.numpy()
+    assert np.array_equal(om.topk_select(l, 3), ref)
+
+
+def check_gelu_closed_form():
+    """GeLU(z) = z*Phi(z): GeLU(0) = 0, GeLU(1) = Phi(1), GeLU(-1) = -(1 - Phi(1)), -> z and 0 in the tails; matches torch's erf GeLU."""
+    facts = _load("page_facts.json")["gelu_closed_form"]
+    phi1 = facts["phi_1"]
+    g = om.gelu(np.array([0.0, 1.0, -1.0, 12.0, -12.0]))
+    assert g[0] == 0.0
+    assert abs(g[1] - phi1) < 1e-15
+    assert abs(g[2] + (1.0 - phi1)) < 1e-15
+    assert abs(g[3] - 12.0) < 1e-15 and abs(g[4]) < 1e-30
+    z = np.linspace(-6, 6, 1001)
+    ref = torch.nn.functional.gelu(torch.from_numpy(z), approximate="none").numpy()
+    # 1 + erf(z/sqrt 2) cancels for z < 0, so compare absolutely (the tanh form differs by ~1e-3)
+    assert np.max(np.abs(om.gelu(z) - ref)) < 1e-14
+
+
+def check_single_expert_is_mlp():
+    """k = E = 1: the layer is the plain two-layer GeLU MLP (gate = 1), computed here with torch."""
+    rng = np.random.default_rng(4)
+    x, w_r, w1, w2 = _rand_layer(rng, T=5, d=6, F=6, E=1)
+    w1[0] = rng.standard_normal((6, 6))   # asymmetric square matrices: a transposed operand shows
+    res = om.forward(x, w_r, w1, w2, k=1)
+    tx = torch.from_numpy(x)
+    ref = torch.nn.functional.gelu(tx @ torch.from_numpy(w1[0]), approximate="none") @ torch.from_numpy(w2[0])
+    assert np.allclose(res["gate"], 1.0, rtol=0, atol=0)
+    assert np.allclose(res["out"], ref.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def check_k_equals_E_is_softmax_mixture():
+    """k = E: every expert is used and the layer is the dense softmax mixture sum_e p_e FFN_e(x) (torch einsum)."""
+    rng = np.random.default_rng(5)
+    x, w_r, w1, w2 = _rand_layer(rng, T=9, d=5, F=7, E=3)
+    res = om.forward(x, w_r, w1, w2, k=3)
+    tx = torch.from_numpy(x)
+    p = torch.softmax(tx @ torch.from_numpy(w_r), dim=1)
+    h = torch.nn.functional.gelu(torch.einsum("td,edf->etf", tx, torch.from_numpy(w1)), approximate="none")
+    y = torch.einsum("etf,efd->etd", h, torch.from_numpy(w2))
+    ref = torch.einsum("te,etd->td", p, y)
+    assert np.allclose(res["out"], ref.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def check_routed_equals_dense_bruteforce():
+    """The routed forward equals the brute-force all-experts evaluation masked to the top-k (to 1e-12 relative)."""
+    rng = np.random.default_rng(6)
+    for (T, d, F, E, k) in [(16, 8, 12, 8, 2), (11, 16, 16, 3, 2), (7, 4, 5, 2, 1), (13, 6, 9, 8, 8), (3, 8, 8, 5, 3)]:
+        x, w_r, w1, w2 = _rand_layer(rng, T, d, F, E)
+        b_r = rng.standard_normal(E) * 0.3
+        routed = om.forward(x, w_r, w1, w2, k, b_r)["out"]
+        dense = om.dense_forward(x, w_r, w1, w2, k, b_r)
+        rms = math.sqrt(float(np.mean(dense ** 2)))
+        assert np.max(np.abs(routed - dense)) / rms < 1e-12
+
+
+def check_routing_invariants():
+    """Exactly k distinct experts per token; gates are the softmax probabilities, non-increasing by slot, summing to <= 1 (< 1 when E > k)."""
+    rng = np.random.default_rng(7)
+    for (E, k) in [(8, 2), (128, 2), (4, 4), (16, 3)]:
+        l = rng.standard_normal((200, E))
+        p = om.softmax(l)
+        idx = om.topk_select(l, k)
+        gate = om.gates_of(p, idx)
+        assert all(len(set(r)) == k for r in idx.tolist())
+        assert np.array_equal(gate, p[np.arange(200)[:, None], idx])
+        assert np.all(np.diff(gate, axis=1) <= 0)
+        s = gate.sum(axis=1)
+        assert np.all(s <= 1.0 + 1e-15)
+        if E > k:
+            assert np.all(s < 1.0)
+
+
+def check_activation_fraction():
+    """csdn/6a919c0d §2.2: top-2 of 128 experts activates 2/128 = 1.5625% of them for every token."""
+    f = _load("page_facts.json")["activation_fraction"]
+    rng = np.random.default_rng(8)
+    l = rng.standard_normal((300, f["E"]))
+    idx = om.topk_select(l, f["k"])
+    counts = om.dispatch(idx, f["E"])["counts"]
+    assert counts.sum() == 300 * f["k"]
+    assert counts.sum() / (300 * f["E"]) == f["fraction"]
+
+
+def check_dispatch_stable_sort():
+    """The permutation equals numpy's stable argsort of the assignments by expert; counts and offsets match bincount/cumsum."""
+    rng = np.random.default_rng(9)
+    for (T, k, E) in [(40, 2, 7), (1, 2, 3), (100, 3, 16), (64, 2, 2)]:
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+        gate = rng.random((T, k))
+        dp = om.dispatch(idx, E, gate)
+        flat = idx.reshape(-1)
+        order = np.argsort(flat, kind="stable")
+        assert np.array_equal(dp["perm_token"], order // k)
+        inv = np.empty_like(order); inv[order] = np.arange(T * k)
+        assert np.array_equal(dp["row_of"].reshape(-1), inv)
+        assert np.array_equal(dp["counts"], np.bincount(flat, minlength=E))
+        assert np.array_equal(dp["offsets"], np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=E))]))
+        assert np.array_equal(dp["row_gate"], gate.reshape(-1)[order])
+
+
+def check_steps_compose_to_forward():
+    """Dispatch -> per-row expert FFN with gate -> combine reproduces the forward pass."""
+    rng = np.random.default_rng(10)
+    x, w_r, w1, w2 = _rand_layer(rng, T=21, d=8, F=10, E=5)
+    res = om.forward(x, w_r, w1, w2, k=2)
+    dp = om.dispatch(res["idx"], 5, res["gate"])
+    y_perm = om.expert_rows_ffn(x[dp["perm_token"]], dp["offsets"], dp["row_gate"], w1, w2)
+    out = om.combine(y_perm, dp["row_of"])
+    assert np.allclose(out, res["out"], rtol=1e-13, atol=1e-14)
+    rows = np.array([0, 5, 17, 41])
+    part = om.expert_rows_ffn(x[dp["perm_token"]], dp["offsets"], dp["row_gate"], w1, w2, rows=rows)
+    assert np.allclose(part, y_perm[rows], rtol=1e-13, atol=1e-15)
+
+
+def check_ambiguous_tokens():
+    """Tokens with a top-(k+1) adjacent gap below the threshold are flagged, others are not."""
+    l = np.array([[3.0, 2.0, 1.0, 0.0],
+                  [3.0, 3.0 - 5e-4, 1.0, 0.0],
+                  [3.0, 2.0, 2.0 - 5e-4, 0.0],
+                  [3.0, 2.0, 1.0, 1.0 - 5e-4],
+                  [3.0, 2.0, 2.0 - 2e-3, 0.0]])
+    assert om.ambiguous_tokens(l, 2, 1e-3).tolist() == [1, 2]
+
+
+PINS = [check_worked_example, check_router_closed_form, check_softmax_library, check_topk_ties_and_order,
+        check_gelu_closed_form, check_single_expert_is_mlp, check_k_equals_E_is_softmax_mixture,
+        check_routed_equals_dense_bruteforce, check_routing_invariants, check_activation_fraction,
+        check_dispatch_stable_sort, check_steps_compose_to_forward, check_ambiguous_tokens]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin()
+
+
+# ----------------------------------------------------------------------------- planted mistakes
+
+def _mut_gelu_sign(z):
+    z = np.asarray(z, np.float64)
+    return 0.5 * z * (1.0 - scipy.special.erf(z / math.sqrt(2.0)))
+
+
+def _mut_gelu_tanh(z):
+    z = np.asarray(z, np.float64)
+    return 0.5 * z * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (z + 0.044715 * z ** 3)))
+
+
+def _mut_softmax_unnormalised(l):
+    l = np.asarray(l, np.float64)
+    return np.exp(l - l.max(axis=1, keepdims=True))
+
+
+def _mut_topk_smallest(l, k):
+    return np.argsort(np.asarray(l), axis=1, kind="stable")[:, :k]
+
+
+def _mut_topk_last_on_tie(l, k):
+    l = np.asarray(l, np.float64)
+    E = l.shape[1]
+    rev = _ORIG_TOPK(l[:, ::-1], k)
+    return E - 1 - rev
+
+
+def _mut_gates_renormalised(p, idx):
+    g = np.take_along_axis(np.asarray(p), np.asarray(idx), axis=1)
+    return g / g.sum(axis=1, keepdims=True)
+
+
+def _mut_ffn_transposed_w1(x_rows, w1_e, w2_e):
+    return om.gelu(np.asarray(x_rows) @ np.asarray(w1_e).T) @ np.asarray(w2_e)
+
+
+def _mut_router_drops_bias(x, w_r, b_r=None):
+    return np.asarray(x, np.float64) @ np.asarray(w_r, np.float64)
+
+
+def _mut_dispatch_unstable(idx, E, gate=None):
+    res = _ORIG_DISPATCH(idx, E, gate)
+    # reverse the order of rows inside each expert's range
+    offs = res["offsets"]
+    row_of = res["row_of"].copy()
+    for t in range(row_of.shape[0]):
+        for j in range(row_of.shape[1]):
+            r = row_of[t, j]
+            e = np.searchsorted(offs, r, side="right") - 1
+            row_of[t, j] = offs[e] + offs[e + 1] - 1 - r
+    perm = np.empty_like(res["perm_token"])
+    for t in range(row_of.shape[0]):
+        for j in range(row_of.shape[1]):
+            perm[row_of[t, j]] = t
+    res = dict(res, row_of=row_of, perm_token=perm)
+    return res
+
+
+def _mut_combine_first_slot_twice(y_perm, row_of):
+    row_of = np.asarray(row_of).copy()
+    row_of[:, 1:] = row_of[:, :1]
+    return _ORIG_COMBINE(y_perm, row_of)
+
+
+def _mut_forward_drops_last_slot(x, w_r, w1, w2, k, b_r=None):
+    res = _ORIG_FORWARD(x, w_r, w1, w2, k, b_r)
+    res = dict(res)
+    res["out"] = res["out"] - res["gate"][:, -1:] * res["y"][-1] if k > 1 else res["out"]
+    return res
+
+
+_ORIG_DISPATCH = om.dispatch
+_ORIG_TOPK = om.topk_select
+_ORIG_COMBINE = om.combine
+_ORIG_FORWARD = om.forward
+
+MUTANTS = {
+    "gelu_sign": ("gelu", _mut_gelu_sign),
+    "gelu_tanh": ("gelu", _mut_gelu_tanh),
+    "softmax_unnormalised": ("softmax", _mut_softmax_unnormalised),
+    "topk_smallest": ("topk_select", _mut_topk_smallest),
+    "topk_last_on_tie": ("topk_select", _mut_topk_last_on_tie),
+    "gates_renormalised": ("gates_of", _mut_gates_renormalised),
+    "ffn_transposed_w1": ("expert_ffn", _mut_ffn_transposed_w1),
+    "router_drops_bias": ("router_logits", _mut_router_drops_bias),
+    "dispatch_unstable": ("dispatch", _mut_dispatch_unstable),
+    "combine_first_slot_twice": ("combine", _mut_combine_first_slot_twice),
+    "forward_drops_last_slot": ("forward", _mut_forward_drops_last_slot),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistakes(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(om, attr, fn)
+    failed = []
+    for pin in PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            failed.append(pin.__name__)
+    assert failed, f"planted mistake {name} was caught by no pin"
+
+
+def test_package_exports():
+    for name in ["router_logits", "softmax", "topk_select", "gates_of", "gelu", "expert_ffn", "forward",
+                 "dense_forward", "dispatch", "expert_rows_ffn", "combine", "ambiguous_tokens", "top_share"]:
+        assert callable(getattr(oracle, name))
