@@ -1,0 +1,186 @@
+/*
+ * moe.h — C ABI of the GB300 (sm_103a) sparse top-k Mixture-of-Experts FFN layer, forward pass.
+ *
+ * The layer, for T tokens x[T, d], E experts, top-k and expert width d_ff = F:
+ *   logits = x W_r (+ b_r), p = softmax(logits), the k largest logits pick the
+ *   experts (lower index wins a tie), gate = p of each chosen expert,
+ *   out[t] = sum_j gate[t, j] * W2_e (GeLU(W1_e x[t])) over the k chosen experts e.
+ *
+ * Pages (none has a title of its own; each is named by its address):
+ *   csdn/6a919c0d     devpress.csdn.net/awstech/6a919c0d2b83d06f0ec6f601.html
+ *   csdn/6a462027     devpress.csdn.net/awstech/6a46202710ee7a33f285c5a4.html
+ *   aicoding/6a320eef aicoding.csdn.net/6a320eef10ee7a33f27e52b3.html
+ *
+ * Conventions shared by every call
+ *  - All tensor pointers are DEVICE pointers, allocated and owned by the caller;
+ *    the library never allocates, frees or synchronises (moe_get_device_status
+ *    alone synchronises its stream). Tensors are dense row-major and 16-byte aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Every call only enqueues work on it and returns.
+ *  - Element type `dt`: MOE_DTYPE_F32 (x, W_r, W1, W2, out and the intermediates in
+ *    fp32) or MOE_DTYPE_BF16 (those tensors in bf16, accumulation in fp32).
+ *    Router bias, gates and row gates are always fp32; indices are int32.
+ *  - Limits: 0 <= T (T = 0 is a no-op), 1 <= k <= min(E, 8), E <= 1024,
+ *    d and F multiples of 8 and >= 8, T*k < 2^31, T*max(d,F) < 2^40.
+ *  - Host-side argument checks fail with MOE_ERR_INVALID_ARG before anything is
+ *    launched. A failed launch returns MOE_ERR_CUDA. Checks made on the device
+ *    (an expert index out of range, a wait that timed out) do not fault: they
+ *    record the first error in the workspace's status word, skip the offending
+ *    item, and are read back with moe_get_device_status.
+ *  - Workspace: caller-allocated device scratch of at least
+ *    moe_workspace_bytes(T, d, F, E, k, dt) bytes (one such block serves every
+ *    call with those sizes), 256-byte aligned, prepared once with
+ *    moe_workspace_init. Calls that share a workspace must not overlap in time.
+ *  - The library holds no global mutable state; distinct workspaces may be used
+ *    from distinct host threads.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* bad sizes, null pointer, misalignment, workspace too small */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid arguments this build has no kernel for (e.g. a path forced on the wrong dtype) */
+  MOE_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE_CHECK = 4,  /* a device-side range check failed (see moe_get_device_status) */
+  MOE_ERR_DEVICE_TIMEOUT = 5 /* a bounded device-side wait gave up */
+} moe_status;
+
+typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
+
+/* Kernel family for the expert FFN (a3, a4). AUTO picks TENSOR for bf16 with more than
+ * 256 routed rows, STREAM for bf16 with at most 256 routed rows, SIMT for fp32. */
+typedef enum {
+  MOE_PATH_AUTO = 0,
+  MOE_PATH_TENSOR = 1, /* tcgen05/TMEM grouped GEMM fed by TMA (bf16 only) */
+  MOE_PATH_STREAM = 2, /* weight-streaming column-slab kernel for few rows per expert (bf16 only) */
+  MOE_PATH_SIMT = 3    /* CUDA-core tiled grouped GEMM (fp32 and bf16) */
+} moe_path;
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_router_topk — router GEMM, softmax and deterministic top-k, fused, one warp per token.
+ *   csdn/6a919c0d §2.2 steps 1-4 (single linear router with one output per expert, softmax,
+ *   keep the k most confident experts, weights = their confidences); aicoding/6a320eef §3.2
+ *   (h x W_router, W_router is d x E; Softmax; top-2; weights = the p values); csdn/6a919c0d
+ *   §4.2 (stabilise with the maximum logit).
+ * In:  x [T, d] (dt), w_r [d, E] (dt), b_r [E] fp32 or NULL (added to the logits).
+ * Out: topk_idx [T, k] int32, topk_gate [T, k] fp32. Slot j holds the (j+1)-th largest logit;
+ *      equal logits go to the lower expert index. gate = softmax probability (fp32 logits,
+ *      fp32 softmax), not renormalised over the k experts.
+ * Errors: MOE_ERR_INVALID_ARG on bad sizes/pointers. No device-side checks.
+ */
+moe_status moe_router_topk(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
+                           moe_dtype dt, int32_t* topk_idx, float* topk_gate, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_dispatch — per-expert histogram, exclusive scan, stable permutation and row gather.
+ *   csdn/6a462027 §4.2 steps 4-5 (find the selected experts, scatter each expert's tokens to it).
+ * In:  x [T, d] (dt), topk_idx [T, k] int32, topk_gate [T, k] fp32.
+ * Out: counts [E] int32 (assignments per expert), offsets [E+1] int32 (exclusive scan,
+ *      offsets[E] = T*k), row_of [T, k] int32 (row of assignment (t, j)), perm_token [T*k] int32
+ *      (token of each row), row_gate [T*k] fp32 (gate of each row), x_perm [T*k, d] (dt, row r is
+ *      x[perm_token[r]]). Within an expert, rows follow row-major (t, j) order; every output is
+ *      exact (bit-reproducible).
+ * Workspace: status word and per-block count tables.
+ * Errors: an index outside [0, E) records MOE_ERR_DEVICE_CHECK (detail = flat assignment index)
+ *      and that assignment is dropped from every output (its row_of entry is -1).
+ */
+moe_status moe_dispatch(const void* x, const int32_t* topk_idx, const float* topk_gate, int T, int d, int E,
+                        int k, moe_dtype dt, int32_t* counts, int32_t* offsets, int32_t* perm_token,
+                        int32_t* row_of, float* row_gate, void* x_perm, void* workspace, size_t ws_bytes,
+                        void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_expert_up — grouped GEMM1 with the GeLU epilogue:  h[r, :] = GeLU(x_perm[r, :] W1[e])
+ * for every row r in expert e's range [offsets[e], offsets[e+1]).
+ *   csdn/6a462027 §3.2 (homogeneous d -> d_ff -> d GELU experts with their own W1, W2) and §4.2
+ *   step 6 ("in practice a grouped GEMM"); GeLU is the erf form.
+ * In:  x_perm [T*k, d] (dt), w1 [E, d, F] (dt, expert-major, row-major per expert), offsets [E+1].
+ * Out: h [T*k, F] (dt). bf16: fp32 accumulation, GeLU in fp32, one round-to-nearest-even.
+ * Workspace: status word.
+ */
+moe_status moe_expert_up(const void* x_perm, const void* w1, const int32_t* offsets, int T, int d, int F, int E,
+                         int k, moe_dtype dt, void* h, void* workspace, size_t ws_bytes, void* stream);
+moe_status moe_expert_up_ex(const void* x_perm, const void* w1, const int32_t* offsets, int T, int d, int F,
+                            int E, int k, moe_dtype dt, moe_path path, void* h, void* workspace, size_t ws_bytes,
+                            void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_expert_down — grouped GEMM2 with the gate epilogue:  y_perm[r, :] = row_gate[r] * (h[r, :] W2[e]).
+ *   csdn/6a919c0d §2.2 step 4 (each expert's output weighted by its confidence).
+ * In:  h [T*k, F] (dt), w2 [E, F, d] (dt), offsets [E+1], row_gate [T*k] fp32.
+ * Out: y_perm [T*k, d] (dt).
+ * Workspace: status word.
+ */
+moe_status moe_expert_down(const void* h, const void* w2, const int32_t* offsets, const float* row_gate, int T,
+                           int d, int F, int E, int k, moe_dtype dt, void* y_perm, void* workspace,
+                           size_t ws_bytes, void* stream);
+moe_status moe_expert_down_ex(const void* h, const void* w2, const int32_t* offsets, const float* row_gate,
+                              int T, int d, int F, int E, int k, moe_dtype dt, moe_path path, void* y_perm,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_grouped_ffn — moe_expert_up then moe_expert_down, with h kept in the workspace.
+ * In:  x_perm [T*k, d], w1 [E, d, F], w2 [E, F, d], offsets [E+1], row_gate [T*k].
+ * Out: y_perm [T*k, d] (dt).
+ */
+moe_status moe_grouped_ffn(const void* x_perm, const void* w1, const void* w2, const int32_t* offsets,
+                           const float* row_gate, int T, int d, int F, int E, int k, moe_dtype dt, void* y_perm,
+                           void* workspace, size_t ws_bytes, void* stream);
+moe_status moe_grouped_ffn_ex(const void* x_perm, const void* w1, const void* w2, const int32_t* offsets,
+                              const float* row_gate, int T, int d, int F, int E, int k, moe_dtype dt,
+                              moe_path path, void* y_perm, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_combine — out[t, :] = sum_{j = 0..k-1} y_perm[row_of[t, j], :], summed in fp32 in slot
+ * order j = 0, 1, ..., then rounded once to dt (round-to-nearest-even for bf16).
+ *   csdn/6a462027 §4.2 step 7 (sum the expert outputs back per token, "scatter_add").
+ * In:  y_perm [T*k, d] (dt), row_of [T, k] int32.  Out: out [T, d] (dt).
+ * A row_of entry outside [0, T*k) contributes nothing (dispatch writes -1 for a dropped item).
+ */
+moe_status moe_combine(const void* y_perm, const int32_t* row_of, int T, int d, int k, moe_dtype dt, void* out,
+                       void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_forward — the whole layer: router_topk, dispatch, expert_up, expert_down, combine.
+ * In:  x [T, d], w_r [d, E], b_r [E] or NULL, w1 [E, d, F], w2 [E, F, d].
+ * Out: out [T, d] (dt). topk_idx [T, k], topk_gate [T, k] and counts [E] are optional copies of
+ *      the routing (NULL: kept in the workspace only).
+ */
+moe_status moe_forward(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2, int T,
+                       int d, int F, int E, int k, moe_dtype dt, void* out, int32_t* topk_idx, float* topk_gate,
+                       int32_t* counts, void* workspace, size_t ws_bytes, void* stream);
+moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2,
+                          int T, int d, int F, int E, int k, moe_dtype dt, moe_path path, void* out,
+                          int32_t* topk_idx, float* topk_gate, int32_t* counts, void* workspace, size_t ws_bytes,
+                          void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Workspace and status.
+ * moe_workspace_bytes: bytes of workspace every call with these sizes needs (0 on bad sizes).
+ * moe_workspace_init:  clears the status word (async on `stream`); call once after allocating.
+ * moe_get_device_status: synchronises `stream`, returns and clears the first device-side error
+ *      recorded in the workspace (MOE_OK if none); *detail (nullable) receives its detail value.
+ * moe_status_string: static text for a status code.
+ */
+size_t moe_workspace_bytes(int T, int d, int F, int E, int k, moe_dtype dt);
+moe_status moe_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+moe_status moe_get_device_status(void* workspace, int32_t* detail, void* stream);
+const char* moe_status_string(moe_status s);
+
+/* Self-test of the bounded device wait every pipelined kernel uses: launches one CTA that waits
+ * on a barrier nothing will complete, gives up after timeout_us microseconds, records
+ * MOE_ERR_DEVICE_TIMEOUT in the workspace and returns; no fault, the context stays usable. */
+moe_status moe_selftest_wait_timeout(void* workspace, size_t ws_bytes, int timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -12,5 +12,5 @@ routines for the special cases, brute force on tiny inputs). There is no
 """
 from .moe import (  # noqa: F401
     router_logits, softmax, topk_select, gates_of, gelu, expert_ffn, forward, dense_forward,
-    dispatch, expert_rows_ffn, combine, ambiguous_tokens, top_share,
+    dispatch, expert_rows_ffn, expert_rows_up, expert_rows_down, combine, ambiguous_tokens, top_share,
 )

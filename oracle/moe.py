@@ -217,6 +217,47 @@ def expert_rows_ffn(x_perm: np.ndarray, offsets: np.ndarray, row_gate: np.ndarra
     return y
 
 
+def _expert_of_rows(offsets: np.ndarray, rows: np.ndarray) -> np.ndarray:
+    return np.searchsorted(np.asarray(offsets), rows, side="right") - 1
+
+
+def expert_rows_up(x_perm: np.ndarray, offsets: np.ndarray, w1, rows: Optional[np.ndarray] = None) -> np.ndarray:
+    """h[r] = GeLU(x_perm[r] W1_e) for the expert e whose range holds row r (first half of FFN_e).
+
+    csdn/6a462027 §3.2 (the d -> d_ff GELU layer of each expert).
+    """
+    x_perm = np.asarray(x_perm, np.float64)
+    rows = np.arange(x_perm.shape[0]) if rows is None else np.asarray(rows)
+    eo = _expert_of_rows(offsets, rows)
+    out = None
+    for e in np.unique(eo):
+        sel = np.nonzero(eo == e)[0]
+        h = gelu(x_perm[rows[sel]] @ np.asarray(w1[int(e)], np.float64))
+        if out is None:
+            out = np.zeros((len(rows), h.shape[1]), np.float64)
+        out[sel] = h
+    return out if out is not None else np.zeros((0, 0))
+
+
+def expert_rows_down(h: np.ndarray, offsets: np.ndarray, row_gate: np.ndarray, w2,
+                     rows: Optional[np.ndarray] = None) -> np.ndarray:
+    """y_perm[r] = row_gate[r] * (h[r] W2_e) (second half of FFN_e, weighted by the gate).
+
+    csdn/6a462027 §3.2 (the d_ff -> d layer); csdn/6a919c0d §2.2 step 4 (weight = confidence).
+    """
+    h = np.asarray(h, np.float64)
+    rows = np.arange(h.shape[0]) if rows is None else np.asarray(rows)
+    eo = _expert_of_rows(offsets, rows)
+    out = None
+    for e in np.unique(eo):
+        sel = np.nonzero(eo == e)[0]
+        y = np.asarray(row_gate, np.float64)[rows[sel], None] * (h[rows[sel]] @ np.asarray(w2[int(e)], np.float64))
+        if out is None:
+            out = np.zeros((len(rows), y.shape[1]), np.float64)
+        out[sel] = y
+    return out if out is not None else np.zeros((0, 0))
+
+
 def combine(y_perm: np.ndarray, row_of: np.ndarray) -> np.ndarray:
     """out[t] = sum_{j=0..k-1} y_perm[row_of[t, j]], summed in slot order.
 

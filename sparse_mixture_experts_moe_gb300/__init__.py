@@ -1,0 +1,65 @@
+"""GB300 (sm_103a) sparse top-k Mixture-of-Experts FFN layer, forward pass.
+
+The layer runs in hand-written CUDA kernels behind the C ABI of include/moe.h
+(libmoe.so, built in-tree). PyTorch only provides device memory and streams.
+
+    layer = MoELayer(w_r, w1, w2, k=2)          # weights: CUDA tensors, bf16 or fp32
+    out = layer(x)                              # x: [T, d] CUDA tensor
+
+Weights layout: w_r [d, E], w1 [E, d, d_ff], w2 [E, d_ff, d], optional fp32 router bias b_r [E].
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+from . import _lib
+from ._lib import (  # noqa: F401
+    MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK, MOE_ERR_DEVICE_TIMEOUT,
+    MOE_DTYPE_F32, MOE_DTYPE_BF16, PATH_AUTO, PATH_TENSOR, PATH_STREAM, PATH_SIMT, MoeError,
+    router_topk, dispatch, expert_up, expert_down, grouped_ffn, combine, forward, workspace_bytes, workspace_init,
+    get_device_status, status_string, selftest_wait_timeout, lib,
+)
+
+
+class MoELayer:
+    """Holds the layer's weights and a reusable workspace; calling it runs moe_forward on the current stream."""
+
+    def __init__(self, w_r, w1, w2, k: int = 2, b_r=None, path: int = PATH_AUTO):
+        import torch
+        if not (w_r.is_cuda and w1.is_cuda and w2.is_cuda):
+            raise ValueError("MoELayer: weights must be CUDA tensors")
+        self.d, self.E = int(w_r.shape[0]), int(w_r.shape[1])
+        self.F = int(w1.shape[2])
+        if tuple(w1.shape) != (self.E, self.d, self.F) or tuple(w2.shape) != (self.E, self.F, self.d):
+            raise ValueError("MoELayer: expected w1 [E, d, F] and w2 [E, F, d]")
+        self.k = int(k)
+        self.dt = _lib.dtype_code(w1)
+        self.w_r, self.w1, self.w2 = w_r.contiguous(), w1.contiguous(), w2.contiguous()
+        self.b_r = None if b_r is None else b_r.to(torch.float32).contiguous()
+        self.path = path
+        self._ws = None
+        self._ws_T = -1
+
+    def workspace(self, T: int):
+        import torch
+        if self._ws is None or T > self._ws_T:
+            n = workspace_bytes(T, self.d, self.F, self.E, self.k, self.dt)
+            if n == 0:
+                raise MoeError(MOE_ERR_INVALID_ARG, "moe_workspace_bytes")
+            self._ws = torch.empty(n, dtype=torch.uint8, device=self.w1.device)
+            workspace_init(self._ws)
+            self._ws_T = T
+        return self._ws
+
+    def __call__(self, x, out: Optional["object"] = None, topk_idx=None, topk_gate=None, counts=None):
+        import torch
+        T = int(x.shape[0])
+        if out is None:
+            out = torch.empty_like(x)
+        forward(x, self.w_r, self.b_r, self.w1, self.w2, T, self.d, self.F, self.E, self.k, self.dt, out,
+                self.workspace(T), topk_idx=topk_idx, topk_gate=topk_gate, counts=counts, path=self.path)
+        return out
+
+    def device_status(self):
+        """(status, detail) of the first device-side error since the last call; synchronises."""
+        return get_device_status(self._ws) if self._ws is not None else (MOE_OK, 0)

@@ -1,0 +1,286 @@
+// C ABI of the layer (include/moe.h): host-side validation, workspace layout, path
+// choice and step sequencing. Every entry point validates all arguments before it
+// makes any CUDA call, so invalid calls fail the same way with or without a GPU.
+#include <cstdlib>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 148;
+  return sms;
+}
+
+namespace {
+
+constexpr int kStreamPathMaxRows = 256;
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+inline size_t elem_bytes(int dt) { return dt == MOE_DTYPE_BF16 ? 2 : 4; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Workspace regions, in this order; each starts on a 256-byte boundary.
+struct Layout {
+  size_t header, blk_counts, blk_base, topk_idx, topk_gate, counts, offsets, perm_token, row_of, row_gate, h,
+      x_perm, y_perm, end;
+  size_t dispatch_end, ffn_end, grouped_end;
+  Layout(int T, int d, int F, int E, int k, int dt) {
+    const size_t A = (size_t)T * k, eb = elem_bytes(dt);
+    const size_t nb = (A + kDispatchChunk - 1) / kDispatchChunk;
+    size_t o = 0;
+    header = o; o += align256(kWsHeaderBytes);
+    blk_counts = o; o += align256(nb * E * 4);
+    blk_base = o; o += align256(nb * E * 4);
+    dispatch_end = o;
+    topk_idx = o; o += align256(A * 4);
+    topk_gate = o; o += align256(A * 4);
+    counts = o; o += align256((size_t)E * 4);
+    offsets = o; o += align256((size_t)(E + 1) * 4);
+    perm_token = o; o += align256(A * 4);
+    row_of = o; o += align256(A * 4);
+    row_gate = o; o += align256(A * 4);
+    h = o; o += align256(A * F * eb);
+    grouped_end = o;
+    x_perm = o; o += align256(A * d * eb);
+    y_perm = o; o += align256(A * d * eb);
+    end = o;
+    ffn_end = align256(kWsHeaderBytes);
+  }
+};
+
+bool sizes_ok(int T, int d, int F, int E, int k, int dt) {
+  if (dt != MOE_DTYPE_F32 && dt != MOE_DTYPE_BF16) return false;
+  if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 8 || k > E) return false;
+  if (d < 8 || d % 8 != 0 || F < 8 || F % 8 != 0) return false;
+  const long long A = (long long)T * k;
+  if (A >= (1ll << 31)) return false;
+  const long long big = d > F ? d : F;
+  if ((long long)T * big > (1ll << 40)) return false;
+  return true;
+}
+
+uint64_t wait_timeout_ns() {
+  const char* s = std::getenv("MOE_WAIT_TIMEOUT_MS");
+  long long ms = s != nullptr ? std::atoll(s) : 2000;
+  if (ms <= 0) ms = 2000;
+  return (uint64_t)ms * 1000000ull;
+}
+
+inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename P>
+inline P* at(void* ws, size_t off) { return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off); }
+
+moe_path resolve_path(moe_path path, int dt, int rows) {
+  if (path != MOE_PATH_AUTO) return path;
+  if (dt == MOE_DTYPE_F32) return MOE_PATH_SIMT;
+  return rows <= kStreamPathMaxRows ? MOE_PATH_STREAM : MOE_PATH_TENSOR;
+}
+
+bool path_ok(moe_path path, int dt) {
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_SIMT) return false;
+  return true;
+}
+
+moe_status run_ffn_half(moe_path path, FfnArgs& args, cudaStream_t s) {
+  path = resolve_path(path, args.dt, args.rows);
+  if ((path == MOE_PATH_TENSOR || path == MOE_PATH_STREAM) && args.dt != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+  cudaError_t e;
+  switch (path) {
+    case MOE_PATH_TENSOR: e = launch_ffn_tensor(args, s); break;
+    case MOE_PATH_STREAM: e = launch_ffn_stream(args, s); break;
+    default: e = launch_ffn_simt(args, s); break;
+  }
+  if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(e);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: no kernel for this combination";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or launch failed";
+    case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK: a device-side range check failed";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a bounded device-side wait gave up";
+  }
+  return "unknown moe_status";
+}
+
+size_t moe_workspace_bytes(int T, int d, int F, int E, int k, moe_dtype dt) {
+  if (!sizes_ok(T, d, F, E, k, dt)) return 0;
+  return Layout(T, d, F, E, k, dt).end;
+}
+
+moe_status moe_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (workspace == nullptr || ws_bytes < kWsHeaderBytes || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(workspace, 0, kWsHeaderBytes, (cudaStream_t)stream));
+}
+
+moe_status moe_get_device_status(void* workspace, int32_t* detail, void* stream) {
+  if (workspace == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t word[2] = {0, 0};
+  if (cudaMemcpy(word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (detail != nullptr) *detail = word[1];
+  return (moe_status)word[0];
+}
+
+moe_status moe_router_topk(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
+                           moe_dtype dt, int32_t* topk_idx, float* topk_gate, void* stream) {
+  if (!sizes_ok(T, d, 8, E, k, dt)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (x == nullptr || w_r == nullptr || topk_idx == nullptr || topk_gate == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, topk_idx, topk_gate, (cudaStream_t)stream));
+}
+
+moe_status moe_dispatch(const void* x, const int32_t* topk_idx, const float* topk_gate, int T, int d, int E,
+                        int k, moe_dtype dt, int32_t* counts, int32_t* offsets, int32_t* perm_token,
+                        int32_t* row_of, float* row_gate, void* x_perm, void* workspace, size_t ws_bytes,
+                        void* stream) {
+  if (!sizes_ok(T, d, 8, E, k, dt)) return MOE_ERR_INVALID_ARG;
+  if (counts == nullptr || offsets == nullptr || workspace == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (x == nullptr || topk_idx == nullptr || topk_gate == nullptr || perm_token == nullptr ||
+                row_of == nullptr || row_gate == nullptr || x_perm == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm) || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  const Layout L(T, d, 8, E, k, dt);
+  if (ws_bytes < L.dispatch_end) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_dispatch(x, topk_idx, topk_gate, T, d, E, k, dt, counts, offsets, perm_token, row_of,
+                                     row_gate, x_perm, at<int32_t>(workspace, L.blk_counts),
+                                     at<int32_t>(workspace, L.blk_base), at<int>(workspace, L.header),
+                                     (cudaStream_t)stream));
+}
+
+static moe_status expert_half(int stage, const void* a, const void* w, const int32_t* offsets,
+                              const float* row_gate, int T, int d, int F, int E, int k, moe_dtype dt, moe_path path,
+                              void* out, void* workspace, size_t ws_bytes, void* stream) {
+  if (!sizes_ok(T, d, F, E, k, dt) || !path_ok(path, dt)) return MOE_ERR_INVALID_ARG;
+  if (workspace == nullptr || ws_bytes < kWsHeaderBytes || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (a == nullptr || w == nullptr || offsets == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (stage == 2 && row_gate == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(w) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  FfnArgs args;
+  args.a = a; args.w = w; args.offsets = offsets; args.row_gate = row_gate; args.out = out;
+  args.rows = T * k; args.E = E; args.dt = dt; args.stage = stage;
+  args.K = stage == 1 ? d : F;
+  args.N = stage == 1 ? F : d;
+  args.status = at<int>(workspace, 0);
+  args.timeout_ns = wait_timeout_ns();
+  return run_ffn_half(path, args, (cudaStream_t)stream);
+}
+
+moe_status moe_expert_up_ex(const void* x_perm, const void* w1, const int32_t* offsets, int T, int d, int F,
+                            int E, int k, moe_dtype dt, moe_path path, void* h, void* workspace, size_t ws_bytes,
+                            void* stream) {
+  return expert_half(1, x_perm, w1, offsets, nullptr, T, d, F, E, k, dt, path, h, workspace, ws_bytes, stream);
+}
+moe_status moe_expert_up(const void* x_perm, const void* w1, const int32_t* offsets, int T, int d, int F, int E,
+                         int k, moe_dtype dt, void* h, void* workspace, size_t ws_bytes, void* stream) {
+  return moe_expert_up_ex(x_perm, w1, offsets, T, d, F, E, k, dt, MOE_PATH_AUTO, h, workspace, ws_bytes, stream);
+}
+moe_status moe_expert_down_ex(const void* h, const void* w2, const int32_t* offsets, const float* row_gate,
+                              int T, int d, int F, int E, int k, moe_dtype dt, moe_path path, void* y_perm,
+                              void* workspace, size_t ws_bytes, void* stream) {
+  return expert_half(2, h, w2, offsets, row_gate, T, d, F, E, k, dt, path, y_perm, workspace, ws_bytes, stream);
+}
+moe_status moe_expert_down(const void* h, const void* w2, const int32_t* offsets, const float* row_gate, int T,
+                           int d, int F, int E, int k, moe_dtype dt, void* y_perm, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  return moe_expert_down_ex(h, w2, offsets, row_gate, T, d, F, E, k, dt, MOE_PATH_AUTO, y_perm, workspace,
+                            ws_bytes, stream);
+}
+
+moe_status moe_grouped_ffn_ex(const void* x_perm, const void* w1, const void* w2, const int32_t* offsets,
+                              const float* row_gate, int T, int d, int F, int E, int k, moe_dtype dt,
+                              moe_path path, void* y_perm, void* workspace, size_t ws_bytes, void* stream) {
+  if (!sizes_ok(T, d, F, E, k, dt) || !path_ok(path, dt)) return MOE_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  const Layout L(T, d, F, E, k, dt);
+  if (ws_bytes < L.grouped_end) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  void* h = at<void>(workspace, L.h);
+  moe_status st = moe_expert_up_ex(x_perm, w1, offsets, T, d, F, E, k, dt, path, h, workspace, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  return moe_expert_down_ex(h, w2, offsets, row_gate, T, d, F, E, k, dt, path, y_perm, workspace, ws_bytes, stream);
+}
+moe_status moe_grouped_ffn(const void* x_perm, const void* w1, const void* w2, const int32_t* offsets,
+                           const float* row_gate, int T, int d, int F, int E, int k, moe_dtype dt, void* y_perm,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  return moe_grouped_ffn_ex(x_perm, w1, w2, offsets, row_gate, T, d, F, E, k, dt, MOE_PATH_AUTO, y_perm,
+                            workspace, ws_bytes, stream);
+}
+
+moe_status moe_combine(const void* y_perm, const int32_t* row_of, int T, int d, int k, moe_dtype dt, void* out,
+                       void* stream) {
+  if (!sizes_ok(T, d, 8, k, k, dt)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (y_perm == nullptr || row_of == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(y_perm, row_of, T, d, k, dt, out, (cudaStream_t)stream));
+}
+
+moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2,
+                          int T, int d, int F, int E, int k, moe_dtype dt, moe_path path, void* out,
+                          int32_t* topk_idx, float* topk_gate, int32_t* counts, void* workspace, size_t ws_bytes,
+                          void* stream) {
+  if (!sizes_ok(T, d, F, E, k, dt) || !path_ok(path, dt)) return MOE_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  const Layout L(T, d, F, E, k, dt);
+  if (ws_bytes < L.end) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (x == nullptr || w_r == nullptr || w1 == nullptr || w2 == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_r) || !aligned16(w1) || !aligned16(w2) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  int32_t* idx = topk_idx != nullptr ? topk_idx : at<int32_t>(workspace, L.topk_idx);
+  float* gate = topk_gate != nullptr ? topk_gate : at<float>(workspace, L.topk_gate);
+  int32_t* cnt = counts != nullptr ? counts : at<int32_t>(workspace, L.counts);
+  int32_t* offs = at<int32_t>(workspace, L.offsets);
+  int32_t* perm = at<int32_t>(workspace, L.perm_token);
+  int32_t* rowof = at<int32_t>(workspace, L.row_of);
+  float* rgate = at<float>(workspace, L.row_gate);
+  void* xp = at<void>(workspace, L.x_perm);
+  void* h = at<void>(workspace, L.h);
+  void* yp = at<void>(workspace, L.y_perm);
+  moe_status st = moe_router_topk(x, w_r, b_r, T, d, E, k, dt, idx, gate, stream);
+  if (st != MOE_OK) return st;
+  st = moe_dispatch(x, idx, gate, T, d, E, k, dt, cnt, offs, perm, rowof, rgate, xp, workspace, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  st = moe_expert_up_ex(xp, w1, offs, T, d, F, E, k, dt, path, h, workspace, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  st = moe_expert_down_ex(h, w2, offs, rgate, T, d, F, E, k, dt, path, yp, workspace, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  return moe_combine(yp, rowof, T, d, k, dt, out, stream);
+}
+moe_status moe_forward(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2, int T,
+                       int d, int F, int E, int k, moe_dtype dt, void* out, int32_t* topk_idx, float* topk_gate,
+                       int32_t* counts, void* workspace, size_t ws_bytes, void* stream) {
+  return moe_forward_ex(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, MOE_PATH_AUTO, out, topk_idx, topk_gate, counts,
+                        workspace, ws_bytes, stream);
+}
+
+moe_status moe_selftest_wait_timeout(void* workspace, size_t ws_bytes, int timeout_us, void* stream) {
+  if (workspace == nullptr || ws_bytes < kWsHeaderBytes || !aligned16(workspace) || timeout_us <= 0 ||
+      timeout_us > 10000000)
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_selftest_wait(at<int>(workspace, 0), (uint64_t)timeout_us * 1000ull, (cudaStream_t)stream));
+}
+
+}  // extern "C"

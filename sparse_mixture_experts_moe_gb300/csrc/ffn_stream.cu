@@ -1,0 +1,167 @@
+// Weight-streaming grouped expert FFN for batches with few rows per expert (decode).
+// csdn/6a919c0d §2.3: with top-2 routing each token reads two experts' full W1 and W2
+// from HBM, so the layer is bound by moving weights, not by arithmetic.
+//
+// Work unit = (expert with at least one row, 64-column slab of its weight matrix).
+// A CTA owns the slab for the full depth K, so the GeLU (up) or gate (down)
+// epilogue applies locally and no partial sums leave the CTA. Each k-row of the
+// slab is 128 contiguous bytes read by 8 lanes with 16-byte loads; 8 loads per
+// thread are in flight. The expert's rows (at most 8 per pass; more rows take
+// more passes) are staged in shared memory as fp32 in 1024-deep chunks.
+// Partial sums are combined in a fixed order (xor-butterfly in the warp, then
+// warps in index order), so results are reproducible.
+// Units are ordered slab-fastest, so CTAs running together stream neighbouring
+// slabs of the same matrix rows.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256, kWarps = 8;
+constexpr int NS = 64;            // columns per slab
+constexpr int LPR = NS / 8;       // lanes per k-row: 8 (16 bytes each)
+constexpr int RPW = 32 / LPR;     // k-rows per warp per step: 4
+constexpr int KSTEP = kWarps * RPW;  // k-rows per CTA step: 32
+constexpr int RMAX = 8;           // rows per pass
+constexpr int KC = 1024;          // k-depth staged per chunk
+constexpr int kUnroll = 8;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
+  v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+  v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
+}
+
+template <int STAGE>
+__global__ void __launch_bounds__(kThreads)
+ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ w,
+                  const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
+                  __nv_bfloat16* __restrict__ out) {
+  extern __shared__ __align__(16) float smem[];
+  float* sA = smem;                         // [RMAX][KC]
+  float* sRed = sA + RMAX * KC;             // [kWarps][RMAX][NS]
+  int* sAct = reinterpret_cast<int*>(sRed + kWarps * RMAX * NS);  // [E] experts with rows
+  __shared__ int s_nact;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (warp == 0) {
+    int base = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const bool act = e < E && offsets[e + 1] > offsets[e];
+      const unsigned m = __ballot_sync(0xffffffffu, act);
+      if (act) sAct[base + __popc(m & ((1u << lane) - 1u))] = e;
+      base += __popc(m);
+    }
+    if (lane == 0) s_nact = base;
+  }
+  __syncthreads();
+  const int nslab = (N + NS - 1) / NS;
+  const int units = s_nact * nslab;
+  const int kr = lane / LPR;            // k-row of this lane within the warp's group of RPW
+  const int cg = lane % LPR;            // 8-column group of this lane
+
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int e = sAct[u / nslab];
+    const int n0 = (u % nslab) * NS;
+    const int col = n0 + cg * 8;
+    const bool col_ok = col < N;
+    const __nv_bfloat16* we = w + (size_t)e * K * N;
+    const int r_begin = offsets[e], r_end = offsets[e + 1];
+    for (int rp = r_begin; rp < r_end; rp += RMAX) {
+      const int R = min(RMAX, r_end - rp);
+      float acc[RMAX][8];
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+
+      for (int kc = 0; kc < K; kc += KC) {
+        const int kn = min(KC, K - kc);
+        __syncthreads();
+        for (int i = tid; i < R * KC; i += kThreads) {
+          const int r = i / KC, kk = i % KC;
+          sA[i] = kk < kn ? __bfloat162float(a[(size_t)(rp + r) * K + kc + kk]) : 0.f;
+        }
+        __syncthreads();
+        for (int k0 = 0; k0 < kn; k0 += KSTEP * kUnroll) {
+          uint4 wv[kUnroll];
+#pragma unroll
+          for (int i = 0; i < kUnroll; ++i) {
+            const int kk = k0 + i * KSTEP + warp * RPW + kr;
+            if (col_ok && kk < kn)
+              wv[i] = __ldg(reinterpret_cast<const uint4*>(we + (size_t)(kc + kk) * N + col));
+            else
+              wv[i] = make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int i = 0; i < kUnroll; ++i) {
+            const int kk = k0 + i * KSTEP + warp * RPW + kr;
+            if (kk >= kn) break;
+            float wf[8];
+            bf16x8_to_f32(wv[i], wf);
+#pragma unroll
+            for (int r = 0; r < RMAX; ++r) {
+              if (r >= R) break;
+              const float av = sA[r * KC + kk];
+#pragma unroll
+              for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av, wf[c], acc[r][c]);
+            }
+          }
+        }
+      }
+      // Combine the RPW k-row groups of the warp (lanes cg, cg+8, cg+16, cg+24), then the warps.
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          float v = acc[r][c];
+          v += __shfl_xor_sync(0xffffffffu, v, LPR);
+          v += __shfl_xor_sync(0xffffffffu, v, 2 * LPR);
+          acc[r][c] = v;
+        }
+      if (lane < LPR) {
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) sRed[(warp * RMAX + r) * NS + cg * 8 + c] = acc[r][c];
+      }
+      __syncthreads();
+      for (int i = tid; i < R * NS; i += kThreads) {
+        const int r = i / NS, c = i % NS;
+        const int gn = n0 + c;
+        if (gn >= N) continue;
+        float v = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < kWarps; ++wi) v += sRed[(wi * RMAX + r) * NS + c];
+        const int grow = rp + r;
+        v = STAGE == 1 ? gelu_erf(v) : row_gate[grow] * v;
+        out[(size_t)grow * N + gn] = __float2bfloat16_rn(v);
+      }
+    }
+  }
+}
+
+template <int STAGE>
+cudaError_t launch_t(const FfnArgs& p, cudaStream_t s) {
+  const size_t smem = (size_t)(RMAX * KC + kWarps * RMAX * NS) * sizeof(float) + (size_t)p.E * sizeof(int);
+  auto kern = ffn_stream_kernel<STAGE>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int nslab = (p.N + NS - 1) / NS;
+  const long long max_units = (long long)(p.rows < p.E ? p.rows : p.E) * nslab;
+  long long grid = (long long)device_sm_count() * 4;
+  if (grid > max_units) grid = max_units;
+  kern<<<(int)grid, kThreads, smem, s>>>((const __nv_bfloat16*)p.a, (const __nv_bfloat16*)p.w, p.offsets,
+                                         p.row_gate, p.K, p.N, p.E, (__nv_bfloat16*)p.out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_stream(const FfnArgs& p, cudaStream_t s) {
+  if (p.rows == 0) return cudaSuccess;
+  if (p.dt != MOE_DTYPE_BF16) return cudaErrorNotSupported;
+  return p.stage == 1 ? launch_t<1>(p, s) : launch_t<2>(p, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,45 @@
+// Host-side launchers of the layer's kernels (internal to the library).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Dispatch processes the T*k assignments in chunks of this many (one CTA each).
+constexpr int kDispatchChunk = 256;
+
+cudaError_t launch_router_topk(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
+                               int dt, int32_t* idx, float* gate, cudaStream_t s);
+
+// blk_counts / blk_base: [ceil(A / kDispatchChunk), E] int32 scratch each.
+cudaError_t launch_dispatch(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
+                            int dt, int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* row_of,
+                            float* row_gate, void* x_perm, int32_t* blk_counts, int32_t* blk_base, int* status,
+                            cudaStream_t s);
+
+cudaError_t launch_combine(const void* y_perm, const int32_t* row_of, int T, int d, int k, int dt, void* out,
+                           cudaStream_t s);
+
+// Expert FFN halves. stage 1: out = GeLU(a W1[e]) (N = F, K = d);
+// stage 2: out = row_gate * (a W2[e]) (N = d, K = F).
+struct FfnArgs {
+  const void* a;          // [rows, K]
+  const void* w;          // [E, K, N]
+  const int32_t* offsets; // [E+1]
+  const float* row_gate;  // [rows] (stage 2)
+  void* out;              // [rows, N]
+  int rows, K, N, E, dt, stage;
+  int* status;
+  uint64_t timeout_ns;
+};
+cudaError_t launch_ffn_simt(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_ffn_stream(const FfnArgs& a, cudaStream_t s);
+// Returns cudaErrorNotSupported when no tensor-map encoder is available.
+cudaError_t launch_ffn_tensor(const FfnArgs& a, cudaStream_t s);
+
+cudaError_t launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace moe

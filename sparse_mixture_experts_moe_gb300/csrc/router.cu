@@ -1,0 +1,149 @@
+// Router: logits = x W_r (+ b_r), softmax over the E experts, deterministic top-k.
+// csdn/6a919c0d §2.2 steps 1-4; aicoding/6a320eef §3.2; csdn/6a919c0d §4.2 (max subtraction).
+//
+// One CTA = 4 warps and 4*TPW tokens. W_r is staged through shared memory in
+// 32-row slabs (as fp32) and shared by every token of the CTA; lane l owns four
+// consecutive experts of the current 128-expert chunk and TPW tokens, so each
+// 16-byte W load feeds 4*TPW FMAs. Logits land in shared memory; then the warp
+// that owns a token does its softmax and k rounds of (max logit, lowest index)
+// selection with warp shuffles. All sums use a fixed order: results are
+// reproducible run to run.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kDK = 32;      // W_r rows per staged slab
+constexpr int kEC = 128;     // experts per chunk (4 per lane)
+
+template <typename T, int TPW>
+__global__ void __launch_bounds__(kWarps * 32)
+router_topk_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const float* __restrict__ b_r, int Tn,
+                   int d, int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate) {
+  constexpr int TB = kWarps * TPW;
+  extern __shared__ __align__(16) float smem[];
+  float* sW = smem;                    // [kDK][kEC]
+  float* sX = sW + kDK * kEC;          // [TB][kDK]
+  float* sL = sX + TB * kDK;           // [TB][E]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tok0 = blockIdx.x * TB;
+
+  for (int ec = 0; ec < E; ec += kEC) {
+    float acc[TPW][4];
+#pragma unroll
+    for (int t = 0; t < TPW; ++t)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) acc[t][m] = 0.f;
+
+    for (int k0 = 0; k0 < d; k0 += kDK) {
+      __syncthreads();
+      for (int i = tid; i < kDK * kEC; i += kWarps * 32) {
+        const int r = i / kEC, c = i % kEC;
+        const int gk = k0 + r, ge = ec + c;
+        sW[i] = (gk < d && ge < E) ? to_f32(w_r[(size_t)gk * E + ge]) : 0.f;
+      }
+      for (int i = tid; i < TB * kDK; i += kWarps * 32) {
+        const int t = i / kDK, c = i % kDK;
+        const int gt = tok0 + t, gk = k0 + c;
+        sX[i] = (gt < Tn && gk < d) ? to_f32(x[(size_t)gt * d + gk]) : 0.f;
+      }
+      __syncthreads();
+#pragma unroll 2
+      for (int kk = 0; kk < kDK; kk += 4) {
+        float4 w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) w[q] = *reinterpret_cast<const float4*>(&sW[(kk + q) * kEC + 4 * lane]);
+#pragma unroll
+        for (int t = 0; t < TPW; ++t) {
+          const float4 xv = *reinterpret_cast<const float4*>(&sX[(warp * TPW + t) * kDK + kk]);
+          acc[t][0] = fmaf(xv.x, w[0].x, acc[t][0]); acc[t][1] = fmaf(xv.x, w[0].y, acc[t][1]);
+          acc[t][2] = fmaf(xv.x, w[0].z, acc[t][2]); acc[t][3] = fmaf(xv.x, w[0].w, acc[t][3]);
+          acc[t][0] = fmaf(xv.y, w[1].x, acc[t][0]); acc[t][1] = fmaf(xv.y, w[1].y, acc[t][1]);
+          acc[t][2] = fmaf(xv.y, w[1].z, acc[t][2]); acc[t][3] = fmaf(xv.y, w[1].w, acc[t][3]);
+          acc[t][0] = fmaf(xv.z, w[2].x, acc[t][0]); acc[t][1] = fmaf(xv.z, w[2].y, acc[t][1]);
+          acc[t][2] = fmaf(xv.z, w[2].z, acc[t][2]); acc[t][3] = fmaf(xv.z, w[2].w, acc[t][3]);
+          acc[t][0] = fmaf(xv.w, w[3].x, acc[t][0]); acc[t][1] = fmaf(xv.w, w[3].y, acc[t][1]);
+          acc[t][2] = fmaf(xv.w, w[3].z, acc[t][2]); acc[t][3] = fmaf(xv.w, w[3].w, acc[t][3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < TPW; ++t)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int e = ec + 4 * lane + m;
+        if (e < E) sL[(warp * TPW + t) * E + e] = acc[t][m];
+      }
+  }
+  __syncwarp();
+
+  // Softmax and top-k: each warp finishes its own tokens (it wrote all their logits).
+  for (int t = 0; t < TPW; ++t) {
+    const int tok = tok0 + warp * TPW + t;
+    if (tok >= Tn) break;
+    float* row = sL + (warp * TPW + t) * E;
+    float m = -INFINITY;
+    for (int e = lane; e < E; e += 32) {
+      const float v = row[e] + (b_r != nullptr ? b_r[e] : 0.f);
+      row[e] = v;
+      m = fmaxf(m, v);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float s = 0.f;
+    for (int e = lane; e < E; e += 32) s += expf(row[e] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    __syncwarp();
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+      for (int e = lane; e < E; e += 32) {
+        const float v = row[e];
+        if (v > bv) { bv = v; be = e; }  // ascending e within a lane: ties keep the lower index
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+      }
+      if (lane == 0) {
+        topk_idx[(size_t)tok * k + j] = be;
+        topk_gate[(size_t)tok * k + j] = expf(bv - m) / s;
+      }
+      if ((be & 31) == lane) row[be] = -INFINITY;
+      __syncwarp();
+    }
+  }
+}
+
+template <typename T, int TPW>
+cudaError_t launch_router_t(const void* x, const void* w_r, const float* b_r, int Tn, int d, int E, int k,
+                            int32_t* idx, float* gate, cudaStream_t s) {
+  constexpr int TB = kWarps * TPW;
+  const size_t smem = (size_t)(kDK * kEC + TB * kDK + TB * E) * sizeof(float);
+  auto kern = router_topk_kernel<T, TPW>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int grid = (Tn + TB - 1) / TB;
+  kern<<<grid, kWarps * 32, smem, s>>>((const T*)x, (const T*)w_r, b_r, Tn, d, E, k, idx, gate);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_router_topk(const void* x, const void* w_r, const float* b_r, int Tn, int d, int E, int k,
+                               int dt, int32_t* idx, float* gate, cudaStream_t s) {
+  if (Tn == 0) return cudaSuccess;
+  const bool small_e = E <= 256;
+  if (dt == MOE_DTYPE_BF16)
+    return small_e ? launch_router_t<__nv_bfloat16, 8>(x, w_r, b_r, Tn, d, E, k, idx, gate, s)
+                   : launch_router_t<__nv_bfloat16, 2>(x, w_r, b_r, Tn, d, E, k, idx, gate, s);
+  return small_e ? launch_router_t<float, 8>(x, w_r, b_r, Tn, d, E, k, idx, gate, s)
+                 : launch_router_t<float, 2>(x, w_r, b_r, Tn, d, E, k, idx, gate, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,145 @@
+"""Seeded layer instances for the tests: inputs on the device, their exact values on the host.
+
+Every tensor comes from ``inputgen`` (seed, stream, draw attempt). Tokens whose
+fp64 top-(k+1) logits have an adjacent gap below 1e-3 are re-drawn (new attempt
+for that row) until none is left, so every routing index is decided by a margin
+far above fp32 rounding. The re-draw test routes with the oracle: it lives here,
+in test infrastructure, not in the generator.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional
+
+import numpy as np
+import torch
+
+import inputgen as ig
+import oracle
+
+MIN_GAP = 1e-3
+HOST_DRAW_MAX = 1 << 22  # tensors up to this many elements are drawn on the host, larger ones on the device
+
+
+def torch_dtype(dt: int):
+    return torch.bfloat16 if dt == ig.DTYPE_BF16 else torch.float32
+
+
+def rel_rms_err(got: np.ndarray, ref: np.ndarray) -> float:
+    """max |got - ref| / sqrt(mean(ref^2)), in fp64."""
+    ref = np.asarray(ref, np.float64)
+    got = np.asarray(got, np.float64)
+    rms = math.sqrt(float(np.mean(ref * ref)))
+    return float(np.max(np.abs(got - ref))) / rms if rms > 0 else float(np.max(np.abs(got - ref)))
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    """Exact fp64 values of a device tensor (bf16 and fp32 upcast exactly)."""
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def device_tensor(shape, seed, stream, sigma, dt, device, attempt=0, host=False):
+    """A generator tensor on the device (host draw for small tensors, device fill for large ones)."""
+    n = int(np.prod(shape))
+    key = ig.stream_key(seed, stream, attempt)
+    if host or n <= HOST_DRAW_MAX:
+        a = ig.draw(0, n, key, sigma, dt)
+        t = torch.from_numpy(a.view(np.int16) if dt == ig.DTYPE_BF16 else a)
+        if dt == ig.DTYPE_BF16:
+            t = t.view(torch.bfloat16)
+        return t.reshape(shape).to(device)
+    t = torch.empty(shape, dtype=torch_dtype(dt), device=device)
+    ig.fill_device(t, 0, key, sigma, dt, torch.cuda.current_stream().cuda_stream)
+    return t
+
+
+@dataclass
+class Case:
+    T: int
+    d: int
+    F: int
+    E: int
+    k: int
+    dt: int
+    x: torch.Tensor
+    w_r: torch.Tensor
+    w1: torch.Tensor
+    w2: torch.Tensor
+    b_r: Optional[torch.Tensor]
+    x64: np.ndarray
+    wr64: np.ndarray
+    br64: Optional[np.ndarray]
+    redrawn: int = 0
+    _w64: dict = field(default_factory=dict)
+
+    @property
+    def A(self):
+        return self.T * self.k
+
+    def w1_host(self):
+        return ExpertView(self.w1, self._w64, "w1")
+
+    def w2_host(self):
+        return ExpertView(self.w2, self._w64, "w2")
+
+
+class ExpertView:
+    """w[e] as exact fp64 on the host, copied from the device on first use (small layers are cached)."""
+
+    def __init__(self, t: torch.Tensor, cache: dict, name: str):
+        self.t, self.cache, self.name = t, cache, name
+        self.cacheable = t[0].numel() <= (1 << 22)
+
+    def __getitem__(self, e):
+        key = (self.name, int(e))
+        if key in self.cache:
+            return self.cache[key]
+        v = self.t[int(e)].float().cpu().numpy().astype(np.float64)
+        if self.cacheable:
+            self.cache[key] = v
+        return v
+
+
+def make_case(T, d, F, E, k, dt, seed=0, bias_scale=None, bias=None, device="cuda", redraw=True) -> Case:
+    """Seeded layer instance; x and W_r also kept as exact fp64 on the host."""
+    tdt = torch_dtype(dt)
+    x = device_tensor((T, d), seed, ig.STREAM_X, 1.0, dt, device)
+    w_r = device_tensor((d, E), seed, ig.STREAM_WR, ig.sigma_for_fan_in(d), dt, device)
+    w1 = device_tensor((E, d, F), seed, ig.STREAM_W1, ig.sigma_for_fan_in(d), dt, device)
+    w2 = device_tensor((E, F, d), seed, ig.STREAM_W2, ig.sigma_for_fan_in(F), dt, device)
+    b_r = br64 = None
+    if bias_scale is not None or bias is not None:
+        b = ig.skew_bias(E, bias_scale) if bias is None else np.asarray(bias, np.float32)
+        b_r = torch.from_numpy(b).to(device)
+        br64 = b.astype(np.float64)
+    x64 = to_f64(x)
+    wr64 = to_f64(w_r)
+    redrawn = 0
+    if redraw and T > 0:
+        attempts = np.zeros(T, np.int64)
+        for _ in range(64):
+            bad = oracle.ambiguous_tokens(oracle.router_logits(x64, wr64, br64), k, MIN_GAP)
+            if len(bad) == 0:
+                break
+            redrawn += len(bad)
+            for t in bad:
+                attempts[t] += 1
+                key = ig.stream_key(seed, ig.STREAM_X, int(attempts[t]))
+                row = ig.draw(t * d, d, key, 1.0, dt)
+                x64[t] = ig.as_f64(row, dt)
+                rt = torch.from_numpy(row.view(np.int16) if dt == ig.DTYPE_BF16 else row)
+                if dt == ig.DTYPE_BF16:
+                    rt = rt.view(torch.bfloat16)
+                x[t] = rt.to(device)
+        else:
+            raise RuntimeError("re-draw did not converge")
+    return Case(T, d, F, E, k, dt, x, w_r, w1, w2, b_r, x64, wr64, br64, redrawn)
+
+
+def workspace_for(case: Case) -> torch.Tensor:
+    import sparse_mixture_experts_moe_gb300 as moe
+    n = moe.workspace_bytes(case.T, case.d, case.F, case.E, case.k, case.dt)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=case.x.device)
+    moe.workspace_init(ws)
+    return ws

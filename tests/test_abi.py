@@ -1,0 +1,93 @@
+"""C ABI checks that need no GPU: the library loads, exports every entry point the
+header declares, and rejects invalid arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_mixture_experts_moe_gb300 as moe
+from sparse_mixture_experts_moe_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_layer_calls():
+    names = header_functions()
+    for required in ["moe_router_topk", "moe_dispatch", "moe_grouped_ffn", "moe_combine", "moe_forward",
+                     "moe_expert_up", "moe_expert_down", "moe_workspace_bytes", "moe_get_device_status"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = _lib.lib()
+    missing = [n for n in header_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(header_functions()) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_status_strings():
+    for s in range(6):
+        assert moe.status_string(s).startswith("MOE_")
+
+
+def test_workspace_bytes():
+    n = moe.workspace_bytes(4096, 1024, 4096, 16, 2, moe.MOE_DTYPE_BF16)
+    A = 8192
+    # at least x_perm + h + y_perm
+    assert n >= A * 1024 * 2 * 2 + A * 4096 * 2
+    assert n % 256 == 0
+    assert moe.workspace_bytes(64, 128, 256, 8, 9, moe.MOE_DTYPE_F32) == 0     # k > E
+    assert moe.workspace_bytes(64, 130, 256, 8, 2, moe.MOE_DTYPE_F32) == 0     # d % 8
+    assert moe.workspace_bytes(64, 128, 256, 1025, 2, moe.MOE_DTYPE_F32) == 0  # E > 1024
+    assert moe.workspace_bytes(0, 128, 256, 8, 2, moe.MOE_DTYPE_F32) > 0       # T = 0 is valid
+
+
+FAKE = 1 << 20  # a non-null, 16-byte aligned address that is never dereferenced
+
+
+@pytest.mark.parametrize("T,d,E,k,dt", [
+    (-1, 128, 8, 2, 0), (64, 0, 8, 2, 0), (64, 12, 8, 2, 0), (64, 128, 8, 0, 0), (64, 128, 8, 9, 0),
+    (64, 128, 2, 3, 0), (64, 128, 1025, 2, 0), (64, 128, 8, 2, 7)])
+def test_router_rejects_bad_sizes_without_gpu(T, d, E, k, dt):
+    rc = _lib.lib().moe_router_topk(FAKE, FAKE, None, T, d, E, k, dt, FAKE, FAKE, None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+
+
+def test_null_and_misaligned_pointers_rejected_without_gpu():
+    lib = _lib.lib()
+    assert lib.moe_router_topk(None, FAKE, None, 4, 128, 8, 2, 1, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_router_topk(FAKE + 2, FAKE, None, 4, 128, 8, 2, 1, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(None, FAKE, 4, 128, 2, 1, FAKE, None) == moe.MOE_ERR_INVALID_ARG
+    ws_small = 100
+    assert lib.moe_forward(FAKE, FAKE, None, FAKE, FAKE, 4, 128, 256, 8, 2, 1, FAKE, None, None, None, FAKE,
+                           ws_small, None) == moe.MOE_ERR_INVALID_ARG
+    n = moe.workspace_bytes(4, 128, 256, 8, 2, 1)
+    assert lib.moe_dispatch(FAKE, FAKE, FAKE, 4, 128, 8, 2, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 256,
+                            None) == moe.MOE_ERR_INVALID_ARG  # workspace too small for the count tables
+    assert lib.moe_expert_up_ex(FAKE, FAKE, FAKE, 4, 128, 256, 8, 2, 1, 9, FAKE, FAKE, n,
+                                None) == moe.MOE_ERR_INVALID_ARG  # unknown path
+    assert lib.moe_selftest_wait_timeout(FAKE, n, 0, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_zero_tokens_is_a_no_op_without_gpu():
+    lib = _lib.lib()
+    n = moe.workspace_bytes(0, 128, 256, 8, 2, 1)
+    assert lib.moe_router_topk(FAKE, FAKE, None, 0, 128, 8, 2, 1, FAKE, FAKE, None) == moe.MOE_OK
+    assert lib.moe_combine(FAKE, FAKE, 0, 128, 2, 1, FAKE, None) == moe.MOE_OK
+    assert lib.moe_forward(FAKE, FAKE, None, FAKE, FAKE, 0, 128, 256, 8, 2, 1, FAKE, None, None, None, FAKE, n,
+                           None) == moe.MOE_OK
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "libmoe.so"))
+    monkeypatch.setattr(_lib, "_LIB", None)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _lib.lib()

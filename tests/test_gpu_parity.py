@@ -1,0 +1,299 @@
+"""GPU path vs the fp64 oracle, through the C ABI, at sizes the oracle finishes in seconds.
+
+Bars (stated by the layer's specification): routing indices, counts, offsets and the
+permutation bit-exact; outputs within max relative-to-RMS error 1e-4 (fp32) and
+2e-2 (bf16). Shapes span several 128x256 tensor-core tiles with ragged row and
+column tails, several dispatch chunks, and the degenerate cases of the method.
+Each step is also checked on its own, fed by inputs that do not come from the
+GPU path (oracle routing, or generator tensors for h and y_perm).
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputgen as ig
+from inputgen import workloads
+import oracle
+import sparse_mixture_experts_moe_gb300 as moe
+from moe_cases import make_case, rel_rms_err, to_f64, workspace_for, device_tensor, torch_dtype
+
+pytestmark = pytest.mark.gpu
+
+BF16, F32 = ig.DTYPE_BF16, ig.DTYPE_F32
+TOL = {F32: 1e-4, BF16: 2e-2}
+DEV = "cuda"
+
+
+def run_router(c):
+    idx = torch.empty((c.T, c.k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((c.T, c.k), dtype=torch.float32, device=DEV)
+    moe.router_topk(c.x, c.w_r, c.b_r, c.T, c.d, c.E, c.k, c.dt, idx, gate)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), gate.cpu().numpy()
+
+
+def oracle_routing(c):
+    logits = oracle.router_logits(c.x64, c.wr64, c.br64)
+    p = oracle.softmax(logits)
+    idx = oracle.topk_select(logits, c.k)
+    return idx, oracle.gates_of(p, idx)
+
+
+ROUTER_CASES = [
+    dict(T=64, d=128, F=256, E=8, k=2, dt=F32),            # the tiny fp32 layer
+    dict(T=300, d=320, F=64, E=16, k=2, dt=BF16),
+    dict(T=257, d=256, F=64, E=128, k=2, dt=BF16),
+    dict(T=33, d=64, F=64, E=1024, k=8, dt=BF16),          # largest E and k
+    dict(T=50, d=96, F=64, E=2, k=2, dt=F32),              # E = k
+    dict(T=70, d=64, F=64, E=5, k=1, dt=BF16),
+    dict(T=1, d=8, F=8, E=3, k=2, dt=F32),
+]
+
+
+@pytest.mark.parametrize("cfg", ROUTER_CASES, ids=lambda c: "T{T}_d{d}_E{E}_k{k}_{dt}".format(**c))
+def test_router_topk(cfg):
+    c = make_case(**cfg)
+    idx, gate = run_router(c)
+    ridx, rgate = oracle_routing(c)
+    assert np.array_equal(idx, ridx)
+    assert np.max(np.abs(gate - rgate)) < 1e-5
+    assert np.all(gate.sum(axis=1) <= 1.0 + 1e-6)
+
+
+def test_router_skew_bias():
+    c = make_case(T=400, d=256, F=64, E=128, k=2, dt=BF16, bias_scale=workloads.SKEW_BIAS_SCALE)
+    idx, gate = run_router(c)
+    ridx, rgate = oracle_routing(c)
+    assert np.array_equal(idx, ridx)
+    assert np.max(np.abs(gate - rgate)) < 1e-5
+
+
+DISPATCH_CASES = [
+    dict(T=1000, d=64, E=128, k=2, dt=BF16),   # 8 chunks, ragged last chunk
+    dict(T=300, d=40, E=1024, k=8, dt=F32),    # 10 chunks, E = 1024
+    dict(T=3, d=8, E=4, k=2, dt=BF16),
+    dict(T=513, d=128, E=16, k=2, dt=F32),
+]
+
+
+def run_dispatch(c, idx, gate):
+    A, E = c.A, c.E
+    out = dict(counts=torch.empty(E, dtype=torch.int32, device=DEV),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device=DEV),
+               perm_token=torch.empty(A, dtype=torch.int32, device=DEV),
+               row_of=torch.empty((c.T, c.k), dtype=torch.int32, device=DEV),
+               row_gate=torch.empty(A, dtype=torch.float32, device=DEV),
+               x_perm=torch.empty((A, c.d), dtype=torch_dtype(c.dt), device=DEV))
+    ws = workspace_for(c)
+    ti = torch.from_numpy(idx.astype(np.int32)).to(DEV)
+    tg = torch.from_numpy(gate.astype(np.float32)).to(DEV)
+    moe.dispatch(c.x, ti, tg, c.T, c.d, E, c.k, c.dt, out["counts"], out["offsets"], out["perm_token"],
+                 out["row_of"], out["row_gate"], out["x_perm"], ws)
+    st, detail = moe.get_device_status(ws)
+    return out, st, detail
+
+
+@pytest.mark.parametrize("cfg", DISPATCH_CASES, ids=lambda c: "T{T}_E{E}_k{k}".format(**c))
+def test_dispatch(cfg):
+    c = make_case(F=64, **cfg)
+    ridx, rgate = oracle_routing(c)
+    out, st, _ = run_dispatch(c, ridx, rgate)
+    assert st == moe.MOE_OK
+    ref = oracle.dispatch(ridx, c.E, rgate.astype(np.float32))
+    assert np.array_equal(out["counts"].cpu().numpy(), ref["counts"])
+    assert np.array_equal(out["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(out["perm_token"].cpu().numpy(), ref["perm_token"])
+    assert np.array_equal(out["row_of"].cpu().numpy(), ref["row_of"])
+    assert np.array_equal(out["row_gate"].cpu().numpy(), ref["row_gate"].astype(np.float32))
+    assert np.array_equal(to_f64(out["x_perm"]), c.x64[ref["perm_token"]])
+
+
+def test_dispatch_flags_out_of_range_index():
+    c = make_case(T=200, d=64, F=64, E=16, k=2, dt=BF16)
+    ridx, rgate = oracle_routing(c)
+    bad = ridx.copy()
+    bad[77, 1] = 16  # out of range
+    out, st, detail = run_dispatch(c, bad, rgate)
+    assert st == moe.MOE_ERR_DEVICE_CHECK and detail == 77 * 2 + 1
+    row_of = out["row_of"].cpu().numpy()
+    assert row_of[77, 1] == -1
+    assert out["counts"].cpu().numpy().sum() == c.A - 1
+    # the context is still usable and the status was cleared
+    out2, st2, _ = run_dispatch(c, ridx, rgate)
+    assert st2 == moe.MOE_OK
+
+
+# ----------------------------------------------------------------------------- expert FFN halves
+
+FFN_CASES = [
+    # (T, d, F, E, k, dt, path)
+    (600, 320, 704, 6, 2, BF16, moe.PATH_TENSOR),   # 2 row tiles per expert + tails, N tail 704 = 2.75 x 256
+    (700, 256, 512, 3, 2, BF16, moe.PATH_TENSOR),   # ~467 rows per expert: 4 row tiles
+    (96, 64, 128, 8, 2, BF16, moe.PATH_TENSOR),     # K = 64: one k-block, N < 256
+    (600, 320, 704, 6, 2, BF16, moe.PATH_SIMT),
+    (12, 512, 384, 16, 2, BF16, moe.PATH_STREAM),
+    (64, 1024, 512, 8, 2, BF16, moe.PATH_STREAM),   # up to 8+ rows per expert: several passes
+    (64, 128, 256, 8, 2, F32, moe.PATH_SIMT),
+]
+
+
+def _ffn_inputs(c):
+    ridx, rgate = oracle_routing(c)
+    dp = oracle.dispatch(ridx, c.E, rgate.astype(np.float32))
+    x_perm = c.x[torch.from_numpy(dp["perm_token"]).to(DEV)].contiguous()
+    offsets = torch.from_numpy(dp["offsets"].astype(np.int32)).to(DEV)
+    row_gate = torch.from_numpy(dp["row_gate"].astype(np.float32)).to(DEV)
+    return dp, x_perm, offsets, row_gate
+
+
+@pytest.mark.parametrize("cfg", FFN_CASES, ids=lambda c: "T{}_d{}_F{}_E{}_dt{}_path{}".format(*c[:4], c[5], c[6]))
+def test_expert_up(cfg):
+    T, d, F, E, k, dt, path = cfg
+    c = make_case(T=T, d=d, F=F, E=E, k=k, dt=dt)
+    dp, x_perm, offsets, _ = _ffn_inputs(c)
+    h = torch.zeros((c.A, F), dtype=torch_dtype(dt), device=DEV)
+    ws = workspace_for(c)
+    moe.expert_up(x_perm, c.w1, offsets, T, d, F, E, k, dt, h, ws, path=path)
+    st, _ = moe.get_device_status(ws)
+    assert st == moe.MOE_OK
+    ref = oracle.expert_rows_up(c.x64[dp["perm_token"]], dp["offsets"], c.w1_host())
+    assert rel_rms_err(to_f64(h), ref) < TOL[dt]
+
+
+@pytest.mark.parametrize("cfg", FFN_CASES, ids=lambda c: "T{}_d{}_F{}_E{}_dt{}_path{}".format(*c[:4], c[5], c[6]))
+def test_expert_down(cfg):
+    T, d, F, E, k, dt, path = cfg
+    c = make_case(T=T, d=d, F=F, E=E, k=k, dt=dt)
+    dp, _, offsets, row_gate = _ffn_inputs(c)
+    # h from the generator (stream 5), not from the GPU's up-projection
+    h = device_tensor((c.A, F), 0, 5, 1.0, dt, DEV)
+    y = torch.zeros((c.A, d), dtype=torch_dtype(dt), device=DEV)
+    ws = workspace_for(c)
+    moe.expert_down(h, c.w2, offsets, row_gate, T, d, F, E, k, dt, y, ws, path=path)
+    st, _ = moe.get_device_status(ws)
+    assert st == moe.MOE_OK
+    ref = oracle.expert_rows_down(to_f64(h), dp["offsets"], dp["row_gate"], c.w2_host())
+    assert rel_rms_err(to_f64(y), ref) < TOL[dt]
+
+
+@pytest.mark.parametrize("dt", [BF16, F32])
+def test_combine(dt):
+    T, d, k = 333, 136, 3
+    c = make_case(T=T, d=d, F=64, E=7, k=k, dt=dt)
+    ridx, rgate = oracle_routing(c)
+    dp = oracle.dispatch(ridx, c.E, rgate)
+    y = device_tensor((T * k, d), 0, 6, 1.0, dt, DEV)
+    out = torch.empty((T, d), dtype=torch_dtype(dt), device=DEV)
+    moe.combine(y, torch.from_numpy(dp["row_of"].astype(np.int32)).to(DEV), T, d, k, dt, out)
+    ref = oracle.combine(to_f64(y), dp["row_of"])
+    got = to_f64(out)
+    # one rounding of the fp32 sum: within a bf16 / fp32 half-ulp of the exact value (2x margin)
+    rel = 2.0 ** -8 if dt == BF16 else 2.0 ** -22
+    assert np.all(np.abs(got - ref) <= rel * np.abs(ref) + 1e-30)
+
+
+# ----------------------------------------------------------------------------- whole layer
+
+FORWARD_CASES = [
+    dict(T=64, d=128, F=256, E=8, k=2, dt=F32, path=moe.PATH_AUTO),          # the tiny fp32 layer
+    dict(T=640, d=256, F=512, E=16, k=2, dt=BF16, path=moe.PATH_AUTO),       # tensor-core path
+    dict(T=640, d=256, F=512, E=16, k=2, dt=BF16, path=moe.PATH_SIMT),
+    dict(T=600, d=320, F=704, E=6, k=2, dt=BF16, path=moe.PATH_TENSOR),
+    dict(T=384, d=512, F=1024, E=128, k=2, dt=BF16, path=moe.PATH_TENSOR),   # many nearly empty experts
+    dict(T=8, d=1024, F=1024, E=128, k=2, dt=BF16, path=moe.PATH_AUTO),      # decode-shaped: streaming path
+    dict(T=64, d=512, F=512, E=32, k=2, dt=BF16, path=moe.PATH_STREAM),
+    dict(T=8, d=512, F=512, E=32, k=2, dt=BF16, path=moe.PATH_TENSOR),       # decode shape on the tensor path
+    dict(T=1, d=256, F=256, E=16, k=2, dt=BF16, path=moe.PATH_AUTO),         # one token
+    dict(T=77, d=64, F=96, E=2, k=2, dt=F32, path=moe.PATH_AUTO),            # E = k
+    dict(T=50, d=64, F=64, E=1, k=1, dt=F32, path=moe.PATH_AUTO),            # a single dense expert
+    dict(T=93, d=8, F=8, E=4, k=1, dt=BF16, path=moe.PATH_TENSOR),           # smallest d, F
+    dict(T=40, d=64, F=64, E=1024, k=8, dt=BF16, path=moe.PATH_AUTO),        # largest E and k
+]
+
+
+def run_forward(c, path=moe.PATH_AUTO):
+    out = torch.empty((c.T, c.d), dtype=torch_dtype(c.dt), device=DEV)
+    idx = torch.empty((c.T, c.k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((c.T, c.k), dtype=torch.float32, device=DEV)
+    counts = torch.empty(c.E, dtype=torch.int32, device=DEV)
+    ws = workspace_for(c)
+    moe.forward(c.x, c.w_r, c.b_r, c.w1, c.w2, c.T, c.d, c.F, c.E, c.k, c.dt, out, ws, topk_idx=idx,
+                topk_gate=gate, counts=counts, path=path)
+    st, detail = moe.get_device_status(ws)
+    assert st == moe.MOE_OK, (st, detail)
+    return out, idx.cpu().numpy(), gate.cpu().numpy(), counts.cpu().numpy()
+
+
+@pytest.mark.parametrize("cfg", FORWARD_CASES,
+                         ids=lambda c: "T{T}_d{d}_F{F}_E{E}_k{k}_dt{dt}_path{path}".format(**c))
+def test_forward(cfg):
+    cfg = dict(cfg)
+    path = cfg.pop("path")
+    c = make_case(**cfg)
+    out, idx, gate, counts = run_forward(c, path)
+    ref = oracle.forward(c.x64, c.wr64, c.w1_host(), c.w2_host(), c.k, c.br64)
+    assert np.array_equal(idx, ref["idx"])
+    assert np.array_equal(counts, oracle.dispatch(ref["idx"], c.E)["counts"])
+    assert np.max(np.abs(gate - ref["gate"])) < 1e-5
+    assert rel_rms_err(to_f64(out), ref["out"]) < TOL[c.dt]
+
+
+def test_forward_all_tokens_to_one_expert():
+    b = np.zeros(8, np.float32)
+    b[3] = 50.0  # expert 3 is every token's first choice; the rest of the ranking is the plain router's
+    c = make_case(T=300, d=128, F=256, E=8, k=2, dt=BF16, bias=b)
+    out, idx, gate, counts = run_forward(c)
+    ref = oracle.forward(c.x64, c.wr64, c.w1_host(), c.w2_host(), 2, c.br64)
+    assert counts[3] == c.T
+    assert np.all(idx[:, 0] == 3)
+    assert np.array_equal(idx, ref["idx"])
+    assert rel_rms_err(to_f64(out), ref["out"]) < TOL[BF16]
+
+
+def test_forward_zero_tokens():
+    c = make_case(T=0, d=64, F=64, E=4, k=2, dt=BF16)
+    out = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(moe.workspace_bytes(0, 64, 64, 4, 2, BF16), dtype=torch.uint8, device=DEV)
+    moe.workspace_init(ws)
+    moe.forward(c.x, c.w_r, None, c.w1, c.w2, 0, 64, 64, 4, 2, BF16, out, ws)
+    assert moe.get_device_status(ws)[0] == moe.MOE_OK
+
+
+@pytest.mark.parametrize("path", [moe.PATH_TENSOR, moe.PATH_STREAM])
+def test_forward_is_bit_reproducible(path):
+    c = make_case(T=256, d=512, F=512, E=16, k=2, dt=BF16)
+    a = run_forward(c, path)[0]
+    b = run_forward(c, path)[0]
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_layer_object_matches_oracle():
+    c = make_case(T=200, d=256, F=512, E=8, k=2, dt=BF16)
+    layer = moe.MoELayer(c.w_r, c.w1, c.w2, k=2)
+    out = layer(c.x)
+    assert layer.device_status()[0] == moe.MOE_OK
+    ref = oracle.forward(c.x64, c.wr64, c.w1_host(), c.w2_host(), 2)
+    assert rel_rms_err(to_f64(out), ref["out"]) < TOL[BF16]
+
+
+def test_bounded_wait_times_out_without_fault():
+    ws = torch.empty(4096, dtype=torch.uint8, device=DEV)
+    moe.workspace_init(ws)
+    moe.selftest_wait_timeout(ws, 2000)
+    st, detail = moe.get_device_status(ws)
+    assert st == moe.MOE_ERR_DEVICE_TIMEOUT and detail == 99
+    # the context stays usable
+    c = make_case(T=16, d=64, F=64, E=4, k=2, dt=F32)
+    out, idx, _, _ = run_forward(c)
+    assert np.array_equal(idx, oracle_routing(c)[0])
+
+
+def test_device_generator_matches_host():
+    t = torch.empty(1 << 20, dtype=torch.bfloat16, device=DEV)
+    key = ig.stream_key(0, ig.STREAM_W1)
+    ig.fill_device(t, 5000, key, ig.sigma_for_fan_in(4096), BF16)
+    host = ig.draw(5000, 1 << 20, key, ig.sigma_for_fan_in(4096), BF16)
+    assert np.array_equal(t.view(torch.int16).cpu().numpy().view(np.uint16), host)
+    t32 = torch.empty(4099, dtype=torch.float32, device=DEV)
+    ig.fill_device(t32, 7, key, 1.0, F32)
+    assert np.array_equal(t32.cpu().numpy(), ig.draw(7, 4099, key, 1.0, F32))

@@ -209,6 +209,11 @@ def check_steps_compose_to_forward():
     rows = np.array([0, 5, 17, 41])
     part = om.expert_rows_ffn(x[dp["perm_token"]], dp["offsets"], dp["row_gate"], w1, w2, rows=rows)
     assert np.allclose(part, y_perm[rows], rtol=1e-13, atol=1e-15)
+    h = om.expert_rows_up(x[dp["perm_token"]], dp["offsets"], w1)
+    y2 = om.expert_rows_down(h, dp["offsets"], dp["row_gate"], w2)
+    assert np.allclose(y2, y_perm, rtol=1e-13, atol=1e-15)
+    h_part = om.expert_rows_up(x[dp["perm_token"]], dp["offsets"], w1, rows=rows)
+    assert np.allclose(h_part, h[rows], rtol=1e-13, atol=1e-15)
 
 
 def check_ambiguous_tokens():
@@ -339,5 +344,5 @@ def test_planted_mistakes(name, monkeypatch):
 
 def test_package_exports():
     for name in ["router_logits", "softmax", "topk_select", "gates_of", "gelu", "expert_ffn", "forward",
-                 "dense_forward", "dispatch", "expert_rows_ffn", "combine", "ambiguous_tokens", "top_share"]:
+                 "dense_forward", "dispatch", "expert_rows_ffn", "expert_rows_up", "expert_rows_down", "combine", "ambiguous_tokens", "top_share"]:
         assert callable(getattr(oracle, name))
