@@ -1,0 +1,504 @@
+#!/usr/bin/env python3
+"""Throughput of the sparse top-k MoE FFN layer's forward pass on GB300.
+
+One step = one full forward pass of the layer (router + softmax + top-k, dispatch,
+up-projection + GeLU, down-projection + gate, combine) over one batch of seeded
+synthetic tokens, through the library's C ABI. Prints one JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+value      tokens/s of the whole job, device-timed with CUDA events over exactly K steps of
+           moe_forward (inputs resident in HBM), max over ranks.
+e2e        the same metric through the public layer object with the host->device copy of the
+           step's tokens (pinned) and the device->host copy of its output inside the timed region.
+roofline   the dominant kernel, timed live with CUDA events around its own C ABI call on the
+           launching stream, against the measured peak in MEASURED_PEAKS.json.
+cpu_baseline  the fp64 oracle on the host cores on a bounded prefix of the same batch.
+--impl reference  the oracle alone, timed on the host cores, on the same workload and metric.
+
+With N > 1 (torchrun) every rank runs its own replica of the layer on its own GPU with its own
+batch (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s; % of BF16 tensor peak (prefill) / % HBM BW (decode)"
+DEFAULT_WORKLOAD = "e16_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS_PER_STEP = 8  # router 1, dispatch 4 (count, scan, scatter, gather), up 1, down 1, combine 1
+L2_BYTES = 126 * 2**20
+TC_SOURCES = ["sparse_mixture_experts_moe_gb300/csrc/ffn_tc.cu", "sparse_mixture_experts_moe_gb300/csrc/common.cuh"]
+STREAM_SOURCES = ["sparse_mixture_experts_moe_gb300/csrc/ffn_stream.cu",
+                  "sparse_mixture_experts_moe_gb300/csrc/common.cuh"]
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sources_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def stored_traffic(kernel, workload, src_paths):
+    """Per-launch DRAM bytes from the committed ncu summary, or None if absent or the kernel changed."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        entries = json.load(f)
+    sha = sources_sha(src_paths)
+    for e in entries:
+        if e.get("kernel") == kernel and e.get("workload") == workload and e.get("source_sha256") == sha:
+            return e.get("bytes_per_launch")
+    return None
+
+
+def workload_config(w):
+    wbytes = w.E * 2 * w.d * w.F * (2 if w.dtype == 1 else 4)
+    return {"workload": f"{w.name}: T={w.T} d={w.d} d_ff={w.F} E={w.E} top-{w.k}"
+                        + (" skewed router bias" if w.skew else ""),
+            "T": w.T, "d": w.d, "d_ff": w.F, "E": w.E, "k": w.k,
+            "l2": f"inputs larger than L2: {wbytes / 1e6:.0f} MB of expert weights vs {L2_BYTES / 2**20:.0f} MB L2",
+            "timing": "CUDA events on the launching stream, max over ranks"}
+
+
+# ----------------------------------------------------------------------------- inputs
+
+def make_inputs(w, device, seed=0):
+    import numpy as np
+    import torch
+    import inputgen as ig
+    from inputgen import workloads
+    tdt = torch.bfloat16 if w.dtype == ig.DTYPE_BF16 else torch.float32
+    s = torch.cuda.current_stream().cuda_stream
+
+    def fill(shape, stream_id, sigma):
+        t = torch.empty(shape, dtype=tdt, device=device)
+        ig.fill_device(t, 0, ig.stream_key(seed, stream_id), sigma, w.dtype, s)
+        return t
+
+    x = fill((w.T, w.d), ig.STREAM_X, 1.0)
+    w_r = fill((w.d, w.E), ig.STREAM_WR, ig.sigma_for_fan_in(w.d))
+    w1 = fill((w.E, w.d, w.F), ig.STREAM_W1, ig.sigma_for_fan_in(w.d))
+    w2 = fill((w.E, w.F, w.d), ig.STREAM_W2, ig.sigma_for_fan_in(w.F))
+    b_r = None
+    c = workloads.bias_scale(w)
+    if c is not None:
+        b_r = torch.from_numpy(ig.skew_bias(w.E, c)).to(device)
+    torch.cuda.synchronize()
+    return x, w_r, b_r, w1, w2
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (host-stamped) of SM clock and throttle reasons while the GPU works."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        def pick(lo, hi):
+            return [p for (t, p) in self.samples if lo <= t <= hi]
+        win = pick(t0 - 0.15, t1 + 0.15)
+        window = "timed region"
+        if len(win) < 1:
+            win = [p for (_, p) in self.samples]
+            window = "whole GPU phase (timed region shorter than the 100 ms sampling period)"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in win if num(p[0]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in win:
+            for name, v in zip(names, p[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(win[0][1]),
+                "power_w_max": max((num(p[2]) or 0.0) for p in win), "reasons": sorted(reasons),
+                "samples": len(win), "window": window}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def host_copy(w, x, w_r, b_r, w1, w2, tokens):
+    import numpy as np
+    return dict(x=x[:tokens].double().cpu().numpy(), w_r=w_r.double().cpu().numpy(),
+                b_r=None if b_r is None else b_r.double().cpu().numpy(),
+                w1=HostExperts(w1), w2=HostExperts(w2))
+
+
+class HostExperts:
+    """Expert matrices as exact fp64 host arrays, copied once before any timing."""
+
+    def __init__(self, t):
+        self.t = t
+        self.cache = {}
+
+    def preload(self, experts):
+        for e in experts:
+            if e not in self.cache:
+                self.cache[e] = self.t[e].double().cpu().numpy()
+
+    def __getitem__(self, e):
+        return self.cache[int(e)]
+
+
+def oracle_sample(w, x, w_r, b_r, w1, w2, target_s, max_tokens=None):
+    """Times oracle.forward on a prefix of the batch; returns (tokens/s, tokens, seconds, cores)."""
+    import numpy as np
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    max_tokens = w.T if max_tokens is None else min(max_tokens, w.T)
+    # keep the fp64 copies of the touched experts within ~6 GB of host memory
+    per_expert = 2 * w.d * w.F * 8
+    expert_budget = max(2, int(6e9 // per_expert))
+    n = min(max_tokens, 64 if w.E * per_expert > 6e9 else 256)
+    h = host_copy(w, x, w_r, b_r, w1, w2, max_tokens)
+
+    def run(ntok):
+        xs = h["x"][:ntok]
+        idx = oracle.topk_select(oracle.router_logits(xs, h["w_r"], h["b_r"]), w.k)
+        experts = sorted(set(int(e) for e in np.unique(idx)))
+        if len(experts) > expert_budget:
+            return None
+        h["w1"].preload(experts)
+        h["w2"].preload(experts)
+        t0 = time.perf_counter()
+        oracle.forward(xs, h["w_r"], h["w1"], h["w2"], w.k, h["b_r"])
+        return time.perf_counter() - t0
+
+    dt = run(n)
+    while dt is None and n > 1:
+        n = max(1, n // 2)
+        dt = run(n)
+    if dt is None:
+        raise RuntimeError("oracle sample: even one token touches more experts than the host budget")
+    while dt < target_s / 4 and n < max_tokens:
+        n2 = min(max_tokens, max(n + 1, int(n * min(8.0, target_s / max(dt, 1e-3)))))
+        dt2 = run(n2)
+        if dt2 is None:
+            break
+        n, dt = n2, dt2
+    return n / dt, n, dt, cores
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, w, rank, world, device):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import sparse_mixture_experts_moe_gb300 as moe
+
+    x, w_r, b_r, w1, w2 = make_inputs(w, device, seed=rank)
+    T, d, F, E, k, dt = w.T, w.d, w.F, w.E, w.k, w.dtype
+    A = T * k
+    out = torch.empty_like(x)
+    ws = torch.empty(moe.workspace_bytes(T, d, F, E, k, dt), dtype=torch.uint8, device=device)
+    moe.workspace_init(ws)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.forward(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws)
+
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else os.environ["CUDA_VISIBLE_DEVICES"].split(",")[torch.cuda.current_device()])
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    st, detail = moe.get_device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status after warm-up: {moe.status_string(st)} ({detail})")
+
+    # --- timed region: exactly K steps of moe_forward
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_total = float(ms_t.item())
+    ms_per_step = ms_total / args.steps
+    value = world * T / (ms_per_step / 1e3)
+
+    # --- per-kernel timing: the same step as its separate C ABI calls, events between them
+    idx = torch.empty((T, k), dtype=torch.int32, device=device)
+    gate = torch.empty((T, k), dtype=torch.float32, device=device)
+    counts = torch.empty(E, dtype=torch.int32, device=device)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=device)
+    perm = torch.empty(A, dtype=torch.int32, device=device)
+    row_of = torch.empty((T, k), dtype=torch.int32, device=device)
+    row_gate = torch.empty(A, dtype=torch.float32, device=device)
+    x_perm = torch.empty((A, d), dtype=x.dtype, device=device)
+    h = torch.empty((A, F), dtype=x.dtype, device=device)
+    y_perm = torch.empty((A, d), dtype=torch.float32, device=device)
+    names = ["router_topk", "dispatch", "expert_up", "expert_down", "combine"]
+    reps = max(args.steps, 10)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(reps)]
+    for r in range(reps):
+        e = evs[r]
+        e[0].record(stream)
+        moe.router_topk(x, w_r, b_r, T, d, E, k, dt, idx, gate)
+        e[1].record(stream)
+        moe.dispatch(x, idx, gate, T, d, E, k, dt, counts, offsets, perm, row_of, row_gate, x_perm, ws)
+        e[2].record(stream)
+        moe.expert_up(x_perm, w1, offsets, T, d, F, E, k, dt, h, ws)
+        e[3].record(stream)
+        moe.expert_down(h, w2, offsets, row_gate, T, d, F, E, k, dt, y_perm, ws)
+        e[4].record(stream)
+        moe.combine(y_perm, row_of, T, d, k, dt, out)
+        e[5].record(stream)
+    torch.cuda.synchronize()
+    kern_ms = {n: statistics.mean(evs[r][i].elapsed_time(evs[r][i + 1]) for r in range(reps))
+               for i, n in enumerate(names)}
+    counts_h = counts.cpu().numpy()
+    touched = int((counts_h > 0).sum())
+
+    # --- e2e: public layer object, pinned host tokens in, output back to the host, every step
+    layer = moe.MoELayer(w_r, w1, w2, k=k, b_r=b_r)
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    x_dev = torch.empty_like(x)
+    out_dev = torch.empty_like(out)
+    for _ in range(3):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer(x_dev, out=out_dev)
+        out_host.copy_(out_dev, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        layer(x_dev, out=out_dev)
+        out_host.copy_(out_dev, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1) / args.steps], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_value = world * T / (float(e2e_ms.item()) / 1e3)
+    st, detail = moe.get_device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status after timing: {moe.status_string(st)} ({detail})")
+    clocks.stop()
+    clk = clocks.summary(t_wall0, t_wall1)
+
+    # --- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    eb = 2 if dt == 1 else 4
+    dom = max(["expert_up", "expert_down"], key=lambda n: kern_ms[n])
+    stream_path = dt == 1 and A <= 256
+    if stream_path:
+        # weight streaming: bytes = touched experts' matrix + the routed rows in and out
+        if dom == "expert_up":
+            alg_bytes = touched * d * F * eb + A * d * eb + A * F * eb
+        else:
+            alg_bytes = touched * F * d * eb + A * F * eb + A * d * eb
+        achieved = alg_bytes / (kern_ms[dom] / 1e3) / 1e9
+        roof = {"kernel": f"ffn_stream_kernel ({dom})", "bound": "hbm", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": stored_traffic(f"ffn_stream_kernel<{1 if dom == 'expert_up' else 2}>", w.name,
+                                          STREAM_SOURCES),
+                "alg_bytes_per_launch": alg_bytes, "ms_per_launch": kern_ms[dom],
+                "peak_source": f"{peak_src} hbm_gbs"}
+    else:
+        alg_flops = 2.0 * A * d * F
+        achieved = alg_flops / (kern_ms[dom] / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"kernel": f"ffn_tc_kernel ({dom})", "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": stored_traffic(f"ffn_tc_kernel<{1 if dom == 'expert_up' else 2}>", w.name, TC_SOURCES),
+                "alg_flops_per_launch": alg_flops, "ms_per_launch": kern_ms[dom],
+                "peak_source": f"{peak_src} bf16_tflops (burst: the kernel runs in a short step)"}
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if dt == 1 else "f32", "data": "synthetic (seeded inputgen draws)",
+        "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "roofline": roof,
+        "kernel_ms": kern_ms,
+        "experts_touched": touched,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * x.element_size(),
+                "d2h_bytes_per_step": out.numel() * out.element_size()},
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, n, secs, cores = oracle_sample(w, x, w_r, b_r, w1, w2, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                  "sample": f"first {n} of the batch's {T} tokens, fp64 oracle forward, "
+                                            f"{secs:.2f} s"}
+    return result
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, w):
+    """The fp64 oracle on the host cores: K timed steps (after W untimed), each a bounded prefix of the batch."""
+    import torch
+    import oracle
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    if device == "cuda":
+        x, w_r, b_r, w1, w2 = make_inputs(w, device)
+    else:
+        x, w_r, b_r, w1, w2 = _cpu_inputs(w)
+    budget_per_step = 150.0 / max(1, args.steps + args.warmup)
+    v, n, secs, cores = oracle_sample(w, x, w_r, b_r, w1, w2, min(args.cpu_seconds, budget_per_step))
+    h = host_copy(w, x, w_r, b_r, w1, w2, n)
+    import numpy as np
+    idx = oracle.topk_select(oracle.router_logits(h["x"], h["w_r"], h["b_r"]), w.k)
+    experts = sorted(set(int(e) for e in np.unique(idx)))
+    h["w1"].preload(experts)
+    h["w2"].preload(experts)
+    for _ in range(args.warmup):
+        oracle.forward(h["x"], h["w_r"], h["w1"], h["w2"], w.k, h["b_r"])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward(h["x"], h["w_r"], h["w1"], h["w2"], w.k, h["b_r"])
+    secs = (time.perf_counter() - t0) / max(1, args.steps)
+    value = n / secs
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded inputgen draws)",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {n} of the batch's {w.T} tokens per step, fp64 oracle forward"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def _cpu_inputs(w):
+    import torch
+    import inputgen as ig
+    from inputgen import workloads
+    if w.E * w.d * w.F > (1 << 27):
+        raise RuntimeError("reference arm without a GPU supports only small workloads")
+    tdt = torch.bfloat16 if w.dtype == ig.DTYPE_BF16 else torch.float32
+
+    def draw(shape, sid, sigma):
+        import numpy as np
+        n = int(np.prod(shape))
+        a = ig.draw(0, n, ig.stream_key(0, sid), sigma, w.dtype)
+        t = torch.from_numpy(a.view(np.int16) if w.dtype == ig.DTYPE_BF16 else a)
+        return (t.view(torch.bfloat16) if w.dtype == ig.DTYPE_BF16 else t).reshape(shape)
+    x = draw((w.T, w.d), ig.STREAM_X, 1.0)
+    w_r = draw((w.d, w.E), ig.STREAM_WR, ig.sigma_for_fan_in(w.d))
+    w1 = draw((w.E, w.d, w.F), ig.STREAM_W1, ig.sigma_for_fan_in(w.d))
+    w2 = draw((w.E, w.F, w.d), ig.STREAM_W2, ig.sigma_for_fan_in(w.F))
+    c = workloads.bias_scale(w)
+    b_r = None if c is None else torch.from_numpy(ig.skew_bias(w.E, c))
+    return x, w_r, b_r, w1, w2
+
+
+def main():
+    args = parse_args()
+    from inputgen import workloads
+    w = workloads.get(args.workload)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, w)), flush=True)
+        return 0
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    res = run_ours(args, w, rank, world, device)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -17,9 +17,10 @@
  *    alone synchronises its stream). Tensors are dense row-major and 16-byte aligned.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
  *    Every call only enqueues work on it and returns.
- *  - Element type `dt`: MOE_DTYPE_F32 (x, W_r, W1, W2, out and the intermediates in
- *    fp32) or MOE_DTYPE_BF16 (those tensors in bf16, accumulation in fp32).
- *    Router bias, gates and row gates are always fp32; indices are int32.
+ *  - Element type `dt`: MOE_DTYPE_F32 (x, W_r, W1, W2, x_perm, h and out in fp32) or
+ *    MOE_DTYPE_BF16 (those tensors in bf16, accumulation in fp32). Router bias, gates,
+ *    row gates and the gated expert outputs y_perm are always fp32 (so the k-way sum of
+ *    the combine rounds once); indices are int32.
  *  - Limits: 0 <= T (T = 0 is a no-op), 1 <= k <= min(E, 8), E <= 1024,
  *    d and F multiples of 8 and >= 8, T*k < 2^31, T*max(d,F) < 2^40.
  *  - Host-side argument checks fail with MOE_ERR_INVALID_ARG before anything is
@@ -116,7 +117,7 @@ moe_status moe_expert_up_ex(const void* x_perm, const void* w1, const int32_t* o
  * moe_expert_down — grouped GEMM2 with the gate epilogue:  y_perm[r, :] = row_gate[r] * (h[r, :] W2[e]).
  *   csdn/6a919c0d §2.2 step 4 (each expert's output weighted by its confidence).
  * In:  h [T*k, F] (dt), w2 [E, F, d] (dt), offsets [E+1], row_gate [T*k] fp32.
- * Out: y_perm [T*k, d] (dt).
+ * Out: y_perm [T*k, d] fp32 (fp32 accumulation, gate multiplied in fp32, no rounding to dt).
  * Workspace: status word.
  */
 moe_status moe_expert_down(const void* h, const void* w2, const int32_t* offsets, const float* row_gate, int T,
@@ -129,7 +130,7 @@ moe_status moe_expert_down_ex(const void* h, const void* w2, const int32_t* offs
 /* ---------------------------------------------------------------------------------------------
  * moe_grouped_ffn — moe_expert_up then moe_expert_down, with h kept in the workspace.
  * In:  x_perm [T*k, d], w1 [E, d, F], w2 [E, F, d], offsets [E+1], row_gate [T*k].
- * Out: y_perm [T*k, d] (dt).
+ * Out: y_perm [T*k, d] fp32.
  */
 moe_status moe_grouped_ffn(const void* x_perm, const void* w1, const void* w2, const int32_t* offsets,
                            const float* row_gate, int T, int d, int F, int E, int k, moe_dtype dt, void* y_perm,
@@ -140,9 +141,10 @@ moe_status moe_grouped_ffn_ex(const void* x_perm, const void* w1, const void* w2
 
 /* ---------------------------------------------------------------------------------------------
  * moe_combine — out[t, :] = sum_{j = 0..k-1} y_perm[row_of[t, j], :], summed in fp32 in slot
- * order j = 0, 1, ..., then rounded once to dt (round-to-nearest-even for bf16).
+ * order j = 0, 1, ..., then rounded once to `dt`, the element type of `out` (round-to-nearest-even
+ * for bf16; fp32 keeps the sum as it is).
  *   csdn/6a462027 §4.2 step 7 (sum the expert outputs back per token, "scatter_add").
- * In:  y_perm [T*k, d] (dt), row_of [T, k] int32.  Out: out [T, d] (dt).
+ * In:  y_perm [T*k, d] fp32, row_of [T, k] int32.  Out: out [T, d] (dt).
  * A row_of entry outside [0, T*k) contributes nothing (dispatch writes -1 for a dropped item).
  */
 moe_status moe_combine(const void* y_perm, const int32_t* row_of, int T, int d, int k, moe_dtype dt, void* out,
@@ -151,14 +153,15 @@ moe_status moe_combine(const void* y_perm, const int32_t* row_of, int T, int d, 
 /* ---------------------------------------------------------------------------------------------
  * moe_forward — the whole layer: router_topk, dispatch, expert_up, expert_down, combine.
  * In:  x [T, d], w_r [d, E], b_r [E] or NULL, w1 [E, d, F], w2 [E, F, d].
- * Out: out [T, d] (dt). topk_idx [T, k], topk_gate [T, k] and counts [E] are optional copies of
- *      the routing (NULL: kept in the workspace only).
+ * Out: out [T, d] (dt; moe_forward_ex takes the output's element type `out_dt` separately, e.g.
+ *      fp32 output of a bf16 layer). topk_idx [T, k], topk_gate [T, k] and counts [E] are optional
+ *      copies of the routing (NULL: kept in the workspace only).
  */
 moe_status moe_forward(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2, int T,
                        int d, int F, int E, int k, moe_dtype dt, void* out, int32_t* topk_idx, float* topk_gate,
                        int32_t* counts, void* workspace, size_t ws_bytes, void* stream);
 moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2,
-                          int T, int d, int F, int E, int k, moe_dtype dt, moe_path path, void* out,
+                          int T, int d, int F, int E, int k, moe_dtype dt, moe_dtype out_dt, moe_path path, void* out,
                           int32_t* topk_idx, float* topk_gate, int32_t* counts, void* workspace, size_t ws_bytes,
                           void* stream);
 

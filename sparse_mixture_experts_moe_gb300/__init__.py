@@ -51,13 +51,16 @@ class MoELayer:
             self._ws_T = T
         return self._ws
 
-    def __call__(self, x, out: Optional["object"] = None, topk_idx=None, topk_gate=None, counts=None):
+    def __call__(self, x, out: Optional["object"] = None, topk_idx=None, topk_gate=None, counts=None,
+                 out_dtype=None):
+        """Forward pass of x [T, d]; the output is in x's dtype unless out / out_dtype say otherwise."""
         import torch
         T = int(x.shape[0])
         if out is None:
-            out = torch.empty_like(x)
+            out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=x.device)
         forward(x, self.w_r, self.b_r, self.w1, self.w2, T, self.d, self.F, self.E, self.k, self.dt, out,
-                self.workspace(T), topk_idx=topk_idx, topk_gate=topk_gate, counts=counts, path=self.path)
+                self.workspace(T), topk_idx=topk_idx, topk_gate=topk_gate, counts=counts, path=self.path,
+                out_dt=_lib.dtype_code(out))
         return out
 
     def device_status(self):

@@ -41,7 +41,7 @@ SIGNATURES = {
     "moe_grouped_ffn_ex": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
     "moe_combine": [_p, _p, _i, _i, _i, _i, _p, _p],
     "moe_forward": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _sz, _p],
-    "moe_forward_ex": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _sz, _p],
+    "moe_forward_ex": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _sz, _p],
     "moe_workspace_bytes": [_i, _i, _i, _i, _i, _i],
     "moe_workspace_init": [_p, _sz, _p],
     "moe_get_device_status": [_p, _p, _p],
@@ -168,8 +168,11 @@ def combine(y_perm, row_of, T, d, k, dt, out, stream=None, check=True):
 
 
 def forward(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws, topk_idx=None, topk_gate=None, counts=None,
-            path=PATH_AUTO, stream=None, check=True):
-    rc = lib().moe_forward_ex(_ptr(x), _ptr(w_r), _ptr(b_r), _ptr(w1), _ptr(w2), T, d, F, E, k, dt, path, _ptr(out),
+            path=PATH_AUTO, out_dt=None, stream=None, check=True):
+    """out_dt: element type of `out` (default: dt)."""
+    out_dt = dt if out_dt is None else out_dt
+    rc = lib().moe_forward_ex(_ptr(x), _ptr(w_r), _ptr(b_r), _ptr(w1), _ptr(w2), T, d, F, E, k, dt, out_dt, path,
+                              _ptr(out),
                               _ptr(topk_idx), _ptr(topk_gate), _ptr(counts), _ptr(ws),
                               ws.numel() * ws.element_size(), _stream(stream))
     return _check(rc, "moe_forward") if check else rc

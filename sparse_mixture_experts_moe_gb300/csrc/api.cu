@@ -47,7 +47,7 @@ struct Layout {
     h = o; o += align256(A * F * eb);
     grouped_end = o;
     x_perm = o; o += align256(A * d * eb);
-    y_perm = o; o += align256(A * d * eb);
+    y_perm = o; o += align256(A * d * 4);
     end = o;
     ffn_end = align256(kWsHeaderBytes);
   }
@@ -238,10 +238,11 @@ moe_status moe_combine(const void* y_perm, const int32_t* row_of, int T, int d, 
 }
 
 moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2,
-                          int T, int d, int F, int E, int k, moe_dtype dt, moe_path path, void* out,
-                          int32_t* topk_idx, float* topk_gate, int32_t* counts, void* workspace, size_t ws_bytes,
-                          void* stream) {
+                          int T, int d, int F, int E, int k, moe_dtype dt, moe_dtype out_dt, moe_path path,
+                          void* out, int32_t* topk_idx, float* topk_gate, int32_t* counts, void* workspace,
+                          size_t ws_bytes, void* stream) {
   if (!sizes_ok(T, d, F, E, k, dt) || !path_ok(path, dt)) return MOE_ERR_INVALID_ARG;
+  if (out_dt != MOE_DTYPE_F32 && out_dt != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   if (workspace == nullptr || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
   const Layout L(T, d, F, E, k, dt);
   if (ws_bytes < L.end) return MOE_ERR_INVALID_ARG;
@@ -267,13 +268,13 @@ moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, cons
   if (st != MOE_OK) return st;
   st = moe_expert_down_ex(h, w2, offs, rgate, T, d, F, E, k, dt, path, yp, workspace, ws_bytes, stream);
   if (st != MOE_OK) return st;
-  return moe_combine(yp, rowof, T, d, k, dt, out, stream);
+  return moe_combine(yp, rowof, T, d, k, out_dt, out, stream);
 }
 moe_status moe_forward(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2, int T,
                        int d, int F, int E, int k, moe_dtype dt, void* out, int32_t* topk_idx, float* topk_gate,
                        int32_t* counts, void* workspace, size_t ws_bytes, void* stream) {
-  return moe_forward_ex(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, MOE_PATH_AUTO, out, topk_idx, topk_gate, counts,
-                        workspace, ws_bytes, stream);
+  return moe_forward_ex(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, dt, MOE_PATH_AUTO, out, topk_idx, topk_gate,
+                        counts, workspace, ws_bytes, stream);
 }
 
 moe_status moe_selftest_wait_timeout(void* workspace, size_t ws_bytes, int timeout_us, void* stream) {

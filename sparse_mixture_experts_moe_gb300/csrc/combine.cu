@@ -2,19 +2,14 @@
 // csdn/6a462027 §4.2 step 7 (sum the expert outputs back per token). The gate was
 // already applied per row by the down-projection epilogue.
 //
-// One warp per token; each lane owns groups of 8 consecutive elements (16 bytes
-// of bf16, 32 bytes of fp32) and reads them with 128-bit loads.
+// One warp per token; each lane owns groups of 8 consecutive columns and reads the
+// fp32 rows with 128-bit loads.
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace moe {
 namespace {
 
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
-  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
-  v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
-  v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
-}
 __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
   const float4 a = __ldg(reinterpret_cast<const float4*>(p));
   const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
@@ -31,9 +26,10 @@ __device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
   reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
+// y_perm is fp32 for every element type, so the output is rounded exactly once.
 template <typename T>
 __global__ void __launch_bounds__(256)
-combine_kernel(const T* __restrict__ y_perm, const int32_t* __restrict__ row_of, int Tn, int d, int k, int A,
+combine_kernel(const float* __restrict__ y_perm, const int32_t* __restrict__ row_of, int Tn, int d, int k, int A,
                T* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -72,7 +68,7 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* row_of, int Tn, in
   if (blocks > cap) blocks = cap;
   const int A = Tn * k;
   if (dt == MOE_DTYPE_BF16)
-    combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>((const __nv_bfloat16*)y_perm, row_of, Tn, d, k, A,
+    combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>((const float*)y_perm, row_of, Tn, d, k, A,
                                                          (__nv_bfloat16*)out);
   else
     combine_kernel<float><<<blocks, 256, 0, s>>>((const float*)y_perm, row_of, Tn, d, k, A, (float*)out);

@@ -12,10 +12,11 @@ namespace {
 
 constexpr int BM = 64, BN = 64, BK = 16;
 
-template <typename T, int STAGE>
+// up (STAGE 1) writes h in the layer's element type; down (STAGE 2) writes fp32 y_perm.
+template <typename T, int STAGE, typename OutT>
 __global__ void __launch_bounds__(256)
 ffn_simt_kernel(const T* __restrict__ a, const T* __restrict__ w, const int32_t* __restrict__ offsets,
-                const float* __restrict__ row_gate, int K, int N, int E, T* __restrict__ out) {
+                const float* __restrict__ row_gate, int K, int N, int E, OutT* __restrict__ out) {
   __shared__ float sA[BK][BM + 4];
   __shared__ float sB[BK][BN + 4];
   __shared__ int s_e, s_m0, s_mend;
@@ -74,7 +75,7 @@ ffn_simt_kernel(const T* __restrict__ a, const T* __restrict__ w, const int32_t*
       const int gn = n0 + tc * 4 + j;
       if (gn >= N) continue;
       const float v = STAGE == 1 ? gelu_erf(acc[i][j]) : g * acc[i][j];
-      out[(size_t)gr * N + gn] = from_f32<T>(v);
+      out[(size_t)gr * N + gn] = from_f32<OutT>(v);
     }
   }
 }
@@ -85,11 +86,11 @@ cudaError_t launch_t(const FfnArgs& p, cudaStream_t s) {
   dim3 grid((p.N + BN - 1) / BN, max_items);
   if (max_items > 65535) return cudaErrorInvalidConfiguration;
   if (p.stage == 1)
-    ffn_simt_kernel<T, 1><<<grid, 256, 0, s>>>((const T*)p.a, (const T*)p.w, p.offsets, p.row_gate, p.K, p.N, p.E,
-                                               (T*)p.out);
+    ffn_simt_kernel<T, 1, T><<<grid, 256, 0, s>>>((const T*)p.a, (const T*)p.w, p.offsets, p.row_gate, p.K, p.N,
+                                                  p.E, (T*)p.out);
   else
-    ffn_simt_kernel<T, 2><<<grid, 256, 0, s>>>((const T*)p.a, (const T*)p.w, p.offsets, p.row_gate, p.K, p.N, p.E,
-                                               (T*)p.out);
+    ffn_simt_kernel<T, 2, float><<<grid, 256, 0, s>>>((const T*)p.a, (const T*)p.w, p.offsets, p.row_gate, p.K,
+                                                      p.N, p.E, (float*)p.out);
   return cudaGetLastError();
 }
 

@@ -32,11 +32,12 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
   v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
 }
 
-template <int STAGE>
+// up (STAGE 1) writes bf16 h; down (STAGE 2) writes fp32 y_perm.
+template <int STAGE, typename OutT>
 __global__ void __launch_bounds__(kThreads)
 ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ w,
                   const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
-                  __nv_bfloat16* __restrict__ out) {
+                  OutT* __restrict__ out) {
   extern __shared__ __align__(16) float smem[];
   float* sA = smem;                         // [RMAX][KC]
   float* sRed = sA + RMAX * KC;             // [kWarps][RMAX][NS]
@@ -135,16 +136,16 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __re
         for (int wi = 0; wi < kWarps; ++wi) v += sRed[(wi * RMAX + r) * NS + c];
         const int grow = rp + r;
         v = STAGE == 1 ? gelu_erf(v) : row_gate[grow] * v;
-        out[(size_t)grow * N + gn] = __float2bfloat16_rn(v);
+        out[(size_t)grow * N + gn] = from_f32<OutT>(v);
       }
     }
   }
 }
 
-template <int STAGE>
+template <int STAGE, typename OutT>
 cudaError_t launch_t(const FfnArgs& p, cudaStream_t s) {
   const size_t smem = (size_t)(RMAX * KC + kWarps * RMAX * NS) * sizeof(float) + (size_t)p.E * sizeof(int);
-  auto kern = ffn_stream_kernel<STAGE>;
+  auto kern = ffn_stream_kernel<STAGE, OutT>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int nslab = (p.N + NS - 1) / NS;
@@ -152,7 +153,7 @@ cudaError_t launch_t(const FfnArgs& p, cudaStream_t s) {
   long long grid = (long long)device_sm_count() * 4;
   if (grid > max_units) grid = max_units;
   kern<<<(int)grid, kThreads, smem, s>>>((const __nv_bfloat16*)p.a, (const __nv_bfloat16*)p.w, p.offsets,
-                                         p.row_gate, p.K, p.N, p.E, (__nv_bfloat16*)p.out);
+                                         p.row_gate, p.K, p.N, p.E, (OutT*)p.out);
   return cudaGetLastError();
 }
 
@@ -161,7 +162,7 @@ cudaError_t launch_t(const FfnArgs& p, cudaStream_t s) {
 cudaError_t launch_ffn_stream(const FfnArgs& p, cudaStream_t s) {
   if (p.rows == 0) return cudaSuccess;
   if (p.dt != MOE_DTYPE_BF16) return cudaErrorNotSupported;
-  return p.stage == 1 ? launch_t<1>(p, s) : launch_t<2>(p, s);
+  return p.stage == 1 ? launch_t<1, __nv_bfloat16>(p, s) : launch_t<2, float>(p, s);
 }
 
 }  // namespace moe

@@ -5,7 +5,7 @@
 //
 // out[r, n] = epi( sum_k a[r, k] * w[e][k, n] ) for every row r of expert e's range.
 //   up   (stage 1): a = x_perm [rows, d], w = W1 [E, d, F], epi = GeLU (erf form)
-//   down (stage 2): a = h [rows, F],      w = W2 [E, F, d], epi = row_gate[r] * .
+//   down (stage 2): a = h [rows, F],      w = W2 [E, F, d], epi = row_gate[r] * ., fp32 output
 //
 // Tiles: 128 rows x 256 columns x 64-deep k-blocks, one tcgen05.mma of M=128, N=256, K=16
 // per 16 k. A tiles are K-major, B tiles MN-major (the weights are stored [K, N], N
@@ -16,7 +16,8 @@
 // Persistent CTAs, one per SM, 6 warps:
 //   warp 0      TMA producer (one lane): A tile + 4 B sub-tiles per stage, 4 stages
 //   warp 1      TMEM allocator and MMA issuer (one lane)
-//   warps 2..5  epilogue: tcgen05.ld -> GeLU / gate -> bf16 -> swizzled staging -> TMA store
+//   warps 2..5  epilogue: tcgen05.ld -> GeLU -> bf16 (up) or gate -> fp32 (down) -> swizzled
+//               staging -> TMA store
 // Work items are (expert, 256-column block, 128-row tile), the row tile fastest, so the
 // CTAs that run at the same time share the same weight tile (read once from HBM, then from
 // L2). The item list is derived on the device from `offsets`: no host round trip.
@@ -90,11 +91,18 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
 }
 
 template <int STAGE>
+struct EpiOut { using T = __nv_bfloat16; };
+template <>
+struct EpiOut<2> { using T = float; };
+
+template <int STAGE>
 __global__ void __launch_bounds__(kThreads, 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              const __grid_constant__ CUtensorMap tmC, __nv_bfloat16* __restrict__ out,
+              const __grid_constant__ CUtensorMap tmC, typename EpiOut<STAGE>::T* __restrict__ out,
               const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
               int* status, uint64_t timeout_ns) {
+  using OutT = typename EpiOut<STAGE>::T;
+  constexpr int CW = 128 / (int)sizeof(OutT);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -224,22 +232,28 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       const bool group_full = it.row0 + 32 * q + 31 < it.row_end;
       float g = 1.f;
       if (STAGE == 2 && row_ok) g = row_gate[grow];
-      for (int c = 0; c < BN; c += 64) {
+      // One staging row is 128 bytes: 64 bf16 columns (up) or 32 fp32 columns (down).
+      for (int c = 0; c < BN; c += CW) {
         if (it.n0 + c >= N) break;
-        uint32_t v0[32], v1[32];
         const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN + c);
-        tmem_ld_32x32b_x32(taddr, v0);
-        tmem_ld_32x32b_x32(taddr + 32, v1);
-        tmem_ld_wait();
         uint32_t packed[32];
+        if (STAGE == 1) {
+          uint32_t v0[32], v1[32];
+          tmem_ld_32x32b_x32(taddr, v0);
+          tmem_ld_32x32b_x32(taddr + 32, v1);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float f0 = __uint_as_float(v0[2 * i]), f1 = __uint_as_float(v0[2 * i + 1]);
-          float h0 = __uint_as_float(v1[2 * i]), h1 = __uint_as_float(v1[2 * i + 1]);
-          if (STAGE == 1) { f0 = gelu_erf(f0); f1 = gelu_erf(f1); h0 = gelu_erf(h0); h1 = gelu_erf(h1); }
-          else { f0 *= g; f1 *= g; h0 *= g; h1 *= g; }
-          packed[i] = pack_bf16x2(f0, f1);
-          packed[16 + i] = pack_bf16x2(h0, h1);
+          for (int i = 0; i < 16; ++i) {
+            packed[i] = pack_bf16x2(gelu_erf(__uint_as_float(v0[2 * i])), gelu_erf(__uint_as_float(v0[2 * i + 1])));
+            packed[16 + i] =
+                pack_bf16x2(gelu_erf(__uint_as_float(v1[2 * i])), gelu_erf(__uint_as_float(v1[2 * i + 1])));
+          }
+        } else {
+          uint32_t v0[32];
+          tmem_ld_32x32b_x32(taddr, v0);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) packed[i] = __float_as_uint(g * __uint_as_float(v0[i]));
         }
         if (group_full) {
           if (lane == 0) bulk_wait_group_read0();  // the previous store has finished reading the buffer
@@ -259,11 +273,12 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           }
         } else if (row_ok) {
           // The 32-row group straddles the end of the expert's rows: plain stores of the valid rows.
-          __nv_bfloat16* dst = out + (size_t)grow * N + it.n0 + c;
+          OutT* dst = out + (size_t)grow * N + it.n0 + c;
+          constexpr int per16 = 16 / (int)sizeof(OutT);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            if (it.n0 + c + 8 * j < N)
-              *reinterpret_cast<uint4*>(dst + 8 * j) =
+            if (it.n0 + c + per16 * j < N)
+              *reinterpret_cast<uint4*>(dst + per16 * j) =
                   make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
         }
       }
@@ -317,11 +332,11 @@ EncodeTiledFn tensor_map_encoder() {
   return fn;
 }
 
-// bf16 tensor map, 128-byte swizzle, zero fill outside the tensor.
-bool encode_bf16(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
-                 const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+// Tensor map with 128-byte swizzle, zero fill outside the tensor.
+bool encode(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType type, const void* ptr, int rank,
+            const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box) {
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims,
+  const CUresult r = enc(m, type, (cuuint32_t)rank, const_cast<void*>(ptr), dims,
                          strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -339,19 +354,23 @@ cudaError_t launch_ffn_tensor(const FfnArgs& p, cudaStream_t s) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.rows};
     const cuuint64_t str[1] = {(cuuint64_t)p.K * 2};
     const cuuint32_t box[2] = {BK, BM};
-    if (!encode_bf16(enc, &tmA, p.a, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode(enc, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.K, (cuuint64_t)p.E};
     const cuuint64_t str[2] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.K * p.N * 2};
     const cuuint32_t box[3] = {64, BK, 1};
-    if (!encode_bf16(enc, &tmB, p.w, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode(enc, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.w, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
+    // up writes bf16 h (64-column boxes), down writes fp32 y_perm (32-column boxes): 128-byte rows
+    const bool f32_out = p.stage == 2;
     const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.rows};
-    const cuuint64_t str[1] = {(cuuint64_t)p.N * 2};
-    const cuuint32_t box[2] = {64, 32};
-    if (!encode_bf16(enc, &tmC, p.out, 2, dims, str, box)) return cudaErrorInvalidValue;
+    const cuuint64_t str[1] = {(cuuint64_t)p.N * (f32_out ? 4 : 2)};
+    const cuuint32_t box[2] = {f32_out ? 32u : 64u, 32};
+    if (!encode(enc, &tmC, f32_out ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.out, 2,
+                dims, str, box))
+      return cudaErrorInvalidValue;
   }
   const size_t smem = smem_bytes_for(p.E);
   const int NB = (p.N + BN - 1) / BN;
@@ -367,7 +386,7 @@ cudaError_t launch_ffn_tensor(const FfnArgs& p, cudaStream_t s) {
   } else {
     err = cudaFuncSetAttribute(ffn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    ffn_tc_kernel<2><<<grid, kThreads, smem, s>>>(tmA, tmB, tmC, (__nv_bfloat16*)p.out, p.offsets, p.row_gate,
+    ffn_tc_kernel<2><<<grid, kThreads, smem, s>>>(tmA, tmB, tmC, (float*)p.out, p.offsets, p.row_gate,
                                                   p.K, p.N, p.E, p.status, p.timeout_ns);
   }
   return cudaGetLastError();
