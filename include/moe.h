@@ -99,6 +99,28 @@ moe_status moe_dispatch(const void* x, const int32_t* topk_idx, const float* top
                         void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * moe_dispatch_noalloc — moe_dispatch without a workspace, for callers that cannot provide device
+ *   scratch memory: a plugin that its host framework gives only input and output buffers (the
+ *   framework owns all device memory through its own pool), or a latency-critical loop that must
+ *   not call cudaMalloc, which can block and synchronise the device. The pages have no counterpart
+ *   of this call; it exists for such callers only.
+ * Same inputs, outputs and results as moe_dispatch (bit for bit). The per-chunk count tables live in
+ *   a fixed 1 MiB array inside the library's own device memory, one copy per GPU that loads the
+ *   library, held until the process exits. Limit: ceil(T*k / 256) * E <= 131072 (for example
+ *   T*k <= 262144 with E = 128, T*k <= 32768 with E = 1024); larger sizes return
+ *   MOE_ERR_INVALID_ARG before anything is launched. Nothing is allocated and nothing is freed.
+ * The first call on each device looks up the array's device address (host code cannot use the
+ *   array's name as a pointer) and caches it; make that first call before any stream capture.
+ * Every call on a device shares the array and leaves its contents behind; each call rewrites all
+ *   it reads, so no clearing is needed between calls, but calls whose kernels overlap on the GPU
+ *   (e.g. on two streams at once) race on it and must not be issued that way.
+ * An index outside [0, E) is dropped (row_of entry -1, offsets[E] < T*k); no status word is kept.
+ */
+moe_status moe_dispatch_noalloc(const void* x, const int32_t* topk_idx, const float* topk_gate, int T, int d,
+                                int E, int k, moe_dtype dt, int32_t* counts, int32_t* offsets, int32_t* perm_token,
+                                int32_t* row_of, float* row_gate, void* x_perm, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * moe_expert_up — grouped GEMM1 with the GeLU epilogue:  h[r, :] = GeLU(x_perm[r, :] W1[e])
  * for every row r in expert e's range [offsets[e], offsets[e+1]).
  *   csdn/6a462027 §3.2 (homogeneous d -> d_ff -> d GELU experts with their own W1, W2) and §4.2

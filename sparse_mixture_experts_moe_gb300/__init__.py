@@ -16,7 +16,7 @@ from . import _lib
 from ._lib import (  # noqa: F401
     MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK, MOE_ERR_DEVICE_TIMEOUT,
     MOE_DTYPE_F32, MOE_DTYPE_BF16, PATH_AUTO, PATH_TENSOR, PATH_STREAM, PATH_SIMT, MoeError,
-    router_topk, dispatch, expert_up, expert_down, grouped_ffn, combine, forward, workspace_bytes, workspace_init,
+    router_topk, dispatch, dispatch_noalloc, expert_up, expert_down, grouped_ffn, combine, forward, workspace_bytes, workspace_init,
     get_device_status, status_string, selftest_wait_timeout, lib,
 )
 

@@ -33,6 +33,7 @@ _sz = ctypes.c_size_t
 SIGNATURES = {
     "moe_router_topk": [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _p],
     "moe_dispatch": [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _sz, _p],
+    "moe_dispatch_noalloc": [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p],
     "moe_expert_up": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
     "moe_expert_up_ex": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
     "moe_expert_down": [_p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
@@ -141,6 +142,15 @@ def dispatch(x, topk_idx, topk_gate, T, d, E, k, dt, counts, offsets, perm_token
                             _ptr(perm_token), _ptr(row_of), _ptr(row_gate), _ptr(x_perm), _ptr(ws),
                             ws.numel() * ws.element_size(), _stream(stream))
     return _check(rc, "moe_dispatch") if check else rc
+
+
+def dispatch_noalloc(x, topk_idx, topk_gate, T, d, E, k, dt, counts, offsets, perm_token, row_of, row_gate,
+                     x_perm, stream=None, check=True):
+    """moe_dispatch without a workspace: the count tables live in the library's fixed per-GPU array."""
+    rc = lib().moe_dispatch_noalloc(_ptr(x), _ptr(topk_idx), _ptr(topk_gate), T, d, E, k, dt, _ptr(counts),
+                                    _ptr(offsets), _ptr(perm_token), _ptr(row_of), _ptr(row_gate), _ptr(x_perm),
+                                    _stream(stream))
+    return _check(rc, "moe_dispatch_noalloc") if check else rc
 
 
 def expert_up(x_perm, w1, offsets, T, d, F, E, k, dt, h, ws, path=PATH_AUTO, stream=None, check=True):
