@@ -75,7 +75,11 @@ typedef enum {
  * Out: topk_idx [T, k] int32, topk_gate [T, k] fp32. Slot j holds the (j+1)-th largest logit;
  *      equal logits go to the lower expert index. gate = softmax probability (fp32 logits,
  *      fp32 softmax), not renormalised over the k experts.
- * Errors: MOE_ERR_INVALID_ARG on bad sizes/pointers. No device-side checks.
+ * Kernels: bf16 with E <= 256 and E % 8 == 0 computes the logits on the tensor cores (tcgen05,
+ *      fp32 accumulation in TMEM), one token per epilogue thread; other layers use a CUDA-core
+ *      kernel (fp32 FMA). Both select on fp32 logits.
+ * Errors: MOE_ERR_INVALID_ARG on bad sizes/pointers. This call keeps no status word (it has no
+ *      workspace); within moe_forward a timed-out device wait is reported through the workspace.
  */
 moe_status moe_router_topk(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
                            moe_dtype dt, int32_t* topk_idx, float* topk_gate, void* stream);

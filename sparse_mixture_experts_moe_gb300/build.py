@@ -21,7 +21,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
 
-LIB_SOURCES = ["api.cu", "router.cu", "dispatch.cu", "dispatch_noalloc.cu", "ffn_simt.cu", "ffn_stream.cu",
+LIB_SOURCES = ["api.cu", "router.cu", "router_tc.cu", "dispatch.cu", "dispatch_noalloc.cu", "ffn_simt.cu", "ffn_stream.cu",
                "ffn_tc.cu", "combine.cu"]
 LIB_PATH = os.path.join(PKG, "libmoe.so")
 INPUTGEN_SRC = os.path.join(ROOT, "inputgen", "fill.cu")

@@ -147,7 +147,8 @@ moe_status moe_router_topk(const void* x, const void* w_r, const float* b_r, int
   if (T == 0) return MOE_OK;
   if (x == nullptr || w_r == nullptr || topk_idx == nullptr || topk_gate == nullptr) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, topk_idx, topk_gate, (cudaStream_t)stream));
+  return cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, topk_idx, topk_gate, nullptr,
+                                        wait_timeout_ns(), (cudaStream_t)stream));
 }
 
 moe_status moe_dispatch(const void* x, const int32_t* topk_idx, const float* topk_gate, int T, int d, int E,
@@ -260,7 +261,8 @@ moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, cons
   void* xp = at<void>(workspace, L.x_perm);
   void* h = at<void>(workspace, L.h);
   void* yp = at<void>(workspace, L.y_perm);
-  moe_status st = moe_router_topk(x, w_r, b_r, T, d, E, k, dt, idx, gate, stream);
+  moe_status st = cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, idx, gate, at<int>(workspace, 0),
+                                                 wait_timeout_ns(), (cudaStream_t)stream));
   if (st != MOE_OK) return st;
   st = moe_dispatch(x, idx, gate, T, d, E, k, dt, cnt, offs, perm, rowof, rgate, xp, workspace, ws_bytes, stream);
   if (st != MOE_OK) return st;

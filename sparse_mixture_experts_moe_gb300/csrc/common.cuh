@@ -88,6 +88,27 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// Bounded wait shared by the warps of one CTA: gives up when another warp has raised
+// *abort_flag, or after timeout_ns, in which case it records MOE_ERR_DEVICE_TIMEOUT
+// (detail = role) and raises the flag so the other warps unwind too.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                              volatile int* abort_flag, int* status, int role) {
+#pragma unroll 1
+  for (int i = 0; i < 256; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      record_error(status, MOE_ERR_DEVICE_TIMEOUT, role);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");

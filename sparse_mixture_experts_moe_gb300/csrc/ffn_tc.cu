@@ -72,24 +72,6 @@ __device__ __forceinline__ Item decode_item(int w, const int* P, int E, int NB, 
   return it;
 }
 
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
-                                              volatile int* abort_flag, int* status, int role) {
-#pragma unroll 1
-  for (int i = 0; i < 256; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-#pragma unroll 1
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > timeout_ns) {
-      record_error(status, MOE_ERR_DEVICE_TIMEOUT, role);
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
-
 template <int STAGE>
 struct EpiOut { using T = __nv_bfloat16; };
 template <>
@@ -315,9 +297,7 @@ __global__ void selftest_wait_kernel(int* status, uint64_t timeout_ns) {
   __syncthreads();
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+}  // namespace
 
 EncodeTiledFn tensor_map_encoder() {
   static EncodeTiledFn fn = []() -> EncodeTiledFn {
@@ -332,17 +312,14 @@ EncodeTiledFn tensor_map_encoder() {
   return fn;
 }
 
-// Tensor map with 128-byte swizzle, zero fill outside the tensor.
-bool encode(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType type, const void* ptr, int rank,
-            const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+bool encode_tmap(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType type, const void* ptr, int rank,
+                 const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box) {
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = enc(m, type, (cuuint32_t)rank, const_cast<void*>(ptr), dims,
-                         strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = enc(m, type, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides_bytes, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 cudaError_t launch_ffn_tensor(const FfnArgs& p, cudaStream_t s) {
   if (p.rows == 0) return cudaSuccess;
@@ -354,13 +331,13 @@ cudaError_t launch_ffn_tensor(const FfnArgs& p, cudaStream_t s) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.rows};
     const cuuint64_t str[1] = {(cuuint64_t)p.K * 2};
     const cuuint32_t box[2] = {BK, BM};
-    if (!encode(enc, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_tmap(enc, &tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.K, (cuuint64_t)p.E};
     const cuuint64_t str[2] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.K * p.N * 2};
     const cuuint32_t box[3] = {64, BK, 1};
-    if (!encode(enc, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.w, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!encode_tmap(enc, &tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.w, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     // up writes bf16 h (64-column boxes), down writes fp32 y_perm (32-column boxes): 128-byte rows
@@ -368,7 +345,7 @@ cudaError_t launch_ffn_tensor(const FfnArgs& p, cudaStream_t s) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.rows};
     const cuuint64_t str[1] = {(cuuint64_t)p.N * (f32_out ? 4 : 2)};
     const cuuint32_t box[2] = {f32_out ? 32u : 64u, 32};
-    if (!encode(enc, &tmC, f32_out ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.out, 2,
+    if (!encode_tmap(enc, &tmC, f32_out ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.out, 2,
                 dims, str, box))
       return cudaErrorInvalidValue;
   }

@@ -9,8 +9,10 @@ namespace moe {
 // Dispatch processes the T*k assignments in chunks of this many (one CTA each).
 constexpr int kDispatchChunk = 256;
 
+// status (nullable) receives a device-side wait timeout of the tensor-core router.
 cudaError_t launch_router_topk(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
-                               int dt, int32_t* idx, float* gate, cudaStream_t s);
+                               int dt, int32_t* idx, float* gate, int* status, uint64_t timeout_ns,
+                               cudaStream_t s);
 
 // blk_counts / blk_base: [ceil(A / kDispatchChunk), E] int32 scratch each.
 cudaError_t launch_dispatch(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
@@ -39,6 +41,19 @@ cudaError_t launch_ffn_stream(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_ffn_tensor(const FfnArgs& a, cudaStream_t s);
 
 cudaError_t launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s);
+
+// Router on the tensor cores (bf16, E <= 256, E % 8 == 0). Returns cudaErrorNotSupported otherwise.
+cudaError_t launch_router_tc(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
+                             int32_t* idx, float* gate, int* status, uint64_t timeout_ns, cudaStream_t s);
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link-time driver dependency).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
+// Tiled tensor map with 128-byte swizzle and zero fill outside the tensor.
+bool encode_tmap(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType type, const void* ptr, int rank,
+                 const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box);
 
 int device_sm_count();
 

@@ -1,6 +1,8 @@
 // Router: logits = x W_r (+ b_r), softmax over the E experts, deterministic top-k.
 // csdn/6a919c0d §2.2 steps 1-4; aicoding/6a320eef §3.2; csdn/6a919c0d §4.2 (max subtraction).
 //
+// CUDA-core version, for fp32 layers and for E > 256 or E not a multiple of 8; bf16
+// layers with E <= 256 use the tensor-core router in router_tc.cu.
 // One CTA = 4 warps and 4*TPW tokens. W_r is staged through shared memory in
 // 32-row slabs (as fp32) and shared by every token of the CTA; lane l owns four
 // consecutive experts of the current 128-expert chunk and TPW tokens, so each
@@ -136,8 +138,14 @@ cudaError_t launch_router_t(const void* x, const void* w_r, const float* b_r, in
 }  // namespace
 
 cudaError_t launch_router_topk(const void* x, const void* w_r, const float* b_r, int Tn, int d, int E, int k,
-                               int dt, int32_t* idx, float* gate, cudaStream_t s) {
+                               int dt, int32_t* idx, float* gate, int* status, uint64_t timeout_ns,
+                               cudaStream_t s) {
   if (Tn == 0) return cudaSuccess;
+  // bf16 with E <= 256 (E % 8 == 0 for TMA row strides): tensor cores; otherwise this CUDA-core kernel.
+  if (dt == MOE_DTYPE_BF16 && E <= 256 && E % 8 == 0) {
+    const cudaError_t e = launch_router_tc(x, w_r, b_r, Tn, d, E, k, idx, gate, status, timeout_ns, s);
+    if (e != cudaErrorNotSupported) return e;
+  }
   const bool small_e = E <= 256;
   if (dt == MOE_DTYPE_BF16)
     return small_e ? launch_router_t<__nv_bfloat16, 8>(x, w_r, b_r, Tn, d, E, k, idx, gate, s)

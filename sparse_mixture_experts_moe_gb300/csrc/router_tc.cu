@@ -1,0 +1,233 @@
+// Router on the tensor cores: logits = x W_r (+ b_r), softmax over the E experts and
+// deterministic top-k, fused in one kernel.
+// csdn/6a919c0d §2.2 steps 1-4; aicoding/6a320eef §3.2; csdn/6a919c0d §4.2 (max subtraction).
+//
+// The router is a dense [T, d] x [d, E] contraction, so each CTA computes the logits of
+// 128 tokens with tcgen05.mma (M = 128 tokens, N = E rounded up to 64, K = d in 64-deep
+// blocks fed by TMA) into a TMEM accumulator. In TMEM, lane r holds token r's logits, so
+// each epilogue thread owns one token: it reads its row 32 columns at a time with
+// tcgen05.ld, keeps the k best (logit, expert) pairs in registers (a strictly greater
+// logit displaces, so equal logits keep the lower expert index first) and the maximum,
+// then sums exp(l - max) in ascending expert order and writes the k gates
+// exp(l_j - max) / sum. Fixed orders everywhere: results are reproducible.
+//
+// Warps: 0 = TMA producer, 1 = TMEM allocator + MMA issuer, 2..5 = one token per thread.
+// All waits are bounded (see wait_or_abort).
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int kTileXBytes = BM * BK * 2;     // 16 KB
+constexpr int kTileWSubBytes = BK * 64 * 2;  // 8 KB: 64 k-rows x 64 experts
+constexpr int kThreads = 192;
+constexpr int kNumBars = 2 * STAGES + 2;
+
+template <int EN>
+constexpr size_t router_smem_bytes() {
+  return 1024 + (size_t)STAGES * (kTileXBytes + EN / 64 * kTileWSubBytes) + 8 * kNumBars + 16;
+}
+
+// Insert (v, e) into the descending list bv/bi of length k (k <= KMAX). A value equal to an
+// entry already present goes after it: the scan is in ascending e, so lower indices stay first.
+template <int KMAX>
+__device__ __forceinline__ void topk_insert(float (&bv)[KMAX], int (&bi)[KMAX], int k, float v, int e) {
+#pragma unroll
+  for (int p = 0; p < KMAX; ++p) {
+    if (p < k && v > bv[p]) {
+      const float tv = bv[p];
+      const int ti = bi[p];
+      bv[p] = v; bi[p] = e;
+      v = tv; e = ti;
+    }
+  }
+}
+
+template <int EN, int KMAX>
+__global__ void __launch_bounds__(kThreads, 1)
+router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                 const float* __restrict__ b_r, int Tn, int d, int E, int k, int32_t* __restrict__ topk_idx,
+                 float* __restrict__ topk_gate, int* status, uint64_t timeout_ns) {
+  constexpr int kTileWBytes = EN / 64 * kTileWSubBytes;
+  constexpr int kStageBytes = kTileXBytes + kTileWBytes;
+  constexpr uint32_t kCols = EN;  // 64, 128 or 256: a power of two >= 32
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sX = base;
+  const uint32_t sW = base + STAGES * kTileXBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, DONE = 2 * STAGES + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * BM;
+  const int KB = (d + BK - 1) / BK;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(bar(FULL + s), 1); mbar_init(bar(EMPTY + s), 1); }
+    mbar_init(bar(TFULL), 1);
+    mbar_init(bar(DONE), 1);
+    fence_mbar_init();
+    *abort_flag = 0;
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, filled = 0, fill_phase = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!wait_or_abort(bar(EMPTY + stage), phase ^ 1u, timeout_ns, abort_flag, status, 11)) break;
+        mbar_arrive_expect_tx(bar(FULL + stage), kStageBytes);
+        tma_load_2d(sX + stage * kTileXBytes, &tmX, kb * BK, t0, bar(FULL + stage));
+#pragma unroll
+        for (int j = 0; j < EN / 64; ++j)
+          tma_load_2d(sW + stage * kTileWBytes + j * kTileWSubBytes, &tmW, 64 * j, kb * BK, bar(FULL + stage));
+        filled |= 1u << stage;
+        fill_phase = (fill_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      for (int s = 0; s < STAGES; ++s)
+        if (filled & (1u << s)) mbar_wait_bounded(bar(FULL + s), (fill_phase >> s) & 1u, timeout_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_bf16_f32(BM, EN, /*b_mn_major=*/true);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!wait_or_abort(bar(FULL + stage), phase, timeout_ns, abort_flag, status, 12)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t a_desc = make_smem_desc_sw128(sX + stage * kTileXBytes, 16, 1024);
+        const uint64_t b_desc = make_smem_desc_sw128(sW + stage * kTileWBytes, kTileWSubBytes, 1024);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          tc_mma_f16(tmem_base, a_desc + (uint64_t)((kk * 32) >> 4), b_desc + (uint64_t)((kk * 16 * 128) >> 4),
+                     idesc, (kb | kk) != 0 ? 1u : 0u);
+        tc_commit(bar(EMPTY + stage));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (ok) tc_commit(bar(TFULL));
+      tc_commit(bar(DONE));
+      mbar_wait_bounded(bar(DONE), 0, timeout_ns);
+    }
+  } else {
+    const int q = warp & 3;
+    const int tok = t0 + 32 * q + lane;
+    const bool ok = wait_or_abort(bar(TFULL), 0, timeout_ns, abort_flag, status, 13);
+    if (ok) {
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16);
+      float bv[KMAX];
+      int bi[KMAX];
+#pragma unroll
+      for (int p = 0; p < KMAX; ++p) { bv[p] = -INFINITY; bi[p] = 0x7fffffff; }
+      // pass 1: the k largest logits (the first of them is the maximum)
+#pragma unroll 1
+      for (int c = 0; c < EN; c += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + (uint32_t)c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int e = c + j;
+          if (e < E) topk_insert<KMAX>(bv, bi, k, __uint_as_float(v[j]) + (b_r != nullptr ? b_r[e] : 0.f), e);
+        }
+      }
+      const float m = bv[0];
+      // pass 2: sum of exp(l - max), ascending expert order
+      float ssum = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < EN; c += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + (uint32_t)c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int e = c + j;
+          if (e < E) ssum += expf(__uint_as_float(v[j]) + (b_r != nullptr ? b_r[e] : 0.f) - m);
+        }
+      }
+      if (tok < Tn) {
+#pragma unroll
+        for (int p = 0; p < KMAX; ++p) {
+          if (p < k) {
+            topk_idx[(size_t)tok * k + p] = bi[p];
+            topk_gate[(size_t)tok * k + p] = expf(bv[p] - m) / ssum;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kCols);
+  }
+}
+
+template <int EN, int KMAX>
+cudaError_t launch_en(const CUtensorMap& tmX, const CUtensorMap& tmW, const float* b_r, int Tn, int d, int E,
+                      int k, int32_t* idx, float* gate, int* status, uint64_t timeout_ns, cudaStream_t s) {
+  const size_t smem = router_smem_bytes<EN>();
+  auto kern = router_tc_kernel<EN, KMAX>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  kern<<<(Tn + BM - 1) / BM, kThreads, smem, s>>>(tmX, tmW, b_r, Tn, d, E, k, idx, gate, status, timeout_ns);
+  return cudaGetLastError();
+}
+
+template <int KMAX>
+cudaError_t launch_k(const CUtensorMap& tmX, const CUtensorMap& tmW, const float* b_r, int Tn, int d, int E, int k,
+                     int32_t* idx, float* gate, int* status, uint64_t timeout_ns, cudaStream_t s) {
+  if (E <= 64) return launch_en<64, KMAX>(tmX, tmW, b_r, Tn, d, E, k, idx, gate, status, timeout_ns, s);
+  if (E <= 128) return launch_en<128, KMAX>(tmX, tmW, b_r, Tn, d, E, k, idx, gate, status, timeout_ns, s);
+  return launch_en<256, KMAX>(tmX, tmW, b_r, Tn, d, E, k, idx, gate, status, timeout_ns, s);
+}
+
+}  // namespace
+
+cudaError_t launch_router_tc(const void* x, const void* w_r, const float* b_r, int Tn, int d, int E, int k,
+                             int32_t* idx, float* gate, int* status, uint64_t timeout_ns, cudaStream_t s) {
+  if (Tn == 0) return cudaSuccess;
+  if (E > 256 || E % 8 != 0) return cudaErrorNotSupported;
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  CUtensorMap tmX, tmW;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)Tn};
+    const cuuint64_t str[1] = {(cuuint64_t)d * 2};
+    const cuuint32_t box[2] = {BK, BM};
+    if (!encode_tmap(enc, &tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)E, (cuuint64_t)d};
+    const cuuint64_t str[1] = {(cuuint64_t)E * 2};
+    const cuuint32_t box[2] = {64, BK};
+    if (!encode_tmap(enc, &tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_r, 2, dims, str, box))
+      return cudaErrorInvalidValue;
+  }
+  if (k <= 2) return launch_k<2>(tmX, tmW, b_r, Tn, d, E, k, idx, gate, status, timeout_ns, s);
+  return launch_k<8>(tmX, tmW, b_r, Tn, d, E, k, idx, gate, status, timeout_ns, s);
+}
+
+}  // namespace moe
