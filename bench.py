@@ -87,13 +87,31 @@ def stored_traffic(kernel, workload, src_paths):
     return None
 
 
-def workload_config(w):
+def workload_config(w, timing="CUDA events on the launching stream, max over ranks"):
     wbytes = w.E * 2 * w.d * w.F * (2 if w.dtype == 1 else 4)
+    if wbytes > L2_BYTES:
+        l2 = f"inputs larger than L2: {wbytes / 1e6:.0f} MB of expert weights vs {L2_BYTES / 2**20:.0f} MB L2"
+    else:
+        l2 = f"inputs fit in L2 ({wbytes / 1e6:.1f} MB of expert weights), no flush: a latency case"
     return {"workload": f"{w.name}: T={w.T} d={w.d} d_ff={w.F} E={w.E} top-{w.k}"
                         + (" skewed router bias" if w.skew else ""),
-            "T": w.T, "d": w.d, "d_ff": w.F, "E": w.E, "k": w.k,
-            "l2": f"inputs larger than L2: {wbytes / 1e6:.0f} MB of expert weights vs {L2_BYTES / 2**20:.0f} MB L2",
-            "timing": "CUDA events on the launching stream, max over ranks"}
+            "T": w.T, "d": w.d, "d_ff": w.F, "E": w.E, "k": w.k, "l2": l2, "timing": timing}
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's); no-op for one rank."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes its own batch in the (max-over-ranks) step time."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
 
 
 # ----------------------------------------------------------------------------- inputs
@@ -292,13 +310,9 @@ def run_ours(args, w, rank, world, device):
     t_wall1 = time.time()
     if world > 1:
         dist.barrier()
-    ms_total = ev0.elapsed_time(ev1)
-    ms_t = torch.tensor([ms_total], dtype=torch.float64, device=device)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_total = float(ms_t.item())
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world, device)
     ms_per_step = ms_total / args.steps
-    value = world * T / (ms_per_step / 1e3)
+    value = job_tokens_per_s(T, world, ms_per_step)
 
     # --- per-kernel timing: the same step as its separate C ABI calls, events between them
     idx = torch.empty((T, k), dtype=torch.int32, device=device)
@@ -354,10 +368,7 @@ def run_ours(args, w, rank, world, device):
         out_host.copy_(out_dev, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = torch.tensor([e0.elapsed_time(e1) / args.steps], dtype=torch.float64, device=device)
-    if world > 1:
-        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
-    e2e_value = world * T / (float(e2e_ms.item()) / 1e3)
+    e2e_value = job_tokens_per_s(T, world, max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device))
     st, detail = moe.get_device_status(ws)
     if st != moe.MOE_OK:
         raise RuntimeError(f"device status after timing: {moe.status_string(st)} ({detail})")
@@ -443,7 +454,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded inputgen draws)",
-        "config": workload_config(w),
+        "config": workload_config(w, timing="host wall clock (time.perf_counter) around K oracle steps"),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"first {n} of the batch's {w.T} tokens per step, fp64 oracle forward"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

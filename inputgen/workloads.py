@@ -51,6 +51,9 @@ WORKLOADS = {
     "decode_t1": Workload("decode_t1", T=1, d=8192, F=8192, E=128, k=2, dtype=DTYPE_BF16),
     "decode_t8": Workload("decode_t8", T=8, d=8192, F=8192, E=128, k=2, dtype=DTYPE_BF16),
     "decode_t64": Workload("decode_t64", T=64, d=8192, F=8192, E=128, k=2, dtype=DTYPE_BF16),
+    # Profiling-size decode layer: the decode layer's per-expert shape with 16 experts (4.3 GB), small
+    # enough for a full ncu capture of the streaming kernel.
+    "decode_t1_e16": Workload("decode_t1_e16", T=1, d=8192, F=8192, E=16, k=2, dtype=DTYPE_BF16),
     # Skew-routed layer: T=16384, power-law router bias, else as the prefill layer.
     "skew_e128": Workload("skew_e128", T=16384, d=4096, F=8192, E=128, k=2, dtype=DTYPE_BF16,
                           skew=True),
