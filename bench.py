@@ -379,7 +379,7 @@ def run_ours(args, w, rank, world, device):
     peaks, peak_src = load_peaks()
     eb = 2 if dt == 1 else 4
     dom = max(["expert_up", "expert_down"], key=lambda n: kern_ms[n])
-    stream_path = dt == 1 and A <= 256
+    stream_path = dt == 1 and A <= 256  # the library's automatic choice (include/moe.h, moe_path)
     if stream_path:
         # weight streaming: bytes = touched experts' matrix + the routed rows in and out
         if dom == "expert_up":

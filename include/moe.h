@@ -56,13 +56,14 @@ typedef enum {
 
 typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
 
-/* Kernel family for the expert FFN (a3, a4). AUTO picks TENSOR for bf16 with more than
- * 256 routed rows, STREAM for bf16 with at most 256 routed rows, SIMT for fp32. */
+/* Kernel family for the expert FFN (a3, a4). AUTO picks, for bf16: STREAM with at most 256 routed
+ * rows, TENSOR otherwise; SIMT for fp32. TENSOR_PAIR is available on request (measured slower). */
 typedef enum {
   MOE_PATH_AUTO = 0,
-  MOE_PATH_TENSOR = 1, /* tcgen05/TMEM grouped GEMM fed by TMA (bf16 only) */
-  MOE_PATH_STREAM = 2, /* weight-streaming column-slab kernel for few rows per expert (bf16 only) */
-  MOE_PATH_SIMT = 3    /* CUDA-core tiled grouped GEMM (fp32 and bf16) */
+  MOE_PATH_TENSOR = 1,      /* tcgen05/TMEM grouped GEMM fed by TMA, 128x256 tiles per CTA (bf16 only) */
+  MOE_PATH_STREAM = 2,      /* weight-streaming column-slab kernel for few rows per expert (bf16 only) */
+  MOE_PATH_SIMT = 3,        /* CUDA-core tiled grouped GEMM (fp32 and bf16) */
+  MOE_PATH_TENSOR_PAIR = 4  /* tcgen05 cta_group::2 on CTA pairs, 256x256 tiles (bf16 only) */
 } moe_path;
 
 /* ---------------------------------------------------------------------------------------------

@@ -15,7 +15,7 @@ from typing import Optional
 from . import _lib
 from ._lib import (  # noqa: F401
     MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK, MOE_ERR_DEVICE_TIMEOUT,
-    MOE_DTYPE_F32, MOE_DTYPE_BF16, PATH_AUTO, PATH_TENSOR, PATH_STREAM, PATH_SIMT, MoeError,
+    MOE_DTYPE_F32, MOE_DTYPE_BF16, PATH_AUTO, PATH_TENSOR, PATH_STREAM, PATH_SIMT, PATH_TENSOR_PAIR, MoeError,
     router_topk, dispatch, dispatch_noalloc, expert_up, expert_down, grouped_ffn, combine, forward, workspace_bytes, workspace_init,
     get_device_status, status_string, selftest_wait_timeout, lib,
 )

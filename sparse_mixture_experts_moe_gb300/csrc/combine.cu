@@ -31,6 +31,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ y_perm, const int32_t* __restrict__ row_of, int Tn, int d, int k, int A,
                T* __restrict__ out) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -39,6 +41,7 @@ combine_kernel(const float* __restrict__ y_perm, const int32_t* __restrict__ row
     int rows[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) rows[j] = j < k ? row_of[(size_t)t * k + j] : -1;
+#pragma unroll 2
     for (int g = lane; g < groups; g += 32) {
       float acc[8];
 #pragma unroll
@@ -68,11 +71,10 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* row_of, int Tn, in
   if (blocks > cap) blocks = cap;
   const int A = Tn * k;
   if (dt == MOE_DTYPE_BF16)
-    combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>((const float*)y_perm, row_of, Tn, d, k, A,
-                                                         (__nv_bfloat16*)out);
-  else
-    combine_kernel<float><<<blocks, 256, 0, s>>>((const float*)y_perm, row_of, Tn, d, k, A, (float*)out);
-  return cudaGetLastError();
+    return launch_pdl(combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, s, (const float*)y_perm, row_of, Tn,
+                      d, k, A, (__nv_bfloat16*)out);
+  return launch_pdl(combine_kernel<float>, dim3(blocks), dim3(256), 0, s, (const float*)y_perm, row_of, Tn, d, k, A,
+                    (float*)out);
 }
 
 }  // namespace moe

@@ -1,6 +1,10 @@
 // Dispatch: per-expert histogram, exclusive scan, stable permutation and row gather.
 // csdn/6a462027 §4.2 steps 4-5 (group each expert's tokens: "in practice a scatter").
 //
+// moe_dispatch runs count+scan (one kernel, the last CTA scans), scatter and gather as three
+// launches with programmatic dependent launch; moe_dispatch_noalloc runs the four separate
+// kernels below (count, scan, scatter, gather).
+//
 // The T*k assignments, in row-major (t, j) order, are cut into chunks of 256
 // (one CTA each).
 //   count:   shared-memory histogram of a chunk -> blk_counts[chunk][e]
@@ -79,6 +83,8 @@ __global__ void __launch_bounds__(kChunk)
 dispatch_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int A, int k, int E,
                         const int32_t* __restrict__ blk_base, int32_t* __restrict__ row_of,
                         int32_t* __restrict__ perm_token, float* __restrict__ row_gate) {
+  griddep_launch_dependents();
+  griddep_wait();
   extern __shared__ int wcnt[];  // [kWarpsPerChunk][E]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < kWarpsPerChunk * E; i += kChunk) wcnt[i] = 0;
@@ -110,6 +116,8 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict
 __global__ void __launch_bounds__(256)
 dispatch_gather_kernel(const int4* __restrict__ x, const int32_t* __restrict__ perm_token,
                        const int32_t* __restrict__ offsets, int E, int vec_per_row, int4* __restrict__ x_perm) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int rows = offsets[E];
   const int lane = threadIdx.x & 31;
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -124,6 +132,110 @@ dispatch_gather_kernel(const int4* __restrict__ x, const int32_t* __restrict__ p
     }
     for (; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
   }
+}
+
+// Histogram of one chunk, and for the CTA that finishes last (an atomic ticket, nobody waits)
+// the scan: counts[e], offsets (exclusive scan over experts) and blk_base[c][e] = offsets[e] +
+// counts of chunks before c. The 256 threads are (expert, chunk group) pairs so the chunk tables
+// are summed in parallel; every sum runs in a fixed order, so results do not depend on timing.
+// `done` is zero before the call and is reset to zero by the last CTA.
+__global__ void __launch_bounds__(kChunk)
+dispatch_count_scan_kernel(const int32_t* __restrict__ idx, int A, int E, int nb, int32_t* __restrict__ blk_counts,
+                           int32_t* __restrict__ blk_base, int32_t* __restrict__ counts,
+                           int32_t* __restrict__ offsets, int* status, int* done) {
+  griddep_launch_dependents();
+  griddep_wait();
+  extern __shared__ int sm[];
+  int* hist = sm;            // [E]
+  int* tot = hist + E;       // [E]
+  int* offs = tot + E;       // [E + 1]
+  int* sgrp = offs + E + 1;  // [kChunk]: per (group, expert) sums, then their exclusive prefixes
+  __shared__ int s_last;
+  __shared__ int warp_tot[kChunk / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += kChunk) hist[e] = 0;
+  __syncthreads();
+  const int a = blockIdx.x * kChunk + tid;
+  if (a < A) {
+    const int e = idx[a];
+    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    else record_error(status, MOE_ERR_DEVICE_CHECK, a);
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kChunk) blk_counts[(size_t)blockIdx.x * E + e] = hist[e];
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(done, 1) == nb - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // pass 1: totals per expert; for E <= 256, G groups of consecutive chunks per expert
+  const int width = E < kChunk ? E : kChunk;
+  const int G = E < kChunk ? kChunk / E : 1;
+  const int L = (nb + G - 1) / G;
+  const int g = tid / width;
+  for (int e0 = 0; e0 < E; e0 += width) {
+    const int e = e0 + tid % width;
+    const bool valid = g < G && e < E;
+    int sum = 0;
+    if (valid)
+      for (int c = g * L; c < nb && c < (g + 1) * L; ++c) sum += __ldcg(blk_counts + (size_t)c * E + e);
+    if (g < G) sgrp[g * width + tid % width] = sum;
+    __syncthreads();
+    if (tid < width && e0 + tid < E) {
+      int run = 0;
+      for (int gg = 0; gg < G; ++gg) {
+        const int v = sgrp[gg * width + tid];
+        sgrp[gg * width + tid] = run;
+        run += v;
+      }
+      tot[e0 + tid] = run;
+    }
+    __syncthreads();
+  }
+  // exclusive scan of the totals over experts (thread t owns experts 4t .. 4t+3)
+  int loc[4], local = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = 4 * tid + j;
+    loc[j] = e < E ? tot[e] : 0;
+    local += loc[j];
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int run = incl - local;
+  for (int w = 0; w < warp; ++w) run += warp_tot[w];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int e = 4 * tid + j;
+    if (e < E) {
+      offs[e] = run;
+      counts[e] = loc[j];
+      offsets[e] = run;
+    }
+    run += loc[j];
+  }
+  if (tid == kChunk - 1) offsets[E] = run;
+  __syncthreads();
+  // pass 2: per-chunk bases (E <= 256: the group prefixes are still in sgrp; E > 256: one group)
+  for (int e0 = 0; e0 < E; e0 += width) {
+    const int e = e0 + tid % width;
+    if (g < G && e < E) {
+      int r = offs[e] + (E < kChunk ? sgrp[g * width + tid % width] : 0);
+      for (int c = g * L; c < nb && c < (g + 1) * L; ++c) {
+        blk_base[(size_t)c * E + e] = r;
+        r += __ldcg(blk_counts + (size_t)c * E + e);
+      }
+    }
+  }
+  if (tid == 0) *done = 0;
 }
 
 }  // namespace
@@ -155,6 +267,40 @@ cudaError_t launch_dispatch(const void* x, const int32_t* idx, const float* gate
   dispatch_gather_kernel<<<blocks, 256, 0, s>>>((const int4*)x, perm_token, offsets, E, vec_per_row,
                                                 (int4*)x_perm);
   return cudaGetLastError();
+}
+
+}  // namespace moe
+
+
+namespace moe {
+
+// Three launches with programmatic dependent launch: count + scan, scatter, gather.
+cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
+                                 int dt, int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* row_of,
+                                 float* row_gate, void* x_perm, int32_t* blk_counts, int32_t* blk_base, int* status,
+                                 int* done, cudaStream_t s) {
+  const int A = T * k;
+  if (A == 0)
+    return launch_dispatch(x, idx, gate, T, d, E, k, dt, counts, offsets, perm_token, row_of, row_gate, x_perm,
+                           blk_counts, blk_base, status, s);
+  const int nb = (A + kChunk - 1) / kChunk;
+  const size_t cs_smem = (size_t)(3 * E + 1 + kChunk) * sizeof(int);
+  cudaError_t err = launch_pdl(dispatch_count_scan_kernel, dim3(nb), dim3(kChunk), cs_smem, s, idx, A, E, nb,
+                               blk_counts, blk_base, counts, offsets, status, done);
+  if (err != cudaSuccess) return err;
+  const size_t sc_smem = (size_t)kWarpsPerChunk * E * sizeof(int);
+  err = cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc_smem);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(dispatch_scatter_kernel, dim3(nb), dim3(kChunk), sc_smem, s, idx, gate, A, k, E,
+                   (const int32_t*)blk_base, row_of, perm_token, row_gate);
+  if (err != cudaSuccess) return err;
+  const size_t elem = dt == MOE_DTYPE_BF16 ? 2 : 4;
+  const int vec_per_row = (int)((size_t)d * elem / 16);
+  int blocks = (A + 7) / 8;
+  const int cap = device_sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  return launch_pdl(dispatch_gather_kernel, dim3(blocks), dim3(256), 0, s, (const int4*)x, (const int32_t*)perm_token,
+                    (const int32_t*)offsets, E, vec_per_row, (int4*)x_perm);
 }
 
 }  // namespace moe

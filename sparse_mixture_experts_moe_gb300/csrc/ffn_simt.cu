@@ -21,6 +21,8 @@ ffn_simt_kernel(const T* __restrict__ a, const T* __restrict__ w, const int32_t*
   __shared__ float sB[BK][BN + 4];
   __shared__ int s_e, s_m0, s_mend;
   const int tid = threadIdx.x;
+  griddep_launch_dependents();
+  griddep_wait();
   if (tid == 0) {
     // Locate work item blockIdx.y in the list of (expert, 64-row tile) pairs.
     int item = blockIdx.y, e_found = -1, m0 = 0, mend = 0;
@@ -86,12 +88,11 @@ cudaError_t launch_t(const FfnArgs& p, cudaStream_t s) {
   dim3 grid((p.N + BN - 1) / BN, max_items);
   if (max_items > 65535) return cudaErrorInvalidConfiguration;
   if (p.stage == 1)
-    ffn_simt_kernel<T, 1, T><<<grid, 256, 0, s>>>((const T*)p.a, (const T*)p.w, p.offsets, p.row_gate, p.K, p.N,
-                                                  p.E, (T*)p.out);
+    return launch_pdl(ffn_simt_kernel<T, 1, T>, grid, dim3(256), 0, s, (const T*)p.a, (const T*)p.w, p.offsets,
+                      p.row_gate, p.K, p.N, p.E, (T*)p.out);
   else
-    ffn_simt_kernel<T, 2, float><<<grid, 256, 0, s>>>((const T*)p.a, (const T*)p.w, p.offsets, p.row_gate, p.K,
-                                                      p.N, p.E, (float*)p.out);
-  return cudaGetLastError();
+    return launch_pdl(ffn_simt_kernel<T, 2, float>, grid, dim3(256), 0, s, (const T*)p.a, (const T*)p.w, p.offsets,
+                      p.row_gate, p.K, p.N, p.E, (float*)p.out);
 }
 
 }  // namespace

@@ -6,8 +6,8 @@
 // A CTA owns the slab for the full depth K, so the GeLU (up) or gate (down)
 // epilogue applies locally and no partial sums leave the CTA. Each k-row of the
 // slab is 128 contiguous bytes read by 8 lanes with 16-byte loads; 8 loads per
-// thread are in flight. The expert's rows (at most 8 per pass; more rows take
-// more passes) are staged in shared memory as fp32 in 1024-deep chunks.
+// thread are in flight. The expert's rows (at most 2 or 8 per pass, by batch size;
+// more rows take more passes) are staged in shared memory as fp32 in 1024-deep chunks.
 // Partial sums are combined in a fixed order (xor-butterfly in the warp, then
 // warps in index order), so results are reproducible.
 // Units are ordered slab-fastest, so CTAs running together stream neighbouring
@@ -23,7 +23,6 @@ constexpr int NS = 64;            // columns per slab
 constexpr int LPR = NS / 8;       // lanes per k-row: 8 (16 bytes each)
 constexpr int RPW = 32 / LPR;     // k-rows per warp per step: 4
 constexpr int KSTEP = kWarps * RPW;  // k-rows per CTA step: 32
-constexpr int RMAX = 8;           // rows per pass
 constexpr int KC = 1024;          // k-depth staged per chunk
 constexpr int kUnroll = 8;
 
@@ -33,7 +32,8 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
 }
 
 // up (STAGE 1) writes bf16 h; down (STAGE 2) writes fp32 y_perm.
-template <int STAGE, typename OutT>
+// RMAX rows of an expert per pass over its weights (more rows take more passes).
+template <int STAGE, typename OutT, int RMAX>
 __global__ void __launch_bounds__(kThreads)
 ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ w,
                   const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
@@ -44,6 +44,8 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __re
   int* sAct = reinterpret_cast<int*>(sRed + kWarps * RMAX * NS);  // [E] experts with rows
   __shared__ int s_nact;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == 0) {
     int base = 0;
@@ -135,26 +137,25 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __re
 #pragma unroll
         for (int wi = 0; wi < kWarps; ++wi) v += sRed[(wi * RMAX + r) * NS + c];
         const int grow = rp + r;
-        v = STAGE == 1 ? gelu_erf(v) : row_gate[grow] * v;
+        v = STAGE == 1 ? gelu_as(v) : row_gate[grow] * v;
         out[(size_t)grow * N + gn] = from_f32<OutT>(v);
       }
     }
   }
 }
 
-template <int STAGE, typename OutT>
+template <int STAGE, typename OutT, int RMAX>
 cudaError_t launch_t(const FfnArgs& p, cudaStream_t s) {
   const size_t smem = (size_t)(RMAX * KC + kWarps * RMAX * NS) * sizeof(float) + (size_t)p.E * sizeof(int);
-  auto kern = ffn_stream_kernel<STAGE, OutT>;
+  auto kern = ffn_stream_kernel<STAGE, OutT, RMAX>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int nslab = (p.N + NS - 1) / NS;
   const long long max_units = (long long)(p.rows < p.E ? p.rows : p.E) * nslab;
-  long long grid = (long long)device_sm_count() * 4;
+  long long grid = (long long)device_sm_count() * (RMAX <= 2 ? 8 : 4);
   if (grid > max_units) grid = max_units;
-  kern<<<(int)grid, kThreads, smem, s>>>((const __nv_bfloat16*)p.a, (const __nv_bfloat16*)p.w, p.offsets,
-                                         p.row_gate, p.K, p.N, p.E, (OutT*)p.out);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, (const __nv_bfloat16*)p.a,
+                    (const __nv_bfloat16*)p.w, p.offsets, p.row_gate, p.K, p.N, p.E, (OutT*)p.out);
 }
 
 }  // namespace
@@ -162,7 +163,10 @@ cudaError_t launch_t(const FfnArgs& p, cudaStream_t s) {
 cudaError_t launch_ffn_stream(const FfnArgs& p, cudaStream_t s) {
   if (p.rows == 0) return cudaSuccess;
   if (p.dt != MOE_DTYPE_BF16) return cudaErrorNotSupported;
-  return p.stage == 1 ? launch_t<1, __nv_bfloat16>(p, s) : launch_t<2, float>(p, s);
+  // Rows per expert are at most T*k; small batches keep fewer accumulators (more CTAs per SM).
+  if (p.rows <= 4)
+    return p.stage == 1 ? launch_t<1, __nv_bfloat16, 2>(p, s) : launch_t<2, float, 2>(p, s);
+  return p.stage == 1 ? launch_t<1, __nv_bfloat16, 8>(p, s) : launch_t<2, float, 8>(p, s);
 }
 
 }  // namespace moe

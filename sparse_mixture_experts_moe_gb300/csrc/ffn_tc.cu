@@ -4,7 +4,7 @@
 // (csdn/6a919c0d §2.2 step 4).
 //
 // out[r, n] = epi( sum_k a[r, k] * w[e][k, n] ) for every row r of expert e's range.
-//   up   (stage 1): a = x_perm [rows, d], w = W1 [E, d, F], epi = GeLU (erf form)
+//   up   (stage 1): a = x_perm [rows, d], w = W1 [E, d, F], epi = GeLU (erf form, gelu_as)
 //   down (stage 2): a = h [rows, F],      w = W2 [E, F, d], epi = row_gate[r] * ., fp32 output
 //
 // Tiles: 128 rows x 256 columns x 64-deep k-blocks, one tcgen05.mma of M=128, N=256, K=16
@@ -13,10 +13,11 @@
 // lives in TMEM; two accumulators (512 columns) let the epilogue of one tile overlap the
 // main loop of the next.
 //
-// Persistent CTAs, one per SM, 6 warps:
-//   warp 0      TMA producer (one lane): A tile + 4 B sub-tiles per stage, 4 stages
+// Persistent CTAs, one per SM, 10 warps:
+//   warp 0      TMA producer (one lane): A tile + 4 B sub-tiles per stage, 4 stages (3 when E is
+//               large)
 //   warp 1      TMEM allocator and MMA issuer (one lane)
-//   warps 2..5  epilogue: tcgen05.ld -> GeLU -> bf16 (up) or gate -> fp32 (down) -> swizzled
+//   warps 2..9  epilogue (two per TMEM lane quarter, half the columns each): tcgen05.ld -> GeLU -> bf16 (up) or gate -> fp32 (down) -> swizzled
 //               staging -> TMA store
 // Work items are (expert, 256-column block, 128-row tile), the row tile fastest, so the
 // CTAs that run at the same time share the same weight tile (read once from HBM, then from
@@ -34,20 +35,22 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int kTileABytes = BM * BK * 2;           // 16 KB
 constexpr int kTileBSubBytes = BK * 64 * 2;        // 8 KB: 64 k-rows x 64 columns
 constexpr int kTileBBytes = BK * BN * 2;           // 32 KB
 constexpr int kStageBytes = kTileABytes + kTileBBytes;
-constexpr int kEpiWarps = 4;
-constexpr int kStagingBytes = 32 * 128;            // per epilogue warp: 32 rows x 64 bf16
+// Two epilogue warps per TMEM lane quarter, each taking half of the tile's 256 columns.
+constexpr int kEpiWarps = 8;
+constexpr int kStagingBytes = 32 * 128;            // per epilogue warp: 32 rows x 128 bytes
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 2 * BN;
-constexpr int kNumBars = 2 * STAGES + 5;
+constexpr int kMaxSmem = 232448;                   // opt-in shared memory per CTA on sm_103a
 
-__host__ __device__ constexpr size_t smem_bytes_for(int E) {
-  return 1024 /* alignment slack */ + (size_t)STAGES * kStageBytes + (size_t)kEpiWarps * kStagingBytes +
-         8 * kNumBars + 16 + 4 * (size_t)(E + 1);
+__host__ __device__ constexpr int num_bars(int nst) { return 2 * nst + 5; }
+__host__ __device__ constexpr size_t smem_bytes_for(int E, int nst) {
+  return 1024 /* alignment slack */ + (size_t)nst * kStageBytes + (size_t)kEpiWarps * kStagingBytes +
+         8 * num_bars(nst) + 16 + 4 * (size_t)(E + 1);
 }
 
 struct Item {
@@ -77,7 +80,7 @@ struct EpiOut { using T = __nv_bfloat16; };
 template <>
 struct EpiOut<2> { using T = float; };
 
-template <int STAGE>
+template <int STAGE, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
 ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmC, typename EpiOut<STAGE>::T* __restrict__ out,
@@ -93,7 +96,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   const uint32_t sB = base + STAGES * kTileABytes;
   const uint32_t sStg = sB + STAGES * kTileBBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * kStageBytes + kEpiWarps * kStagingBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + num_bars(STAGES));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* P = reinterpret_cast<int*>(tmem_slot + 4);  // [E+1] exclusive scan of 128-row tiles per expert
   auto bar = [&](int i) { return smem_u32(bars + i); };
@@ -115,6 +118,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  griddep_launch_dependents();
+  griddep_wait();  // offsets, rows and weights may come from earlier kernels in the stream
   if (warp == 2) {
     int run = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
@@ -200,8 +205,9 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       mbar_wait_bounded(bar(DONE), 0, timeout_ns);
     }
   } else {
-    // -------------------------------------------------------------- epilogue (warps 2..5)
-    const int q = warp & 3;  // TMEM lanes 32q .. 32q+31 belong to this warp
+    // -------------------------------------------------------------- epilogue (warps 2..9)
+    const int q = warp & 3;                   // TMEM lanes 32q .. 32q+31 belong to this warp
+    const int c_begin = ((warp - 2) >> 2) * (BN / 2);  // and this half of the tile's columns
     const uint32_t stg = sStg + (uint32_t)((warp - 2) * kStagingBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -215,7 +221,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       float g = 1.f;
       if (STAGE == 2 && row_ok) g = row_gate[grow];
       // One staging row is 128 bytes: 64 bf16 columns (up) or 32 fp32 columns (down).
-      for (int c = 0; c < BN; c += CW) {
+      for (int c = c_begin; c < c_begin + BN / 2; c += CW) {
         if (it.n0 + c >= N) break;
         const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN + c);
         uint32_t packed[32];
@@ -226,9 +232,9 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            packed[i] = pack_bf16x2(gelu_erf(__uint_as_float(v0[2 * i])), gelu_erf(__uint_as_float(v0[2 * i + 1])));
+            packed[i] = pack_bf16x2(gelu_as(__uint_as_float(v0[2 * i])), gelu_as(__uint_as_float(v0[2 * i + 1])));
             packed[16 + i] =
-                pack_bf16x2(gelu_erf(__uint_as_float(v1[2 * i])), gelu_erf(__uint_as_float(v1[2 * i + 1])));
+                pack_bf16x2(gelu_as(__uint_as_float(v1[2 * i])), gelu_as(__uint_as_float(v1[2 * i + 1])));
           }
         } else {
           uint32_t v0[32];
@@ -349,24 +355,27 @@ cudaError_t launch_ffn_tensor(const FfnArgs& p, cudaStream_t s) {
                 dims, str, box))
       return cudaErrorInvalidValue;
   }
-  const size_t smem = smem_bytes_for(p.E);
+  const bool four = smem_bytes_for(p.E, 4) <= (size_t)kMaxSmem;
+  const size_t smem = smem_bytes_for(p.E, four ? 4 : 3);
   const int NB = (p.N + BN - 1) / BN;
   const long long max_items = ((long long)(p.rows + BM - 1) / BM + p.E) * NB;
   int grid = device_sm_count();
   if ((long long)grid > max_items) grid = (int)max_items;
   cudaError_t err;
   if (p.stage == 1) {
-    err = cudaFuncSetAttribute(ffn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = four ? ffn_tc_kernel<1, 4> : ffn_tc_kernel<1, 3>;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    ffn_tc_kernel<1><<<grid, kThreads, smem, s>>>(tmA, tmB, tmC, (__nv_bfloat16*)p.out, p.offsets, p.row_gate,
-                                                  p.K, p.N, p.E, p.status, p.timeout_ns);
+    err = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, tmA, tmB, tmC, (__nv_bfloat16*)p.out, p.offsets,
+                     p.row_gate, p.K, p.N, p.E, p.status, p.timeout_ns);
   } else {
-    err = cudaFuncSetAttribute(ffn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = four ? ffn_tc_kernel<2, 4> : ffn_tc_kernel<2, 3>;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    ffn_tc_kernel<2><<<grid, kThreads, smem, s>>>(tmA, tmB, tmC, (float*)p.out, p.offsets, p.row_gate,
-                                                  p.K, p.N, p.E, p.status, p.timeout_ns);
+    err = launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, tmA, tmB, tmC, (float*)p.out, p.offsets, p.row_gate,
+                     p.K, p.N, p.E, p.status, p.timeout_ns);
   }
-  return cudaGetLastError();
+  return err;
 }
 
 cudaError_t launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s) {

@@ -6,6 +6,23 @@
 
 namespace moe {
 
+// Launch with programmatic stream serialisation (see griddep_wait in common.cuh).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Dispatch processes the T*k assignments in chunks of this many (one CTA each).
 constexpr int kDispatchChunk = 256;
 
@@ -19,6 +36,13 @@ cudaError_t launch_dispatch(const void* x, const int32_t* idx, const float* gate
                             int dt, int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* row_of,
                             float* row_gate, void* x_perm, int32_t* blk_counts, int32_t* blk_base, int* status,
                             cudaStream_t s);
+
+// Same results as launch_dispatch in three launches (count + scan, scatter, gather). `done` is an int
+// that is zero before the call and zero again after it (the workspace header).
+cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
+                                 int dt, int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* row_of,
+                                 float* row_gate, void* x_perm, int32_t* blk_counts, int32_t* blk_base, int* status,
+                                 int* done, cudaStream_t s);
 
 cudaError_t launch_combine(const void* y_perm, const int32_t* row_of, int T, int d, int k, int dt, void* out,
                            cudaStream_t s);
@@ -39,6 +63,8 @@ cudaError_t launch_ffn_simt(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_ffn_stream(const FfnArgs& a, cudaStream_t s);
 // Returns cudaErrorNotSupported when no tensor-map encoder is available.
 cudaError_t launch_ffn_tensor(const FfnArgs& a, cudaStream_t s);
+// CTA-pair version (cta_group::2, 256-row tiles) for experts with many rows.
+cudaError_t launch_ffn_tensor_pair(const FfnArgs& a, cudaStream_t s);
 
 cudaError_t launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s);
 

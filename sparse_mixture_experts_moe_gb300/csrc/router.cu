@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 router_topk_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const float* __restrict__ b_r, int Tn,
                    int d, int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate) {
   constexpr int TB = kWarps * TPW;
+  griddep_launch_dependents();
+  griddep_wait();
   extern __shared__ __align__(16) float smem[];
   float* sW = smem;                    // [kDK][kEC]
   float* sX = sW + kDK * kEC;          // [TB][kDK]
@@ -131,8 +133,8 @@ cudaError_t launch_router_t(const void* x, const void* w_r, const float* b_r, in
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int grid = (Tn + TB - 1) / TB;
-  kern<<<grid, kWarps * 32, smem, s>>>((const T*)x, (const T*)w_r, b_r, Tn, d, E, k, idx, gate);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kWarps * 32), smem, s, (const T*)x, (const T*)w_r, b_r, Tn, d, E, k, idx,
+                    gate);
 }
 
 }  // namespace

@@ -83,10 +83,12 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     tmem_alloc(smem_u32(tmem_slot), kCols);
     tmem_relinquish();
   }
+  griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();  // x may come from the previous kernel in the stream
 
   if (warp == 0) {
     if (lane == 0) {
@@ -192,8 +194,8 @@ cudaError_t launch_en(const CUtensorMap& tmX, const CUtensorMap& tmW, const floa
   auto kern = router_tc_kernel<EN, KMAX>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  kern<<<(Tn + BM - 1) / BM, kThreads, smem, s>>>(tmX, tmW, b_r, Tn, d, E, k, idx, gate, status, timeout_ns);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((Tn + BM - 1) / BM), dim3(kThreads), smem, s, tmX, tmW, b_r, Tn, d, E, k, idx, gate,
+                    status, timeout_ns);
 }
 
 template <int KMAX>
