@@ -5,9 +5,10 @@
 // Work unit = (expert with at least one row, 64-column slab of its weight matrix).
 // A CTA owns the slab for the full depth K, so the GeLU (up) or gate (down)
 // epilogue applies locally and no partial sums leave the CTA. Each k-row of the
-// slab is 128 contiguous bytes read by 8 lanes with 16-byte loads; 8 loads per
-// thread are in flight. The expert's rows (at most 2 or 8 per pass, by batch size;
-// more rows take more passes) are staged in shared memory as fp32 in 1024-deep chunks.
+// slab is 128 contiguous bytes read by 8 lanes with 16-byte loads; two batches of 8
+// loads per thread are in flight (software pipelining), two CTAs per SM. The expert's
+// rows (2 or 4 per pass, by batch size; more rows take more passes) are staged in
+// shared memory as fp32 in 1024-deep chunks.
 // Partial sums are combined in a fixed order (xor-butterfly in the warp, then
 // warps in index order), so results are reproducible.
 // Units are ordered slab-fastest, so CTAs running together stream neighbouring
@@ -34,7 +35,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
 // up (STAGE 1) writes bf16 h; down (STAGE 2) writes fp32 y_perm.
 // RMAX rows of an expert per pass over its weights (more rows take more passes).
 template <int STAGE, typename OutT, int RMAX>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ w,
                   const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
                   OutT* __restrict__ out) {
@@ -87,8 +88,9 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __re
           sA[i] = kk < kn ? __bfloat162float(a[(size_t)(rp + r) * K + kc + kk]) : 0.f;
         }
         __syncthreads();
-        for (int k0 = 0; k0 < kn; k0 += KSTEP * kUnroll) {
-          uint4 wv[kUnroll];
+        // Software-pipelined: the next batch of kUnroll weight loads is issued before the
+        // current batch is consumed, so two batches per thread are in flight.
+        auto load_batch = [&](int k0, uint4 (&wv)[kUnroll]) {
 #pragma unroll
           for (int i = 0; i < kUnroll; ++i) {
             const int kk = k0 + i * KSTEP + warp * RPW + kr;
@@ -97,12 +99,17 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __re
             else
               wv[i] = make_uint4(0u, 0u, 0u, 0u);
           }
+        };
+        uint4 cur[kUnroll], nxt[kUnroll];
+        load_batch(0, cur);
+        for (int k0 = 0; k0 < kn; k0 += KSTEP * kUnroll) {
+          if (k0 + KSTEP * kUnroll < kn) load_batch(k0 + KSTEP * kUnroll, nxt);
 #pragma unroll
           for (int i = 0; i < kUnroll; ++i) {
             const int kk = k0 + i * KSTEP + warp * RPW + kr;
             if (kk >= kn) break;
             float wf[8];
-            bf16x8_to_f32(wv[i], wf);
+            bf16x8_to_f32(cur[i], wf);
 #pragma unroll
             for (int r = 0; r < RMAX; ++r) {
               if (r >= R) break;
@@ -111,6 +118,8 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __re
               for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av, wf[c], acc[r][c]);
             }
           }
+#pragma unroll
+          for (int i = 0; i < kUnroll; ++i) cur[i] = nxt[i];
         }
       }
       // Combine the RPW k-row groups of the warp (lanes cg, cg+8, cg+16, cg+24), then the warps.
@@ -164,9 +173,10 @@ cudaError_t launch_ffn_stream(const FfnArgs& p, cudaStream_t s) {
   if (p.rows == 0) return cudaSuccess;
   if (p.dt != MOE_DTYPE_BF16) return cudaErrorNotSupported;
   // Rows per expert are at most T*k; small batches keep fewer accumulators (more CTAs per SM).
-  if (p.rows <= 4)
+  // An expert with more rows than a pass holds streams its weights again for the rest.
+  if (p.rows <= 32)
     return p.stage == 1 ? launch_t<1, __nv_bfloat16, 2>(p, s) : launch_t<2, float, 2>(p, s);
-  return p.stage == 1 ? launch_t<1, __nv_bfloat16, 8>(p, s) : launch_t<2, float, 8>(p, s);
+  return p.stage == 1 ? launch_t<1, __nv_bfloat16, 4>(p, s) : launch_t<2, float, 4>(p, s);
 }
 
 }  // namespace moe

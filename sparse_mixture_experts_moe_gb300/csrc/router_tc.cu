@@ -12,6 +12,7 @@
 // exp(l_j - max) / sum. Fixed orders everywhere: results are reproducible.
 //
 // Warps: 0 = TMA producer, 1 = TMEM allocator + MMA issuer, 2..5 = one token per thread.
+// For at most 128 tokens and deep d, a cluster of eight CTAs splits d (router_tc_split_kernel).
 // All waits are bounded (see wait_or_abort).
 #include <cuda.h>
 
@@ -187,9 +188,202 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   }
 }
 
+// Split-K version for at most 128 tokens: a cluster of kSplit CTAs, CTA r accumulating the
+// k-blocks [r*KB/kSplit, (r+1)*KB/kSplit) in its own TMEM. Each epilogue thread copies its
+// token's partial logits to shared memory; after a cluster barrier, CTA r finishes tokens
+// [r*16, r*16+16): one warp per token sums the kSplit partials in rank order (DSMEM loads),
+// then softmax and top-k with warp shuffles (lane l owns experts l, l+32, ...).
+constexpr int kSplit = 8;
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+template <int EN>
+constexpr size_t router_split_smem_bytes() {
+  return router_smem_bytes<EN>() + (size_t)BM * (EN + 1) * sizeof(float);
+}
+
+template <int EN, int KMAX>
+__global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1)
+router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                       const float* __restrict__ b_r, int Tn, int d, int E, int k, int32_t* __restrict__ topk_idx,
+                       float* __restrict__ topk_gate, int* status, uint64_t timeout_ns) {
+  constexpr int kTileWBytes = EN / 64 * kTileWSubBytes;
+  constexpr int kStageBytes = kTileXBytes + kTileWBytes;
+  constexpr uint32_t kCols = EN;
+  constexpr int RS = EN + 1;  // padded row stride of the partial-logit table
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sX = base;
+  const uint32_t sW = base + STAGES * kTileXBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(gbase + STAGES * kStageBytes + 8 * kNumBars + 16);  // [BM][RS]
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, DONE = 2 * STAGES + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int KB = (d + BK - 1) / BK;
+  const int kb0 = (int)rank * KB / kSplit, kb1 = ((int)rank + 1) * KB / kSplit;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(bar(FULL + s), 1); mbar_init(bar(EMPTY + s), 1); }
+    mbar_init(bar(TFULL), 1);
+    mbar_init(bar(DONE), 1);
+    fence_mbar_init();
+    *abort_flag = 0;
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kCols);
+    tmem_relinquish();
+  }
+  griddep_launch_dependents();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, filled = 0, fill_phase = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wait_or_abort(bar(EMPTY + stage), phase ^ 1u, timeout_ns, abort_flag, status, 14)) break;
+        mbar_arrive_expect_tx(bar(FULL + stage), kStageBytes);
+        tma_load_2d(sX + stage * kTileXBytes, &tmX, kb * BK, 0, bar(FULL + stage));
+#pragma unroll
+        for (int j = 0; j < EN / 64; ++j)
+          tma_load_2d(sW + stage * kTileWBytes + j * kTileWSubBytes, &tmW, 64 * j, kb * BK, bar(FULL + stage));
+        filled |= 1u << stage;
+        fill_phase = (fill_phase & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      for (int s = 0; s < STAGES; ++s)
+        if (filled & (1u << s)) mbar_wait_bounded(bar(FULL + s), (fill_phase >> s) & 1u, timeout_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_bf16_f32(BM, EN, /*b_mn_major=*/true);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wait_or_abort(bar(FULL + stage), phase, timeout_ns, abort_flag, status, 15)) { ok = false; break; }
+        tc_fence_after();
+        const uint64_t a_desc = make_smem_desc_sw128(sX + stage * kTileXBytes, 16, 1024);
+        const uint64_t b_desc = make_smem_desc_sw128(sW + stage * kTileWBytes, kTileWSubBytes, 1024);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          tc_mma_f16(tmem_base, a_desc + (uint64_t)((kk * 32) >> 4), b_desc + (uint64_t)((kk * 16 * 128) >> 4),
+                     idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
+        tc_commit(bar(EMPTY + stage));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (ok) tc_commit(bar(TFULL));
+      tc_commit(bar(DONE));
+      mbar_wait_bounded(bar(DONE), 0, timeout_ns);
+    }
+  } else {
+    // partial logits of this CTA's k-range -> shared memory (row = token)
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    const bool ok = wait_or_abort(bar(TFULL), 0, timeout_ns, abort_flag, status, 16);
+    if (ok) {
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16);
+#pragma unroll 1
+      for (int c = 0; c < EN; c += 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + (uint32_t)c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) red[row * RS + c + j] = __uint_as_float(v[j]);
+      }
+    } else {
+      for (int c = 0; c < EN; ++c) red[row * RS + c] = 0.f;
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();  // every CTA's partials are in its shared memory
+
+  if (warp >= 2) {
+    constexpr int kRowsPerCta = BM / kSplit;  // 16
+    constexpr int kEpi = 4;
+    for (int i = warp - 2; i < kRowsPerCta; i += kEpi) {
+      const int row = (int)rank * kRowsPerCta + i;
+      const int tok = row;
+      if (tok >= Tn) break;
+      float lv[EN / 32];
+      float m = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < EN / 32; ++j) {
+        const int e = lane + 32 * j;
+        float v = 0.f;
+        const uint32_t local = smem_u32(red + row * RS + e);
+#pragma unroll
+        for (int c = 0; c < kSplit; ++c) v += ld_shared_cluster_f32(map_to_cta(local, c));
+        v += (b_r != nullptr && e < E) ? b_r[e] : 0.f;
+        lv[j] = e < E ? v : -INFINITY;
+        m = fmaxf(m, lv[j]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float ssum = 0.f;
+#pragma unroll
+      for (int j = 0; j < EN / 32; ++j)
+        if (lane + 32 * j < E) ssum += expf(lv[j] - m);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+      for (int p = 0; p < k; ++p) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < EN / 32; ++j)
+          if (lv[j] > bv) { bv = lv[j]; be = lane + 32 * j; }  // ascending e in a lane: lower index kept
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        }
+        if (lane == 0) {
+          topk_idx[(size_t)tok * k + p] = be;
+          topk_gate[(size_t)tok * k + p] = expf(bv - m) / ssum;
+        }
+#pragma unroll
+        for (int j = 0; j < EN / 32; ++j)
+          if (lane + 32 * j == be) lv[j] = -INFINITY;
+      }
+    }
+  }
+  cluster_sync_all();  // no CTA leaves while a peer may still read its partials
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kCols);
+  }
+}
+
 template <int EN, int KMAX>
 cudaError_t launch_en(const CUtensorMap& tmX, const CUtensorMap& tmW, const float* b_r, int Tn, int d, int E,
                       int k, int32_t* idx, float* gate, int* status, uint64_t timeout_ns, cudaStream_t s) {
+  if (EN <= 128 && Tn <= BM && (d + BK - 1) / BK >= 2 * kSplit) {
+    // few tokens, deep d: one CTA would stream all of W_r alone; split d over a cluster
+    const size_t smem = router_split_smem_bytes<EN>();
+    auto kern = router_tc_split_kernel<EN, KMAX>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(kern, dim3(kSplit), dim3(kThreads), smem, s, tmX, tmW, b_r, Tn, d, E, k, idx, gate, status,
+                      timeout_ns);
+  }
   const size_t smem = router_smem_bytes<EN>();
   auto kern = router_tc_kernel<EN, KMAX>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -60,6 +60,10 @@ ROUTER_CASES = [
     dict(T=50, d=96, F=64, E=2, k=2, dt=F32),              # E = k
     dict(T=70, d=64, F=64, E=5, k=1, dt=BF16),
     dict(T=1, d=8, F=8, E=3, k=2, dt=F32),
+    dict(T=1, d=2048, F=64, E=64, k=2, dt=BF16),           # one token, deep d: split over a cluster
+    dict(T=128, d=1024, F=64, E=128, k=4, dt=BF16),        # the split path's largest batch
+    dict(T=129, d=1024, F=64, E=128, k=2, dt=BF16),        # one token more: two plain CTAs
+    dict(T=40, d=4096, F=64, E=256, k=2, dt=BF16),         # E = 256 keeps the plain kernel
 ]
 
 
@@ -73,8 +77,9 @@ def test_router_topk(cfg):
     assert np.all(gate.sum(axis=1) <= 1.0 + 1e-6)
 
 
-def test_router_skew_bias():
-    c = make_case(T=400, d=256, F=64, E=128, k=2, dt=BF16, bias_scale=workloads.SKEW_BIAS_SCALE)
+@pytest.mark.parametrize("T,d", [(400, 256), (64, 4096)], ids=["plain", "split"])
+def test_router_skew_bias(T, d):
+    c = make_case(T=T, d=d, F=64, E=128, k=2, dt=BF16, bias_scale=workloads.SKEW_BIAS_SCALE)
     idx, gate = run_router(c)
     ridx, rgate = oracle_routing(c)
     assert np.array_equal(idx, ridx)
