@@ -54,6 +54,9 @@ WORKLOADS = {
     # Profiling-size decode layer: the decode layer's per-expert shape with 16 experts (4.3 GB), small
     # enough for a full ncu capture of the streaming kernel.
     "decode_t1_e16": Workload("decode_t1_e16", T=1, d=8192, F=8192, E=16, k=2, dtype=DTYPE_BF16),
+    # Profiling-size prefill layer: the prefill layer's per-expert shape (about 128 rows per expert,
+    # d=4096, d_ff=8192) with 16 experts (2.1 GB), small enough for a full ncu capture.
+    "prefill_e16": Workload("prefill_e16", T=1024, d=4096, F=8192, E=16, k=2, dtype=DTYPE_BF16),
     # Skew-routed layer: T=16384, power-law router bias, else as the prefill layer.
     "skew_e128": Workload("skew_e128", T=16384, d=4096, F=8192, E=128, k=2, dtype=DTYPE_BF16,
                           skew=True),
