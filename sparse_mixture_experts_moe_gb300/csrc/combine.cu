@@ -2,8 +2,8 @@
 // csdn/6a462027 §4.2 step 7 (sum the expert outputs back per token). The gate was
 // already applied per row by the down-projection epilogue.
 //
-// One warp per token; each lane owns groups of 8 consecutive columns and reads the
-// fp32 rows with 128-bit loads.
+// One warp per (token, 256-column chunk), so a single decode token still spreads over many
+// warps; each lane owns 8 consecutive columns and reads the fp32 rows with 128-bit loads.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -37,27 +37,29 @@ combine_kernel(const float* __restrict__ y_perm, const int32_t* __restrict__ row
   const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   const int groups = d / 8;
-  for (int t = gwarp; t < Tn; t += nwarps) {
+  const int chunks = (groups + 31) / 32;  // a warp item: one token, 32 groups of 8 columns
+  const long long items = (long long)Tn * chunks;
+  for (long long item = gwarp; item < items; item += nwarps) {
+    const int t = (int)(item / chunks);
+    const int g = (int)(item % chunks) * 32 + lane;
     int rows[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) rows[j] = j < k ? row_of[(size_t)t * k + j] : -1;
-#pragma unroll 2
-    for (int g = lane; g < groups; g += 32) {
-      float acc[8];
+    if (g >= groups) continue;
+    float acc[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j >= k) break;
-        const int r = rows[j];
-        if (r < 0 || r >= A) continue;
-        float v[8];
-        load8(y_perm + (size_t)r * d + 8 * g, v);
+    for (int j = 0; j < 8; ++j) {
+      if (j >= k) break;
+      const int r = rows[j];
+      if (r < 0 || r >= A) continue;
+      float v[8];
+      load8(y_perm + (size_t)r * d + 8 * g, v);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += v[i];
-      }
-      store8(out + (size_t)t * d + 8 * g, acc);
+      for (int i = 0; i < 8; ++i) acc[i] += v[i];
     }
+    store8(out + (size_t)t * d + 8 * g, acc);
   }
 }
 
@@ -66,7 +68,8 @@ combine_kernel(const float* __restrict__ y_perm, const int32_t* __restrict__ row
 cudaError_t launch_combine(const void* y_perm, const int32_t* row_of, int Tn, int d, int k, int dt, void* out,
                            cudaStream_t s) {
   if (Tn == 0) return cudaSuccess;
-  int blocks = (Tn + 7) / 8;
+  const long long items = (long long)Tn * ((d / 8 + 31) / 32);
+  int blocks = (int)((items + 7) / 8 < 0x7fffffff ? (items + 7) / 8 : 0x7fffffff);
   const int cap = device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
   const int A = Tn * k;

@@ -12,7 +12,8 @@
 // exp(l_j - max) / sum. Fixed orders everywhere: results are reproducible.
 //
 // Warps: 0 = TMA producer, 1 = TMEM allocator + MMA issuer, 2..5 = one token per thread.
-// For at most 128 tokens and deep d, a cluster of eight CTAs splits d (router_tc_split_kernel).
+// For at most 128 tokens, deep d (at least 16 k-blocks) and E <= 128, a cluster of eight CTAs
+// splits d (router_tc_split_kernel).
 // All waits are bounded (see wait_or_abort).
 #include <cuda.h>
 
@@ -188,7 +189,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   }
 }
 
-// Split-K version for at most 128 tokens: a cluster of kSplit CTAs, CTA r accumulating the
+// Split-K version: one cluster of kSplit CTAs per 128-token tile, CTA r accumulating the
 // k-blocks [r*KB/kSplit, (r+1)*KB/kSplit) in its own TMEM. Each epilogue thread copies its
 // token's partial logits to shared memory; after a cluster barrier, CTA r finishes tokens
 // [r*16, r*16+16): one warp per token sums the kSplit partials in rank order (DSMEM loads),
@@ -229,6 +230,7 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
   const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, DONE = 2 * STAGES + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
+  const int t0 = (blockIdx.x / kSplit) * BM;  // this cluster's 128-token tile
   const int KB = (d + BK - 1) / BK;
   const int kb0 = (int)rank * KB / kSplit, kb1 = ((int)rank + 1) * KB / kSplit;
 
@@ -259,7 +261,7 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!wait_or_abort(bar(EMPTY + stage), phase ^ 1u, timeout_ns, abort_flag, status, 14)) break;
         mbar_arrive_expect_tx(bar(FULL + stage), kStageBytes);
-        tma_load_2d(sX + stage * kTileXBytes, &tmX, kb * BK, 0, bar(FULL + stage));
+        tma_load_2d(sX + stage * kTileXBytes, &tmX, kb * BK, t0, bar(FULL + stage));
 #pragma unroll
         for (int j = 0; j < EN / 64; ++j)
           tma_load_2d(sW + stage * kTileWBytes + j * kTileWSubBytes, &tmW, 64 * j, kb * BK, bar(FULL + stage));
@@ -320,7 +322,7 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
     constexpr int kEpi = 4;
     for (int i = warp - 2; i < kRowsPerCta; i += kEpi) {
       const int row = (int)rank * kRowsPerCta + i;
-      const int tok = row;
+      const int tok = t0 + row;
       if (tok >= Tn) break;
       float lv[EN / 32];
       float m = -INFINITY;
@@ -376,13 +378,16 @@ template <int EN, int KMAX>
 cudaError_t launch_en(const CUtensorMap& tmX, const CUtensorMap& tmW, const float* b_r, int Tn, int d, int E,
                       int k, int32_t* idx, float* gate, int* status, uint64_t timeout_ns, cudaStream_t s) {
   if (EN <= 128 && Tn <= BM && (d + BK - 1) / BK >= 2 * kSplit) {
-    // few tokens, deep d: one CTA would stream all of W_r alone; split d over a cluster
+    // one token tile and deep d: a single CTA would stream all of W_r alone, so a cluster of
+    // kSplit CTAs splits d (measured: 51 -> 14 us at T = 1, d = 8192). With more tiles the
+    // DSMEM reduction costs more than it saves (T = 4096, d = 1024: 14.6 -> 27.6 us), so
+    // larger batches keep one CTA per tile.
     const size_t smem = router_split_smem_bytes<EN>();
     auto kern = router_tc_split_kernel<EN, KMAX>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    return launch_pdl(kern, dim3(kSplit), dim3(kThreads), smem, s, tmX, tmW, b_r, Tn, d, E, k, idx, gate, status,
-                      timeout_ns);
+    return launch_pdl(kern, dim3(kSplit * ((Tn + BM - 1) / BM)), dim3(kThreads), smem, s, tmX, tmW, b_r, Tn, d, E,
+                      k, idx, gate, status, timeout_ns);
   }
   const size_t smem = router_smem_bytes<EN>();
   auto kern = router_tc_kernel<EN, KMAX>;

@@ -64,6 +64,8 @@ ROUTER_CASES = [
     dict(T=128, d=1024, F=64, E=128, k=4, dt=BF16),        # the split path's largest batch
     dict(T=129, d=1024, F=64, E=128, k=2, dt=BF16),        # one token more: two plain CTAs
     dict(T=40, d=4096, F=64, E=256, k=2, dt=BF16),         # E = 256 keeps the plain kernel
+    dict(T=1000, d=1024, F=64, E=16, k=2, dt=BF16),        # eight split clusters, ragged last tile
+    dict(T=300, d=2048, F=64, E=128, k=3, dt=BF16),
 ]
 
 
