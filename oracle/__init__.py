@@ -11,6 +11,7 @@ routines for the special cases, brute force on tiny inputs). There is no
 "parity unpinned" function.
 """
 from .moe import (  # noqa: F401
-    router_logits, softmax, topk_select, gates_of, gelu, expert_ffn, forward, dense_forward,
-    dispatch, expert_rows_ffn, expert_rows_up, expert_rows_down, combine, ambiguous_tokens, top_share,
+    router_logits, softmax, topk_select, gates_of, gates_renormalised, gelu, expert_ffn, forward, dense_forward,
+    dispatch, capacity, kept_assignments, expert_rows_ffn, expert_rows_up, expert_rows_down, combine, routing_stats, ambiguous_tokens,
+    top_share,
 )

@@ -91,6 +91,15 @@ def gates_of(p: np.ndarray, idx: np.ndarray) -> np.ndarray:
     return np.take_along_axis(np.asarray(p, np.float64), np.asarray(idx), axis=1)
 
 
+def gates_renormalised(logits: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """w[t, j] = softmax over the k selected logits: exp(l[t, idx_j] - m) / sum_i exp(l[t, idx_i] - m).
+
+    The gate variant of hotelren/2927663 §4.3 (top-k on the router logits, then a softmax over
+    the k selected values only), with m the largest selected logit.
+    """
+    return softmax(np.take_along_axis(np.asarray(logits, np.float64), np.asarray(idx), axis=1))
+
+
 def gelu(z: np.ndarray) -> np.ndarray:
     """GeLU(z) = z * Phi(z) = 0.5 * z * (1 + erf(z / sqrt(2))), the exact (erf) form.
 
@@ -112,7 +121,8 @@ def expert_ffn(x_rows: np.ndarray, w1_e: np.ndarray, w2_e: np.ndarray) -> np.nda
 
 
 def forward(x: np.ndarray, w_r: np.ndarray, w1: Union[np.ndarray, Mapping], w2: Union[np.ndarray, Mapping],
-            k: int, b_r: Optional[np.ndarray] = None) -> dict:
+            k: int, b_r: Optional[np.ndarray] = None, renormalise: bool = False,
+            cap: Optional[int] = None) -> dict:
     """Forward pass of the layer for the tokens in x.
 
     out[t] = sum_{j=0..k-1} gate[t, j] * FFN_{idx[t, j]}(x[t]), summed in slot order.
@@ -121,6 +131,8 @@ def forward(x: np.ndarray, w_r: np.ndarray, w1: Union[np.ndarray, Mapping], w2: 
     csdn/6a462027 §4.2 steps 4-7: route, run only the selected experts, sum the
     outputs weighted by the probabilities). ``w1[e]`` / ``w2[e]`` may be arrays
     or any mapping that yields expert e's matrices; only routed experts are read.
+    With ``renormalise`` the gates are ``gates_renormalised`` instead of the raw probabilities;
+    with a capacity ``cap`` the assignments ``kept_assignments`` drops contribute nothing.
     Returns the output and every routing intermediate.
     """
     x = np.asarray(x, np.float64)
@@ -128,40 +140,72 @@ def forward(x: np.ndarray, w_r: np.ndarray, w1: Union[np.ndarray, Mapping], w2: 
     logits = router_logits(x, w_r, b_r)
     p = softmax(logits)
     idx = topk_select(logits, k)
-    gate = gates_of(p, idx)
+    gate = gates_renormalised(logits, idx) if renormalise else gates_of(p, idx)
     y = np.zeros((k, T, d), np.float64)
     for j in range(k):
         for e in np.unique(idx[:, j]):
             rows = np.nonzero(idx[:, j] == e)[0]
             y[j, rows] = expert_ffn(x[rows], w1[int(e)], w2[int(e)])
+    keep = kept_assignments(idx, w_r.shape[1], cap).astype(np.float64)
     out = np.zeros((T, d), np.float64)
     for j in range(k):
-        out = out + gate[:, j:j + 1] * y[j]
-    return {"out": out, "idx": idx, "gate": gate, "p": p, "logits": logits, "y": y}
+        out = out + (keep[:, j] * gate[:, j])[:, None] * y[j]
+    return {"out": out, "idx": idx, "gate": gate, "p": p, "logits": logits, "y": y, "keep": keep}
 
 
-def dense_forward(x: np.ndarray, w_r: np.ndarray, w1, w2, k: int, b_r: Optional[np.ndarray] = None) -> np.ndarray:
+def dense_forward(x: np.ndarray, w_r: np.ndarray, w1, w2, k: int, b_r: Optional[np.ndarray] = None,
+                  renormalise: bool = False) -> np.ndarray:
     """Brute force: evaluate all E experts on every token and weight them by mask_topk * p.
 
     The mask is the rank definition of top-k, independent of ``topk_select``:
     expert e is kept for token t when fewer than k experts beat it, where e' beats
     e if l[t, e'] > l[t, e], or l[t, e'] == l[t, e] and e' < e. Experts are summed
-    in ascending index order.
+    in ascending index order. With ``renormalise`` each kept weight is divided by the sum of
+    the kept probabilities.
     """
     x = np.asarray(x, np.float64)
     logits = router_logits(x, w_r, b_r)
     p = softmax(logits)
     T, E = logits.shape
-    out = np.zeros_like(x)
+    keep = np.zeros((T, E), np.float64)
     for e in range(E):
         le = logits[:, e:e + 1]
         beats = (logits > le) | ((logits == le) & (np.arange(E)[None, :] < e))
-        keep = (beats.sum(axis=1) < k).astype(np.float64)
-        out = out + (keep * p[:, e])[:, None] * expert_ffn(x, w1[e], w2[e])
+        keep[:, e] = (beats.sum(axis=1) < k).astype(np.float64)
+    weight = keep * p
+    if renormalise:
+        weight = weight / weight.sum(axis=1, keepdims=True)
+    out = np.zeros_like(x)
+    for e in range(E):
+        out = out + weight[:, e:e + 1] * expert_ffn(x, w1[e], w2[e])
     return out
 
 
-def dispatch(idx: np.ndarray, E: int, gate: Optional[np.ndarray] = None) -> dict:
+def capacity(T: int, k: int, E: int, cf: float) -> int:
+    """Expert capacity ceil(T*k/E * cf) (aicoding/6a320eef §3.2; its worked example: T=2048, k=2,
+    E=128, cf=2.0 gives 64)."""
+    return int(math.ceil(T * k / E * cf))
+
+
+def kept_assignments(idx: np.ndarray, E: int, cap: Optional[int]) -> np.ndarray:
+    """keep[t, j]: assignment (t, j) is among the first `cap` assignments of its expert in row-major
+    (t, j) order. Reading of the capacity rule (aicoding/6a320eef §3.2: tokens beyond a full
+    expert's capacity are diverted): the assignments past capacity are dropped."""
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    keep = np.ones((T, k), bool)
+    if cap is None:
+        return keep
+    seen = np.zeros(E, np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = idx[t, j]
+            keep[t, j] = seen[e] < cap
+            seen[e] += 1
+    return keep
+
+
+def dispatch(idx: np.ndarray, E: int, gate: Optional[np.ndarray] = None, cap: Optional[int] = None) -> dict:
     """Per-expert histogram, exclusive scan and stable permutation of the T*k assignments.
 
     counts[e] = #{(t, j) : idx[t, j] == e}; offsets = exclusive scan of counts
@@ -169,24 +213,30 @@ def dispatch(idx: np.ndarray, E: int, gate: Optional[np.ndarray] = None) -> dict
     of earlier assignments, in row-major (t, j) order, routed to the same e.
     perm_token[row] = t and row_gate[row] = gate[t, j] invert that map. This is
     the "scatter" of csdn/6a462027 §4.2 step 5 (group each expert's tokens), done
-    as a counting sort.
+    as a counting sort. With a capacity, only the kept assignments (``kept_assignments``) get
+    rows; a dropped one has row_of = -1.
     """
     idx = np.asarray(idx)
     T, k = idx.shape
+    keep = kept_assignments(idx, E, cap)
     counts = np.zeros(E, np.int64)
     for t in range(T):
         for j in range(k):
-            counts[idx[t, j]] += 1
+            if keep[t, j]:
+                counts[idx[t, j]] += 1
     offsets = np.zeros(E + 1, np.int64)
     for e in range(E):
         offsets[e + 1] = offsets[e] + counts[e]
     seen = np.zeros(E, np.int64)
     row_of = np.empty((T, k), np.int64)
-    perm_token = np.empty(T * k, np.int64)
+    perm_token = np.full(T * k, -1, np.int64)
     row_gate = np.zeros(T * k, np.float64)
     for t in range(T):
         for j in range(k):
             e = idx[t, j]
+            if not keep[t, j]:
+                row_of[t, j] = -1
+                continue
             r = offsets[e] + seen[e]
             seen[e] += 1
             row_of[t, j] = r
@@ -262,15 +312,50 @@ def combine(y_perm: np.ndarray, row_of: np.ndarray) -> np.ndarray:
     """out[t] = sum_{j=0..k-1} y_perm[row_of[t, j]], summed in slot order.
 
     The weighted sum of the k expert outputs (csdn/6a462027 §4.2 step 7,
-    "scatter_add"); the weights were already applied per row.
+    "scatter_add"); the weights were already applied per row. A slot with row -1 (dropped at
+    capacity) contributes nothing.
     """
     y_perm = np.asarray(y_perm, np.float64)
     row_of = np.asarray(row_of)
     T, k = row_of.shape
     out = np.zeros((T, y_perm.shape[1]), np.float64)
     for j in range(k):
-        out = out + y_perm[row_of[:, j]]
+        valid = row_of[:, j] >= 0
+        out = out + np.where(valid[:, None], y_perm[np.where(valid, row_of[:, j], 0)], 0.0)
     return out
+
+
+def routing_stats(logits: np.ndarray, idx: np.ndarray) -> dict:
+    """Statistics of one batch's routing, reported beside the top-k selection.
+
+    soft_load[e] = (1/T) sum_t p[t, e]: the expected share of expert e, the probabilities summed
+        over the batch and divided by the number of tokens (csdn/6a462027 §4.2, its expert-load
+        buffer);
+    hard_load[e] = #{(t, j) : idx[t, j] = e} / (T k): the share of the T*k assignments that go
+        to expert e;
+    balance = sum_e (hard_load[e] - 1/E)^2: the load-balancing term without its weight lambda
+        (aicoding/6a320eef §3.2; csdn/6a462027 §3.1). Reading: the formula's "tokens routed to
+        expert i over all tokens" counts the T*k assignments, so the shares sum to one and the
+        target 1/E is the balanced point;
+    entropy = (1/T) sum_t -sum_e p[t, e] ln p[t, e], in nats: the mean entropy of the router's
+        output distribution (aicoding/6a320eef §5.2, whose alert level lies between 0 and ln 128).
+    The probabilities are the full softmax over the E experts, whatever the gates are.
+    """
+    l = np.asarray(logits, np.float64)
+    idx = np.asarray(idx)
+    T, E = l.shape
+    k = idx.shape[1]
+    p = softmax(l)
+    soft = p.sum(axis=0) / T
+    counts = np.zeros(E, np.int64)
+    for e in idx.reshape(-1):
+        counts[int(e)] += 1
+    hard = counts / float(T * k)
+    balance = float(np.sum((hard - 1.0 / E) ** 2))
+    z = l - l.max(axis=1, keepdims=True)
+    log_p = z - np.log(np.exp(z).sum(axis=1, keepdims=True))  # ln p, finite where p underflows
+    entropy = float(np.mean(-(p * log_p).sum(axis=1)))
+    return {"soft_load": soft, "hard_load": hard, "balance": balance, "entropy": entropy}
 
 
 def ambiguous_tokens(logits: np.ndarray, k: int, min_gap: float) -> np.ndarray:

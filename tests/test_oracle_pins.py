@@ -226,10 +226,122 @@ def check_ambiguous_tokens():
     assert om.ambiguous_tokens(l, 2, 1e-3).tolist() == [1, 2]
 
 
+def check_renormalised_gates():
+    """hotelren §4.3 gates: softmax of the k selected logits equals p_j / sum of the selected p (closed form),
+    matches scipy, sums to one; k = E gives the plain gates; k = 1 gives gate 1; routed equals brute force."""
+    rng = np.random.default_rng(11)
+    l = rng.standard_normal((40, 16)) * 2
+    idx = om.topk_select(l, 3)
+    w = om.gates_renormalised(l, idx)
+    p = om.softmax(l)
+    sel = np.take_along_axis(p, idx, 1)
+    assert np.allclose(w, sel / sel.sum(axis=1, keepdims=True), rtol=1e-13, atol=0)
+    assert np.allclose(w, scipy.special.softmax(np.take_along_axis(l, idx, 1), axis=1), rtol=1e-13, atol=0)
+    assert np.allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-15)
+    full = om.topk_select(l, 16)
+    assert np.allclose(om.gates_renormalised(l, full), om.gates_of(p, full), rtol=1e-12, atol=0)
+    assert np.array_equal(om.gates_renormalised(l, om.topk_select(l, 1)), np.ones((40, 1)))
+    for (T, d, F, E, k) in [(12, 8, 10, 6, 2), (9, 6, 6, 4, 3)]:
+        x, w_r, w1, w2 = _rand_layer(rng, T, d, F, E)
+        routed = om.forward(x, w_r, w1, w2, k, renormalise=True)["out"]
+        dense = om.dense_forward(x, w_r, w1, w2, k, renormalise=True)
+        assert np.max(np.abs(routed - dense)) / math.sqrt(float(np.mean(dense ** 2))) < 1e-12
+
+
+def check_capacity():
+    """aicoding §3.2: capacity ceil(T*k/E*cf) (worked example 64); the first C assignments of each expert in
+    (t, j) order are kept (independently ranked with numpy's stable argsort); a capacity nobody reaches changes
+    nothing; the forward pass with drops equals a per-assignment brute force."""
+    f = _load("page_facts.json")["capacity_worked_example"]
+    assert om.capacity(f["T"], f["k"], f["E"], f["cf"]) == f["capacity"]
+    rng = np.random.default_rng(12)
+    T, k, E = 120, 2, 6
+    l = rng.standard_normal((T, E)) + np.array([1.5, 1.0, 0.0, 0.0, -0.5, -1.0])
+    idx = om.topk_select(l, k)
+    gate = om.gates_of(om.softmax(l), idx)
+    flat = idx.reshape(-1)
+    order = np.argsort(flat, kind="stable")
+    rank = np.empty_like(order)
+    for e in range(E):
+        pos = order[flat[order] == e]
+        rank[pos] = np.arange(len(pos))
+    for C in [1, 3, 17, 1000]:
+        keep = om.kept_assignments(idx, E, C)
+        assert np.array_equal(keep.reshape(-1), rank < C)
+        dp = om.dispatch(idx, E, gate, C)
+        assert np.array_equal(dp["counts"], np.minimum(np.bincount(flat, minlength=E), C))
+        assert np.array_equal(dp["row_of"].reshape(-1) >= 0, keep.reshape(-1))
+        kept_rows = dp["row_of"].reshape(-1)[keep.reshape(-1)]
+        assert np.array_equal(np.sort(kept_rows), np.arange(dp["offsets"][-1]))
+    x, w_r, w1, w2 = _rand_layer(rng, T=40, d=6, F=8, E=5)
+    res = om.forward(x, w_r, w1, w2, 2)
+    assert np.array_equal(om.forward(x, w_r, w1, w2, 2, cap=80)["out"], res["out"])
+    C = 7
+    capped = om.forward(x, w_r, w1, w2, 2, cap=C)["out"]
+    brute = np.zeros_like(capped)
+    seen = {}
+    for t in range(40):
+        for j in range(2):
+            e = int(res["idx"][t, j])
+            if seen.get(e, 0) < C:
+                brute[t] += res["gate"][t, j] * om.expert_ffn(x[t:t + 1], w1[e], w2[e])[0]
+            seen[e] = seen.get(e, 0) + 1
+    assert np.max(np.abs(capped - brute)) < 1e-12
+
+
+def check_routing_stats():
+    """Routing statistics: soft load = column means of scipy's softmax; equal logits give entropy ln E
+    (closed form) and equal soft loads; entropy matches scipy.stats.entropy per token; a batch whose
+    counts are equal by construction has balance exactly 0 while its soft loads differ; every token on
+    one expert (k = 1) gives balance 1 - 1/E (closed form); loops over a tiny case agree."""
+    import scipy.stats
+    rng = np.random.default_rng(13)
+    T, E, k = 50, 8, 2
+    l = rng.standard_normal((T, E)) * 1.5
+    idx = om.topk_select(l, k)
+    st = om.routing_stats(l, idx)
+    sp = scipy.special.softmax(l, axis=1)
+    assert np.allclose(st["soft_load"], sp.mean(axis=0), rtol=1e-13, atol=0)
+    assert abs(st["soft_load"].sum() - 1.0) < 1e-14 and abs(st["hard_load"].sum() - 1.0) < 1e-14
+    assert np.array_equal(st["hard_load"] * T * k, np.bincount(idx.reshape(-1), minlength=E))
+    assert abs(st["entropy"] - float(np.mean(scipy.stats.entropy(sp, axis=1)))) < 1e-13
+    flat = om.routing_stats(np.full((7, 16), 0.3), om.topk_select(np.full((7, 16), 0.3), 2))
+    assert abs(flat["entropy"] - math.log(16)) < 1e-14
+    assert np.allclose(flat["soft_load"], 1.0 / 16, rtol=0, atol=1e-16)
+    # token t prefers expert t % E, by a margin that grows with t: equal counts, unequal soft loads
+    lb = np.zeros((4 * E, E))
+    for t in range(4 * E):
+        lb[t, t % E] = 1.0 + 0.5 * (t % E)
+    bal = om.routing_stats(lb, om.topk_select(lb, 1))
+    assert bal["balance"] == 0.0 and np.std(bal["soft_load"]) > 1e-3
+    one = np.zeros((30, E))
+    one[:, 5] = 3.0
+    r1 = om.routing_stats(one, om.topk_select(one, 1))
+    assert abs(r1["balance"] - (1.0 - 1.0 / E)) < 1e-15
+    ls = rng.standard_normal((5, 4))
+    ids = om.topk_select(ls, 2)
+    soft, ent = [0.0] * 4, 0.0
+    for t in range(5):
+        ex = [math.exp(v) for v in ls[t]]
+        z = sum(ex)
+        for e in range(4):
+            soft[e] += ex[e] / z / 5
+            ent -= ex[e] / z * math.log(ex[e] / z) / 5
+    cnt = [0] * 4
+    for t in range(5):
+        for j in range(2):
+            cnt[ids[t, j]] += 1
+    small = om.routing_stats(ls, ids)
+    assert np.allclose(small["soft_load"], soft, rtol=1e-13, atol=0)
+    assert abs(small["entropy"] - ent) < 1e-13
+    assert abs(small["balance"] - sum((c / 10 - 0.25) ** 2 for c in cnt)) < 1e-15
+
+
 PINS = [check_worked_example, check_router_closed_form, check_softmax_library, check_topk_ties_and_order,
         check_gelu_closed_form, check_single_expert_is_mlp, check_k_equals_E_is_softmax_mixture,
         check_routed_equals_dense_bruteforce, check_routing_invariants, check_activation_fraction,
-        check_dispatch_stable_sort, check_steps_compose_to_forward, check_ambiguous_tokens]
+        check_dispatch_stable_sort, check_steps_compose_to_forward, check_ambiguous_tokens,
+        check_renormalised_gates, check_capacity, check_routing_stats]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -270,6 +382,15 @@ def _mut_gates_renormalised(p, idx):
     return g / g.sum(axis=1, keepdims=True)
 
 
+def _mut_renormalised_over_all(logits, idx):
+    return np.take_along_axis(om.softmax(logits), np.asarray(idx), axis=1)
+
+
+def _mut_capacity_keeps_last(idx, E, cap):
+    keep = _ORIG_KEPT(np.asarray(idx)[::-1], E, cap)
+    return keep[::-1]
+
+
 def _mut_ffn_transposed_w1(x_rows, w1_e, w2_e):
     return om.gelu(np.asarray(x_rows) @ np.asarray(w1_e).T) @ np.asarray(w2_e)
 
@@ -278,20 +399,23 @@ def _mut_router_drops_bias(x, w_r, b_r=None):
     return np.asarray(x, np.float64) @ np.asarray(w_r, np.float64)
 
 
-def _mut_dispatch_unstable(idx, E, gate=None):
-    res = _ORIG_DISPATCH(idx, E, gate)
+def _mut_dispatch_unstable(idx, E, gate=None, cap=None):
+    res = _ORIG_DISPATCH(idx, E, gate, cap)
     # reverse the order of rows inside each expert's range
     offs = res["offsets"]
     row_of = res["row_of"].copy()
     for t in range(row_of.shape[0]):
         for j in range(row_of.shape[1]):
             r = row_of[t, j]
+            if r < 0:
+                continue
             e = np.searchsorted(offs, r, side="right") - 1
             row_of[t, j] = offs[e] + offs[e + 1] - 1 - r
-    perm = np.empty_like(res["perm_token"])
+    perm = np.full_like(res["perm_token"], -1)
     for t in range(row_of.shape[0]):
         for j in range(row_of.shape[1]):
-            perm[row_of[t, j]] = t
+            if row_of[t, j] >= 0:
+                perm[row_of[t, j]] = t
     res = dict(res, row_of=row_of, perm_token=perm)
     return res
 
@@ -302,17 +426,38 @@ def _mut_combine_first_slot_twice(y_perm, row_of):
     return _ORIG_COMBINE(y_perm, row_of)
 
 
-def _mut_forward_drops_last_slot(x, w_r, w1, w2, k, b_r=None):
-    res = _ORIG_FORWARD(x, w_r, w1, w2, k, b_r)
+def _mut_forward_drops_last_slot(x, w_r, w1, w2, k, b_r=None, renormalise=False, cap=None):
+    res = _ORIG_FORWARD(x, w_r, w1, w2, k, b_r, renormalise, cap)
     res = dict(res)
     res["out"] = res["out"] - res["gate"][:, -1:] * res["y"][-1] if k > 1 else res["out"]
     return res
 
 
+def _mut_stats(change):
+    def f(logits, idx):
+        st = dict(_ORIG_STATS(logits, idx))
+        l = np.asarray(logits, np.float64)
+        T, E = l.shape
+        k = np.asarray(idx).shape[1]
+        if change == "log2":
+            st["entropy"] = st["entropy"] / math.log(2.0)
+        elif change == "soft_over_assignments":
+            st["soft_load"] = st["soft_load"] / k
+        elif change == "balance_of_soft_load":
+            st["balance"] = float(np.sum((st["soft_load"] - 1.0 / E) ** 2))
+        elif change == "hard_over_tokens":
+            st["hard_load"] = st["hard_load"] * k
+            st["balance"] = float(np.sum((st["hard_load"] - 1.0 / E) ** 2))
+        return st
+    return f
+
+
 _ORIG_DISPATCH = om.dispatch
 _ORIG_TOPK = om.topk_select
+_ORIG_KEPT = om.kept_assignments
 _ORIG_COMBINE = om.combine
 _ORIG_FORWARD = om.forward
+_ORIG_STATS = om.routing_stats
 
 MUTANTS = {
     "gelu_sign": ("gelu", _mut_gelu_sign),
@@ -321,11 +466,17 @@ MUTANTS = {
     "topk_smallest": ("topk_select", _mut_topk_smallest),
     "topk_last_on_tie": ("topk_select", _mut_topk_last_on_tie),
     "gates_renormalised": ("gates_of", _mut_gates_renormalised),
+    "renormalised_over_all_experts": ("gates_renormalised", _mut_renormalised_over_all),
+    "capacity_keeps_last": ("kept_assignments", _mut_capacity_keeps_last),
     "ffn_transposed_w1": ("expert_ffn", _mut_ffn_transposed_w1),
     "router_drops_bias": ("router_logits", _mut_router_drops_bias),
     "dispatch_unstable": ("dispatch", _mut_dispatch_unstable),
     "combine_first_slot_twice": ("combine", _mut_combine_first_slot_twice),
     "forward_drops_last_slot": ("forward", _mut_forward_drops_last_slot),
+    "stats_entropy_log2": ("routing_stats", _mut_stats("log2")),
+    "stats_soft_load_over_assignments": ("routing_stats", _mut_stats("soft_over_assignments")),
+    "stats_balance_of_soft_load": ("routing_stats", _mut_stats("balance_of_soft_load")),
+    "stats_hard_load_over_tokens": ("routing_stats", _mut_stats("hard_over_tokens")),
 }
 
 
@@ -344,5 +495,5 @@ def test_planted_mistakes(name, monkeypatch):
 
 def test_package_exports():
     for name in ["router_logits", "softmax", "topk_select", "gates_of", "gelu", "expert_ffn", "forward",
-                 "dense_forward", "dispatch", "expert_rows_ffn", "expert_rows_up", "expert_rows_down", "combine", "ambiguous_tokens", "top_share"]:
+                 "dense_forward", "gates_renormalised", "dispatch", "capacity", "kept_assignments", "expert_rows_ffn", "expert_rows_up", "expert_rows_down", "combine", "routing_stats", "ambiguous_tokens", "top_share"]:
         assert callable(getattr(oracle, name))
