@@ -85,6 +85,32 @@ typedef enum {
 moe_status moe_router_topk(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
                            moe_dtype dt, int32_t* topk_idx, float* topk_gate, void* stream);
 
+/* Router flags (moe_router_topk_ex, moe_forward_ex; 0 = the layer as defined above).
+ * MOE_GATES_RENORMALISE: gate[t, j] = softmax over the k chosen logits only, exp(l_j - m) /
+ *   sum_i exp(l_i - m) over the chosen i (hotelren/2927663 §4.3, top-k on the logits, then a
+ *   softmax of the selected values); the gates of a token sum to one. */
+enum { MOE_GATES_RENORMALISE = 1 };
+moe_status moe_router_topk_ex(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
+                              moe_dtype dt, int flags, int32_t* topk_idx, float* topk_gate, void* stream);
+
+/* moe_router_topk_stats — moe_router_topk_ex that also writes the batch's routing statistics,
+ *   computed inside the router kernel beside the top-k. p is the full softmax over the E experts
+ *   (whatever the gates are); `stats` is a device array of MOE_ROUTER_STATS_LEN(E) floats:
+ *     stats[e]         (1/T) sum_t p[t, e]: soft load of expert e (csdn/6a462027 §4.2, the
+ *                      probabilities summed over the batch divided by the token count);
+ *     stats[E + e]     #{(t, j) : idx[t, j] = e} / (T k): expert e's share of the assignments;
+ *     stats[2E]        sum_e (stats[E + e] - 1/E)^2: the load-balancing term before its weight
+ *                      lambda (aicoding/6a320eef §3.2; csdn/6a462027 §3.1);
+ *     stats[2E + 1]    (1/T) sum_t -sum_e p[t, e] ln p[t, e]: mean router entropy in nats
+ *                      (aicoding/6a320eef §5.2).
+ *   Partial sums per CTA go to the workspace (moe_workspace_bytes with any d, F covers them);
+ *   the CTA that finishes last reduces them in a fixed order, so the values are reproducible.
+ *   T = 0: nothing is written. A workspace that is too small or NULL: MOE_ERR_INVALID_ARG. */
+#define MOE_ROUTER_STATS_LEN(E) (2 * (E) + 2)
+moe_status moe_router_topk_stats(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
+                                 moe_dtype dt, int flags, int32_t* topk_idx, float* topk_gate, float* stats,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------------------------------------
  * moe_dispatch — per-expert histogram, exclusive scan, stable permutation and row gather.
  *   csdn/6a462027 §4.2 steps 4-5 (find the selected experts, scatter each expert's tokens to it).
@@ -102,6 +128,18 @@ moe_status moe_dispatch(const void* x, const int32_t* topk_idx, const float* top
                         int k, moe_dtype dt, int32_t* counts, int32_t* offsets, int32_t* perm_token,
                         int32_t* row_of, float* row_gate, void* x_perm, void* workspace, size_t ws_bytes,
                         void* stream);
+
+/* moe_dispatch_ex — moe_dispatch with an expert capacity (aicoding/6a320eef §3.2: capacity =
+ *   ceil(batch * k / num_experts * capacity_factor); an expert that is full diverts further tokens).
+ *   capacity > 0: each expert keeps its first `capacity` assignments in row-major (t, j) order and the
+ *   later ones are dropped (row_of = -1, no row, no contribution to the output); counts[e] is the
+ *   number kept. capacity = 0: no limit (moe_dispatch). Negative: MOE_ERR_INVALID_ARG.
+ * moe_capacity — ceil(T * k / E * cf) as an int, -1 on bad arguments. */
+moe_status moe_dispatch_ex(const void* x, const int32_t* topk_idx, const float* topk_gate, int T, int d, int E,
+                           int k, moe_dtype dt, int capacity, int32_t* counts, int32_t* offsets,
+                           int32_t* perm_token, int32_t* row_of, float* row_gate, void* x_perm, void* workspace,
+                           size_t ws_bytes, void* stream);
+int moe_capacity(int T, int k, int E, double cf);
 
 /* ---------------------------------------------------------------------------------------------
  * moe_dispatch_noalloc — moe_dispatch without a workspace, for callers that cannot provide device
@@ -180,17 +218,20 @@ moe_status moe_combine(const void* y_perm, const int32_t* row_of, int T, int d, 
 /* ---------------------------------------------------------------------------------------------
  * moe_forward — the whole layer: router_topk, dispatch, expert_up, expert_down, combine.
  * In:  x [T, d], w_r [d, E], b_r [E] or NULL, w1 [E, d, F], w2 [E, F, d].
- * Out: out [T, d] (dt; moe_forward_ex takes the output's element type `out_dt` separately, e.g.
- *      fp32 output of a bf16 layer). topk_idx [T, k], topk_gate [T, k] and counts [E] are optional
- *      copies of the routing (NULL: kept in the workspace only).
+ * Out: out [T, d] (dt), and optional copies of the routing (NULL: kept in the workspace only):
+ *      topk_idx [T, k], topk_gate [T, k], counts [E].
+ * moe_forward_ex also takes: the output's element type `out_dt` (e.g. fp32 output of a bf16
+ *      layer), the FFN kernel family `path`, router `flags` (MOE_GATES_RENORMALISE), an expert
+ *      `capacity` (as in moe_dispatch_ex; 0 = no limit) and `router_stats` (NULL, or
+ *      MOE_ROUTER_STATS_LEN(E) floats as in moe_router_topk_stats).
  */
 moe_status moe_forward(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2, int T,
                        int d, int F, int E, int k, moe_dtype dt, void* out, int32_t* topk_idx, float* topk_gate,
                        int32_t* counts, void* workspace, size_t ws_bytes, void* stream);
 moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2,
-                          int T, int d, int F, int E, int k, moe_dtype dt, moe_dtype out_dt, moe_path path, void* out,
-                          int32_t* topk_idx, float* topk_gate, int32_t* counts, void* workspace, size_t ws_bytes,
-                          void* stream);
+                          int T, int d, int F, int E, int k, moe_dtype dt, moe_dtype out_dt, moe_path path,
+                          int flags, int capacity, void* out, int32_t* topk_idx, float* topk_gate,
+                          int32_t* counts, float* router_stats, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Workspace and status.

@@ -15,8 +15,8 @@ from typing import Optional
 from . import _lib
 from ._lib import (  # noqa: F401
     MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK, MOE_ERR_DEVICE_TIMEOUT,
-    MOE_DTYPE_F32, MOE_DTYPE_BF16, PATH_AUTO, PATH_TENSOR, PATH_STREAM, PATH_SIMT, PATH_TENSOR_PAIR, MoeError,
-    router_topk, dispatch, dispatch_noalloc, expert_up, expert_down, grouped_ffn, combine, forward, workspace_bytes, workspace_init,
+    GATES_RENORMALISE, MOE_DTYPE_F32, MOE_DTYPE_BF16, PATH_AUTO, PATH_TENSOR, PATH_STREAM, PATH_SIMT, PATH_TENSOR_PAIR, MoeError,
+    router_topk, router_topk_stats, router_stats_len, dispatch, dispatch_noalloc, capacity, expert_up, expert_down, grouped_ffn, combine, forward, workspace_bytes, workspace_init,
     get_device_status, status_string, selftest_wait_timeout, lib,
 )
 
@@ -24,7 +24,10 @@ from ._lib import (  # noqa: F401
 class MoELayer:
     """Holds the layer's weights and a reusable workspace; calling it runs moe_forward on the current stream."""
 
-    def __init__(self, w_r, w1, w2, k: int = 2, b_r=None, path: int = PATH_AUTO):
+    def __init__(self, w_r, w1, w2, k: int = 2, b_r=None, path: int = PATH_AUTO, renormalise: bool = False,
+                 capacity_factor: Optional[float] = None):
+        """capacity_factor: None for no expert capacity, else each call keeps at most
+        ceil(T * k / E * capacity_factor) assignments per expert (the later ones are dropped)."""
         import torch
         if not (w_r.is_cuda and w1.is_cuda and w2.is_cuda):
             raise ValueError("MoELayer: weights must be CUDA tensors")
@@ -37,6 +40,8 @@ class MoELayer:
         self.w_r, self.w1, self.w2 = w_r.contiguous(), w1.contiguous(), w2.contiguous()
         self.b_r = None if b_r is None else b_r.to(torch.float32).contiguous()
         self.path = path
+        self.renormalise = renormalise
+        self.capacity_factor = capacity_factor
         self._ws = None
         self._ws_T = -1
 
@@ -52,15 +57,19 @@ class MoELayer:
         return self._ws
 
     def __call__(self, x, out: Optional["object"] = None, topk_idx=None, topk_gate=None, counts=None,
-                 out_dtype=None):
-        """Forward pass of x [T, d]; the output is in x's dtype unless out / out_dtype say otherwise."""
+                 out_dtype=None, router_stats=None):
+        """Forward pass of x [T, d]; the output is in x's dtype unless out / out_dtype say otherwise.
+        router_stats: optional float32 device tensor of router_stats_len(E) for the routing statistics."""
         import torch
         T = int(x.shape[0])
         if out is None:
             out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=x.device)
+        cap = 0 if self.capacity_factor is None else capacity(T, self.k, self.E, self.capacity_factor)
+        if cap < 0:
+            raise MoeError(MOE_ERR_INVALID_ARG, "capacity_factor")
         forward(x, self.w_r, self.b_r, self.w1, self.w2, T, self.d, self.F, self.E, self.k, self.dt, out,
                 self.workspace(T), topk_idx=topk_idx, topk_gate=topk_gate, counts=counts, path=self.path,
-                out_dt=_lib.dtype_code(out))
+                out_dt=_lib.dtype_code(out), renormalise=self.renormalise, capacity=cap, router_stats=router_stats)
         return out
 
     def device_status(self):

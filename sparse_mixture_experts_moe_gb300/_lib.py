@@ -24,6 +24,7 @@ MOE_DTYPE_F32 = 0
 MOE_DTYPE_BF16 = 1
 
 PATH_AUTO, PATH_TENSOR, PATH_STREAM, PATH_SIMT, PATH_TENSOR_PAIR = 0, 1, 2, 3, 4
+GATES_RENORMALISE = 1
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -32,7 +33,10 @@ _sz = ctypes.c_size_t
 # name -> argument types (all return int moe_status unless listed in _RESTYPES)
 SIGNATURES = {
     "moe_router_topk": [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _p],
+    "moe_router_topk_ex": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p],
     "moe_dispatch": [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _sz, _p],
+    "moe_dispatch_ex": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _sz, _p],
+    "moe_capacity": [_i, _i, _i, ctypes.c_double],
     "moe_dispatch_noalloc": [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p],
     "moe_expert_up": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
     "moe_expert_up_ex": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
@@ -42,7 +46,8 @@ SIGNATURES = {
     "moe_grouped_ffn_ex": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
     "moe_combine": [_p, _p, _i, _i, _i, _i, _p, _p],
     "moe_forward": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _sz, _p],
-    "moe_forward_ex": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _sz, _p],
+    "moe_forward_ex": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _sz, _p],
+    "moe_router_topk_stats": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _sz, _p],
     "moe_workspace_bytes": [_i, _i, _i, _i, _i, _i],
     "moe_workspace_init": [_p, _sz, _p],
     "moe_get_device_status": [_p, _p, _p],
@@ -130,17 +135,39 @@ def get_device_status(ws, stream=None):
     return rc, detail.value
 
 
-def router_topk(x, w_r, b_r, T, d, E, k, dt, topk_idx, topk_gate, stream=None, check=True):
-    rc = lib().moe_router_topk(_ptr(x), _ptr(w_r), _ptr(b_r), T, d, E, k, dt, _ptr(topk_idx), _ptr(topk_gate),
-                               _stream(stream))
+def router_topk(x, w_r, b_r, T, d, E, k, dt, topk_idx, topk_gate, renormalise=False, stream=None, check=True):
+    """renormalise: gates are the softmax over the k chosen logits (GATES_RENORMALISE)."""
+    rc = lib().moe_router_topk_ex(_ptr(x), _ptr(w_r), _ptr(b_r), T, d, E, k, dt,
+                                  GATES_RENORMALISE if renormalise else 0, _ptr(topk_idx), _ptr(topk_gate),
+                                  _stream(stream))
     return _check(rc, "moe_router_topk") if check else rc
 
 
+def router_stats_len(E) -> int:
+    """Floats of the routing-statistics output: soft load [E], assignment share [E], balance, entropy."""
+    return 2 * E + 2
+
+
+def router_topk_stats(x, w_r, b_r, T, d, E, k, dt, topk_idx, topk_gate, stats, ws, renormalise=False, stream=None,
+                      check=True):
+    """moe_router_topk_stats: the router plus the batch's routing statistics in `stats`."""
+    rc = lib().moe_router_topk_stats(_ptr(x), _ptr(w_r), _ptr(b_r), T, d, E, k, dt,
+                                     GATES_RENORMALISE if renormalise else 0, _ptr(topk_idx), _ptr(topk_gate),
+                                     _ptr(stats), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    return _check(rc, "moe_router_topk_stats") if check else rc
+
+
+def capacity(T, k, E, cf) -> int:
+    """ceil(T*k/E*cf), the expert capacity moe_dispatch_ex / moe_forward_ex take."""
+    return int(lib().moe_capacity(T, k, E, float(cf)))
+
+
 def dispatch(x, topk_idx, topk_gate, T, d, E, k, dt, counts, offsets, perm_token, row_of, row_gate, x_perm, ws,
-             stream=None, check=True):
-    rc = lib().moe_dispatch(_ptr(x), _ptr(topk_idx), _ptr(topk_gate), T, d, E, k, dt, _ptr(counts), _ptr(offsets),
-                            _ptr(perm_token), _ptr(row_of), _ptr(row_gate), _ptr(x_perm), _ptr(ws),
-                            ws.numel() * ws.element_size(), _stream(stream))
+             capacity=0, stream=None, check=True):
+    """capacity > 0: each expert keeps its first `capacity` assignments (moe_dispatch_ex)."""
+    rc = lib().moe_dispatch_ex(_ptr(x), _ptr(topk_idx), _ptr(topk_gate), T, d, E, k, dt, int(capacity),
+                               _ptr(counts), _ptr(offsets), _ptr(perm_token), _ptr(row_of), _ptr(row_gate),
+                               _ptr(x_perm), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     return _check(rc, "moe_dispatch") if check else rc
 
 
@@ -178,12 +205,13 @@ def combine(y_perm, row_of, T, d, k, dt, out, stream=None, check=True):
 
 
 def forward(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws, topk_idx=None, topk_gate=None, counts=None,
-            path=PATH_AUTO, out_dt=None, stream=None, check=True):
-    """out_dt: element type of `out` (default: dt)."""
+            path=PATH_AUTO, out_dt=None, renormalise=False, capacity=0, router_stats=None, stream=None, check=True):
+    """out_dt: element type of `out` (default: dt); renormalise: GATES_RENORMALISE; capacity: as dispatch;
+    router_stats: None or a float32 device tensor of router_stats_len(E) (as router_topk_stats)."""
     out_dt = dt if out_dt is None else out_dt
     rc = lib().moe_forward_ex(_ptr(x), _ptr(w_r), _ptr(b_r), _ptr(w1), _ptr(w2), T, d, F, E, k, dt, out_dt, path,
-                              _ptr(out),
-                              _ptr(topk_idx), _ptr(topk_gate), _ptr(counts), _ptr(ws),
+                              GATES_RENORMALISE if renormalise else 0, int(capacity), _ptr(out),
+                              _ptr(topk_idx), _ptr(topk_gate), _ptr(counts), _ptr(router_stats), _ptr(ws),
                               ws.numel() * ws.element_size(), _stream(stream))
     return _check(rc, "moe_forward") if check else rc
 

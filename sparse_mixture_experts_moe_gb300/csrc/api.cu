@@ -1,6 +1,7 @@
 // C ABI of the layer (include/moe.h): host-side validation, workspace layout, path
 // choice and step sequencing. Every entry point validates all arguments before it
 // makes any CUDA call, so invalid calls fail the same way with or without a GPU.
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 
@@ -26,14 +27,17 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Workspace regions, in this order; each starts on a 256-byte boundary.
 struct Layout {
-  size_t header, blk_counts, blk_base, topk_idx, topk_gate, counts, offsets, perm_token, row_of, row_gate, h,
-      x_perm, y_perm, end;
-  size_t dispatch_end, ffn_end, grouped_end;
+  size_t header, stats_part, blk_counts, blk_base, topk_idx, topk_gate, counts, offsets, perm_token, row_of,
+      row_gate, h, x_perm, y_perm, end;
+  size_t stats_end, dispatch_end, ffn_end, grouped_end;
   Layout(int T, int d, int F, int E, int k, int dt) {
     const size_t A = (size_t)T * k, eb = elem_bytes(dt);
     const size_t nb = (A + kDispatchChunk - 1) / kDispatchChunk;
+    const size_t stat_rows = ((size_t)T + kRouterStatsTokensPerCta - 1) / kRouterStatsTokensPerCta;
     size_t o = 0;
     header = o; o += align256(kWsHeaderBytes);
+    stats_part = o; o += align256(stat_rows * (2 * (size_t)E + 1) * 4);
+    stats_end = o;
     blk_counts = o; o += align256(nb * E * 4);
     blk_base = o; o += align256(nb * E * 4);
     dispatch_end = o;
@@ -149,19 +153,53 @@ moe_status moe_get_device_status(void* workspace, int32_t* detail, void* stream)
 
 moe_status moe_router_topk(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
                            moe_dtype dt, int32_t* topk_idx, float* topk_gate, void* stream) {
-  if (!sizes_ok(T, d, 8, E, k, dt)) return MOE_ERR_INVALID_ARG;
+  return moe_router_topk_ex(x, w_r, b_r, T, d, E, k, dt, 0, topk_idx, topk_gate, stream);
+}
+
+moe_status moe_router_topk_stats(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
+                                 moe_dtype dt, int flags, int32_t* topk_idx, float* topk_gate, float* stats,
+                                 void* workspace, size_t ws_bytes, void* stream) {
+  if (!sizes_ok(T, d, 8, E, k, dt) || (flags & ~MOE_GATES_RENORMALISE) != 0) return MOE_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned16(workspace) || stats == nullptr) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < Layout(T, d, 8, E, k, dt).stats_end) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (x == nullptr || w_r == nullptr || topk_idx == nullptr || topk_gate == nullptr) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, topk_idx, topk_gate, nullptr,
-                                        wait_timeout_ns(), (cudaStream_t)stream));
+  // header words: [0] status, [1] detail, [3] the statistics ticket
+  const RouterStats st{at<float>(workspace, Layout(T, d, 8, E, k, dt).stats_part), stats, at<int>(workspace, 0) + 3};
+  return cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, flags, st, topk_idx, topk_gate,
+                                        at<int>(workspace, 0), wait_timeout_ns(), (cudaStream_t)stream));
+}
+
+moe_status moe_router_topk_ex(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
+                              moe_dtype dt, int flags, int32_t* topk_idx, float* topk_gate, void* stream) {
+  if (!sizes_ok(T, d, 8, E, k, dt) || (flags & ~MOE_GATES_RENORMALISE) != 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (x == nullptr || w_r == nullptr || topk_idx == nullptr || topk_gate == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, flags, RouterStats{nullptr, nullptr, nullptr},
+                                        topk_idx, topk_gate, nullptr, wait_timeout_ns(), (cudaStream_t)stream));
 }
 
 moe_status moe_dispatch(const void* x, const int32_t* topk_idx, const float* topk_gate, int T, int d, int E,
                         int k, moe_dtype dt, int32_t* counts, int32_t* offsets, int32_t* perm_token,
                         int32_t* row_of, float* row_gate, void* x_perm, void* workspace, size_t ws_bytes,
                         void* stream) {
-  if (!sizes_ok(T, d, 8, E, k, dt)) return MOE_ERR_INVALID_ARG;
+  return moe_dispatch_ex(x, topk_idx, topk_gate, T, d, E, k, dt, 0, counts, offsets, perm_token, row_of, row_gate,
+                         x_perm, workspace, ws_bytes, stream);
+}
+
+int moe_capacity(int T, int k, int E, double cf) {
+  if (T < 0 || k < 1 || E < 1 || !(cf > 0.0)) return -1;
+  const double c = std::ceil((double)T * k / E * cf);
+  return c > 2147483647.0 ? -1 : (int)c;
+}
+
+moe_status moe_dispatch_ex(const void* x, const int32_t* topk_idx, const float* topk_gate, int T, int d, int E,
+                           int k, moe_dtype dt, int capacity, int32_t* counts, int32_t* offsets,
+                           int32_t* perm_token, int32_t* row_of, float* row_gate, void* x_perm, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  if (!sizes_ok(T, d, 8, E, k, dt) || capacity < 0) return MOE_ERR_INVALID_ARG;
   if (counts == nullptr || offsets == nullptr || workspace == nullptr) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (x == nullptr || topk_idx == nullptr || topk_gate == nullptr || perm_token == nullptr ||
                 row_of == nullptr || row_gate == nullptr || x_perm == nullptr))
@@ -169,9 +207,9 @@ moe_status moe_dispatch(const void* x, const int32_t* topk_idx, const float* top
   if (!aligned16(x) || !aligned16(x_perm) || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
   const Layout L(T, d, 8, E, k, dt);
   if (ws_bytes < L.dispatch_end) return MOE_ERR_INVALID_ARG;
-  // header words: [0] status, [1] detail, [2] the count kernel's ticket counter
-  return cuda_status(launch_dispatch_fast(x, topk_idx, topk_gate, T, d, E, k, dt, counts, offsets, perm_token,
-                                          row_of, row_gate, x_perm, at<int32_t>(workspace, L.blk_counts),
+  // header words: [0] status, [1] detail, [2] the count kernel's ticket, [3] the router statistics ticket
+  return cuda_status(launch_dispatch_fast(x, topk_idx, topk_gate, T, d, E, k, dt, capacity, counts, offsets,
+                                          perm_token, row_of, row_gate, x_perm, at<int32_t>(workspace, L.blk_counts),
                                           at<int32_t>(workspace, L.blk_base), at<int>(workspace, L.header),
                                           at<int>(workspace, L.header) + 2, (cudaStream_t)stream));
 }
@@ -247,9 +285,10 @@ moe_status moe_combine(const void* y_perm, const int32_t* row_of, int T, int d, 
 
 moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2,
                           int T, int d, int F, int E, int k, moe_dtype dt, moe_dtype out_dt, moe_path path,
-                          void* out, int32_t* topk_idx, float* topk_gate, int32_t* counts, void* workspace,
-                          size_t ws_bytes, void* stream) {
-  if (!sizes_ok(T, d, F, E, k, dt) || !path_ok(path, dt)) return MOE_ERR_INVALID_ARG;
+                          int flags, int capacity, void* out, int32_t* topk_idx, float* topk_gate,
+                          int32_t* counts, float* router_stats, void* workspace, size_t ws_bytes, void* stream) {
+  if (!sizes_ok(T, d, F, E, k, dt) || !path_ok(path, dt) || capacity < 0) return MOE_ERR_INVALID_ARG;
+  if ((flags & ~MOE_GATES_RENORMALISE) != 0) return MOE_ERR_INVALID_ARG;
   if (out_dt != MOE_DTYPE_F32 && out_dt != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   if (workspace == nullptr || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
   const Layout L(T, d, F, E, k, dt);
@@ -268,10 +307,13 @@ moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, cons
   void* xp = at<void>(workspace, L.x_perm);
   void* h = at<void>(workspace, L.h);
   void* yp = at<void>(workspace, L.y_perm);
-  moe_status st = cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, idx, gate, at<int>(workspace, 0),
-                                                 wait_timeout_ns(), (cudaStream_t)stream));
+  const RouterStats rs{router_stats != nullptr ? at<float>(workspace, L.stats_part) : nullptr, router_stats,
+                       at<int>(workspace, 0) + 3};
+  moe_status st = cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, flags, rs, idx, gate,
+                                                 at<int>(workspace, 0), wait_timeout_ns(), (cudaStream_t)stream));
   if (st != MOE_OK) return st;
-  st = moe_dispatch(x, idx, gate, T, d, E, k, dt, cnt, offs, perm, rowof, rgate, xp, workspace, ws_bytes, stream);
+  st = moe_dispatch_ex(x, idx, gate, T, d, E, k, dt, capacity, cnt, offs, perm, rowof, rgate, xp, workspace,
+                       ws_bytes, stream);
   if (st != MOE_OK) return st;
   st = moe_expert_up_ex(xp, w1, offs, T, d, F, E, k, dt, path, h, workspace, ws_bytes, stream);
   if (st != MOE_OK) return st;
@@ -282,8 +324,8 @@ moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, cons
 moe_status moe_forward(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2, int T,
                        int d, int F, int E, int k, moe_dtype dt, void* out, int32_t* topk_idx, float* topk_gate,
                        int32_t* counts, void* workspace, size_t ws_bytes, void* stream) {
-  return moe_forward_ex(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, dt, MOE_PATH_AUTO, out, topk_idx, topk_gate,
-                        counts, workspace, ws_bytes, stream);
+  return moe_forward_ex(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, dt, MOE_PATH_AUTO, 0, 0, out, topk_idx, topk_gate,
+                        counts, nullptr, workspace, ws_bytes, stream);
 }
 
 moe_status moe_selftest_wait_timeout(void* workspace, size_t ws_bytes, int timeout_us, void* stream) {

@@ -81,8 +81,9 @@ dispatch_scan_kernel(const int32_t* __restrict__ blk_counts, int nb, int E, int3
 
 __global__ void __launch_bounds__(kChunk)
 dispatch_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int A, int k, int E,
-                        const int32_t* __restrict__ blk_base, int32_t* __restrict__ row_of,
-                        int32_t* __restrict__ perm_token, float* __restrict__ row_gate) {
+                        const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets, int cap,
+                        int32_t* __restrict__ row_of, int32_t* __restrict__ perm_token,
+                        float* __restrict__ row_gate) {
   griddep_launch_dependents();
   griddep_wait();
   extern __shared__ int wcnt[];  // [kWarpsPerChunk][E]
@@ -104,9 +105,13 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict
       int pre = 0;
       for (int w = 0; w < warp; ++w) pre += wcnt[w * E + e];
       const int row = blk_base[(size_t)blockIdx.x * E + e] + pre + rank;
-      row_of[a] = row;
-      perm_token[row] = a / k;
-      row_gate[row] = gate[a];
+      if (cap > 0 && row - offsets[e] >= cap) {
+        row_of[a] = -1;  // past the expert's capacity: dropped
+      } else {
+        row_of[a] = row;
+        perm_token[row] = a / k;
+        row_gate[row] = gate[a];
+      }
     } else {
       row_of[a] = -1;
     }
@@ -140,9 +145,9 @@ dispatch_gather_kernel(const int4* __restrict__ x, const int32_t* __restrict__ p
 // are summed in parallel; every sum runs in a fixed order, so results do not depend on timing.
 // `done` is zero before the call and is reset to zero by the last CTA.
 __global__ void __launch_bounds__(kChunk)
-dispatch_count_scan_kernel(const int32_t* __restrict__ idx, int A, int E, int nb, int32_t* __restrict__ blk_counts,
-                           int32_t* __restrict__ blk_base, int32_t* __restrict__ counts,
-                           int32_t* __restrict__ offsets, int* status, int* done) {
+dispatch_count_scan_kernel(const int32_t* __restrict__ idx, int A, int E, int nb, int cap,
+                           int32_t* __restrict__ blk_counts, int32_t* __restrict__ blk_base,
+                           int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int* status, int* done) {
   griddep_launch_dependents();
   griddep_wait();
   extern __shared__ int sm[];
@@ -199,7 +204,7 @@ dispatch_count_scan_kernel(const int32_t* __restrict__ idx, int A, int E, int nb
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int e = 4 * tid + j;
-    loc[j] = e < E ? tot[e] : 0;
+    loc[j] = e < E ? (cap > 0 ? min(tot[e], cap) : tot[e]) : 0;  // rows kept per expert
     local += loc[j];
   }
   int incl = local;
@@ -257,13 +262,14 @@ cudaError_t launch_dispatch(const void* x, const int32_t* idx, const float* gate
   cudaError_t err = cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)sc_smem);
   if (err != cudaSuccess) return err;
-  dispatch_scatter_kernel<<<nb, kChunk, sc_smem, s>>>(idx, gate, A, k, E, blk_base, row_of, perm_token, row_gate);
+  dispatch_scatter_kernel<<<nb, kChunk, sc_smem, s>>>(idx, gate, A, k, E, blk_base, offsets, 0, row_of, perm_token,
+                                                      row_gate);
   const size_t elem = dt == MOE_DTYPE_BF16 ? 2 : 4;
   const int vec_per_row = (int)((size_t)d * elem / 16);
   const int warps_needed = A;
   int blocks = (warps_needed + 7) / 8;
-  const int cap = device_sm_count() * 8;
-  if (blocks > cap) blocks = cap;
+  const int max_blocks = device_sm_count() * 8;
+  if (blocks > max_blocks) blocks = max_blocks;
   dispatch_gather_kernel<<<blocks, 256, 0, s>>>((const int4*)x, perm_token, offsets, E, vec_per_row,
                                                 (int4*)x_perm);
   return cudaGetLastError();
@@ -276,29 +282,29 @@ namespace moe {
 
 // Three launches with programmatic dependent launch: count + scan, scatter, gather.
 cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
-                                 int dt, int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* row_of,
-                                 float* row_gate, void* x_perm, int32_t* blk_counts, int32_t* blk_base, int* status,
-                                 int* done, cudaStream_t s) {
+                                 int dt, int cap, int32_t* counts, int32_t* offsets, int32_t* perm_token,
+                                 int32_t* row_of, float* row_gate, void* x_perm, int32_t* blk_counts,
+                                 int32_t* blk_base, int* status, int* done, cudaStream_t s) {
   const int A = T * k;
   if (A == 0)
     return launch_dispatch(x, idx, gate, T, d, E, k, dt, counts, offsets, perm_token, row_of, row_gate, x_perm,
                            blk_counts, blk_base, status, s);
   const int nb = (A + kChunk - 1) / kChunk;
   const size_t cs_smem = (size_t)(3 * E + 1 + kChunk) * sizeof(int);
-  cudaError_t err = launch_pdl(dispatch_count_scan_kernel, dim3(nb), dim3(kChunk), cs_smem, s, idx, A, E, nb,
+  cudaError_t err = launch_pdl(dispatch_count_scan_kernel, dim3(nb), dim3(kChunk), cs_smem, s, idx, A, E, nb, cap,
                                blk_counts, blk_base, counts, offsets, status, done);
   if (err != cudaSuccess) return err;
   const size_t sc_smem = (size_t)kWarpsPerChunk * E * sizeof(int);
   err = cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc_smem);
   if (err != cudaSuccess) return err;
   err = launch_pdl(dispatch_scatter_kernel, dim3(nb), dim3(kChunk), sc_smem, s, idx, gate, A, k, E,
-                   (const int32_t*)blk_base, row_of, perm_token, row_gate);
+                   (const int32_t*)blk_base, (const int32_t*)offsets, cap, row_of, perm_token, row_gate);
   if (err != cudaSuccess) return err;
   const size_t elem = dt == MOE_DTYPE_BF16 ? 2 : 4;
   const int vec_per_row = (int)((size_t)d * elem / 16);
   int blocks = (A + 7) / 8;
-  const int cap = device_sm_count() * 8;
-  if (blocks > cap) blocks = cap;
+  const int max_blocks = device_sm_count() * 8;
+  if (blocks > max_blocks) blocks = max_blocks;
   return launch_pdl(dispatch_gather_kernel, dim3(blocks), dim3(256), 0, s, (const int4*)x, (const int32_t*)perm_token,
                     (const int32_t*)offsets, E, vec_per_row, (int4*)x_perm);
 }

@@ -27,9 +27,19 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 constexpr int kDispatchChunk = 256;
 
 // status (nullable) receives a device-side wait timeout of the tensor-core router.
+// Routing statistics written by the router launch (part == nullptr: none). part: one row of
+// 2E + 1 words per CTA of the launch (at most ceil(T / 8) CTAs); out: 2E + 2 floats; ticket: a
+// word that is zero before the launch and that the last CTA resets to zero.
+struct RouterStats {
+  float* part;
+  float* out;
+  int* ticket;
+};
+constexpr int kRouterStatsTokensPerCta = 8;  // fewest tokens any router CTA owns
+
 cudaError_t launch_router_topk(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
-                               int dt, int32_t* idx, float* gate, int* status, uint64_t timeout_ns,
-                               cudaStream_t s);
+                               int dt, int flags, const RouterStats& st, int32_t* idx, float* gate, int* status,
+                               uint64_t timeout_ns, cudaStream_t s);
 
 // blk_counts / blk_base: [ceil(A / kDispatchChunk), E] int32 scratch each.
 cudaError_t launch_dispatch(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
@@ -39,10 +49,11 @@ cudaError_t launch_dispatch(const void* x, const int32_t* idx, const float* gate
 
 // Same results as launch_dispatch in three launches (count + scan, scatter, gather). `done` is an int
 // that is zero before the call and zero again after it (the workspace header).
+// cap > 0: each expert keeps its first cap assignments in (t, j) order, the rest get row -1.
 cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
-                                 int dt, int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* row_of,
-                                 float* row_gate, void* x_perm, int32_t* blk_counts, int32_t* blk_base, int* status,
-                                 int* done, cudaStream_t s);
+                                 int dt, int cap, int32_t* counts, int32_t* offsets, int32_t* perm_token,
+                                 int32_t* row_of, float* row_gate, void* x_perm, int32_t* blk_counts,
+                                 int32_t* blk_base, int* status, int* done, cudaStream_t s);
 
 cudaError_t launch_combine(const void* y_perm, const int32_t* row_of, int T, int d, int k, int dt, void* out,
                            cudaStream_t s);
@@ -70,7 +81,8 @@ cudaError_t launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t 
 
 // Router on the tensor cores (bf16, E <= 256, E % 8 == 0). Returns cudaErrorNotSupported otherwise.
 cudaError_t launch_router_tc(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
-                             int32_t* idx, float* gate, int* status, uint64_t timeout_ns, cudaStream_t s);
+                             int renorm, const RouterStats& st, int32_t* idx, float* gate, int* status,
+                             uint64_t timeout_ns, cudaStream_t s);
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link-time driver dependency).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

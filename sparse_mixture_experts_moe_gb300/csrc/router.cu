@@ -12,6 +12,7 @@
 // reproducible run to run.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "router_stats.cuh"
 
 namespace moe {
 namespace {
@@ -23,7 +24,8 @@ constexpr int kEC = 128;     // experts per chunk (4 per lane)
 template <typename T, int TPW>
 __global__ void __launch_bounds__(kWarps * 32)
 router_topk_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const float* __restrict__ b_r, int Tn,
-                   int d, int E, int k, int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate) {
+                   int d, int E, int k, int renorm, RouterStats st, int32_t* __restrict__ topk_idx,
+                   float* __restrict__ topk_gate) {
   constexpr int TB = kWarps * TPW;
   griddep_launch_dependents();
   griddep_wait();
@@ -31,8 +33,14 @@ router_topk_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const flo
   float* sW = smem;                    // [kDK][kEC]
   float* sX = sW + kDK * kEC;          // [TB][kDK]
   float* sL = sX + TB * kDK;           // [TB][E]
+  float* sSoft = sL + TB * E;          // statistics only: [kWarps][E] soft-load sums, per warp
+  float* sEnt = sSoft + kWarps * E;    // [kWarps] entropy sums
+  int* sCnt = reinterpret_cast<int*>(sEnt + kWarps);  // [E] assignment counts
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tok0 = blockIdx.x * TB;
+  const bool stats = st.part != nullptr;
+  if (stats)
+    for (int i = tid; i < kWarps * E + kWarps + E; i += kWarps * 32) sSoft[i] = 0.f;  // zero bits: also int 0
 
   for (int ec = 0; ec < E; ec += kEC) {
     float acc[TPW][4];
@@ -84,6 +92,7 @@ router_topk_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const flo
   __syncwarp();
 
   // Softmax and top-k: each warp finishes its own tokens (it wrote all their logits).
+  float went = 0.f;
   for (int t = 0; t < TPW; ++t) {
     const int tok = tok0 + warp * TPW + t;
     if (tok >= Tn) break;
@@ -100,7 +109,19 @@ router_topk_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const flo
     for (int e = lane; e < E; e += 32) s += expf(row[e] - m);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (stats) {
+      // p = exp(z) / s with z = l - max; entropy = ln s - sum p z. Lane l owns columns l mod 32.
+      float hs = 0.f;
+      for (int e = lane; e < E; e += 32) {
+        const float z = row[e] - m;
+        const float p = expf(z) / s;
+        sSoft[warp * E + e] += p;
+        hs += p * z;
+      }
+      went += logf(s) - warp_sum_xor(hs);
+    }
     __syncwarp();
+    float sel[8];
     for (int j = 0; j < k; ++j) {
       float bv = -INFINITY;
       int be = 0x7fffffff;
@@ -114,46 +135,60 @@ router_topk_kernel(const T* __restrict__ x, const T* __restrict__ w_r, const flo
         const int oe = __shfl_xor_sync(0xffffffffu, be, o);
         if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
       }
+      sel[j] = bv;
       if (lane == 0) {
         topk_idx[(size_t)tok * k + j] = be;
-        topk_gate[(size_t)tok * k + j] = expf(bv - m) / s;
+        if (stats) atomicAdd(&sCnt[be], 1);
       }
       if ((be & 31) == lane) row[be] = -INFINITY;
       __syncwarp();
     }
+    // gates: softmax probabilities, or (renorm) the softmax over the k chosen logits
+    float ks = 0.f;
+    if (renorm)
+      for (int j = 0; j < k; ++j) ks += expf(sel[j] - m);
+    if (lane == 0)
+      for (int j = 0; j < k; ++j) topk_gate[(size_t)tok * k + j] = expf(sel[j] - m) / (renorm ? ks : s);
+  }
+  if (stats) {
+    if (lane == 0) sEnt[warp] = went;
+    router_stats_cta(st, sSoft, kWarps, E, sEnt, sCnt, E, Tn, k);
   }
 }
 
 template <typename T, int TPW>
 cudaError_t launch_router_t(const void* x, const void* w_r, const float* b_r, int Tn, int d, int E, int k,
-                            int32_t* idx, float* gate, cudaStream_t s) {
+                            int renorm, const RouterStats& st, int32_t* idx, float* gate, cudaStream_t s) {
   constexpr int TB = kWarps * TPW;
-  const size_t smem = (size_t)(kDK * kEC + TB * kDK + TB * E) * sizeof(float);
+  static_assert(TB >= kRouterStatsTokensPerCta, "statistics rows are sized for 8 tokens per CTA");
+  const size_t stat_words = st.part != nullptr ? (size_t)(kWarps * E + kWarps + E) : 0;
+  const size_t smem = (size_t)(kDK * kEC + TB * kDK + TB * E + stat_words) * sizeof(float);
   auto kern = router_topk_kernel<T, TPW>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int grid = (Tn + TB - 1) / TB;
-  return launch_pdl(kern, dim3(grid), dim3(kWarps * 32), smem, s, (const T*)x, (const T*)w_r, b_r, Tn, d, E, k, idx,
-                    gate);
+  return launch_pdl(kern, dim3(grid), dim3(kWarps * 32), smem, s, (const T*)x, (const T*)w_r, b_r, Tn, d, E, k,
+                    renorm, st, idx, gate);
 }
 
 }  // namespace
 
 cudaError_t launch_router_topk(const void* x, const void* w_r, const float* b_r, int Tn, int d, int E, int k,
-                               int dt, int32_t* idx, float* gate, int* status, uint64_t timeout_ns,
-                               cudaStream_t s) {
+                               int dt, int flags, const RouterStats& st, int32_t* idx, float* gate, int* status,
+                               uint64_t timeout_ns, cudaStream_t s) {
+  const int renorm = (flags & MOE_GATES_RENORMALISE) != 0;
   if (Tn == 0) return cudaSuccess;
   // bf16 with E <= 256 (E % 8 == 0 for TMA row strides): tensor cores; otherwise this CUDA-core kernel.
   if (dt == MOE_DTYPE_BF16 && E <= 256 && E % 8 == 0) {
-    const cudaError_t e = launch_router_tc(x, w_r, b_r, Tn, d, E, k, idx, gate, status, timeout_ns, s);
+    const cudaError_t e = launch_router_tc(x, w_r, b_r, Tn, d, E, k, renorm, st, idx, gate, status, timeout_ns, s);
     if (e != cudaErrorNotSupported) return e;
   }
   const bool small_e = E <= 256;
   if (dt == MOE_DTYPE_BF16)
-    return small_e ? launch_router_t<__nv_bfloat16, 8>(x, w_r, b_r, Tn, d, E, k, idx, gate, s)
-                   : launch_router_t<__nv_bfloat16, 2>(x, w_r, b_r, Tn, d, E, k, idx, gate, s);
-  return small_e ? launch_router_t<float, 8>(x, w_r, b_r, Tn, d, E, k, idx, gate, s)
-                 : launch_router_t<float, 2>(x, w_r, b_r, Tn, d, E, k, idx, gate, s);
+    return small_e ? launch_router_t<__nv_bfloat16, 8>(x, w_r, b_r, Tn, d, E, k, renorm, st, idx, gate, s)
+                   : launch_router_t<__nv_bfloat16, 2>(x, w_r, b_r, Tn, d, E, k, renorm, st, idx, gate, s);
+  return small_e ? launch_router_t<float, 8>(x, w_r, b_r, Tn, d, E, k, renorm, st, idx, gate, s)
+                 : launch_router_t<float, 2>(x, w_r, b_r, Tn, d, E, k, renorm, st, idx, gate, s);
 }
 
 }  // namespace moe

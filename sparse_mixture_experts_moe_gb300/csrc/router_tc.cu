@@ -19,6 +19,7 @@
 
 #include "common.cuh"
 #include "kernels.cuh"
+#include "router_stats.cuh"
 
 namespace moe {
 namespace {
@@ -32,6 +33,12 @@ constexpr int kNumBars = 2 * STAGES + 2;
 template <int EN>
 constexpr size_t router_smem_bytes() {
   return 1024 + (size_t)STAGES * (kTileXBytes + EN / 64 * kTileWSubBytes) + 8 * kNumBars + 16;
+}
+
+// Routing statistics: [4][EN] per-warp soft-load sums, [4] entropy sums, [EN] counts.
+template <int EN>
+constexpr size_t router_stat_bytes() {
+  return (size_t)(5 * EN + 4) * sizeof(float);
 }
 
 // Insert (v, e) into the descending list bv/bi of length k (k <= KMAX). A value equal to an
@@ -52,8 +59,8 @@ __device__ __forceinline__ void topk_insert(float (&bv)[KMAX], int (&bi)[KMAX], 
 template <int EN, int KMAX>
 __global__ void __launch_bounds__(kThreads, 1)
 router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                 const float* __restrict__ b_r, int Tn, int d, int E, int k, int32_t* __restrict__ topk_idx,
-                 float* __restrict__ topk_gate, int* status, uint64_t timeout_ns) {
+                 const float* __restrict__ b_r, int Tn, int d, int E, int k, int renorm, RouterStats st,
+                 int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate, int* status, uint64_t timeout_ns) {
   constexpr int kTileWBytes = EN / 64 * kTileWSubBytes;
   constexpr int kStageBytes = kTileXBytes + kTileWBytes;
   constexpr uint32_t kCols = EN;  // 64, 128 or 256: a power of two >= 32
@@ -66,11 +73,17 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* s_soft = reinterpret_cast<float*>(gbase + STAGES * kStageBytes + 8 * kNumBars + 16);  // [4][EN]
+  float* s_ent = s_soft + 4 * EN;                                                             // [4]
+  int* s_cnt = reinterpret_cast<int*>(s_ent + 4);                                             // [EN]
+  const bool stats = st.part != nullptr;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, DONE = 2 * STAGES + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * BM;
   const int KB = (d + BK - 1) / BK;
+  if (stats)
+    for (int i = threadIdx.x; i < 5 * EN + 4; i += kThreads) s_soft[i] = 0.f;  // zero bits: also int 0
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(bar(FULL + s), 1); mbar_init(bar(EMPTY + s), 1); }
@@ -135,7 +148,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   } else {
     const int q = warp & 3;
     const int tok = t0 + 32 * q + lane;
-    const bool ok = wait_or_abort(bar(TFULL), 0, timeout_ns, abort_flag, status, 13);
+    // warp-uniform: the TMEM loads and shuffles below are warp-collective
+    const bool ok = __all_sync(0xffffffffu, wait_or_abort(bar(TFULL), 0, timeout_ns, abort_flag, status, 13));
     if (ok) {
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16);
@@ -156,10 +170,17 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         }
       }
       const float m = bv[0];
-      // pass 2: sum of exp(l - max), ascending expert order
-      float ssum = 0.f;
+      // pass 2: sum of exp(l - max) in ascending expert order (the softmax denominator; skipped
+      // for renormalised gates unless the statistics want it), and for renormalised gates the
+      // sum over the k chosen logits in slot order
+      float ssum = 0.f, ksum = 0.f;
+      if (renorm) {
+#pragma unroll
+        for (int p = 0; p < KMAX; ++p)
+          if (p < k) ksum += expf(bv[p] - m);
+      }
 #pragma unroll 1
-      for (int c = 0; c < EN; c += 32) {
+      for (int c = 0; c < (renorm && !stats ? 0 : EN); c += 32) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + (uint32_t)c, v);
         tmem_ld_wait();
@@ -169,14 +190,39 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
           if (e < E) ssum += expf(__uint_as_float(v[j]) + (b_r != nullptr ? b_r[e] : 0.f) - m);
         }
       }
+      const float gden = renorm ? ksum : ssum;
       if (tok < Tn) {
 #pragma unroll
         for (int p = 0; p < KMAX; ++p) {
           if (p < k) {
             topk_idx[(size_t)tok * k + p] = bi[p];
-            topk_gate[(size_t)tok * k + p] = expf(bv[p] - m) / ssum;
+            topk_gate[(size_t)tok * k + p] = expf(bv[p] - m) / gden;
+            if (stats) atomicAdd(&s_cnt[bi[p]], 1);
           }
         }
+      }
+      if (stats) {
+        // pass 3: p = exp(z) / ssum with z = l - max; per-warp column sums of p over the warp's
+        // 32 tokens, and the token entropy ln ssum - sum p z
+        float hs = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < EN; c += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + (uint32_t)c, v);
+          tmem_ld_wait();
+          float pv[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int e = c + j;
+            const float z = __uint_as_float(v[j]) + (b_r != nullptr && e < E ? b_r[e] : 0.f) - m;
+            const float p = (tok < Tn && e < E) ? expf(z) / ssum : 0.f;
+            pv[j] = p;
+            hs += p * z;
+          }
+          s_soft[q * EN + c + lane] = warp_column_sums(pv);
+        }
+        const float ent = warp_sum_xor(tok < Tn ? logf(ssum) - hs : 0.f);
+        if (lane == 0) s_ent[q] = ent;
       }
     }
   }
@@ -187,6 +233,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     tc_fence_after();
     tmem_dealloc(tmem_base, kCols);
   }
+  if (stats) router_stats_cta(st, s_soft, 4, EN, s_ent, s_cnt, E, Tn, k);
 }
 
 // Split-K version: one cluster of kSplit CTAs per 128-token tile, CTA r accumulating the
@@ -204,14 +251,15 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
 
 template <int EN>
 constexpr size_t router_split_smem_bytes() {
-  return router_smem_bytes<EN>() + (size_t)BM * (EN + 1) * sizeof(float);
+  return router_smem_bytes<EN>() + (size_t)BM * (EN + 1) * sizeof(float) + router_stat_bytes<EN>();
 }
 
 template <int EN, int KMAX>
 __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1)
 router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                       const float* __restrict__ b_r, int Tn, int d, int E, int k, int32_t* __restrict__ topk_idx,
-                       float* __restrict__ topk_gate, int* status, uint64_t timeout_ns) {
+                       const float* __restrict__ b_r, int Tn, int d, int E, int k, int renorm,
+                       RouterStats st, int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate,
+                       int* status, uint64_t timeout_ns) {
   constexpr int kTileWBytes = EN / 64 * kTileWSubBytes;
   constexpr int kStageBytes = kTileXBytes + kTileWBytes;
   constexpr uint32_t kCols = EN;
@@ -226,6 +274,12 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(gbase + STAGES * kStageBytes + 8 * kNumBars + 16);  // [BM][RS]
+  float* s_soft = red + BM * RS;                   // statistics: [4][EN] per-warp soft-load sums
+  float* s_ent = s_soft + 4 * EN;                  // [4]
+  int* s_cnt = reinterpret_cast<int*>(s_ent + 4);  // [EN]
+  const bool stats = st.part != nullptr;
+  if (stats)
+    for (int i = threadIdx.x; i < 5 * EN + 4; i += kThreads) s_soft[i] = 0.f;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, DONE = 2 * STAGES + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -298,7 +352,7 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
     // partial logits of this CTA's k-range -> shared memory (row = token)
     const int q = warp & 3;
     const int row = 32 * q + lane;
-    const bool ok = wait_or_abort(bar(TFULL), 0, timeout_ns, abort_flag, status, 16);
+    const bool ok = __all_sync(0xffffffffu, wait_or_abort(bar(TFULL), 0, timeout_ns, abort_flag, status, 16));
     if (ok) {
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16);
@@ -320,6 +374,10 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
   if (warp >= 2) {
     constexpr int kRowsPerCta = BM / kSplit;  // 16
     constexpr int kEpi = 4;
+    float accp[EN / 32];  // statistics: this lane's soft-load sums (experts lane + 32 j)
+#pragma unroll
+    for (int j = 0; j < EN / 32; ++j) accp[j] = 0.f;
+    float went = 0.f;
     for (int i = warp - 2; i < kRowsPerCta; i += kEpi) {
       const int row = (int)rank * kRowsPerCta + i;
       const int tok = t0 + row;
@@ -345,6 +403,20 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
         if (lane + 32 * j < E) ssum += expf(lv[j] - m);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+      if (stats) {
+        float hs = 0.f;
+#pragma unroll
+        for (int j = 0; j < EN / 32; ++j) {
+          if (lane + 32 * j < E) {
+            const float z = lv[j] - m;
+            const float p = expf(z) / ssum;
+            accp[j] += p;
+            hs += p * z;
+          }
+        }
+        went += logf(ssum) - warp_sum_xor(hs);
+      }
+      float sel[8];
       for (int p = 0; p < k; ++p) {
         float bv = -INFINITY;
         int be = 0x7fffffff;
@@ -357,14 +429,25 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
           const int oe = __shfl_xor_sync(0xffffffffu, be, o);
           if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
         }
+        sel[p] = bv;
         if (lane == 0) {
           topk_idx[(size_t)tok * k + p] = be;
-          topk_gate[(size_t)tok * k + p] = expf(bv - m) / ssum;
+          if (stats) atomicAdd(&s_cnt[be], 1);
         }
 #pragma unroll
         for (int j = 0; j < EN / 32; ++j)
           if (lane + 32 * j == be) lv[j] = -INFINITY;
       }
+      float ksum = 0.f;
+      if (renorm)
+        for (int p = 0; p < k; ++p) ksum += expf(sel[p] - m);
+      if (lane == 0)
+        for (int p = 0; p < k; ++p) topk_gate[(size_t)tok * k + p] = expf(sel[p] - m) / (renorm ? ksum : ssum);
+    }
+    if (stats) {
+#pragma unroll
+      for (int j = 0; j < EN / 32; ++j) s_soft[(warp - 2) * EN + lane + 32 * j] = accp[j];
+      if (lane == 0) s_ent[warp - 2] = went;
     }
   }
   cluster_sync_all();  // no CTA leaves while a peer may still read its partials
@@ -372,11 +455,13 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
     tc_fence_after();
     tmem_dealloc(tmem_base, kCols);
   }
+  if (stats) router_stats_cta(st, s_soft, 4, EN, s_ent, s_cnt, E, Tn, k);
 }
 
 template <int EN, int KMAX>
 cudaError_t launch_en(const CUtensorMap& tmX, const CUtensorMap& tmW, const float* b_r, int Tn, int d, int E,
-                      int k, int32_t* idx, float* gate, int* status, uint64_t timeout_ns, cudaStream_t s) {
+                      int k, int renorm, const RouterStats& st, int32_t* idx, float* gate, int* status,
+                      uint64_t timeout_ns, cudaStream_t s) {
   if (EN <= 128 && Tn <= BM && (d + BK - 1) / BK >= 2 * kSplit) {
     // one token tile and deep d: a single CTA would stream all of W_r alone, so a cluster of
     // kSplit CTAs splits d (measured: 51 -> 14 us at T = 1, d = 8192). With more tiles the
@@ -387,28 +472,30 @@ cudaError_t launch_en(const CUtensorMap& tmX, const CUtensorMap& tmW, const floa
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3(kSplit * ((Tn + BM - 1) / BM)), dim3(kThreads), smem, s, tmX, tmW, b_r, Tn, d, E,
-                      k, idx, gate, status, timeout_ns);
+                      k, renorm, st, idx, gate, status, timeout_ns);
   }
-  const size_t smem = router_smem_bytes<EN>();
+  const size_t smem = router_smem_bytes<EN>() + router_stat_bytes<EN>();
   auto kern = router_tc_kernel<EN, KMAX>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(kern, dim3((Tn + BM - 1) / BM), dim3(kThreads), smem, s, tmX, tmW, b_r, Tn, d, E, k, idx, gate,
-                    status, timeout_ns);
+  return launch_pdl(kern, dim3((Tn + BM - 1) / BM), dim3(kThreads), smem, s, tmX, tmW, b_r, Tn, d, E, k, renorm, st,
+                    idx, gate, status, timeout_ns);
 }
 
 template <int KMAX>
 cudaError_t launch_k(const CUtensorMap& tmX, const CUtensorMap& tmW, const float* b_r, int Tn, int d, int E, int k,
-                     int32_t* idx, float* gate, int* status, uint64_t timeout_ns, cudaStream_t s) {
-  if (E <= 64) return launch_en<64, KMAX>(tmX, tmW, b_r, Tn, d, E, k, idx, gate, status, timeout_ns, s);
-  if (E <= 128) return launch_en<128, KMAX>(tmX, tmW, b_r, Tn, d, E, k, idx, gate, status, timeout_ns, s);
-  return launch_en<256, KMAX>(tmX, tmW, b_r, Tn, d, E, k, idx, gate, status, timeout_ns, s);
+                     int renorm, const RouterStats& st, int32_t* idx, float* gate, int* status, uint64_t timeout_ns,
+                     cudaStream_t s) {
+  if (E <= 64) return launch_en<64, KMAX>(tmX, tmW, b_r, Tn, d, E, k, renorm, st, idx, gate, status, timeout_ns, s);
+  if (E <= 128) return launch_en<128, KMAX>(tmX, tmW, b_r, Tn, d, E, k, renorm, st, idx, gate, status, timeout_ns, s);
+  return launch_en<256, KMAX>(tmX, tmW, b_r, Tn, d, E, k, renorm, st, idx, gate, status, timeout_ns, s);
 }
 
 }  // namespace
 
 cudaError_t launch_router_tc(const void* x, const void* w_r, const float* b_r, int Tn, int d, int E, int k,
-                             int32_t* idx, float* gate, int* status, uint64_t timeout_ns, cudaStream_t s) {
+                             int renorm, const RouterStats& st, int32_t* idx, float* gate, int* status,
+                             uint64_t timeout_ns, cudaStream_t s) {
   if (Tn == 0) return cudaSuccess;
   if (E > 256 || E % 8 != 0) return cudaErrorNotSupported;
   EncodeTiledFn enc = tensor_map_encoder();
@@ -427,8 +514,8 @@ cudaError_t launch_router_tc(const void* x, const void* w_r, const float* b_r, i
     if (!encode_tmap(enc, &tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_r, 2, dims, str, box))
       return cudaErrorInvalidValue;
   }
-  if (k <= 2) return launch_k<2>(tmX, tmW, b_r, Tn, d, E, k, idx, gate, status, timeout_ns, s);
-  return launch_k<8>(tmX, tmW, b_r, Tn, d, E, k, idx, gate, status, timeout_ns, s);
+  if (k <= 2) return launch_k<2>(tmX, tmW, b_r, Tn, d, E, k, renorm, st, idx, gate, status, timeout_ns, s);
+  return launch_k<8>(tmX, tmW, b_r, Tn, d, E, k, renorm, st, idx, gate, status, timeout_ns, s);
 }
 
 }  // namespace moe

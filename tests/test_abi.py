@@ -91,3 +91,12 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_LIB", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         _lib.lib()
+
+
+def test_capacity_helper_matches_oracle():
+    import oracle
+    for T, k, E, cf in [(2048, 2, 128, 2.0), (1000, 2, 16, 1.0), (1000, 2, 16, 1.25), (37, 2, 4, 0.05),
+                        (1, 8, 1024, 1.0), (0, 2, 16, 1.0), (65536, 8, 7, 3.3)]:
+        assert moe.capacity(T, k, E, cf) == oracle.capacity(T, k, E, cf)
+    assert moe.capacity(16, 2, 4, 0.0) == -1
+    assert moe.capacity(16, 0, 4, 1.0) == -1

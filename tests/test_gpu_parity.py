@@ -96,7 +96,7 @@ DISPATCH_CASES = [
 ]
 
 
-def run_dispatch(c, idx, gate):
+def run_dispatch(c, idx, gate, capacity=0):
     A, E = c.A, c.E
     out = dict(counts=torch.empty(E, dtype=torch.int32, device=DEV),
                offsets=torch.empty(E + 1, dtype=torch.int32, device=DEV),
@@ -108,7 +108,7 @@ def run_dispatch(c, idx, gate):
     ti = torch.from_numpy(idx.astype(np.int32)).to(DEV)
     tg = torch.from_numpy(gate.astype(np.float32)).to(DEV)
     moe.dispatch(c.x, ti, tg, c.T, c.d, E, c.k, c.dt, out["counts"], out["offsets"], out["perm_token"],
-                 out["row_of"], out["row_gate"], out["x_perm"], ws)
+                 out["row_of"], out["row_gate"], out["x_perm"], ws, capacity=capacity)
     st, detail = moe.get_device_status(ws)
     return out, st, detail
 
@@ -126,6 +126,45 @@ def test_dispatch(cfg):
     assert np.array_equal(out["row_of"].cpu().numpy(), ref["row_of"])
     assert np.array_equal(out["row_gate"].cpu().numpy(), ref["row_gate"].astype(np.float32))
     assert np.array_equal(to_f64(out["x_perm"]), c.x64[ref["perm_token"]])
+
+
+def _skewed(E, hot=3, boost=2.5):
+    b = np.zeros(E, np.float32)
+    b[:hot] = boost  # a few popular experts, so a capacity factor of 1 drops assignments
+    return b
+
+
+@pytest.mark.parametrize("cfg,cf", [(dict(T=1000, d=64, E=16, k=2, dt=BF16), 1.0),
+                                    (dict(T=1000, d=64, E=16, k=2, dt=BF16), 1.25),
+                                    (dict(T=300, d=40, E=1024, k=8, dt=F32), 1.0),
+                                    (dict(T=513, d=128, E=16, k=2, dt=F32), 100.0),   # nothing dropped
+                                    (dict(T=37, d=8, E=4, k=2, dt=BF16), 0.05)],      # capacity 1
+                         ids=["e16_cf1", "e16_cf1.25", "e1024_cf1", "no_drop", "cap1"])
+def test_dispatch_capacity(cfg, cf):
+    c = make_case(F=64, bias=_skewed(cfg["E"]), **cfg)
+    ridx, rgate = oracle_routing(c)
+    C = oracle.capacity(c.T, c.k, c.E, cf)
+    assert moe.capacity(c.T, c.k, c.E, cf) == C
+    out, st, _ = run_dispatch(c, ridx, rgate, capacity=C)
+    assert st == moe.MOE_OK
+    ref = oracle.dispatch(ridx, c.E, rgate.astype(np.float32), cap=C)
+    if cf <= 1.0:
+        assert ref["offsets"][-1] < c.A  # the case does drop assignments
+    rows = int(ref["offsets"][-1])
+    assert np.array_equal(out["counts"].cpu().numpy(), ref["counts"])
+    assert np.array_equal(out["offsets"].cpu().numpy(), ref["offsets"])
+    assert np.array_equal(out["row_of"].cpu().numpy(), ref["row_of"])
+    assert np.array_equal(out["perm_token"].cpu().numpy()[:rows], ref["perm_token"][:rows])
+    assert np.array_equal(out["row_gate"].cpu().numpy()[:rows], ref["row_gate"][:rows].astype(np.float32))
+    assert np.array_equal(to_f64(out["x_perm"])[:rows], c.x64[ref["perm_token"][:rows]])
+
+
+def test_dispatch_rejects_negative_capacity():
+    c = make_case(T=16, d=64, F=64, E=4, k=2, dt=BF16)
+    ridx, rgate = oracle_routing(c)
+    with pytest.raises(moe.MoeError) as e:
+        run_dispatch(c, ridx, rgate, capacity=-1)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
 
 
 def test_dispatch_flags_out_of_range_index():
@@ -271,14 +310,16 @@ def test_forward(cfg):
         check_bf16_output(c, path, out, ref["out"])
 
 
-def output_tolerance(c, ref):
+def output_tolerance(c, ref, cap=None):
     """The stated bar (1e-4 fp32, 2e-2 bf16), unless the bf16 path's one documented intermediate
-    rounding (h to bf16) already exceeds it on this shape (small d_ff, large k): then 1.1x the error
-    that rounding alone causes, computed with the oracle, plus 2e-3."""
+    rounding (h to bf16) already exceeds it on this shape (small d_ff, large k, or a capacity that
+    leaves most tokens one expert): then 1.1x the error that rounding alone causes, computed with
+    the oracle, plus 2e-3."""
     if c.dt != BF16:
         return TOL[c.dt]
-    dp = oracle.dispatch(ref["idx"], c.E, ref["gate"])
-    h = oracle.expert_rows_up(c.x64[dp["perm_token"]], dp["offsets"], c.w1_host())
+    dp = oracle.dispatch(ref["idx"], c.E, ref["gate"], cap=cap)
+    rows = int(dp["offsets"][-1])
+    h = oracle.expert_rows_up(c.x64[dp["perm_token"][:rows]], dp["offsets"], c.w1_host())
     h_b = ig.as_f64(ig.f32_to_bf16_bits(h.astype(np.float32)), BF16)
     y = oracle.expert_rows_down(h_b, dp["offsets"], dp["row_gate"], c.w2_host())
     rounded = rel_rms_err(oracle.combine(y, dp["row_of"]), ref["out"])
@@ -304,6 +345,145 @@ def test_forward_all_tokens_to_one_expert():
     assert np.all(idx[:, 0] == 3)
     assert np.array_equal(idx, ref["idx"])
     assert rel_rms_err(to_f64(out), ref["out"]) < TOL[BF16]
+
+
+@pytest.mark.parametrize("cfg", [dict(T=300, d=320, F=64, E=16, k=2, dt=BF16), dict(T=64, d=4096, F=64, E=128, k=4, dt=BF16),
+                                 dict(T=70, d=64, F=64, E=5, k=3, dt=F32), dict(T=33, d=64, F=64, E=1024, k=8, dt=BF16)],
+                         ids=["tc", "split", "simt_f32", "simt_e1024"])
+def test_router_renormalised_gates(cfg):
+    c = make_case(**cfg)
+    idx = torch.empty((c.T, c.k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((c.T, c.k), dtype=torch.float32, device=DEV)
+    moe.router_topk(c.x, c.w_r, c.b_r, c.T, c.d, c.E, c.k, c.dt, idx, gate, renormalise=True)
+    logits = oracle.router_logits(c.x64, c.wr64, c.br64)
+    ridx = oracle.topk_select(logits, c.k)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    g = gate.cpu().numpy()
+    assert np.max(np.abs(g - oracle.gates_renormalised(logits, ridx))) < 1e-5
+    assert np.allclose(g.sum(axis=1), 1.0, atol=1e-5)
+
+
+@pytest.mark.parametrize("path", [moe.PATH_AUTO, moe.PATH_STREAM])
+def test_forward_renormalised_gates(path):
+    c = make_case(T=256 if path == moe.PATH_AUTO else 16, d=512, F=512, E=16, k=2, dt=BF16)
+    out = torch.empty((c.T, c.d), dtype=torch.float32, device=DEV)
+    ws = workspace_for(c)
+    moe.forward(c.x, c.w_r, None, c.w1, c.w2, c.T, c.d, c.F, c.E, c.k, c.dt, out, ws, path=path, out_dt=F32,
+                renormalise=True)
+    assert moe.get_device_status(ws)[0] == moe.MOE_OK
+    ref = oracle.forward(c.x64, c.wr64, c.w1_host(), c.w2_host(), c.k, renormalise=True)
+    assert rel_rms_err(to_f64(out), ref["out"]) < TOL[BF16]
+
+
+@pytest.mark.parametrize("cfg", [dict(T=640, d=256, F=512, E=16, k=2, dt=BF16, path=moe.PATH_AUTO, cf=1.0),
+                                 dict(T=640, d=256, F=512, E=16, k=2, dt=BF16, path=moe.PATH_TENSOR_PAIR, cf=1.0),
+                                 dict(T=24, d=512, F=512, E=16, k=2, dt=BF16, path=moe.PATH_STREAM, cf=1.0),
+                                 dict(T=200, d=128, F=256, E=8, k=2, dt=F32, path=moe.PATH_AUTO, cf=1.25),
+                                 dict(T=640, d=256, F=512, E=16, k=2, dt=BF16, path=moe.PATH_SIMT, cf=0.5)],
+                         ids=["tensor", "pair", "stream", "simt_f32", "simt_half"])
+def test_forward_capacity(cfg):
+    cfg = dict(cfg)
+    path, cf = cfg.pop("path"), cfg.pop("cf")
+    c = make_case(bias=_skewed(cfg["E"]), **cfg)
+    C = oracle.capacity(c.T, c.k, c.E, cf)
+    out = torch.empty((c.T, c.d), dtype=torch.float32, device=DEV)
+    counts = torch.empty(c.E, dtype=torch.int32, device=DEV)
+    ws = workspace_for(c)
+    moe.forward(c.x, c.w_r, c.b_r, c.w1, c.w2, c.T, c.d, c.F, c.E, c.k, c.dt, out, ws, counts=counts, path=path,
+                out_dt=F32, capacity=C)
+    st, detail = moe.get_device_status(ws)
+    assert st == moe.MOE_OK, (st, detail)
+    ref = oracle.forward(c.x64, c.wr64, c.w1_host(), c.w2_host(), c.k, c.br64, cap=C)
+    assert not ref["keep"].all()  # some assignments are dropped
+    assert np.array_equal(counts.cpu().numpy(), oracle.dispatch(ref["idx"], c.E, cap=C)["counts"])
+    assert np.all(counts.cpu().numpy() <= C)
+    got = to_f64(out)
+    assert rel_rms_err(got, ref["out"]) < output_tolerance(c, ref, cap=C)
+    # a token with every assignment dropped gets an exact zero
+    gone = ~ref["keep"].any(axis=1)
+    assert np.all(got[gone] == 0.0)
+
+
+STATS_CASES = [
+    dict(T=1000, d=256, E=16, k=2, dt=BF16),      # tensor-core router, 8 CTAs
+    dict(T=64, d=4096, E=128, k=4, dt=BF16),      # split-K cluster router
+    dict(T=300, d=64, E=24, k=3, dt=F32),         # CUDA-core router, 10 CTAs
+    dict(T=100, d=64, E=1024, k=8, dt=BF16),      # CUDA-core router, E = 1024
+    dict(T=1, d=128, E=64, k=2, dt=BF16),         # one token
+]
+
+
+def check_stats(got, logits, idx, T, E, k):
+    ref = oracle.routing_stats(logits, idx)
+    g = got.cpu().numpy().astype(np.float64)
+    assert g.shape == (moe.router_stats_len(E),)
+    assert np.allclose(g[:E], ref["soft_load"], rtol=1e-4, atol=1e-7)
+    assert np.array_equal(got.cpu().numpy()[E:2 * E], ref["hard_load"].astype(np.float32))
+    assert abs(g[2 * E] - ref["balance"]) <= 1e-6 * ref["balance"] + 1e-9
+    assert abs(g[2 * E + 1] - ref["entropy"]) <= 1e-4 * ref["entropy"] + 1e-6
+
+
+@pytest.mark.parametrize("cfg", STATS_CASES, ids=["tc", "split", "simt_f32", "simt_e1024", "one_token"])
+@pytest.mark.parametrize("renormalise", [False, True], ids=["raw", "renorm"])
+def test_router_stats(cfg, renormalise):
+    ws = None
+    for seed, bias in [(0, None), (5, _skewed(cfg["E"]))]:  # the second call also checks the ticket reset
+        c = make_case(F=64, seed=seed, bias=bias, **cfg)
+        if ws is None:
+            ws = workspace_for(c)
+        idx = torch.empty((c.T, c.k), dtype=torch.int32, device=DEV)
+        gate = torch.empty((c.T, c.k), dtype=torch.float32, device=DEV)
+        stats = torch.full((moe.router_stats_len(c.E),), float("nan"), dtype=torch.float32, device=DEV)
+        moe.router_topk_stats(c.x, c.w_r, c.b_r, c.T, c.d, c.E, c.k, c.dt, idx, gate, stats, ws,
+                              renormalise=renormalise)
+        assert moe.get_device_status(ws)[0] == moe.MOE_OK
+        logits = oracle.router_logits(c.x64, c.wr64, c.br64)
+        ridx = oracle.topk_select(logits, c.k)
+        assert np.array_equal(idx.cpu().numpy(), ridx)
+        want = oracle.gates_renormalised(logits, ridx) if renormalise else oracle.gates_of(oracle.softmax(logits), ridx)
+        assert np.max(np.abs(gate.cpu().numpy() - want)) < 1e-5
+        check_stats(stats, logits, ridx, c.T, c.E, c.k)
+        again = torch.empty_like(stats)
+        moe.router_topk_stats(c.x, c.w_r, c.b_r, c.T, c.d, c.E, c.k, c.dt, idx, gate, again, ws,
+                              renormalise=renormalise)
+        assert torch.equal(again.view(torch.int32), stats.view(torch.int32))  # fixed reduction order
+
+
+def test_forward_writes_router_stats():
+    c = make_case(T=640, d=256, F=512, E=16, k=2, dt=BF16, bias=_skewed(16, boost=0.5))
+    out = torch.empty((c.T, c.d), dtype=torch.float32, device=DEV)
+    stats = torch.empty(moe.router_stats_len(c.E), dtype=torch.float32, device=DEV)
+    ws = workspace_for(c)
+    moe.forward(c.x, c.w_r, c.b_r, c.w1, c.w2, c.T, c.d, c.F, c.E, c.k, c.dt, out, ws, out_dt=F32, router_stats=stats)
+    assert moe.get_device_status(ws)[0] == moe.MOE_OK
+    logits = oracle.router_logits(c.x64, c.wr64, c.br64)
+    check_stats(stats, logits, oracle.topk_select(logits, c.k), c.T, c.E, c.k)
+    ref = oracle.forward(c.x64, c.wr64, c.w1_host(), c.w2_host(), c.k, c.br64)
+    assert rel_rms_err(to_f64(out), ref["out"]) < TOL[BF16]
+
+
+def test_router_stats_rejects_small_workspace():
+    c = make_case(T=256, d=64, F=64, E=16, k=2, dt=BF16)
+    idx = torch.empty((c.T, c.k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((c.T, c.k), dtype=torch.float32, device=DEV)
+    stats = torch.empty(moe.router_stats_len(c.E), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(512, dtype=torch.uint8, device=DEV)
+    with pytest.raises(moe.MoeError) as e:
+        moe.router_topk_stats(c.x, c.w_r, None, c.T, c.d, c.E, c.k, c.dt, idx, gate, stats, ws)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+
+
+def test_layer_object_capacity_and_stats():
+    c = make_case(T=512, d=256, F=256, E=16, k=2, dt=BF16, bias=_skewed(16))
+    layer = moe.MoELayer(c.w_r, c.w1, c.w2, k=2, b_r=c.b_r, capacity_factor=1.25)
+    stats = torch.empty(moe.router_stats_len(16), dtype=torch.float32, device=DEV)
+    out = layer(c.x, out_dtype=torch.float32, router_stats=stats)
+    assert layer.device_status()[0] == moe.MOE_OK
+    C = oracle.capacity(512, 2, 16, 1.25)
+    ref = oracle.forward(c.x64, c.wr64, c.w1_host(), c.w2_host(), 2, c.br64, cap=C)
+    assert not ref["keep"].all()
+    assert rel_rms_err(to_f64(out), ref["out"]) < output_tolerance(c, ref, cap=C)
+    check_stats(stats, ref["logits"], ref["idx"], 512, 16, 2)
 
 
 def test_forward_zero_tokens():
