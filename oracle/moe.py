@@ -358,6 +358,55 @@ def routing_stats(logits: np.ndarray, idx: np.ndarray) -> dict:
     return {"soft_load": soft, "hard_load": hard, "balance": balance, "entropy": entropy}
 
 
+QBLOCK = 64
+
+
+def quantize_blocks(w: np.ndarray, bits: int) -> dict:
+    """Block quantisation of one weight matrix w [K, N] (csdn/6a462500 §4.3, 64 x 64 blocks with
+    their own min / max; csdn/6a919c0d §2.3 and §3 for INT4 / INT8 expert weights).
+
+    For each 64 x 64 block: scale = (max - min) / (2^bits - 1) and the code of w is
+    round((w - min) / scale), so the block's min gets code 0 and its max the top code. Reading:
+    the page's dequantisation adds the zero point back on top of codes that already had it
+    removed, which loses the block minimum; here w is restored as min + code * scale. A block
+    whose values are all equal has scale 0 and codes 0. The codes are integers decided by
+    floating point, so they are decided in fp32 (the weights are bf16 or fp32, exact in fp32):
+    fp32 subtraction and division, rounding half to even.
+    """
+    w32 = np.asarray(w, np.float32)
+    K, N = w32.shape
+    if K % QBLOCK or N % QBLOCK:
+        raise ValueError("quantize_blocks: K and N must be multiples of 64")
+    levels = np.float32(2 ** bits - 1)
+    codes = np.zeros((K, N), np.uint8)
+    scale = np.zeros((K // QBLOCK, N // QBLOCK), np.float32)
+    wmin = np.zeros((K // QBLOCK, N // QBLOCK), np.float32)
+    for bi in range(K // QBLOCK):
+        for bj in range(N // QBLOCK):
+            blk = w32[bi * QBLOCK:(bi + 1) * QBLOCK, bj * QBLOCK:(bj + 1) * QBLOCK]
+            lo, hi = blk.min(), blk.max()
+            s = np.float32(np.float32(hi - lo) / levels)
+            scale[bi, bj], wmin[bi, bj] = s, lo
+            if s > 0:
+                q = np.rint((blk - lo) / s)  # float32 operands: fp32 subtraction and division
+                codes[bi * QBLOCK:(bi + 1) * QBLOCK, bj * QBLOCK:(bj + 1) * QBLOCK] = q.astype(np.uint8)
+    return {"codes": codes, "scale": scale, "min": wmin, "bits": bits}
+
+
+def dequantize_blocks(q: Mapping) -> np.ndarray:
+    """w_hat = min + code * scale per 64 x 64 block, in fp64 (the inverse map of quantize_blocks)."""
+    codes = np.asarray(q["codes"], np.float64)
+    s = np.repeat(np.repeat(np.asarray(q["scale"], np.float64), QBLOCK, 0), QBLOCK, 1)
+    m = np.repeat(np.repeat(np.asarray(q["min"], np.float64), QBLOCK, 0), QBLOCK, 1)
+    return m + codes * s
+
+
+def packed_code_bytes(K: int, N: int, bits: int) -> int:
+    """Bytes of the codes of a K x N matrix at `bits` per weight (csdn/6a462500 §4.3 counts a
+    52,428,800-weight fp16 matrix as 104,857,600 bytes and its INT4 codes as 26,214,400)."""
+    return K * N * bits // 8
+
+
 def ambiguous_tokens(logits: np.ndarray, k: int, min_gap: float) -> np.ndarray:
     """Tokens whose top-(k+1) logits (top-k when E == k) have an adjacent gap below min_gap.
 

@@ -337,11 +337,50 @@ def check_routing_stats():
     assert abs(small["balance"] - sum((c / 10 - 0.25) ** 2 for c in cnt)) < 1e-15
 
 
+def check_block_quantizer():
+    """csdn/6a462500 §4.3 block quantizer: the page's size example (fp16 bytes -> INT4 code bytes); per
+    64 x 64 block the minimum gets code 0 and the maximum the top code; codes are monotone in w; every
+    weight is restored within half a step (the rounding bound); an equally spaced block with a
+    power-of-two step is restored exactly; a flat block has scale 0 and is restored exactly."""
+    f = _load("page_facts.json")["int4_size_example"]
+    n_weights = f["fp16_bytes"] // 2
+    assert om.packed_code_bytes(8192, n_weights // 8192, 4) == f["int4_code_bytes"]
+    assert om.packed_code_bytes(8192, n_weights // 8192, 8) == 2 * f["int4_code_bytes"]
+    rng = np.random.default_rng(14)
+    w = (rng.standard_normal((128, 192)) * 0.05).astype(np.float32)
+    for bits in (4, 8):
+        q = om.quantize_blocks(w, bits)
+        top = 2 ** bits - 1
+        assert q["scale"].shape == (2, 3) and q["min"].shape == (2, 3)
+        assert q["codes"].min() >= 0 and q["codes"].max() <= top
+        wh = om.dequantize_blocks(q)
+        for bi in range(2):
+            for bj in range(3):
+                sl = (slice(64 * bi, 64 * bi + 64), slice(64 * bj, 64 * bj + 64))
+                blk, c = w[sl].astype(np.float64), q["codes"][sl]
+                assert c.reshape(-1)[np.argmin(blk)] == 0 and c.reshape(-1)[np.argmax(blk)] == top
+                assert q["min"][bi, bj] == blk.min()
+                order = np.argsort(blk.reshape(-1), kind="stable")
+                assert np.all(np.diff(c.reshape(-1)[order].astype(np.int64)) >= 0)
+                step = (blk.max() - blk.min()) / top
+                assert np.max(np.abs(wh[sl] - blk)) <= 0.5 * step * (1 + 1e-5)
+    grid = np.zeros((64, 64), np.float32)
+    for i in range(64):
+        for j in range(64):
+            grid[i, j] = -0.75 + 0.125 * ((3 * i + j) % 16)
+    qg = om.quantize_blocks(grid, 4)
+    assert qg["scale"][0, 0] == 0.125 and np.array_equal(om.dequantize_blocks(qg), grid.astype(np.float64))
+    flat = np.full((64, 128), 0.3, np.float32)
+    qf = om.quantize_blocks(flat, 4)
+    assert np.all(qf["scale"] == 0) and np.all(qf["codes"] == 0)
+    assert np.array_equal(om.dequantize_blocks(qf), flat.astype(np.float64))
+
+
 PINS = [check_worked_example, check_router_closed_form, check_softmax_library, check_topk_ties_and_order,
         check_gelu_closed_form, check_single_expert_is_mlp, check_k_equals_E_is_softmax_mixture,
         check_routed_equals_dense_bruteforce, check_routing_invariants, check_activation_fraction,
         check_dispatch_stable_sort, check_steps_compose_to_forward, check_ambiguous_tokens,
-        check_renormalised_gates, check_capacity, check_routing_stats]
+        check_renormalised_gates, check_capacity, check_routing_stats, check_block_quantizer]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -452,12 +491,40 @@ def _mut_stats(change):
     return f
 
 
+def _mut_dequant_drops_min(q):
+    c = np.asarray(q["codes"], np.float64)
+    s = np.repeat(np.repeat(np.asarray(q["scale"], np.float64), 64, 0), 64, 1)
+    return c * s  # the block minimum is lost
+
+
+def _mut_quant_floor(w, bits):
+    q = dict(_ORIG_QUANT(w, bits))
+    w32 = np.asarray(w, np.float32)
+    s = np.repeat(np.repeat(q["scale"], 64, 0), 64, 1)
+    m = np.repeat(np.repeat(q["min"], 64, 0), 64, 1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q["codes"] = np.where(s > 0, np.floor((w32 - m) / s), 0).astype(np.uint8)
+    return q
+
+
+def _mut_quant_levels(w, bits):
+    q = dict(_ORIG_QUANT(w, bits))
+    w32 = np.asarray(w, np.float32)
+    s = np.repeat(np.repeat(q["scale"], 64, 0), 64, 1) * np.float32((2 ** bits - 1) / 2 ** bits)
+    m = np.repeat(np.repeat(q["min"], 64, 0), 64, 1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q["codes"] = np.where(s > 0, np.rint((w32 - m) / s), 0).astype(np.int64).clip(0, 255).astype(np.uint8)
+    q["scale"] = q["scale"] * np.float32((2 ** bits - 1) / 2 ** bits)
+    return q
+
+
 _ORIG_DISPATCH = om.dispatch
 _ORIG_TOPK = om.topk_select
 _ORIG_KEPT = om.kept_assignments
 _ORIG_COMBINE = om.combine
 _ORIG_FORWARD = om.forward
 _ORIG_STATS = om.routing_stats
+_ORIG_QUANT = om.quantize_blocks
 
 MUTANTS = {
     "gelu_sign": ("gelu", _mut_gelu_sign),
@@ -477,6 +544,9 @@ MUTANTS = {
     "stats_soft_load_over_assignments": ("routing_stats", _mut_stats("soft_over_assignments")),
     "stats_balance_of_soft_load": ("routing_stats", _mut_stats("balance_of_soft_load")),
     "stats_hard_load_over_tokens": ("routing_stats", _mut_stats("hard_over_tokens")),
+    "dequant_drops_min": ("dequantize_blocks", _mut_dequant_drops_min),
+    "quant_floor": ("quantize_blocks", _mut_quant_floor),
+    "quant_2^bits_levels": ("quantize_blocks", _mut_quant_levels),
 }
 
 
@@ -495,5 +565,6 @@ def test_planted_mistakes(name, monkeypatch):
 
 def test_package_exports():
     for name in ["router_logits", "softmax", "topk_select", "gates_of", "gelu", "expert_ffn", "forward",
-                 "dense_forward", "gates_renormalised", "dispatch", "capacity", "kept_assignments", "expert_rows_ffn", "expert_rows_up", "expert_rows_down", "combine", "routing_stats", "ambiguous_tokens", "top_share"]:
+                 "dense_forward", "gates_renormalised", "dispatch", "capacity", "kept_assignments", "expert_rows_ffn", "expert_rows_up", "expert_rows_down", "combine", "routing_stats", "quantize_blocks", "dequantize_blocks",
+                 "packed_code_bytes", "ambiguous_tokens", "top_share"]:
         assert callable(getattr(oracle, name))
