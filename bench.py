@@ -37,9 +37,10 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s; % of BF16 tensor peak (prefill) / % HBM BW (decode)"
 DEFAULT_WORKLOAD = "e16_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNELS_PER_STEP = 8  # router 1, dispatch 4 (count, scan, scatter, gather), up 1, down 1, combine 1
+KERNELS_PER_STEP = 7  # router 1, dispatch 3 (count + scan, scatter, gather), up 1, down 1, combine 1
 L2_BYTES = 126 * 2**20
 TC_SOURCES = ["sparse_mixture_experts_moe_gb300/csrc/ffn_tc.cu", "sparse_mixture_experts_moe_gb300/csrc/common.cuh"]
+QUANT_SOURCES = ["sparse_mixture_experts_moe_gb300/csrc/quant.cu", "sparse_mixture_experts_moe_gb300/csrc/common.cuh"]
 STREAM_SOURCES = ["sparse_mixture_experts_moe_gb300/csrc/ffn_stream.cu",
                   "sparse_mixture_experts_moe_gb300/csrc/common.cuh"]
 
@@ -53,6 +54,10 @@ def parse_args():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    p.add_argument("--weight-bits", type=int, default=0, choices=[0, 4, 8],
+                   help="0: the bf16 layer; 4 / 8: expert weights block-quantised to INT4 / INT8 (bf16 layers)")
+    p.add_argument("--launch", default="graph", choices=["graph", "direct"],
+                   help="graph: replay a CUDA graph of the layer per step; direct: one C ABI call per kernel")
     return p.parse_args()
 
 
@@ -284,8 +289,31 @@ def run_ours(args, w, rank, world, device):
     moe.workspace_init(ws)
     stream = torch.cuda.current_stream()
 
-    def step():
-        moe.forward(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws)
+    qbits = args.weight_bits
+    q1 = q2 = None
+    if qbits:
+        if dt != 1:
+            raise SystemExit("--weight-bits needs a bf16 workload")
+        q1, q2 = moe.quantize(w1, qbits), moe.quantize(w2, qbits)  # once, before timing
+        torch.cuda.synchronize()
+
+    def direct_step(s=None):
+        if qbits:
+            moe.forward_q(x, w_r, b_r, q1, q2, T, d, F, E, k, qbits, out, ws, stream=s)
+        else:
+            moe.forward(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws, stream=s)
+
+    graph = None
+    if args.launch == "graph":
+        # the layer's kernels captured once (moe_graph_capture_begin / _end); each step replays all of them
+        with moe.GraphCapture(keep=(x, w_r, b_r, w1, w2, out, ws, q1, q2)) as cap:
+            direct_step(cap.stream)
+        graph = cap.graph
+
+        def step():
+            graph.launch(stream)
+    else:
+        step = direct_step
 
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
                           else os.environ["CUDA_VISIBLE_DEVICES"].split(",")[torch.cuda.current_device()])
@@ -314,6 +342,20 @@ def run_ours(args, w, rank, world, device):
     ms_per_step = ms_total / args.steps
     value = job_tokens_per_s(T, world, ms_per_step)
 
+    # --- context: the same K steps as one host call per kernel (no graph)
+    ms_direct = None
+    if graph is not None:
+        for _ in range(3):
+            direct_step()
+        torch.cuda.synchronize()
+        ed0, ed1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ed0.record(stream)
+        for _ in range(args.steps):
+            direct_step()
+        ed1.record(stream)
+        torch.cuda.synchronize()
+        ms_direct = max_over_ranks(ed0.elapsed_time(ed1), world, device) / args.steps
+
     # --- per-kernel timing: the same step as its separate C ABI calls, events between them
     idx = torch.empty((T, k), dtype=torch.int32, device=device)
     gate = torch.empty((T, k), dtype=torch.float32, device=device)
@@ -335,9 +377,15 @@ def run_ours(args, w, rank, world, device):
         e[1].record(stream)
         moe.dispatch(x, idx, gate, T, d, E, k, dt, counts, offsets, perm, row_of, row_gate, x_perm, ws)
         e[2].record(stream)
-        moe.expert_up(x_perm, w1, offsets, T, d, F, E, k, dt, h, ws)
+        if qbits:
+            moe.expert_up_q(x_perm, q1[0], q1[1], offsets, T, d, F, E, k, qbits, h)
+        else:
+            moe.expert_up(x_perm, w1, offsets, T, d, F, E, k, dt, h, ws)
         e[3].record(stream)
-        moe.expert_down(h, w2, offsets, row_gate, T, d, F, E, k, dt, y_perm, ws)
+        if qbits:
+            moe.expert_down_q(h, q2[0], q2[1], offsets, row_gate, T, d, F, E, k, qbits, y_perm)
+        else:
+            moe.expert_down(h, w2, offsets, row_gate, T, d, F, E, k, dt, y_perm, ws)
         e[4].record(stream)
         moe.combine(y_perm, row_of, T, d, k, dt, out)
         e[5].record(stream)
@@ -348,14 +396,22 @@ def run_ours(args, w, rank, world, device):
     touched = int((counts_h > 0).sum())
 
     # --- e2e: public layer object, pinned host tokens in, output back to the host, every step
-    layer = moe.MoELayer(w_r, w1, w2, k=k, b_r=b_r)
+    layer = moe.MoELayer(w_r, w1, w2, k=k, b_r=b_r, weight_bits=qbits or None)
     x_host = x.cpu().pin_memory()
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     x_dev = torch.empty_like(x)
     out_dev = torch.empty_like(out)
+    if graph is not None:
+        layer_graph = layer.graph(x_dev, out_dev)
+
+        def layer_step():
+            layer_graph.launch(stream)
+    else:
+        def layer_step():
+            layer(x_dev, out=out_dev)
     for _ in range(3):
         x_dev.copy_(x_host, non_blocking=True)
-        layer(x_dev, out=out_dev)
+        layer_step()
         out_host.copy_(out_dev, non_blocking=True)
     torch.cuda.synchronize()
     if world > 1:
@@ -364,7 +420,7 @@ def run_ours(args, w, rank, world, device):
     e0.record(stream)
     for _ in range(args.steps):
         x_dev.copy_(x_host, non_blocking=True)
-        layer(x_dev, out=out_dev)
+        layer_step()
         out_host.copy_(out_dev, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -380,7 +436,19 @@ def run_ours(args, w, rank, world, device):
     eb = 2 if dt == 1 else 4
     dom = max(["expert_up", "expert_down"], key=lambda n: kern_ms[n])
     stream_path = dt == 1 and A <= 256  # the library's automatic choice (include/moe.h, moe_path)
-    if stream_path:
+    if qbits:
+        # quantised weight streaming: codes + (scale, min) of the touched experts + rows in and out
+        K_, N_ = (d, F) if dom == "expert_up" else (F, d)
+        wbytes = K_ * N_ * qbits // 8 + (K_ // 64) * (N_ // 64) * 8
+        alg_bytes = touched * wbytes + A * K_ * eb + A * N_ * (eb if dom == "expert_up" else 4)
+        achieved = alg_bytes / (kern_ms[dom] / 1e3) / 1e9
+        roof = {"kernel": f"ffn_stream_q_kernel<{qbits}> ({dom})", "bound": "hbm", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": stored_traffic(f"ffn_stream_q_kernel<{qbits}, {1 if dom == 'expert_up' else 2}>",
+                                          w.name, QUANT_SOURCES),
+                "alg_bytes_per_launch": alg_bytes, "ms_per_launch": kern_ms[dom],
+                "peak_source": f"{peak_src} hbm_gbs"}
+    elif stream_path:
         # weight streaming: bytes = touched experts' matrix + the routed rows in and out
         if dom == "expert_up":
             alg_bytes = touched * d * F * eb + A * d * eb + A * F * eb
@@ -407,7 +475,12 @@ def run_ours(args, w, rank, world, device):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if dt == 1 else "f32", "data": "synthetic (seeded inputgen draws)",
-        "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "single GPU",
+                       weights=(f"INT{qbits} codes, 64x64 blocks with fp32 (scale, min), quantised once before "
+                                "timing" if qbits else "bf16" if dt == 1 else "fp32"),
+                       launch=("CUDA graph of the layer's kernels (moe_forward_graph_create), one graph launch "
+                               "per step" if graph is not None else "one C ABI call per kernel")),
+        "ms_per_step_direct_calls": ms_direct,
         "roofline": roof,
         "kernel_ms": kern_ms,
         "experts_touched": touched,
@@ -416,7 +489,7 @@ def run_ours(args, w, rank, world, device):
         "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not qbits:
         v, n, secs, cores = oracle_sample(w, x, w_r, b_r, w1, w2, args.cpu_seconds)
         result["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                   "sample": f"first {n} of the batch's {T} tokens, fp64 oracle forward, "

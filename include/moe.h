@@ -251,6 +251,67 @@ const char* moe_status_string(moe_status s);
  * MOE_ERR_DEVICE_TIMEOUT in the workspace and returns; no fault, the context stays usable. */
 moe_status moe_selftest_wait_timeout(void* workspace, size_t ws_bytes, int timeout_us, void* stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Block-quantised expert weights (INT4 / INT8) for weight streaming.
+ *   csdn/6a462500 §4.3 (64 x 64 blocks, per-block min and max, codes of 4 bits); csdn/6a919c0d
+ *   §2.3 (INT4 expert weights halve the bytes moved again; INT8 as the middle tier).
+ * Quantisation of each 64 x 64 block of each expert's [K, N] matrix: scale = (max - min) /
+ *   (2^bits - 1), code = round((w - min) / scale) in fp32 (correctly rounded subtraction and
+ *   division, ties to even), restored as w ~ min + code * scale (|error| <= scale / 2). A block of
+ *   equal values has scale 0 and codes 0. bits is 4 or 8; K and N must be multiples of 64.
+ * Layout of `codes` (moe_qweight_bytes(K, N, E, bits) bytes, 16-byte aligned): per expert,
+ *   16-byte tiles of 8 consecutive columns by 16/bits consecutive k-rows, row-major over
+ *   (k / (16/bits), n / 8). INT4: 32-bit word j of a tile is its k-row j, nibble c (bits 4c..4c+3)
+ *   is column c. INT8: 64-bit half j is k-row j, byte c is column c.
+ * Layout of `scale_min` (moe_qscale_bytes(K, N, E) bytes, 8-byte aligned): fp32 pairs
+ *   (scale, min), [E][K/64][N/64].
+ * moe_quantize_weights: w [E, K, N] (bf16 or fp32) -> codes, scale_min on the device.
+ * moe_expert_up_q / moe_expert_down_q: moe_expert_up / moe_expert_down (bf16 activations; h bf16,
+ *   y_perm fp32) reading quantised W1 [E, d, F] / W2 [E, F, d]; weight-streaming kernel for any
+ *   number of rows (built for decode batches). moe_forward_q: the whole layer with them (x, w_r
+ *   bf16; out_dt, flags, capacity, router_stats and the workspace as in moe_forward_ex).
+ * Sizes 0 / MOE_ERR_INVALID_ARG on bad sizes, NULL or misaligned pointers. */
+size_t moe_qweight_bytes(int K, int N, int E, int bits);
+size_t moe_qscale_bytes(int K, int N, int E);
+moe_status moe_quantize_weights(const void* w, int K, int N, int E, moe_dtype dt, int bits, void* codes,
+                                float* scale_min, void* stream);
+moe_status moe_expert_up_q(const void* x_perm, const void* w1_codes, const float* w1_scale_min,
+                           const int32_t* offsets, int T, int d, int F, int E, int k, int bits, void* h,
+                           void* stream);
+moe_status moe_expert_down_q(const void* h, const void* w2_codes, const float* w2_scale_min,
+                             const int32_t* offsets, const float* row_gate, int T, int d, int F, int E, int k,
+                             int bits, void* y_perm, void* stream);
+moe_status moe_forward_q(const void* x, const void* w_r, const float* b_r, const void* w1_codes,
+                         const float* w1_scale_min, const void* w2_codes, const float* w2_scale_min, int T, int d,
+                         int F, int E, int k, int bits, moe_dtype out_dt, int flags, int capacity, void* out,
+                         int32_t* topk_idx, float* topk_gate, int32_t* counts, float* router_stats, void* workspace,
+                         size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * CUDA-graph replay of the whole layer.
+ * moe_forward_graph_create: records the kernels of one moe_forward_ex call with these arguments
+ *      (captured on a private stream; nothing runs) and instantiates them as a CUDA graph. Every
+ *      pointer and size is fixed in the graph: each launch runs the full layer again on the
+ *      current contents of the same buffers, with one host call instead of one per kernel.
+ *      Argument errors are those of moe_forward_ex; *graph is NULL on any error.
+ * moe_graph_launch: enqueues one replay on `stream`. The buffers must stay allocated and the
+ *      usual stream ordering applies (write x before, read out after, on or after `stream`).
+ * moe_graph_destroy: frees the graph (NULL is a no-op).
+ * moe_graph_capture_begin / moe_graph_capture_end: the general form. begin returns a private
+ *      stream in capture; every moe_* call given that stream is recorded, not run; end stops the
+ *      capture, instantiates what was recorded into *graph and destroys the stream (always, also
+ *      on error). Use it for moe_forward_q or for a sequence of the separate entry points. */
+typedef struct moe_graph_s* moe_graph;
+moe_status moe_graph_capture_begin(void** capture_stream);
+moe_status moe_forward_graph_create(const void* x, const void* w_r, const float* b_r, const void* w1,
+                                    const void* w2, int T, int d, int F, int E, int k, moe_dtype dt,
+                                    moe_dtype out_dt, moe_path path, int flags, int capacity, void* out,
+                                    int32_t* topk_idx, float* topk_gate, int32_t* counts, float* router_stats,
+                                    void* workspace, size_t ws_bytes, moe_graph* graph);
+moe_status moe_graph_capture_end(void* capture_stream, moe_graph* graph);
+moe_status moe_graph_launch(moe_graph graph, void* stream);
+moe_status moe_graph_destroy(moe_graph graph);
+
 #ifdef __cplusplus
 }
 #endif

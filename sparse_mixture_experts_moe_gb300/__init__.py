@@ -16,7 +16,8 @@ from . import _lib
 from ._lib import (  # noqa: F401
     MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK, MOE_ERR_DEVICE_TIMEOUT,
     GATES_RENORMALISE, MOE_DTYPE_F32, MOE_DTYPE_BF16, PATH_AUTO, PATH_TENSOR, PATH_STREAM, PATH_SIMT, PATH_TENSOR_PAIR, MoeError,
-    router_topk, router_topk_stats, router_stats_len, dispatch, dispatch_noalloc, capacity, expert_up, expert_down, grouped_ffn, combine, forward, workspace_bytes, workspace_init,
+    ForwardGraph, GraphCapture, CapturedGraph, qweight_bytes, qscale_bytes, quantize_weights, quantize,
+    expert_up_q, expert_down_q, forward_q, router_topk, router_topk_stats, router_stats_len, dispatch, dispatch_noalloc, capacity, expert_up, expert_down, grouped_ffn, combine, forward, workspace_bytes, workspace_init,
     get_device_status, status_string, selftest_wait_timeout, lib,
 )
 
@@ -25,9 +26,11 @@ class MoELayer:
     """Holds the layer's weights and a reusable workspace; calling it runs moe_forward on the current stream."""
 
     def __init__(self, w_r, w1, w2, k: int = 2, b_r=None, path: int = PATH_AUTO, renormalise: bool = False,
-                 capacity_factor: Optional[float] = None):
+                 capacity_factor: Optional[float] = None, weight_bits: Optional[int] = None):
         """capacity_factor: None for no expert capacity, else each call keeps at most
-        ceil(T * k / E * capacity_factor) assignments per expert (the later ones are dropped)."""
+        ceil(T * k / E * capacity_factor) assignments per expert (the later ones are dropped).
+        weight_bits: None keeps w1 / w2 as given; 4 or 8 quantises them once, here, to 64 x 64-block
+        INT4 / INT8 codes (moe_quantize_weights) that every call streams instead (bf16 layers)."""
         import torch
         if not (w_r.is_cuda and w1.is_cuda and w2.is_cuda):
             raise ValueError("MoELayer: weights must be CUDA tensors")
@@ -42,6 +45,13 @@ class MoELayer:
         self.path = path
         self.renormalise = renormalise
         self.capacity_factor = capacity_factor
+        self.weight_bits = weight_bits
+        self.q1 = self.q2 = None
+        if weight_bits is not None:
+            if self.dt != MOE_DTYPE_BF16:
+                raise ValueError("MoELayer: quantised expert weights need a bf16 layer")
+            self.q1 = quantize(self.w1, weight_bits)
+            self.q2 = quantize(self.w2, weight_bits)
         self._ws = None
         self._ws_T = -1
 
@@ -67,10 +77,34 @@ class MoELayer:
         cap = 0 if self.capacity_factor is None else capacity(T, self.k, self.E, self.capacity_factor)
         if cap < 0:
             raise MoeError(MOE_ERR_INVALID_ARG, "capacity_factor")
-        forward(x, self.w_r, self.b_r, self.w1, self.w2, T, self.d, self.F, self.E, self.k, self.dt, out,
-                self.workspace(T), topk_idx=topk_idx, topk_gate=topk_gate, counts=counts, path=self.path,
-                out_dt=_lib.dtype_code(out), renormalise=self.renormalise, capacity=cap, router_stats=router_stats)
+        self._run(x, out, T, cap, topk_idx, topk_gate, counts, router_stats, None)
         return out
+
+    def _run(self, x, out, T, cap, topk_idx, topk_gate, counts, router_stats, stream):
+        if self.weight_bits is not None:
+            forward_q(x, self.w_r, self.b_r, self.q1, self.q2, T, self.d, self.F, self.E, self.k, self.weight_bits,
+                      out, self.workspace(T), topk_idx=topk_idx, topk_gate=topk_gate, counts=counts,
+                      out_dt=_lib.dtype_code(out), renormalise=self.renormalise, capacity=cap,
+                      router_stats=router_stats, stream=stream)
+        else:
+            forward(x, self.w_r, self.b_r, self.w1, self.w2, T, self.d, self.F, self.E, self.k, self.dt, out,
+                    self.workspace(T), topk_idx=topk_idx, topk_gate=topk_gate, counts=counts, path=self.path,
+                    out_dt=_lib.dtype_code(out), renormalise=self.renormalise, capacity=cap,
+                    router_stats=router_stats, stream=stream)
+
+    def graph(self, x, out, topk_idx=None, topk_gate=None, counts=None, router_stats=None) -> CapturedGraph:
+        """A CUDA graph of this layer on these buffers: graph.launch() reruns the layer on the current
+        contents of x and writes out (one host call per step)."""
+        T = int(x.shape[0])
+        cap = 0 if self.capacity_factor is None else capacity(T, self.k, self.E, self.capacity_factor)
+        if cap < 0:
+            raise MoeError(MOE_ERR_INVALID_ARG, "capacity_factor")
+        ws = self.workspace(T)
+        keep = (x, out, ws, topk_idx, topk_gate, counts, router_stats, self.w_r, self.b_r, self.w1, self.w2,
+                self.q1, self.q2)
+        with GraphCapture(keep=keep) as cap_:
+            self._run(x, out, T, cap, topk_idx, topk_gate, counts, router_stats, cap_.stream)
+        return cap_.graph
 
     def device_status(self):
         """(status, detail) of the first device-side error since the last call; synchronises."""

@@ -47,6 +47,19 @@ SIGNATURES = {
     "moe_combine": [_p, _p, _i, _i, _i, _i, _p, _p],
     "moe_forward": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _sz, _p],
     "moe_forward_ex": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _sz, _p],
+    "moe_forward_graph_create": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p,
+                                 _sz, _p],
+    "moe_graph_launch": [_p, _p],
+    "moe_graph_capture_begin": [_p],
+    "moe_graph_capture_end": [_p, _p],
+    "moe_qweight_bytes": [_i, _i, _i, _i],
+    "moe_qscale_bytes": [_i, _i, _i],
+    "moe_quantize_weights": [_p, _i, _i, _i, _i, _i, _p, _p, _p],
+    "moe_expert_up_q": [_p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p],
+    "moe_expert_down_q": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p],
+    "moe_forward_q": [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p,
+                      _sz, _p],
+    "moe_graph_destroy": [_p],
     "moe_router_topk_stats": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _sz, _p],
     "moe_workspace_bytes": [_i, _i, _i, _i, _i, _i],
     "moe_workspace_init": [_p, _sz, _p],
@@ -54,7 +67,8 @@ SIGNATURES = {
     "moe_status_string": [_i],
     "moe_selftest_wait_timeout": [_p, _sz, _i, _p],
 }
-_RESTYPES = {"moe_workspace_bytes": ctypes.c_size_t, "moe_status_string": ctypes.c_char_p}
+_RESTYPES = {"moe_workspace_bytes": ctypes.c_size_t, "moe_status_string": ctypes.c_char_p,
+             "moe_qweight_bytes": ctypes.c_size_t, "moe_qscale_bytes": ctypes.c_size_t}
 
 _LIB = None
 
@@ -214,6 +228,133 @@ def forward(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws, topk_idx=None, topk
                               _ptr(topk_idx), _ptr(topk_gate), _ptr(counts), _ptr(router_stats), _ptr(ws),
                               ws.numel() * ws.element_size(), _stream(stream))
     return _check(rc, "moe_forward") if check else rc
+
+
+class ForwardGraph:
+    """The layer's kernels for one fixed set of buffers, captured once as a CUDA graph
+    (moe_forward_graph_create); launch() replays the whole layer with one host call. The tensors
+    passed at creation are kept referenced so that their memory outlives the graph."""
+
+    def __init__(self, x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws, topk_idx=None, topk_gate=None, counts=None,
+                 path=PATH_AUTO, out_dt=None, renormalise=False, capacity=0, router_stats=None):
+        out_dt = dt if out_dt is None else out_dt
+        self._keep = (x, w_r, b_r, w1, w2, out, ws, topk_idx, topk_gate, counts, router_stats)
+        h = ctypes.c_void_p()
+        self._lib = lib()
+        rc = self._lib.moe_forward_graph_create(
+            _ptr(x), _ptr(w_r), _ptr(b_r), _ptr(w1), _ptr(w2), T, d, F, E, k, dt, out_dt, path,
+            GATES_RENORMALISE if renormalise else 0, int(capacity), _ptr(out), _ptr(topk_idx), _ptr(topk_gate),
+            _ptr(counts), _ptr(router_stats), _ptr(ws), ws.numel() * ws.element_size(), ctypes.byref(h))
+        _check(rc, "moe_forward_graph_create")
+        self._h = h
+
+    def launch(self, stream=None):
+        return _check(self._lib.moe_graph_launch(self._h, _stream(stream)), "moe_graph_launch")
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value is not None:
+            self._lib.moe_graph_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        self.close()
+
+
+class GraphCapture:
+    """Records the moe_* calls made with `cap.stream` inside the with-block into a CUDA graph
+    (moe_graph_capture_begin / _end); `cap.graph` then replays them with launch(). Keep the
+    tensors those calls used alive while the graph is in use (pass them as keep=...)."""
+
+    def __init__(self, keep=()):
+        self._keep = tuple(keep)
+        self.stream = None
+        self.graph = None
+
+    def __enter__(self):
+        cs = ctypes.c_void_p()
+        _check(lib().moe_graph_capture_begin(ctypes.byref(cs)), "moe_graph_capture_begin")
+        self.stream = cs.value
+        return self
+
+    def __exit__(self, exc_type, exc, tb):
+        h = ctypes.c_void_p()
+        rc = lib().moe_graph_capture_end(self.stream, ctypes.byref(h))
+        if exc_type is None:
+            _check(rc, "moe_graph_capture_end")
+            self.graph = CapturedGraph(h, self._keep)
+        elif rc == MOE_OK:
+            lib().moe_graph_destroy(h)
+        return False
+
+
+class CapturedGraph:
+    def __init__(self, handle, keep):
+        self._h = handle
+        self._keep = keep
+        self._lib = lib()
+
+    def launch(self, stream=None):
+        return _check(self._lib.moe_graph_launch(self._h, _stream(stream)), "moe_graph_launch")
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value is not None:
+            self._lib.moe_graph_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        self.close()
+
+
+# ------------------------------------------------------------------ block-quantised weights
+
+def qweight_bytes(K, N, E, bits) -> int:
+    return int(lib().moe_qweight_bytes(K, N, E, bits))
+
+
+def qscale_bytes(K, N, E) -> int:
+    return int(lib().moe_qscale_bytes(K, N, E))
+
+
+def quantize_weights(w, K, N, E, dt, bits, codes, scale_min, stream=None, check=True):
+    """w [E, K, N] -> codes (moe_qweight_bytes bytes) and scale_min ([E, K/64, N/64, 2] fp32)."""
+    rc = lib().moe_quantize_weights(_ptr(w), K, N, E, dt, bits, _ptr(codes), _ptr(scale_min), _stream(stream))
+    return _check(rc, "moe_quantize_weights") if check else rc
+
+
+def quantize(w, bits, stream=None):
+    """Quantise a device tensor w [E, K, N] (bf16 or fp32); returns (codes uint8, scale_min fp32)."""
+    import torch
+    E, K, N = (int(v) for v in w.shape)
+    nb = qweight_bytes(K, N, E, bits)
+    if nb == 0:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_qweight_bytes")
+    codes = torch.empty(nb, dtype=torch.uint8, device=w.device)
+    sm = torch.empty((E, K // 64, N // 64, 2), dtype=torch.float32, device=w.device)
+    quantize_weights(w.contiguous(), K, N, E, dtype_code(w), bits, codes, sm, stream)
+    return codes, sm
+
+
+def expert_up_q(x_perm, codes, scale_min, offsets, T, d, F, E, k, bits, h, stream=None, check=True):
+    rc = lib().moe_expert_up_q(_ptr(x_perm), _ptr(codes), _ptr(scale_min), _ptr(offsets), T, d, F, E, k, bits,
+                               _ptr(h), _stream(stream))
+    return _check(rc, "moe_expert_up_q") if check else rc
+
+
+def expert_down_q(h, codes, scale_min, offsets, row_gate, T, d, F, E, k, bits, y_perm, stream=None, check=True):
+    rc = lib().moe_expert_down_q(_ptr(h), _ptr(codes), _ptr(scale_min), _ptr(offsets), _ptr(row_gate), T, d, F, E,
+                                 k, bits, _ptr(y_perm), _stream(stream))
+    return _check(rc, "moe_expert_down_q") if check else rc
+
+
+def forward_q(x, w_r, b_r, w1q, w2q, T, d, F, E, k, bits, out, ws, topk_idx=None, topk_gate=None, counts=None,
+              out_dt=None, renormalise=False, capacity=0, router_stats=None, stream=None, check=True):
+    """The layer with block-quantised expert weights; w1q / w2q are (codes, scale_min) pairs."""
+    out_dt = MOE_DTYPE_BF16 if out_dt is None else out_dt
+    rc = lib().moe_forward_q(_ptr(x), _ptr(w_r), _ptr(b_r), _ptr(w1q[0]), _ptr(w1q[1]), _ptr(w2q[0]),
+                             _ptr(w2q[1]), T, d, F, E, k, bits, out_dt, GATES_RENORMALISE if renormalise else 0,
+                             int(capacity), _ptr(out), _ptr(topk_idx), _ptr(topk_gate), _ptr(counts),
+                             _ptr(router_stats), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    return _check(rc, "moe_forward_q") if check else rc
 
 
 def selftest_wait_timeout(ws, timeout_us, stream=None, check=True):

@@ -274,6 +274,55 @@ moe_status moe_grouped_ffn(const void* x_perm, const void* w1, const void* w2, c
                             workspace, ws_bytes, stream);
 }
 
+// ------------------------------------------------------------------ block-quantised weights
+namespace {
+bool qsizes_ok(int K, int N, int E, int bits) {
+  return (bits == 4 || bits == 8) && K >= 64 && N >= 64 && K % 64 == 0 && N % 64 == 0 && E >= 1 && E <= 1024;
+}
+inline bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+
+moe_status expert_half_q(int stage, const void* a, const void* codes, const float* scale_min,
+                         const int32_t* offsets, const float* row_gate, int T, int d, int F, int E, int k, int bits,
+                         void* out, void* stream) {
+  if (!sizes_ok(T, d, F, E, k, MOE_DTYPE_BF16)) return MOE_ERR_INVALID_ARG;
+  const int K = stage == 1 ? d : F, N = stage == 1 ? F : d;
+  if (!qsizes_ok(K, N, E, bits)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (a == nullptr || codes == nullptr || scale_min == nullptr || offsets == nullptr || out == nullptr ||
+      (stage == 2 && row_gate == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(codes) || !aligned8(scale_min) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  QFfnArgs p{a, codes, scale_min, offsets, row_gate, out, T * k, K, N, E, bits, stage};
+  return cuda_status(launch_ffn_stream_q(p, (cudaStream_t)stream));
+}
+}  // namespace
+
+size_t moe_qweight_bytes(int K, int N, int E, int bits) {
+  if (!qsizes_ok(K, N, E, bits)) return 0;
+  return (size_t)E * K * N * bits / 8;
+}
+size_t moe_qscale_bytes(int K, int N, int E) {
+  if (!qsizes_ok(K, N, E, 4)) return 0;
+  return (size_t)E * (K / 64) * (N / 64) * 2 * sizeof(float);
+}
+moe_status moe_quantize_weights(const void* w, int K, int N, int E, moe_dtype dt, int bits, void* codes,
+                                float* scale_min, void* stream) {
+  if (!qsizes_ok(K, N, E, bits) || (dt != MOE_DTYPE_BF16 && dt != MOE_DTYPE_F32)) return MOE_ERR_INVALID_ARG;
+  if (w == nullptr || codes == nullptr || scale_min == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w) || !aligned16(codes) || !aligned8(scale_min)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize(w, K, N, E, dt, bits, codes, scale_min, (cudaStream_t)stream));
+}
+moe_status moe_expert_up_q(const void* x_perm, const void* w1_codes, const float* w1_scale_min,
+                           const int32_t* offsets, int T, int d, int F, int E, int k, int bits, void* h,
+                           void* stream) {
+  return expert_half_q(1, x_perm, w1_codes, w1_scale_min, offsets, nullptr, T, d, F, E, k, bits, h, stream);
+}
+moe_status moe_expert_down_q(const void* h, const void* w2_codes, const float* w2_scale_min,
+                             const int32_t* offsets, const float* row_gate, int T, int d, int F, int E, int k,
+                             int bits, void* y_perm, void* stream) {
+  return expert_half_q(2, h, w2_codes, w2_scale_min, offsets, row_gate, T, d, F, E, k, bits, y_perm, stream);
+}
+
 moe_status moe_combine(const void* y_perm, const int32_t* row_of, int T, int d, int k, moe_dtype dt, void* out,
                        void* stream) {
   if (!sizes_ok(T, d, 8, k, k, dt)) return MOE_ERR_INVALID_ARG;
@@ -321,6 +370,45 @@ moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, cons
   if (st != MOE_OK) return st;
   return moe_combine(yp, rowof, T, d, k, out_dt, out, stream);
 }
+moe_status moe_forward_q(const void* x, const void* w_r, const float* b_r, const void* w1_codes,
+                         const float* w1_scale_min, const void* w2_codes, const float* w2_scale_min, int T, int d,
+                         int F, int E, int k, int bits, moe_dtype out_dt, int flags, int capacity, void* out,
+                         int32_t* topk_idx, float* topk_gate, int32_t* counts, float* router_stats, void* workspace,
+                         size_t ws_bytes, void* stream) {
+  const moe_dtype dt = MOE_DTYPE_BF16;
+  if (!sizes_ok(T, d, F, E, k, dt) || !qsizes_ok(d, F, E, bits) || capacity < 0) return MOE_ERR_INVALID_ARG;
+  if ((flags & ~MOE_GATES_RENORMALISE) != 0) return MOE_ERR_INVALID_ARG;
+  if (out_dt != MOE_DTYPE_F32 && out_dt != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  const Layout L(T, d, F, E, k, dt);
+  if (ws_bytes < L.end) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (x == nullptr || w_r == nullptr || out == nullptr || !aligned16(x) || !aligned16(w_r) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  int32_t* idx = topk_idx != nullptr ? topk_idx : at<int32_t>(workspace, L.topk_idx);
+  float* gate = topk_gate != nullptr ? topk_gate : at<float>(workspace, L.topk_gate);
+  int32_t* cnt = counts != nullptr ? counts : at<int32_t>(workspace, L.counts);
+  int32_t* offs = at<int32_t>(workspace, L.offsets);
+  int32_t* rowof = at<int32_t>(workspace, L.row_of);
+  float* rgate = at<float>(workspace, L.row_gate);
+  void* xp = at<void>(workspace, L.x_perm);
+  void* h = at<void>(workspace, L.h);
+  void* yp = at<void>(workspace, L.y_perm);
+  const RouterStats rs{router_stats != nullptr ? at<float>(workspace, L.stats_part) : nullptr, router_stats,
+                       at<int>(workspace, 0) + 3};
+  moe_status st = cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, flags, rs, idx, gate,
+                                                 at<int>(workspace, 0), wait_timeout_ns(), (cudaStream_t)stream));
+  if (st != MOE_OK) return st;
+  st = moe_dispatch_ex(x, idx, gate, T, d, E, k, dt, capacity, cnt, offs, at<int32_t>(workspace, L.perm_token),
+                       rowof, rgate, xp, workspace, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  st = moe_expert_up_q(xp, w1_codes, w1_scale_min, offs, T, d, F, E, k, bits, h, stream);
+  if (st != MOE_OK) return st;
+  st = moe_expert_down_q(h, w2_codes, w2_scale_min, offs, rgate, T, d, F, E, k, bits, yp, stream);
+  if (st != MOE_OK) return st;
+  return moe_combine(yp, rowof, T, d, k, out_dt, out, stream);
+}
+
 moe_status moe_forward(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2, int T,
                        int d, int F, int E, int k, moe_dtype dt, void* out, int32_t* topk_idx, float* topk_gate,
                        int32_t* counts, void* workspace, size_t ws_bytes, void* stream) {

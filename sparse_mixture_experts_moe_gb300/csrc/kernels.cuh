@@ -71,6 +71,21 @@ struct FfnArgs {
   uint64_t timeout_ns;
 };
 cudaError_t launch_ffn_simt(const FfnArgs& a, cudaStream_t s);
+
+// Block-quantised weights (quant.cu): codes in 16-byte tiles of 8 columns x 16/bits k-rows,
+// (scale, min) per 64 x 64 block.
+struct QFfnArgs {
+  const void* a;          // [rows, K] bf16
+  const void* codes;      // [E, K/(16/bits), N/8] 16-byte tiles
+  const float* scale_min; // [E, K/64, N/64] (scale, min) pairs
+  const int32_t* offsets; // [E+1]
+  const float* row_gate;  // [rows] (stage 2)
+  void* out;              // [rows, N]: bf16 (stage 1) or fp32 (stage 2)
+  int rows, K, N, E, bits, stage;
+};
+cudaError_t launch_quantize(const void* w, int K, int N, int E, int dt, int bits, void* codes, float* scale_min,
+                            cudaStream_t s);
+cudaError_t launch_ffn_stream_q(const QFfnArgs& a, cudaStream_t s);
 cudaError_t launch_ffn_stream(const FfnArgs& a, cudaStream_t s);
 // Returns cudaErrorNotSupported when no tensor-map encoder is available.
 cudaError_t launch_ffn_tensor(const FfnArgs& a, cudaStream_t s);

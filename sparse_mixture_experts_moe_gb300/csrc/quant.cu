@@ -1,0 +1,312 @@
+// Block quantisation of expert weights and the weight-streaming expert FFN that reads them.
+// csdn/6a462500 §4.3 (64 x 64 blocks, each with its own min and max); csdn/6a919c0d §2.3 (decode
+// is bound by moving expert weights, so fewer bytes per weight is the lever).
+//
+// Quantiser: per 64 x 64 block, scale = (max - min) / (2^bits - 1) and
+// code = round((w - min) / scale), in fp32 with correctly rounded subtraction and division and
+// rounding half to even, so the codes are a deterministic function of the weights; w is restored
+// as min + code * scale (the page's dequantisation would lose the block minimum).
+//
+// Memory format of the codes of one [K, N] matrix: 16-byte tiles of 8 consecutive columns by
+// KT = 16 / bits consecutive k-rows, tiles row-major over (k / KT, n / 8). Inside a tile: INT4,
+// 32-bit word j holds the tile's k-row j, nibble c (bits 4c..4c+3) is column c; INT8, 64-bit
+// half j holds k-row j, byte c is column c. Eight
+// lanes reading one 16-byte tile each cover a 64-column slab of KT k-rows with one coalesced
+// 128-byte request, and a tile never straddles a 64 x 64 block. Scales: one (scale, min) float
+// pair per block, [K/64][N/64] per expert.
+//
+// Streaming kernel: the structure of ffn_stream.cu (work unit = (expert with rows, 64-column
+// slab), full depth per CTA, fixed-order reductions) with the dequantisation folded into the
+// dot product: sum_k a_k (min_b + c_k scale_b) = sum_b [ (a scale_b) . c  +  min_b sum a ].
+// Per weight that is one byte permute into a 2^23-offset float, one subtraction (exact) and one
+// FMA per activation row; the column-independent a * min term is accumulated once per k-row.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int QB = 64;  // block edge
+constexpr int kThreads = 256, kWarps = 8;
+constexpr int NS = 64;              // columns per slab (one block column)
+constexpr int LPR = NS / 8;         // lanes per tile row: 8
+constexpr int RPW = 32 / LPR;       // tile rows per warp per step: 4
+constexpr int GSTEP = kWarps * RPW; // tile rows per CTA step: 32
+constexpr int KC = 1024;            // k-depth of activations staged per chunk
+constexpr int kUnroll = 4;
+constexpr float kMagic = 8388608.0f;  // 2^23: a byte b placed in the low mantissa bits reads 2^23 + b
+
+// ------------------------------------------------------------------ quantiser
+template <typename T, int BITS>
+__global__ void __launch_bounds__(256)
+quantize_kernel(const T* __restrict__ w, int K, int N, uint4* __restrict__ codes, float2* __restrict__ sm) {
+  constexpr int KT = 16 / BITS;  // k-rows per tile: 128 bits / (8 columns x BITS)
+  static_assert(KT * 8 * BITS == 128, "a tile is 16 bytes");
+  constexpr float levels = (float)((1 << BITS) - 1);
+  __shared__ float blk[QB][QB + 1];
+  __shared__ float s_lo[kWarps], s_hi[kWarps];
+  const int nbj = N / QB, nbi = K / QB;
+  const int bj = blockIdx.x % nbj;
+  const int bi = (blockIdx.x / nbj) % nbi;
+  const int e = blockIdx.x / (nbj * nbi);
+  const T* src = w + ((size_t)e * K + (size_t)bi * QB) * N + (size_t)bj * QB;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float lo = INFINITY, hi = -INFINITY;
+  for (int i = tid; i < QB * QB; i += 256) {
+    const int r = i / QB, c = i % QB;
+    const float v = to_f32(src[(size_t)r * N + c]);
+    blk[r][c] = v;
+    lo = fminf(lo, v);
+    hi = fmaxf(hi, v);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if (lane == 0) { s_lo[warp] = lo; s_hi[warp] = hi; }
+  __syncthreads();
+  lo = s_lo[0];
+  hi = s_hi[0];
+  for (int i = 1; i < kWarps; ++i) { lo = fminf(lo, s_lo[i]); hi = fmaxf(hi, s_hi[i]); }
+  const float scale = __fdiv_rn(__fsub_rn(hi, lo), levels);
+  if (tid == 0) sm[((size_t)e * nbi + bi) * nbj + bj] = make_float2(scale, lo);
+  auto code = [&](int r, int c) -> uint32_t {
+    if (!(scale > 0.f)) return 0u;
+    return (uint32_t)rintf(__fdiv_rn(__fsub_rn(blk[r][c], lo), scale));
+  };
+  constexpr int tiles = (QB / KT) * (QB / 8);  // 128 (INT4) or 256 (INT8)
+  for (int t = tid; t < tiles; t += 256) {
+    const int kgl = t / (QB / 8), ngl = t % (QB / 8);
+    uint32_t word[4];
+    if (BITS == 4) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t v = 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v |= code(kgl * KT + j, ngl * 8 + c) << (4 * c);
+        word[j] = v;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v = 0;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) v |= code(kgl * KT + j, ngl * 8 + 4 * h + c) << (8 * c);
+          word[2 * j + h] = v;
+        }
+    }
+    const size_t kg = (size_t)bi * (QB / KT) + kgl, ng = (size_t)bj * (QB / 8) + ngl;
+    codes[((size_t)e * (K / KT) + kg) * (N / 8) + ng] = make_uint4(word[0], word[1], word[2], word[3]);
+  }
+}
+
+// ------------------------------------------------------------------ streaming FFN
+// Codes of the 8 columns of one k-row, as exact floats 0 .. 2^bits - 1.
+__device__ __forceinline__ void int4_row(uint32_t wd, float (&c)[8]) {
+  const uint32_t even = wd & 0x0F0F0F0Fu;         // columns 0, 2, 4, 6 in bytes 0..3
+  const uint32_t odd = (wd >> 4) & 0x0F0F0F0Fu;   // columns 1, 3, 5, 7
+  c[0] = __uint_as_float(__byte_perm(even, 0x4B000000u, 0x7540)) - kMagic;
+  c[2] = __uint_as_float(__byte_perm(even, 0x4B000000u, 0x7541)) - kMagic;
+  c[4] = __uint_as_float(__byte_perm(even, 0x4B000000u, 0x7542)) - kMagic;
+  c[6] = __uint_as_float(__byte_perm(even, 0x4B000000u, 0x7543)) - kMagic;
+  c[1] = __uint_as_float(__byte_perm(odd, 0x4B000000u, 0x7540)) - kMagic;
+  c[3] = __uint_as_float(__byte_perm(odd, 0x4B000000u, 0x7541)) - kMagic;
+  c[5] = __uint_as_float(__byte_perm(odd, 0x4B000000u, 0x7542)) - kMagic;
+  c[7] = __uint_as_float(__byte_perm(odd, 0x4B000000u, 0x7543)) - kMagic;
+}
+__device__ __forceinline__ void int8_row(uint32_t w0, uint32_t w1, float (&c)[8]) {
+  c[0] = __uint_as_float(__byte_perm(w0, 0x4B000000u, 0x7540)) - kMagic;
+  c[1] = __uint_as_float(__byte_perm(w0, 0x4B000000u, 0x7541)) - kMagic;
+  c[2] = __uint_as_float(__byte_perm(w0, 0x4B000000u, 0x7542)) - kMagic;
+  c[3] = __uint_as_float(__byte_perm(w0, 0x4B000000u, 0x7543)) - kMagic;
+  c[4] = __uint_as_float(__byte_perm(w1, 0x4B000000u, 0x7540)) - kMagic;
+  c[5] = __uint_as_float(__byte_perm(w1, 0x4B000000u, 0x7541)) - kMagic;
+  c[6] = __uint_as_float(__byte_perm(w1, 0x4B000000u, 0x7542)) - kMagic;
+  c[7] = __uint_as_float(__byte_perm(w1, 0x4B000000u, 0x7543)) - kMagic;
+}
+
+template <int BITS, int STAGE, typename OutT, int RMAX>
+__global__ void __launch_bounds__(kThreads, 2)
+ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const uint4* __restrict__ codes,
+                    const float2* __restrict__ sm, const int32_t* __restrict__ offsets,
+                    const float* __restrict__ row_gate, int K, int N, int E, OutT* __restrict__ out) {
+  constexpr int KT = 16 / BITS;  // k-rows per tile: 128 bits / (8 columns x BITS)
+  static_assert(KT * 8 * BITS == 128 && (BITS == 4 ? KT == 4 : KT == 2), "tile words hold KT k-rows");
+  extern __shared__ __align__(16) float smem[];
+  float* sA = smem;                                     // [RMAX][KC]
+  float* sRed = sA + RMAX * KC;                         // [kWarps][RMAX][NS]
+  float2* sSM = reinterpret_cast<float2*>(sRed + kWarps * RMAX * NS);  // [K / 64] this slab's blocks
+  int* sAct = reinterpret_cast<int*>(sSM + K / QB);     // [E] experts with rows
+  __shared__ int s_nact;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_launch_dependents();
+  griddep_wait();
+
+  if (warp == 0) {
+    int base = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const bool act = e < E && offsets[e + 1] > offsets[e];
+      const unsigned m = __ballot_sync(0xffffffffu, act);
+      if (act) sAct[base + __popc(m & ((1u << lane) - 1u))] = e;
+      base += __popc(m);
+    }
+    if (lane == 0) s_nact = base;
+  }
+  __syncthreads();
+  const int nslab = N / NS;
+  const int units = s_nact * nslab;
+  const int kr = lane / LPR;  // tile row of this lane within the warp's group of RPW
+  const int cg = lane % LPR;  // 8-column group of this lane
+  const int KG = K / KT, NG = N / 8, NB = N / QB;
+
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int e = sAct[u / nslab];
+    const int slab = u % nslab;
+    const int n0 = slab * NS;
+    const uint4* ce = codes + (size_t)e * KG * NG + (size_t)slab * LPR + cg;
+    __syncthreads();  // the previous unit is done with sSM
+    for (int b = tid; b < K / QB; b += kThreads) sSM[b] = sm[((size_t)e * (K / QB) + b) * NB + slab];
+    const int r_begin = offsets[e], r_end = offsets[e + 1];
+    for (int rp = r_begin; rp < r_end; rp += RMAX) {
+      const int R = min(RMAX, r_end - rp);
+      float acc[RMAX][8], accm[RMAX];
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) {
+        accm[r] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+      }
+      for (int kc = 0; kc < K; kc += KC) {
+        const int kn = min(KC, K - kc);  // a multiple of 64
+        const int gn = kn / KT;          // tile rows in this chunk
+        __syncthreads();
+        for (int i = tid; i < R * KC; i += kThreads) {
+          const int r = i / KC, kk = i % KC;
+          sA[i] = kk < kn ? __bfloat162float(a[(size_t)(rp + r) * K + kc + kk]) : 0.f;
+        }
+        __syncthreads();
+        auto load_batch = [&](int g0, uint4 (&t)[kUnroll]) {
+#pragma unroll
+          for (int i = 0; i < kUnroll; ++i) {
+            const int g = g0 + i * GSTEP + warp * RPW + kr;
+            t[i] = g < gn ? __ldg(ce + (size_t)(kc / KT + g) * NG) : make_uint4(0u, 0u, 0u, 0u);
+          }
+        };
+        uint4 cur[kUnroll], nxt[kUnroll];
+        load_batch(0, cur);
+        for (int g0 = 0; g0 < gn; g0 += GSTEP * kUnroll) {
+          if (g0 + GSTEP * kUnroll < gn) load_batch(g0 + GSTEP * kUnroll, nxt);
+#pragma unroll
+          for (int i = 0; i < kUnroll; ++i) {
+            const int g = g0 + i * GSTEP + warp * RPW + kr;
+            if (g >= gn) break;
+            const int k0 = g * KT;  // first k-row of the tile within the chunk
+            const float2 q = sSM[(kc + k0) / QB];
+            const uint32_t wd[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
+#pragma unroll
+            for (int j = 0; j < KT; ++j) {
+              float cf[8];
+              if (BITS == 4) int4_row(wd[j], cf);
+              else int8_row(wd[2 * j], wd[2 * j + 1], cf);
+#pragma unroll
+              for (int r = 0; r < RMAX; ++r) {
+                if (r >= R) break;
+                const float av = sA[r * KC + k0 + j];
+                const float as = av * q.x;
+                accm[r] = fmaf(av, q.y, accm[r]);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(as, cf[c], acc[r][c]);
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < kUnroll; ++i) cur[i] = nxt[i];
+        }
+      }
+      // Fold the column-independent min term in, then combine the warp's RPW tile rows (lanes cg,
+      // cg+8, cg+16, cg+24) and the warps, in fixed orders.
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          float v = acc[r][c] + accm[r];
+          v += __shfl_xor_sync(0xffffffffu, v, LPR);
+          v += __shfl_xor_sync(0xffffffffu, v, 2 * LPR);
+          acc[r][c] = v;
+        }
+      if (lane < LPR) {
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) sRed[(warp * RMAX + r) * NS + cg * 8 + c] = acc[r][c];
+      }
+      __syncthreads();
+      for (int i = tid; i < R * NS; i += kThreads) {
+        const int r = i / NS, c = i % NS;
+        float v = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < kWarps; ++wi) v += sRed[(wi * RMAX + r) * NS + c];
+        const int grow = rp + r;
+        v = STAGE == 1 ? gelu_as(v) : row_gate[grow] * v;
+        out[(size_t)grow * N + n0 + c] = from_f32<OutT>(v);
+      }
+    }
+  }
+}
+
+template <int BITS, int STAGE, typename OutT, int RMAX>
+cudaError_t launch_q(const QFfnArgs& p, cudaStream_t s) {
+  const size_t smem = (size_t)(RMAX * KC + kWarps * RMAX * NS) * sizeof(float) +
+                      (size_t)(p.K / QB) * sizeof(float2) + (size_t)p.E * sizeof(int);
+  auto kern = ffn_stream_q_kernel<BITS, STAGE, OutT, RMAX>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int nslab = p.N / NS;
+  const long long max_units = (long long)(p.rows < p.E ? p.rows : p.E) * nslab;
+  long long grid = (long long)device_sm_count() * (RMAX <= 2 ? 8 : 4);
+  if (grid > max_units) grid = max_units;
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, (const __nv_bfloat16*)p.a,
+                    (const uint4*)p.codes, (const float2*)p.scale_min, p.offsets, p.row_gate, p.K, p.N, p.E,
+                    (OutT*)p.out);
+}
+
+template <int BITS>
+cudaError_t launch_q_bits(const QFfnArgs& p, cudaStream_t s) {
+  if (p.rows <= 32)
+    return p.stage == 1 ? launch_q<BITS, 1, __nv_bfloat16, 2>(p, s) : launch_q<BITS, 2, float, 2>(p, s);
+  return p.stage == 1 ? launch_q<BITS, 1, __nv_bfloat16, 4>(p, s) : launch_q<BITS, 2, float, 4>(p, s);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const void* w, int K, int N, int E, int dt, int bits, void* codes, float* scale_min,
+                            cudaStream_t s) {
+  const long long blocks = (long long)E * (K / QB) * (N / QB);
+  if (blocks == 0) return cudaSuccess;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)blocks);
+  if (dt == MOE_DTYPE_BF16) {
+    if (bits == 4)
+      quantize_kernel<__nv_bfloat16, 4><<<grid, 256, 0, s>>>((const __nv_bfloat16*)w, K, N, (uint4*)codes,
+                                                             (float2*)scale_min);
+    else
+      quantize_kernel<__nv_bfloat16, 8><<<grid, 256, 0, s>>>((const __nv_bfloat16*)w, K, N, (uint4*)codes,
+                                                             (float2*)scale_min);
+  } else {
+    if (bits == 4)
+      quantize_kernel<float, 4><<<grid, 256, 0, s>>>((const float*)w, K, N, (uint4*)codes, (float2*)scale_min);
+    else
+      quantize_kernel<float, 8><<<grid, 256, 0, s>>>((const float*)w, K, N, (uint4*)codes, (float2*)scale_min);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ffn_stream_q(const QFfnArgs& p, cudaStream_t s) {
+  if (p.rows == 0) return cudaSuccess;
+  return p.bits == 4 ? launch_q_bits<4>(p, s) : launch_q_bits<8>(p, s);
+}
+
+}  // namespace moe

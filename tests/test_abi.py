@@ -100,3 +100,23 @@ def test_capacity_helper_matches_oracle():
         assert moe.capacity(T, k, E, cf) == oracle.capacity(T, k, E, cf)
     assert moe.capacity(16, 2, 4, 0.0) == -1
     assert moe.capacity(16, 0, 4, 1.0) == -1
+
+
+def test_graph_handles_rejected_without_gpu():
+    lib = _lib.lib()
+    assert lib.moe_graph_launch(None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_graph_destroy(None) == moe.MOE_OK
+    assert lib.moe_forward_graph_create(*([None] * 5), 4, 64, 64, 8, 2, 1, 1, 0, 0, 0, *([None] * 6), 0,
+                                        None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_quantised_sizes_without_gpu():
+    lib = _lib.lib()
+    assert moe.qweight_bytes(8192, 8192, 128, 4) == 128 * 8192 * 8192 // 2
+    assert moe.qweight_bytes(8192, 8192, 128, 8) == 128 * 8192 * 8192
+    assert moe.qscale_bytes(1024, 4096, 16) == 16 * 16 * 64 * 8
+    assert moe.qweight_bytes(100, 64, 2, 4) == 0 and moe.qweight_bytes(64, 64, 2, 3) == 0
+    FAKE = 4096
+    assert lib.moe_quantize_weights(FAKE, 64, 64, 1, 1, 5, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_graph_capture_begin(None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_graph_capture_end(None, None) == moe.MOE_ERR_INVALID_ARG
