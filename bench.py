@@ -56,6 +56,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     p.add_argument("--weight-bits", type=int, default=0, choices=[0, 4, 8],
                    help="0: the bf16 layer; 4 / 8: expert weights block-quantised to INT4 / INT8 (bf16 layers)")
+    p.add_argument("--ffn-path", default="auto", choices=["auto", "tensor", "stream", "simt", "pair", "tensor_t"],
+                   help="expert FFN kernel family (moe_path); auto = the library's own choice")
     p.add_argument("--launch", default="graph", choices=["graph", "direct"],
                    help="graph: replay a CUDA graph of the layer per step; direct: one C ABI call per kernel")
     return p.parse_args()
@@ -152,7 +154,7 @@ class ClockSampler:
     """nvidia-smi samples (host-stamped) of SM clock and throttle reasons while the GPU works."""
     FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
-              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap", "clocks.mem"]
 
     def __init__(self, gpu_index):
         self.samples = []
@@ -204,7 +206,9 @@ class ClockSampler:
             for name, v in zip(names, p[4:8]):
                 if v.strip().lower() == "active":
                     reasons.add(name)
+        mem = [num(p[8]) for p in win if num(p[8]) is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(win[0][1]),
+                "mem_mhz": statistics.median(mem) if mem else None,
                 "power_w_max": max((num(p[2]) or 0.0) for p in win), "reasons": sorted(reasons),
                 "samples": len(win), "window": window}
 
@@ -290,6 +294,8 @@ def run_ours(args, w, rank, world, device):
     stream = torch.cuda.current_stream()
 
     qbits = args.weight_bits
+    fpath = {"auto": moe.PATH_AUTO, "tensor": moe.PATH_TENSOR, "stream": moe.PATH_STREAM, "simt": moe.PATH_SIMT,
+             "pair": moe.PATH_TENSOR_PAIR, "tensor_t": moe.PATH_TENSOR_T}[args.ffn_path]
     q1 = q2 = None
     if qbits:
         if dt != 1:
@@ -301,7 +307,7 @@ def run_ours(args, w, rank, world, device):
         if qbits:
             moe.forward_q(x, w_r, b_r, q1, q2, T, d, F, E, k, qbits, out, ws, stream=s)
         else:
-            moe.forward(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws, stream=s)
+            moe.forward(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws, path=fpath, stream=s)
 
     graph = None
     if args.launch == "graph":
@@ -380,12 +386,12 @@ def run_ours(args, w, rank, world, device):
         if qbits:
             moe.expert_up_q(x_perm, q1[0], q1[1], offsets, T, d, F, E, k, qbits, h)
         else:
-            moe.expert_up(x_perm, w1, offsets, T, d, F, E, k, dt, h, ws)
+            moe.expert_up(x_perm, w1, offsets, T, d, F, E, k, dt, h, ws, path=fpath)
         e[3].record(stream)
         if qbits:
             moe.expert_down_q(h, q2[0], q2[1], offsets, row_gate, T, d, F, E, k, qbits, y_perm)
         else:
-            moe.expert_down(h, w2, offsets, row_gate, T, d, F, E, k, dt, y_perm, ws)
+            moe.expert_down(h, w2, offsets, row_gate, T, d, F, E, k, dt, y_perm, ws, path=fpath)
         e[4].record(stream)
         moe.combine(y_perm, row_of, T, d, k, dt, out)
         e[5].record(stream)
@@ -396,7 +402,7 @@ def run_ours(args, w, rank, world, device):
     touched = int((counts_h > 0).sum())
 
     # --- e2e: public layer object, pinned host tokens in, output back to the host, every step
-    layer = moe.MoELayer(w_r, w1, w2, k=k, b_r=b_r, weight_bits=qbits or None)
+    layer = moe.MoELayer(w_r, w1, w2, k=k, b_r=b_r, path=fpath, weight_bits=qbits or None)
     x_host = x.cpu().pin_memory()
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     x_dev = torch.empty_like(x)
@@ -435,7 +441,7 @@ def run_ours(args, w, rank, world, device):
     peaks, peak_src = load_peaks()
     eb = 2 if dt == 1 else 4
     dom = max(["expert_up", "expert_down"], key=lambda n: kern_ms[n])
-    stream_path = dt == 1 and A <= 256  # the library's automatic choice (include/moe.h, moe_path)
+    stream_path = fpath == moe.PATH_STREAM or (fpath == moe.PATH_AUTO and dt == 1 and A <= 256)  # include/moe.h
     if qbits:
         # quantised weight streaming: codes + (scale, min) of the touched experts + rows in and out
         K_, N_ = (d, F) if dom == "expert_up" else (F, d)
@@ -465,9 +471,11 @@ def run_ours(args, w, rank, world, device):
         alg_flops = 2.0 * A * d * F
         achieved = alg_flops / (kern_ms[dom] / 1e3) / 1e12
         peak = peaks["bf16_tflops"]
-        roof = {"kernel": f"ffn_tc_kernel ({dom})", "bound": "tensor", "achieved": achieved, "peak": peak,
+        kname = {moe.PATH_TENSOR_PAIR: "ffn_tc2_kernel", moe.PATH_TENSOR_T: "ffn_tct_kernel"}.get(fpath, "ffn_tc_kernel")
+        roof = {"kernel": f"{kname} ({dom})", "bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": stored_traffic(f"ffn_tc_kernel<{1 if dom == 'expert_up' else 2}>", w.name, TC_SOURCES),
+                "traffic": (stored_traffic(f"ffn_tc_kernel<{1 if dom == 'expert_up' else 2}>", w.name, TC_SOURCES)
+                            if kname == "ffn_tc_kernel" else None),
                 "alg_flops_per_launch": alg_flops, "ms_per_launch": kern_ms[dom],
                 "peak_source": f"{peak_src} bf16_tflops (burst: the kernel runs in a short step)"}
 
@@ -478,6 +486,7 @@ def run_ours(args, w, rank, world, device):
         "config": dict(workload_config(w), parallelism=f"replicas x{world}" if world > 1 else "single GPU",
                        weights=(f"INT{qbits} codes, 64x64 blocks with fp32 (scale, min), quantised once before "
                                 "timing" if qbits else "bf16" if dt == 1 else "fp32"),
+                       ffn_path=args.ffn_path,
                        launch=("CUDA graph of the layer's kernels (moe_forward_graph_create), one graph launch "
                                "per step" if graph is not None else "one C ABI call per kernel")),
         "ms_per_step_direct_calls": ms_direct,

@@ -63,7 +63,9 @@ typedef enum {
   MOE_PATH_TENSOR = 1,      /* tcgen05/TMEM grouped GEMM fed by TMA, 128x256 tiles per CTA (bf16 only) */
   MOE_PATH_STREAM = 2,      /* weight-streaming column-slab kernel for few rows per expert (bf16 only) */
   MOE_PATH_SIMT = 3,        /* CUDA-core tiled grouped GEMM (fp32 and bf16) */
-  MOE_PATH_TENSOR_PAIR = 4  /* tcgen05 cta_group::2 on CTA pairs, 256x256 tiles (bf16 only) */
+  MOE_PATH_TENSOR_PAIR = 4, /* tcgen05 cta_group::2 on CTA pairs, 256x256 tiles (bf16 only) */
+  MOE_PATH_TENSOR_T = 5     /* tcgen05 cta_group::2 with the product transposed: 256 output features x
+                               up to 256 rows per pair tile, rows rounded up to 16 (bf16 only) */
 } moe_path;
 
 /* ---------------------------------------------------------------------------------------------

@@ -23,7 +23,7 @@ MOE_ERR_DEVICE_TIMEOUT = 5
 MOE_DTYPE_F32 = 0
 MOE_DTYPE_BF16 = 1
 
-PATH_AUTO, PATH_TENSOR, PATH_STREAM, PATH_SIMT, PATH_TENSOR_PAIR = 0, 1, 2, 3, 4
+PATH_AUTO, PATH_TENSOR, PATH_STREAM, PATH_SIMT, PATH_TENSOR_PAIR, PATH_TENSOR_T = 0, 1, 2, 3, 4, 5
 GATES_RENORMALISE = 1
 
 _p = ctypes.c_void_p

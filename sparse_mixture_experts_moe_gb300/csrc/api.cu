@@ -91,18 +91,20 @@ moe_path resolve_path(moe_path path, int dt, int rows, int E) {
 
 bool path_ok(moe_path path, int dt) {
   (void)dt;
-  return path >= MOE_PATH_AUTO && path <= MOE_PATH_TENSOR_PAIR;
+  return path >= MOE_PATH_AUTO && path <= MOE_PATH_TENSOR_T;
 }
 
 moe_status run_ffn_half(moe_path path, FfnArgs& args, cudaStream_t s) {
   path = resolve_path(path, args.dt, args.rows, args.E);
-  if ((path == MOE_PATH_TENSOR || path == MOE_PATH_STREAM || path == MOE_PATH_TENSOR_PAIR) &&
+  if ((path == MOE_PATH_TENSOR || path == MOE_PATH_STREAM || path == MOE_PATH_TENSOR_PAIR ||
+       path == MOE_PATH_TENSOR_T) &&
       args.dt != MOE_DTYPE_BF16)
     return MOE_ERR_UNSUPPORTED;
   cudaError_t e;
   switch (path) {
     case MOE_PATH_TENSOR: e = launch_ffn_tensor(args, s); break;
     case MOE_PATH_TENSOR_PAIR: e = launch_ffn_tensor_pair(args, s); break;
+    case MOE_PATH_TENSOR_T: e = launch_ffn_tensor_t(args, s); break;
     case MOE_PATH_STREAM: e = launch_ffn_stream(args, s); break;
     default: e = launch_ffn_simt(args, s); break;
   }

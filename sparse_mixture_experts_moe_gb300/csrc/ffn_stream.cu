@@ -25,11 +25,32 @@ constexpr int LPR = NS / 8;       // lanes per k-row: 8 (16 bytes each)
 constexpr int RPW = 32 / LPR;     // k-rows per warp per step: 4
 constexpr int KSTEP = kWarps * RPW;  // k-rows per CTA step: 32
 constexpr int KC = 1024;          // k-depth staged per chunk
-constexpr int kUnroll = 8;
+// Weight loads per thread per batch (two batches in flight): 8 with 2 rows a pass; with 4 rows
+// the accumulators take the registers, and 8 would spill.
+template <int RMAX>
+constexpr int unroll_for() { return RMAX <= 2 ? 8 : 6; }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
   v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
   v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
+}
+
+// Rows rp .. rp+R-1, k-range [kc, kc+kn) of the bf16 activations -> sA as fp32 (row stride KC),
+// with 16-byte loads; K and kn are multiples of 8 and the rows 16-byte aligned.
+__device__ __forceinline__ void stage_rows(const __nv_bfloat16* __restrict__ a, int K, int rp, int R, int kc, int kn,
+                                           float* sA) {
+  const int per_row = KC / 8;
+  for (int i = threadIdx.x; i < R * per_row; i += kThreads) {
+    const int r = i / per_row, kk = (i % per_row) * 8;
+    float v[8];
+    if (kk < kn) bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(a + (size_t)(rp + r) * K + kc + kk)), v);
+    else
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.f;
+    float4* dst = reinterpret_cast<float4*>(sA + r * KC + kk);
+    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
 }
 
 // up (STAGE 1) writes bf16 h; down (STAGE 2) writes fp32 y_perm.
@@ -39,6 +60,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ w,
                   const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
                   OutT* __restrict__ out) {
+  constexpr int kUnroll = unroll_for<RMAX>();
   extern __shared__ __align__(16) float smem[];
   float* sA = smem;                         // [RMAX][KC]
   float* sRed = sA + RMAX * KC;             // [kWarps][RMAX][NS]
@@ -74,22 +96,17 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __re
     const int r_begin = offsets[e], r_end = offsets[e + 1];
     for (int rp = r_begin; rp < r_end; rp += RMAX) {
       const int R = min(RMAX, r_end - rp);
-      float acc[RMAX][8];
+      uint64_t acc2[RMAX][4];  // column pairs (2p, 2p+1) of each row, fp32x2
 #pragma unroll
       for (int r = 0; r < RMAX; ++r)
 #pragma unroll
-        for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+        for (int p = 0; p < 4; ++p) acc2[r][p] = 0ull;
 
       for (int kc = 0; kc < K; kc += KC) {
         const int kn = min(KC, K - kc);
-        __syncthreads();
-        for (int i = tid; i < R * KC; i += kThreads) {
-          const int r = i / KC, kk = i % KC;
-          sA[i] = kk < kn ? __bfloat162float(a[(size_t)(rp + r) * K + kc + kk]) : 0.f;
-        }
-        __syncthreads();
         // Software-pipelined: the next batch of kUnroll weight loads is issued before the
-        // current batch is consumed, so two batches per thread are in flight.
+        // current batch is consumed, so two batches per thread are in flight. The first batch
+        // goes out before the activations are staged, so staging overlaps the weight stream.
         auto load_batch = [&](int k0, uint4 (&wv)[kUnroll]) {
 #pragma unroll
           for (int i = 0; i < kUnroll; ++i) {
@@ -102,20 +119,27 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __re
         };
         uint4 cur[kUnroll], nxt[kUnroll];
         load_batch(0, cur);
+        __syncthreads();
+        stage_rows(a, K, rp, R, kc, kn, sA);
+        __syncthreads();
         for (int k0 = 0; k0 < kn; k0 += KSTEP * kUnroll) {
           if (k0 + KSTEP * kUnroll < kn) load_batch(k0 + KSTEP * kUnroll, nxt);
 #pragma unroll
           for (int i = 0; i < kUnroll; ++i) {
             const int kk = k0 + i * KSTEP + warp * RPW + kr;
             if (kk >= kn) break;
-            float wf[8];
-            bf16x8_to_f32(cur[i], wf);
+            // bf16 pair (lo, hi) of each 32-bit word -> two fp32 in one 64-bit register
+            const uint32_t wv[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
+            uint64_t w2[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) w2[p] = ((uint64_t)(wv[p] & 0xFFFF0000u) << 32) | (uint64_t)(wv[p] << 16);
 #pragma unroll
             for (int r = 0; r < RMAX; ++r) {
               if (r >= R) break;
               const float av = sA[r * KC + kk];
+              const uint64_t av2 = f2_pack(av, av);
 #pragma unroll
-              for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(av, wf[c], acc[r][c]);
+              for (int p = 0; p < 4; ++p) acc2[r][p] = ffma2(av2, w2[p], acc2[r][p]);
             }
           }
 #pragma unroll
@@ -123,11 +147,12 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __re
         }
       }
       // Combine the RPW k-row groups of the warp (lanes cg, cg+8, cg+16, cg+24), then the warps.
+      float acc[RMAX][8];
 #pragma unroll
       for (int r = 0; r < RMAX; ++r)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          float v = acc[r][c];
+          float v = c & 1 ? f2_hi(acc2[r][c >> 1]) : f2_lo(acc2[r][c >> 1]);
           v += __shfl_xor_sync(0xffffffffu, v, LPR);
           v += __shfl_xor_sync(0xffffffffu, v, 2 * LPR);
           acc[r][c] = v;

@@ -1,0 +1,334 @@
+// Grouped expert GEMM on CTA pairs with the product transposed: D^T = W^T x^T.
+// Same math and epilogues as ffn_tc.cu (csdn/6a462027 §3.2 and §4.2 step 6; gate:
+// csdn/6a919c0d §2.2 step 4):
+//   up   (stage 1): h[r]      = GeLU(x_perm[r] W1[e])            (bf16 out)
+//   down (stage 2): y_perm[r] = row_gate[r] * (h[r] W2[e])        (fp32 out)
+//
+// Why transposed: an expert's routed rows are a ragged count, the output features are not
+// (d_ff and d are multiples of 256 in every workload). With the features on the MMA's M side
+// (256 per CTA pair, 128 per CTA, from the weights stored N-contiguous: an MN-major A operand)
+// and the rows on its N side (K-major B operand from x_perm), a tile covers up to 256 rows and
+// its N is the row count rounded up to 16. An expert's last tile therefore wastes at most 15
+// rows, where a 256-row M tile wastes up to 255. Per CTA and 64-deep k-block the loads are
+// 16 KB of weights + 16 KB of rows (32 KB, against 48 KB for one-CTA 128x256 tiles), so six or
+// seven stages fit in shared memory.
+//
+// Roles (both CTAs run 10 warps):
+//   warp 0      TMA producer of this CTA's halves (128 features of W, up to 128 rows of x);
+//               the loads complete on the leader CTA's "full" barrier
+//   warp 1      TMEM allocation for the pair; in the leader also the MMA issuer
+//               (tcgen05.mma.cta_group::2, M = 256, N = rows of the tile)
+//   warps 2..9  epilogue: TMEM lane = output feature, TMEM column = row; each warp takes 32
+//               features x half of the tile's rows and stores 32 consecutive features of a row
+//               per instruction (coalesced), then arrives on the leader's "accumulator empty"
+// All waits are bounded; on a timeout the CTA records MOE_ERR_DEVICE_TIMEOUT and unwinds.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BF = 256;                           // features per pair tile (MMA M)
+constexpr int BR = 256;                           // rows per tile at most (MMA N)
+constexpr int BK = 64;
+constexpr int kTileASubBytes = BK * 64 * 2;       // 8 KB: 64 k-rows x 64 features
+constexpr int kTileABytes = 2 * kTileASubBytes;   // 16 KB: this CTA's 128 features
+constexpr int kTileBBytes = (BR / 2) * BK * 2;    // 16 KB: up to 128 rows of this CTA's half
+constexpr int kStageBytes = kTileABytes + kTileBBytes;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr uint32_t kTmemCols = 2 * BR;            // two accumulators of up to 256 columns
+constexpr int kMaxSmem = 232448;
+
+__host__ __device__ constexpr int num_bars(int nst) { return 2 * nst + 5; }
+__host__ __device__ constexpr size_t smem_bytes_for(int E, int nst) {
+  return 1024 + (size_t)nst * kStageBytes + 8 * num_bars(nst) + 16 + 4 * (size_t)(E + 1);
+}
+
+// kind::f16, bf16 A and B, fp32 D, A MN-major (bit 15), B K-major, N >> 3 at 17, M >> 4 at 24.
+__host__ __device__ constexpr uint32_t idesc_tn(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+struct Item {
+  int e, row0, nrows, f0;
+};
+
+// Item w of the list (expert, 256-feature block, 256-row tile), row tile fastest: the pairs that
+// run at the same time share a weight slab (read once from HBM, then from L2).
+__device__ __forceinline__ Item decode_item(int w, const int* P, int E, int NB, const int32_t* offsets) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P[mid] * NB <= w) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int mt = P[e + 1] - P[e];
+  const int r = w - P[e] * NB;
+  Item it;
+  it.e = e;
+  it.row0 = offsets[e] + (r % mt) * BR;
+  it.nrows = min(BR, offsets[e + 1] - it.row0);
+  it.f0 = (r / mt) * BF;
+  return it;
+}
+
+template <int STAGE>
+struct EpiOut { using T = __nv_bfloat16; };
+template <>
+struct EpiOut<2> { using T = float; };
+
+template <int STAGE, int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+               typename EpiOut<STAGE>::T* __restrict__ out, const int32_t* __restrict__ offsets,
+               const float* __restrict__ row_gate, int K, int N, int E, int* status, uint64_t timeout_ns) {
+  using OutT = typename EpiOut<STAGE>::T;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA = base;                          // weights: [stage][2 sub-boxes][64 k][64 f]
+  const uint32_t sB = base + STAGES * kTileABytes;   // rows:    [stage][128 rows][64 k]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + num_bars(STAGES));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* P = reinterpret_cast<int*>(tmem_slot + 4);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
+  const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, TEMPTY = 2 * STAGES + 2, DONE = 2 * STAGES + 4;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) { mbar_init(bar(FULL + s), 1); mbar_init(bar(EMPTY + s), 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(bar(TFULL + a), 1); mbar_init(bar(TEMPTY + a), 2 * kEpiWarps); }
+    mbar_init(bar(DONE), 1);
+    fence_mbar_init();
+    *abort_flag = 0;
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  griddep_launch_dependents();
+  griddep_wait();
+  if (warp == 2) {
+    int run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      int mt = 0;
+      if (e < E) {
+        const int cnt = offsets[e + 1] - offsets[e];
+        mt = cnt > 0 ? (cnt + BR - 1) / BR : 0;
+      }
+      int incl = mt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < E) P[e] = run + incl - mt;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) P[E] = run;
+  }
+  // Both CTAs' barriers must be initialised before any signal crosses to the peer.
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int NB = (N + BF - 1) / BF;
+  const int KB = (K + BK - 1) / BK;
+  const int total_items = P[E] * NB;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0, filled = 0, fill_phase = 0;
+      for (int w = pair; w < total_items && !*abort_flag; w += npairs) {
+        const Item it = decode_item(w, P, E, NB, offsets);
+        const int nt = (it.nrows + 15) & ~15;           // MMA N: rows rounded up to 16
+        const int frow = it.row0 + (nt / 2) * (int)rank;  // this CTA holds rows [nt/2 * rank, +nt/2)
+        const int feat = it.f0 + (BF / 2) * (int)rank;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_or_abort(bar(EMPTY + stage), phase ^ 1u, timeout_ns, abort_flag, status, 41)) goto producer_out;
+          const uint32_t full_leader = map_to_cta(bar(FULL + stage), 0);
+          if (leader) mbar_arrive_expect_tx(bar(FULL + stage), 2 * kStageBytes);
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            tma_load_3d_pair(sA + stage * kTileABytes + j * kTileASubBytes, &tmW, feat + 64 * j, kb * BK, it.e,
+                             full_leader);
+          tma_load_2d_pair(sB + stage * kTileBBytes, &tmX, kb * BK, frow, full_leader);
+          filled |= 1u << stage;
+          fill_phase = (fill_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+    producer_out:
+      // Copies in flight must land before shared memory goes away: the leader waits for the phases
+      // it armed (they count both CTAs' bytes); the peer waits until the MMAs released its last fills.
+      for (int s = 0; s < STAGES; ++s) {
+        if (!(filled & (1u << s))) continue;
+        const uint32_t ph = (fill_phase >> s) & 1u;
+        if (leader) mbar_wait_bounded(bar(FULL + s), ph, timeout_ns);
+        else mbar_wait_bounded(bar(EMPTY + s), ph, timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      if (leader) {
+        // ---------------------------------------------------------- MMA issuer (leader only)
+        int stage = 0, acc = 0;
+        uint32_t phase = 0, acc_phase = 0;
+        for (int w = pair; w < total_items && !*abort_flag; w += npairs) {
+          const Item it = decode_item(w, P, E, NB, offsets);
+          const uint32_t idesc = idesc_tn(BF, (it.nrows + 15) & ~15);
+          if (!wait_or_abort(bar(TEMPTY + acc), acc_phase ^ 1u, timeout_ns, abort_flag, status, 42)) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BR);
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!wait_or_abort(bar(FULL + stage), phase, timeout_ns, abort_flag, status, 42)) goto mma_out;
+            tc_fence_after();
+            // A: MN-major, two 64-feature atoms 8 KB apart; B: K-major rows.
+            const uint64_t a_desc = make_smem_desc_sw128(sA + stage * kTileABytes, kTileASubBytes, 1024);
+            const uint64_t b_desc = make_smem_desc_sw128(sB + stage * kTileBBytes, 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              tc_mma_f16_pair(d_tmem, a_desc + (uint64_t)((kk * 16 * 128) >> 4), b_desc + (uint64_t)((kk * 32) >> 4),
+                              idesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_commit_pair(bar(EMPTY + stage), 0x3);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+          tc_commit_pair(bar(TFULL + acc), 0x3);
+          if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+      mma_out:
+        tc_commit_pair(bar(DONE), 0x3);
+      }
+      // Both CTAs: every MMA writing this CTA's TMEM has completed before TMEM is freed.
+      mbar_wait_bounded(bar(DONE), 0, timeout_ns);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (warps 2..9)
+    const int q = warp & 3;                              // TMEM lanes 32q .. 32q+31: features
+    const int c_begin = ((warp - 2) >> 2) * (BR / 2);    // this warp's half of the rows
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int w = pair; w < total_items && !*abort_flag; w += npairs) {
+      const Item it = decode_item(w, P, E, NB, offsets);
+      // warp-uniform: the TMEM loads below are warp-collective
+      if (!__all_sync(0xffffffffu, wait_or_abort(bar(TFULL + acc), acc_phase, timeout_ns, abort_flag, status, 43)))
+        break;
+      tc_fence_after();
+      const int f = it.f0 + (BF / 2) * (int)rank + 32 * q + lane;
+      const bool f_ok = f < N;
+      // 64 rows per step: two TMEM loads behind one wait, then the epilogue of all 64 values as
+      // independent chains (no per-row branch inside the arithmetic), then the guarded stores.
+      for (int c = c_begin; c < c_begin + BR / 2 && c < it.nrows; c += 64) {
+        const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BR + c);
+        uint32_t v[64];
+        tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld_wait();
+        const int nvalid = min(64, it.nrows - c);
+        const int r0 = it.row0 + c;
+        float res[64];
+        if (STAGE == 1) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) res[i] = gelu_as(__uint_as_float(v[i]));
+        } else {
+          const float g0 = lane < nvalid ? row_gate[r0 + lane] : 0.f;
+          const float g1 = lane + 32 < nvalid ? row_gate[r0 + 32 + lane] : 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            res[i] = __shfl_sync(0xffffffffu, g0, i) * __uint_as_float(v[i]);
+            res[32 + i] = __shfl_sync(0xffffffffu, g1, i) * __uint_as_float(v[32 + i]);
+          }
+        }
+        if (f_ok) {
+          OutT* dst = out + (size_t)r0 * N + f;
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i < nvalid) dst[(size_t)i * N] = from_f32<OutT>(res[i]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_cta(bar(TEMPTY + acc), 0));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  // No signal may target a CTA that has left, and no MMA may still write TMEM being freed.
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+template <int STAGE, int STAGES>
+cudaError_t launch_tct(const FfnArgs& p, const CUtensorMap& tmX, const CUtensorMap& tmW, size_t smem,
+                       cudaStream_t s) {
+  using OutT = typename EpiOut<STAGE>::T;
+  auto kern = ffn_tct_kernel<STAGE, STAGES>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  // Persistent: as many pairs as can be resident at once (two-SM clusters may not tile every SM).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(device_sm_count());
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0)
+    clusters = device_sm_count() / 2;
+  const int NB = (p.N + BF - 1) / BF;
+  const long long max_items = ((long long)(p.rows + BR - 1) / BR + p.E) * NB;
+  long long pairs = clusters < max_items ? clusters : max_items;
+  return launch_pdl(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), smem, s, tmX, tmW, (OutT*)p.out, p.offsets,
+                    p.row_gate, p.K, p.N, p.E, p.status, p.timeout_ns);
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_tensor_t(const FfnArgs& p, cudaStream_t s) {
+  if (p.rows == 0) return cudaSuccess;
+  if (p.dt != MOE_DTYPE_BF16) return cudaErrorNotSupported;
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  CUtensorMap tmX, tmW;
+  {
+    // rows of x_perm (or h): K-major B operand, 64 k x 128 rows per box
+    const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.rows};
+    const cuuint64_t str[1] = {(cuuint64_t)p.K * 2};
+    const cuuint32_t box[2] = {BK, BR / 2};
+    if (!encode_tmap(enc, &tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, 2, dims, str, box))
+      return cudaErrorInvalidValue;
+  }
+  {
+    // weights [E][K][N]: MN-major A operand, 64 features x 64 k per box
+    const cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.K, (cuuint64_t)p.E};
+    const cuuint64_t str[2] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.K * p.N * 2};
+    const cuuint32_t box[3] = {64, BK, 1};
+    if (!encode_tmap(enc, &tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.w, 3, dims, str, box))
+      return cudaErrorInvalidValue;
+  }
+  const bool seven = smem_bytes_for(p.E, 7) <= (size_t)kMaxSmem;
+  const size_t smem = smem_bytes_for(p.E, seven ? 7 : 6);
+  if (p.stage == 1)
+    return seven ? launch_tct<1, 7>(p, tmX, tmW, smem, s) : launch_tct<1, 6>(p, tmX, tmW, smem, s);
+  return seven ? launch_tct<2, 7>(p, tmX, tmW, smem, s) : launch_tct<2, 6>(p, tmX, tmW, smem, s);
+}
+
+}  // namespace moe

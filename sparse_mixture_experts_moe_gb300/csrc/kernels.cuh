@@ -91,6 +91,8 @@ cudaError_t launch_ffn_stream(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_ffn_tensor(const FfnArgs& a, cudaStream_t s);
 // CTA-pair version (cta_group::2, 256-row tiles) for experts with many rows.
 cudaError_t launch_ffn_tensor_pair(const FfnArgs& a, cudaStream_t s);
+// CTA-pair version with the product transposed (features on M, rows on N in steps of 16).
+cudaError_t launch_ffn_tensor_t(const FfnArgs& a, cudaStream_t s);
 
 cudaError_t launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s);
 

@@ -104,28 +104,43 @@ quantize_kernel(const T* __restrict__ w, int K, int N, uint4* __restrict__ codes
 }
 
 // ------------------------------------------------------------------ streaming FFN
-// Codes of the 8 columns of one k-row, as exact floats 0 .. 2^bits - 1.
-__device__ __forceinline__ void int4_row(uint32_t wd, float (&c)[8]) {
+// Codes of the 8 columns of one k-row as exact floats 0 .. 2^bits - 1, in column pairs
+// (2p, 2p+1) packed for the fp32x2 instructions: a byte permute places each code in the low
+// mantissa bits of 2^23, one packed subtraction removes the 2^23.
+__device__ __forceinline__ uint32_t magic_byte(uint32_t w, uint32_t sel) { return __byte_perm(w, 0x4B000000u, sel); }
+__device__ __forceinline__ void int4_row(uint32_t wd, uint64_t (&c)[4]) {
   const uint32_t even = wd & 0x0F0F0F0Fu;         // columns 0, 2, 4, 6 in bytes 0..3
   const uint32_t odd = (wd >> 4) & 0x0F0F0F0Fu;   // columns 1, 3, 5, 7
-  c[0] = __uint_as_float(__byte_perm(even, 0x4B000000u, 0x7540)) - kMagic;
-  c[2] = __uint_as_float(__byte_perm(even, 0x4B000000u, 0x7541)) - kMagic;
-  c[4] = __uint_as_float(__byte_perm(even, 0x4B000000u, 0x7542)) - kMagic;
-  c[6] = __uint_as_float(__byte_perm(even, 0x4B000000u, 0x7543)) - kMagic;
-  c[1] = __uint_as_float(__byte_perm(odd, 0x4B000000u, 0x7540)) - kMagic;
-  c[3] = __uint_as_float(__byte_perm(odd, 0x4B000000u, 0x7541)) - kMagic;
-  c[5] = __uint_as_float(__byte_perm(odd, 0x4B000000u, 0x7542)) - kMagic;
-  c[7] = __uint_as_float(__byte_perm(odd, 0x4B000000u, 0x7543)) - kMagic;
+  const uint64_t neg = f2_pack(-kMagic, -kMagic);
+#pragma unroll
+  for (int p = 0; p < 4; ++p)
+    c[p] = fadd2(((uint64_t)magic_byte(odd, 0x7540 + p) << 32) | magic_byte(even, 0x7540 + p), neg);
 }
-__device__ __forceinline__ void int8_row(uint32_t w0, uint32_t w1, float (&c)[8]) {
-  c[0] = __uint_as_float(__byte_perm(w0, 0x4B000000u, 0x7540)) - kMagic;
-  c[1] = __uint_as_float(__byte_perm(w0, 0x4B000000u, 0x7541)) - kMagic;
-  c[2] = __uint_as_float(__byte_perm(w0, 0x4B000000u, 0x7542)) - kMagic;
-  c[3] = __uint_as_float(__byte_perm(w0, 0x4B000000u, 0x7543)) - kMagic;
-  c[4] = __uint_as_float(__byte_perm(w1, 0x4B000000u, 0x7540)) - kMagic;
-  c[5] = __uint_as_float(__byte_perm(w1, 0x4B000000u, 0x7541)) - kMagic;
-  c[6] = __uint_as_float(__byte_perm(w1, 0x4B000000u, 0x7542)) - kMagic;
-  c[7] = __uint_as_float(__byte_perm(w1, 0x4B000000u, 0x7543)) - kMagic;
+__device__ __forceinline__ void int8_row(uint32_t w0, uint32_t w1, uint64_t (&c)[4]) {
+  const uint64_t neg = f2_pack(-kMagic, -kMagic);
+  c[0] = fadd2(((uint64_t)magic_byte(w0, 0x7541) << 32) | magic_byte(w0, 0x7540), neg);
+  c[1] = fadd2(((uint64_t)magic_byte(w0, 0x7543) << 32) | magic_byte(w0, 0x7542), neg);
+  c[2] = fadd2(((uint64_t)magic_byte(w1, 0x7541) << 32) | magic_byte(w1, 0x7540), neg);
+  c[3] = fadd2(((uint64_t)magic_byte(w1, 0x7543) << 32) | magic_byte(w1, 0x7542), neg);
+}
+
+// Rows rp .. rp+R-1, k-range [kc, kc+kn) of the bf16 activations -> sA as fp32 (row stride KC),
+// with 16-byte loads (K and kn are multiples of 64, rows 16-byte aligned).
+__device__ __forceinline__ void stage_rows_q(const __nv_bfloat16* __restrict__ a, int K, int rp, int R, int kc,
+                                             int kn, float* sA) {
+  const int per_row = KC / 8;
+  for (int i = threadIdx.x; i < R * per_row; i += kThreads) {
+    const int r = i / per_row, kk = (i % per_row) * 8;
+    float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+    if (kk < kn) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(a + (size_t)(rp + r) * K + kc + kk));
+      lo = make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
+      hi = make_float4(bf16lo(u.z), bf16hi(u.z), bf16lo(u.w), bf16hi(u.w));
+    }
+    float4* dst = reinterpret_cast<float4*>(sA + r * KC + kk);
+    dst[0] = lo;
+    dst[1] = hi;
+  }
 }
 
 template <int BITS, int STAGE, typename OutT, int RMAX>
@@ -173,22 +188,17 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const uint4* __restrict
     const int r_begin = offsets[e], r_end = offsets[e + 1];
     for (int rp = r_begin; rp < r_end; rp += RMAX) {
       const int R = min(RMAX, r_end - rp);
-      float acc[RMAX][8], accm[RMAX];
+      uint64_t acc2[RMAX][4];  // column pairs (2p, 2p+1) of each row
+      float accm[RMAX];
 #pragma unroll
       for (int r = 0; r < RMAX; ++r) {
         accm[r] = 0.f;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) acc[r][c] = 0.f;
+        for (int p = 0; p < 4; ++p) acc2[r][p] = 0ull;
       }
       for (int kc = 0; kc < K; kc += KC) {
         const int kn = min(KC, K - kc);  // a multiple of 64
         const int gn = kn / KT;          // tile rows in this chunk
-        __syncthreads();
-        for (int i = tid; i < R * KC; i += kThreads) {
-          const int r = i / KC, kk = i % KC;
-          sA[i] = kk < kn ? __bfloat162float(a[(size_t)(rp + r) * K + kc + kk]) : 0.f;
-        }
-        __syncthreads();
         auto load_batch = [&](int g0, uint4 (&t)[kUnroll]) {
 #pragma unroll
           for (int i = 0; i < kUnroll; ++i) {
@@ -197,7 +207,10 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const uint4* __restrict
           }
         };
         uint4 cur[kUnroll], nxt[kUnroll];
-        load_batch(0, cur);
+        load_batch(0, cur);  // in flight while the activations are staged
+        __syncthreads();
+        stage_rows_q(a, K, rp, R, kc, kn, sA);
+        __syncthreads();
         for (int g0 = 0; g0 < gn; g0 += GSTEP * kUnroll) {
           if (g0 + GSTEP * kUnroll < gn) load_batch(g0 + GSTEP * kUnroll, nxt);
 #pragma unroll
@@ -209,17 +222,18 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const uint4* __restrict
             const uint32_t wd[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
 #pragma unroll
             for (int j = 0; j < KT; ++j) {
-              float cf[8];
-              if (BITS == 4) int4_row(wd[j], cf);
-              else int8_row(wd[2 * j], wd[2 * j + 1], cf);
+              uint64_t cp[4];
+              if (BITS == 4) int4_row(wd[j], cp);
+              else int8_row(wd[2 * j], wd[2 * j + 1], cp);
 #pragma unroll
               for (int r = 0; r < RMAX; ++r) {
                 if (r >= R) break;
                 const float av = sA[r * KC + k0 + j];
                 const float as = av * q.x;
                 accm[r] = fmaf(av, q.y, accm[r]);
+                const uint64_t as2 = f2_pack(as, as);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) acc[r][c] = fmaf(as, cf[c], acc[r][c]);
+                for (int p = 0; p < 4; ++p) acc2[r][p] = ffma2(as2, cp[p], acc2[r][p]);
               }
             }
           }
@@ -229,11 +243,12 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const uint4* __restrict
       }
       // Fold the column-independent min term in, then combine the warp's RPW tile rows (lanes cg,
       // cg+8, cg+16, cg+24) and the warps, in fixed orders.
+      float acc[RMAX][8];
 #pragma unroll
       for (int r = 0; r < RMAX; ++r)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          float v = acc[r][c] + accm[r];
+          float v = (c & 1 ? f2_hi(acc2[r][c >> 1]) : f2_lo(acc2[r][c >> 1])) + accm[r];
           v += __shfl_xor_sync(0xffffffffu, v, LPR);
           v += __shfl_xor_sync(0xffffffffu, v, 2 * LPR);
           acc[r][c] = v;

@@ -196,6 +196,10 @@ FFN_CASES = [
     (1100, 320, 704, 3, 2, BF16, moe.PATH_TENSOR_PAIR),  # ~733 rows/expert: 3 pair tiles + tails, N tail
     (600, 320, 704, 6, 2, BF16, moe.PATH_TENSOR_PAIR),   # ~200 rows/expert: one partly empty pair tile each
     (96, 64, 128, 8, 2, BF16, moe.PATH_TENSOR_PAIR),     # K = 64, N < 256, most rows of the pair idle
+    (1100, 320, 704, 3, 2, BF16, moe.PATH_TENSOR_T),     # ~733 rows/expert: 3 row tiles, feature tail 704
+    (600, 320, 704, 6, 2, BF16, moe.PATH_TENSOR_T),      # ~200 rows/expert: one tile of N = rows rounded to 16
+    (96, 64, 128, 8, 2, BF16, moe.PATH_TENSOR_T),        # K = 64, 24 rows per expert, 128 features
+    (37, 128, 264, 5, 2, BF16, moe.PATH_TENSOR_T),       # odd row counts (N = 16 tiles), F = 264 not a multiple of 64
 ]
 
 
@@ -277,6 +281,9 @@ FORWARD_CASES = [
     dict(T=2048, d=256, F=512, E=8, k=2, dt=BF16, path=moe.PATH_TENSOR_PAIR),  # 1024 rows/expert: 4 pair tiles
     dict(T=640, d=256, F=512, E=16, k=2, dt=BF16, path=moe.PATH_TENSOR_PAIR),
     dict(T=300, d=64, F=64, E=1024, k=8, dt=BF16, path=moe.PATH_TENSOR_PAIR),  # E = 1024: five stages
+    dict(T=2048, d=256, F=512, E=8, k=2, dt=BF16, path=moe.PATH_TENSOR_T),     # 512 rows/expert: 2 full row tiles
+    dict(T=640, d=256, F=512, E=16, k=2, dt=BF16, path=moe.PATH_TENSOR_T),
+    dict(T=300, d=64, F=64, E=1024, k=8, dt=BF16, path=moe.PATH_TENSOR_T),     # E = 1024: six stages
 ]
 
 
@@ -495,7 +502,7 @@ def test_forward_zero_tokens():
     assert moe.get_device_status(ws)[0] == moe.MOE_OK
 
 
-@pytest.mark.parametrize("path", [moe.PATH_TENSOR, moe.PATH_STREAM, moe.PATH_TENSOR_PAIR])
+@pytest.mark.parametrize("path", [moe.PATH_TENSOR, moe.PATH_STREAM, moe.PATH_TENSOR_PAIR, moe.PATH_TENSOR_T])
 def test_forward_is_bit_reproducible(path):
     c = make_case(T=256, d=512, F=512, E=16, k=2, dt=BF16)
     a = run_forward(c, path)[0]
