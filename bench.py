@@ -40,6 +40,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNELS_PER_STEP = 7  # router 1, dispatch 3 (count + scan, scatter, gather), up 1, down 1, combine 1
 L2_BYTES = 126 * 2**20
 TC_SOURCES = ["sparse_mixture_experts_moe_gb300/csrc/ffn_tc.cu", "sparse_mixture_experts_moe_gb300/csrc/common.cuh"]
+TCT_SOURCES = ["sparse_mixture_experts_moe_gb300/csrc/ffn_tct.cu", "sparse_mixture_experts_moe_gb300/csrc/common.cuh"]
 QUANT_SOURCES = ["sparse_mixture_experts_moe_gb300/csrc/quant.cu", "sparse_mixture_experts_moe_gb300/csrc/common.cuh"]
 STREAM_SOURCES = ["sparse_mixture_experts_moe_gb300/csrc/ffn_stream.cu",
                   "sparse_mixture_experts_moe_gb300/csrc/common.cuh"]
@@ -441,7 +442,10 @@ def run_ours(args, w, rank, world, device):
     peaks, peak_src = load_peaks()
     eb = 2 if dt == 1 else 4
     dom = max(["expert_up", "expert_down"], key=lambda n: kern_ms[n])
-    stream_path = fpath == moe.PATH_STREAM or (fpath == moe.PATH_AUTO and dt == 1 and A <= 256)  # include/moe.h
+    # the kernel family each GEMM ran (AUTO resolves per GEMM: moe_ffn_path)
+    run_path = {n: (fpath if fpath != moe.PATH_AUTO else moe.ffn_path(T, k, E, F if n == "expert_up" else d, dt))
+                for n in ("expert_up", "expert_down")}
+    stream_path = run_path[dom] == moe.PATH_STREAM
     if qbits:
         # quantised weight streaming: codes + (scale, min) of the touched experts + rows in and out
         K_, N_ = (d, F) if dom == "expert_up" else (F, d)
@@ -471,11 +475,12 @@ def run_ours(args, w, rank, world, device):
         alg_flops = 2.0 * A * d * F
         achieved = alg_flops / (kern_ms[dom] / 1e3) / 1e12
         peak = peaks["bf16_tflops"]
-        kname = {moe.PATH_TENSOR_PAIR: "ffn_tc2_kernel", moe.PATH_TENSOR_T: "ffn_tct_kernel"}.get(fpath, "ffn_tc_kernel")
+        kname = {moe.PATH_TENSOR_PAIR: "ffn_tc2_kernel", moe.PATH_TENSOR_T: "ffn_tct_kernel"}.get(run_path[dom],
+                                                                                               "ffn_tc_kernel")
         roof = {"kernel": f"{kname} ({dom})", "bound": "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": (stored_traffic(f"ffn_tc_kernel<{1 if dom == 'expert_up' else 2}>", w.name, TC_SOURCES)
-                            if kname == "ffn_tc_kernel" else None),
+                "traffic": stored_traffic(f"{kname}<{1 if dom == 'expert_up' else 2}>", w.name,
+                                          TCT_SOURCES if kname == "ffn_tct_kernel" else TC_SOURCES),
                 "alg_flops_per_launch": alg_flops, "ms_per_launch": kern_ms[dom],
                 "peak_source": f"{peak_src} bf16_tflops (burst: the kernel runs in a short step)"}
 

@@ -57,7 +57,9 @@ typedef enum {
 typedef enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype;
 
 /* Kernel family for the expert FFN (a3, a4). AUTO picks, for bf16: STREAM with at most 256 routed
- * rows, TENSOR otherwise; SIMT for fp32. TENSOR_PAIR is available on request (measured slower). */
+ * rows; otherwise TENSOR_T when the GEMM has at least three 256-row x 256-feature items per resident
+ * CTA pair (rows assumed evenly spread over the experts), else TENSOR; SIMT for fp32. TENSOR_PAIR
+ * is available on request (measured slower). */
 typedef enum {
   MOE_PATH_AUTO = 0,
   MOE_PATH_TENSOR = 1,      /* tcgen05/TMEM grouped GEMM fed by TMA, 128x256 tiles per CTA (bf16 only) */
@@ -67,6 +69,9 @@ typedef enum {
   MOE_PATH_TENSOR_T = 5     /* tcgen05 cta_group::2 with the product transposed: 256 output features x
                                up to 256 rows per pair tile, rows rounded up to 16 (bf16 only) */
 } moe_path;
+/* The family AUTO runs for an expert GEMM of T*k routed rows, E experts and N output columns
+ * (N = d_ff for expert_up, d for expert_down); -1 on bad arguments. Host only. */
+int moe_ffn_path(int T, int k, int E, int N, moe_dtype dt);
 
 /* ---------------------------------------------------------------------------------------------
  * moe_router_topk — router GEMM, softmax and deterministic top-k, fused, one warp per token.

@@ -37,6 +37,7 @@ SIGNATURES = {
     "moe_dispatch": [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _sz, _p],
     "moe_dispatch_ex": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _sz, _p],
     "moe_capacity": [_i, _i, _i, ctypes.c_double],
+    "moe_ffn_path": [_i, _i, _i, _i, _i],
     "moe_dispatch_noalloc": [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p],
     "moe_expert_up": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
     "moe_expert_up_ex": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
@@ -169,6 +170,11 @@ def router_topk_stats(x, w_r, b_r, T, d, E, k, dt, topk_idx, topk_gate, stats, w
                                      GATES_RENORMALISE if renormalise else 0, _ptr(topk_idx), _ptr(topk_gate),
                                      _ptr(stats), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     return _check(rc, "moe_router_topk_stats") if check else rc
+
+
+def ffn_path(T, k, E, N, dt) -> int:
+    """The kernel family (PATH_*) AUTO runs for an expert GEMM with N output columns."""
+    return int(lib().moe_ffn_path(T, k, E, N, dt))
 
 
 def capacity(T, k, E, cf) -> int:

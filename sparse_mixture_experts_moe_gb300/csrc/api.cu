@@ -80,13 +80,21 @@ inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK 
 template <typename P>
 inline P* at(void* ws, size_t off) { return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off); }
 
-moe_path resolve_path(moe_path path, int dt, int rows, int E) {
+// AUTO: fp32 -> SIMT; bf16 with at most 256 routed rows -> STREAM (weight streaming); otherwise
+// the transposed CTA-pair GEMM when it has at least three 256-row items per resident pair (its
+// operand feed and ragged-row handling are the better ones, measured faster on e16 up, prefill and
+// skew), else the one-CTA GEMM, which balances a few large items better (e16 down: 63 against
+// 78 us). The item count assumes the rows spread evenly over the experts: the host does not read
+// the device's counts.
+moe_path resolve_path(moe_path path, int dt, int rows, int E, int N) {
   if (path != MOE_PATH_AUTO) return path;
   if (dt == MOE_DTYPE_F32) return MOE_PATH_SIMT;
-  // The CTA-pair kernel is correct but measured slower than the one-CTA kernel on every workload
-  // here (e16: 81/76 us against 71/63 us for up/down), so AUTO does not pick it.
-  (void)E;
-  return rows <= kStreamPathMaxRows ? MOE_PATH_STREAM : MOE_PATH_TENSOR;
+  if (rows <= kStreamPathMaxRows) return MOE_PATH_STREAM;
+  const long long active = rows < E ? rows : E;
+  const long long rpe = (rows + active - 1) / active;
+  const long long items = active * ((rpe + 255) / 256) * ((N + 255) / 256);
+  const long long pairs = device_sm_count() / 2;
+  return items >= 3 * pairs ? MOE_PATH_TENSOR_T : MOE_PATH_TENSOR;
 }
 
 bool path_ok(moe_path path, int dt) {
@@ -95,7 +103,7 @@ bool path_ok(moe_path path, int dt) {
 }
 
 moe_status run_ffn_half(moe_path path, FfnArgs& args, cudaStream_t s) {
-  path = resolve_path(path, args.dt, args.rows, args.E);
+  path = resolve_path(path, args.dt, args.rows, args.E, args.N);
   if ((path == MOE_PATH_TENSOR || path == MOE_PATH_STREAM || path == MOE_PATH_TENSOR_PAIR ||
        path == MOE_PATH_TENSOR_T) &&
       args.dt != MOE_DTYPE_BF16)
@@ -298,6 +306,11 @@ moe_status expert_half_q(int stage, const void* a, const void* codes, const floa
   return cuda_status(launch_ffn_stream_q(p, (cudaStream_t)stream));
 }
 }  // namespace
+
+int moe_ffn_path(int T, int k, int E, int N, moe_dtype dt) {
+  if (T < 0 || k < 1 || E < 1 || N < 1 || (dt != MOE_DTYPE_F32 && dt != MOE_DTYPE_BF16)) return -1;
+  return (int)resolve_path(MOE_PATH_AUTO, dt, T * k, E, N);
+}
 
 size_t moe_qweight_bytes(int K, int N, int E, int bits) {
   if (!qsizes_ok(K, N, E, bits)) return 0;

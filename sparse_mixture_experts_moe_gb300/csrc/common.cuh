@@ -30,9 +30,14 @@ __device__ __forceinline__ float gelu_erf(float z) {
 // t = 1 / (1 + p x), x >= 0, |error| <= 1.5e-7. For z < 0, 1 + erf(z/sqrt 2) = erfc(|z|/sqrt 2) is
 // used directly, so small negative outputs keep their relative accuracy. Used where the result is
 // rounded to bf16 (2^-9 relative), far coarser than the approximation.
+__device__ __forceinline__ float rcp_approx(float d) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));  // the hardware reciprocal, ~1 ulp
+  return r;
+}
 __device__ __forceinline__ float gelu_as(float z) {
   const float x = fabsf(z) * 0.70710678118654752440f;
-  const float t = __fdividef(1.0f, fmaf(0.3275911f, x, 1.0f));
+  const float t = rcp_approx(fmaf(0.3275911f, x, 1.0f));  // 1 + p x is in [1, 2.4e38): no special cases
   float poly = fmaf(1.061405429f, t, -1.453152027f);
   poly = fmaf(poly, t, 1.421413741f);
   poly = fmaf(poly, t, -0.284496736f);

@@ -326,6 +326,14 @@ bool encode_tmap(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType type, co
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+bool encode_tmap_plain(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType type, const void* ptr, int rank,
+                       const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, type, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides_bytes, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 cudaError_t launch_ffn_tensor(const FfnArgs& p, cudaStream_t s) {
   if (p.rows == 0) return cudaSuccess;

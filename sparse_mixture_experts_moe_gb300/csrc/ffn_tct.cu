@@ -13,14 +13,17 @@
 // 16 KB of weights + 16 KB of rows (32 KB, against 48 KB for one-CTA 128x256 tiles), so six or
 // seven stages fit in shared memory.
 //
-// Roles (both CTAs run 10 warps):
+// Roles (both CTAs run 18 warps):
 //   warp 0      TMA producer of this CTA's halves (128 features of W, up to 128 rows of x);
 //               the loads complete on the leader CTA's "full" barrier
 //   warp 1      TMEM allocation for the pair; in the leader also the MMA issuer
 //               (tcgen05.mma.cta_group::2, M = 256, N = rows of the tile)
-//   warps 2..9  epilogue: TMEM lane = output feature, TMEM column = row; each warp takes 32
-//               features x half of the tile's rows and stores 32 consecutive features of a row
-//               per instruction (coalesced), then arrives on the leader's "accumulator empty"
+//   warps 2..17 epilogue: TMEM lane = output feature, TMEM column = row; warp w reads lane
+//               quarter w mod 4 (32 features) and a quarter of the tile's rows, 32 rows a step.
+//               Up: GeLU, bf16, a [32 rows][32 features] tile in shared memory, one TMA store;
+//               down: gate, fp32, 32 consecutive features of a row per store instruction. Then
+//               an arrival on the leader's "accumulator empty". Sixteen warps (four per
+//               scheduler) hide the GeLU's dependent MUFU/FMA chains, which eight did not.
 // All waits are bounded; on a timeout the CTA records MOE_ERR_DEVICE_TIMEOUT and unwinds.
 #include <cuda.h>
 
@@ -37,14 +40,18 @@ constexpr int kTileASubBytes = BK * 64 * 2;       // 8 KB: 64 k-rows x 64 featur
 constexpr int kTileABytes = 2 * kTileASubBytes;   // 16 KB: this CTA's 128 features
 constexpr int kTileBBytes = (BR / 2) * BK * 2;    // 16 KB: up to 128 rows of this CTA's half
 constexpr int kStageBytes = kTileABytes + kTileBBytes;
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kEpiWarps = 16;                     // four per TMEM lane quarter: enough warps to hide
+constexpr int kThreads = 64 + 32 * kEpiWarps;     // the GeLU's dependent chains and the TMEM loads
+constexpr int kSegRows = BR * 4 / kEpiWarps;      // rows of a tile per epilogue warp: 64
+constexpr int CR = 32;                            // rows per epilogue step (one tcgen05.ld x32)
+constexpr int kStgBytes = CR * 32 * 2;            // per epilogue warp (up): 32 rows x 32 bf16 features
 constexpr uint32_t kTmemCols = 2 * BR;            // two accumulators of up to 256 columns
 constexpr int kMaxSmem = 232448;
 
 __host__ __device__ constexpr int num_bars(int nst) { return 2 * nst + 5; }
-__host__ __device__ constexpr size_t smem_bytes_for(int E, int nst) {
-  return 1024 + (size_t)nst * kStageBytes + 8 * num_bars(nst) + 16 + 4 * (size_t)(E + 1);
+__host__ __device__ constexpr size_t stg_bytes(int stage) { return stage == 1 ? (size_t)kEpiWarps * kStgBytes : 0; }
+__host__ __device__ constexpr size_t smem_bytes_for(int E, int nst, int stage) {
+  return 1024 + (size_t)nst * kStageBytes + stg_bytes(stage) + 8 * num_bars(nst) + 16 + 4 * (size_t)(E + 1);
 }
 
 // kind::f16, bf16 A and B, fp32 D, A MN-major (bit 15), B K-major, N >> 3 at 17, M >> 4 at 24.
@@ -57,9 +64,9 @@ struct Item {
   int e, row0, nrows, f0;
 };
 
-// Item w of the list (expert, 256-feature block, 256-row tile), row tile fastest: the pairs that
-// run at the same time share a weight slab (read once from HBM, then from L2).
-__device__ __forceinline__ Item decode_item(int w, const int* P, int E, int NB, const int32_t* offsets) {
+// Item w of the list (expert, 256-feature block, row tile of up to `rt` rows), row tile fastest:
+// the pairs that run at the same time share a weight slab (read once from HBM, then from L2).
+__device__ __forceinline__ Item decode_item(int w, const int* P, int E, int NB, const int32_t* offsets, int rt) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -70,8 +77,8 @@ __device__ __forceinline__ Item decode_item(int w, const int* P, int E, int NB, 
   const int r = w - P[e] * NB;
   Item it;
   it.e = e;
-  it.row0 = offsets[e] + (r % mt) * BR;
-  it.nrows = min(BR, offsets[e + 1] - it.row0);
+  it.row0 = offsets[e] + (r % mt) * rt;
+  it.nrows = min(rt, offsets[e + 1] - it.row0);
   it.f0 = (r / mt) * BF;
   return it;
 }
@@ -84,8 +91,9 @@ struct EpiOut<2> { using T = float; };
 template <int STAGE, int STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-               typename EpiOut<STAGE>::T* __restrict__ out, const int32_t* __restrict__ offsets,
-               const float* __restrict__ row_gate, int K, int N, int E, int* status, uint64_t timeout_ns) {
+               const __grid_constant__ CUtensorMap tmH, typename EpiOut<STAGE>::T* __restrict__ out, const int32_t* __restrict__ offsets,
+               const float* __restrict__ row_gate, int K, int N, int E, int rt, int* status,
+               uint64_t timeout_ns) {
   using OutT = typename EpiOut<STAGE>::T;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -93,7 +101,8 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sA = base;                          // weights: [stage][2 sub-boxes][64 k][64 f]
   const uint32_t sB = base + STAGES * kTileABytes;   // rows:    [stage][128 rows][64 k]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * kStageBytes);
+  const uint32_t sStg = base + STAGES * kStageBytes;  // up: per-warp output staging [32 rows][32 f]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * kStageBytes + stg_bytes(STAGE));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + num_bars(STAGES));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* P = reinterpret_cast<int*>(tmem_slot + 4);
@@ -113,6 +122,7 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     *abort_flag = 0;
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmW);
+    if (STAGE == 1) tma_prefetch_desc(&tmH);
   }
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
@@ -127,7 +137,7 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       int mt = 0;
       if (e < E) {
         const int cnt = offsets[e + 1] - offsets[e];
-        mt = cnt > 0 ? (cnt + BR - 1) / BR : 0;
+        mt = cnt > 0 ? (cnt + rt - 1) / rt : 0;
       }
       int incl = mt;
 #pragma unroll
@@ -156,14 +166,15 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       int stage = 0;
       uint32_t phase = 0, filled = 0, fill_phase = 0;
       for (int w = pair; w < total_items && !*abort_flag; w += npairs) {
-        const Item it = decode_item(w, P, E, NB, offsets);
+        const Item it = decode_item(w, P, E, NB, offsets, rt);
         const int nt = (it.nrows + 15) & ~15;           // MMA N: rows rounded up to 16
         const int frow = it.row0 + (nt / 2) * (int)rank;  // this CTA holds rows [nt/2 * rank, +nt/2)
         const int feat = it.f0 + (BF / 2) * (int)rank;
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_or_abort(bar(EMPTY + stage), phase ^ 1u, timeout_ns, abort_flag, status, 41)) goto producer_out;
           const uint32_t full_leader = map_to_cta(bar(FULL + stage), 0);
-          if (leader) mbar_arrive_expect_tx(bar(FULL + stage), 2 * kStageBytes);
+          // both CTAs' bytes: 128 features of W and rt/2 rows of x each (the x box is rt/2 rows high)
+          if (leader) mbar_arrive_expect_tx(bar(FULL + stage), 2 * (kTileABytes + (rt / 2) * BK * 2));
 #pragma unroll
           for (int j = 0; j < 2; ++j)
             tma_load_3d_pair(sA + stage * kTileABytes + j * kTileASubBytes, &tmW, feat + 64 * j, kb * BK, it.e,
@@ -191,7 +202,7 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         for (int w = pair; w < total_items && !*abort_flag; w += npairs) {
-          const Item it = decode_item(w, P, E, NB, offsets);
+          const Item it = decode_item(w, P, E, NB, offsets, rt);
           const uint32_t idesc = idesc_tn(BF, (it.nrows + 15) & ~15);
           if (!wait_or_abort(bar(TEMPTY + acc), acc_phase ^ 1u, timeout_ns, abort_flag, status, 42)) break;
           tc_fence_after();
@@ -221,44 +232,56 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   } else {
     // -------------------------------------------------------------- epilogue (warps 2..9)
     const int q = warp & 3;                              // TMEM lanes 32q .. 32q+31: features
-    const int c_begin = ((warp - 2) >> 2) * (BR / 2);    // this warp's half of the rows
+    const int c_begin = ((warp - 2) >> 2) * kSegRows;     // this warp's quarter of the rows
+    const uint32_t stg = sStg + (uint32_t)((warp - 2) * kStgBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int w = pair; w < total_items && !*abort_flag; w += npairs) {
-      const Item it = decode_item(w, P, E, NB, offsets);
+      const Item it = decode_item(w, P, E, NB, offsets, rt);
       // warp-uniform: the TMEM loads below are warp-collective
       if (!__all_sync(0xffffffffu, wait_or_abort(bar(TFULL + acc), acc_phase, timeout_ns, abort_flag, status, 43)))
         break;
       tc_fence_after();
       const int f = it.f0 + (BF / 2) * (int)rank + 32 * q + lane;
       const bool f_ok = f < N;
-      // 64 rows per step: two TMEM loads behind one wait, then the epilogue of all 64 values as
-      // independent chains (no per-row branch inside the arithmetic), then the guarded stores.
-      for (int c = c_begin; c < c_begin + BR / 2 && c < it.nrows; c += 64) {
+      // CR rows per step: the epilogue of all CR values as independent chains (no per-row branch
+      // inside the arithmetic), then the stores.
+      for (int c = c_begin; c < c_begin + kSegRows && c < it.nrows; c += CR) {
         const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BR + c);
-        uint32_t v[64];
-        tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(v));
-        tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        uint32_t v[CR];
+        tmem_ld_32x32b_x32(taddr, v);
         tmem_ld_wait();
-        const int nvalid = min(64, it.nrows - c);
+        const int nvalid = min(CR, it.nrows - c);
         const int r0 = it.row0 + c;
-        float res[64];
+        float res[CR];
         if (STAGE == 1) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) res[i] = gelu_as(__uint_as_float(v[i]));
+          for (int i = 0; i < CR; ++i) res[i] = gelu_as(__uint_as_float(v[i]));
         } else {
           const float g0 = lane < nvalid ? row_gate[r0 + lane] : 0.f;
-          const float g1 = lane + 32 < nvalid ? row_gate[r0 + 32 + lane] : 0.f;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            res[i] = __shfl_sync(0xffffffffu, g0, i) * __uint_as_float(v[i]);
-            res[32 + i] = __shfl_sync(0xffffffffu, g1, i) * __uint_as_float(v[32 + i]);
-          }
+          for (int i = 0; i < CR; ++i) res[i] = __shfl_sync(0xffffffffu, g0, i) * __uint_as_float(v[i]);
         }
-        if (f_ok) {
+        if (STAGE == 1 && nvalid == CR) {
+          // CR rows x 32 features through shared memory, one TMA store (columns past N are clipped)
+          if (lane == 0) bulk_wait_group_read0();  // the previous store has finished reading the buffer
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < CR; ++i) {
+            const unsigned short b = __bfloat16_as_ushort(__float2bfloat16_rn(res[i]));
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(stg + (uint32_t)(i * 64 + lane * 2)), "h"(b) : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmH, stg, it.f0 + (BF / 2) * (int)rank + 32 * q, r0);
+            bulk_commit_group();
+          }
+        } else if (f_ok) {
+          // a chunk that crosses the end of the expert's rows (or the fp32 down output): plain stores
           OutT* dst = out + (size_t)r0 * N + f;
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
+          for (int i = 0; i < CR; ++i)
             if (i < nvalid) dst[(size_t)i * N] = from_f32<OutT>(res[i]);
         }
       }
@@ -267,6 +290,8 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       if (lane == 0) mbar_arrive_cluster(map_to_cta(bar(TEMPTY + acc), 0));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
+    if (STAGE == 1 && lane == 0) bulk_wait_group0();  // stores read shared memory until they complete
+    __syncwarp();
   }
 
   // No signal may target a CTA that has left, and no MMA may still write TMEM being freed.
@@ -279,8 +304,8 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 }
 
 template <int STAGE, int STAGES>
-cudaError_t launch_tct(const FfnArgs& p, const CUtensorMap& tmX, const CUtensorMap& tmW, size_t smem,
-                       cudaStream_t s) {
+cudaError_t launch_tct(const FfnArgs& p, EncodeTiledFn enc, const CUtensorMap& tmW, const CUtensorMap& tmH,
+                       size_t smem, cudaStream_t s) {
   using OutT = typename EpiOut<STAGE>::T;
   auto kern = ffn_tct_kernel<STAGE, STAGES>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -294,10 +319,24 @@ cudaError_t launch_tct(const FfnArgs& p, const CUtensorMap& tmX, const CUtensorM
   if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0)
     clusters = device_sm_count() / 2;
   const int NB = (p.N + BF - 1) / BF;
-  const long long max_items = ((long long)(p.rows + BR - 1) / BR + p.E) * NB;
+  // Row tiles of 256 unless that leaves fewer than three items per resident pair (then the last
+  // round runs mostly empty); the estimate spreads the rows evenly over the experts.
+  const long long active = p.rows < p.E ? p.rows : p.E;
+  const long long rpe = (p.rows + active - 1) / active;
+  const int rt = active * ((rpe + BR - 1) / BR) * NB >= 3LL * clusters ? BR : BR / 2;
+  CUtensorMap tmX;
+  {
+    // rows of x_perm (or h): K-major B operand, 64 k x rt/2 rows per box (one CTA's half of a tile)
+    const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.rows};
+    const cuuint64_t str[1] = {(cuuint64_t)p.K * 2};
+    const cuuint32_t box[2] = {BK, (cuuint32_t)(rt / 2)};
+    if (!encode_tmap(enc, &tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, 2, dims, str, box))
+      return cudaErrorInvalidValue;
+  }
+  const long long max_items = ((long long)(p.rows + rt - 1) / rt + p.E) * NB;
   long long pairs = clusters < max_items ? clusters : max_items;
-  return launch_pdl(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), smem, s, tmX, tmW, (OutT*)p.out, p.offsets,
-                    p.row_gate, p.K, p.N, p.E, p.status, p.timeout_ns);
+  return launch_pdl(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), smem, s, tmX, tmW, tmH, (OutT*)p.out,
+                    p.offsets, p.row_gate, p.K, p.N, p.E, rt, p.status, p.timeout_ns);
 }
 
 }  // namespace
@@ -307,15 +346,7 @@ cudaError_t launch_ffn_tensor_t(const FfnArgs& p, cudaStream_t s) {
   if (p.dt != MOE_DTYPE_BF16) return cudaErrorNotSupported;
   EncodeTiledFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
-  CUtensorMap tmX, tmW;
-  {
-    // rows of x_perm (or h): K-major B operand, 64 k x 128 rows per box
-    const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.rows};
-    const cuuint64_t str[1] = {(cuuint64_t)p.K * 2};
-    const cuuint32_t box[2] = {BK, BR / 2};
-    if (!encode_tmap(enc, &tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, 2, dims, str, box))
-      return cudaErrorInvalidValue;
-  }
+  CUtensorMap tmW;
   {
     // weights [E][K][N]: MN-major A operand, 64 features x 64 k per box
     const cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.K, (cuuint64_t)p.E};
@@ -324,11 +355,20 @@ cudaError_t launch_ffn_tensor_t(const FfnArgs& p, cudaStream_t s) {
     if (!encode_tmap(enc, &tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.w, 3, dims, str, box))
       return cudaErrorInvalidValue;
   }
-  const bool seven = smem_bytes_for(p.E, 7) <= (size_t)kMaxSmem;
-  const size_t smem = smem_bytes_for(p.E, seven ? 7 : 6);
-  if (p.stage == 1)
-    return seven ? launch_tct<1, 7>(p, tmX, tmW, smem, s) : launch_tct<1, 6>(p, tmX, tmW, smem, s);
-  return seven ? launch_tct<2, 7>(p, tmX, tmW, smem, s) : launch_tct<2, 6>(p, tmX, tmW, smem, s);
+  CUtensorMap tmH = tmW;  // up: h [rows][N] bf16, 32 features x CR rows per store, no swizzle
+  if (p.stage == 1) {
+    const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.rows};
+    const cuuint64_t str[1] = {(cuuint64_t)p.N * 2};
+    const cuuint32_t box[2] = {32, CR};
+    if (!encode_tmap_plain(enc, &tmH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.out, 2, dims, str, box))
+      return cudaErrorInvalidValue;
+    const bool six = smem_bytes_for(p.E, 6, 1) <= (size_t)kMaxSmem;
+    const size_t smem = smem_bytes_for(p.E, six ? 6 : 5, 1);
+    return six ? launch_tct<1, 6>(p, enc, tmW, tmH, smem, s) : launch_tct<1, 5>(p, enc, tmW, tmH, smem, s);
+  }
+  const bool seven = smem_bytes_for(p.E, 7, 2) <= (size_t)kMaxSmem;
+  const size_t smem = smem_bytes_for(p.E, seven ? 7 : 6, 2);
+  return seven ? launch_tct<2, 7>(p, enc, tmW, tmH, smem, s) : launch_tct<2, 6>(p, enc, tmW, tmH, smem, s);
 }
 
 }  // namespace moe

@@ -109,6 +109,9 @@ EncodeTiledFn tensor_map_encoder();
 // Tiled tensor map with 128-byte swizzle and zero fill outside the tensor.
 bool encode_tmap(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType type, const void* ptr, int rank,
                  const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box);
+// The same without swizzle: the shared-memory box is plain row-major.
+bool encode_tmap_plain(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType type, const void* ptr, int rank,
+                       const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box);
 
 int device_sm_count();
 

@@ -200,6 +200,7 @@ FFN_CASES = [
     (600, 320, 704, 6, 2, BF16, moe.PATH_TENSOR_T),      # ~200 rows/expert: one tile of N = rows rounded to 16
     (96, 64, 128, 8, 2, BF16, moe.PATH_TENSOR_T),        # K = 64, 24 rows per expert, 128 features
     (37, 128, 264, 5, 2, BF16, moe.PATH_TENSOR_T),       # odd row counts (N = 16 tiles), F = 264 not a multiple of 64
+    (2048, 256, 4096, 8, 2, BF16, moe.PATH_TENSOR_T),    # enough items for 256-row tiles (up), 128-row (down)
 ]
 
 
