@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s; % of BF16 tensor peak (prefill) / % HBM BW (decode)"
 DEFAULT_WORKLOAD = "e16_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNELS_PER_STEP = 7  # router 1, dispatch 3 (count + scan, scatter, gather), up 1, down 1, combine 1
+KERNELS_PER_STEP = 6  # router 1, dispatch 2 (count + scan, scatter + gather), up 1, down 1, combine 1
 L2_BYTES = 126 * 2**20
 TC_SOURCES = ["sparse_mixture_experts_moe_gb300/csrc/ffn_tc.cu", "sparse_mixture_experts_moe_gb300/csrc/common.cuh"]
 TCT_SOURCES = ["sparse_mixture_experts_moe_gb300/csrc/ffn_tct.cu", "sparse_mixture_experts_moe_gb300/csrc/common.cuh"]

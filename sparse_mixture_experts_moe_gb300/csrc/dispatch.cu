@@ -118,6 +118,66 @@ dispatch_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict
   }
 }
 
+// Scatter and gather in one kernel: `split` CTAs per 256-assignment chunk each compute the chunk's
+// stable ranks (cheap, redundant), the first of them writes row_of / perm_token / row_gate, and
+// each copies its share of the chunk's rows x[t] -> x_perm[row] (one warp per row, 16-byte vectors).
+// Dropped assignments (capacity) get row -1 and are not copied.
+__global__ void __launch_bounds__(kChunk)
+dispatch_scatter_gather_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int A, int k,
+                               int E, const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets,
+                               int cap, int split, const int4* __restrict__ x, int vec_per_row,
+                               int32_t* __restrict__ row_of, int32_t* __restrict__ perm_token,
+                               float* __restrict__ row_gate, int4* __restrict__ x_perm) {
+  griddep_launch_dependents();
+  griddep_wait();
+  extern __shared__ int wcnt[];  // [kWarpsPerChunk][E], then the chunk's rows [kChunk]
+  int* srow = wcnt + kWarpsPerChunk * E;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunk = blockIdx.x / split, part = blockIdx.x % split;
+  for (int i = tid; i < kWarpsPerChunk * E; i += kChunk) wcnt[i] = 0;
+  __syncthreads();
+  const int a = chunk * kChunk + tid;
+  int e = -1;
+  if (a < A) {
+    e = idx[a];
+    if (e < 0 || e >= E) e = -1;
+  }
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(peers);
+  __syncthreads();
+  int row = -1;
+  if (e >= 0) {
+    int pre = 0;
+    for (int w = 0; w < warp; ++w) pre += wcnt[w * E + e];
+    row = blk_base[(size_t)chunk * E + e] + pre + rank;
+    if (cap > 0 && row - offsets[e] >= cap) row = -1;  // past the expert's capacity: dropped
+  }
+  srow[tid] = row;
+  if (part == 0 && a < A) {
+    row_of[a] = row;
+    if (row >= 0) {
+      perm_token[row] = a / k;
+      row_gate[row] = gate[a];
+    }
+  }
+  __syncthreads();
+  // rows of this part: assignments part, part + split, ... of the chunk, one warp each
+  const int n_here = min(kChunk, A - chunk * kChunk);
+  for (int i = part + split * warp; i < n_here; i += split * kWarpsPerChunk) {
+    const int r = srow[i];
+    if (r < 0) continue;
+    const int4* src = x + (size_t)((chunk * kChunk + i) / k) * vec_per_row;
+    int4* dst = x_perm + (size_t)r * vec_per_row;
+    int v = lane;
+    for (; v + 96 < vec_per_row; v += 128) {
+      const int4 v0 = __ldg(src + v), v1 = __ldg(src + v + 32), v2 = __ldg(src + v + 64), v3 = __ldg(src + v + 96);
+      dst[v] = v0; dst[v + 32] = v1; dst[v + 64] = v2; dst[v + 96] = v3;
+    }
+    for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
 __global__ void __launch_bounds__(256)
 dispatch_gather_kernel(const int4* __restrict__ x, const int32_t* __restrict__ perm_token,
                        const int32_t* __restrict__ offsets, int E, int vec_per_row, int4* __restrict__ x_perm) {
@@ -280,7 +340,7 @@ cudaError_t launch_dispatch(const void* x, const int32_t* idx, const float* gate
 
 namespace moe {
 
-// Three launches with programmatic dependent launch: count + scan, scatter, gather.
+// Two launches with programmatic dependent launch: count + scan, then scatter + gather.
 cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
                                  int dt, int cap, int32_t* counts, int32_t* offsets, int32_t* perm_token,
                                  int32_t* row_of, float* row_gate, void* x_perm, int32_t* blk_counts,
@@ -294,19 +354,19 @@ cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float*
   cudaError_t err = launch_pdl(dispatch_count_scan_kernel, dim3(nb), dim3(kChunk), cs_smem, s, idx, A, E, nb, cap,
                                blk_counts, blk_base, counts, offsets, status, done);
   if (err != cudaSuccess) return err;
-  const size_t sc_smem = (size_t)kWarpsPerChunk * E * sizeof(int);
-  err = cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sc_smem);
-  if (err != cudaSuccess) return err;
-  err = launch_pdl(dispatch_scatter_kernel, dim3(nb), dim3(kChunk), sc_smem, s, idx, gate, A, k, E,
-                   (const int32_t*)blk_base, (const int32_t*)offsets, cap, row_of, perm_token, row_gate);
+  // scatter + gather: enough CTAs per chunk that the row copy is spread over the SMs
+  const size_t sc_smem = (size_t)(kWarpsPerChunk * E + kChunk) * sizeof(int);
+  err = cudaFuncSetAttribute(dispatch_scatter_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sc_smem);
   if (err != cudaSuccess) return err;
   const size_t elem = dt == MOE_DTYPE_BF16 ? 2 : 4;
   const int vec_per_row = (int)((size_t)d * elem / 16);
-  int blocks = (A + 7) / 8;
-  const int max_blocks = device_sm_count() * 8;
-  if (blocks > max_blocks) blocks = max_blocks;
-  return launch_pdl(dispatch_gather_kernel, dim3(blocks), dim3(256), 0, s, (const int4*)x, (const int32_t*)perm_token,
-                    (const int32_t*)offsets, E, vec_per_row, (int4*)x_perm);
+  int split = (2 * device_sm_count() + nb - 1) / nb;
+  if (split > 8) split = 8;
+  if (split < 1) split = 1;
+  return launch_pdl(dispatch_scatter_gather_kernel, dim3(nb * split), dim3(kChunk), sc_smem, s, idx, gate, A, k, E,
+                    (const int32_t*)blk_base, (const int32_t*)offsets, cap, split, (const int4*)x, vec_per_row,
+                    row_of, perm_token, row_gate, (int4*)x_perm);
 }
 
 }  // namespace moe

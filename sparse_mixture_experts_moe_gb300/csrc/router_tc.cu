@@ -24,15 +24,23 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int BM = 128, BK = 64;
 constexpr int kTileXBytes = BM * BK * 2;     // 16 KB
 constexpr int kTileWSubBytes = BK * 64 * 2;  // 8 KB: 64 k-rows x 64 experts
 constexpr int kThreads = 192;
-constexpr int kNumBars = 2 * STAGES + 2;
+__host__ __device__ constexpr int num_bars(int nst) { return 2 * nst + 2; }
 
+// Pipeline depth: about 192 KB of x and W_r tiles in flight per CTA (the router streams x once and
+// is bound by load latency): 8 stages of 24 KB (E <= 64), 6 of 32 KB (E <= 128), 4 of 48 KB.
 template <int EN>
+constexpr int stages_plain() { return EN <= 64 ? 8 : EN <= 128 ? 6 : 4; }
+// The split kernel also holds the 128 x EN partial-logit table.
+template <int EN>
+constexpr int stages_split() { return EN <= 64 ? 6 : 4; }
+
+template <int EN, int NST>
 constexpr size_t router_smem_bytes() {
-  return 1024 + (size_t)STAGES * (kTileXBytes + EN / 64 * kTileWSubBytes) + 8 * kNumBars + 16;
+  return 1024 + (size_t)NST * (kTileXBytes + EN / 64 * kTileWSubBytes) + 8 * num_bars(NST) + 16;
 }
 
 // Routing statistics: [4][EN] per-warp soft-load sums, [4] entropy sums, [EN] counts.
@@ -56,7 +64,7 @@ __device__ __forceinline__ void topk_insert(float (&bv)[KMAX], int (&bi)[KMAX], 
   }
 }
 
-template <int EN, int KMAX>
+template <int EN, int KMAX, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
 router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                  const float* __restrict__ b_r, int Tn, int d, int E, int k, int renorm, RouterStats st,
@@ -71,9 +79,9 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   const uint32_t sX = base;
   const uint32_t sW = base + STAGES * kTileXBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * kStageBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + num_bars(STAGES));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* s_soft = reinterpret_cast<float*>(gbase + STAGES * kStageBytes + 8 * kNumBars + 16);  // [4][EN]
+  float* s_soft = reinterpret_cast<float*>(gbase + STAGES * kStageBytes + 8 * num_bars(STAGES) + 16);  // [4][EN]
   float* s_ent = s_soft + 4 * EN;                                                             // [4]
   int* s_cnt = reinterpret_cast<int*>(s_ent + 4);                                             // [EN]
   const bool stats = st.part != nullptr;
@@ -251,10 +259,11 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
 
 template <int EN>
 constexpr size_t router_split_smem_bytes() {
-  return router_smem_bytes<EN>() + (size_t)BM * (EN + 1) * sizeof(float) + router_stat_bytes<EN>();
+  return router_smem_bytes<EN, stages_split<EN>()>() + (size_t)BM * (EN + 1) * sizeof(float) +
+         router_stat_bytes<EN>();
 }
 
-template <int EN, int KMAX>
+template <int EN, int KMAX, int STAGES>
 __global__ void __cluster_dims__(kSplit, 1, 1) __launch_bounds__(kThreads, 1)
 router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                        const float* __restrict__ b_r, int Tn, int d, int E, int k, int renorm,
@@ -271,9 +280,9 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
   const uint32_t sX = base;
   const uint32_t sW = base + STAGES * kTileXBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * kStageBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + num_bars(STAGES));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* red = reinterpret_cast<float*>(gbase + STAGES * kStageBytes + 8 * kNumBars + 16);  // [BM][RS]
+  float* red = reinterpret_cast<float*>(gbase + STAGES * kStageBytes + 8 * num_bars(STAGES) + 16);  // [BM][RS]
   float* s_soft = red + BM * RS;                   // statistics: [4][EN] per-warp soft-load sums
   float* s_ent = s_soft + 4 * EN;                  // [4]
   int* s_cnt = reinterpret_cast<int*>(s_ent + 4);  // [EN]
@@ -468,14 +477,14 @@ cudaError_t launch_en(const CUtensorMap& tmX, const CUtensorMap& tmW, const floa
     // DSMEM reduction costs more than it saves (T = 4096, d = 1024: 14.6 -> 27.6 us), so
     // larger batches keep one CTA per tile.
     const size_t smem = router_split_smem_bytes<EN>();
-    auto kern = router_tc_split_kernel<EN, KMAX>;
+    auto kern = router_tc_split_kernel<EN, KMAX, stages_split<EN>()>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3(kSplit * ((Tn + BM - 1) / BM)), dim3(kThreads), smem, s, tmX, tmW, b_r, Tn, d, E,
                       k, renorm, st, idx, gate, status, timeout_ns);
   }
-  const size_t smem = router_smem_bytes<EN>() + router_stat_bytes<EN>();
-  auto kern = router_tc_kernel<EN, KMAX>;
+  const size_t smem = router_smem_bytes<EN, stages_plain<EN>()>() + router_stat_bytes<EN>();
+  auto kern = router_tc_kernel<EN, KMAX, stages_plain<EN>()>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   return launch_pdl(kern, dim3((Tn + BM - 1) / BM), dim3(kThreads), smem, s, tmX, tmW, b_r, Tn, d, E, k, renorm, st,
