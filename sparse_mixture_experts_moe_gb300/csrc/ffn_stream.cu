@@ -24,7 +24,10 @@ constexpr int NS = 64;            // columns per slab
 constexpr int LPR = NS / 8;       // lanes per k-row: 8 (16 bytes each)
 constexpr int RPW = 32 / LPR;     // k-rows per warp per step: 4
 constexpr int KSTEP = kWarps * RPW;  // k-rows per CTA step: 32
-constexpr int KC = 1024;          // k-depth staged per chunk
+// k-depth of activations staged per chunk: 32 KB of fp32 rows. Each chunk restarts the weight
+// stream behind two barriers, so chunks are made as deep as the two-CTAs-per-SM budget allows.
+template <int RMAX>
+constexpr int kc_for() { return RMAX <= 2 ? 4096 : 2048; }
 // Weight loads per thread per batch (two batches in flight): 8 with 2 rows a pass; with 4 rows
 // the accumulators take the registers, and 8 would spill.
 template <int RMAX>
@@ -37,6 +40,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
 
 // Rows rp .. rp+R-1, k-range [kc, kc+kn) of the bf16 activations -> sA as fp32 (row stride KC),
 // with 16-byte loads; K and kn are multiples of 8 and the rows 16-byte aligned.
+template <int KC>
 __device__ __forceinline__ void stage_rows(const __nv_bfloat16* __restrict__ a, int K, int rp, int R, int kc, int kn,
                                            float* sA) {
   const int per_row = KC / 8;
@@ -61,6 +65,7 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __re
                   const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
                   OutT* __restrict__ out) {
   constexpr int kUnroll = unroll_for<RMAX>();
+  constexpr int KC = kc_for<RMAX>();
   extern __shared__ __align__(16) float smem[];
   float* sA = smem;                         // [RMAX][KC]
   float* sRed = sA + RMAX * KC;             // [kWarps][RMAX][NS]
@@ -120,7 +125,7 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __re
         uint4 cur[kUnroll], nxt[kUnroll];
         load_batch(0, cur);
         __syncthreads();
-        stage_rows(a, K, rp, R, kc, kn, sA);
+        stage_rows<KC>(a, K, rp, R, kc, kn, sA);
         __syncthreads();
         for (int k0 = 0; k0 < kn; k0 += KSTEP * kUnroll) {
           if (k0 + KSTEP * kUnroll < kn) load_batch(k0 + KSTEP * kUnroll, nxt);
@@ -180,7 +185,7 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __re
 
 template <int STAGE, typename OutT, int RMAX>
 cudaError_t launch_t(const FfnArgs& p, cudaStream_t s) {
-  const size_t smem = (size_t)(RMAX * KC + kWarps * RMAX * NS) * sizeof(float) + (size_t)p.E * sizeof(int);
+  const size_t smem = (size_t)(RMAX * kc_for<RMAX>() + kWarps * RMAX * NS) * sizeof(float) + (size_t)p.E * sizeof(int);
   auto kern = ffn_stream_kernel<STAGE, OutT, RMAX>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;

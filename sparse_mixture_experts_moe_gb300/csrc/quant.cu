@@ -32,7 +32,10 @@ constexpr int NS = 64;              // columns per slab (one block column)
 constexpr int LPR = NS / 8;         // lanes per tile row: 8
 constexpr int RPW = 32 / LPR;       // tile rows per warp per step: 4
 constexpr int GSTEP = kWarps * RPW; // tile rows per CTA step: 32
-constexpr int KC = 1024;            // k-depth of activations staged per chunk
+// k-depth of activations staged per chunk (32 KB of fp32 rows): deep, since each chunk restarts
+// the code stream behind two barriers and a 4-bit chunk is little work per thread.
+template <int RMAX>
+constexpr int kc_for() { return RMAX <= 2 ? 4096 : 2048; }
 constexpr int kUnroll = 4;
 constexpr float kMagic = 8388608.0f;  // 2^23: a byte b placed in the low mantissa bits reads 2^23 + b
 
@@ -126,6 +129,7 @@ __device__ __forceinline__ void int8_row(uint32_t w0, uint32_t w1, uint64_t (&c)
 
 // Rows rp .. rp+R-1, k-range [kc, kc+kn) of the bf16 activations -> sA as fp32 (row stride KC),
 // with 16-byte loads (K and kn are multiples of 64, rows 16-byte aligned).
+template <int KC>
 __device__ __forceinline__ void stage_rows_q(const __nv_bfloat16* __restrict__ a, int K, int rp, int R, int kc,
                                              int kn, float* sA) {
   const int per_row = KC / 8;
@@ -150,6 +154,7 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const uint4* __restrict
                     const float* __restrict__ row_gate, int K, int N, int E, OutT* __restrict__ out) {
   constexpr int KT = 16 / BITS;  // k-rows per tile: 128 bits / (8 columns x BITS)
   static_assert(KT * 8 * BITS == 128 && (BITS == 4 ? KT == 4 : KT == 2), "tile words hold KT k-rows");
+  constexpr int KC = kc_for<RMAX>();
   extern __shared__ __align__(16) float smem[];
   float* sA = smem;                                     // [RMAX][KC]
   float* sRed = sA + RMAX * KC;                         // [kWarps][RMAX][NS]
@@ -209,7 +214,7 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const uint4* __restrict
         uint4 cur[kUnroll], nxt[kUnroll];
         load_batch(0, cur);  // in flight while the activations are staged
         __syncthreads();
-        stage_rows_q(a, K, rp, R, kc, kn, sA);
+        stage_rows_q<KC>(a, K, rp, R, kc, kn, sA);
         __syncthreads();
         for (int g0 = 0; g0 < gn; g0 += GSTEP * kUnroll) {
           if (g0 + GSTEP * kUnroll < gn) load_batch(g0 + GSTEP * kUnroll, nxt);
@@ -274,7 +279,7 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const uint4* __restrict
 
 template <int BITS, int STAGE, typename OutT, int RMAX>
 cudaError_t launch_q(const QFfnArgs& p, cudaStream_t s) {
-  const size_t smem = (size_t)(RMAX * KC + kWarps * RMAX * NS) * sizeof(float) +
+  const size_t smem = (size_t)(RMAX * kc_for<RMAX>() + kWarps * RMAX * NS) * sizeof(float) +
                       (size_t)(p.K / QB) * sizeof(float2) + (size_t)p.E * sizeof(int);
   auto kern = ffn_stream_q_kernel<BITS, STAGE, OutT, RMAX>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
