@@ -64,9 +64,13 @@ struct Item {
   int e, row0, nrows, f0;
 };
 
-// Item w of the list (expert, 256-feature block, row tile of up to `rt` rows), row tile fastest:
-// the pairs that run at the same time share a weight slab (read once from HBM, then from L2).
-__device__ __forceinline__ Item decode_item(int w, const int* P, int E, int NB, const int32_t* offsets, int rt) {
+// Item w of the list (expert, 256-feature block, row tile), row tile fastest: the pairs that run
+// at the same time share a weight slab (read once from HBM, then from L2). An expert with cnt rows
+// has ceil(cnt / 256) row tiles: of 256 rows and a ragged last one, or (balanced) of equal size
+// rounded up to 16, so that few items per pair do not leave a round of full items behind a round
+// of tiny ones (cnt = 530: 192 + 192 + 146 rows instead of 256 + 256 + 18).
+__device__ __forceinline__ Item decode_item(int w, const int* P, int E, int NB, const int32_t* offsets,
+                                            int balanced) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -75,10 +79,16 @@ __device__ __forceinline__ Item decode_item(int w, const int* P, int E, int NB, 
   const int e = lo;
   const int mt = P[e + 1] - P[e];
   const int r = w - P[e] * NB;
+  const int cnt = offsets[e + 1] - offsets[e];
+  int rte = BR;
+  if (balanced) {
+    const int b = ((cnt + mt - 1) / mt + 15) & ~15;
+    if ((mt - 1) * b < cnt) rte = b;  // every tile keeps at least one row
+  }
   Item it;
   it.e = e;
-  it.row0 = offsets[e] + (r % mt) * rt;
-  it.nrows = min(rt, offsets[e + 1] - it.row0);
+  it.row0 = offsets[e] + (r % mt) * rte;
+  it.nrows = min(rte, offsets[e + 1] - it.row0);
   it.f0 = (r / mt) * BF;
   return it;
 }
@@ -92,7 +102,7 @@ template <int STAGE, int STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                const __grid_constant__ CUtensorMap tmH, typename EpiOut<STAGE>::T* __restrict__ out, const int32_t* __restrict__ offsets,
-               const float* __restrict__ row_gate, int K, int N, int E, int rt, int* status,
+               const float* __restrict__ row_gate, int K, int N, int E, int balanced, int* status,
                uint64_t timeout_ns) {
   using OutT = typename EpiOut<STAGE>::T;
   extern __shared__ uint8_t smem_raw[];
@@ -137,7 +147,7 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       int mt = 0;
       if (e < E) {
         const int cnt = offsets[e + 1] - offsets[e];
-        mt = cnt > 0 ? (cnt + rt - 1) / rt : 0;
+        mt = cnt > 0 ? (cnt + BR - 1) / BR : 0;
       }
       int incl = mt;
 #pragma unroll
@@ -166,15 +176,14 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       int stage = 0;
       uint32_t phase = 0, filled = 0, fill_phase = 0;
       for (int w = pair; w < total_items && !*abort_flag; w += npairs) {
-        const Item it = decode_item(w, P, E, NB, offsets, rt);
+        const Item it = decode_item(w, P, E, NB, offsets, balanced);
         const int nt = (it.nrows + 15) & ~15;           // MMA N: rows rounded up to 16
         const int frow = it.row0 + (nt / 2) * (int)rank;  // this CTA holds rows [nt/2 * rank, +nt/2)
         const int feat = it.f0 + (BF / 2) * (int)rank;
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_or_abort(bar(EMPTY + stage), phase ^ 1u, timeout_ns, abort_flag, status, 41)) goto producer_out;
           const uint32_t full_leader = map_to_cta(bar(FULL + stage), 0);
-          // both CTAs' bytes: 128 features of W and rt/2 rows of x each (the x box is rt/2 rows high)
-          if (leader) mbar_arrive_expect_tx(bar(FULL + stage), 2 * (kTileABytes + (rt / 2) * BK * 2));
+          if (leader) mbar_arrive_expect_tx(bar(FULL + stage), 2 * kStageBytes);  // both CTAs' bytes
 #pragma unroll
           for (int j = 0; j < 2; ++j)
             tma_load_3d_pair(sA + stage * kTileABytes + j * kTileASubBytes, &tmW, feat + 64 * j, kb * BK, it.e,
@@ -202,7 +211,7 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         for (int w = pair; w < total_items && !*abort_flag; w += npairs) {
-          const Item it = decode_item(w, P, E, NB, offsets, rt);
+          const Item it = decode_item(w, P, E, NB, offsets, balanced);
           const uint32_t idesc = idesc_tn(BF, (it.nrows + 15) & ~15);
           if (!wait_or_abort(bar(TEMPTY + acc), acc_phase ^ 1u, timeout_ns, abort_flag, status, 42)) break;
           tc_fence_after();
@@ -237,7 +246,7 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int w = pair; w < total_items && !*abort_flag; w += npairs) {
-      const Item it = decode_item(w, P, E, NB, offsets, rt);
+      const Item it = decode_item(w, P, E, NB, offsets, balanced);
       // warp-uniform: the TMEM loads below are warp-collective
       if (!__all_sync(0xffffffffu, wait_or_abort(bar(TFULL + acc), acc_phase, timeout_ns, abort_flag, status, 43)))
         break;
@@ -319,24 +328,24 @@ cudaError_t launch_tct(const FfnArgs& p, EncodeTiledFn enc, const CUtensorMap& t
   if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0)
     clusters = device_sm_count() / 2;
   const int NB = (p.N + BF - 1) / BF;
-  // Row tiles of 256 unless that leaves fewer than three items per resident pair (then the last
-  // round runs mostly empty); the estimate spreads the rows evenly over the experts.
+  // Balanced row tiles when there are fewer than three items per resident pair (the estimate
+  // spreads the rows evenly over the experts); 256-row tiles otherwise.
   const long long active = p.rows < p.E ? p.rows : p.E;
   const long long rpe = (p.rows + active - 1) / active;
-  const int rt = active * ((rpe + BR - 1) / BR) * NB >= 3LL * clusters ? BR : BR / 2;
+  const int balanced = active * ((rpe + BR - 1) / BR) * NB >= 3LL * clusters ? 0 : 1;
   CUtensorMap tmX;
   {
-    // rows of x_perm (or h): K-major B operand, 64 k x rt/2 rows per box (one CTA's half of a tile)
+    // rows of x_perm (or h): K-major B operand, 64 k x 128 rows per box (one CTA's half of a tile)
     const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.rows};
     const cuuint64_t str[1] = {(cuuint64_t)p.K * 2};
-    const cuuint32_t box[2] = {BK, (cuuint32_t)(rt / 2)};
+    const cuuint32_t box[2] = {BK, BR / 2};
     if (!encode_tmap(enc, &tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, 2, dims, str, box))
       return cudaErrorInvalidValue;
   }
-  const long long max_items = ((long long)(p.rows + rt - 1) / rt + p.E) * NB;
+  const long long max_items = ((long long)(p.rows + BR - 1) / BR + p.E) * NB;
   long long pairs = clusters < max_items ? clusters : max_items;
   return launch_pdl(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), smem, s, tmX, tmW, tmH, (OutT*)p.out,
-                    p.offsets, p.row_gate, p.K, p.N, p.E, rt, p.status, p.timeout_ns);
+                    p.offsets, p.row_gate, p.K, p.N, p.E, balanced, p.status, p.timeout_ns);
 }
 
 }  // namespace
