@@ -347,6 +347,29 @@ moe_status moe_combine(const void* y_perm, const int32_t* row_of, int T, int d, 
   return cuda_status(launch_combine(y_perm, row_of, T, d, k, dt, out, (cudaStream_t)stream));
 }
 
+namespace {
+// Router, then dispatch. With k = 2 a tensor-core router tile (128 tokens) holds exactly one dispatch
+// chunk (256 assignments), so the router also writes each chunk's expert histogram and the dispatch
+// needs no count kernel; otherwise (or when the CUDA-core router ran) the two-kernel dispatch.
+moe_status route_and_dispatch(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
+                              moe_dtype dt, int flags, int capacity, RouterStats rs, int32_t* idx, float* gate,
+                              int32_t* cnt, int32_t* offs, int32_t* perm, int32_t* rowof, float* rgate, void* xp,
+                              const Layout& L, void* workspace, size_t ws_bytes, void* stream) {
+  rs.hist = k * 128 == kDispatchChunk ? at<int32_t>(workspace, L.blk_counts) : nullptr;
+  bool wrote_hist = false;
+  moe_status st = cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, flags, rs, idx, gate,
+                                                 at<int>(workspace, 0), wait_timeout_ns(), (cudaStream_t)stream,
+                                                 &wrote_hist));
+  if (st != MOE_OK) return st;
+  if (wrote_hist)
+    return cuda_status(launch_dispatch_from_hist(x, idx, gate, T, d, E, k, dt, capacity,
+                                                 at<int32_t>(workspace, L.blk_counts), cnt, offs, perm, rowof,
+                                                 rgate, xp, (cudaStream_t)stream));
+  return moe_dispatch_ex(x, idx, gate, T, d, E, k, dt, capacity, cnt, offs, perm, rowof, rgate, xp, workspace,
+                         ws_bytes, stream);
+}
+}  // namespace
+
 moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2,
                           int T, int d, int F, int E, int k, moe_dtype dt, moe_dtype out_dt, moe_path path,
                           int flags, int capacity, void* out, int32_t* topk_idx, float* topk_gate,
@@ -373,11 +396,8 @@ moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, cons
   void* yp = at<void>(workspace, L.y_perm);
   const RouterStats rs{router_stats != nullptr ? at<float>(workspace, L.stats_part) : nullptr, router_stats,
                        at<int>(workspace, 0) + 3};
-  moe_status st = cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, flags, rs, idx, gate,
-                                                 at<int>(workspace, 0), wait_timeout_ns(), (cudaStream_t)stream));
-  if (st != MOE_OK) return st;
-  st = moe_dispatch_ex(x, idx, gate, T, d, E, k, dt, capacity, cnt, offs, perm, rowof, rgate, xp, workspace,
-                       ws_bytes, stream);
+  moe_status st = route_and_dispatch(x, w_r, b_r, T, d, E, k, dt, flags, capacity, rs, idx, gate, cnt, offs, perm,
+                                     rowof, rgate, xp, L, workspace, ws_bytes, stream);
   if (st != MOE_OK) return st;
   st = moe_expert_up_ex(xp, w1, offs, T, d, F, E, k, dt, path, h, workspace, ws_bytes, stream);
   if (st != MOE_OK) return st;
@@ -411,11 +431,9 @@ moe_status moe_forward_q(const void* x, const void* w_r, const float* b_r, const
   void* yp = at<void>(workspace, L.y_perm);
   const RouterStats rs{router_stats != nullptr ? at<float>(workspace, L.stats_part) : nullptr, router_stats,
                        at<int>(workspace, 0) + 3};
-  moe_status st = cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, flags, rs, idx, gate,
-                                                 at<int>(workspace, 0), wait_timeout_ns(), (cudaStream_t)stream));
-  if (st != MOE_OK) return st;
-  st = moe_dispatch_ex(x, idx, gate, T, d, E, k, dt, capacity, cnt, offs, at<int32_t>(workspace, L.perm_token),
-                       rowof, rgate, xp, workspace, ws_bytes, stream);
+  moe_status st = route_and_dispatch(x, w_r, b_r, T, d, E, k, dt, flags, capacity, rs, idx, gate, cnt, offs,
+                                     at<int32_t>(workspace, L.perm_token), rowof, rgate, xp, L, workspace, ws_bytes,
+                                     stream);
   if (st != MOE_OK) return st;
   st = moe_expert_up_q(xp, w1_codes, w1_scale_min, offs, T, d, F, E, k, bits, h, stream);
   if (st != MOE_OK) return st;

@@ -178,6 +178,113 @@ dispatch_scatter_gather_kernel(const int32_t* __restrict__ idx, const float* __r
   }
 }
 
+// The same scatter + gather when the per-chunk histograms are already in blk_counts (written by the
+// router): every CTA first rebuilds, in a fixed order, the experts' totals (clipped at the capacity),
+// their exclusive scan (offsets) and its chunk's bases; CTA 0 writes counts and offsets. Reading
+// nb x E counts per CTA replaces a separate count kernel.
+__global__ void __launch_bounds__(kChunk)
+dispatch_from_hist_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int A, int k, int E,
+                          int nb, const int32_t* __restrict__ blk_counts, int cap, int split,
+                          const int4* __restrict__ x, int vec_per_row, int32_t* __restrict__ counts,
+                          int32_t* __restrict__ offsets, int32_t* __restrict__ row_of,
+                          int32_t* __restrict__ perm_token, float* __restrict__ row_gate, int4* __restrict__ x_perm) {
+  griddep_launch_dependents();
+  griddep_wait();
+  extern __shared__ int sm[];
+  int* wcnt = sm;                              // [kWarpsPerChunk][E]
+  int* srow = wcnt + kWarpsPerChunk * E;       // [kChunk]
+  int* sbase = srow + kChunk;                  // [E]: this chunk's first row per expert
+  int* soff = sbase + E;                       // [E]: offsets
+  __shared__ int warp_tot[kChunk / 32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunk = blockIdx.x / split, part = blockIdx.x % split;
+  // totals and this chunk's prefix: thread (g, e) sums the chunks c = g (mod G) of expert e (E <= kChunk),
+  // then thread e adds the G partials in order
+  __shared__ int s_tp[2][kChunk];
+  const int G = kChunk / E;
+  if (tid < G * E) {
+    const int e = tid % E, g = tid / E;
+    int tot = 0, p = 0;
+    for (int c = g; c < nb; c += G) {
+      const int v = blk_counts[(size_t)c * E + e];
+      tot += v;
+      if (c < chunk) p += v;
+    }
+    s_tp[0][tid] = tot;
+    s_tp[1][tid] = p;
+  }
+  for (int i = tid; i < kWarpsPerChunk * E; i += kChunk) wcnt[i] = 0;
+  __syncthreads();
+  int kept = 0, pre = 0;
+  if (tid < E) {
+    int tot = 0;
+    for (int g = 0; g < G; ++g) {
+      tot += s_tp[0][g * E + tid];
+      pre += s_tp[1][g * E + tid];
+    }
+    kept = cap > 0 ? min(tot, cap) : tot;
+  }
+  int incl = kept;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int run = incl - kept;
+  for (int w = 0; w < warp; ++w) run += warp_tot[w];
+  if (tid < E) {
+    soff[tid] = run;
+    sbase[tid] = run + pre;
+    if (blockIdx.x == 0) {
+      counts[tid] = kept;
+      offsets[tid] = run;
+    }
+  }
+  run += kept;
+  if (blockIdx.x == 0 && tid == kChunk - 1) offsets[E] = run;
+  const int a = chunk * kChunk + tid;
+  int e = -1;
+  if (a < A) {
+    e = idx[a];
+    if (e < 0 || e >= E) e = -1;
+  }
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(peers);
+  __syncthreads();
+  int row = -1;
+  if (e >= 0) {
+    int p = 0;
+    for (int w = 0; w < warp; ++w) p += wcnt[w * E + e];
+    row = sbase[e] + p + rank;
+    if (cap > 0 && row - soff[e] >= cap) row = -1;  // past the expert's capacity: dropped
+  }
+  srow[tid] = row;
+  if (part == 0 && a < A) {
+    row_of[a] = row;
+    if (row >= 0) {
+      perm_token[row] = a / k;
+      row_gate[row] = gate[a];
+    }
+  }
+  __syncthreads();
+  const int n_here = min(kChunk, A - chunk * kChunk);
+  for (int i = part + split * warp; i < n_here; i += split * kWarpsPerChunk) {
+    const int r = srow[i];
+    if (r < 0) continue;
+    const int4* src = x + (size_t)((chunk * kChunk + i) / k) * vec_per_row;
+    int4* dst = x_perm + (size_t)r * vec_per_row;
+    int v = lane;
+    for (; v + 96 < vec_per_row; v += 128) {
+      const int4 v0 = __ldg(src + v), v1 = __ldg(src + v + 32), v2 = __ldg(src + v + 64), v3 = __ldg(src + v + 96);
+      dst[v] = v0; dst[v + 32] = v1; dst[v + 64] = v2; dst[v + 96] = v3;
+    }
+    for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
 __global__ void __launch_bounds__(256)
 dispatch_gather_kernel(const int4* __restrict__ x, const int32_t* __restrict__ perm_token,
                        const int32_t* __restrict__ offsets, int E, int vec_per_row, int4* __restrict__ x_perm) {
@@ -367,6 +474,27 @@ cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float*
   return launch_pdl(dispatch_scatter_gather_kernel, dim3(nb * split), dim3(kChunk), sc_smem, s, idx, gate, A, k, E,
                     (const int32_t*)blk_base, (const int32_t*)offsets, cap, split, (const int4*)x, vec_per_row,
                     row_of, perm_token, row_gate, (int4*)x_perm);
+}
+
+cudaError_t launch_dispatch_from_hist(const void* x, const int32_t* idx, const float* gate, int T, int d, int E,
+                                      int k, int dt, int cap, const int32_t* blk_counts, int32_t* counts,
+                                      int32_t* offsets, int32_t* perm_token, int32_t* row_of, float* row_gate,
+                                      void* x_perm, cudaStream_t s) {
+  const int A = T * k;
+  if (A == 0 || E > kChunk) return cudaErrorInvalidValue;
+  const int nb = (A + kChunk - 1) / kChunk;
+  const size_t smem = (size_t)(kWarpsPerChunk * E + kChunk + 2 * E) * sizeof(int);
+  cudaError_t err = cudaFuncSetAttribute(dispatch_from_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+  if (err != cudaSuccess) return err;
+  const size_t elem = dt == MOE_DTYPE_BF16 ? 2 : 4;
+  const int vec_per_row = (int)((size_t)d * elem / 16);
+  int split = (2 * device_sm_count() + nb - 1) / nb;
+  if (split > 8) split = 8;
+  if (split < 1) split = 1;
+  return launch_pdl(dispatch_from_hist_kernel, dim3(nb * split), dim3(kChunk), smem, s, idx, gate, A, k, E, nb,
+                    blk_counts, cap, split, (const int4*)x, vec_per_row, counts, offsets, row_of, perm_token,
+                    row_gate, (int4*)x_perm);
 }
 
 }  // namespace moe

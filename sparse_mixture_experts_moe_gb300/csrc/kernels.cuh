@@ -34,12 +34,16 @@ struct RouterStats {
   float* part;
   float* out;
   int* ticket;
+  // Optional (nullptr: none): the dispatch histogram of each 128-token tile, written by the
+  // tensor-core routers as hist[tile][e] (with k = 2 a tile's assignments are one dispatch chunk).
+  int32_t* hist;
 };
 constexpr int kRouterStatsTokensPerCta = 8;  // fewest tokens any router CTA owns
 
+// *wrote_hist (nullable) tells whether st.hist was filled (only the tensor-core routers do it).
 cudaError_t launch_router_topk(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
                                int dt, int flags, const RouterStats& st, int32_t* idx, float* gate, int* status,
-                               uint64_t timeout_ns, cudaStream_t s);
+                               uint64_t timeout_ns, cudaStream_t s, bool* wrote_hist = nullptr);
 
 // blk_counts / blk_base: [ceil(A / kDispatchChunk), E] int32 scratch each.
 cudaError_t launch_dispatch(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
@@ -49,6 +53,13 @@ cudaError_t launch_dispatch(const void* x, const int32_t* idx, const float* gate
 
 // Same results as launch_dispatch in three launches (count + scan, scatter, gather). `done` is an int
 // that is zero before the call and zero again after it (the workspace header).
+// Scatter + gather from per-chunk histograms already in blk_counts (written by the router for
+// k = 2): every CTA rebuilds totals, offsets and its chunk's bases itself; CTA 0 writes counts and
+// offsets. No count kernel.
+cudaError_t launch_dispatch_from_hist(const void* x, const int32_t* idx, const float* gate, int T, int d, int E,
+                                      int k, int dt, int cap, const int32_t* blk_counts, int32_t* counts,
+                                      int32_t* offsets, int32_t* perm_token, int32_t* row_of, float* row_gate,
+                                      void* x_perm, cudaStream_t s);
 // cap > 0: each expert keeps its first cap assignments in (t, j) order, the rest get row -1.
 cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
                                  int dt, int cap, int32_t* counts, int32_t* offsets, int32_t* perm_token,

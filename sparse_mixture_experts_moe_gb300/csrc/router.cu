@@ -175,20 +175,26 @@ cudaError_t launch_router_t(const void* x, const void* w_r, const float* b_r, in
 
 cudaError_t launch_router_topk(const void* x, const void* w_r, const float* b_r, int Tn, int d, int E, int k,
                                int dt, int flags, const RouterStats& st, int32_t* idx, float* gate, int* status,
-                               uint64_t timeout_ns, cudaStream_t s) {
+                               uint64_t timeout_ns, cudaStream_t s, bool* wrote_hist) {
   const int renorm = (flags & MOE_GATES_RENORMALISE) != 0;
+  if (wrote_hist != nullptr) *wrote_hist = false;
   if (Tn == 0) return cudaSuccess;
   // bf16 with E <= 256 (E % 8 == 0 for TMA row strides): tensor cores; otherwise this CUDA-core kernel.
   if (dt == MOE_DTYPE_BF16 && E <= 256 && E % 8 == 0) {
     const cudaError_t e = launch_router_tc(x, w_r, b_r, Tn, d, E, k, renorm, st, idx, gate, status, timeout_ns, s);
-    if (e != cudaErrorNotSupported) return e;
+    if (e != cudaErrorNotSupported) {
+      if (wrote_hist != nullptr) *wrote_hist = e == cudaSuccess && st.hist != nullptr;
+      return e;
+    }
   }
+  // the CUDA-core router fills no histogram
+  const RouterStats st_nohist{st.part, st.out, st.ticket, nullptr};
   const bool small_e = E <= 256;
   if (dt == MOE_DTYPE_BF16)
-    return small_e ? launch_router_t<__nv_bfloat16, 8>(x, w_r, b_r, Tn, d, E, k, renorm, st, idx, gate, s)
-                   : launch_router_t<__nv_bfloat16, 2>(x, w_r, b_r, Tn, d, E, k, renorm, st, idx, gate, s);
-  return small_e ? launch_router_t<float, 8>(x, w_r, b_r, Tn, d, E, k, renorm, st, idx, gate, s)
-                 : launch_router_t<float, 2>(x, w_r, b_r, Tn, d, E, k, renorm, st, idx, gate, s);
+    return small_e ? launch_router_t<__nv_bfloat16, 8>(x, w_r, b_r, Tn, d, E, k, renorm, st_nohist, idx, gate, s)
+                   : launch_router_t<__nv_bfloat16, 2>(x, w_r, b_r, Tn, d, E, k, renorm, st_nohist, idx, gate, s);
+  return small_e ? launch_router_t<float, 8>(x, w_r, b_r, Tn, d, E, k, renorm, st_nohist, idx, gate, s)
+                 : launch_router_t<float, 2>(x, w_r, b_r, Tn, d, E, k, renorm, st_nohist, idx, gate, s);
 }
 
 }  // namespace moe

@@ -85,12 +85,13 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
   float* s_ent = s_soft + 4 * EN;                                                             // [4]
   int* s_cnt = reinterpret_cast<int*>(s_ent + 4);                                             // [EN]
   const bool stats = st.part != nullptr;
+  const bool hist = st.hist != nullptr;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, DONE = 2 * STAGES + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * BM;
   const int KB = (d + BK - 1) / BK;
-  if (stats)
+  if (stats || hist)
     for (int i = threadIdx.x; i < 5 * EN + 4; i += kThreads) s_soft[i] = 0.f;  // zero bits: also int 0
 
   if (warp == 0 && lane == 0) {
@@ -205,7 +206,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
           if (p < k) {
             topk_idx[(size_t)tok * k + p] = bi[p];
             topk_gate[(size_t)tok * k + p] = expf(bv[p] - m) / gden;
-            if (stats) atomicAdd(&s_cnt[bi[p]], 1);
+            if (stats || hist) atomicAdd(&s_cnt[bi[p]], 1);
           }
         }
       }
@@ -241,6 +242,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
     tc_fence_after();
     tmem_dealloc(tmem_base, kCols);
   }
+  if (hist)
+    for (int e = threadIdx.x; e < E; e += kThreads) st.hist[(size_t)blockIdx.x * E + e] = s_cnt[e];
   if (stats) router_stats_cta(st, s_soft, 4, EN, s_ent, s_cnt, E, Tn, k);
 }
 
@@ -287,7 +290,8 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
   float* s_ent = s_soft + 4 * EN;                  // [4]
   int* s_cnt = reinterpret_cast<int*>(s_ent + 4);  // [EN]
   const bool stats = st.part != nullptr;
-  if (stats)
+  const bool hist = st.hist != nullptr;
+  if (stats || hist)
     for (int i = threadIdx.x; i < 5 * EN + 4; i += kThreads) s_soft[i] = 0.f;
   auto bar = [&](int i) { return smem_u32(bars + i); };
   const int FULL = 0, EMPTY = STAGES, TFULL = 2 * STAGES, DONE = 2 * STAGES + 1;
@@ -441,7 +445,7 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
         sel[p] = bv;
         if (lane == 0) {
           topk_idx[(size_t)tok * k + p] = be;
-          if (stats) atomicAdd(&s_cnt[be], 1);
+          if (stats || hist) atomicAdd(&s_cnt[be], 1);
         }
 #pragma unroll
         for (int j = 0; j < EN / 32; ++j)
@@ -459,11 +463,26 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
       if (lane == 0) s_ent[warp - 2] = went;
     }
   }
-  cluster_sync_all();  // no CTA leaves while a peer may still read its partials
+  if (hist) {
+    // the tile's histogram: every CTA moves its rows' counts into rank 0's (integer adds: exact), so
+    // the statistics partials still sum to each expert's count once
+    __syncthreads();
+    if (rank != 0)
+      for (int e = threadIdx.x; e < E; e += kThreads) {
+        const int v = s_cnt[e];
+        s_cnt[e] = 0;
+        if (v != 0)
+          asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(map_to_cta(smem_u32(s_cnt + e), 0)), "r"(v)
+                       : "memory");
+      }
+  }
+  cluster_sync_all();  // no CTA leaves while a peer may still read its partials (or add to its counts)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kCols);
   }
+  if (hist && rank == 0)
+    for (int e = threadIdx.x; e < E; e += kThreads) st.hist[(size_t)(blockIdx.x / kSplit) * E + e] = s_cnt[e];
   if (stats) router_stats_cta(st, s_soft, 4, EN, s_ent, s_cnt, E, Tn, k);
 }
 
