@@ -35,11 +35,12 @@ namespace {
 
 constexpr int BF = 256;                           // features per pair tile (MMA M)
 constexpr int BR = 256;                           // rows per tile at most (MMA N)
-constexpr int BK = 64;
-constexpr int kTileASubBytes = BK * 64 * 2;       // 8 KB: 64 k-rows x 64 features
-constexpr int kTileABytes = 2 * kTileASubBytes;   // 16 KB: this CTA's 128 features
-constexpr int kTileBBytes = (BR / 2) * BK * 2;    // 16 KB: up to 128 rows of this CTA's half
-constexpr int kStageBytes = kTileABytes + kTileBBytes;
+constexpr int BK = 64;                            // k per MMA-operand block (one 128-byte swizzle row)
+// A pipeline stage holds KSUB consecutive k-blocks (1 or 2) of both operands.
+template <int KSUB> constexpr int kTileASubBytes = KSUB * BK * 64 * 2;  // one 64-feature atom: 8 / 16 KB
+template <int KSUB> constexpr int kTileABytes = 2 * kTileASubBytes<KSUB>;  // this CTA's 128 features
+template <int KSUB> constexpr int kTileBBytes = KSUB * (BR / 2) * BK * 2;  // up to 128 rows of this CTA's half
+template <int KSUB> constexpr int kStageBytes = kTileABytes<KSUB> + kTileBBytes<KSUB>;
 constexpr int kEpiWarps = 16;                     // four per TMEM lane quarter: enough warps to hide
 constexpr int kThreads = 64 + 32 * kEpiWarps;     // the GeLU's dependent chains and the TMEM loads
 constexpr int kSegRows = BR * 4 / kEpiWarps;      // rows of a tile per epilogue warp: 64
@@ -50,8 +51,16 @@ constexpr int kMaxSmem = 232448;
 
 __host__ __device__ constexpr int num_bars(int nst) { return 2 * nst + 5; }
 __host__ __device__ constexpr size_t stg_bytes(int stage) { return stage == 1 ? (size_t)kEpiWarps * kStgBytes : 0; }
-__host__ __device__ constexpr size_t smem_bytes_for(int E, int nst, int stage) {
-  return 1024 + (size_t)nst * kStageBytes + stg_bytes(stage) + 8 * num_bars(nst) + 16 + 4 * (size_t)(E + 1);
+__host__ __device__ constexpr size_t smem_bytes_for(int E, int nst, int stage, int ksub) {
+  return 1024 + (size_t)nst * ksub * 32768 + stg_bytes(stage) + 8 * num_bars(nst) + 16 + 4 * (size_t)(E + 1);
+}
+
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap, int c0, int c1, int c2, int c3,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
 }
 
 // kind::f16, bf16 A and B, fp32 D, A MN-major (bit 15), B K-major, N >> 3 at 17, M >> 4 at 24.
@@ -98,21 +107,26 @@ struct EpiOut { using T = __nv_bfloat16; };
 template <>
 struct EpiOut<2> { using T = float; };
 
-template <int STAGE, int STAGES>
+// tmW: with a_one_box, the weights as [E][N/64][K][64] (4D: one box is this CTA's two 64-feature
+// atoms of KSUB k-blocks, a single copy); otherwise [E][K][N] (3D: one box per atom and k-block).
+// tmX: KSUB = 1, x rows as [rows][K] (2D); KSUB = 2, as [K/64][rows][64] (3D: both k-blocks at once).
+template <int STAGE, int STAGES, int KSUB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-               const __grid_constant__ CUtensorMap tmH, typename EpiOut<STAGE>::T* __restrict__ out, const int32_t* __restrict__ offsets,
-               const float* __restrict__ row_gate, int K, int N, int E, int balanced, int* status,
-               uint64_t timeout_ns) {
+               const __grid_constant__ CUtensorMap tmH, typename EpiOut<STAGE>::T* __restrict__ out,
+               const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
+               int balanced, int a_one_box, int* status, uint64_t timeout_ns) {
   using OutT = typename EpiOut<STAGE>::T;
+  constexpr int kTileABytes_ = kTileABytes<KSUB>, kTileASubBytes_ = kTileASubBytes<KSUB>;
+  constexpr int kTileBBytes_ = kTileBBytes<KSUB>, kStageBytes_ = kStageBytes<KSUB>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sA = base;                          // weights: [stage][2 sub-boxes][64 k][64 f]
-  const uint32_t sB = base + STAGES * kTileABytes;   // rows:    [stage][128 rows][64 k]
-  const uint32_t sStg = base + STAGES * kStageBytes;  // up: per-warp output staging [32 rows][32 f]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * kStageBytes + stg_bytes(STAGE));
+  const uint32_t sA = base;                            // weights: [stage][2 atoms][KSUB*64 k][64 f]
+  const uint32_t sB = base + STAGES * kTileABytes_;    // rows:    [stage][KSUB][128 rows][64 k]
+  const uint32_t sStg = base + STAGES * kStageBytes_;  // up: per-warp output staging [32 rows][32 f]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * kStageBytes_ + stg_bytes(STAGE));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + num_bars(STAGES));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* P = reinterpret_cast<int*>(tmem_slot + 4);
@@ -167,7 +181,7 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 
   const uint32_t tmem_base = *tmem_slot;
   const int NB = (N + BF - 1) / BF;
-  const int KB = (K + BK - 1) / BK;
+  const int KB = (K + BK * KSUB - 1) / (BK * KSUB);  // pipeline stages per item
   const int total_items = P[E] * NB;
 
   if (warp == 0) {
@@ -183,12 +197,19 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_or_abort(bar(EMPTY + stage), phase ^ 1u, timeout_ns, abort_flag, status, 41)) goto producer_out;
           const uint32_t full_leader = map_to_cta(bar(FULL + stage), 0);
-          if (leader) mbar_arrive_expect_tx(bar(FULL + stage), 2 * kStageBytes);  // both CTAs' bytes
+          if (leader) mbar_arrive_expect_tx(bar(FULL + stage), 2 * kStageBytes_);  // both CTAs' bytes
+          if (a_one_box) {
+            tma_load_4d_pair(sA + stage * kTileABytes_, &tmW, 0, kb * BK * KSUB, feat / 64, it.e, full_leader);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-            tma_load_3d_pair(sA + stage * kTileABytes + j * kTileASubBytes, &tmW, feat + 64 * j, kb * BK, it.e,
-                             full_leader);
-          tma_load_2d_pair(sB + stage * kTileBBytes, &tmX, kb * BK, frow, full_leader);
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int u = 0; u < KSUB; ++u)
+                tma_load_3d_pair(sA + stage * kTileABytes_ + j * kTileASubBytes_ + u * BK * 128, &tmW, feat + 64 * j,
+                                 (kb * KSUB + u) * BK, it.e, full_leader);
+          }
+          if (KSUB == 1) tma_load_2d_pair(sB + stage * kTileBBytes_, &tmX, kb * BK, frow, full_leader);
+          else tma_load_3d_pair(sB + stage * kTileBBytes_, &tmX, 0, frow, kb * KSUB, full_leader);
           filled |= 1u << stage;
           fill_phase = (fill_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -219,13 +240,16 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
           for (int kb = 0; kb < KB; ++kb) {
             if (!wait_or_abort(bar(FULL + stage), phase, timeout_ns, abort_flag, status, 42)) goto mma_out;
             tc_fence_after();
-            // A: MN-major, two 64-feature atoms 8 KB apart; B: K-major rows.
-            const uint64_t a_desc = make_smem_desc_sw128(sA + stage * kTileABytes, kTileASubBytes, 1024);
-            const uint64_t b_desc = make_smem_desc_sw128(sB + stage * kTileBBytes, 16, 1024);
+            // A: MN-major, two 64-feature atoms kTileASubBytes apart, 128 bytes per k; B: K-major
+            // rows, one 16 KB block per 64 k.
+            const uint64_t a_desc = make_smem_desc_sw128(sA + stage * kTileABytes_, kTileASubBytes_, 1024);
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              tc_mma_f16_pair(d_tmem, a_desc + (uint64_t)((kk * 16 * 128) >> 4), b_desc + (uint64_t)((kk * 32) >> 4),
-                              idesc, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < KSUB * BK / 16; ++kk) {
+              const uint64_t b_desc =
+                  make_smem_desc_sw128(sB + stage * kTileBBytes_ + (kk / 4) * (kTileBBytes_ / KSUB), 16, 1024);
+              tc_mma_f16_pair(d_tmem, a_desc + (uint64_t)((kk * 16 * 128) >> 4),
+                              b_desc + (uint64_t)(((kk % 4) * 32) >> 4), idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
             tc_commit_pair(bar(EMPTY + stage), 0x3);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
@@ -312,11 +336,19 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   }
 }
 
-template <int STAGE, int STAGES>
-cudaError_t launch_tct(const FfnArgs& p, EncodeTiledFn enc, const CUtensorMap& tmW, const CUtensorMap& tmH,
-                       size_t smem, cudaStream_t s) {
+// 128-byte-swizzled bf16 tensor map of up to four dimensions (strides in bytes, dims 1..rank-1).
+bool encode_sw128(EncodeTiledFn enc, CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+                  const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides_bytes, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int STAGE, int STAGES, int KSUB>
+cudaError_t launch_tct(const FfnArgs& p, EncodeTiledFn enc, const CUtensorMap& tmH, size_t smem, cudaStream_t s) {
   using OutT = typename EpiOut<STAGE>::T;
-  auto kern = ffn_tct_kernel<STAGE, STAGES>;
+  auto kern = ffn_tct_kernel<STAGE, STAGES, KSUB>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   // Persistent: as many pairs as can be resident at once (two-SM clusters may not tile every SM).
@@ -333,19 +365,39 @@ cudaError_t launch_tct(const FfnArgs& p, EncodeTiledFn enc, const CUtensorMap& t
   const long long active = p.rows < p.E ? p.rows : p.E;
   const long long rpe = (p.rows + active - 1) / active;
   const int balanced = active * ((rpe + BR - 1) / BR) * NB >= 3LL * clusters ? 0 : 1;
-  CUtensorMap tmX;
-  {
-    // rows of x_perm (or h): K-major B operand, 64 k x 128 rows per box (one CTA's half of a tile)
+  CUtensorMap tmW, tmX;
+  // Weights [E][K][N], MN-major A operand. N a multiple of 64: viewed as [E][N/64][K][64] so one
+  // box brings both of this CTA's 64-feature atoms (the fewer copies a stage takes, the faster the
+  // SM's copy engine feeds it); otherwise one [KSUB*64 k][64 f] box per atom and k-block.
+  const int a_one_box = p.N % 64 == 0;
+  if (a_one_box) {
+    const cuuint64_t dims[4] = {64, (cuuint64_t)p.K, (cuuint64_t)p.N / 64, (cuuint64_t)p.E};
+    const cuuint64_t str[3] = {(cuuint64_t)p.N * 2, 128, (cuuint64_t)p.K * p.N * 2};
+    const cuuint32_t box[4] = {64, BK * KSUB, 2, 1};
+    if (!encode_sw128(enc, &tmW, p.w, 4, dims, str, box)) return cudaErrorInvalidValue;
+  } else {
+    const cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.K, (cuuint64_t)p.E};
+    const cuuint64_t str[2] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.K * p.N * 2};
+    const cuuint32_t box[3] = {64, BK, 1};
+    if (!encode_sw128(enc, &tmW, p.w, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  // Rows of x_perm (or h): K-major B operand, 128 rows (one CTA's half of a tile) per box: a
+  // [rows][K] view for one k-block, a [K/64][rows][64] view (K a multiple of 128) for two.
+  if (KSUB == 1) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.rows};
     const cuuint64_t str[1] = {(cuuint64_t)p.K * 2};
     const cuuint32_t box[2] = {BK, BR / 2};
-    if (!encode_tmap(enc, &tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, 2, dims, str, box))
-      return cudaErrorInvalidValue;
+    if (!encode_sw128(enc, &tmX, p.a, 2, dims, str, box)) return cudaErrorInvalidValue;
+  } else {
+    const cuuint64_t dims[3] = {64, (cuuint64_t)p.rows, (cuuint64_t)p.K / 64};
+    const cuuint64_t str[2] = {(cuuint64_t)p.K * 2, 128};
+    const cuuint32_t box[3] = {64, BR / 2, KSUB};
+    if (!encode_sw128(enc, &tmX, p.a, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   const long long max_items = ((long long)(p.rows + BR - 1) / BR + p.E) * NB;
   long long pairs = clusters < max_items ? clusters : max_items;
   return launch_pdl(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), smem, s, tmX, tmW, tmH, (OutT*)p.out,
-                    p.offsets, p.row_gate, p.K, p.N, p.E, balanced, p.status, p.timeout_ns);
+                    p.offsets, p.row_gate, p.K, p.N, p.E, balanced, a_one_box, p.status, p.timeout_ns);
 }
 
 }  // namespace
@@ -355,29 +407,31 @@ cudaError_t launch_ffn_tensor_t(const FfnArgs& p, cudaStream_t s) {
   if (p.dt != MOE_DTYPE_BF16) return cudaErrorNotSupported;
   EncodeTiledFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
-  CUtensorMap tmW;
-  {
-    // weights [E][K][N]: MN-major A operand, 64 features x 64 k per box
-    const cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.K, (cuuint64_t)p.E};
-    const cuuint64_t str[2] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.K * p.N * 2};
-    const cuuint32_t box[3] = {64, BK, 1};
-    if (!encode_tmap(enc, &tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.w, 3, dims, str, box))
-      return cudaErrorInvalidValue;
-  }
-  CUtensorMap tmH = tmW;  // up: h [rows][N] bf16, 32 features x CR rows per store, no swizzle
+  // Two k-blocks per stage (64 KB, three stages) when K allows it and each weight slab serves about
+  // two or more row tiles, i.e. is mostly read from L2: fewer, larger copies per MMA (e16 up:
+  // 73.7 -> 70.6 us). When every slab streams from HBM once (prefill), six or seven 32 KB stages
+  // hide HBM latency better (1.34 vs 1.35 ms).
+  const long long active = p.rows < p.E ? p.rows : p.E;
+  const long long rpe = (p.rows + active - 1) / active;
+  const bool ksub2_ok = p.K % 128 == 0 && rpe >= 2 * BR;
+  CUtensorMap tmH{};  // up: h [rows][N] bf16, 32 features x CR rows per store, no swizzle
   if (p.stage == 1) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.rows};
     const cuuint64_t str[1] = {(cuuint64_t)p.N * 2};
     const cuuint32_t box[2] = {32, CR};
     if (!encode_tmap_plain(enc, &tmH, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.out, 2, dims, str, box))
       return cudaErrorInvalidValue;
-    const bool six = smem_bytes_for(p.E, 6, 1) <= (size_t)kMaxSmem;
-    const size_t smem = smem_bytes_for(p.E, six ? 6 : 5, 1);
-    return six ? launch_tct<1, 6>(p, enc, tmW, tmH, smem, s) : launch_tct<1, 5>(p, enc, tmW, tmH, smem, s);
+    if (ksub2_ok && smem_bytes_for(p.E, 3, 1, 2) <= (size_t)kMaxSmem)
+      return launch_tct<1, 3, 2>(p, enc, tmH, smem_bytes_for(p.E, 3, 1, 2), s);
+    const bool six = smem_bytes_for(p.E, 6, 1, 1) <= (size_t)kMaxSmem;
+    const size_t smem = smem_bytes_for(p.E, six ? 6 : 5, 1, 1);
+    return six ? launch_tct<1, 6, 1>(p, enc, tmH, smem, s) : launch_tct<1, 5, 1>(p, enc, tmH, smem, s);
   }
-  const bool seven = smem_bytes_for(p.E, 7, 2) <= (size_t)kMaxSmem;
-  const size_t smem = smem_bytes_for(p.E, seven ? 7 : 6, 2);
-  return seven ? launch_tct<2, 7>(p, enc, tmW, tmH, smem, s) : launch_tct<2, 6>(p, enc, tmW, tmH, smem, s);
+  if (ksub2_ok && smem_bytes_for(p.E, 3, 2, 2) <= (size_t)kMaxSmem)
+    return launch_tct<2, 3, 2>(p, enc, tmH, smem_bytes_for(p.E, 3, 2, 2), s);
+  const bool seven = smem_bytes_for(p.E, 7, 2, 1) <= (size_t)kMaxSmem;
+  const size_t smem = smem_bytes_for(p.E, seven ? 7 : 6, 2, 1);
+  return seven ? launch_tct<2, 7, 1>(p, enc, tmH, smem, s) : launch_tct<2, 6, 1>(p, enc, tmH, smem, s);
 }
 
 }  // namespace moe

@@ -470,6 +470,36 @@ def test_forward_writes_router_stats():
     assert rel_rms_err(to_f64(out), ref["out"]) < TOL[BF16]
 
 
+HIST_CASES = [
+    dict(T=100, d=2048, E=64, cap_factor=0.0),     # split-K cluster router: ranks add into rank 0's counts
+    dict(T=1000, d=128, E=256, cap_factor=0.0),    # E = 256: one chunk group per expert
+    dict(T=2049, d=64, E=16, cap_factor=1.1),      # 17 chunks, a 1-token tail tile, capacity drops
+    dict(T=777, d=256, E=8, cap_factor=0.6),       # most assignments dropped
+]
+
+
+@pytest.mark.parametrize("cfg", HIST_CASES, ids=["split", "e256", "tail_cap", "cap_small"])
+def test_forward_router_histogram_dispatch(cfg):
+    """Top-2 bf16 forward: the router's per-tile histograms feed the one-kernel dispatch. Counts,
+    indices and output against the oracle, with router statistics written in the same call."""
+    T, d, E = cfg["T"], cfg["d"], cfg["E"]
+    c = make_case(T=T, d=d, F=128, E=E, k=2, dt=BF16, bias=_skewed(E))
+    C = oracle.capacity(T, 2, E, cfg["cap_factor"]) if cfg["cap_factor"] > 0 else 0
+    out = torch.empty((T, d), dtype=torch.float32, device=DEV)
+    idx = torch.empty((T, 2), dtype=torch.int32, device=DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    stats = torch.empty(moe.router_stats_len(E), dtype=torch.float32, device=DEV)
+    ws = workspace_for(c)
+    moe.forward(c.x, c.w_r, c.b_r, c.w1, c.w2, T, d, c.F, E, 2, BF16, out, ws, topk_idx=idx, counts=counts,
+                out_dt=F32, capacity=C, router_stats=stats)
+    assert moe.get_device_status(ws)[0] == moe.MOE_OK
+    ref = oracle.forward(c.x64, c.wr64, c.w1_host(), c.w2_host(), 2, c.br64, cap=C if C else None)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    assert np.array_equal(counts.cpu().numpy(), oracle.dispatch(ref["idx"], E, cap=C if C else None)["counts"])
+    check_stats(stats, ref["logits"], ref["idx"], T, E, 2)
+    assert rel_rms_err(to_f64(out), ref["out"]) < output_tolerance(c, ref, cap=C if C else None)
+
+
 def test_router_stats_rejects_small_workspace():
     c = make_case(T=256, d=64, F=64, E=16, k=2, dt=BF16)
     idx = torch.empty((c.T, c.k), dtype=torch.int32, device=DEV)
