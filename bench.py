@@ -38,11 +38,14 @@ METRIC = "MoE-layer tokens/s; % of BF16 tensor peak (prefill) / % HBM BW (decode
 DEFAULT_WORKLOAD = "e16_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # router 1, dispatch 2 (count + scan, scatter + gather), up 1, down 1, combine 1; with top-2 and the
-# tensor-core router (bf16, E <= 256, E % 8 == 0) the router writes the dispatch histogram: dispatch 1
+# tensor-core router (bf16, E <= 256, E % 8 == 0) the router writes the dispatch histogram: dispatch 1;
+# a bf16 batch of at most 8 tokens (E even) routes and dispatches in one launch: 4 in all
 KERNELS_PER_STEP = 6
 
 
-def kernels_per_step(k, E, bf16):
+def kernels_per_step(T, k, E, bf16):
+    if bf16 and T <= 8 and E % 2 == 0:
+        return 4
     fused = k == 2 and bf16 and E <= 256 and E % 8 == 0
     return KERNELS_PER_STEP - 1 if fused else KERNELS_PER_STEP
 L2_BYTES = 126 * 2**20
@@ -370,7 +373,7 @@ def run_ours(args, w, rank, world, device):
         torch.cuda.synchronize()
         ms_direct = max_over_ranks(ed0.elapsed_time(ed1), world, device) / args.steps
 
-    # --- per-kernel timing: the same step as its separate C ABI calls, events between them
+    # --- per-kernel timing: the step as its separate C ABI calls (dispatch: the two-kernel public entry)
     idx = torch.empty((T, k), dtype=torch.int32, device=device)
     gate = torch.empty((T, k), dtype=torch.float32, device=device)
     counts = torch.empty(E, dtype=torch.int32, device=device)
@@ -381,31 +384,39 @@ def run_ours(args, w, rank, world, device):
     x_perm = torch.empty((A, d), dtype=x.dtype, device=device)
     h = torch.empty((A, F), dtype=x.dtype, device=device)
     y_perm = torch.empty((A, d), dtype=torch.float32, device=device)
-    names = ["router_topk", "dispatch", "expert_up", "expert_down", "combine"]
+    # Each kernel is launched R times back to back between two events on the launching stream, so
+    # the host's per-call work (argument marshalling, tensor maps) overlaps the previous launch and
+    # only device time is measured; repeated calls on the same inputs give the same outputs.
     reps = max(args.steps, 10)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(reps)]
-    for r in range(reps):
-        e = evs[r]
-        e[0].record(stream)
-        moe.router_topk(x, w_r, b_r, T, d, E, k, dt, idx, gate)
-        e[1].record(stream)
-        moe.dispatch(x, idx, gate, T, d, E, k, dt, counts, offsets, perm, row_of, row_gate, x_perm, ws)
-        e[2].record(stream)
+
+    def up_call():
         if qbits:
             moe.expert_up_q(x_perm, q1[0], q1[1], offsets, T, d, F, E, k, qbits, h)
         else:
             moe.expert_up(x_perm, w1, offsets, T, d, F, E, k, dt, h, ws, path=fpath)
-        e[3].record(stream)
+
+    def down_call():
         if qbits:
             moe.expert_down_q(h, q2[0], q2[1], offsets, row_gate, T, d, F, E, k, qbits, y_perm)
         else:
             moe.expert_down(h, w2, offsets, row_gate, T, d, F, E, k, dt, y_perm, ws, path=fpath)
-        e[4].record(stream)
-        moe.combine(y_perm, row_of, T, d, k, dt, out)
-        e[5].record(stream)
-    torch.cuda.synchronize()
-    kern_ms = {n: statistics.mean(evs[r][i].elapsed_time(evs[r][i + 1]) for r in range(reps))
-               for i, n in enumerate(names)}
+
+    calls = [("router_topk", lambda: moe.router_topk(x, w_r, b_r, T, d, E, k, dt, idx, gate)),
+             ("dispatch", lambda: moe.dispatch(x, idx, gate, T, d, E, k, dt, counts, offsets, perm, row_of, row_gate,
+                                               x_perm, ws)),
+             ("expert_up", up_call), ("expert_down", down_call),
+             ("combine", lambda: moe.combine(y_perm, row_of, T, d, k, dt, out))]
+    kern_ms = {}
+    for name, fn in calls:
+        fn()  # warm-up, and the inputs of the next kernel
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(reps):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        kern_ms[name] = ev0.elapsed_time(ev1) / reps
     counts_h = counts.cpu().numpy()
     touched = int((counts_h > 0).sum())
 
@@ -507,7 +518,7 @@ def run_ours(args, w, rank, world, device):
         "experts_touched": touched,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * x.element_size(),
                 "d2h_bytes_per_step": out.numel() * out.element_size()},
-        "gpu_launches": kernels_per_step(k, E, dt == 1) * args.steps,
+        "gpu_launches": kernels_per_step(T, k, E, dt == 1) * args.steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not qbits:

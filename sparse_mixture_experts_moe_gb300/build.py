@@ -21,9 +21,9 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
 
-LIB_SOURCES = ["api.cu", "router.cu", "router_tc.cu", "dispatch.cu", "dispatch_noalloc.cu", "ffn_simt.cu", "ffn_stream.cu",
-               "ffn_tc.cu", "ffn_tc2.cu", "combine.cu", "graph.cu",
-               "quant.cu", "ffn_tct.cu"]
+LIB_SOURCES = ["api.cu", "router.cu", "router_tc.cu", "router_small.cu", "dispatch.cu", "dispatch_noalloc.cu",
+               "ffn_simt.cu", "ffn_stream.cu", "ffn_tc.cu", "ffn_tc2.cu", "combine.cu", "graph.cu", "quant.cu",
+               "ffn_tct.cu"]
 LIB_PATH = os.path.join(PKG, "libmoe.so")
 INPUTGEN_SRC = os.path.join(ROOT, "inputgen", "fill.cu")
 INPUTGEN_PATH = os.path.join(ROOT, "inputgen", "libinputgen.so")

@@ -224,9 +224,11 @@ moe_status moe_dispatch_ex(const void* x, const int32_t* topk_idx, const float* 
                                           at<int>(workspace, L.header) + 2, (cudaStream_t)stream));
 }
 
+// a_rows (nullable): row r of `a` is a[a_rows[r]] (the weight-streaming path only).
 static moe_status expert_half(int stage, const void* a, const void* w, const int32_t* offsets,
                               const float* row_gate, int T, int d, int F, int E, int k, moe_dtype dt, moe_path path,
-                              void* out, void* workspace, size_t ws_bytes, void* stream) {
+                              void* out, void* workspace, size_t ws_bytes, void* stream,
+                              const int32_t* a_rows = nullptr) {
   if (!sizes_ok(T, d, F, E, k, dt) || !path_ok(path, dt)) return MOE_ERR_INVALID_ARG;
   if (workspace == nullptr || ws_bytes < kWsHeaderBytes || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
@@ -240,6 +242,7 @@ static moe_status expert_half(int stage, const void* a, const void* w, const int
   args.N = stage == 1 ? F : d;
   args.status = at<int>(workspace, 0);
   args.timeout_ns = wait_timeout_ns();
+  args.a_rows = a_rows;
   return run_ffn_half(path, args, (cudaStream_t)stream);
 }
 
@@ -293,7 +296,7 @@ inline bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7
 
 moe_status expert_half_q(int stage, const void* a, const void* codes, const float* scale_min,
                          const int32_t* offsets, const float* row_gate, int T, int d, int F, int E, int k, int bits,
-                         void* out, void* stream) {
+                         void* out, void* stream, const int32_t* a_rows = nullptr) {
   if (!sizes_ok(T, d, F, E, k, MOE_DTYPE_BF16)) return MOE_ERR_INVALID_ARG;
   const int K = stage == 1 ? d : F, N = stage == 1 ? F : d;
   if (!qsizes_ok(K, N, E, bits)) return MOE_ERR_INVALID_ARG;
@@ -302,7 +305,7 @@ moe_status expert_half_q(int stage, const void* a, const void* codes, const floa
       (stage == 2 && row_gate == nullptr))
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(a) || !aligned16(codes) || !aligned8(scale_min) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
-  QFfnArgs p{a, codes, scale_min, offsets, row_gate, out, T * k, K, N, E, bits, stage};
+  QFfnArgs p{a, codes, scale_min, offsets, row_gate, out, T * k, K, N, E, bits, stage, a_rows};
   return cuda_status(launch_ffn_stream_q(p, (cudaStream_t)stream));
 }
 }  // namespace
@@ -351,10 +354,21 @@ namespace {
 // Router, then dispatch. With k = 2 a tensor-core router tile (128 tokens) holds exactly one dispatch
 // chunk (256 assignments), so the router also writes each chunk's expert histogram and the dispatch
 // needs no count kernel; otherwise (or when the CUDA-core router ran) the two-kernel dispatch.
+// small_ok: the expert GEMMs will stream weights; then a batch of at most 8 tokens (no statistics)
+// takes the one-launch router + dispatch, which writes no x_perm: *rows_via_perm tells the caller
+// to read x through perm_token instead.
 moe_status route_and_dispatch(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
                               moe_dtype dt, int flags, int capacity, RouterStats rs, int32_t* idx, float* gate,
                               int32_t* cnt, int32_t* offs, int32_t* perm, int32_t* rowof, float* rgate, void* xp,
-                              const Layout& L, void* workspace, size_t ws_bytes, void* stream) {
+                              const Layout& L, void* workspace, size_t ws_bytes, void* stream, bool small_ok,
+                              bool* rows_via_perm) {
+  *rows_via_perm = false;
+  if (small_ok && rs.part == nullptr && route_small_ok(T, d, E, k, dt, L.end - L.y_perm)) {
+    *rows_via_perm = true;
+    return cuda_status(launch_route_small(x, w_r, b_r, T, d, E, k, (flags & MOE_GATES_RENORMALISE) != 0, capacity,
+                                          at<float>(workspace, L.y_perm), at<int>(workspace, 0) + 2, idx, gate, cnt,
+                                          offs, perm, rowof, rgate, (cudaStream_t)stream));
+  }
   rs.hist = k * 128 == kDispatchChunk ? at<int32_t>(workspace, L.blk_counts) : nullptr;
   bool wrote_hist = false;
   moe_status st = cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, flags, rs, idx, gate,
@@ -396,10 +410,14 @@ moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, cons
   void* yp = at<void>(workspace, L.y_perm);
   const RouterStats rs{router_stats != nullptr ? at<float>(workspace, L.stats_part) : nullptr, router_stats,
                        at<int>(workspace, 0) + 3};
+  const bool small_ok = resolve_path(path, dt, T * k, E, F) == MOE_PATH_STREAM &&
+                        resolve_path(path, dt, T * k, E, d) == MOE_PATH_STREAM;
+  bool via_perm = false;
   moe_status st = route_and_dispatch(x, w_r, b_r, T, d, E, k, dt, flags, capacity, rs, idx, gate, cnt, offs, perm,
-                                     rowof, rgate, xp, L, workspace, ws_bytes, stream);
+                                     rowof, rgate, xp, L, workspace, ws_bytes, stream, small_ok, &via_perm);
   if (st != MOE_OK) return st;
-  st = moe_expert_up_ex(xp, w1, offs, T, d, F, E, k, dt, path, h, workspace, ws_bytes, stream);
+  st = via_perm ? expert_half(1, x, w1, offs, nullptr, T, d, F, E, k, dt, path, h, workspace, ws_bytes, stream, perm)
+                : moe_expert_up_ex(xp, w1, offs, T, d, F, E, k, dt, path, h, workspace, ws_bytes, stream);
   if (st != MOE_OK) return st;
   st = moe_expert_down_ex(h, w2, offs, rgate, T, d, F, E, k, dt, path, yp, workspace, ws_bytes, stream);
   if (st != MOE_OK) return st;
@@ -431,11 +449,13 @@ moe_status moe_forward_q(const void* x, const void* w_r, const float* b_r, const
   void* yp = at<void>(workspace, L.y_perm);
   const RouterStats rs{router_stats != nullptr ? at<float>(workspace, L.stats_part) : nullptr, router_stats,
                        at<int>(workspace, 0) + 3};
-  moe_status st = route_and_dispatch(x, w_r, b_r, T, d, E, k, dt, flags, capacity, rs, idx, gate, cnt, offs,
-                                     at<int32_t>(workspace, L.perm_token), rowof, rgate, xp, L, workspace, ws_bytes,
-                                     stream);
+  int32_t* perm = at<int32_t>(workspace, L.perm_token);
+  bool via_perm = false;
+  moe_status st = route_and_dispatch(x, w_r, b_r, T, d, E, k, dt, flags, capacity, rs, idx, gate, cnt, offs, perm,
+                                     rowof, rgate, xp, L, workspace, ws_bytes, stream, true, &via_perm);
   if (st != MOE_OK) return st;
-  st = moe_expert_up_q(xp, w1_codes, w1_scale_min, offs, T, d, F, E, k, bits, h, stream);
+  st = via_perm ? expert_half_q(1, x, w1_codes, w1_scale_min, offs, nullptr, T, d, F, E, k, bits, h, stream, perm)
+                : moe_expert_up_q(xp, w1_codes, w1_scale_min, offs, T, d, F, E, k, bits, h, stream);
   if (st != MOE_OK) return st;
   st = moe_expert_down_q(h, w2_codes, w2_scale_min, offs, rgate, T, d, F, E, k, bits, yp, stream);
   if (st != MOE_OK) return st;

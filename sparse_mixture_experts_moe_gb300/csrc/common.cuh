@@ -173,12 +173,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
       ::"r"(dst), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
-// Pulls a box of a tensor into L2 ahead of its TMA load (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0), "r"(c1),
-               "r"(c2)
-               : "memory");
-}
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
                ::"l"(tmap), "r"(c0), "r"(c1), "r"(src)

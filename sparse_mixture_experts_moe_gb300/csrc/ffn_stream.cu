@@ -38,16 +38,18 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
   v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
 }
 
-// Rows rp .. rp+R-1, k-range [kc, kc+kn) of the bf16 activations -> sA as fp32 (row stride KC),
-// with 16-byte loads; K and kn are multiples of 8 and the rows 16-byte aligned.
+// Rows rp .. rp+R-1 (through a_rows when given), k-range [kc, kc+kn) of the bf16 activations ->
+// sA as fp32 (row stride KC), with 16-byte loads; K and kn are multiples of 8 and the rows 16-byte
+// aligned.
 template <int KC>
-__device__ __forceinline__ void stage_rows(const __nv_bfloat16* __restrict__ a, int K, int rp, int R, int kc, int kn,
-                                           float* sA) {
+__device__ __forceinline__ void stage_rows(const __nv_bfloat16* __restrict__ a, const int32_t* __restrict__ a_rows,
+                                           int K, int rp, int R, int kc, int kn, float* sA) {
   const int per_row = KC / 8;
   for (int i = threadIdx.x; i < R * per_row; i += kThreads) {
     const int r = i / per_row, kk = (i % per_row) * 8;
+    const size_t src = a_rows != nullptr ? (size_t)a_rows[rp + r] : (size_t)(rp + r);
     float v[8];
-    if (kk < kn) bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(a + (size_t)(rp + r) * K + kc + kk)), v);
+    if (kk < kn) bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(a + src * K + kc + kk)), v);
     else
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] = 0.f;
@@ -61,9 +63,9 @@ __device__ __forceinline__ void stage_rows(const __nv_bfloat16* __restrict__ a, 
 // RMAX rows of an expert per pass over its weights (more rows take more passes).
 template <int STAGE, typename OutT, int RMAX>
 __global__ void __launch_bounds__(kThreads, 2)
-ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ w,
-                  const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
-                  OutT* __restrict__ out) {
+ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restrict__ a_rows,
+                  const __nv_bfloat16* __restrict__ w, const int32_t* __restrict__ offsets,
+                  const float* __restrict__ row_gate, int K, int N, int E, OutT* __restrict__ out) {
   constexpr int kUnroll = unroll_for<RMAX>();
   constexpr int KC = kc_for<RMAX>();
   extern __shared__ __align__(16) float smem[];
@@ -125,7 +127,7 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __re
         uint4 cur[kUnroll], nxt[kUnroll];
         load_batch(0, cur);
         __syncthreads();
-        stage_rows<KC>(a, K, rp, R, kc, kn, sA);
+        stage_rows<KC>(a, a_rows, K, rp, R, kc, kn, sA);
         __syncthreads();
         for (int k0 = 0; k0 < kn; k0 += KSTEP * kUnroll) {
           if (k0 + KSTEP * kUnroll < kn) load_batch(k0 + KSTEP * kUnroll, nxt);
@@ -193,7 +195,7 @@ cudaError_t launch_t(const FfnArgs& p, cudaStream_t s) {
   const long long max_units = (long long)(p.rows < p.E ? p.rows : p.E) * nslab;
   long long grid = (long long)device_sm_count() * (RMAX <= 2 ? 8 : 4);
   if (grid > max_units) grid = max_units;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, (const __nv_bfloat16*)p.a,
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, (const __nv_bfloat16*)p.a, p.a_rows,
                     (const __nv_bfloat16*)p.w, p.offsets, p.row_gate, p.K, p.N, p.E, (OutT*)p.out);
 }
 

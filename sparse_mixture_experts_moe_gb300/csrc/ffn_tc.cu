@@ -17,8 +17,8 @@
 //   warp 0      TMA producer (one lane): A tile + 4 B sub-tiles per stage, 4 stages (3 when E is
 //               large)
 //   warp 1      TMEM allocator and MMA issuer (one lane)
-//   warps 2..9  epilogue (two per TMEM lane quarter, half the columns each): tcgen05.ld -> GeLU -> bf16 (up) or gate -> fp32 (down) -> swizzled
-//               staging -> TMA store
+//   warps 2..9  epilogue (two per TMEM lane quarter, half the columns each): tcgen05.ld ->
+//               GeLU -> bf16 (up) or gate -> fp32 (down) -> swizzled staging -> TMA store
 // Work items are (expert, 256-column block, 128-row tile), the row tile fastest, so the
 // CTAs that run at the same time share the same weight tile (read once from HBM, then from
 // L2). The item list is derived on the device from `offsets`: no host round trip.

@@ -72,7 +72,7 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* row_of, int T, int
 // Expert FFN halves. stage 1: out = GeLU(a W1[e]) (N = F, K = d);
 // stage 2: out = row_gate * (a W2[e]) (N = d, K = F).
 struct FfnArgs {
-  const void* a;          // [rows, K]
+  const void* a;          // [rows, K], or (a_rows != nullptr) row r is a[a_rows[r]]
   const void* w;          // [E, K, N]
   const int32_t* offsets; // [E+1]
   const float* row_gate;  // [rows] (stage 2)
@@ -80,6 +80,7 @@ struct FfnArgs {
   int rows, K, N, E, dt, stage;
   int* status;
   uint64_t timeout_ns;
+  const int32_t* a_rows;  // nullable row map of `a` (weight-streaming kernels only)
 };
 cudaError_t launch_ffn_simt(const FfnArgs& a, cudaStream_t s);
 
@@ -93,6 +94,7 @@ struct QFfnArgs {
   const float* row_gate;  // [rows] (stage 2)
   void* out;              // [rows, N]: bf16 (stage 1) or fp32 (stage 2)
   int rows, K, N, E, bits, stage;
+  const int32_t* a_rows;  // nullable: row r of `a` is a[a_rows[r]]
 };
 cudaError_t launch_quantize(const void* w, int K, int N, int E, int dt, int bits, void* codes, float* scale_min,
                             cudaStream_t s);
@@ -106,6 +108,14 @@ cudaError_t launch_ffn_tensor_pair(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_ffn_tensor_t(const FfnArgs& a, cudaStream_t s);
 
 cudaError_t launch_selftest_wait(int* status, uint64_t timeout_ns, cudaStream_t s);
+
+// Router + dispatch for T <= 8 in one launch (router_small.cu): routing arrays only, no x_perm.
+// partials: (#clusters) x T x E floats of scratch; ticket: zero before, reset to zero after.
+bool route_small_ok(int T, int d, int E, int k, int dt, size_t partial_bytes_avail);
+cudaError_t launch_route_small(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
+                               int renorm, int cap, float* partials, int* ticket, int32_t* idx, float* gate,
+                               int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* row_of,
+                               float* row_gate, cudaStream_t s);
 
 // Router on the tensor cores (bf16, E <= 256, E % 8 == 0). Returns cudaErrorNotSupported otherwise.
 cudaError_t launch_router_tc(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,

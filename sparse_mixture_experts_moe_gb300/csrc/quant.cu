@@ -130,14 +130,15 @@ __device__ __forceinline__ void int8_row(uint32_t w0, uint32_t w1, uint64_t (&c)
 // Rows rp .. rp+R-1, k-range [kc, kc+kn) of the bf16 activations -> sA as fp32 (row stride KC),
 // with 16-byte loads (K and kn are multiples of 64, rows 16-byte aligned).
 template <int KC>
-__device__ __forceinline__ void stage_rows_q(const __nv_bfloat16* __restrict__ a, int K, int rp, int R, int kc,
-                                             int kn, float* sA) {
+__device__ __forceinline__ void stage_rows_q(const __nv_bfloat16* __restrict__ a, const int32_t* __restrict__ a_rows,
+                                             int K, int rp, int R, int kc, int kn, float* sA) {
   const int per_row = KC / 8;
   for (int i = threadIdx.x; i < R * per_row; i += kThreads) {
     const int r = i / per_row, kk = (i % per_row) * 8;
+    const size_t src = a_rows != nullptr ? (size_t)a_rows[rp + r] : (size_t)(rp + r);
     float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
     if (kk < kn) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(a + (size_t)(rp + r) * K + kc + kk));
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(a + src * K + kc + kk));
       lo = make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
       hi = make_float4(bf16lo(u.z), bf16hi(u.z), bf16lo(u.w), bf16hi(u.w));
     }
@@ -149,7 +150,8 @@ __device__ __forceinline__ void stage_rows_q(const __nv_bfloat16* __restrict__ a
 
 template <int BITS, int STAGE, typename OutT, int RMAX>
 __global__ void __launch_bounds__(kThreads, 2)
-ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const uint4* __restrict__ codes,
+ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restrict__ a_rows,
+                    const uint4* __restrict__ codes,
                     const float2* __restrict__ sm, const int32_t* __restrict__ offsets,
                     const float* __restrict__ row_gate, int K, int N, int E, OutT* __restrict__ out) {
   constexpr int KT = 16 / BITS;  // k-rows per tile: 128 bits / (8 columns x BITS)
@@ -214,7 +216,7 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const uint4* __restrict
         uint4 cur[kUnroll], nxt[kUnroll];
         load_batch(0, cur);  // in flight while the activations are staged
         __syncthreads();
-        stage_rows_q<KC>(a, K, rp, R, kc, kn, sA);
+        stage_rows_q<KC>(a, a_rows, K, rp, R, kc, kn, sA);
         __syncthreads();
         for (int g0 = 0; g0 < gn; g0 += GSTEP * kUnroll) {
           if (g0 + GSTEP * kUnroll < gn) load_batch(g0 + GSTEP * kUnroll, nxt);
@@ -288,7 +290,7 @@ cudaError_t launch_q(const QFfnArgs& p, cudaStream_t s) {
   const long long max_units = (long long)(p.rows < p.E ? p.rows : p.E) * nslab;
   long long grid = (long long)device_sm_count() * (RMAX <= 2 ? 8 : 4);
   if (grid > max_units) grid = max_units;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, (const __nv_bfloat16*)p.a,
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, (const __nv_bfloat16*)p.a, p.a_rows,
                     (const uint4*)p.codes, (const float2*)p.scale_min, p.offsets, p.row_gate, p.K, p.N, p.E,
                     (OutT*)p.out);
 }
