@@ -39,12 +39,12 @@ DEFAULT_WORKLOAD = "e16_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # router 1, dispatch 2 (count + scan, scatter + gather), up 1, down 1, combine 1; with top-2 and the
 # tensor-core router (bf16, E <= 256, E % 8 == 0) the router writes the dispatch histogram: dispatch 1;
-# a bf16 batch of at most 8 tokens (E even) routes and dispatches in one launch: 4 in all
+# a bf16 batch of at most 8 tokens (E % 8 == 0) routes and dispatches in one launch: 4 in all
 KERNELS_PER_STEP = 6
 
 
 def kernels_per_step(T, k, E, bf16):
-    if bf16 and T <= 8 and E % 2 == 0:
+    if bf16 and T <= 8 and E % 8 == 0:
         return 4
     fused = k == 2 and bf16 and E <= 256 and E % 8 == 0
     return KERNELS_PER_STEP - 1 if fused else KERNELS_PER_STEP

@@ -34,14 +34,15 @@ CASES = [
     dict(T=8, d=1024, F=128, E=128, k=2),             # a decode batch: 16 CTAs
     dict(T=3, d=64, F=64, E=8, k=8),                  # k = E: every expert, 8 CTAs with 8 rows each
     dict(T=5, d=256, F=64, E=1024, k=4),              # E = 1024: two passes over expert pairs
-    dict(T=2, d=136, F=64, E=6, k=1),                 # d = 17 x 8: CTAs with empty row ranges
+    dict(T=2, d=136, F=64, E=8, k=1),                 # d = 17 x 8: CTAs with empty row ranges
+    dict(T=2, d=136, F=64, E=6, k=1),                 # E % 8 != 0: the separate router and dispatch
     dict(T=8, d=512, F=64, E=16, k=2, cf=0.5),        # capacity: assignments dropped
     dict(T=4, d=512, F=64, E=32, k=3, bias=True),     # router bias
 ]
 
 
 @pytest.mark.parametrize("renormalise", [False, True], ids=["raw", "renorm"])
-@pytest.mark.parametrize("cfg", CASES, ids=["t1", "t8", "k_eq_e", "e1024", "d136", "cap", "bias"])
+@pytest.mark.parametrize("cfg", CASES, ids=["t1", "t8", "k_eq_e", "e1024", "d136", "e6", "cap", "bias"])
 def test_forward_small_batch(cfg, renormalise):
     cfg = dict(cfg)
     cf = cfg.pop("cf", 0.0)
