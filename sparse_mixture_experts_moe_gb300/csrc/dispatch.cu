@@ -198,6 +198,10 @@ dispatch_from_hist_kernel(const int32_t* __restrict__ idx, const float* __restri
   __shared__ int warp_tot[kChunk / 32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int chunk = blockIdx.x / split, part = blockIdx.x % split;
+  // this thread's assignment and gate: loads in flight while the histograms are summed
+  const int a = chunk * kChunk + tid;
+  const int e_raw = a < A ? idx[a] : -1;
+  const float g_a = (part == 0 && a < A) ? gate[a] : 0.f;
   // totals and this chunk's prefix: thread (g, e) sums the chunks c = g (mod G) of expert e (E <= kChunk),
   // then thread e adds the G partials in order
   __shared__ int s_tp[2][kChunk];
@@ -244,12 +248,7 @@ dispatch_from_hist_kernel(const int32_t* __restrict__ idx, const float* __restri
   }
   run += kept;
   if (blockIdx.x == 0 && tid == kChunk - 1) offsets[E] = run;
-  const int a = chunk * kChunk + tid;
-  int e = -1;
-  if (a < A) {
-    e = idx[a];
-    if (e < 0 || e >= E) e = -1;
-  }
+  const int e = (e_raw < 0 || e_raw >= E) ? -1 : e_raw;
   const unsigned peers = __match_any_sync(0xffffffffu, e);
   const int rank = __popc(peers & ((1u << lane) - 1u));
   if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(peers);
@@ -266,24 +265,51 @@ dispatch_from_hist_kernel(const int32_t* __restrict__ idx, const float* __restri
     row_of[a] = row;
     if (row >= 0) {
       perm_token[row] = a / k;
-      row_gate[row] = gate[a];
+      row_gate[row] = g_a;
     }
   }
   __syncthreads();
+  // the gather: each warp copies its rows four at a time, all sixteen 16-byte loads per lane in
+  // flight before the stores (rows i0 + j * stride)
   const int n_here = min(kChunk, A - chunk * kChunk);
-  for (int i = part + split * warp; i < n_here; i += split * kWarpsPerChunk) {
-    const int r = srow[i];
-    if (r < 0) continue;
-    const int4* src = x + (size_t)((chunk * kChunk + i) / k) * vec_per_row;
-    int4* dst = x_perm + (size_t)r * vec_per_row;
-    int v = lane;
-    for (; v + 96 < vec_per_row; v += 128) {
-      const int4 v0 = __ldg(src + v), v1 = __ldg(src + v + 32), v2 = __ldg(src + v + 64), v3 = __ldg(src + v + 96);
-      dst[v] = v0; dst[v + 32] = v1; dst[v + 64] = v2; dst[v + 96] = v3;
+  const int stride = split * kWarpsPerChunk;
+  for (int i0 = part + split * warp; i0 < n_here; i0 += 4 * stride) {
+    int rr[4];
+    const int4* src[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + j * stride;
+      rr[j] = i < n_here ? srow[i] : -1;
+      src[j] = x + (size_t)((chunk * kChunk + (i < n_here ? i : 0)) / k) * vec_per_row;
     }
-    for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    for (int v0 = 0; v0 < vec_per_row; v0 += 128) {
+      int4 buf[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // unconditional loads from valid addresses; stores predicated
+          const int v = v0 + lane + 32 * q;
+          const int4* ptr = src[j] + (v < vec_per_row ? v : 0);
+          asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(buf[j][q].x), "=r"(buf[j][q].y), "=r"(buf[j][q].z), "=r"(buf[j][q].w)
+                       : "l"(ptr));
+        }
+      asm volatile("" ::: "memory");  // keep all sixteen loads ahead of the stores
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int v = v0 + lane + 32 * q;
+          if (rr[j] >= 0 && v < vec_per_row)
+            asm volatile("st.global.v4.s32 [%0], {%1, %2, %3, %4};" ::"l"(x_perm + (size_t)rr[j] * vec_per_row + v),
+                         "r"(buf[j][q].x), "r"(buf[j][q].y), "r"(buf[j][q].z), "r"(buf[j][q].w)
+                         : "memory");
+        }
+    }
   }
 }
+
+
 
 __global__ void __launch_bounds__(256)
 dispatch_gather_kernel(const int4* __restrict__ x, const int32_t* __restrict__ perm_token,
