@@ -37,17 +37,6 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s; % of BF16 tensor peak (prefill) / % HBM BW (decode)"
 DEFAULT_WORKLOAD = "e16_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# router 1, dispatch 2 (count + scan, scatter + gather), up 1, down 1, combine 1; with top-2 and the
-# tensor-core router (bf16, E <= 256, E % 8 == 0) the router writes the dispatch histogram: dispatch 1;
-# a bf16 batch of at most 8 tokens (E % 8 == 0) routes and dispatches in one launch: 4 in all
-KERNELS_PER_STEP = 6
-
-
-def kernels_per_step(T, k, E, bf16):
-    if bf16 and T <= 8 and E % 8 == 0:
-        return 4
-    fused = k == 2 and bf16 and E <= 256 and E % 8 == 0
-    return KERNELS_PER_STEP - 1 if fused else KERNELS_PER_STEP
 L2_BYTES = 126 * 2**20
 TC_SOURCES = ["sparse_mixture_experts_moe_gb300/csrc/ffn_tc.cu", "sparse_mixture_experts_moe_gb300/csrc/common.cuh"]
 TCT_SOURCES = ["sparse_mixture_experts_moe_gb300/csrc/ffn_tct.cu", "sparse_mixture_experts_moe_gb300/csrc/common.cuh"]
@@ -518,7 +507,7 @@ def run_ours(args, w, rank, world, device):
         "experts_touched": touched,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * x.element_size(),
                 "d2h_bytes_per_step": out.numel() * out.element_size()},
-        "gpu_launches": kernels_per_step(T, k, E, dt == 1) * args.steps,
+        "gpu_launches": moe.forward_launches(T, d, F, E, k, dt, moe.PATH_STREAM if qbits else fpath) * args.steps,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not qbits:

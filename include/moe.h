@@ -72,6 +72,13 @@ typedef enum {
 /* The family AUTO runs for an expert GEMM of T*k routed rows, E experts and N output columns
  * (N = d_ff for expert_up, d for expert_down); -1 on bad arguments. Host only. */
 int moe_ffn_path(int T, int k, int E, int N, moe_dtype dt);
+/* Kernel launches of one moe_forward_ex call with these arguments (router_stats: nonzero when a
+ * statistics output is passed): 4 for at most 8 bf16 tokens with weight-streaming GEMMs (router
+ * and dispatch in one launch, E % 8 == 0, no statistics), 5 with top-2 and the tensor-core router
+ * (the router writes the dispatch histograms), 6 otherwise (router, dispatch count + scatter, two
+ * expert GEMMs, combine); 0 for T = 0; -1 on bad arguments. moe_forward_q follows the same rules
+ * with weight-streaming GEMMs. Host only: nothing is launched. */
+int moe_forward_launches(int T, int d, int F, int E, int k, moe_dtype dt, moe_path path, int router_stats);
 
 /* ---------------------------------------------------------------------------------------------
  * moe_router_topk — router GEMM, softmax and deterministic top-k, fused, one warp per token.

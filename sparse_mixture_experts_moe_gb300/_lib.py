@@ -38,6 +38,7 @@ SIGNATURES = {
     "moe_dispatch_ex": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _sz, _p],
     "moe_capacity": [_i, _i, _i, ctypes.c_double],
     "moe_ffn_path": [_i, _i, _i, _i, _i],
+    "moe_forward_launches": [_i, _i, _i, _i, _i, _i, _i, _i],
     "moe_dispatch_noalloc": [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p],
     "moe_expert_up": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
     "moe_expert_up_ex": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
@@ -175,6 +176,11 @@ def router_topk_stats(x, w_r, b_r, T, d, E, k, dt, topk_idx, topk_gate, stats, w
 def ffn_path(T, k, E, N, dt) -> int:
     """The kernel family (PATH_*) AUTO runs for an expert GEMM with N output columns."""
     return int(lib().moe_ffn_path(T, k, E, N, dt))
+
+
+def forward_launches(T, d, F, E, k, dt, path=PATH_AUTO, router_stats=False) -> int:
+    """Kernel launches of one forward call with these arguments (moe_forward_launches); host only."""
+    return int(lib().moe_forward_launches(T, d, F, E, k, dt, path, 1 if router_stats else 0))
 
 
 def capacity(T, k, E, cf) -> int:

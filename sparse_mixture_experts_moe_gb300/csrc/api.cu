@@ -315,6 +315,18 @@ int moe_ffn_path(int T, int k, int E, int N, moe_dtype dt) {
   return (int)resolve_path(MOE_PATH_AUTO, dt, T * k, E, N);
 }
 
+int moe_forward_launches(int T, int d, int F, int E, int k, moe_dtype dt, moe_path path, int router_stats) {
+  if (!sizes_ok(T, d, F, E, k, dt) || !path_ok(path, dt)) return -1;
+  if (T == 0) return 0;
+  // the decisions of moe_forward_ex and route_and_dispatch
+  const Layout L(T, d, F, E, k, dt);
+  const bool small_ok = resolve_path(path, dt, T * k, E, F) == MOE_PATH_STREAM &&
+                        resolve_path(path, dt, T * k, E, d) == MOE_PATH_STREAM;
+  if (small_ok && !router_stats && route_small_ok(T, d, E, k, dt, L.end - L.y_perm)) return 4;
+  const bool tc_router = dt == MOE_DTYPE_BF16 && E <= 256 && E % 8 == 0;
+  return tc_router && k * 128 == kDispatchChunk ? 5 : 6;
+}
+
 size_t moe_qweight_bytes(int K, int N, int E, int bits) {
   if (!qsizes_ok(K, N, E, bits)) return 0;
   return (size_t)E * K * N * bits / 8;

@@ -120,3 +120,24 @@ def test_quantised_sizes_without_gpu():
     assert lib.moe_quantize_weights(FAKE, 64, 64, 1, 1, 5, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_graph_capture_begin(None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_graph_capture_end(None, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_forward_launch_plan_without_gpu():
+    """How many kernels one forward call launches, from the library's own decisions."""
+    BF16, F32 = moe.MOE_DTYPE_BF16, moe.MOE_DTYPE_F32
+    # decode: router + dispatch in one launch, two weight-streaming GEMMs, combine
+    assert moe.forward_launches(1, 8192, 8192, 128, 2, BF16) == 4
+    assert moe.forward_launches(8, 8192, 8192, 128, 2, BF16) == 4
+    # statistics, E % 8 != 0, or a GEMM family other than streaming: the separate router and dispatch
+    assert moe.forward_launches(1, 8192, 8192, 128, 2, BF16, router_stats=True) == 5
+    assert moe.forward_launches(2, 136, 64, 6, 1, BF16) == 6
+    assert moe.forward_launches(1, 1024, 1024, 16, 2, BF16, path=moe.PATH_TENSOR) == 5
+    # top-2 with the tensor-core router: the router writes the dispatch histograms
+    assert moe.forward_launches(4096, 1024, 4096, 16, 2, BF16) == 5
+    assert moe.forward_launches(8192, 4096, 8192, 128, 2, BF16) == 5
+    # otherwise six: k != 2, E > 256, fp32
+    assert moe.forward_launches(4096, 1024, 4096, 16, 4, BF16) == 6
+    assert moe.forward_launches(4096, 1024, 4096, 512, 2, BF16) == 6
+    assert moe.forward_launches(64, 128, 256, 8, 2, F32) == 6
+    assert moe.forward_launches(0, 128, 256, 8, 2, BF16) == 0
+    assert moe.forward_launches(4, 100, 256, 8, 2, BF16) == -1  # d % 8 != 0
