@@ -9,10 +9,11 @@ synthetic tokens, through the library's C ABI. Prints one JSON line on rank 0.
 
 value      tokens/s of the whole job, device-timed with CUDA events over exactly K steps of
            moe_forward (inputs resident in HBM), max over ranks.
-e2e        the same metric through the public layer object with the host->device copy of the
-           step's tokens (pinned) and the device->host copy of its output inside the timed region.
-roofline   the dominant kernel, timed live with CUDA events around its own C ABI call on the
-           launching stream, against the measured peak in MEASURED_PEAKS.json.
+e2e        the same metric through the public layer object with the host->device copy of every
+           step's tokens (pinned) and the device->host copy of its output inside the timed region,
+           double-buffered: a step's copies overlap the neighbouring steps' compute.
+roofline   the dominant kernel, timed live with CUDA events over back-to-back launches of its own
+           C ABI call on the launching stream, against the measured peak in MEASURED_PEAKS.json.
 cpu_baseline  the fp64 oracle on the host cores on a bounded prefix of the same batch.
 --impl reference  the oracle alone, timed on the host cores, on the same workload and metric.
 
@@ -409,33 +410,58 @@ def run_ours(args, w, rank, world, device):
     counts_h = counts.cpu().numpy()
     touched = int((counts_h > 0).sum())
 
-    # --- e2e: public layer object, pinned host tokens in, output back to the host, every step
+    # --- e2e: public layer object, pinned host tokens in, output back to the host, every step.
+    # Double-buffered as a serving loop runs it: step i's input copy (its own stream) overlaps step
+    # i-1's compute, and step i's output copy (a third stream) overlaps step i+1's compute; events
+    # keep a buffer from being refilled before the step that used it has finished with it.
     layer = moe.MoELayer(w_r, w1, w2, k=k, b_r=b_r, path=fpath, weight_bits=qbits or None)
     x_host = x.cpu().pin_memory()
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    x_dev = torch.empty_like(x)
-    out_dev = torch.empty_like(out)
+    out_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(x) for _ in range(2)]
+    out_dev = [torch.empty_like(out) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
     if graph is not None:
-        layer_graph = layer.graph(x_dev, out_dev)
+        layer_graphs = [layer.graph(x_dev[b], out_dev[b]) for b in range(2)]
 
-        def layer_step():
-            layer_graph.launch(stream)
+        def layer_step(b):
+            layer_graphs[b].launch(stream)
     else:
-        def layer_step():
-            layer(x_dev, out=out_dev)
-    for _ in range(3):
-        x_dev.copy_(x_host, non_blocking=True)
-        layer_step()
-        out_host.copy_(out_dev, non_blocking=True)
+        def layer_step(b):
+            with torch.cuda.stream(stream):
+                layer(x_dev[b], out=out_dev[b])
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_steps(n):
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_comp[b])        # step i-2 has read x_dev[b]
+                x_dev[b].copy_(x_host, non_blocking=True)
+                ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_out[b])           # step i-2's output has left out_dev[b]
+            layer_step(b)
+            ev_comp[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[b])
+                out_host[b].copy_(out_dev[b], non_blocking=True)
+                ev_out[b].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+
+    e2e_steps(4)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        layer_step()
-        out_host.copy_(out_dev, non_blocking=True)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    e2e_steps(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_value = job_tokens_per_s(T, world, max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device))
@@ -506,7 +532,8 @@ def run_ours(args, w, rank, world, device):
         "kernel_ms": kern_ms,
         "experts_touched": touched,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * x.element_size(),
-                "d2h_bytes_per_step": out.numel() * out.element_size()},
+                "d2h_bytes_per_step": out.numel() * out.element_size(),
+                "copies": "every step, double-buffered on their own streams (overlapping neighbouring steps)"},
         "gpu_launches": moe.forward_launches(T, d, F, E, k, dt, moe.PATH_STREAM if qbits else fpath) * args.steps,
         "clocks": clk,
     }
