@@ -17,9 +17,10 @@ BF16, F32 = ig.DTYPE_BF16, ig.DTYPE_F32
 
 @pytest.mark.parametrize("cfg", [dict(T=640, d=256, F=512, E=16, k=2, dt=BF16, path=moe.PATH_AUTO),
                                  dict(T=8, d=1024, F=1024, E=32, k=2, dt=BF16, path=moe.PATH_AUTO),
+                                 dict(T=1, d=2048, F=1024, E=64, k=2, dt=BF16, path=moe.PATH_AUTO),
                                  dict(T=64, d=128, F=256, E=8, k=2, dt=F32, path=moe.PATH_AUTO),
                                  dict(T=300, d=256, F=256, E=16, k=2, dt=BF16, path=moe.PATH_TENSOR_PAIR)],
-                         ids=["tensor", "stream", "simt_f32", "pair"])
+                         ids=["tensor", "stream", "stream_t1", "simt_f32", "pair"])
 def test_graph_matches_direct_call(cfg):
     cfg = dict(cfg)
     path = cfg.pop("path")
