@@ -37,12 +37,13 @@ CASES = [
     dict(T=2, d=136, F=64, E=8, k=1),                 # d = 17 x 8: CTAs with empty row ranges
     dict(T=2, d=136, F=64, E=6, k=1),                 # E % 8 != 0: the separate router and dispatch
     dict(T=8, d=512, F=64, E=16, k=2, cf=0.5),        # capacity: assignments dropped
+    dict(T=2, d=512, F=64, E=8, k=4, cf=0.5),         # capacity on the plain-CTA (T <= 2) variant
     dict(T=4, d=512, F=64, E=32, k=3, bias=True),     # router bias
 ]
 
 
 @pytest.mark.parametrize("renormalise", [False, True], ids=["raw", "renorm"])
-@pytest.mark.parametrize("cfg", CASES, ids=["t1", "t8", "k_eq_e", "e1024", "d136", "e6", "cap", "bias"])
+@pytest.mark.parametrize("cfg", CASES, ids=["t1", "t8", "k_eq_e", "e1024", "d136", "e6", "cap", "cap_t2", "bias"])
 def test_forward_small_batch(cfg, renormalise):
     cfg = dict(cfg)
     cf = cfg.pop("cf", 0.0)
