@@ -305,7 +305,7 @@ moe_status expert_half_q(int stage, const void* a, const void* codes, const floa
       (stage == 2 && row_gate == nullptr))
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(a) || !aligned16(codes) || !aligned8(scale_min) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
-  QFfnArgs p{a, codes, scale_min, offsets, row_gate, out, T * k, K, N, E, bits, stage, a_rows};
+  QFfnArgs p{a, codes, scale_min, offsets, row_gate, out, T * k, K, N, E, bits, stage, a_rows, T};
   return cuda_status(launch_ffn_stream_q(p, (cudaStream_t)stream));
 }
 }  // namespace

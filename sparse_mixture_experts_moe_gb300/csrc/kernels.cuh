@@ -94,7 +94,8 @@ struct QFfnArgs {
   const float* row_gate;  // [rows] (stage 2)
   void* out;              // [rows, N]: bf16 (stage 1) or fp32 (stage 2)
   int rows, K, N, E, bits, stage;
-  const int32_t* a_rows;  // nullable: row r of `a` is a[a_rows[r]]
+  const int32_t* a_rows;    // nullable: row r of `a` is a[a_rows[r]]
+  int max_rows_per_expert;  // an upper bound (T: a token's k experts are distinct); 0: unknown
 };
 cudaError_t launch_quantize(const void* w, int K, int N, int E, int dt, int bits, void* codes, float* scale_min,
                             cudaStream_t s);
