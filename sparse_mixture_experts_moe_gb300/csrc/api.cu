@@ -243,6 +243,7 @@ static moe_status expert_half(int stage, const void* a, const void* w, const int
   args.status = at<int>(workspace, 0);
   args.timeout_ns = wait_timeout_ns();
   args.a_rows = a_rows;
+  args.max_rows_per_expert = T;
   return run_ffn_half(path, args, (cudaStream_t)stream);
 }
 

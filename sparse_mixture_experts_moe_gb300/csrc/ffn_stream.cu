@@ -31,7 +31,7 @@ constexpr int kc_for() { return RMAX <= 2 ? 4096 : 2048; }
 // Weight loads per thread per batch (two batches in flight): 8 with 2 rows a pass; with 4 rows
 // the accumulators take the registers, and 8 would spill.
 template <int RMAX>
-constexpr int unroll_for() { return RMAX <= 2 ? 8 : 6; }
+constexpr int unroll_for() { return RMAX == 1 ? 9 : RMAX <= 2 ? 8 : 6; }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
   v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
@@ -206,6 +206,8 @@ cudaError_t launch_ffn_stream(const FfnArgs& p, cudaStream_t s) {
   if (p.dt != MOE_DTYPE_BF16) return cudaErrorNotSupported;
   // Rows per expert are at most T*k; small batches keep fewer accumulators (more CTAs per SM).
   // An expert with more rows than a pass holds streams its weights again for the rest.
+  if (p.max_rows_per_expert == 1)
+    return p.stage == 1 ? launch_t<1, __nv_bfloat16, 1>(p, s) : launch_t<2, float, 1>(p, s);
   if (p.rows <= 32)
     return p.stage == 1 ? launch_t<1, __nv_bfloat16, 2>(p, s) : launch_t<2, float, 2>(p, s);
   return p.stage == 1 ? launch_t<1, __nv_bfloat16, 4>(p, s) : launch_t<2, float, 4>(p, s);

@@ -81,6 +81,7 @@ struct FfnArgs {
   int* status;
   uint64_t timeout_ns;
   const int32_t* a_rows;  // nullable row map of `a` (weight-streaming kernels only)
+  int max_rows_per_expert;  // an upper bound (T: a token's k experts are distinct); 0: unknown
 };
 cudaError_t launch_ffn_simt(const FfnArgs& a, cudaStream_t s);
 
