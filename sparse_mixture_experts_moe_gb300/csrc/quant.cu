@@ -36,10 +36,10 @@ constexpr int GSTEP = kWarps * RPW; // tile rows per CTA step: 32
 // the code stream behind two barriers and a 4-bit chunk is little work per thread.
 template <int RMAX>
 constexpr int kc_for() { return RMAX <= 2 ? 4096 : 2048; }
-// Code tiles per thread per batch (two batches in flight). One row a pass (a single token: each
-// expert gets one row) leaves registers for more tiles in flight.
-template <int RMAX>
-constexpr int unroll_q() { return RMAX == 1 ? 8 : 4; }
+// Code tiles per thread per batch (two batches in flight): as many as the registers allow without
+// spilling, which is more with fewer rows a pass (a single token: each expert gets one row).
+template <int BITS, int RMAX>
+constexpr int unroll_q() { return RMAX == 1 ? 8 : RMAX == 2 ? (BITS == 4 ? 8 : 6) : (BITS == 4 ? 6 : 4); }
 constexpr float kMagic = 8388608.0f;  // 2^23: a byte b placed in the low mantissa bits reads 2^23 + b
 
 // ------------------------------------------------------------------ quantiser
@@ -160,7 +160,7 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restri
   constexpr int KT = 16 / BITS;  // k-rows per tile: 128 bits / (8 columns x BITS)
   static_assert(KT * 8 * BITS == 128 && (BITS == 4 ? KT == 4 : KT == 2), "tile words hold KT k-rows");
   constexpr int KC = kc_for<RMAX>();
-  constexpr int kUnroll = unroll_q<RMAX>();
+  constexpr int kUnroll = unroll_q<BITS, RMAX>();
   extern __shared__ __align__(16) float smem[];
   float* sA = smem;                                     // [RMAX][KC]
   float* sRed = sA + RMAX * KC;                         // [kWarps][RMAX][NS]
