@@ -17,9 +17,12 @@
 //
 // Streaming kernel: the structure of ffn_stream.cu (work unit = (expert with rows, 64-column
 // slab), full depth per CTA, fixed-order reductions) with the dequantisation folded into the
-// dot product: sum_k a_k (min_b + c_k scale_b) = sum_b [ (a scale_b) . c  +  min_b sum a ].
+// dot product: sum_k a_k (min_b + c_k scale_b) = sum_b [ (a scale_b) . (c - m) + (min_b + m scale_b) sum a ]
+// with the centre m = 2^(bits-1).
 // Per weight that is one byte permute into a 2^23-offset float, one subtraction (exact) and one
-// FMA per activation row; the column-independent a * min term is accumulated once per k-row.
+// FMA per activation row. The activations are staged already multiplied by their block's scale,
+// and the column-independent term (min_b times the block's activation sum) is formed once per row
+// from block sums taken while staging, not by every lane of the slab.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -110,20 +113,24 @@ quantize_kernel(const T* __restrict__ w, int K, int N, uint4* __restrict__ codes
 }
 
 // ------------------------------------------------------------------ streaming FFN
-// Codes of the 8 columns of one k-row as exact floats 0 .. 2^bits - 1, in column pairs
-// (2p, 2p+1) packed for the fp32x2 instructions: a byte permute places each code in the low
-// mantissa bits of 2^23, one packed subtraction removes the 2^23.
+// Codes of the 8 columns of one k-row as exact centred floats c - 2^(bits-1) (-8 .. 7 for INT4,
+// -128 .. 127 for INT8), in column pairs (2p, 2p+1) packed for the fp32x2 instructions: a byte
+// permute places each code in the low mantissa bits of 2^23, one packed subtraction of
+// 2^23 + 2^(bits-1) (exact) leaves the centred code. Centring halves the scaled term that the
+// block-minimum term otherwise cancels in part, and with it the term's rounding error.
+template <int BITS>
+constexpr float kCentre = (float)(1 << (BITS - 1));
 __device__ __forceinline__ uint32_t magic_byte(uint32_t w, uint32_t sel) { return __byte_perm(w, 0x4B000000u, sel); }
 __device__ __forceinline__ void int4_row(uint32_t wd, uint64_t (&c)[4]) {
   const uint32_t even = wd & 0x0F0F0F0Fu;         // columns 0, 2, 4, 6 in bytes 0..3
   const uint32_t odd = (wd >> 4) & 0x0F0F0F0Fu;   // columns 1, 3, 5, 7
-  const uint64_t neg = f2_pack(-kMagic, -kMagic);
+  const uint64_t neg = f2_pack(-(kMagic + kCentre<4>), -(kMagic + kCentre<4>));
 #pragma unroll
   for (int p = 0; p < 4; ++p)
     c[p] = fadd2(((uint64_t)magic_byte(odd, 0x7540 + p) << 32) | magic_byte(even, 0x7540 + p), neg);
 }
 __device__ __forceinline__ void int8_row(uint32_t w0, uint32_t w1, uint64_t (&c)[4]) {
-  const uint64_t neg = f2_pack(-kMagic, -kMagic);
+  const uint64_t neg = f2_pack(-(kMagic + kCentre<8>), -(kMagic + kCentre<8>));
   c[0] = fadd2(((uint64_t)magic_byte(w0, 0x7541) << 32) | magic_byte(w0, 0x7540), neg);
   c[1] = fadd2(((uint64_t)magic_byte(w0, 0x7543) << 32) | magic_byte(w0, 0x7542), neg);
   c[2] = fadd2(((uint64_t)magic_byte(w1, 0x7541) << 32) | magic_byte(w1, 0x7540), neg);
@@ -131,23 +138,36 @@ __device__ __forceinline__ void int8_row(uint32_t w0, uint32_t w1, uint64_t (&c)
 }
 
 // Rows rp .. rp+R-1, k-range [kc, kc+kn) of the bf16 activations -> sA as fp32 (row stride KC),
-// with 16-byte loads (K and kn are multiples of 64, rows 16-byte aligned).
+// each multiplied by its block's scale (the same for every lane of the slab, so done once here
+// instead of by each of the eight lanes that share a k-row); sBS[r][b] receives the plain sum of the
+// row's 64 activations of block b (eight 8-value partials of consecutive lanes, added as a fixed
+// xor tree), for the block-minimum term. 16-byte loads (K and kn are multiples of 64, rows 16-byte
+// aligned); every lane of a warp runs the same number of iterations (R * KC / 8 is a multiple of the
+// block size).
 template <int KC>
 __device__ __forceinline__ void stage_rows_q(const __nv_bfloat16* __restrict__ a, const int32_t* __restrict__ a_rows,
-                                             int K, int rp, int R, int kc, int kn, float* sA) {
+                                             int K, int rp, int R, int kc, int kn, const float2* sSM, float* sA,
+                                             float* sBS) {
   const int per_row = KC / 8;
   for (int i = threadIdx.x; i < R * per_row; i += kThreads) {
     const int r = i / per_row, kk = (i % per_row) * 8;
     const size_t src = a_rows != nullptr ? (size_t)a_rows[rp + r] : (size_t)(rp + r);
-    float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (kk < kn) {
       const uint4 u = __ldg(reinterpret_cast<const uint4*>(a + src * K + kc + kk));
-      lo = make_float4(bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y));
-      hi = make_float4(bf16lo(u.z), bf16hi(u.z), bf16lo(u.w), bf16hi(u.w));
+      v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+      v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
     }
+    const float sc = kk < kn ? sSM[(kc + kk) / QB].x : 0.f;
     float4* dst = reinterpret_cast<float4*>(sA + r * KC + kk);
-    dst[0] = lo;
-    dst[1] = hi;
+    dst[0] = make_float4(v[0] * sc, v[1] * sc, v[2] * sc, v[3] * sc);
+    dst[1] = make_float4(v[4] * sc, v[5] * sc, v[6] * sc, v[7] * sc);
+    float s8 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s8 += v[j];
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) s8 += __shfl_xor_sync(0xffffffffu, s8, o);
+    if ((threadIdx.x & 7) == 0) sBS[r * (KC / QB) + kk / QB] = s8;
   }
 }
 
@@ -165,7 +185,9 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restri
   float* sA = smem;                                     // [RMAX][KC]
   float* sRed = sA + RMAX * KC;                         // [kWarps][RMAX][NS]
   float2* sSM = reinterpret_cast<float2*>(sRed + kWarps * RMAX * NS);  // [K / 64] this slab's blocks
-  int* sAct = reinterpret_cast<int*>(sSM + K / QB);     // [E] experts with rows
+  float* sBS = reinterpret_cast<float*>(sSM + K / QB);  // [RMAX][KC / 64] activation block sums
+  float* sMin = sBS + RMAX * (KC / QB);                 // [RMAX] block-minimum term of each row
+  int* sAct = reinterpret_cast<int*>(sMin + RMAX);      // [E] experts with rows
   __shared__ int s_nact;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   griddep_launch_dependents();
@@ -200,13 +222,11 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restri
     for (int rp = r_begin; rp < r_end; rp += RMAX) {
       const int R = min(RMAX, r_end - rp);
       uint64_t acc2[RMAX][4];  // column pairs (2p, 2p+1) of each row
-      float accm[RMAX];
 #pragma unroll
-      for (int r = 0; r < RMAX; ++r) {
-        accm[r] = 0.f;
+      for (int r = 0; r < RMAX; ++r)
 #pragma unroll
         for (int p = 0; p < 4; ++p) acc2[r][p] = 0ull;
-      }
+      float min_term = 0.f;  // thread r < R: row r's sum over blocks of (min_b + m scale_b) * (sum of a over b)
       for (int kc = 0; kc < K; kc += KC) {
         const int kn = min(KC, K - kc);  // a multiple of 64
         const int gn = kn / KT;          // tile rows in this chunk
@@ -220,8 +240,13 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restri
         uint4 cur[kUnroll], nxt[kUnroll];
         load_batch(0, cur);  // in flight while the activations are staged
         __syncthreads();
-        stage_rows_q<KC>(a, a_rows, K, rp, R, kc, kn, sA);
+        stage_rows_q<KC>(a, a_rows, K, rp, R, kc, kn, sSM, sA, sBS);
         __syncthreads();
+        if (tid < R)
+          for (int b = 0; b < kn / QB; ++b) {  // w = (min + centre * scale) + (c - centre) * scale
+            const float2 q = sSM[kc / QB + b];
+            min_term = fmaf(fmaf(kCentre<BITS>, q.x, q.y), sBS[tid * (KC / QB) + b], min_term);
+          }
         for (int g0 = 0; g0 < gn; g0 += GSTEP * kUnroll) {
           if (g0 + GSTEP * kUnroll < gn) load_batch(g0 + GSTEP * kUnroll, nxt);
 #pragma unroll
@@ -229,7 +254,6 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restri
             const int g = g0 + i * GSTEP + warp * RPW + kr;
             if (g >= gn) break;
             const int k0 = g * KT;  // first k-row of the tile within the chunk
-            const float2 q = sSM[(kc + k0) / QB];
             const uint32_t wd[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
 #pragma unroll
             for (int j = 0; j < KT; ++j) {
@@ -239,9 +263,7 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restri
 #pragma unroll
               for (int r = 0; r < RMAX; ++r) {
                 if (r >= R) break;
-                const float av = sA[r * KC + k0 + j];
-                const float as = av * q.x;
-                accm[r] = fmaf(av, q.y, accm[r]);
+                const float as = sA[r * KC + k0 + j];  // activation times its block's scale
                 const uint64_t as2 = f2_pack(as, as);
 #pragma unroll
                 for (int p = 0; p < 4; ++p) acc2[r][p] = ffma2(as2, cp[p], acc2[r][p]);
@@ -252,14 +274,15 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restri
           for (int i = 0; i < kUnroll; ++i) cur[i] = nxt[i];
         }
       }
-      // Fold the column-independent min term in, then combine the warp's RPW tile rows (lanes cg,
-      // cg+8, cg+16, cg+24) and the warps, in fixed orders.
+      // Combine the warp's RPW tile rows (lanes cg, cg+8, cg+16, cg+24) and the warps in fixed
+      // orders, then add each row's column-independent block-minimum term.
+      if (tid < R) sMin[tid] = min_term;
       float acc[RMAX][8];
 #pragma unroll
       for (int r = 0; r < RMAX; ++r)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          float v = (c & 1 ? f2_hi(acc2[r][c >> 1]) : f2_lo(acc2[r][c >> 1])) + accm[r];
+          float v = c & 1 ? f2_hi(acc2[r][c >> 1]) : f2_lo(acc2[r][c >> 1]);
           v += __shfl_xor_sync(0xffffffffu, v, LPR);
           v += __shfl_xor_sync(0xffffffffu, v, 2 * LPR);
           acc[r][c] = v;
@@ -275,6 +298,7 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restri
         float v = 0.f;
 #pragma unroll
         for (int wi = 0; wi < kWarps; ++wi) v += sRed[(wi * RMAX + r) * NS + c];
+        v += sMin[r];
         const int grow = rp + r;
         v = STAGE == 1 ? gelu_as(v) : row_gate[grow] * v;
         out[(size_t)grow * N + n0 + c] = from_f32<OutT>(v);
@@ -286,7 +310,8 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restri
 template <int BITS, int STAGE, typename OutT, int RMAX>
 cudaError_t launch_q(const QFfnArgs& p, cudaStream_t s) {
   const size_t smem = (size_t)(RMAX * kc_for<RMAX>() + kWarps * RMAX * NS) * sizeof(float) +
-                      (size_t)(p.K / QB) * sizeof(float2) + (size_t)p.E * sizeof(int);
+                      (size_t)(p.K / QB) * sizeof(float2) +
+                      (size_t)(RMAX * (kc_for<RMAX>() / QB) + RMAX) * sizeof(float) + (size_t)p.E * sizeof(int);
   auto kern = ffn_stream_q_kernel<BITS, STAGE, OutT, RMAX>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
