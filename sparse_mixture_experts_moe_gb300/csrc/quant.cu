@@ -42,7 +42,7 @@ constexpr int kc_for() { return RMAX <= 2 ? 4096 : 2048; }
 // Code tiles per thread per batch (two batches in flight): as many as the registers allow without
 // spilling, which is more with fewer rows a pass (a single token: each expert gets one row).
 template <int BITS, int RMAX>
-constexpr int unroll_q() { return RMAX == 1 ? 8 : RMAX == 2 ? (BITS == 4 ? 8 : 6) : (BITS == 4 ? 6 : 4); }
+constexpr int unroll_q() { return RMAX <= 2 ? 8 : 6; }
 constexpr float kMagic = 8388608.0f;  // 2^23: a byte b placed in the low mantissa bits reads 2^23 + b
 
 // ------------------------------------------------------------------ quantiser
