@@ -239,8 +239,9 @@ class HostExperts:
         return self.cache[int(e)]
 
 
-def oracle_sample(w, x, w_r, b_r, w1, w2, target_s, max_tokens=None):
-    """Times oracle.forward on a prefix of the batch; returns (tokens/s, tokens, seconds, cores)."""
+def oracle_sample(w, x, w_r, b_r, w1, w2, target_s, max_tokens=None, repeat=True):
+    """Times oracle.forward on a prefix of the batch, or on the whole batch repeated when one pass is
+    short of the target; returns (tokens/s, tokens per pass, seconds, cores, passes)."""
     import numpy as np
     import oracle
     cores = len(os.sched_getaffinity(0))
@@ -251,7 +252,7 @@ def oracle_sample(w, x, w_r, b_r, w1, w2, target_s, max_tokens=None):
     n = min(max_tokens, 64 if w.E * per_expert > 6e9 else 256)
     h = host_copy(w, x, w_r, b_r, w1, w2, max_tokens)
 
-    def run(ntok):
+    def run(ntok, passes=1):
         xs = h["x"][:ntok]
         idx = oracle.topk_select(oracle.router_logits(xs, h["w_r"], h["b_r"]), w.k)
         experts = sorted(set(int(e) for e in np.unique(idx)))
@@ -260,7 +261,8 @@ def oracle_sample(w, x, w_r, b_r, w1, w2, target_s, max_tokens=None):
         h["w1"].preload(experts)
         h["w2"].preload(experts)
         t0 = time.perf_counter()
-        oracle.forward(xs, h["w_r"], h["w1"], h["w2"], w.k, h["b_r"])
+        for _ in range(passes):
+            oracle.forward(xs, h["w_r"], h["w1"], h["w2"], w.k, h["b_r"])
         return time.perf_counter() - t0
 
     dt = run(n)
@@ -275,7 +277,11 @@ def oracle_sample(w, x, w_r, b_r, w1, w2, target_s, max_tokens=None):
         if dt2 is None:
             break
         n, dt = n2, dt2
-    return n / dt, n, dt, cores
+    passes = 1
+    if repeat and n == max_tokens and dt < target_s / 4:  # the whole batch is short: repeat it
+        passes = max(2, min(64, int(target_s / 2 / max(dt, 1e-3))))
+        dt = run(n, passes)
+    return n * passes / dt, n, dt, cores, passes
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -538,10 +544,11 @@ def run_ours(args, w, rank, world, device):
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not qbits:
-        v, n, secs, cores = oracle_sample(w, x, w_r, b_r, w1, w2, args.cpu_seconds)
+        v, n, secs, cores, passes = oracle_sample(w, x, w_r, b_r, w1, w2, args.cpu_seconds)
         result["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                  "sample": f"first {n} of the batch's {T} tokens, fp64 oracle forward, "
-                                            f"{secs:.2f} s"}
+                                  "sample": (f"the batch's {T} tokens, fp64 oracle forward, {passes} passes"
+                                             if passes > 1 else f"first {n} of the batch's {T} tokens, fp64 oracle "
+                                             "forward") + f", {secs:.2f} s"}
     return result
 
 
@@ -557,7 +564,8 @@ def run_reference(args, w):
     else:
         x, w_r, b_r, w1, w2 = _cpu_inputs(w)
     budget_per_step = 150.0 / max(1, args.steps + args.warmup)
-    v, n, secs, cores = oracle_sample(w, x, w_r, b_r, w1, w2, min(args.cpu_seconds, budget_per_step))
+    v, n, secs, cores, passes = oracle_sample(w, x, w_r, b_r, w1, w2, min(args.cpu_seconds, budget_per_step),
+                                              repeat=False)
     h = host_copy(w, x, w_r, b_r, w1, w2, n)
     import numpy as np
     idx = oracle.topk_select(oracle.router_logits(h["x"], h["w_r"], h["b_r"]), w.k)
