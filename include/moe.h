@@ -238,6 +238,11 @@ moe_status moe_combine(const void* y_perm, const int32_t* row_of, int T, int d, 
  *      layer), the FFN kernel family `path`, router `flags` (MOE_GATES_RENORMALISE), an expert
  *      `capacity` (as in moe_dispatch_ex; 0 = no limit) and `router_stats` (NULL, or
  *      MOE_ROUTER_STATS_LEN(E) floats as in moe_router_topk_stats).
+ * Kernels (same results as the separate calls; moe_forward_launches gives the count): with top-2 and
+ *      the tensor-core router, the router also writes each 128-token tile's expert histogram and the
+ *      dispatch is one launch; for at most 8 bf16 tokens with weight-streaming GEMMs (E % 8 == 0, no
+ *      statistics) one launch routes and dispatches, and the up-projection reads x through
+ *      perm_token (the workspace's x_perm is then not written).
  */
 moe_status moe_forward(const void* x, const void* w_r, const float* b_r, const void* w1, const void* w2, int T,
                        int d, int F, int E, int k, moe_dtype dt, void* out, int32_t* topk_idx, float* topk_gate,
