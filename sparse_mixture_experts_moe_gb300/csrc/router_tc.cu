@@ -168,7 +168,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
       for (int p = 0; p < KMAX; ++p) { bv[p] = -INFINITY; bi[p] = 0x7fffffff; }
       // pass 1: the k largest logits (the first of them is the maximum)
 #pragma unroll 1
-      for (int c = 0; c < EN; c += 32) {
+      for (int c = 0; c < E; c += 32) {  // the padding columns past E are not read
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + (uint32_t)c, v);
         tmem_ld_wait();
@@ -189,7 +189,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
           if (p < k) ksum += expf(bv[p] - m);
       }
 #pragma unroll 1
-      for (int c = 0; c < (renorm && !stats ? 0 : EN); c += 32) {
+      for (int c = 0; c < (renorm && !stats ? 0 : E); c += 32) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + (uint32_t)c, v);
         tmem_ld_wait();
@@ -215,7 +215,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant_
         // 32 tokens, and the token entropy ln ssum - sum p z
         float hs = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < EN; c += 32) {
+        for (int c = 0; c < E; c += 32) {  // the padding columns past E are not read
           uint32_t v[32];
           tmem_ld_32x32b_x32(taddr + (uint32_t)c, v);
           tmem_ld_wait();
@@ -370,7 +370,7 @@ router_tc_split_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_con
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16);
 #pragma unroll 1
-      for (int c = 0; c < EN; c += 32) {
+      for (int c = 0; c < E; c += 32) {  // the padding columns past E are not read
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + (uint32_t)c, v);
         tmem_ld_wait();
