@@ -31,7 +31,7 @@ constexpr int kc_for() { return RMAX <= 2 ? 4096 : 2048; }
 // Weight loads per thread per batch (two batches in flight): 8 with 2 rows a pass; with 4 rows
 // the accumulators take the registers, and 8 would spill.
 template <int RMAX>
-constexpr int unroll_for() { return RMAX == 1 ? 9 : RMAX <= 2 ? 8 : 6; }
+constexpr int unroll_for() { return RMAX == 1 ? 9 : RMAX <= 2 ? 8 : 7; }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
   v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
