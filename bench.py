@@ -504,9 +504,9 @@ def run_ours(args, w, rank, world, device):
         else:
             alg_bytes = touched * F * d * eb + A * F * eb + A * d * eb
         achieved = alg_bytes / (kern_ms[dom] / 1e3) / 1e9
-        roof = {"kernel": f"ffn_stream_kernel ({dom})", "bound": "hbm", "achieved": achieved,
+        roof = {"kernel": f"ffn_stream_tma_kernel ({dom})", "bound": "hbm", "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "traffic": stored_traffic(f"ffn_stream_kernel<{1 if dom == 'expert_up' else 2}>", w.name,
+                "traffic": stored_traffic(f"ffn_stream_tma_kernel<{1 if dom == 'expert_up' else 2}>", w.name,
                                           STREAM_SOURCES),
                 "alg_bytes_per_launch": alg_bytes, "ms_per_launch": kern_ms[dom],
                 "peak_source": f"{peak_src} hbm_gbs"}

@@ -4,34 +4,35 @@
 //
 // Work unit = (expert with at least one row, 64-column slab of its weight matrix).
 // A CTA owns the slab for the full depth K, so the GeLU (up) or gate (down)
-// epilogue applies locally and no partial sums leave the CTA. Each k-row of the
-// slab is 128 contiguous bytes read by 8 lanes with 16-byte loads; two batches of 8
-// loads per thread are in flight (software pipelining), two CTAs per SM. The expert's
-// rows (2 or 4 per pass, by batch size; more rows take more passes) are staged in
-// shared memory as fp32 in 1024-deep chunks.
+// epilogue applies locally and no partial sums leave the CTA. Units are ordered
+// slab-fastest, so CTAs running together stream neighbouring slabs of the same
+// matrix rows.
+//
+// The weights arrive by TMA: one producer warp keeps a ring of five 16 KB boxes
+// (64 columns x 128 k-rows of one expert) in flight per CTA, two CTAs per SM, so the
+// bytes in flight do not depend on registers. The eight consumer warps read each box
+// from shared memory, 8 lanes x 16 bytes per k-row, and release it to the producer.
+// The expert's rows (1, 2 or 4 per pass, by batch size; more rows take more passes)
+// are staged as fp32 in shared memory between named barriers of the consumer warps
+// only, so the weight stream never waits for them.
 // Partial sums are combined in a fixed order (xor-butterfly in the warp, then
 // warps in index order), so results are reproducible.
-// Units are ordered slab-fastest, so CTAs running together stream neighbouring
-// slabs of the same matrix rows.
+//
+// Ring depth, box height and L2 promotion were swept on decode shapes (d = d_ff =
+// 8192, 1/8/64 tokens): 128-row boxes five deep without promotion were best or
+// within noise of the best everywhere; three deep fell to 0.83 of HBM for one token,
+// and 64-row boxes lost 2-5%.
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256, kWarps = 8;
-constexpr int NS = 64;            // columns per slab
-constexpr int LPR = NS / 8;       // lanes per k-row: 8 (16 bytes each)
-constexpr int RPW = 32 / LPR;     // k-rows per warp per step: 4
-constexpr int KSTEP = kWarps * RPW;  // k-rows per CTA step: 32
-// k-depth of activations staged per chunk: 32 KB of fp32 rows. Each chunk restarts the weight
-// stream behind two barriers, so chunks are made as deep as the two-CTAs-per-SM budget allows.
-template <int RMAX>
-constexpr int kc_for() { return RMAX <= 2 ? 4096 : 2048; }
-// Weight loads per thread per batch (two batches in flight): 8 with 2 rows a pass; with 4 rows
-// the accumulators take the registers, and 8 would spill.
-template <int RMAX>
-constexpr int unroll_for() { return RMAX == 1 ? 9 : RMAX <= 2 ? 8 : 7; }
+constexpr int kThreads = 256, kWarps = 8;  // consumer warps
+constexpr int NS = 64;                     // columns per slab
+constexpr int LPR = NS / 8;                // lanes per k-row: 8 (16 bytes each)
+constexpr int RPW = 32 / LPR;              // k-rows per warp per step: 4
+constexpr int KSTEP = kWarps * RPW;        // k-rows per CTA step: 32
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&v)[8]) {
   v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
@@ -59,24 +60,47 @@ __device__ __forceinline__ void stage_rows(const __nv_bfloat16* __restrict__ a, 
   }
 }
 
-// up (STAGE 1) writes bf16 h; down (STAGE 2) writes fp32 y_perm.
-// RMAX rows of an expert per pass over its weights (more rows take more passes).
+constexpr int kTmaRows = 128;                    // k-rows per box
+constexpr int kTmaBoxBytes = kTmaRows * NS * 2;  // 16 KB
+constexpr int kTmaStages = 5;                    // boxes in flight per CTA
+constexpr int kTmaThreads = kThreads + 32;       // 8 consumer warps + the producer warp
+constexpr int kTmaActFloats = 4096;              // staged activations: RMAX rows x 4096/RMAX
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
 template <int STAGE, typename OutT, int RMAX>
-__global__ void __launch_bounds__(kThreads, 2)
-ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restrict__ a_rows,
-                  const __nv_bfloat16* __restrict__ w, const int32_t* __restrict__ offsets,
-                  const float* __restrict__ row_gate, int K, int N, int E, OutT* __restrict__ out) {
-  constexpr int kUnroll = unroll_for<RMAX>();
-  constexpr int KC = kc_for<RMAX>();
-  extern __shared__ __align__(16) float smem[];
-  float* sA = smem;                         // [RMAX][KC]
-  float* sRed = sA + RMAX * KC;             // [kWarps][RMAX][NS]
-  int* sAct = reinterpret_cast<int*>(sRed + kWarps * RMAX * NS);  // [E] experts with rows
-  __shared__ int s_nact;
+__global__ void __launch_bounds__(kTmaThreads, 2)
+ffn_stream_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __nv_bfloat16* __restrict__ a,
+                      const int32_t* __restrict__ a_rows, const int32_t* __restrict__ offsets,
+                      const float* __restrict__ row_gate, int K, int N, int E, int nst, OutT* __restrict__ out,
+                      int* status, uint64_t timeout_ns) {
+  constexpr int KC = kTmaActFloats / RMAX;  // a multiple of kTmaRows
+  extern __shared__ uint8_t smem_raw[];
+  // ring [nst][kTmaRows][NS] bf16 | sA [RMAX][KC] fp32 (the epilogue's per-warp sums reuse it)
+  // | sAct [E] | full [nst], empty [nst] mbarriers
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t ring = (raw + 127u) & ~127u;
+  uint8_t* gring = smem_raw + (ring - raw);
+  float* sA = reinterpret_cast<float*>(gring + nst * kTmaBoxBytes);
+  float* sRed = sA;  // [kWarps][RMAX][NS]
+  int* sAct = reinterpret_cast<int*>(sA + RMAX * KC);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sAct + ((E + 1) & ~1));
+  __shared__ int s_nact, s_abort;
+  volatile int* abort_flag = &s_abort;
+  auto full = [&](int st) { return smem_u32(bars + st); };
+  auto empty = [&](int st) { return smem_u32(bars + nst + st); };
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == kWarps && lane == 0) {
+    for (int st = 0; st < nst; ++st) {
+      mbar_init(full(st), 1);
+      mbar_init(empty(st), kWarps);
+    }
+    fence_mbar_init();
+    *abort_flag = 0;
+    tma_prefetch_desc(&tmW);
+  }
   griddep_launch_dependents();
   griddep_wait();
-
   if (warp == 0) {
     int base = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
@@ -91,69 +115,86 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restrict
   __syncthreads();
   const int nslab = (N + NS - 1) / NS;
   const int units = s_nact * nslab;
-  const int kr = lane / LPR;            // k-row of this lane within the warp's group of RPW
-  const int cg = lane % LPR;            // 8-column group of this lane
+  const int KB = (K + kTmaRows - 1) / kTmaRows;  // boxes per pass; rows past K arrive as zeros
 
+  if (warp == kWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t phase = 0, filled = 0, fill_phase = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int e = sAct[u / nslab], n0 = (u % nslab) * NS;
+        const int passes = (offsets[e + 1] - offsets[e] + RMAX - 1) / RMAX;
+        for (int ps = 0; ps < passes; ++ps)
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!wait_or_abort(empty(st), phase ^ 1u, timeout_ns, abort_flag, status, 51)) goto producer_out;
+            mbar_arrive_expect_tx(full(st), kTmaBoxBytes);
+            tma_load_3d(ring + st * kTmaBoxBytes, &tmW, n0, kb * kTmaRows, e, full(st));
+            filled |= 1u << st;
+            fill_phase = (fill_phase & ~(1u << st)) | (phase << st);
+            if (++st == nst) { st = 0; phase ^= 1u; }
+          }
+      }
+    producer_out:
+      // copies in flight land before the CTA (and its shared memory) goes away
+      for (int q = 0; q < nst; ++q)
+        if (filled & (1u << q)) mbar_wait_bounded(full(q), (fill_phase >> q) & 1u, timeout_ns);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers (warps 0..7)
+  // Every consumer warp runs the same trip counts, so the named barriers always match; after a
+  // failed wait (recorded in the status word) the warps skip the arithmetic and run to the end.
+  const int kr = lane / LPR, cg = lane % LPR;
+  int st = 0;
+  uint32_t phase = 0;
+  bool ok = true;
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
     const int e = sAct[u / nslab];
     const int n0 = (u % nslab) * NS;
-    const int col = n0 + cg * 8;
-    const bool col_ok = col < N;
-    const __nv_bfloat16* we = w + (size_t)e * K * N;
     const int r_begin = offsets[e], r_end = offsets[e + 1];
     for (int rp = r_begin; rp < r_end; rp += RMAX) {
       const int R = min(RMAX, r_end - rp);
-      uint64_t acc2[RMAX][4];  // column pairs (2p, 2p+1) of each row, fp32x2
+      uint64_t acc2[RMAX][4];
 #pragma unroll
       for (int r = 0; r < RMAX; ++r)
 #pragma unroll
-        for (int p = 0; p < 4; ++p) acc2[r][p] = 0ull;
-
+        for (int q = 0; q < 4; ++q) acc2[r][q] = 0ull;
       for (int kc = 0; kc < K; kc += KC) {
         const int kn = min(KC, K - kc);
-        // Software-pipelined: the next batch of kUnroll weight loads is issued before the
-        // current batch is consumed, so two batches per thread are in flight. The first batch
-        // goes out before the activations are staged, so staging overlaps the weight stream.
-        auto load_batch = [&](int k0, uint4 (&wv)[kUnroll]) {
-#pragma unroll
-          for (int i = 0; i < kUnroll; ++i) {
-            const int kk = k0 + i * KSTEP + warp * RPW + kr;
-            if (col_ok && kk < kn)
-              wv[i] = __ldg(reinterpret_cast<const uint4*>(we + (size_t)(kc + kk) * N + col));
-            else
-              wv[i] = make_uint4(0u, 0u, 0u, 0u);
-          }
-        };
-        uint4 cur[kUnroll], nxt[kUnroll];
-        load_batch(0, cur);
-        __syncthreads();
+        consumer_sync();  // the previous chunk's activations (or the last epilogue's sums) are read
         stage_rows<KC>(a, a_rows, K, rp, R, kc, kn, sA);
-        __syncthreads();
-        for (int k0 = 0; k0 < kn; k0 += KSTEP * kUnroll) {
-          if (k0 + KSTEP * kUnroll < kn) load_batch(k0 + KSTEP * kUnroll, nxt);
+        consumer_sync();
+        for (int kb = 0; kb < kn; kb += kTmaRows) {
+          if (ok) ok = wait_or_abort(full(st), phase, timeout_ns, abort_flag, status, 52);
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok) {
+            const uint8_t* box = gring + st * kTmaBoxBytes;
 #pragma unroll
-          for (int i = 0; i < kUnroll; ++i) {
-            const int kk = k0 + i * KSTEP + warp * RPW + kr;
-            if (kk >= kn) break;
-            // bf16 pair (lo, hi) of each 32-bit word -> two fp32 in one 64-bit register
-            const uint32_t wv[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
-            uint64_t w2[4];
+            for (int i = 0; i < kTmaRows / KSTEP; ++i) {
+              const int kk = i * KSTEP + warp * RPW + kr;  // k-row within the box
+              const uint4 v = *reinterpret_cast<const uint4*>(box + kk * (NS * 2) + cg * 16);
+              const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+              uint64_t w2[4];
 #pragma unroll
-            for (int p = 0; p < 4; ++p) w2[p] = ((uint64_t)(wv[p] & 0xFFFF0000u) << 32) | (uint64_t)(wv[p] << 16);
+              for (int q = 0; q < 4; ++q) w2[q] = ((uint64_t)(wv[q] & 0xFFFF0000u) << 32) | (uint64_t)(wv[q] << 16);
 #pragma unroll
-            for (int r = 0; r < RMAX; ++r) {
-              if (r >= R) break;
-              const float av = sA[r * KC + kk];
-              const uint64_t av2 = f2_pack(av, av);
+              for (int r = 0; r < RMAX; ++r) {
+                if (r >= R) break;
+                const float av = sA[r * KC + kb + kk];
+                const uint64_t av2 = f2_pack(av, av);
 #pragma unroll
-              for (int p = 0; p < 4; ++p) acc2[r][p] = ffma2(av2, w2[p], acc2[r][p]);
+                for (int q = 0; q < 4; ++q) acc2[r][q] = ffma2(av2, w2[q], acc2[r][q]);
+              }
             }
           }
-#pragma unroll
-          for (int i = 0; i < kUnroll; ++i) cur[i] = nxt[i];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty(st));  // the box's slot goes back to the producer
+          if (++st == nst) { st = 0; phase ^= 1u; }
         }
       }
-      // Combine the RPW k-row groups of the warp (lanes cg, cg+8, cg+16, cg+24), then the warps.
+      // the warp's RPW k-row groups (lanes cg, cg+8, cg+16, cg+24), then the warps in index order
       float acc[RMAX][8];
 #pragma unroll
       for (int r = 0; r < RMAX; ++r)
@@ -164,12 +205,13 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restrict
           v += __shfl_xor_sync(0xffffffffu, v, 2 * LPR);
           acc[r][c] = v;
         }
+      consumer_sync();  // sRed overlays the activations
       if (lane < LPR) {
         for (int r = 0; r < R; ++r)
 #pragma unroll
           for (int c = 0; c < 8; ++c) sRed[(warp * RMAX + r) * NS + cg * 8 + c] = acc[r][c];
       }
-      __syncthreads();
+      consumer_sync();
       for (int i = tid; i < R * NS; i += kThreads) {
         const int r = i / NS, c = i % NS;
         const int gn = n0 + c;
@@ -185,18 +227,40 @@ ffn_stream_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restrict
   }
 }
 
+constexpr size_t kSmPerSmBytes = 228 * 1024;  // shared memory per SM, of which 1 KB per resident CTA is reserved
+
+size_t tma_smem_bytes(int nst, int E) {
+  return 128 + (size_t)nst * kTmaBoxBytes + (size_t)kTmaActFloats * sizeof(float) + (size_t)((E + 1) & ~1) * 4 +
+         (size_t)2 * nst * 8;
+}
+
 template <int STAGE, typename OutT, int RMAX>
-cudaError_t launch_t(const FfnArgs& p, cudaStream_t s) {
-  const size_t smem = (size_t)(RMAX * kc_for<RMAX>() + kWarps * RMAX * NS) * sizeof(float) + (size_t)p.E * sizeof(int);
-  auto kern = ffn_stream_kernel<STAGE, OutT, RMAX>;
+cudaError_t launch_tma(const FfnArgs& p, EncodeTiledFn enc, cudaStream_t s) {
+  // the deepest ring that keeps two CTAs per SM
+  // five boxes deep, fewer where a large E leaves no room for two CTAs per SM
+  int nst = kTmaStages;
+  while (nst > 2 && 2 * (tma_smem_bytes(nst, p.E) + 1024) > kSmPerSmBytes) --nst;
+  const size_t smem = tma_smem_bytes(nst, p.E);
+  auto kern = ffn_stream_tma_kernel<STAGE, OutT, RMAX>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
+  // weights [E][K][N] as a 3D map: 64 columns x 128 k-rows of one expert per box, no swizzle, no L2
+  // promotion (each weight byte is read once); rows past K and columns past N arrive as zeros
+  CUtensorMap tmW;
+  const cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.K, (cuuint64_t)p.E};
+  const cuuint64_t str[2] = {(cuuint64_t)p.N * 2, (cuuint64_t)p.K * p.N * 2};
+  const cuuint32_t box[3] = {NS, kTmaRows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.w), dims, str, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   const int nslab = (p.N + NS - 1) / NS;
   const long long max_units = (long long)(p.rows < p.E ? p.rows : p.E) * nslab;
-  long long grid = (long long)device_sm_count() * (RMAX <= 2 ? 8 : 4);
+  long long grid = 2LL * device_sm_count();  // persistent: the resident CTAs loop over the units
   if (grid > max_units) grid = max_units;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, (const __nv_bfloat16*)p.a, p.a_rows,
-                    (const __nv_bfloat16*)p.w, p.offsets, p.row_gate, p.K, p.N, p.E, (OutT*)p.out);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, s, tmW, (const __nv_bfloat16*)p.a, p.a_rows,
+                    p.offsets, p.row_gate, p.K, p.N, p.E, nst, (OutT*)p.out, p.status, p.timeout_ns);
 }
 
 }  // namespace
@@ -204,13 +268,15 @@ cudaError_t launch_t(const FfnArgs& p, cudaStream_t s) {
 cudaError_t launch_ffn_stream(const FfnArgs& p, cudaStream_t s) {
   if (p.rows == 0) return cudaSuccess;
   if (p.dt != MOE_DTYPE_BF16) return cudaErrorNotSupported;
-  // Rows per expert are at most T*k; small batches keep fewer accumulators (more CTAs per SM).
-  // An expert with more rows than a pass holds streams its weights again for the rest.
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  // Rows per expert are at most T*k; one row a pass for one token, two for small batches, four
+  // otherwise. An expert with more rows than a pass holds streams its weights again for the rest.
   if (p.max_rows_per_expert == 1)
-    return p.stage == 1 ? launch_t<1, __nv_bfloat16, 1>(p, s) : launch_t<2, float, 1>(p, s);
+    return p.stage == 1 ? launch_tma<1, __nv_bfloat16, 1>(p, enc, s) : launch_tma<2, float, 1>(p, enc, s);
   if (p.rows <= 32)
-    return p.stage == 1 ? launch_t<1, __nv_bfloat16, 2>(p, s) : launch_t<2, float, 2>(p, s);
-  return p.stage == 1 ? launch_t<1, __nv_bfloat16, 4>(p, s) : launch_t<2, float, 4>(p, s);
+    return p.stage == 1 ? launch_tma<1, __nv_bfloat16, 2>(p, enc, s) : launch_tma<2, float, 2>(p, enc, s);
+  return p.stage == 1 ? launch_tma<1, __nv_bfloat16, 4>(p, enc, s) : launch_tma<2, float, 4>(p, enc, s);
 }
 
 }  // namespace moe

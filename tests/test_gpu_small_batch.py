@@ -1,5 +1,6 @@
 """Decode-sized batches (T <= 8, bf16, weight-streaming GEMMs): the one-launch router + dispatch,
-whose FFN reads x rows through the permutation, against the fp64 oracle.
+whose FFN reads x rows through the permutation (and, for one token, splits the weight slabs between
+CTAs, stream-K), against the fp64 oracle.
 
 Bars as for every forward: routing indices and counts bit-exact, gates within 1e-5, the output
 within 2e-2 of its RMS (or the bf16-h rounding bound when that alone is larger).
@@ -39,11 +40,14 @@ CASES = [
     dict(T=8, d=512, F=64, E=16, k=2, cf=0.5),        # capacity: assignments dropped
     dict(T=2, d=512, F=64, E=8, k=4, cf=0.5),         # capacity on the plain-CTA (T <= 2) variant
     dict(T=4, d=512, F=64, E=32, k=3, bias=True),     # router bias
+    dict(T=1, d=136, F=200, E=8, k=3),                # one token, ragged slabs: stream-K pieces of 8
+    dict(T=1, d=2048, F=1024, E=16, k=8),             # one token, k = 8: slabs split between two CTAs
 ]
 
 
 @pytest.mark.parametrize("renormalise", [False, True], ids=["raw", "renorm"])
-@pytest.mark.parametrize("cfg", CASES, ids=["t1", "t8", "k_eq_e", "e1024", "d136", "e6", "cap", "cap_t2", "bias"])
+@pytest.mark.parametrize("cfg", CASES, ids=["t1", "t8", "k_eq_e", "e1024", "d136", "e6", "cap", "cap_t2", "bias",
+                                         "t1_ragged", "t1_k8"])
 def test_forward_small_batch(cfg, renormalise):
     cfg = dict(cfg)
     cf = cfg.pop("cf", 0.0)
