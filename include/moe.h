@@ -289,6 +289,9 @@ moe_status moe_selftest_wait_timeout(void* workspace, size_t ws_bytes, int timeo
  *   y_perm fp32) reading quantised W1 [E, d, F] / W2 [E, F, d]; weight-streaming kernel for any
  *   number of rows (built for decode batches). moe_forward_q: the whole layer with them (x, w_r
  *   bf16; out_dt, flags, capacity, router_stats and the workspace as in moe_forward_ex).
+ *   The streaming kernel's waits on its own copies are bounded: moe_forward_q records a wait that
+ *   gave up as MOE_ERR_DEVICE_TIMEOUT in its workspace; moe_expert_up_q / moe_expert_down_q take
+ *   no workspace, so there the kernel ends early without a record.
  * Sizes 0 / MOE_ERR_INVALID_ARG on bad sizes, NULL or misaligned pointers. */
 size_t moe_qweight_bytes(int K, int N, int E, int bits);
 size_t moe_qscale_bytes(int K, int N, int E);

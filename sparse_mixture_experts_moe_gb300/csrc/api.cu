@@ -297,7 +297,7 @@ inline bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7
 
 moe_status expert_half_q(int stage, const void* a, const void* codes, const float* scale_min,
                          const int32_t* offsets, const float* row_gate, int T, int d, int F, int E, int k, int bits,
-                         void* out, void* stream, const int32_t* a_rows = nullptr) {
+                         void* out, void* stream, const int32_t* a_rows = nullptr, int* status = nullptr) {
   if (!sizes_ok(T, d, F, E, k, MOE_DTYPE_BF16)) return MOE_ERR_INVALID_ARG;
   const int K = stage == 1 ? d : F, N = stage == 1 ? F : d;
   if (!qsizes_ok(K, N, E, bits)) return MOE_ERR_INVALID_ARG;
@@ -306,7 +306,8 @@ moe_status expert_half_q(int stage, const void* a, const void* codes, const floa
       (stage == 2 && row_gate == nullptr))
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(a) || !aligned16(codes) || !aligned8(scale_min) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
-  QFfnArgs p{a, codes, scale_min, offsets, row_gate, out, T * k, K, N, E, bits, stage, a_rows, T};
+  QFfnArgs p{a, codes, scale_min, offsets, row_gate, out, T * k, K, N, E, bits, stage, a_rows, T, status,
+             wait_timeout_ns()};
   return cuda_status(launch_ffn_stream_q(p, (cudaStream_t)stream));
 }
 }  // namespace
@@ -467,10 +468,11 @@ moe_status moe_forward_q(const void* x, const void* w_r, const float* b_r, const
   moe_status st = route_and_dispatch(x, w_r, b_r, T, d, E, k, dt, flags, capacity, rs, idx, gate, cnt, offs, perm,
                                      rowof, rgate, xp, L, workspace, ws_bytes, stream, true, &via_perm);
   if (st != MOE_OK) return st;
-  st = via_perm ? expert_half_q(1, x, w1_codes, w1_scale_min, offs, nullptr, T, d, F, E, k, bits, h, stream, perm)
-                : moe_expert_up_q(xp, w1_codes, w1_scale_min, offs, T, d, F, E, k, bits, h, stream);
+  int* status = at<int>(workspace, 0);
+  st = expert_half_q(1, via_perm ? x : xp, w1_codes, w1_scale_min, offs, nullptr, T, d, F, E, k, bits, h, stream,
+                     via_perm ? perm : nullptr, status);
   if (st != MOE_OK) return st;
-  st = moe_expert_down_q(h, w2_codes, w2_scale_min, offs, rgate, T, d, F, E, k, bits, yp, stream);
+  st = expert_half_q(2, h, w2_codes, w2_scale_min, offs, rgate, T, d, F, E, k, bits, yp, stream, nullptr, status);
   if (st != MOE_OK) return st;
   return moe_combine(yp, rowof, T, d, k, out_dt, out, stream);
 }

@@ -65,6 +65,8 @@ constexpr int kTmaBoxBytes = kTmaRows * NS * 2;  // 16 KB
 constexpr int kTmaStages = 5;                    // boxes in flight per CTA
 constexpr int kTmaThreads = kThreads + 32;       // 8 consumer warps + the producer warp
 constexpr int kTmaActFloats = 4096;              // staged activations: RMAX rows x 4096/RMAX
+constexpr int kBarSlotBytes = 128;               // the ring's mbarriers: 2 x kTmaStages x 8 bytes
+static_assert(2 * kTmaStages * 8 <= kBarSlotBytes, "the mbarriers fit their slot");
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
 
@@ -76,15 +78,15 @@ ffn_stream_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __nv_bfloat
                       int* status, uint64_t timeout_ns) {
   constexpr int KC = kTmaActFloats / RMAX;  // a multiple of kTmaRows
   extern __shared__ uint8_t smem_raw[];
-  // ring [nst][kTmaRows][NS] bf16 | sA [RMAX][KC] fp32 (the epilogue's per-warp sums reuse it)
-  // | sAct [E] | full [nst], empty [nst] mbarriers
+  // ring [nst][kTmaRows][NS] bf16 (128-byte aligned) | full [nst], empty [nst] mbarriers in a
+  // 128-byte slot | sA [RMAX][KC] fp32 (the epilogue's per-warp sums reuse it) | sAct [E]
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t ring = (raw + 127u) & ~127u;
   uint8_t* gring = smem_raw + (ring - raw);
-  float* sA = reinterpret_cast<float*>(gring + nst * kTmaBoxBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gring + nst * kTmaBoxBytes);
+  float* sA = reinterpret_cast<float*>(gring + nst * kTmaBoxBytes + kBarSlotBytes);
   float* sRed = sA;  // [kWarps][RMAX][NS]
   int* sAct = reinterpret_cast<int*>(sA + RMAX * KC);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sAct + ((E + 1) & ~1));
   __shared__ int s_nact, s_abort;
   volatile int* abort_flag = &s_abort;
   auto full = [&](int st) { return smem_u32(bars + st); };
@@ -230,8 +232,7 @@ ffn_stream_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __nv_bfloat
 constexpr size_t kSmPerSmBytes = 228 * 1024;  // shared memory per SM, of which 1 KB per resident CTA is reserved
 
 size_t tma_smem_bytes(int nst, int E) {
-  return 128 + (size_t)nst * kTmaBoxBytes + (size_t)kTmaActFloats * sizeof(float) + (size_t)((E + 1) & ~1) * 4 +
-         (size_t)2 * nst * 8;
+  return 128 + (size_t)nst * kTmaBoxBytes + kBarSlotBytes + (size_t)kTmaActFloats * sizeof(float) + (size_t)E * 4;
 }
 
 template <int STAGE, typename OutT, int RMAX>

@@ -97,6 +97,8 @@ struct QFfnArgs {
   int rows, K, N, E, bits, stage;
   const int32_t* a_rows;    // nullable: row r of `a` is a[a_rows[r]]
   int max_rows_per_expert;  // an upper bound (T: a token's k experts are distinct); 0: unknown
+  int* status;              // nullable: where a bounded device wait that gave up is recorded
+  uint64_t timeout_ns;
 };
 cudaError_t launch_quantize(const void* w, int K, int N, int E, int dt, int bits, void* codes, float* scale_min,
                             cudaStream_t s);

@@ -35,14 +35,6 @@ constexpr int NS = 64;              // columns per slab (one block column)
 constexpr int LPR = NS / 8;         // lanes per tile row: 8
 constexpr int RPW = 32 / LPR;       // tile rows per warp per step: 4
 constexpr int GSTEP = kWarps * RPW; // tile rows per CTA step: 32
-// k-depth of activations staged per chunk (32 KB of fp32 rows): deep, since each chunk restarts
-// the code stream behind two barriers and a 4-bit chunk is little work per thread.
-template <int RMAX>
-constexpr int kc_for() { return RMAX <= 2 ? 4096 : 2048; }
-// Code tiles per thread per batch (two batches in flight): as many as the registers allow without
-// spilling, which is more with fewer rows a pass (a single token: each expert gets one row).
-template <int BITS, int RMAX>
-constexpr int unroll_q() { return RMAX <= 2 ? 8 : 6; }
 constexpr float kMagic = 8388608.0f;  // 2^23: a byte b placed in the low mantissa bits reads 2^23 + b
 
 // ------------------------------------------------------------------ quantiser
@@ -171,28 +163,61 @@ __device__ __forceinline__ void stage_rows_q(const __nv_bfloat16* __restrict__ a
   }
 }
 
+constexpr int kTmaTileRows = 128;                      // tile rows per box (128 x KT k-rows)
+constexpr int kTmaBoxBytes = kTmaTileRows * LPR * 16;  // 16 KB: 8 tiles (64 columns) per tile row
+constexpr int kTmaStages = 5;                          // boxes in flight per CTA
+constexpr int kTmaThreads = kThreads + 32;             // 8 consumer warps + the producer warp
+constexpr int kTmaActFloats = 4096;                    // staged activations: RMAX rows x 4096/RMAX
+constexpr int kBarSlotBytes = 128;                     // the ring's mbarriers: 2 x kTmaStages x 8 bytes
+static_assert(2 * kTmaStages * 8 <= kBarSlotBytes, "the mbarriers fit their slot");
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
+// The code stream arrives by TMA: one producer warp keeps a ring of 16 KB boxes (the 8 tiles of a
+// 64-column slab for 128 consecutive tile rows of one expert) in flight, two CTAs per SM, and the
+// eight consumer warps read the tiles from shared memory, one 16-byte tile per lane, and release
+// each box. The activations, the slab's (scale, min) pairs and the block sums are staged between
+// named barriers of the consumer warps only, so the code stream never waits for them.
 template <int BITS, int STAGE, typename OutT, int RMAX>
-__global__ void __launch_bounds__(kThreads, 2)
-ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restrict__ a_rows,
-                    const uint4* __restrict__ codes,
-                    const float2* __restrict__ sm, const int32_t* __restrict__ offsets,
-                    const float* __restrict__ row_gate, int K, int N, int E, OutT* __restrict__ out) {
+__global__ void __launch_bounds__(kTmaThreads, 2)
+ffn_stream_q_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16* __restrict__ a,
+                    const int32_t* __restrict__ a_rows, const float2* __restrict__ sm,
+                    const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
+                    int nst, OutT* __restrict__ out, int* status, uint64_t timeout_ns) {
   constexpr int KT = 16 / BITS;  // k-rows per tile: 128 bits / (8 columns x BITS)
   static_assert(KT * 8 * BITS == 128 && (BITS == 4 ? KT == 4 : KT == 2), "tile words hold KT k-rows");
-  constexpr int KC = kc_for<RMAX>();
-  constexpr int kUnroll = unroll_q<BITS, RMAX>();
-  extern __shared__ __align__(16) float smem[];
-  float* sA = smem;                                     // [RMAX][KC]
-  float* sRed = sA + RMAX * KC;                         // [kWarps][RMAX][NS]
-  float2* sSM = reinterpret_cast<float2*>(sRed + kWarps * RMAX * NS);  // [K / 64] this slab's blocks
-  float* sBS = reinterpret_cast<float*>(sSM + K / QB);  // [RMAX][KC / 64] activation block sums
-  float* sMin = sBS + RMAX * (KC / QB);                 // [RMAX] block-minimum term of each row
-  int* sAct = reinterpret_cast<int*>(sMin + RMAX);      // [E] experts with rows
-  __shared__ int s_nact;
+  constexpr int KC = kTmaActFloats / RMAX;  // a multiple of the k-rows of a box (128 KT)
+  static_assert(KC % (kTmaTileRows * KT) == 0, "a chunk holds whole boxes");
+  extern __shared__ uint8_t smem_raw[];
+  // ring [nst][128 tile rows][8 tiles] (128-byte aligned) | full [nst], empty [nst] mbarriers in
+  // a 128-byte slot | sA [RMAX][KC] (the epilogue's per-warp sums reuse it) | sSM [K/64]
+  // | sBS [RMAX][KC/64] | sMin [RMAX] | sAct [E]
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t ring = (raw + 127u) & ~127u;
+  uint8_t* gring = smem_raw + (ring - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gring + nst * kTmaBoxBytes);
+  float* sA = reinterpret_cast<float*>(gring + nst * kTmaBoxBytes + kBarSlotBytes);
+  float* sRed = sA;  // [kWarps][RMAX][NS]
+  float2* sSM = reinterpret_cast<float2*>(sA + RMAX * KC);
+  float* sBS = reinterpret_cast<float*>(sSM + K / QB);
+  float* sMin = sBS + RMAX * (KC / QB);
+  int* sAct = reinterpret_cast<int*>(sMin + RMAX);
+  __shared__ int s_nact, s_abort;
+  volatile int* abort_flag = &s_abort;
+  auto full = [&](int st) { return smem_u32(bars + st); };
+  auto empty = [&](int st) { return smem_u32(bars + nst + st); };
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == kWarps && lane == 0) {
+    for (int st = 0; st < nst; ++st) {
+      mbar_init(full(st), 1);
+      mbar_init(empty(st), kWarps);
+    }
+    fence_mbar_init();
+    *abort_flag = 0;
+    tma_prefetch_desc(&tmC);
+  }
   griddep_launch_dependents();
   griddep_wait();
-
   if (warp == 0) {
     int base = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
@@ -207,16 +232,49 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restri
   __syncthreads();
   const int nslab = N / NS;
   const int units = s_nact * nslab;
+  const int KG = K / KT;                                   // tile rows of a matrix
+  const int KB = (KG + kTmaTileRows - 1) / kTmaTileRows;  // boxes per pass; rows past KG arrive as zeros
+
+  if (warp == kWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t phase = 0, filled = 0, fill_phase = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int e = sAct[u / nslab], slab = u % nslab;
+        const int passes = (offsets[e + 1] - offsets[e] + RMAX - 1) / RMAX;
+        for (int ps = 0; ps < passes; ++ps)
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!wait_or_abort(empty(st), phase ^ 1u, timeout_ns, abort_flag, status, 53)) goto producer_out;
+            mbar_arrive_expect_tx(full(st), kTmaBoxBytes);
+            tma_load_3d(ring + st * kTmaBoxBytes, &tmC, slab * NS, kb * kTmaTileRows, e, full(st));
+            filled |= 1u << st;
+            fill_phase = (fill_phase & ~(1u << st)) | (phase << st);
+            if (++st == nst) { st = 0; phase ^= 1u; }
+          }
+      }
+    producer_out:
+      // copies in flight land before the CTA (and its shared memory) goes away
+      for (int q = 0; q < nst; ++q)
+        if (filled & (1u << q)) mbar_wait_bounded(full(q), (fill_phase >> q) & 1u, timeout_ns);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers (warps 0..7)
+  // Every consumer warp runs the same trip counts, so the named barriers always match; after a
+  // failed wait (recorded in the status word) the warps skip the arithmetic and run to the end.
   const int kr = lane / LPR;  // tile row of this lane within the warp's group of RPW
   const int cg = lane % LPR;  // 8-column group of this lane
-  const int KG = K / KT, NG = N / 8, NB = N / QB;
-
+  const int NB = N / QB;
+  int st = 0;
+  uint32_t phase = 0;
+  bool ok = true;
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
     const int e = sAct[u / nslab];
     const int slab = u % nslab;
     const int n0 = slab * NS;
-    const uint4* ce = codes + (size_t)e * KG * NG + (size_t)slab * LPR + cg;
-    __syncthreads();  // the previous unit is done with sSM
+    consumer_sync();  // the previous unit is done with sSM
     for (int b = tid; b < K / QB; b += kThreads) sSM[b] = sm[((size_t)e * (K / QB) + b) * NB + slab];
     const int r_begin = offsets[e], r_end = offsets[e + 1];
     for (int rp = r_begin; rp < r_end; rp += RMAX) {
@@ -225,58 +283,52 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restri
 #pragma unroll
       for (int r = 0; r < RMAX; ++r)
 #pragma unroll
-        for (int p = 0; p < 4; ++p) acc2[r][p] = 0ull;
+        for (int q = 0; q < 4; ++q) acc2[r][q] = 0ull;
       float min_term = 0.f;  // thread r < R: row r's sum over blocks of (min_b + m scale_b) * (sum of a over b)
       for (int kc = 0; kc < K; kc += KC) {
         const int kn = min(KC, K - kc);  // a multiple of 64
-        const int gn = kn / KT;          // tile rows in this chunk
-        auto load_batch = [&](int g0, uint4 (&t)[kUnroll]) {
-#pragma unroll
-          for (int i = 0; i < kUnroll; ++i) {
-            const int g = g0 + i * GSTEP + warp * RPW + kr;
-            t[i] = g < gn ? __ldg(ce + (size_t)(kc / KT + g) * NG) : make_uint4(0u, 0u, 0u, 0u);
-          }
-        };
-        uint4 cur[kUnroll], nxt[kUnroll];
-        load_batch(0, cur);  // in flight while the activations are staged
-        __syncthreads();
+        consumer_sync();  // sSM is written; the previous chunk's activations (or sums) are read
         stage_rows_q<KC>(a, a_rows, K, rp, R, kc, kn, sSM, sA, sBS);
-        __syncthreads();
+        consumer_sync();
         if (tid < R)
           for (int b = 0; b < kn / QB; ++b) {  // w = (min + centre * scale) + (c - centre) * scale
             const float2 q = sSM[kc / QB + b];
             min_term = fmaf(fmaf(kCentre<BITS>, q.x, q.y), sBS[tid * (KC / QB) + b], min_term);
           }
-        for (int g0 = 0; g0 < gn; g0 += GSTEP * kUnroll) {
-          if (g0 + GSTEP * kUnroll < gn) load_batch(g0 + GSTEP * kUnroll, nxt);
+        for (int kb = 0; kb < kn; kb += kTmaTileRows * KT) {
+          if (ok) ok = wait_or_abort(full(st), phase, timeout_ns, abort_flag, status, 54);
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok) {
+            const uint8_t* box = gring + st * kTmaBoxBytes;
 #pragma unroll
-          for (int i = 0; i < kUnroll; ++i) {
-            const int g = g0 + i * GSTEP + warp * RPW + kr;
-            if (g >= gn) break;
-            const int k0 = g * KT;  // first k-row of the tile within the chunk
-            const uint32_t wd[4] = {cur[i].x, cur[i].y, cur[i].z, cur[i].w};
+            for (int i = 0; i < kTmaTileRows / GSTEP; ++i) {
+              const int g = i * GSTEP + warp * RPW + kr;  // tile row within the box
+              const uint4 t = *reinterpret_cast<const uint4*>(box + g * (LPR * 16) + cg * 16);
+              const uint32_t wd[4] = {t.x, t.y, t.z, t.w};
+              const int k0 = kb + g * KT;  // first k-row of the tile within the chunk
 #pragma unroll
-            for (int j = 0; j < KT; ++j) {
-              uint64_t cp[4];
-              if (BITS == 4) int4_row(wd[j], cp);
-              else int8_row(wd[2 * j], wd[2 * j + 1], cp);
+              for (int j = 0; j < KT; ++j) {
+                uint64_t cp[4];
+                if (BITS == 4) int4_row(wd[j], cp);
+                else int8_row(wd[2 * j], wd[2 * j + 1], cp);
 #pragma unroll
-              for (int r = 0; r < RMAX; ++r) {
-                if (r >= R) break;
-                const float as = sA[r * KC + k0 + j];  // activation times its block's scale
-                const uint64_t as2 = f2_pack(as, as);
+                for (int r = 0; r < RMAX; ++r) {
+                  if (r >= R) break;
+                  const float as = sA[r * KC + k0 + j];  // activation times its block's scale
+                  const uint64_t as2 = f2_pack(as, as);
 #pragma unroll
-                for (int p = 0; p < 4; ++p) acc2[r][p] = ffma2(as2, cp[p], acc2[r][p]);
+                  for (int q = 0; q < 4; ++q) acc2[r][q] = ffma2(as2, cp[q], acc2[r][q]);
+                }
               }
             }
           }
-#pragma unroll
-          for (int i = 0; i < kUnroll; ++i) cur[i] = nxt[i];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty(st));  // the box's slot goes back to the producer
+          if (++st == nst) { st = 0; phase ^= 1u; }
         }
       }
       // Combine the warp's RPW tile rows (lanes cg, cg+8, cg+16, cg+24) and the warps in fixed
       // orders, then add each row's column-independent block-minimum term.
-      if (tid < R) sMin[tid] = min_term;
       float acc[RMAX][8];
 #pragma unroll
       for (int r = 0; r < RMAX; ++r)
@@ -287,12 +339,14 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restri
           v += __shfl_xor_sync(0xffffffffu, v, 2 * LPR);
           acc[r][c] = v;
         }
+      consumer_sync();  // sRed overlays the activations
+      if (tid < R) sMin[tid] = min_term;
       if (lane < LPR) {
         for (int r = 0; r < R; ++r)
 #pragma unroll
           for (int c = 0; c < 8; ++c) sRed[(warp * RMAX + r) * NS + cg * 8 + c] = acc[r][c];
       }
-      __syncthreads();
+      consumer_sync();
       for (int i = tid; i < R * NS; i += kThreads) {
         const int r = i / NS, c = i % NS;
         float v = 0.f;
@@ -307,30 +361,51 @@ ffn_stream_q_kernel(const __nv_bfloat16* __restrict__ a, const int32_t* __restri
   }
 }
 
+constexpr size_t kSmPerSmBytes = 228 * 1024;  // shared memory per SM, of which 1 KB per resident CTA is reserved
+
+size_t q_smem_bytes(int RMAX, int nst, int K, int E) {
+  const int KC = kTmaActFloats / RMAX;
+  return 128 + (size_t)nst * kTmaBoxBytes + kBarSlotBytes + (size_t)kTmaActFloats * sizeof(float) +
+         (size_t)(K / QB) * sizeof(float2) + (size_t)(RMAX * (KC / QB) + RMAX) * sizeof(float) + (size_t)E * 4;
+}
+
 template <int BITS, int STAGE, typename OutT, int RMAX>
-cudaError_t launch_q(const QFfnArgs& p, cudaStream_t s) {
-  const size_t smem = (size_t)(RMAX * kc_for<RMAX>() + kWarps * RMAX * NS) * sizeof(float) +
-                      (size_t)(p.K / QB) * sizeof(float2) +
-                      (size_t)(RMAX * (kc_for<RMAX>() / QB) + RMAX) * sizeof(float) + (size_t)p.E * sizeof(int);
+cudaError_t launch_q(const QFfnArgs& p, EncodeTiledFn enc, cudaStream_t s) {
+  // five boxes deep, fewer where a large K or E leaves no room for two CTAs per SM
+  int nst = kTmaStages;
+  while (nst > 2 && 2 * (q_smem_bytes(RMAX, nst, p.K, p.E) + 1024) > kSmPerSmBytes) --nst;
+  const size_t smem = q_smem_bytes(RMAX, nst, p.K, p.E);
   auto kern = ffn_stream_q_kernel<BITS, STAGE, OutT, RMAX>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
+  // codes [E][K/KT][N/8] 16-byte tiles viewed as [E][K/KT][N] 16-bit elements: 128 tile rows of a
+  // 64-column slab per box, no swizzle, no L2 promotion; tile rows past K/KT arrive as zeros
+  constexpr int KT = 16 / BITS;
+  CUtensorMap tmC;
+  const cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)(p.K / KT), (cuuint64_t)p.E};
+  const cuuint64_t str[2] = {(cuuint64_t)p.N * 2, (cuuint64_t)(p.K / KT) * p.N * 2};
+  const cuuint32_t box[3] = {NS, kTmaTileRows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(p.codes), dims, str, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   const int nslab = p.N / NS;
   const long long max_units = (long long)(p.rows < p.E ? p.rows : p.E) * nslab;
-  long long grid = (long long)device_sm_count() * (RMAX <= 2 ? 8 : 4);
+  long long grid = 2LL * device_sm_count();  // persistent: the resident CTAs loop over the units
   if (grid > max_units) grid = max_units;
-  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, (const __nv_bfloat16*)p.a, p.a_rows,
-                    (const uint4*)p.codes, (const float2*)p.scale_min, p.offsets, p.row_gate, p.K, p.N, p.E,
-                    (OutT*)p.out);
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, s, tmC, (const __nv_bfloat16*)p.a,
+                    p.a_rows, (const float2*)p.scale_min, p.offsets, p.row_gate, p.K, p.N, p.E, nst, (OutT*)p.out,
+                    p.status, p.timeout_ns);
 }
 
 template <int BITS>
-cudaError_t launch_q_bits(const QFfnArgs& p, cudaStream_t s) {
+cudaError_t launch_q_bits(const QFfnArgs& p, EncodeTiledFn enc, cudaStream_t s) {
   if (p.max_rows_per_expert == 1)  // a single token: one row per expert
-    return p.stage == 1 ? launch_q<BITS, 1, __nv_bfloat16, 1>(p, s) : launch_q<BITS, 2, float, 1>(p, s);
+    return p.stage == 1 ? launch_q<BITS, 1, __nv_bfloat16, 1>(p, enc, s) : launch_q<BITS, 2, float, 1>(p, enc, s);
   if (p.rows <= 32)
-    return p.stage == 1 ? launch_q<BITS, 1, __nv_bfloat16, 2>(p, s) : launch_q<BITS, 2, float, 2>(p, s);
-  return p.stage == 1 ? launch_q<BITS, 1, __nv_bfloat16, 4>(p, s) : launch_q<BITS, 2, float, 4>(p, s);
+    return p.stage == 1 ? launch_q<BITS, 1, __nv_bfloat16, 2>(p, enc, s) : launch_q<BITS, 2, float, 2>(p, enc, s);
+  return p.stage == 1 ? launch_q<BITS, 1, __nv_bfloat16, 4>(p, enc, s) : launch_q<BITS, 2, float, 4>(p, enc, s);
 }
 
 }  // namespace
@@ -359,7 +434,9 @@ cudaError_t launch_quantize(const void* w, int K, int N, int E, int dt, int bits
 
 cudaError_t launch_ffn_stream_q(const QFfnArgs& p, cudaStream_t s) {
   if (p.rows == 0) return cudaSuccess;
-  return p.bits == 4 ? launch_q_bits<4>(p, s) : launch_q_bits<8>(p, s);
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  return p.bits == 4 ? launch_q_bits<4>(p, enc, s) : launch_q_bits<8>(p, enc, s);
 }
 
 }  // namespace moe
