@@ -14,6 +14,7 @@ e2e        the same metric through the public layer object with the host->device
            double-buffered: a step's copies overlap the neighbouring steps' compute.
 roofline   the dominant kernel, timed live with CUDA events over back-to-back launches of its own
            C ABI call on the launching stream, against the measured peak in MEASURED_PEAKS.json.
+cold_l2    context: one step at a time after a 512 MB scrub write (median of 20), the L2 cold.
 cpu_baseline  the fp64 oracle on the host cores on a bounded prefix of the same batch.
 --impl reference  the oracle alone, timed on the host cores, on the same workload and metric.
 
@@ -369,6 +370,21 @@ def run_ours(args, w, rank, world, device):
         torch.cuda.synchronize()
         ms_direct = max_over_ranks(ed0.elapsed_time(ed1), world, device) / args.steps
 
+    # --- context: steps on a cold L2. Before each, a 512 MB buffer (four times the L2) is written on
+    # the same stream; only the step lies between the two events. The median of 20 is reported.
+    scrub = torch.empty(512 * 2**20 // 4, dtype=torch.float32, device=device)
+    cold = []
+    ec0, ec1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(20):
+        scrub.fill_(float(i))
+        ec0.record(stream)
+        step()
+        ec1.record(stream)
+        torch.cuda.synchronize()
+        cold.append(ec0.elapsed_time(ec1))
+    ms_cold = float(np.median(cold))
+    del scrub
+
     # --- per-kernel timing: the step as its separate C ABI calls (dispatch: the two-kernel public entry)
     idx = torch.empty((T, k), dtype=torch.int32, device=device)
     gate = torch.empty((T, k), dtype=torch.float32, device=device)
@@ -534,6 +550,8 @@ def run_ours(args, w, rank, world, device):
                        launch=("CUDA graph of the layer's kernels (moe_forward_graph_create), one graph launch "
                                "per step" if graph is not None else "one C ABI call per kernel")),
         "ms_per_step_direct_calls": ms_direct,
+        "cold_l2": {"ms_per_step": ms_cold, "value": job_tokens_per_s(T, world, ms_cold),
+                    "how": "each step alone after writing a 512 MB buffer on its stream, median of 20"},
         "roofline": roof,
         "kernel_ms": kern_ms,
         "experts_touched": touched,
