@@ -75,3 +75,48 @@ def test_full_size_workload(name):
     assert rel_rms_err(got32, ref["out"]) < tol
     if w.dtype == ig.DTYPE_BF16:
         assert torch.equal(out_native.view(torch.int16), out32.to(torch.bfloat16).view(torch.int16))
+
+
+class OracleQuantised:
+    """Expert e's matrix as the oracle quantises and restores it (its own 64 x 64 block quantiser on
+    the exact stored weights), computed on access: only routed experts are read."""
+
+    def __init__(self, view, bits):
+        self.view, self.bits = view, bits
+
+    def __getitem__(self, e):
+        w = self.view[e].astype(np.float32)  # exact: bf16 values are fp32 numbers
+        return oracle.dequantize_blocks(oracle.quantize_blocks(w, self.bits))
+
+
+# quantised decode at full size: workload -> sampled tokens for the output check (None: all)
+SAMPLES_Q = {"decode_t1": None, "decode_t8": 4}
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("name", list(SAMPLES_Q))
+def test_full_size_quantised_decode(name, bits):
+    """moe_forward_q on the decode workloads' full sizes (d = d_ff = 8192, E = 128), weights quantised
+    on the device, against the oracle run on the oracle's own quantisation of the same weights."""
+    w = workloads.get(name)
+    c = make_case(T=w.T, d=w.d, F=w.F, E=w.E, k=w.k, dt=w.dtype, bias_scale=workloads.bias_scale(w))
+    q1, q2 = moe.quantize(c.w1, bits), moe.quantize(c.w2, bits)
+    ws = torch.empty(moe.workspace_bytes(w.T, w.d, w.F, w.E, w.k, w.dtype), dtype=torch.uint8, device=DEV)
+    moe.workspace_init(ws)
+    idx = torch.empty((w.T, w.k), dtype=torch.int32, device=DEV)
+    out32 = torch.empty((w.T, w.d), dtype=torch.float32, device=DEV)
+    moe.forward_q(c.x, c.w_r, c.b_r, q1, q2, w.T, w.d, w.F, w.E, w.k, bits, out32, ws, topk_idx=idx,
+                  out_dt=ig.DTYPE_F32)
+    out_bf = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=DEV)
+    moe.forward_q(c.x, c.w_r, c.b_r, q1, q2, w.T, w.d, w.F, w.E, w.k, bits, out_bf, ws)
+    st, detail = moe.get_device_status(ws)
+    assert st == moe.MOE_OK, (moe.status_string(st), detail)
+    ridx = oracle.topk_select(oracle.router_logits(c.x64, c.wr64, c.br64), w.k)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    n = SAMPLES_Q[name]
+    rng = np.random.default_rng(4321)
+    toks = np.arange(w.T) if n is None or n >= w.T else np.sort(rng.choice(w.T, size=n, replace=False))
+    ref = oracle.forward(c.x64[toks], c.wr64, OracleQuantised(c.w1_host(), bits),
+                         OracleQuantised(c.w2_host(), bits), w.k, c.br64)
+    assert rel_rms_err(to_f64(out32)[toks], ref["out"]) < 2e-2
+    assert torch.equal(out_bf.view(torch.int16), out32.to(torch.bfloat16).view(torch.int16))
