@@ -77,3 +77,34 @@ def test_graph_zero_tokens_and_bad_args():
     torch.cuda.synchronize()
     with pytest.raises(moe.MoeError):
         moe.ForwardGraph(c.x, c.w_r, None, c.w1, c.w2, 4, 64, 64, 4, 9, BF16, out, ws)  # k > E
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("T", [1, 8])
+def test_graph_quantised_forward(T, bits):
+    """moe_forward_q recorded into a graph (moe_graph_capture_*, as bench.py replays it) gives the
+    direct call's output bit for bit, and the next replay picks up new input contents."""
+    c = make_case(T=T, d=1024, F=1024, E=32, k=2, dt=BF16)
+    q1, q2 = moe.quantize(c.w1, bits), moe.quantize(c.w2, bits)
+    ws = workspace_for(c)
+    want = torch.empty((c.T, c.d), dtype=torch.float32, device=DEV)
+    moe.forward_q(c.x, c.w_r, c.b_r, q1, q2, c.T, c.d, c.F, c.E, c.k, bits, want, ws, out_dt=F32)
+    out = torch.full((c.T, c.d), float("nan"), dtype=torch.float32, device=DEV)
+    with moe.GraphCapture(keep=(c.x, c.w_r, c.b_r, q1, q2, out, ws)) as cap:
+        moe.forward_q(c.x, c.w_r, c.b_r, q1, q2, c.T, c.d, c.F, c.E, c.k, bits, out, ws, out_dt=F32,
+                      stream=cap.stream)
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all()  # recording runs nothing
+    g = cap.graph
+    for _ in range(2):
+        g.launch()
+    torch.cuda.synchronize()
+    assert moe.get_device_status(ws)[0] == moe.MOE_OK
+    assert torch.equal(out.view(torch.int32), want.view(torch.int32))
+    c.x.copy_(torch.flip(c.x, dims=[0]))
+    want2 = torch.empty_like(want)
+    moe.forward_q(c.x, c.w_r, c.b_r, q1, q2, c.T, c.d, c.F, c.E, c.k, bits, want2, ws, out_dt=F32)
+    g.launch()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int32), want2.view(torch.int32))
+    g.close()
