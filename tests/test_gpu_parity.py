@@ -278,6 +278,9 @@ FORWARD_CASES = [
     dict(T=77, d=64, F=96, E=2, k=2, dt=F32, path=moe.PATH_AUTO),            # E = k
     dict(T=50, d=64, F=64, E=1, k=1, dt=F32, path=moe.PATH_AUTO),            # a single dense expert
     dict(T=93, d=8, F=8, E=4, k=1, dt=BF16, path=moe.PATH_TENSOR),           # smallest d, F
+    dict(T=4, d=8, F=8, E=8, k=2, dt=BF16, path=moe.PATH_STREAM),            # smallest d, F streamed: boxes
+                                                                               # mostly past the matrix edges
+    dict(T=3, d=64, F=72, E=1, k=1, dt=BF16, path=moe.PATH_STREAM),          # one expert, streamed
     dict(T=40, d=64, F=64, E=1024, k=8, dt=BF16, path=moe.PATH_AUTO),        # largest E and k
     dict(T=2048, d=256, F=512, E=8, k=2, dt=BF16, path=moe.PATH_TENSOR_PAIR),  # 1024 rows/expert: 4 pair tiles
     dict(T=640, d=256, F=512, E=16, k=2, dt=BF16, path=moe.PATH_TENSOR_PAIR),

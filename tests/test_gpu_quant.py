@@ -79,8 +79,9 @@ def q_tolerance(c, ref, w1h, w2h):
                                  dict(T=8, d=512, F=768, E=32, k=2),       # decode batch, 2 rows a pass
                                  dict(T=64, d=256, F=512, E=8, k=2),       # 4 rows a pass, several passes
                                  dict(T=300, d=128, F=192, E=4, k=2),      # many passes over each expert
-                                 dict(T=40, d=256, F=256, E=64, k=2)],     # 2 rows a pass, some experts twice
-                         ids=["t1", "t8", "t64", "t300", "t40_e64"])
+                                 dict(T=40, d=256, F=256, E=64, k=2),      # 2 rows a pass, some experts twice
+                                 dict(T=1, d=64, F=64, E=8, k=2)],         # smallest matrices: one block
+                         ids=["t1", "t8", "t64", "t300", "t40_e64", "t1_tiny"])
 def test_forward_q_matches_oracle(cfg, bits):
     c, q1, q2, w1h, w2h = q_case(bits=bits, **cfg)
     out = torch.empty((c.T, c.d), dtype=torch.float32, device=DEV)
