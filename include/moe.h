@@ -81,7 +81,9 @@ int moe_ffn_path(int T, int k, int E, int N, moe_dtype dt);
 int moe_forward_launches(int T, int d, int F, int E, int k, moe_dtype dt, moe_path path, int router_stats);
 
 /* ---------------------------------------------------------------------------------------------
- * moe_router_topk — router GEMM, softmax and deterministic top-k, fused, one warp per token.
+ * moe_router_topk — router GEMM, softmax and deterministic top-k, fused in one kernel: bf16 layers
+ *   compute a 128-token tile's logits on the tensor cores and give each token to one epilogue
+ *   thread for softmax and top-k; other layers use a CUDA-core kernel.
  *   csdn/6a919c0d §2.2 steps 1-4 (single linear router with one output per expert, softmax,
  *   keep the k most confident experts, weights = their confidences); aicoding/6a320eef §3.2
  *   (h x W_router, W_router is d x E; Softmax; top-2; weights = the p values); csdn/6a919c0d
@@ -161,16 +163,18 @@ int moe_capacity(int T, int k, int E, double cf);
  *   framework owns all device memory through its own pool), or a latency-critical loop that must
  *   not call cudaMalloc, which can block and synchronise the device. The pages have no counterpart
  *   of this call; it exists for such callers only.
- * Same inputs, outputs and results as moe_dispatch (bit for bit). The per-chunk count tables live in
- *   a fixed 1 MiB array inside the library's own device memory, one copy per GPU that loads the
+ * Same inputs, outputs and results as moe_dispatch (bit for bit), by the same two launches. The
+ *   per-chunk count tables (and the count kernel's one-word ticket) live in a fixed array of
+ *   1 MiB + 256 bytes inside the library's own device memory, one copy per GPU that loads the
  *   library, held until the process exits. Limit: ceil(T*k / 256) * E <= 131072 (for example
  *   T*k <= 262144 with E = 128, T*k <= 32768 with E = 1024); larger sizes return
  *   MOE_ERR_INVALID_ARG before anything is launched. Nothing is allocated and nothing is freed.
- * The first call on each device looks up the array's device address (host code cannot use the
- *   array's name as a pointer) and caches it; make that first call before any stream capture.
- * Every call on a device shares the array and leaves its contents behind; each call rewrites all
- *   it reads, so no clearing is needed between calls, but calls whose kernels overlap on the GPU
- *   (e.g. on two streams at once) race on it and must not be issued that way.
+ * Every call looks up the array's device address on the current device (host code cannot use the
+ *   array's name as a pointer); the first lookup on a device may load the library's device code,
+ *   so make the first call on each device before any stream capture.
+ * Every call on a device shares the array and leaves its contents behind. Each call clears the
+ *   ticket (a 4-byte memset on `stream`) and rewrites the tables it reads, but calls whose kernels
+ *   overlap on the GPU (e.g. on two streams at once) race on it: issue them in order on one stream.
  * An index outside [0, E) is dropped (row_of entry -1, offsets[E] < T*k); no status word is kept.
  */
 moe_status moe_dispatch_noalloc(const void* x, const int32_t* topk_idx, const float* topk_gate, int T, int d,

@@ -57,6 +57,9 @@ WORKLOADS = {
     # Profiling-size prefill layer: the prefill layer's per-expert shape (about 128 rows per expert,
     # d=4096, d_ff=8192) with 16 experts (2.1 GB), small enough for a full ncu capture.
     "prefill_e16": Workload("prefill_e16", T=1024, d=4096, F=8192, E=16, k=2, dtype=DTYPE_BF16),
+    # Profiling-size skew-routed layer: the skew layer's per-expert shape and router bias with 16
+    # experts and T=2048 (2.1 GB of weights), small enough for a full ncu capture.
+    "skew_e16": Workload("skew_e16", T=2048, d=4096, F=8192, E=16, k=2, dtype=DTYPE_BF16, skew=True),
     # Skew-routed layer: T=16384, power-law router bias, else as the prefill layer.
     "skew_e128": Workload("skew_e128", T=16384, d=4096, F=8192, E=128, k=2, dtype=DTYPE_BF16,
                           skew=True),

@@ -1,9 +1,10 @@
 // Dispatch: per-expert histogram, exclusive scan, stable permutation and row gather.
 // csdn/6a462027 §4.2 steps 4-5 (group each expert's tokens: "in practice a scatter").
 //
-// moe_dispatch runs count+scan (one kernel, the last CTA scans), scatter and gather as three
-// launches with programmatic dependent launch; moe_dispatch_noalloc runs the four separate
-// kernels below (count, scan, scatter, gather).
+// moe_dispatch and moe_dispatch_noalloc run count+scan (one kernel, the last CTA scans) and
+// scatter+gather as two launches with programmatic dependent launch (launch_dispatch_fast). Inside
+// the layer, with the tensor-core router's per-tile histograms, one launch does it all
+// (launch_dispatch_from_hist).
 //
 // The T*k assignments, in row-major (t, j) order, are cut into chunks of 256
 // (one CTA each).
@@ -23,100 +24,6 @@ namespace {
 
 constexpr int kChunk = kDispatchChunk;
 constexpr int kWarpsPerChunk = kChunk / 32;
-
-__global__ void __launch_bounds__(kChunk)
-dispatch_count_kernel(const int32_t* __restrict__ idx, int A, int E, int32_t* __restrict__ blk_counts,
-                      int* status) {
-  extern __shared__ int hist[];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-  __syncthreads();
-  const int a = blockIdx.x * kChunk + threadIdx.x;
-  if (a < A) {
-    const int e = idx[a];
-    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
-    else record_error(status, MOE_ERR_DEVICE_CHECK, a);
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) blk_counts[(size_t)blockIdx.x * E + e] = hist[e];
-}
-
-__global__ void __launch_bounds__(1024)
-dispatch_scan_kernel(const int32_t* __restrict__ blk_counts, int nb, int E, int32_t* __restrict__ blk_base,
-                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
-  __shared__ int warp_tot[32];
-  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-  int total = 0;
-  if (e < E)
-    for (int b = 0; b < nb; ++b) total += blk_counts[(size_t)b * E + e];
-  int incl = total;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = warp_tot[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += v;
-    }
-    warp_tot[lane] = w;  // inclusive over warps
-  }
-  __syncthreads();
-  const int excl = incl - total + (warp > 0 ? warp_tot[warp - 1] : 0);
-  if (e < E) {
-    counts[e] = total;
-    offsets[e] = excl;
-    if (e == E - 1) offsets[E] = excl + total;
-    int run = excl;
-    for (int b = 0; b < nb; ++b) {
-      blk_base[(size_t)b * E + e] = run;
-      run += blk_counts[(size_t)b * E + e];
-    }
-  }
-}
-
-__global__ void __launch_bounds__(kChunk)
-dispatch_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int A, int k, int E,
-                        const int32_t* __restrict__ blk_base, const int32_t* __restrict__ offsets, int cap,
-                        int32_t* __restrict__ row_of, int32_t* __restrict__ perm_token,
-                        float* __restrict__ row_gate) {
-  griddep_launch_dependents();
-  griddep_wait();
-  extern __shared__ int wcnt[];  // [kWarpsPerChunk][E]
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < kWarpsPerChunk * E; i += kChunk) wcnt[i] = 0;
-  __syncthreads();
-  const int a = blockIdx.x * kChunk + tid;
-  int e = -1;
-  if (a < A) {
-    e = idx[a];
-    if (e < 0 || e >= E) e = -1;
-  }
-  const unsigned peers = __match_any_sync(0xffffffffu, e);
-  const int rank = __popc(peers & ((1u << lane) - 1u));
-  if (e >= 0 && rank == 0) wcnt[warp * E + e] = __popc(peers);
-  __syncthreads();
-  if (a < A) {
-    if (e >= 0) {
-      int pre = 0;
-      for (int w = 0; w < warp; ++w) pre += wcnt[w * E + e];
-      const int row = blk_base[(size_t)blockIdx.x * E + e] + pre + rank;
-      if (cap > 0 && row - offsets[e] >= cap) {
-        row_of[a] = -1;  // past the expert's capacity: dropped
-      } else {
-        row_of[a] = row;
-        perm_token[row] = a / k;
-        row_gate[row] = gate[a];
-      }
-    } else {
-      row_of[a] = -1;
-    }
-  }
-}
 
 // Scatter and gather in one kernel: `split` CTAs per 256-assignment chunk each compute the chunk's
 // stable ranks (cheap, redundant), the first of them writes row_of / perm_token / row_gate, and
@@ -311,27 +218,6 @@ dispatch_from_hist_kernel(const int32_t* __restrict__ idx, const float* __restri
 
 
 
-__global__ void __launch_bounds__(256)
-dispatch_gather_kernel(const int4* __restrict__ x, const int32_t* __restrict__ perm_token,
-                       const int32_t* __restrict__ offsets, int E, int vec_per_row, int4* __restrict__ x_perm) {
-  griddep_launch_dependents();
-  griddep_wait();
-  const int rows = offsets[E];
-  const int lane = threadIdx.x & 31;
-  const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  for (int r = gwarp; r < rows; r += nwarps) {
-    const int4* src = x + (size_t)perm_token[r] * vec_per_row;
-    int4* dst = x_perm + (size_t)r * vec_per_row;
-    int i = lane;
-    for (; i + 96 < vec_per_row; i += 128) {
-      const int4 v0 = __ldg(src + i), v1 = __ldg(src + i + 32), v2 = __ldg(src + i + 64), v3 = __ldg(src + i + 96);
-      dst[i] = v0; dst[i + 32] = v1; dst[i + 64] = v2; dst[i + 96] = v3;
-    }
-    for (; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
-  }
-}
-
 // Histogram of one chunk, and for the CTA that finishes last (an atomic ticket, nobody waits)
 // the scan: counts[e], offsets (exclusive scan over experts) and blk_base[c][e] = offsets[e] +
 // counts of chunks before c. The 256 threads are (expert, chunk group) pairs so the chunk tables
@@ -438,40 +324,6 @@ dispatch_count_scan_kernel(const int32_t* __restrict__ idx, int A, int E, int nb
 
 }  // namespace
 
-cudaError_t launch_dispatch(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
-                            int dt, int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* row_of,
-                            float* row_gate, void* x_perm, int32_t* blk_counts, int32_t* blk_base, int* status,
-                            cudaStream_t s) {
-  const int A = T * k;
-  const int nb = (A + kChunk - 1) / kChunk;
-  if (A == 0) {
-    cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
-    if (err == cudaSuccess) err = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s);
-    return err;
-  }
-  dispatch_count_kernel<<<nb, kChunk, E * sizeof(int), s>>>(idx, A, E, blk_counts, status);
-  dispatch_scan_kernel<<<1, 1024, 0, s>>>(blk_counts, nb, E, blk_base, counts, offsets);
-  const size_t sc_smem = (size_t)kWarpsPerChunk * E * sizeof(int);
-  cudaError_t err = cudaFuncSetAttribute(dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sc_smem);
-  if (err != cudaSuccess) return err;
-  dispatch_scatter_kernel<<<nb, kChunk, sc_smem, s>>>(idx, gate, A, k, E, blk_base, offsets, 0, row_of, perm_token,
-                                                      row_gate);
-  const size_t elem = dt == MOE_DTYPE_BF16 ? 2 : 4;
-  const int vec_per_row = (int)((size_t)d * elem / 16);
-  const int warps_needed = A;
-  int blocks = (warps_needed + 7) / 8;
-  const int max_blocks = device_sm_count() * 8;
-  if (blocks > max_blocks) blocks = max_blocks;
-  dispatch_gather_kernel<<<blocks, 256, 0, s>>>((const int4*)x, perm_token, offsets, E, vec_per_row,
-                                                (int4*)x_perm);
-  return cudaGetLastError();
-}
-
-}  // namespace moe
-
-
-namespace moe {
 
 // Two launches with programmatic dependent launch: count + scan, then scatter + gather.
 cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
@@ -479,9 +331,11 @@ cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float*
                                  int32_t* row_of, float* row_gate, void* x_perm, int32_t* blk_counts,
                                  int32_t* blk_base, int* status, int* done, cudaStream_t s) {
   const int A = T * k;
-  if (A == 0)
-    return launch_dispatch(x, idx, gate, T, d, E, k, dt, counts, offsets, perm_token, row_of, row_gate, x_perm,
-                           blk_counts, blk_base, status, s);
+  if (A == 0) {  // no assignments: every count and offset is zero
+    cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
+    if (err == cudaSuccess) err = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s);
+    return err;
+  }
   const int nb = (A + kChunk - 1) / kChunk;
   const size_t cs_smem = (size_t)(3 * E + 1 + kChunk) * sizeof(int);
   cudaError_t err = launch_pdl(dispatch_count_scan_kernel, dim3(nb), dim3(kChunk), cs_smem, s, idx, A, E, nb, cap,

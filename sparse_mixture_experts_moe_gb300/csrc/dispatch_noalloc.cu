@@ -10,44 +10,22 @@
 // library's own device memory (one copy per GPU, held until the process exits).
 //
 // The array is shared by every call on a device and keeps what the last call left in
-// it. Every call rewrites the parts it reads, so nothing has to be cleared between
-// calls, but two calls whose kernels overlap on the GPU (for example on two streams)
-// race on it: issue them in order on one stream.
-#include <mutex>
-
+// it. Every call clears the one word that must start at zero (the count kernel's ticket)
+// and rewrites the tables it reads, but two calls whose kernels overlap on the GPU (for
+// example on two streams) race on it: issue them in order on one stream.
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace moe {
 namespace {
 
-// 1 MiB: both count tables, [ceil(T*k / 256) x E] int32 each.
-constexpr size_t kNoAllocScratchBytes = 1u << 20;
-constexpr size_t kNoAllocMaxTableInts = kNoAllocScratchBytes / (2 * sizeof(int32_t));
-constexpr int kMaxDevices = 64;
+// 1 MiB of count tables, [ceil(T*k / 256) x E] int32 each, after a 256-byte slot whose first word
+// is the count kernel's ticket (the CTA that finishes last scans and sets it back to zero).
+constexpr size_t kNoAllocTicketBytes = 256;
+constexpr size_t kNoAllocTableBytes = 1u << 20;
+constexpr size_t kNoAllocMaxTableInts = kNoAllocTableBytes / (2 * sizeof(int32_t));
 
-static __device__ __align__(256) int32_t g_dispatch_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
-
-// Device address of g_dispatch_scratch on the current device. The first call on each
-// device looks the address up (host code cannot use the array's name as a device
-// pointer) and caches it; later calls on that device reuse it.
-cudaError_t scratch_address(int32_t** out) {
-  static std::mutex mu;
-  static void* addr[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_dispatch_scratch);
-    if (err != cudaSuccess) return err;
-    addr[dev] = p;
-  }
-  *out = static_cast<int32_t*>(addr[dev]);
-  return cudaSuccess;
-}
+static __device__ __align__(256) int32_t g_dispatch_scratch[(kNoAllocTicketBytes + kNoAllocTableBytes) / sizeof(int32_t)];
 
 }  // namespace
 }  // namespace moe
@@ -69,13 +47,21 @@ extern "C" moe_status moe_dispatch_noalloc(const void* x, const int32_t* topk_id
     return MOE_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0 || (reinterpret_cast<uintptr_t>(x_perm) & 15u) != 0)
     return MOE_ERR_INVALID_ARG;
-  int32_t* scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
-  int32_t* blk_counts = scratch;
-  int32_t* blk_base = scratch + kNoAllocMaxTableInts;
+  // The array's device address on the current device, looked up on every call: host code cannot
+  // use the array's name as a device pointer, and a cached address would go stale after a reset of
+  // the device's context.
+  void* base = nullptr;
+  if (cudaGetSymbolAddress(&base, g_dispatch_scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  int32_t* ticket = static_cast<int32_t*>(base);
+  int32_t* blk_counts = ticket + kNoAllocTicketBytes / sizeof(int32_t);
+  int32_t* blk_base = blk_counts + kNoAllocMaxTableInts;
+  // The ticket must start at zero; the previous call's last CTA left it so, and it is cleared
+  // again here so that no earlier call's state can matter.
+  if (A > 0 && cudaMemsetAsync(ticket, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
   // No status word: an index outside [0, E) is dropped (its row_of entry is -1, offsets[E] < T*k).
-  const cudaError_t err = launch_dispatch(x, topk_idx, topk_gate, T, d, E, k, dt, counts, offsets, perm_token,
-                                          row_of, row_gate, x_perm, blk_counts, blk_base, nullptr,
-                                          (cudaStream_t)stream);
+  const cudaError_t err = launch_dispatch_fast(x, topk_idx, topk_gate, T, d, E, k, dt, 0, counts, offsets,
+                                               perm_token, row_of, row_gate, x_perm, blk_counts, blk_base, nullptr,
+                                               ticket, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -45,14 +45,9 @@ cudaError_t launch_router_topk(const void* x, const void* w_r, const float* b_r,
                                int dt, int flags, const RouterStats& st, int32_t* idx, float* gate, int* status,
                                uint64_t timeout_ns, cudaStream_t s, bool* wrote_hist = nullptr);
 
-// blk_counts / blk_base: [ceil(A / kDispatchChunk), E] int32 scratch each.
-cudaError_t launch_dispatch(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
-                            int dt, int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* row_of,
-                            float* row_gate, void* x_perm, int32_t* blk_counts, int32_t* blk_base, int* status,
-                            cudaStream_t s);
-
-// Same results as launch_dispatch in three launches (count + scan, scatter, gather). `done` is an int
-// that is zero before the call and zero again after it (the workspace header).
+// Dispatch in two launches (count + scan, then scatter + gather). blk_counts / blk_base:
+// [ceil(A / kDispatchChunk), E] int32 scratch each; `done` is an int that is zero before the call and
+// zero again after it (the workspace header); status (nullable) receives out-of-range indices.
 // Scatter + gather from per-chunk histograms already in blk_counts (written by the router for
 // k = 2): every CTA rebuilds totals, offsets and its chunk's bases itself; CTA 0 writes counts and
 // offsets. No count kernel.

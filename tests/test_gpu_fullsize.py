@@ -1,10 +1,12 @@
 """The layer at its full workload sizes, in the launch configuration bench.py times
 (moe_forward, automatic kernel choice), against the fp64 oracle.
 
-Routing indices and per-expert counts are compared for every token (the oracle's
-logits are cheap); outputs are compared on a sample of tokens that the oracle
-evaluates one expert matrix at a time (max relative-to-RMS error 2e-2 on the fp32
-output; the bf16 output must be that fp32 output rounded once).
+Routing indices and per-expert counts are compared for every token, and so are the outputs:
+the oracle evaluates the routed rows one expert at a time (each routed expert's matrices are
+read once), then sums each token's k rows in slot order (max relative-to-RMS error 1e-4 for the
+fp32 layer, 2e-2 for the bf16 layers, on the fp32 output; the bf16 output must be that fp32
+output rounded once). The public dispatch entry is also run at every full size on the oracle's
+routing and compared bit for bit. Outputs sit inside guard bands that must stay untouched.
 """
 import gc
 
@@ -16,22 +18,13 @@ import inputgen as ig
 import oracle
 import sparse_mixture_experts_moe_gb300 as moe
 from inputgen import workloads
-from moe_cases import make_case, rel_rms_err, to_f64
+from moe_cases import Guarded, guarded_workspace, make_case, rel_rms_err, to_f64, torch_dtype
 
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 
-# workload -> number of sampled tokens for the output check (None: all tokens)
-SAMPLES = {
-    "tiny_fp32": None,
-    "e16_bf16": None,
-    "prefill_e128": 12,
-    "skew_e128": 12,
-    "decode_t1": None,
-    "decode_t8": None,
-    "decode_t64": 6,
-}
+FULL = ["tiny_fp32", "e16_bf16", "prefill_e128", "skew_e128", "decode_t1", "decode_t8", "decode_t64"]
 
 
 @pytest.fixture(autouse=True)
@@ -41,40 +34,77 @@ def _free_memory():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("name", list(SAMPLES))
+def oracle_routing(c):
+    logits = oracle.router_logits(c.x64, c.wr64, c.br64)
+    idx = oracle.topk_select(logits, c.k)
+    return idx, oracle.gates_of(oracle.softmax(logits), idx)
+
+
+def oracle_all_tokens(c, ridx, rgate):
+    """out[t] for every token: dispatch, the routed rows of each expert through FFN_e times the gate,
+    and the fixed-order k-way sum (the oracle's step functions, which compose to its forward pass)."""
+    dp = oracle.dispatch(ridx, c.E, rgate)
+    y = oracle.expert_rows_ffn(c.x64[dp["perm_token"]], dp["offsets"], dp["row_gate"], c.w1_host(), c.w2_host())
+    return oracle.combine(y, dp["row_of"])
+
+
+@pytest.mark.parametrize("name", FULL)
 def test_full_size_workload(name):
     w = workloads.get(name)
     c = make_case(T=w.T, d=w.d, F=w.F, E=w.E, k=w.k, dt=w.dtype, bias_scale=workloads.bias_scale(w))
-    ws = torch.empty(moe.workspace_bytes(w.T, w.d, w.F, w.E, w.k, w.dtype), dtype=torch.uint8, device=DEV)
-    moe.workspace_init(ws)
+    ws = guarded_workspace(c)
     idx = torch.empty((w.T, w.k), dtype=torch.int32, device=DEV)
     counts = torch.empty(w.E, dtype=torch.int32, device=DEV)
-    out32 = torch.empty((w.T, w.d), dtype=torch.float32, device=DEV)
-    moe.forward(c.x, c.w_r, c.b_r, c.w1, c.w2, w.T, w.d, w.F, w.E, w.k, w.dtype, out32, ws, topk_idx=idx,
+    out32 = Guarded((w.T, w.d), torch.float32)
+    moe.forward(c.x, c.w_r, c.b_r, c.w1, c.w2, w.T, w.d, w.F, w.E, w.k, w.dtype, out32.t, ws.t, topk_idx=idx,
                 counts=counts, out_dt=ig.DTYPE_F32)
-    out_native = torch.empty((w.T, w.d), dtype=torch.bfloat16 if w.dtype == ig.DTYPE_BF16 else torch.float32,
-                             device=DEV)
-    moe.forward(c.x, c.w_r, c.b_r, c.w1, c.w2, w.T, w.d, w.F, w.E, w.k, w.dtype, out_native, ws)
-    st, detail = moe.get_device_status(ws)
+    out_native = Guarded((w.T, w.d), torch_dtype(w.dtype))
+    moe.forward(c.x, c.w_r, c.b_r, c.w1, c.w2, w.T, w.d, w.F, w.E, w.k, w.dtype, out_native.t, ws.t)
+    st, detail = moe.get_device_status(ws.t)
     assert st == moe.MOE_OK, (moe.status_string(st), detail)
+    assert out32.intact() and out_native.intact() and ws.intact()
 
     # routing of every token, bit-exact
-    logits = oracle.router_logits(c.x64, c.wr64, c.br64)
-    ridx = oracle.topk_select(logits, w.k)
+    ridx, rgate = oracle_routing(c)
     assert np.array_equal(idx.cpu().numpy(), ridx)
     assert np.array_equal(counts.cpu().numpy(), oracle.dispatch(ridx, w.E)["counts"])
 
-    # outputs on sampled tokens
-    n = SAMPLES[name]
-    rng = np.random.default_rng(1234)
-    toks = np.arange(w.T) if n is None or n >= w.T else np.sort(rng.choice(w.T, size=n, replace=False))
-    ref = oracle.forward(c.x64[toks], c.wr64, c.w1_host(), c.w2_host(), w.k, c.br64)
-    assert np.array_equal(ref["idx"], ridx[toks])
+    # outputs of every token
+    ref = oracle_all_tokens(c, ridx, rgate)
     tol = 1e-4 if w.dtype == ig.DTYPE_F32 else 2e-2
-    got32 = to_f64(out32)[toks]
-    assert rel_rms_err(got32, ref["out"]) < tol
+    err = rel_rms_err(to_f64(out32.t), ref)
+    assert err < tol, err
     if w.dtype == ig.DTYPE_BF16:
-        assert torch.equal(out_native.view(torch.int16), out32.to(torch.bfloat16).view(torch.int16))
+        assert torch.equal(out_native.t.view(torch.int16), out32.t.to(torch.bfloat16).view(torch.int16))
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_dispatch(name):
+    """moe_dispatch on the oracle's routing of the full workload: counts, offsets, perm_token, row_of,
+    row_gate and x_perm bit for bit, every output inside untouched guard bands."""
+    w = workloads.get(name)
+    c = make_case(T=w.T, d=w.d, F=8, E=w.E, k=w.k, dt=w.dtype, bias_scale=workloads.bias_scale(w))
+    ridx, rgate = oracle_routing(c)
+    A = c.A
+    g = dict(counts=Guarded(w.E, torch.int32), offsets=Guarded(w.E + 1, torch.int32),
+             perm_token=Guarded(A, torch.int32), row_of=Guarded((w.T, w.k), torch.int32),
+             row_gate=Guarded(A, torch.float32), x_perm=Guarded((A, w.d), torch_dtype(w.dtype)))
+    ws = guarded_workspace(c)
+    ti = torch.from_numpy(ridx.astype(np.int32)).to(DEV)
+    tg = torch.from_numpy(rgate.astype(np.float32)).to(DEV)
+    moe.dispatch(c.x, ti, tg, w.T, w.d, w.E, w.k, w.dtype, g["counts"].t, g["offsets"].t, g["perm_token"].t,
+                 g["row_of"].t, g["row_gate"].t, g["x_perm"].t, ws.t)
+    st, detail = moe.get_device_status(ws.t)
+    assert st == moe.MOE_OK, (moe.status_string(st), detail)
+    for n, b in g.items():
+        assert b.intact(), n
+    assert ws.intact()
+    ref = oracle.dispatch(ridx, w.E, rgate.astype(np.float32))
+    for n in ("counts", "offsets", "perm_token", "row_of"):
+        assert np.array_equal(g[n].t.cpu().numpy(), ref[n]), n
+    assert np.array_equal(g["row_gate"].t.cpu().numpy(), ref["row_gate"].astype(np.float32))
+    perm = torch.from_numpy(ref["perm_token"]).to(DEV)
+    assert torch.equal(g["x_perm"].t, c.x[perm])
 
 
 class OracleQuantised:
@@ -89,34 +119,30 @@ class OracleQuantised:
         return oracle.dequantize_blocks(oracle.quantize_blocks(w, self.bits))
 
 
-# quantised decode at full size: workload -> sampled tokens for the output check (None: all)
-SAMPLES_Q = {"decode_t1": None, "decode_t8": 4}
-
-
 @pytest.mark.parametrize("bits", [4, 8])
-@pytest.mark.parametrize("name", list(SAMPLES_Q))
+@pytest.mark.parametrize("name", ["decode_t1", "decode_t8"])
 def test_full_size_quantised_decode(name, bits):
     """moe_forward_q on the decode workloads' full sizes (d = d_ff = 8192, E = 128), weights quantised
-    on the device, against the oracle run on the oracle's own quantisation of the same weights."""
+    on the device, against the oracle run on the oracle's own quantisation of the same weights, on
+    every token."""
     w = workloads.get(name)
     c = make_case(T=w.T, d=w.d, F=w.F, E=w.E, k=w.k, dt=w.dtype, bias_scale=workloads.bias_scale(w))
     q1, q2 = moe.quantize(c.w1, bits), moe.quantize(c.w2, bits)
-    ws = torch.empty(moe.workspace_bytes(w.T, w.d, w.F, w.E, w.k, w.dtype), dtype=torch.uint8, device=DEV)
-    moe.workspace_init(ws)
+    ws = guarded_workspace(c)
     idx = torch.empty((w.T, w.k), dtype=torch.int32, device=DEV)
-    out32 = torch.empty((w.T, w.d), dtype=torch.float32, device=DEV)
-    moe.forward_q(c.x, c.w_r, c.b_r, q1, q2, w.T, w.d, w.F, w.E, w.k, bits, out32, ws, topk_idx=idx,
+    out32 = Guarded((w.T, w.d), torch.float32)
+    moe.forward_q(c.x, c.w_r, c.b_r, q1, q2, w.T, w.d, w.F, w.E, w.k, bits, out32.t, ws.t, topk_idx=idx,
                   out_dt=ig.DTYPE_F32)
-    out_bf = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=DEV)
-    moe.forward_q(c.x, c.w_r, c.b_r, q1, q2, w.T, w.d, w.F, w.E, w.k, bits, out_bf, ws)
-    st, detail = moe.get_device_status(ws)
+    out_bf = Guarded((w.T, w.d), torch.bfloat16)
+    moe.forward_q(c.x, c.w_r, c.b_r, q1, q2, w.T, w.d, w.F, w.E, w.k, bits, out_bf.t, ws.t)
+    st, detail = moe.get_device_status(ws.t)
     assert st == moe.MOE_OK, (moe.status_string(st), detail)
-    ridx = oracle.topk_select(oracle.router_logits(c.x64, c.wr64, c.br64), w.k)
+    assert out32.intact() and out_bf.intact() and ws.intact()
+    ridx, rgate = oracle_routing(c)
     assert np.array_equal(idx.cpu().numpy(), ridx)
-    n = SAMPLES_Q[name]
-    rng = np.random.default_rng(4321)
-    toks = np.arange(w.T) if n is None or n >= w.T else np.sort(rng.choice(w.T, size=n, replace=False))
-    ref = oracle.forward(c.x64[toks], c.wr64, OracleQuantised(c.w1_host(), bits),
-                         OracleQuantised(c.w2_host(), bits), w.k, c.br64)
-    assert rel_rms_err(to_f64(out32)[toks], ref["out"]) < 2e-2
-    assert torch.equal(out_bf.view(torch.int16), out32.to(torch.bfloat16).view(torch.int16))
+    dp = oracle.dispatch(ridx, c.E, rgate)
+    y = oracle.expert_rows_ffn(c.x64[dp["perm_token"]], dp["offsets"], dp["row_gate"],
+                               OracleQuantised(c.w1_host(), bits), OracleQuantised(c.w2_host(), bits))
+    ref = oracle.combine(y, dp["row_of"])
+    assert rel_rms_err(to_f64(out32.t), ref) < 2e-2
+    assert torch.equal(out_bf.t.view(torch.int16), out32.t.to(torch.bfloat16).view(torch.int16))

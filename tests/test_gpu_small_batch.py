@@ -12,22 +12,12 @@ import torch
 import inputgen as ig
 import oracle
 import sparse_mixture_experts_moe_gb300 as moe
-from moe_cases import make_case, rel_rms_err, to_f64, workspace_for
+from moe_cases import make_case, output_tolerance, rel_rms_err, to_f64, workspace_for
 
 pytestmark = pytest.mark.gpu
 
 BF16 = ig.DTYPE_BF16
 DEV = "cuda"
-
-
-def tolerance(c, ref, cap):
-    """2e-2, or 1.1x the error that rounding h to bf16 alone causes on this shape, plus 2e-3."""
-    dp = oracle.dispatch(ref["idx"], c.E, ref["gate"], cap=cap)
-    rows = int(dp["offsets"][-1])
-    h = oracle.expert_rows_up(c.x64[dp["perm_token"][:rows]], dp["offsets"], c.w1_host())
-    hb = ig.as_f64(ig.f32_to_bf16_bits(h.astype(np.float32)), BF16)
-    y = oracle.expert_rows_down(hb, dp["offsets"], dp["row_gate"], c.w2_host())
-    return max(2e-2, 1.1 * rel_rms_err(oracle.combine(y, dp["row_of"]), ref["out"]) + 2e-3)
 
 
 CASES = [
@@ -70,7 +60,7 @@ def test_forward_small_batch(cfg, renormalise):
         assert np.max(np.abs(gate.cpu().numpy() - ref["gate"])) < 1e-5
         assert np.array_equal(counts.cpu().numpy(),
                               oracle.dispatch(ref["idx"], E, cap=cap if cap else None)["counts"])
-        assert rel_rms_err(to_f64(out), ref["out"]) < tolerance(c, ref, cap if cap else None)
+        assert rel_rms_err(to_f64(out), ref["out"]) < output_tolerance(c, ref, cap if cap else None)[0]
 
 
 def test_small_batch_matches_separate_calls():

@@ -4,10 +4,11 @@ Such callers (a plugin that its host framework hands only input and output buffe
 or a loop that must not call cudaMalloc because it can block and synchronise the
 device) use this entry point; its count tables live in a fixed per-GPU array inside
 the library. These tests call it through the C ABI and check that it returns
-exactly what moe_dispatch returns with a workspace (indices and copies are compared
-bit for bit, as for every dispatch test), on two calls in a row of different sizes
-(the array keeps the first call's contents), and that sizes beyond its fixed array
-are refused before anything runs.
+exactly what moe_dispatch returns with a workspace and what the oracle's dispatch
+returns (indices and copies are compared bit for bit, as for every dispatch test), on
+two calls in a row of different sizes (the array keeps the first call's contents), at
+exactly its size limit, and that sizes beyond its fixed array are refused before
+anything runs.
 
 This file sorts last so that a run stopping at the first failure has run every
 other test first.
@@ -56,21 +57,39 @@ def _dispatch_both(c, idx, gate, torch):
     return ref, got
 
 
+def _check_case(cfg, torch):
+    import oracle
+    from moe_cases import make_case
+    c = make_case(redraw=False, **cfg)
+    logits = oracle.router_logits(c.x64, c.wr64, c.br64)
+    idx = oracle.topk_select(logits, c.k)
+    gate = oracle.gates_of(oracle.softmax(logits), idx)
+    ref, got = _dispatch_both(c, idx, gate, torch)
+    for name in ["counts", "offsets", "perm_token", "row_of", "row_gate"]:
+        assert torch.equal(ref[name], got[name]), name
+    bits = torch.int16 if c.dt == moe.MOE_DTYPE_BF16 else torch.int32
+    assert torch.equal(ref["x_perm"].view(bits), got["x_perm"].view(bits))
+    assert int(got["offsets"][-1]) == c.A
+    # and directly against the oracle's dispatch
+    want = oracle.dispatch(idx, c.E, gate.astype(np.float32))
+    for name in ["counts", "offsets", "perm_token", "row_of"]:
+        assert np.array_equal(got[name].cpu().numpy(), want[name]), name
+    assert np.array_equal(got["row_gate"].cpu().numpy(), want["row_gate"].astype(np.float32))
+    perm = torch.from_numpy(want["perm_token"]).to(c.x.device)
+    assert torch.equal(got["x_perm"].view(bits), c.x[perm].view(bits))
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_dispatch_on_two_calls_in_a_row():
     import torch
-    import oracle
-    from moe_cases import make_case
     # a larger call that fills more of the shared array, then a smaller one that reuses it
     for cfg in [dict(T=3000, d=64, F=64, E=128, k=2, dt=moe.MOE_DTYPE_BF16),
                 dict(T=257, d=40, F=64, E=16, k=3, dt=moe.MOE_DTYPE_F32)]:
-        c = make_case(**cfg)
-        logits = oracle.router_logits(c.x64, c.wr64, c.br64)
-        idx = oracle.topk_select(logits, c.k)
-        gate = oracle.gates_of(oracle.softmax(logits), idx)
-        ref, got = _dispatch_both(c, idx, gate, torch)
-        for name in ["counts", "offsets", "perm_token", "row_of", "row_gate"]:
-            assert torch.equal(ref[name], got[name]), name
-        bits = torch.int16 if c.dt == moe.MOE_DTYPE_BF16 else torch.int32
-        assert torch.equal(ref["x_perm"].view(bits), got["x_perm"].view(bits))
-        assert int(got["offsets"][-1]) == c.A
+        _check_case(cfg, torch)
+
+
+@pytest.mark.gpu
+def test_noalloc_at_its_size_limit():
+    """ceil(T*k/256) * E == 131072 exactly (T*k = 262144, E = 128): the tables fill the whole array."""
+    import torch
+    _check_case(dict(T=131072, d=8, F=8, E=128, k=2, dt=moe.MOE_DTYPE_BF16), torch)
