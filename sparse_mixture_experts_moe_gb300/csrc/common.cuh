@@ -10,8 +10,10 @@
 namespace moe {
 
 // ------------------------------------------------------------------ workspace header
-// The first 256 bytes of every workspace: status[0] = first error code (0 = none),
-// status[1] = its detail value.
+// The first 256 bytes of every workspace (zeroed by moe_workspace_init): status[0] = first error
+// code (0 = none), status[1] = its detail value; [2] the dispatch count kernel's ticket, [3] the
+// router statistics ticket, [4] the pair GEMM's item counter and [5] its count of finished pairs.
+// Every ticket and counter is zero between calls: the CTA that finishes last sets it back.
 constexpr size_t kWsHeaderBytes = 256;
 
 __device__ __forceinline__ void record_error(int* status, int code, int detail) {

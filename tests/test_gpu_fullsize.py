@@ -3,10 +3,13 @@
 
 Routing indices and per-expert counts are compared for every token, and so are the outputs:
 the oracle evaluates the routed rows one expert at a time (each routed expert's matrices are
-read once), then sums each token's k rows in slot order (max relative-to-RMS error 1e-4 for the
-fp32 layer, 2e-2 for the bf16 layers, on the fp32 output; the bf16 output must be that fp32
-output rounded once). The public dispatch entry is also run at every full size on the oracle's
-routing and compared bit for bit. Outputs sit inside guard bands that must stay untouched.
+read once), then sums each token's k rows in slot order. fp32 layer: max relative-to-RMS error
+1e-4. bf16 layers, on the fp32 output: within 1e-2 of the oracle run with h rounded once to bf16
+(the path's one documented intermediate rounding), and within 2e-2 of the exact oracle, or, on
+the workloads where that rounding alone already costs more (listed and pinned below), within
+1.1x its error plus 2e-3; the bf16 output must be the fp32 output rounded once. The public
+dispatch entry is also run at every full size on the oracle's routing and compared bit for bit.
+Outputs sit inside guard bands that must stay untouched.
 """
 import gc
 
@@ -40,12 +43,34 @@ def oracle_routing(c):
     return idx, oracle.gates_of(oracle.softmax(logits), idx)
 
 
+# Emulation bar: the bf16 path against the oracle with h rounded once to bf16, its one documented
+# intermediate rounding. What remains is fp32 accumulation, the GeLU approximation and the rare h
+# element whose fp32 value rounds to the neighbouring bf16 value; a wrong tile or row shows up at
+# O(1) of the output RMS. Measured 0.0045 (prefill_e128).
+EMULATION_TOL = 1e-2
+
+# Workloads on which the stated metric's bar (max |error| / RMS <= 2e-2 on all T*d outputs) is
+# raised: there the one rounding of h to bf16 alone, evaluated by the oracle, already costs more.
+# Their outputs are heavy-tailed (a token with a gate near 0.5 has outputs up to 19x the RMS), and
+# a rounding error proportional to the output lands far above 2e-2 of the RMS. The bar is then
+# 1.1x that rounding's error plus 2e-3, the rule of every smaller case (moe_cases.output_tolerance).
+FULL_SIZE_RAISED = {"e16_bf16", "prefill_e128", "skew_e128"}
+
+
 def oracle_all_tokens(c, ridx, rgate):
-    """out[t] for every token: dispatch, the routed rows of each expert through FFN_e times the gate,
-    and the fixed-order k-way sum (the oracle's step functions, which compose to its forward pass)."""
+    """out[t] for every token, exact, and the same with h rounded once to bf16 (bf16 layers): dispatch,
+    the routed rows of each expert through both projections, the gate, and the fixed-order k-way sum
+    (the oracle's step functions, which compose to its forward pass; each routed expert's matrices are
+    read once per projection)."""
     dp = oracle.dispatch(ridx, c.E, rgate)
-    y = oracle.expert_rows_ffn(c.x64[dp["perm_token"]], dp["offsets"], dp["row_gate"], c.w1_host(), c.w2_host())
-    return oracle.combine(y, dp["row_of"])
+    h = oracle.expert_rows_up(c.x64[dp["perm_token"]], dp["offsets"], c.w1_host())
+    ref = oracle.combine(oracle.expert_rows_down(h, dp["offsets"], dp["row_gate"], c.w2_host()), dp["row_of"])
+    if c.dt != ig.DTYPE_BF16:
+        return ref, None
+    hb = ig.as_f64(ig.f32_to_bf16_bits(h.astype(np.float32)), ig.DTYPE_BF16)
+    del h
+    emul = oracle.combine(oracle.expert_rows_down(hb, dp["offsets"], dp["row_gate"], c.w2_host()), dp["row_of"])
+    return ref, emul
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -70,12 +95,18 @@ def test_full_size_workload(name):
     assert np.array_equal(counts.cpu().numpy(), oracle.dispatch(ridx, w.E)["counts"])
 
     # outputs of every token
-    ref = oracle_all_tokens(c, ridx, rgate)
-    tol = 1e-4 if w.dtype == ig.DTYPE_F32 else 2e-2
-    err = rel_rms_err(to_f64(out32.t), ref)
-    assert err < tol, err
-    if w.dtype == ig.DTYPE_BF16:
-        assert torch.equal(out_native.t.view(torch.int16), out32.t.to(torch.bfloat16).view(torch.int16))
+    ref, emul = oracle_all_tokens(c, ridx, rgate)
+    got = to_f64(out32.t)
+    err = rel_rms_err(got, ref)
+    if w.dtype == ig.DTYPE_F32:
+        assert err < 1e-4, err
+        return
+    assert rel_rms_err(got, emul) < EMULATION_TOL
+    rounding = rel_rms_err(emul, ref)
+    bar = max(2e-2, 1.1 * rounding + 2e-3)
+    assert (bar > 2e-2) == (name in FULL_SIZE_RAISED), (name, rounding)
+    assert err < bar, (err, bar, rounding)
+    assert torch.equal(out_native.t.view(torch.int16), out32.t.to(torch.bfloat16).view(torch.int16))
 
 
 @pytest.mark.parametrize("name", FULL)
