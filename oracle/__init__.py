@@ -12,7 +12,7 @@ routines for the special cases, brute force on tiny inputs). There is no
 """
 from .moe import (  # noqa: F401
     router_logits, softmax, topk_select, gates_of, gates_renormalised, gelu, expert_ffn, forward, dense_forward,
-    dispatch, capacity, kept_assignments, expert_rows_ffn, expert_rows_up, expert_rows_down, combine, routing_stats, quantize_blocks, dequantize_blocks,
+    dispatch, capacity, kept_assignments, reroute_assignments, expert_rows_ffn, expert_rows_up, expert_rows_down, combine, routing_stats, quantize_blocks, dequantize_blocks,
     packed_code_bytes, ambiguous_tokens,
     top_share,
 )

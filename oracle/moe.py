@@ -122,7 +122,7 @@ def expert_ffn(x_rows: np.ndarray, w1_e: np.ndarray, w2_e: np.ndarray) -> np.nda
 
 def forward(x: np.ndarray, w_r: np.ndarray, w1: Union[np.ndarray, Mapping], w2: Union[np.ndarray, Mapping],
             k: int, b_r: Optional[np.ndarray] = None, renormalise: bool = False,
-            cap: Optional[int] = None) -> dict:
+            cap: Optional[int] = None, reroute: Optional[int] = None) -> dict:
     """Forward pass of the layer for the tokens in x.
 
     out[t] = sum_{j=0..k-1} gate[t, j] * FFN_{idx[t, j]}(x[t]), summed in slot order.
@@ -132,7 +132,9 @@ def forward(x: np.ndarray, w_r: np.ndarray, w1: Union[np.ndarray, Mapping], w2: 
     outputs weighted by the probabilities). ``w1[e]`` / ``w2[e]`` may be arrays
     or any mapping that yields expert e's matrices; only routed experts are read.
     With ``renormalise`` the gates are ``gates_renormalised`` instead of the raw probabilities;
-    with a capacity ``cap`` the assignments ``kept_assignments`` drops contribute nothing.
+    with a capacity ``cap`` the assignments ``kept_assignments`` drops contribute nothing, or, with
+    ``reroute = R`` as well, the assignments go where ``reroute_assignments`` sends them within each
+    token's R best experts (raw gates only).
     Returns the output and every routing intermediate.
     """
     x = np.asarray(x, np.float64)
@@ -141,12 +143,20 @@ def forward(x: np.ndarray, w_r: np.ndarray, w1: Union[np.ndarray, Mapping], w2: 
     p = softmax(logits)
     idx = topk_select(logits, k)
     gate = gates_renormalised(logits, idx) if renormalise else gates_of(p, idx)
+    if reroute is not None and cap is not None:
+        if renormalise:
+            raise ValueError("forward: rerouting uses the raw gates")
+        ranked = topk_select(logits, reroute)
+        idx, gate = reroute_assignments(ranked, gates_of(p, ranked), k, w_r.shape[1], cap)
+        cap = None  # every remaining assignment has room
     y = np.zeros((k, T, d), np.float64)
     for j in range(k):
         for e in np.unique(idx[:, j]):
+            if e < 0:
+                continue
             rows = np.nonzero(idx[:, j] == e)[0]
             y[j, rows] = expert_ffn(x[rows], w1[int(e)], w2[int(e)])
-    keep = kept_assignments(idx, w_r.shape[1], cap).astype(np.float64)
+    keep = (kept_assignments(idx, w_r.shape[1], cap) & (idx >= 0)).astype(np.float64)
     out = np.zeros((T, d), np.float64)
     for j in range(k):
         out = out + (keep[:, j] * gate[:, j])[:, None] * y[j]
@@ -200,9 +210,51 @@ def kept_assignments(idx: np.ndarray, E: int, cap: Optional[int]) -> np.ndarray:
     for t in range(T):
         for j in range(k):
             e = idx[t, j]
+            if e < 0:
+                continue
             keep[t, j] = seen[e] < cap
             seen[e] += 1
     return keep
+
+
+def reroute_assignments(rank_idx: np.ndarray, rank_p: np.ndarray, k: int, E: int, cap: int):
+    """Expert capacity with rerouting: (final_idx [T, k], final_gate [T, k]).
+
+    The capacity rule as aicoding/6a320eef §3.2 states it: when the expert the router chose already
+    holds `cap` queued tokens, the token is rerouted to the next-best expert; csdn/6a919c0d §3.2
+    describes the same as a retry that sends a dropped request to the next-best expert. Reading:
+    the T*k assignments queue in row-major (t, j) order; slot j of token t goes to its chosen expert
+    rank_idx[t, j] while that expert has room, and otherwise to the next expert in the token's
+    ranking (rank_idx[t, k:], best first) that has room, each ranking entry being tried at most once
+    per token; with none left the slot is dropped (final_idx -1, gate 0). The gate of a slot is the
+    router probability of the expert that takes it (rank_p at that rank), so a rerouted slot is
+    weighted by that expert's confidence (csdn/6a919c0d §2.2 step 4). rank_idx / rank_p: each token's
+    R highest-ranked experts and their softmax probabilities, best first (R = E: the whole ranking).
+    """
+    rank_idx = np.asarray(rank_idx)
+    rank_p = np.asarray(rank_p, np.float64)
+    T, R = rank_idx.shape
+    if not (1 <= k <= R):
+        raise ValueError("reroute_assignments: need 1 <= k <= R")
+    held = np.zeros(E, np.int64)
+    final_idx = np.full((T, k), -1, np.int64)
+    final_gate = np.zeros((T, k), np.float64)
+    for t in range(T):
+        nxt = k  # the next ranking entry this token may be rerouted to
+        for j in range(k):
+            e = int(rank_idx[t, j])
+            if held[e] < cap:
+                final_idx[t, j], final_gate[t, j] = e, rank_p[t, j]
+                held[e] += 1
+                continue
+            while nxt < R:
+                c = int(rank_idx[t, nxt])
+                nxt += 1
+                if held[c] < cap:
+                    final_idx[t, j], final_gate[t, j] = c, rank_p[t, nxt - 1]
+                    held[c] += 1
+                    break
+    return final_idx, final_gate
 
 
 def dispatch(idx: np.ndarray, E: int, gate: Optional[np.ndarray] = None, cap: Optional[int] = None) -> dict:
@@ -214,11 +266,12 @@ def dispatch(idx: np.ndarray, E: int, gate: Optional[np.ndarray] = None, cap: Op
     perm_token[row] = t and row_gate[row] = gate[t, j] invert that map. This is
     the "scatter" of csdn/6a462027 §4.2 step 5 (group each expert's tokens), done
     as a counting sort. With a capacity, only the kept assignments (``kept_assignments``) get
-    rows; a dropped one has row_of = -1.
+    rows; a dropped one has row_of = -1, and so has an assignment whose index is already negative
+    (dropped by ``reroute_assignments``).
     """
     idx = np.asarray(idx)
     T, k = idx.shape
-    keep = kept_assignments(idx, E, cap)
+    keep = kept_assignments(idx, E, cap) & (idx >= 0)  # a negative index: an assignment already dropped
     counts = np.zeros(E, np.int64)
     for t in range(T):
         for j in range(k):

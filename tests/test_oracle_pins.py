@@ -289,6 +289,96 @@ def check_capacity():
     assert np.max(np.abs(capped - brute)) < 1e-12
 
 
+def check_capacity_reroute():
+    """Rerouting at capacity (aicoding §3.2, csdn/6a919c0d §3.2): a hand-worked case; the special cases that
+    reduce to plain top-k (capacity nobody reaches) and to the drop rule (no candidates beyond the k chosen);
+    for one slot per token and the whole ranking, the serial rule "each token in turn takes its best expert
+    with room" computed from masked logits; for k slots, a brute force that searches the ranking afresh for
+    every rerouted slot; the forward pass equals a per-assignment sum over the final experts."""
+    # hand-worked: 4 tokens, 3 experts, capacity 1, every token ranks 0 > 1 > 2
+    ri = np.array([[0, 1, 2]] * 4)
+    rp = np.array([[0.5, 0.3, 0.2]] * 4)
+    fi, fg = om.reroute_assignments(ri, rp, 1, 3, 1)
+    assert fi.reshape(-1).tolist() == [0, 1, 2, -1]
+    assert np.allclose(fg.reshape(-1), [0.5, 0.3, 0.2, 0.0], rtol=0, atol=0)
+    # k = 2, capacity 1: token 1 wants 1 (held) -> its rank-2 expert 3; wants 0 (held) -> rank-3 expert 2;
+    # token 2 finds every expert held and is dropped
+    ri = np.array([[0, 1, 2, 3], [1, 0, 3, 2], [0, 1, 2, 3]])
+    rp = np.array([[0.4, 0.3, 0.2, 0.1], [0.4, 0.3, 0.2, 0.1], [0.4, 0.3, 0.2, 0.1]])
+    fi, fg = om.reroute_assignments(ri, rp, 2, 4, 1)
+    assert fi.tolist() == [[0, 1], [3, 2], [-1, -1]]
+    assert fg.tolist() == [[0.4, 0.3], [0.2, 0.1], [0.0, 0.0]]
+    rng = np.random.default_rng(21)
+    for trial in range(12):
+        T, E = int(rng.integers(5, 60)), int(rng.integers(2, 9))
+        k = int(rng.integers(1, min(E, 3) + 1))
+        R = int(rng.integers(k, E + 1))
+        cap = int(rng.integers(1, max(2, T * k // E + 2)))
+        l = rng.standard_normal((T, E)) + np.linspace(1.5, -1.5, E)
+        p = om.softmax(l)
+        ri = om.topk_select(l, R)
+        rp = om.gates_of(p, ri)
+        fi, fg = om.reroute_assignments(ri, rp, k, E, cap)
+        counts = np.bincount(fi[fi >= 0], minlength=E)
+        assert np.all(counts <= cap)
+        for t in range(T):
+            got = fi[t][fi[t] >= 0]
+            assert len(set(got.tolist())) == len(got)                 # distinct experts per token
+            assert set(got.tolist()) <= set(ri[t].tolist())           # within its R best
+        # brute force: every slot in (t, j) order takes its own choice if it has room, else the best-ranked
+        # expert among ranks k..R-1 that has room and does not hold this token already
+        held = np.zeros(E, np.int64)
+        bi = np.full((T, k), -1)
+        bg = np.zeros((T, k))
+        for t in range(T):
+            for j in range(k):
+                cands = [j] if held[ri[t, j]] < cap else [r for r in range(k, R)
+                                                           if held[ri[t, r]] < cap and ri[t, r] not in bi[t]]
+                if cands:
+                    r = cands[0]
+                    bi[t, j], bg[t, j] = ri[t, r], rp[t, r]
+                    held[ri[t, r]] += 1
+        assert np.array_equal(fi, bi) and np.array_equal(fg, bg), trial
+        # a capacity nobody reaches: plain top-k with the raw gates
+        fi2, fg2 = om.reroute_assignments(ri, rp, k, E, T * k)
+        assert np.array_equal(fi2, ri[:, :k]) and np.array_equal(fg2, rp[:, :k])
+        # no candidates beyond the k chosen: the drop rule
+        fi3, _ = om.reroute_assignments(ri[:, :k], rp[:, :k], k, E, cap)
+        assert np.array_equal(fi3 >= 0, om.kept_assignments(ri[:, :k], E, cap))
+        # one slot per token and the whole ranking: each token in turn takes its best expert with room
+        if k == 1 and R == E:
+            held = np.zeros(E, np.int64)
+            for t in range(T):
+                masked = np.where(held < cap, l[t], -np.inf)
+                want = int(np.argmax(masked)) if np.isfinite(masked).any() else -1
+                assert fi[t, 0] == want
+                if want >= 0:
+                    held[want] += 1
+    # the forward pass with rerouting: the final experts' outputs weighted by their probabilities
+    x, w_r, w1, w2 = _rand_layer(rng, T=30, d=6, F=8, E=5)
+    b = np.array([1.5, 1.0, 0.0, -0.5, -1.0])
+    res = om.forward(x, w_r, w1, w2, 2, b_r=b, cap=8, reroute=5)
+    lg = om.router_logits(x, w_r, b)
+    ranked = np.argsort(-lg, axis=1, kind="stable")
+    brute = np.zeros_like(res["out"])
+    held = {}
+    for t in range(30):
+        mine = []
+        for j in range(2):
+            e = int(ranked[t, j])
+            if held.get(e, 0) >= 8:
+                e = next((int(c) for c in ranked[t, 2:] if held.get(int(c), 0) < 8 and int(c) not in mine), -1)
+            if e >= 0:
+                held[e] = held.get(e, 0) + 1
+                mine.append(e)
+                brute[t] += om.softmax(lg)[t, e] * om.expert_ffn(x[t:t + 1], w1[e], w2[e])[0]
+    assert np.max(np.abs(res["out"] - brute)) < 1e-12
+    assert (res["idx"] != om.topk_select(lg, 2)).any()  # something was rerouted
+    dp = om.dispatch(res["idx"], 5, res["gate"])
+    assert np.array_equal(dp["row_of"] >= 0, res["idx"] >= 0)
+    assert dp["offsets"][-1] == (res["idx"] >= 0).sum()
+
+
 def check_routing_stats():
     """Routing statistics: soft load = column means of scipy's softmax; equal logits give entropy ln E
     (closed form) and equal soft loads; entropy matches scipy.stats.entropy per token; a batch whose
@@ -380,7 +470,8 @@ PINS = [check_worked_example, check_router_closed_form, check_softmax_library, c
         check_gelu_closed_form, check_single_expert_is_mlp, check_k_equals_E_is_softmax_mixture,
         check_routed_equals_dense_bruteforce, check_routing_invariants, check_activation_fraction,
         check_dispatch_stable_sort, check_steps_compose_to_forward, check_ambiguous_tokens,
-        check_renormalised_gates, check_capacity, check_routing_stats, check_block_quantizer]
+        check_renormalised_gates, check_capacity, check_capacity_reroute, check_routing_stats,
+        check_block_quantizer]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -465,8 +556,8 @@ def _mut_combine_first_slot_twice(y_perm, row_of):
     return _ORIG_COMBINE(y_perm, row_of)
 
 
-def _mut_forward_drops_last_slot(x, w_r, w1, w2, k, b_r=None, renormalise=False, cap=None):
-    res = _ORIG_FORWARD(x, w_r, w1, w2, k, b_r, renormalise, cap)
+def _mut_forward_drops_last_slot(x, w_r, w1, w2, k, b_r=None, renormalise=False, cap=None, reroute=None):
+    res = _ORIG_FORWARD(x, w_r, w1, w2, k, b_r, renormalise, cap, reroute)
     res = dict(res)
     res["out"] = res["out"] - res["gate"][:, -1:] * res["y"][-1] if k > 1 else res["out"]
     return res
@@ -518,6 +609,34 @@ def _mut_quant_levels(w, bits):
     return q
 
 
+def _mut_reroute(change):
+    def fn(rank_idx, rank_p, k, E, cap):
+        rank_idx = np.asarray(rank_idx)
+        T, R = rank_idx.shape
+        held = np.zeros(E, np.int64)
+        fi, fg = np.full((T, k), -1), np.zeros((T, k))
+        for t in range(T):
+            nxt = k
+            for j in range(k):
+                e = int(rank_idx[t, j])
+                if held[e] < cap:
+                    fi[t, j], fg[t, j] = e, rank_p[t, j]
+                    held[e] += 1
+                    continue
+                if change == "restart":
+                    nxt = k  # the search starts over for every slot: a token may take an expert twice
+                while nxt < R:
+                    c = int(rank_idx[t, nxt])
+                    nxt += 1
+                    if change == "no_room_check" or held[c] < cap:
+                        fi[t, j] = c
+                        fg[t, j] = rank_p[t, j] if change == "original_gate" else rank_p[t, nxt - 1]
+                        held[c] += 1
+                        break
+        return fi, fg
+    return fn
+
+
 _ORIG_DISPATCH = om.dispatch
 _ORIG_TOPK = om.topk_select
 _ORIG_KEPT = om.kept_assignments
@@ -544,6 +663,9 @@ MUTANTS = {
     "stats_soft_load_over_assignments": ("routing_stats", _mut_stats("soft_over_assignments")),
     "stats_balance_of_soft_load": ("routing_stats", _mut_stats("balance_of_soft_load")),
     "stats_hard_load_over_tokens": ("routing_stats", _mut_stats("hard_over_tokens")),
+    "reroute_without_room_check": ("reroute_assignments", _mut_reroute("no_room_check")),
+    "reroute_keeps_original_gate": ("reroute_assignments", _mut_reroute("original_gate")),
+    "reroute_search_restarts": ("reroute_assignments", _mut_reroute("restart")),
     "dequant_drops_min": ("dequantize_blocks", _mut_dequant_drops_min),
     "quant_floor": ("quantize_blocks", _mut_quant_floor),
     "quant_2^bits_levels": ("quantize_blocks", _mut_quant_levels),
@@ -565,6 +687,6 @@ def test_planted_mistakes(name, monkeypatch):
 
 def test_package_exports():
     for name in ["router_logits", "softmax", "topk_select", "gates_of", "gelu", "expert_ffn", "forward",
-                 "dense_forward", "gates_renormalised", "dispatch", "capacity", "kept_assignments", "expert_rows_ffn", "expert_rows_up", "expert_rows_down", "combine", "routing_stats", "quantize_blocks", "dequantize_blocks",
+                 "dense_forward", "gates_renormalised", "dispatch", "capacity", "kept_assignments", "reroute_assignments", "expert_rows_ffn", "expert_rows_up", "expert_rows_down", "combine", "routing_stats", "quantize_blocks", "dequantize_blocks",
                  "packed_code_bytes", "ambiguous_tokens", "top_share"]:
         assert callable(getattr(oracle, name))
