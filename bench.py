@@ -60,6 +60,10 @@ def parse_args():
                    help="0: the bf16 layer; 4 / 8: expert weights block-quantised to INT4 / INT8 (bf16 layers)")
     p.add_argument("--ffn-path", default="auto", choices=["auto", "tensor", "stream", "simt", "pair", "tensor_t"],
                    help="expert FFN kernel family (moe_path); auto = the library's own choice")
+    p.add_argument("--also", default=None,
+                   help="comma-separated extra workloads measured after the headline (graph replays, 20 steps) "
+                        "and reported under 'other_workloads'; default: prefill_e128,decode_t64 when the "
+                        "headline is the default workload, none otherwise; '' for none")
     p.add_argument("--launch", default="graph", choices=["graph", "direct"],
                    help="graph: replay a CUDA graph of the layer per step; direct: one C ABI call per kernel")
     return p.parse_args()
@@ -247,9 +251,13 @@ def oracle_sample(w, x, w_r, b_r, w1, w2, target_s, max_tokens=None, repeat=True
     import oracle
     cores = len(os.sched_getaffinity(0))
     max_tokens = w.T if max_tokens is None else min(max_tokens, w.T)
-    # keep the fp64 copies of the touched experts within ~6 GB of host memory
+    # keep the fp64 copies of the touched experts within a sixth of the host's memory (at most 24 GB)
     per_expert = 2 * w.d * w.F * 8
-    expert_budget = max(2, int(6e9 // per_expert))
+    try:
+        host_bytes = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
+    except (ValueError, OSError, AttributeError):
+        host_bytes = 36e9
+    expert_budget = max(2, int(min(24e9, host_bytes / 6) // per_expert))
     n = min(max_tokens, 64 if w.E * per_expert > 6e9 else 256)
     h = host_copy(w, x, w_r, b_r, w1, w2, max_tokens)
 
@@ -279,13 +287,72 @@ def oracle_sample(w, x, w_r, b_r, w1, w2, target_s, max_tokens=None, repeat=True
             break
         n, dt = n2, dt2
     passes = 1
-    if repeat and n == max_tokens and dt < target_s / 4:  # the whole batch is short: repeat it
-        passes = max(2, min(64, int(target_s / 2 / max(dt, 1e-3))))
+    if repeat and dt < target_s / 4:  # the sample is short (the whole batch, or all the experts the host
+        passes = max(2, min(256, int(target_s / 2 / max(dt, 1e-3))))  # holds): repeat it
         dt = run(n, passes)
     return n * passes / dt, n, dt, cores, passes
 
 
 # ----------------------------------------------------------------------------- our arm
+
+def dominant_roofline(w, kern_ms, touched, fpath, qbits, peaks, peak_src):
+    """Roofline of the slower expert GEMM: algorithmic bytes (weight streaming) or FLOPs (tensor-core
+    GEMMs) per launch over its measured launch time, against the measured peak."""
+    import sparse_mixture_experts_moe_gb300 as moe
+    T, d, F, E, k, dt = w.T, w.d, w.F, w.E, w.k, w.dtype
+    A = T * k
+    eb = 2 if dt == 1 else 4
+    dom = max(["expert_up", "expert_down"], key=lambda n: kern_ms[n])
+    # the kernel family each GEMM ran (AUTO resolves per GEMM: moe_ffn_path)
+    run_path = {n: (fpath if fpath != moe.PATH_AUTO else moe.ffn_path(T, k, E, F if n == "expert_up" else d, dt))
+                for n in ("expert_up", "expert_down")}
+    stream_path = run_path[dom] == moe.PATH_STREAM
+    if qbits:
+        # quantised weight streaming: codes + (scale, min) of the touched experts + rows in and out
+        K_, N_ = (d, F) if dom == "expert_up" else (F, d)
+        wbytes = K_ * N_ * qbits // 8 + (K_ // 64) * (N_ // 64) * 8
+        alg_bytes = touched * wbytes + A * K_ * eb + A * N_ * (eb if dom == "expert_up" else 4)
+        achieved = alg_bytes / (kern_ms[dom] / 1e3) / 1e9
+        roof = {"kernel": f"ffn_stream_q_kernel<{qbits}> ({dom})", "bound": "hbm", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": stored_traffic(f"ffn_stream_q_kernel<{qbits}, {1 if dom == 'expert_up' else 2}>",
+                                          w.name, QUANT_SOURCES),
+                "alg_bytes_per_launch": alg_bytes, "ms_per_launch": kern_ms[dom],
+                "peak_source": f"{peak_src} hbm_gbs"}
+    elif stream_path:
+        # weight streaming: bytes = touched experts' matrix + the routed rows in and out
+        if dom == "expert_up":
+            alg_bytes = touched * d * F * eb + A * d * eb + A * F * eb
+        else:
+            alg_bytes = touched * F * d * eb + A * F * eb + A * d * eb
+        achieved = alg_bytes / (kern_ms[dom] / 1e3) / 1e9
+        roof = {"kernel": f"ffn_stream_tma_kernel ({dom})", "bound": "hbm", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": stored_traffic(f"ffn_stream_tma_kernel<{1 if dom == 'expert_up' else 2}>", w.name,
+                                          STREAM_SOURCES),
+                "alg_bytes_per_launch": alg_bytes, "ms_per_launch": kern_ms[dom],
+                "peak_source": f"{peak_src} hbm_gbs"}
+    else:
+        alg_flops = 2.0 * A * d * F
+        achieved = alg_flops / (kern_ms[dom] / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        kname = {moe.PATH_TENSOR_PAIR: "ffn_tc2_kernel", moe.PATH_TENSOR_T: "ffn_tct_kernel"}.get(run_path[dom],
+                                                                                               "ffn_tc_kernel")
+        # attainable: min(peak, arithmetic intensity x HBM bandwidth), the intensity over the bytes the
+        # GEMM must move (touched experts' weights, rows in, rows out)
+        K_, N_ = (d, F) if dom == "expert_up" else (F, d)
+        must_bytes = touched * K_ * N_ * eb + A * K_ * eb + A * N_ * (eb if dom == "expert_up" else 4)
+        attainable = min(peak, alg_flops / must_bytes * peaks["hbm_gbs"] / 1e3)
+        roof = {"kernel": f"{kname} ({dom})", "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "attainable": attainable,
+                "frac_of_attainable": achieved / attainable,
+                "traffic": stored_traffic(f"{kname}<{1 if dom == 'expert_up' else 2}>", w.name,
+                                          TCT_SOURCES if kname == "ffn_tct_kernel" else TC_SOURCES),
+                "alg_flops_per_launch": alg_flops, "ms_per_launch": kern_ms[dom],
+                "peak_source": f"{peak_src} bf16_tflops (burst: the kernel runs in a short step)"}
+    return roof
+
+
 
 def run_ours(args, w, rank, world, device):
     import numpy as np
@@ -495,49 +562,7 @@ def run_ours(args, w, rank, world, device):
 
     # --- roofline of the dominant kernel
     peaks, peak_src = load_peaks()
-    eb = 2 if dt == 1 else 4
-    dom = max(["expert_up", "expert_down"], key=lambda n: kern_ms[n])
-    # the kernel family each GEMM ran (AUTO resolves per GEMM: moe_ffn_path)
-    run_path = {n: (fpath if fpath != moe.PATH_AUTO else moe.ffn_path(T, k, E, F if n == "expert_up" else d, dt))
-                for n in ("expert_up", "expert_down")}
-    stream_path = run_path[dom] == moe.PATH_STREAM
-    if qbits:
-        # quantised weight streaming: codes + (scale, min) of the touched experts + rows in and out
-        K_, N_ = (d, F) if dom == "expert_up" else (F, d)
-        wbytes = K_ * N_ * qbits // 8 + (K_ // 64) * (N_ // 64) * 8
-        alg_bytes = touched * wbytes + A * K_ * eb + A * N_ * (eb if dom == "expert_up" else 4)
-        achieved = alg_bytes / (kern_ms[dom] / 1e3) / 1e9
-        roof = {"kernel": f"ffn_stream_q_kernel<{qbits}> ({dom})", "bound": "hbm", "achieved": achieved,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "traffic": stored_traffic(f"ffn_stream_q_kernel<{qbits}, {1 if dom == 'expert_up' else 2}>",
-                                          w.name, QUANT_SOURCES),
-                "alg_bytes_per_launch": alg_bytes, "ms_per_launch": kern_ms[dom],
-                "peak_source": f"{peak_src} hbm_gbs"}
-    elif stream_path:
-        # weight streaming: bytes = touched experts' matrix + the routed rows in and out
-        if dom == "expert_up":
-            alg_bytes = touched * d * F * eb + A * d * eb + A * F * eb
-        else:
-            alg_bytes = touched * F * d * eb + A * F * eb + A * d * eb
-        achieved = alg_bytes / (kern_ms[dom] / 1e3) / 1e9
-        roof = {"kernel": f"ffn_stream_tma_kernel ({dom})", "bound": "hbm", "achieved": achieved,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "traffic": stored_traffic(f"ffn_stream_tma_kernel<{1 if dom == 'expert_up' else 2}>", w.name,
-                                          STREAM_SOURCES),
-                "alg_bytes_per_launch": alg_bytes, "ms_per_launch": kern_ms[dom],
-                "peak_source": f"{peak_src} hbm_gbs"}
-    else:
-        alg_flops = 2.0 * A * d * F
-        achieved = alg_flops / (kern_ms[dom] / 1e3) / 1e12
-        peak = peaks["bf16_tflops"]
-        kname = {moe.PATH_TENSOR_PAIR: "ffn_tc2_kernel", moe.PATH_TENSOR_T: "ffn_tct_kernel"}.get(run_path[dom],
-                                                                                               "ffn_tc_kernel")
-        roof = {"kernel": f"{kname} ({dom})", "bound": "tensor", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": stored_traffic(f"{kname}<{1 if dom == 'expert_up' else 2}>", w.name,
-                                          TCT_SOURCES if kname == "ffn_tct_kernel" else TC_SOURCES),
-                "alg_flops_per_launch": alg_flops, "ms_per_launch": kern_ms[dom],
-                "peak_source": f"{peak_src} bf16_tflops (burst: the kernel runs in a short step)"}
+    roof = dominant_roofline(w, kern_ms, touched, fpath, qbits, peaks, peak_src)
 
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -564,10 +589,76 @@ def run_ours(args, w, rank, world, device):
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not qbits:
         v, n, secs, cores, passes = oracle_sample(w, x, w_r, b_r, w1, w2, args.cpu_seconds)
         result["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                  "sample": (f"the batch's {T} tokens, fp64 oracle forward, {passes} passes"
-                                             if passes > 1 else f"first {n} of the batch's {T} tokens, fp64 oracle "
-                                             "forward") + f", {secs:.2f} s"}
+                                  "sample": (f"first {n} of the batch's {T} tokens (as many as the host holds "
+                                             "the touched experts of, in fp64)" if n < T else
+                                             f"the batch's {T} tokens") + ", fp64 oracle forward" +
+                                            (f", {passes} passes" if passes > 1 else "") + f", {secs:.2f} s"}
     return result
+
+
+def measure_extra(name, device, steps=20, warmup=3, reps=10):
+    """One more workload beside the headline: device-timed graph replays of the layer (inputs resident,
+    weights larger than L2), tokens/s, and the roofline of its slower expert GEMM."""
+    import torch
+    import sparse_mixture_experts_moe_gb300 as moe
+    from inputgen import workloads
+    w = workloads.get(name)
+    x, w_r, b_r, w1, w2 = make_inputs(w, device)
+    T, d, F, E, k, dt = w.T, w.d, w.F, w.E, w.k, w.dtype
+    A = T * k
+    out = torch.empty_like(x)
+    ws = torch.empty(moe.workspace_bytes(T, d, F, E, k, dt), dtype=torch.uint8, device=device)
+    moe.workspace_init(ws)
+    stream = torch.cuda.current_stream()
+    with moe.GraphCapture(keep=(x, w_r, b_r, w1, w2, out, ws)) as cap:
+        moe.forward(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws, stream=cap.stream)
+    for _ in range(warmup):
+        cap.graph.launch(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        cap.graph.launch(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    idx = torch.empty((T, k), dtype=torch.int32, device=device)
+    gate = torch.empty((T, k), dtype=torch.float32, device=device)
+    counts = torch.empty(E, dtype=torch.int32, device=device)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=device)
+    perm = torch.empty(A, dtype=torch.int32, device=device)
+    row_of = torch.empty((T, k), dtype=torch.int32, device=device)
+    row_gate = torch.empty(A, dtype=torch.float32, device=device)
+    x_perm = torch.empty((A, d), dtype=x.dtype, device=device)
+    h = torch.empty((A, F), dtype=x.dtype, device=device)
+    y_perm = torch.empty((A, d), dtype=torch.float32, device=device)
+    moe.router_topk(x, w_r, b_r, T, d, E, k, dt, idx, gate)
+    moe.dispatch(x, idx, gate, T, d, E, k, dt, counts, offsets, perm, row_of, row_gate, x_perm, ws)
+    kern_ms = {}
+    for name_, fn in [("expert_up", lambda: moe.expert_up(x_perm, w1, offsets, T, d, F, E, k, dt, h, ws)),
+                      ("expert_down", lambda: moe.expert_down(h, w2, offsets, row_gate, T, d, F, E, k, dt, y_perm,
+                                                              ws))]:
+        fn()
+        torch.cuda.synchronize()
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream)
+        for _ in range(reps):
+            fn()
+        k1.record(stream)
+        torch.cuda.synchronize()
+        kern_ms[name_] = k0.elapsed_time(k1) / reps
+    st, detail = moe.get_device_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status ({name}): {moe.status_string(st)} ({detail})")
+    touched = int((counts > 0).sum().item())
+    peaks, peak_src = load_peaks()
+    roof = dominant_roofline(w, kern_ms, touched, moe.PATH_AUTO, 0, peaks, peak_src)
+    res = {"workload": workload_config(w)["workload"], "value": T / (ms / 1e3), "unit": "tokens/s",
+           "ms_per_step": ms, "steps": steps, "warmup": warmup, "kernel_ms": kern_ms, "experts_touched": touched,
+           "roofline": roof}
+    del x, w_r, w1, w2, ws, out, x_perm, h, y_perm
+    torch.cuda.empty_cache()
+    return res
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -650,6 +741,14 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     res = run_ours(args, w, rank, world, device)
+    also = args.also if args.also is not None else (
+        "prefill_e128,decode_t64" if args.workload == DEFAULT_WORKLOAD and world == 1 else "")
+    extra = [n for n in also.split(",") if n]
+    if extra:
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        res["other_workloads"] = {n: measure_extra(n, device) for n in extra}
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

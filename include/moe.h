@@ -106,6 +106,13 @@ moe_status moe_router_topk(const void* x, const void* w_r, const float* b_r, int
  *   sum_i exp(l_i - m) over the chosen i (hotelren/2927663 §4.3, top-k on the logits, then a
  *   softmax of the selected values); the gates of a token sum to one. */
 enum { MOE_GATES_RENORMALISE = 1 };
+/* MOE_CAPACITY_REROUTE (moe_forward_ex, moe_forward_q only; needs capacity > 0, the raw gates and no
+ *   router_stats): an assignment whose expert already holds `capacity` rows is rerouted as
+ *   moe_dispatch_reroute does, within each token's min(E, 8) best experts, instead of dropped. The
+ *   topk_idx / topk_gate outputs then hold the expert that took each slot (-1 when dropped) and its
+ *   softmax probability; the layer launches the router (for the token's ranking), the rerouting
+ *   kernel and the two-kernel dispatch in place of its usual routing launches. */
+enum { MOE_CAPACITY_REROUTE = 2 };
 moe_status moe_router_topk_ex(const void* x, const void* w_r, const float* b_r, int T, int d, int E, int k,
                               moe_dtype dt, int flags, int32_t* topk_idx, float* topk_gate, void* stream);
 
@@ -156,6 +163,31 @@ moe_status moe_dispatch_ex(const void* x, const int32_t* topk_idx, const float* 
                            int32_t* perm_token, int32_t* row_of, float* row_gate, void* x_perm, void* workspace,
                            size_t ws_bytes, void* stream);
 int moe_capacity(int T, int k, int E, double cf);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_dispatch_reroute — dispatch with an expert capacity that reroutes instead of dropping.
+ *   aicoding/6a320eef §3.2: when the chosen expert's queue is already at capacity, the token is
+ *   rerouted to the next-best expert; csdn/6a919c0d §3.2: a retry sends a dropped request to the
+ *   next-best expert.
+ * The T*k assignments queue in row-major (t, j) order. Slot j of token t asks for rank_idx[t, j];
+ *   if that expert already holds `capacity` assignments, the slot takes the next entry of the token's
+ *   ranking rank_idx[t, k], rank_idx[t, k+1], ... (each entry tried at most once per token) whose
+ *   expert has room, and with none left it is dropped. The slot's gate is rank_gate at the rank that
+ *   took it (the probability of that expert).
+ * In:  x [T, d] (dt), rank_idx [T, R] int32 and rank_gate [T, R] fp32: each token's R best experts,
+ *      best first, distinct (moe_router_topk with k = R gives them); k <= R <= E; capacity >= 1.
+ * Out: final_idx [T, k] int32 (the expert that took each slot, -1 if dropped), final_gate [T, k]
+ *      fp32 (0 if dropped), then counts, offsets, perm_token, row_of, row_gate, x_perm exactly as
+ *      moe_dispatch does for final_idx / final_gate (a dropped slot has row_of -1 and no row; rows
+ *      within an expert keep the (t, j) order; offsets[E] = the rows placed).
+ * Workspace: status word, the dispatch ticket and the per-chunk count tables (moe_workspace_bytes).
+ * One warp places the assignments (a single CTA); then two launches as moe_dispatch. An index outside
+ *   [0, E) in the first k columns is recorded (MOE_ERR_DEVICE_CHECK, detail = assignment) and dropped.
+ */
+moe_status moe_dispatch_reroute(const void* x, const int32_t* rank_idx, const float* rank_gate, int T, int d, int E,
+                                int k, int R, moe_dtype dt, int capacity, int32_t* final_idx, float* final_gate,
+                                int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* row_of,
+                                float* row_gate, void* x_perm, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * moe_dispatch_noalloc — moe_dispatch without a workspace, for callers that cannot provide device
@@ -239,9 +271,10 @@ moe_status moe_combine(const void* y_perm, const int32_t* row_of, int T, int d, 
  * Out: out [T, d] (dt), and optional copies of the routing (NULL: kept in the workspace only):
  *      topk_idx [T, k], topk_gate [T, k], counts [E].
  * moe_forward_ex also takes: the output's element type `out_dt` (e.g. fp32 output of a bf16
- *      layer), the FFN kernel family `path`, router `flags` (MOE_GATES_RENORMALISE), an expert
- *      `capacity` (as in moe_dispatch_ex; 0 = no limit) and `router_stats` (NULL, or
- *      MOE_ROUTER_STATS_LEN(E) floats as in moe_router_topk_stats).
+ *      layer), the FFN kernel family `path`, `flags` (MOE_GATES_RENORMALISE, MOE_CAPACITY_REROUTE),
+ *      an expert `capacity` (as in moe_dispatch_ex, dropping, or rerouting with
+ *      MOE_CAPACITY_REROUTE; 0 = no limit) and `router_stats` (NULL, or MOE_ROUTER_STATS_LEN(E)
+ *      floats as in moe_router_topk_stats).
  * Kernels (same results as the separate calls; moe_forward_launches gives the count): with top-2 and
  *      the tensor-core router, the router also writes each 128-token tile's expert histogram and the
  *      dispatch is one launch; for at most 8 bf16 tokens with weight-streaming GEMMs (E % 8 == 0, no

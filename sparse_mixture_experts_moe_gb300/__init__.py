@@ -15,11 +15,11 @@ from typing import Optional
 from . import _lib
 from ._lib import (  # noqa: F401
     MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK, MOE_ERR_DEVICE_TIMEOUT,
-    GATES_RENORMALISE, MOE_DTYPE_F32, MOE_DTYPE_BF16, PATH_AUTO, PATH_TENSOR, PATH_STREAM, PATH_SIMT, PATH_TENSOR_PAIR, PATH_TENSOR_T,
+    GATES_RENORMALISE, CAPACITY_REROUTE, MOE_DTYPE_F32, MOE_DTYPE_BF16, PATH_AUTO, PATH_TENSOR, PATH_STREAM, PATH_SIMT, PATH_TENSOR_PAIR, PATH_TENSOR_T,
     MoeError,
     ForwardGraph, GraphCapture, ffn_path, forward_launches, CapturedGraph, qweight_bytes, qscale_bytes,
     quantize_weights, quantize,
-    expert_up_q, expert_down_q, forward_q, router_topk, router_topk_stats, router_stats_len, dispatch, dispatch_noalloc, capacity, expert_up, expert_down, grouped_ffn, combine, forward, workspace_bytes, workspace_init,
+    expert_up_q, expert_down_q, forward_q, router_topk, router_topk_stats, router_stats_len, dispatch, dispatch_noalloc, dispatch_reroute, capacity, expert_up, expert_down, grouped_ffn, combine, forward, workspace_bytes, workspace_init,
     get_device_status, status_string, selftest_wait_timeout, lib,
 )
 

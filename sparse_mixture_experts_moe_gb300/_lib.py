@@ -25,6 +25,7 @@ MOE_DTYPE_BF16 = 1
 
 PATH_AUTO, PATH_TENSOR, PATH_STREAM, PATH_SIMT, PATH_TENSOR_PAIR, PATH_TENSOR_T = 0, 1, 2, 3, 4, 5
 GATES_RENORMALISE = 1
+CAPACITY_REROUTE = 2
 
 _p = ctypes.c_void_p
 _i = ctypes.c_int
@@ -40,6 +41,7 @@ SIGNATURES = {
     "moe_ffn_path": [_i, _i, _i, _i, _i],
     "moe_forward_launches": [_i, _i, _i, _i, _i, _i, _i, _i],
     "moe_dispatch_noalloc": [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p],
+    "moe_dispatch_reroute": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p],
     "moe_expert_up": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
     "moe_expert_up_ex": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
     "moe_expert_down": [_p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p, _sz, _p],
@@ -197,6 +199,21 @@ def dispatch(x, topk_idx, topk_gate, T, d, E, k, dt, counts, offsets, perm_token
     return _check(rc, "moe_dispatch") if check else rc
 
 
+def dispatch_reroute(x, rank_idx, rank_gate, T, d, E, k, R, dt, capacity, final_idx, final_gate, counts, offsets,
+                     perm_token, row_of, row_gate, x_perm, ws, stream=None, check=True):
+    """moe_dispatch_reroute: an assignment that meets a full expert takes the next entry of its token's
+    ranking rank_idx[t, k:] with room, or is dropped (final_idx -1)."""
+    rc = lib().moe_dispatch_reroute(_ptr(x), _ptr(rank_idx), _ptr(rank_gate), T, d, E, k, R, dt, int(capacity),
+                                    _ptr(final_idx), _ptr(final_gate), _ptr(counts), _ptr(offsets), _ptr(perm_token),
+                                    _ptr(row_of), _ptr(row_gate), _ptr(x_perm), _ptr(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream))
+    return _check(rc, "moe_dispatch_reroute") if check else rc
+
+
+def _flags(renormalise, reroute):
+    return (GATES_RENORMALISE if renormalise else 0) | (CAPACITY_REROUTE if reroute else 0)
+
+
 def dispatch_noalloc(x, topk_idx, topk_gate, T, d, E, k, dt, counts, offsets, perm_token, row_of, row_gate,
                      x_perm, stream=None, check=True):
     """moe_dispatch without a workspace: the count tables live in the library's fixed per-GPU array."""
@@ -231,12 +248,14 @@ def combine(y_perm, row_of, T, d, k, dt, out, stream=None, check=True):
 
 
 def forward(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws, topk_idx=None, topk_gate=None, counts=None,
-            path=PATH_AUTO, out_dt=None, renormalise=False, capacity=0, router_stats=None, stream=None, check=True):
+            path=PATH_AUTO, out_dt=None, renormalise=False, capacity=0, router_stats=None, stream=None, check=True,
+            reroute=False):
     """out_dt: element type of `out` (default: dt); renormalise: GATES_RENORMALISE; capacity: as dispatch;
+    reroute: CAPACITY_REROUTE (assignments past capacity go to the token's next-best expert with room);
     router_stats: None or a float32 device tensor of router_stats_len(E) (as router_topk_stats)."""
     out_dt = dt if out_dt is None else out_dt
     rc = lib().moe_forward_ex(_ptr(x), _ptr(w_r), _ptr(b_r), _ptr(w1), _ptr(w2), T, d, F, E, k, dt, out_dt, path,
-                              GATES_RENORMALISE if renormalise else 0, int(capacity), _ptr(out),
+                              _flags(renormalise, reroute), int(capacity), _ptr(out),
                               _ptr(topk_idx), _ptr(topk_gate), _ptr(counts), _ptr(router_stats), _ptr(ws),
                               ws.numel() * ws.element_size(), _stream(stream))
     return _check(rc, "moe_forward") if check else rc
@@ -359,11 +378,11 @@ def expert_down_q(h, codes, scale_min, offsets, row_gate, T, d, F, E, k, bits, y
 
 
 def forward_q(x, w_r, b_r, w1q, w2q, T, d, F, E, k, bits, out, ws, topk_idx=None, topk_gate=None, counts=None,
-              out_dt=None, renormalise=False, capacity=0, router_stats=None, stream=None, check=True):
+              out_dt=None, renormalise=False, capacity=0, router_stats=None, stream=None, check=True, reroute=False):
     """The layer with block-quantised expert weights; w1q / w2q are (codes, scale_min) pairs."""
     out_dt = MOE_DTYPE_BF16 if out_dt is None else out_dt
     rc = lib().moe_forward_q(_ptr(x), _ptr(w_r), _ptr(b_r), _ptr(w1q[0]), _ptr(w1q[1]), _ptr(w2q[0]),
-                             _ptr(w2q[1]), T, d, F, E, k, bits, out_dt, GATES_RENORMALISE if renormalise else 0,
+                             _ptr(w2q[1]), T, d, F, E, k, bits, out_dt, _flags(renormalise, reroute),
                              int(capacity), _ptr(out), _ptr(topk_idx), _ptr(topk_gate), _ptr(counts),
                              _ptr(router_stats), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     return _check(rc, "moe_forward_q") if check else rc

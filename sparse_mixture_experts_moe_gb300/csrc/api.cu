@@ -20,6 +20,7 @@ int device_sm_count() {
 namespace {
 
 constexpr int kStreamPathMaxRows = 256;
+constexpr int kMaxRank = 8;  // the ranking entries the layer routes with when it reroutes at capacity
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 inline size_t elem_bytes(int dt) { return dt == MOE_DTYPE_BF16 ? 2 : 4; }
@@ -27,8 +28,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Workspace regions, in this order; each starts on a 256-byte boundary.
 struct Layout {
-  size_t header, stats_part, blk_counts, blk_base, topk_idx, topk_gate, counts, offsets, perm_token, row_of,
-      row_gate, h, x_perm, y_perm, end;
+  size_t header, stats_part, blk_counts, blk_base, topk_idx, topk_gate, rank_idx, rank_gate, counts, offsets,
+      perm_token, row_of, row_gate, h, x_perm, y_perm, end;
   size_t stats_end, dispatch_end, ffn_end, grouped_end;
   Layout(int T, int d, int F, int E, int k, int dt) {
     const size_t A = (size_t)T * k, eb = elem_bytes(dt);
@@ -43,6 +44,8 @@ struct Layout {
     dispatch_end = o;
     topk_idx = o; o += align256(A * 4);
     topk_gate = o; o += align256(A * 4);
+    rank_idx = o; o += align256((size_t)T * kMaxRank * 4);   // rerouting: each token's best experts
+    rank_gate = o; o += align256((size_t)T * kMaxRank * 4);
     counts = o; o += align256((size_t)E * 4);
     offsets = o; o += align256((size_t)(E + 1) * 4);
     perm_token = o; o += align256(A * 4);
@@ -95,6 +98,15 @@ moe_path resolve_path(moe_path path, int dt, int rows, int E, int N) {
   const long long items = active * ((rpe + 255) / 256) * ((N + 255) / 256);
   const long long pairs = device_sm_count() / 2;
   return items >= 3 * pairs ? MOE_PATH_TENSOR_T : MOE_PATH_TENSOR;
+}
+
+// Layer flags: MOE_GATES_RENORMALISE, MOE_CAPACITY_REROUTE; rerouting needs a capacity, the raw gates
+// and no routing statistics.
+bool forward_flags_ok(int flags, int capacity, const float* router_stats) {
+  if ((flags & ~(MOE_GATES_RENORMALISE | MOE_CAPACITY_REROUTE)) != 0) return false;
+  if (flags & MOE_CAPACITY_REROUTE)
+    return capacity > 0 && !(flags & MOE_GATES_RENORMALISE) && router_stats == nullptr;
+  return true;
 }
 
 bool path_ok(moe_path path, int dt) {
@@ -222,6 +234,26 @@ moe_status moe_dispatch_ex(const void* x, const int32_t* topk_idx, const float* 
                                           perm_token, row_of, row_gate, x_perm, at<int32_t>(workspace, L.blk_counts),
                                           at<int32_t>(workspace, L.blk_base), at<int>(workspace, L.header),
                                           at<int>(workspace, L.header) + 2, (cudaStream_t)stream));
+}
+
+moe_status moe_dispatch_reroute(const void* x, const int32_t* rank_idx, const float* rank_gate, int T, int d, int E,
+                                int k, int R, moe_dtype dt, int capacity, int32_t* final_idx, float* final_gate,
+                                int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* row_of,
+                                float* row_gate, void* x_perm, void* workspace, size_t ws_bytes, void* stream) {
+  if (!sizes_ok(T, d, 8, E, k, dt) || R < k || R > E || capacity < 1) return MOE_ERR_INVALID_ARG;
+  if (counts == nullptr || offsets == nullptr || workspace == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (x == nullptr || rank_idx == nullptr || rank_gate == nullptr || final_idx == nullptr ||
+                final_gate == nullptr || perm_token == nullptr || row_of == nullptr || row_gate == nullptr ||
+                x_perm == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm) || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  const Layout L(T, d, 8, E, k, dt);
+  if (ws_bytes < L.dispatch_end) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_dispatch_reroute(x, rank_idx, rank_gate, T, d, E, k, R, dt, capacity, final_idx,
+                                             final_gate, counts, offsets, perm_token, row_of, row_gate, x_perm,
+                                             at<int32_t>(workspace, L.blk_counts), at<int32_t>(workspace, L.blk_base),
+                                             at<int>(workspace, L.header), at<int>(workspace, L.header) + 2,
+                                             (cudaStream_t)stream));
 }
 
 // a_rows (nullable): row r of `a` is a[a_rows[r]] (the weight-streaming path only).
@@ -377,6 +409,20 @@ moe_status route_and_dispatch(const void* x, const void* w_r, const float* b_r, 
                               const Layout& L, void* workspace, size_t ws_bytes, void* stream, bool small_ok,
                               bool* rows_via_perm) {
   *rows_via_perm = false;
+  if (flags & MOE_CAPACITY_REROUTE) {
+    // each token's R best experts, then the rerouting dispatch into the caller's idx / gate
+    const int R = E < kMaxRank ? E : kMaxRank;
+    int32_t* ri = at<int32_t>(workspace, L.rank_idx);
+    float* rg = at<float>(workspace, L.rank_gate);
+    moe_status st = cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, R, dt, 0, RouterStats{nullptr, nullptr, nullptr},
+                                                   ri, rg, at<int>(workspace, 0), wait_timeout_ns(),
+                                                   (cudaStream_t)stream));
+    if (st != MOE_OK) return st;
+    return cuda_status(launch_dispatch_reroute(x, ri, rg, T, d, E, k, R, dt, capacity, idx, gate, cnt, offs, perm,
+                                               rowof, rgate, xp, at<int32_t>(workspace, L.blk_counts),
+                                               at<int32_t>(workspace, L.blk_base), at<int>(workspace, 0),
+                                               at<int>(workspace, 0) + 2, (cudaStream_t)stream));
+  }
   if (small_ok && rs.part == nullptr && route_small_ok(T, d, E, k, dt, L.end - L.y_perm)) {
     *rows_via_perm = true;
     return cuda_status(launch_route_small(x, w_r, b_r, T, d, E, k, (flags & MOE_GATES_RENORMALISE) != 0, capacity,
@@ -403,7 +449,7 @@ moe_status moe_forward_ex(const void* x, const void* w_r, const float* b_r, cons
                           int flags, int capacity, void* out, int32_t* topk_idx, float* topk_gate,
                           int32_t* counts, float* router_stats, void* workspace, size_t ws_bytes, void* stream) {
   if (!sizes_ok(T, d, F, E, k, dt) || !path_ok(path, dt) || capacity < 0) return MOE_ERR_INVALID_ARG;
-  if ((flags & ~MOE_GATES_RENORMALISE) != 0) return MOE_ERR_INVALID_ARG;
+  if (!forward_flags_ok(flags, capacity, router_stats)) return MOE_ERR_INVALID_ARG;
   if (out_dt != MOE_DTYPE_F32 && out_dt != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   if (workspace == nullptr || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
   const Layout L(T, d, F, E, k, dt);
@@ -444,7 +490,7 @@ moe_status moe_forward_q(const void* x, const void* w_r, const float* b_r, const
                          size_t ws_bytes, void* stream) {
   const moe_dtype dt = MOE_DTYPE_BF16;
   if (!sizes_ok(T, d, F, E, k, dt) || !qsizes_ok(d, F, E, bits) || capacity < 0) return MOE_ERR_INVALID_ARG;
-  if ((flags & ~MOE_GATES_RENORMALISE) != 0) return MOE_ERR_INVALID_ARG;
+  if (!forward_flags_ok(flags, capacity, router_stats)) return MOE_ERR_INVALID_ARG;
   if (out_dt != MOE_DTYPE_F32 && out_dt != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   if (workspace == nullptr || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
   const Layout L(T, d, F, E, k, dt);

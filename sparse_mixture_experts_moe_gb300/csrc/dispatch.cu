@@ -224,7 +224,7 @@ dispatch_from_hist_kernel(const int32_t* __restrict__ idx, const float* __restri
 // are summed in parallel; every sum runs in a fixed order, so results do not depend on timing.
 // `done` is zero before the call and is reset to zero by the last CTA.
 __global__ void __launch_bounds__(kChunk)
-dispatch_count_scan_kernel(const int32_t* __restrict__ idx, int A, int E, int nb, int cap,
+dispatch_count_scan_kernel(const int32_t* __restrict__ idx, int A, int E, int nb, int cap, int neg_dropped,
                            int32_t* __restrict__ blk_counts, int32_t* __restrict__ blk_base,
                            int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int* status, int* done) {
   griddep_launch_dependents();
@@ -243,7 +243,7 @@ dispatch_count_scan_kernel(const int32_t* __restrict__ idx, int A, int E, int nb
   if (a < A) {
     const int e = idx[a];
     if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
-    else record_error(status, MOE_ERR_DEVICE_CHECK, a);
+    else if (!(neg_dropped && e < 0)) record_error(status, MOE_ERR_DEVICE_CHECK, a);
   }
   __syncthreads();
   for (int e = tid; e < E; e += kChunk) blk_counts[(size_t)blockIdx.x * E + e] = hist[e];
@@ -322,14 +322,91 @@ dispatch_count_scan_kernel(const int32_t* __restrict__ idx, int A, int E, int nb
   if (tid == 0) *done = 0;
 }
 
-}  // namespace
+// Rerouting at capacity (aicoding/6a320eef §3.2: a token that meets a full expert queue goes to the
+// next-best expert; csdn/6a919c0d §3.2: the retry of a dropped request). One warp walks the T*k
+// assignments in row-major (t, j) order, 32 at a time. rank_idx / rank_p hold each token's R best
+// experts and their probabilities, best first; slot j of token t asks for rank j. While no assignment
+// of the group meets a full expert, the whole group is placed at once (ranks among equal experts from
+// __match_any_sync, as in the dispatch); at the first that does, the ones before it are final, and
+// that one takes the next entry of its token's ranking (ranks k .. R-1, each tried once per token)
+// whose expert has room, or is dropped (-1) when none has; then the group goes on from the next lane.
+// The result is exactly the sequential rule: held[e] counts the assignments placed on e so far.
+// An expert index outside [0, E) is recorded (MOE_ERR_DEVICE_CHECK, detail = assignment) and dropped.
+__global__ void __launch_bounds__(32)
+dispatch_reroute_kernel(const int32_t* __restrict__ rank_idx, const float* __restrict__ rank_p, int T, int k,
+                        int R, int E, int cap, int32_t* __restrict__ final_idx, float* __restrict__ final_gate,
+                        int* status) {
+  griddep_launch_dependents();
+  griddep_wait();
+  extern __shared__ int held[];  // [E]
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) held[e] = 0;
+  __syncwarp();
+  const int A = T * k;
+  int cur_t = -1, cur_next = 0;  // the token whose ranking is being walked, and its next entry (uniform)
+  for (int base = 0; base < A; base += 32) {
+    const int a = base + lane;
+    const bool valid = a < A;
+    const int t = valid ? a / k : 0, j = valid ? a % k : 0;
+    int e = valid ? rank_idx[(size_t)t * R + j] : -1;
+    if (valid && (e < 0 || e >= E)) {
+      record_error(status, MOE_ERR_DEVICE_CHECK, a);
+      e = -1;
+    }
+    const float g = valid ? rank_p[(size_t)t * R + j] : 0.f;
+    int start = 0;
+    while (start < 32) {
+      const bool mine = lane >= start && e >= 0;
+      const unsigned peers = __match_any_sync(0xffffffffu, mine ? e : -1 - lane);
+      const int before = __popc(peers & ((1u << lane) - 1u));  // earlier lanes of this round, same expert
+      const bool fits = mine && held[e] + before < cap;
+      const unsigned over = __ballot_sync(0xffffffffu, mine && !fits);
+      const int first = over ? __ffs(over) - 1 : 32;
+      __syncwarp();  // every lane has read held[] before it changes
+      if (valid && lane >= start && lane < first) {
+        final_idx[a] = e;
+        final_gate[a] = e >= 0 ? g : 0.f;
+        if (e >= 0) atomicAdd(&held[e], 1);
+      }
+      __syncwarp();
+      if (first == 32) break;
+      const int af = base + first;
+      const int tf = af / k;
+      if (tf != cur_t) {
+        cur_t = tf;
+        cur_next = k;
+      }
+      int tgt = -1;
+      float tg = 0.f;
+      while (cur_next < R) {
+        const int c = rank_idx[(size_t)tf * R + cur_next];
+        const float cp = rank_p[(size_t)tf * R + cur_next];
+        ++cur_next;
+        if (c >= 0 && c < E && held[c] < cap) {
+          tgt = c;
+          tg = cp;
+          break;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        final_idx[af] = tgt;
+        final_gate[af] = tg;
+        if (tgt >= 0) held[tgt] += 1;
+      }
+      __syncwarp();
+      start = first + 1;
+    }
+  }
+}
 
+}  // namespace
 
 // Two launches with programmatic dependent launch: count + scan, then scatter + gather.
 cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
                                  int dt, int cap, int32_t* counts, int32_t* offsets, int32_t* perm_token,
                                  int32_t* row_of, float* row_gate, void* x_perm, int32_t* blk_counts,
-                                 int32_t* blk_base, int* status, int* done, cudaStream_t s) {
+                                 int32_t* blk_base, int* status, int* done, cudaStream_t s, int neg_dropped) {
   const int A = T * k;
   if (A == 0) {  // no assignments: every count and offset is zero
     cudaError_t err = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
@@ -339,7 +416,7 @@ cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float*
   const int nb = (A + kChunk - 1) / kChunk;
   const size_t cs_smem = (size_t)(3 * E + 1 + kChunk) * sizeof(int);
   cudaError_t err = launch_pdl(dispatch_count_scan_kernel, dim3(nb), dim3(kChunk), cs_smem, s, idx, A, E, nb, cap,
-                               blk_counts, blk_base, counts, offsets, status, done);
+                               neg_dropped, blk_counts, blk_base, counts, offsets, status, done);
   if (err != cudaSuccess) return err;
   // scatter + gather: enough CTAs per chunk that the row copy is spread over the SMs
   const size_t sc_smem = (size_t)(kWarpsPerChunk * E + kChunk) * sizeof(int);
@@ -354,6 +431,20 @@ cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float*
   return launch_pdl(dispatch_scatter_gather_kernel, dim3(nb * split), dim3(kChunk), sc_smem, s, idx, gate, A, k, E,
                     (const int32_t*)blk_base, (const int32_t*)offsets, cap, split, (const int4*)x, vec_per_row,
                     row_of, perm_token, row_gate, (int4*)x_perm);
+}
+
+cudaError_t launch_dispatch_reroute(const void* x, const int32_t* rank_idx, const float* rank_p, int T, int d, int E,
+                                    int k, int R, int dt, int cap, int32_t* final_idx, float* final_gate,
+                                    int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* row_of,
+                                    float* row_gate, void* x_perm, int32_t* blk_counts, int32_t* blk_base, int* status,
+                                    int* done, cudaStream_t s) {
+  if ((long long)T * k > 0) {
+    cudaError_t err = launch_pdl(dispatch_reroute_kernel, dim3(1), dim3(32), (size_t)E * sizeof(int), s, rank_idx,
+                                 rank_p, T, k, R, E, cap, final_idx, final_gate, status);
+    if (err != cudaSuccess) return err;
+  }
+  return launch_dispatch_fast(x, final_idx, final_gate, T, d, E, k, dt, 0, counts, offsets, perm_token, row_of,
+                              row_gate, x_perm, blk_counts, blk_base, status, done, s, 1);
 }
 
 cudaError_t launch_dispatch_from_hist(const void* x, const int32_t* idx, const float* gate, int T, int d, int E,

@@ -59,7 +59,16 @@ cudaError_t launch_dispatch_from_hist(const void* x, const int32_t* idx, const f
 cudaError_t launch_dispatch_fast(const void* x, const int32_t* idx, const float* gate, int T, int d, int E, int k,
                                  int dt, int cap, int32_t* counts, int32_t* offsets, int32_t* perm_token,
                                  int32_t* row_of, float* row_gate, void* x_perm, int32_t* blk_counts,
-                                 int32_t* blk_base, int* status, int* done, cudaStream_t s);
+                                 int32_t* blk_base, int* status, int* done, cudaStream_t s, int neg_dropped = 0);
+// Rerouting at capacity: one warp places the T*k assignments in (t, j) order, sending an assignment that
+// meets a full expert to the next entry of its token's ranking rank_idx[t, k..R-1] with room (or
+// dropping it: final_idx -1), then the two-launch dispatch of final_idx / final_gate, a negative index
+// being an assignment with no row.
+cudaError_t launch_dispatch_reroute(const void* x, const int32_t* rank_idx, const float* rank_p, int T, int d, int E,
+                                    int k, int R, int dt, int cap, int32_t* final_idx, float* final_gate,
+                                    int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* row_of,
+                                    float* row_gate, void* x_perm, int32_t* blk_counts, int32_t* blk_base, int* status,
+                                    int* done, cudaStream_t s);
 
 cudaError_t launch_combine(const void* y_perm, const int32_t* row_of, int T, int d, int k, int dt, void* out,
                            cudaStream_t s);

@@ -124,10 +124,11 @@ class DrawnExperts:
 
 
 def make_case(T, d, F, E, k, dt, seed=0, bias_scale=None, bias=None, device="cuda", redraw=True,
-              host_only=False) -> Case:
+              host_only=False, gap_k=None) -> Case:
     """Seeded layer instance; x and W_r also kept as exact fp64 on the host. ``host_only``: a CPU case
     whose expert weights are never built as tensors (w1 = w2 = None); the oracle draws the routed
-    experts' matrices on access."""
+    experts' matrices on access. ``gap_k``: re-draw tokens by their top-(gap_k+1) logits instead of the
+    top-(k+1) (cases that use a longer part of each token's ranking)."""
     tdt = torch_dtype(dt)
     if host_only:
         device = "cpu"
@@ -148,7 +149,8 @@ def make_case(T, d, F, E, k, dt, seed=0, bias_scale=None, bias=None, device="cud
     if redraw and T > 0:
         attempts = np.zeros(T, np.int64)
         for _ in range(64):
-            bad = oracle.ambiguous_tokens(oracle.router_logits(x64, wr64, br64), k, MIN_GAP)
+            bad = oracle.ambiguous_tokens(oracle.router_logits(x64, wr64, br64), k if gap_k is None else gap_k,
+                                          MIN_GAP)
             if len(bad) == 0:
                 break
             redrawn += len(bad)

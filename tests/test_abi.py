@@ -141,3 +141,28 @@ def test_forward_launch_plan_without_gpu():
     assert moe.forward_launches(64, 128, 256, 8, 2, F32) == 6
     assert moe.forward_launches(0, 128, 256, 8, 2, BF16) == 0
     assert moe.forward_launches(4, 100, 256, 8, 2, BF16) == -1  # d % 8 != 0
+
+
+def test_reroute_arguments_rejected_without_gpu():
+    """moe_dispatch_reroute wants k <= R <= E and a capacity of at least 1; MOE_CAPACITY_REROUTE on the
+    layer wants a capacity, the raw gates and no routing statistics; unknown flag bits are refused."""
+    lib = _lib.lib()
+    n = moe.workspace_bytes(4, 128, 256, 8, 2, 1)
+    outs = (FAKE,) * 8
+    assert lib.moe_dispatch_reroute(FAKE, FAKE, FAKE, 4, 128, 8, 2, 1, 1, 3, *outs, FAKE, n, None) == \
+        moe.MOE_ERR_INVALID_ARG  # R < k
+    assert lib.moe_dispatch_reroute(FAKE, FAKE, FAKE, 4, 128, 8, 2, 9, 1, 3, *outs, FAKE, n, None) == \
+        moe.MOE_ERR_INVALID_ARG  # R > E
+    assert lib.moe_dispatch_reroute(FAKE, FAKE, FAKE, 4, 128, 8, 2, 4, 1, 0, *outs, FAKE, n, None) == \
+        moe.MOE_ERR_INVALID_ARG  # no capacity
+    assert lib.moe_dispatch_reroute(FAKE, None, FAKE, 4, 128, 8, 2, 4, 1, 3, *outs, FAKE, n, None) == \
+        moe.MOE_ERR_INVALID_ARG  # no ranking
+
+    def fwd(flags, capacity, stats=None):
+        return lib.moe_forward_ex(FAKE, FAKE, None, FAKE, FAKE, 4, 128, 256, 8, 2, 1, 1, 0, flags, capacity, FAKE,
+                                  None, None, None, stats, FAKE, n, None)
+    assert fwd(moe.CAPACITY_REROUTE, 0) == moe.MOE_ERR_INVALID_ARG
+    assert fwd(moe.CAPACITY_REROUTE | moe.GATES_RENORMALISE, 3) == moe.MOE_ERR_INVALID_ARG
+    assert fwd(moe.CAPACITY_REROUTE, 3, stats=FAKE) == moe.MOE_ERR_INVALID_ARG
+    assert fwd(4, 3) == moe.MOE_ERR_INVALID_ARG
+    assert moe.CAPACITY_REROUTE == 2 and moe.GATES_RENORMALISE == 1
