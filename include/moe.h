@@ -315,10 +315,14 @@ moe_status moe_selftest_wait_timeout(void* workspace, size_t ws_bytes, int timeo
  *   (2^bits - 1), code = round((w - min) / scale) in fp32 (correctly rounded subtraction and
  *   division, ties to even), restored as w ~ min + code * scale (|error| <= scale / 2). A block of
  *   equal values has scale 0 and codes 0. bits is 4 or 8; K and N must be multiples of 64.
- * Layout of `codes` (moe_qweight_bytes(K, N, E, bits) bytes, 16-byte aligned): per expert,
- *   16-byte tiles of 8 consecutive columns by 16/bits consecutive k-rows, row-major over
- *   (k / (16/bits), n / 8). INT4: 32-bit word j of a tile is its k-row j, nibble c (bits 4c..4c+3)
- *   is column c. INT8: 64-bit half j is k-row j, byte c is column c.
+ * Layout of `codes` (moe_qweight_bytes(K, N, E, bits) bytes, 16-byte aligned), per expert:
+ *   INT8: 16-byte tiles of 8 consecutive columns by 2 consecutive k-rows, row-major over
+ *   (k / 2, n / 8); 64-bit half j is k-row j, byte c is column c.
+ *   INT4: [N/64][K/16][32][4] 32-bit words: for each 64-column slab and 16-deep k-block, lane
+ *   l = 4g + t holds 4 words; word m covers columns c0 = 16m + g and c1 = c0 + 8 at k-rows
+ *   2t, 2t+1, 2t+8, 2t+9 of the k-block, its nibble i (bits 4i..4i+3) holding (k, column) =
+ *   (2t, c0), (2t, c1), (2t+8, c0), (2t+8, c1), (2t+1, c0), (2t+1, c1), (2t+9, c0), (2t+9, c1)
+ *   for i = 0..7 (the order of an m16n8k16 A fragment, decoded two values per instruction).
  * Layout of `scale_min` (moe_qscale_bytes(K, N, E) bytes, 8-byte aligned): fp32 pairs
  *   (scale, min), [E][K/64][N/64].
  * moe_quantize_weights: w [E, K, N] (bf16 or fp32) -> codes, scale_min on the device.

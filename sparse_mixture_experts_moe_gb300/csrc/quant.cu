@@ -7,22 +7,23 @@
 // rounding half to even, so the codes are a deterministic function of the weights; w is restored
 // as min + code * scale (the page's dequantisation would lose the block minimum).
 //
-// Memory format of the codes of one [K, N] matrix: 16-byte tiles of 8 consecutive columns by
-// KT = 16 / bits consecutive k-rows, tiles row-major over (k / KT, n / 8). Inside a tile: INT4,
-// 32-bit word j holds the tile's k-row j, nibble c (bits 4c..4c+3) is column c; INT8, 64-bit
-// half j holds k-row j, byte c is column c. Eight
-// lanes reading one 16-byte tile each cover a 64-column slab of KT k-rows with one coalesced
-// 128-byte request, and a tile never straddles a 64 x 64 block. Scales: one (scale, min) float
-// pair per block, [K/64][N/64] per expert.
+// Memory format of the codes of one [K, N] matrix. INT8: 16-byte tiles of 8 consecutive columns by 2
+// consecutive k-rows, tiles row-major over (k / 2, n / 8); 64-bit half j holds k-row j, byte c is
+// column c. Eight lanes reading one tile each cover a 64-column slab of 2 k-rows with one coalesced
+// 128-byte request, and a tile never straddles a 64 x 64 block. INT4: the fragment layout of the
+// tensor-core kernel, [N/64 slabs][K/16 k-blocks][32 lanes][4 words] (quantize_kernel describes
+// the nibble order). Scales: one (scale, min) float pair per block, [K/64][N/64] per expert.
 //
-// Streaming kernel: the structure of ffn_stream.cu (work unit = (expert with rows, 64-column
+// INT8 streaming kernel: the structure of ffn_stream.cu (work unit = (expert with rows, 64-column
 // slab), full depth per CTA, fixed-order reductions) with the dequantisation folded into the
 // dot product: sum_k a_k (min_b + c_k scale_b) = sum_b [ (a scale_b) . (c - m) + (min_b + m scale_b) sum a ]
-// with the centre m = 2^(bits-1).
+// with the centre m = 128.
 // Per weight that is one byte permute into a 2^23-offset float, one subtraction (exact) and one
 // FMA per activation row. The activations are staged already multiplied by their block's scale,
 // and the column-independent term (min_b times the block's activation sum) is formed once per row
 // from block sums taken while staging, not by every lane of the slab.
+// INT4 streaming kernel (ffn_stream_q4_kernel): the same units and code stream, the dot products on
+// mma.sync (see there).
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -76,29 +77,40 @@ quantize_kernel(const T* __restrict__ w, int K, int N, uint4* __restrict__ codes
     if (!(scale > 0.f)) return 0u;
     return (uint32_t)rintf(__fdiv_rn(__fsub_rn(blk[r][c], lo), scale));
   };
-  constexpr int tiles = (QB / KT) * (QB / 8);  // 128 (INT4) or 256 (INT8)
+  if (BITS == 4) {
+    // INT4: the fragment layout of the tensor-core streaming kernel. Per (64-column slab, 16-deep
+    // k-block) 512 bytes: lane l = 4g + t holds four words, word m covering columns 16m + g (c0) and
+    // 16m + g + 8 (c1) at k-rows 2t, 2t+1, 2t+8, 2t+9 of the k-block, nibbles (k, c):
+    //   0: (2t, c0)  1: (2t, c1)  2: (2t+8, c0)  3: (2t+8, c1)  4: (2t+1, c0)  5: (2t+1, c1)
+    //   6: (2t+9, c0)  7: (2t+9, c1),
+    // so that (word >> 4i) & 0x000F000F puts register i of an m16n8k16 A fragment (rows = columns of
+    // w, columns = k) in place: nibble i in the low half, nibble i + 4 in the high half.
+    uint32_t* cw = reinterpret_cast<uint32_t*>(codes);
+    for (int wi = tid; wi < (QB / 16) * 32 * 4; wi += 256) {
+      const int m = wi & 3, lane = (wi >> 2) & 31, j = wi >> 7;
+      const int g = lane >> 2, t = lane & 3;
+      const int c0 = 16 * m + g, c1 = c0 + 8, k0 = 16 * j + 2 * t;
+      const uint32_t v = code(k0, c0) | code(k0, c1) << 4 | code(k0 + 8, c0) << 8 | code(k0 + 8, c1) << 12 |
+                         code(k0 + 1, c0) << 16 | code(k0 + 1, c1) << 20 | code(k0 + 9, c0) << 24 |
+                         code(k0 + 9, c1) << 28;
+      const size_t k16 = (size_t)bi * (QB / 16) + j;
+      cw[((((size_t)e * nbj + bj) * (K / 16) + k16) * 32 + lane) * 4 + m] = v;
+    }
+    return;
+  }
+  constexpr int tiles = (QB / KT) * (QB / 8);  // 256 (INT8)
   for (int t = tid; t < tiles; t += 256) {
     const int kgl = t / (QB / 8), ngl = t % (QB / 8);
     uint32_t word[4];
-    if (BITS == 4) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
         uint32_t v = 0;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) v |= code(kgl * KT + j, ngl * 8 + c) << (4 * c);
-        word[j] = v;
+        for (int c = 0; c < 4; ++c) v |= code(kgl * KT + j, ngl * 8 + 4 * h + c) << (8 * c);
+        word[2 * j + h] = v;
       }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t v = 0;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) v |= code(kgl * KT + j, ngl * 8 + 4 * h + c) << (8 * c);
-          word[2 * j + h] = v;
-        }
-    }
     const size_t kg = (size_t)bi * (QB / KT) + kgl, ng = (size_t)bj * (QB / 8) + ngl;
     codes[((size_t)e * (K / KT) + kg) * (N / 8) + ng] = make_uint4(word[0], word[1], word[2], word[3]);
   }
@@ -113,14 +125,6 @@ quantize_kernel(const T* __restrict__ w, int K, int N, uint4* __restrict__ codes
 template <int BITS>
 constexpr float kCentre = (float)(1 << (BITS - 1));
 __device__ __forceinline__ uint32_t magic_byte(uint32_t w, uint32_t sel) { return __byte_perm(w, 0x4B000000u, sel); }
-__device__ __forceinline__ void int4_row(uint32_t wd, uint64_t (&c)[4]) {
-  const uint32_t even = wd & 0x0F0F0F0Fu;         // columns 0, 2, 4, 6 in bytes 0..3
-  const uint32_t odd = (wd >> 4) & 0x0F0F0F0Fu;   // columns 1, 3, 5, 7
-  const uint64_t neg = f2_pack(-(kMagic + kCentre<4>), -(kMagic + kCentre<4>));
-#pragma unroll
-  for (int p = 0; p < 4; ++p)
-    c[p] = fadd2(((uint64_t)magic_byte(odd, 0x7540 + p) << 32) | magic_byte(even, 0x7540 + p), neg);
-}
 __device__ __forceinline__ void int8_row(uint32_t w0, uint32_t w1, uint64_t (&c)[4]) {
   const uint64_t neg = f2_pack(-(kMagic + kCentre<8>), -(kMagic + kCentre<8>));
   c[0] = fadd2(((uint64_t)magic_byte(w0, 0x7541) << 32) | magic_byte(w0, 0x7540), neg);
@@ -234,7 +238,7 @@ ffn_stream_q_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16
                     const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
                     int nst, OutT* __restrict__ out, int* status, uint64_t timeout_ns) {
   constexpr int KT = 16 / BITS;  // k-rows per tile: 128 bits / (8 columns x BITS)
-  static_assert(KT * 8 * BITS == 128 && (BITS == 4 ? KT == 4 : KT == 2), "tile words hold KT k-rows");
+  static_assert(BITS == 8 && KT == 2, "the tile kernel streams INT8 codes (INT4: ffn_stream_q4_kernel)");
   constexpr int KC = kTmaActFloats / RMAX;  // a multiple of the k-rows of a box (128 KT)
   static_assert(KC % (kTmaTileRows * KT) == 0, "a chunk holds whole boxes");
   constexpr int kSets = RMAX == 2 ? 2 : 1;  // accumulator sets
@@ -382,8 +386,7 @@ ffn_stream_q_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16
 #pragma unroll
               for (int j = 0; j < KT; ++j) {
                 uint64_t cp[4];
-                if (BITS == 4) int4_row(wd[j], cp);
-                else int8_row(wd[2 * j], wd[2 * j + 1], cp);
+                int8_row(wd[2 * j], wd[2 * j + 1], cp);
 #pragma unroll
                 for (int r = 0; r < RMAX; ++r) {
                   if (r >= R) break;
@@ -436,7 +439,283 @@ ffn_stream_q_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16
   }
 }
 
+// ------------------------------------------------------------------ INT4 on the tensor cores
+// The INT4 codes of a 64-column slab arrive by TMA like the tiles above (boxes of 16 KB: 32 k-blocks
+// of 16 k-rows, 512 bytes each, in the fragment layout the quantiser writes), and the dot products
+// run on mma.sync m16n8k16 (bf16 in, fp32 accumulate): A = 16 weight columns x 16 k-rows, decoded from
+// one 32-bit word per lane, B = 16 k-rows x 8 activation rows (tokens) from shared memory, so one
+// instruction does 2048 multiply-adds and a pass takes up to 8 rows at the cost of one. Decoding a
+// register pair is one shift and one LOP3 that puts two nibbles n into the low mantissa bits of bf16
+// 128.0 (128 + n, exact), and one packed bf16 subtraction of 136 that leaves the centred code n - 8
+// (exact). Each warp takes one 64-deep k-block of every box, so its products all share one
+// (scale, min) pair: they accumulate in a block accumulator that is scaled and added once per block.
+// The column-independent term (min + 8 scale) * (sum of the block's activations) is formed once per
+// row from block sums taken while staging, as in the kernel above.
+constexpr int kQ4Rows = 8;                     // activation rows per pass: the MMA's N
+constexpr int kQ4BoxK16 = kTmaBoxBytes / 512;  // 16-deep k-blocks per box: 32 (512 k-rows)
+constexpr int kQ4StageElems = 8256;            // staged activations (bf16): R rows x (chunk + 8) at most
+constexpr int kQ4MaxChunkBlocks = 128;         // 64-deep blocks of a chunk at most (R * chunk <= 8192)
+
+// k per staged chunk for R rows: as much of K as R rows fit (whole boxes of 512 k-rows when K does not
+// fit), so one or two rows stage all of K = 8192 at once.
+__host__ __device__ constexpr int q4_chunk(int R, int K) {
+  return (kQ4StageElems / R - 8) / 512 * 512 < K ? (kQ4StageElems / R - 8) / 512 * 512 : K;
+}
+
+__device__ __forceinline__ uint32_t q4_pair(uint32_t word, int shift) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r) : "r"(word >> shift), "r"(0x000F000Fu), "r"(0x43004300u));
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(r), "r"(0x43084308u));  // (128 + n) - 136 = n - 8, exact
+  return r;
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldmatrix_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+template <int STAGE, typename OutT>
+__global__ void __launch_bounds__(kTmaThreads, 2)
+ffn_stream_q4_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16* __restrict__ a,
+                     const int32_t* __restrict__ a_rows, const float2* __restrict__ sm,
+                     const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
+                     int nst, OutT* __restrict__ out, int* status, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  // ring [nst][16 KB] (128-byte aligned) | full [nst], empty [nst] mbarriers in a 128-byte slot |
+  // sX [R][chunk + 8] bf16, kQ4StageElems at most (the epilogue's per-warp sums reuse it) | sSM [K/64]
+  // | sBS [R][chunk / 64] | sMin [kQ4Rows] | sAct [E]. The MMA reads rows R .. 7 from a zero vector.
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t ring = (raw + 127u) & ~127u;
+  uint8_t* gring = smem_raw + (ring - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gring + nst * kTmaBoxBytes);
+  __nv_bfloat16* sX = reinterpret_cast<__nv_bfloat16*>(gring + nst * kTmaBoxBytes + kBarSlotBytes);
+  float* sRed = reinterpret_cast<float*>(sX);  // [kWarps][kQ4Rows][NS]
+  float2* sSM = reinterpret_cast<float2*>(sX + kQ4StageElems);
+  float* sBS = reinterpret_cast<float*>(sSM + K / QB);
+  float* sMin = sBS + kQ4MaxChunkBlocks;
+  int* sAct = reinterpret_cast<int*>(sMin + kQ4Rows);
+  __shared__ int s_nact, s_abort;
+  __shared__ __align__(16) uint4 s_zero;
+  volatile int* abort_flag = &s_abort;
+  auto full = [&](int st) { return smem_u32(bars + st); };
+  auto empty = [&](int st) { return smem_u32(bars + nst + st); };
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == kWarps && lane == 0) {
+    for (int st = 0; st < nst; ++st) {
+      mbar_init(full(st), 1);
+      mbar_init(empty(st), kWarps);
+    }
+    fence_mbar_init();
+    *abort_flag = 0;
+    s_zero = make_uint4(0u, 0u, 0u, 0u);
+    tma_prefetch_desc(&tmC);
+  }
+  griddep_launch_dependents();
+  griddep_wait();
+  if (warp == 0) {
+    int base = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const bool act = e < E && offsets[e + 1] > offsets[e];
+      const unsigned m = __ballot_sync(0xffffffffu, act);
+      if (act) sAct[base + __popc(m & ((1u << lane) - 1u))] = e;
+      base += __popc(m);
+    }
+    if (lane == 0) s_nact = base;
+  }
+  __syncthreads();
+  const int nslab = N / NS;
+  const int units = s_nact * nslab;
+  const int K16 = K / 16;
+  const int KB = (K16 + kQ4BoxK16 - 1) / kQ4BoxK16;  // boxes per pass; k-blocks past K arrive as zeros
+
+  if (warp == kWarps) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      int st = 0;
+      uint32_t phase = 0, filled = 0, fill_phase = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int e = sAct[u / nslab], slab = u % nslab;
+        const int passes = (offsets[e + 1] - offsets[e] + kQ4Rows - 1) / kQ4Rows;
+        for (int ps = 0; ps < passes; ++ps)
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!wait_or_abort(empty(st), phase ^ 1u, timeout_ns, abort_flag, status, 55)) goto producer_out;
+            mbar_arrive_expect_tx(full(st), kTmaBoxBytes);
+            tma_load_3d(ring + st * kTmaBoxBytes, &tmC, 0, kb * kQ4BoxK16, e * nslab + slab, full(st));
+            filled |= 1u << st;
+            fill_phase = (fill_phase & ~(1u << st)) | (phase << st);
+            if (++st == nst) { st = 0; phase ^= 1u; }
+          }
+      }
+    producer_out:
+      for (int q = 0; q < nst; ++q)
+        if (filled & (1u << q)) mbar_wait_bounded(full(q), (fill_phase >> q) & 1u, timeout_ns);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers (warps 0..7)
+  // Every consumer warp runs the same trip counts, so the named barriers always match; after a
+  // failed wait (recorded in the status word) the warps skip the arithmetic and run to the end.
+  const int g = lane >> 2, t = lane & 3;
+  const int NB = N / QB;
+  int st = 0;
+  uint32_t phase = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int e = sAct[u / nslab];
+    const int slab = u % nslab;
+    const int n0 = slab * NS;
+    consumer_sync();  // the previous unit is done with sSM
+    for (int b = tid; b < K / QB; b += kThreads) sSM[b] = sm[((size_t)e * (K / QB) + b) * NB + slab];
+    const int r_begin = offsets[e], r_end = offsets[e + 1];
+    for (int rp = r_begin; rp < r_end; rp += kQ4Rows) {
+      const int R = min(kQ4Rows, r_end - rp);
+      const int kcl = q4_chunk(R, K);  // k per staged chunk
+      const int xs = kcl + 8;          // staged row stride (bf16): 16 bytes mod 128, conflict-free ldmatrix
+      // ldmatrix row addresses: lanes 0-7 rows 0-7 at k, lanes 8-15 the same rows at k + 8; rows past R
+      // read the zero vector (and do not move with k)
+      const int xr = lane & 7;
+      const uint32_t x_lane = xr < R ? smem_u32(sX) + (uint32_t)((xr * xs + ((lane >> 3) & 1) * 8) * 2)
+                                     : smem_u32(&s_zero);
+      const uint32_t x_step = xr < R ? 2u : 0u;
+      float acc[4][4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
+      float min_term = 0.f;  // thread r < R: row r's sum over blocks of (min_b + 8 scale_b) * (sum of a over b)
+      for (int kc = 0; kc < K; kc += kcl) {
+        const int kn = min(kcl, K - kc);  // a multiple of 64
+        consumer_sync();  // sSM is written; the previous chunk's activations (or sums) are read
+        // stage rows rp .. rp+R-1, k in [kc, kc + kn), as bf16, and each row's per-block sums; every
+        // lane of a warp runs the same iterations (the shuffles), groups of 8 lanes share one block
+        const int per_row = kn / 8, total = R * per_row;
+        for (int i0 = 0; i0 < total; i0 += kThreads) {
+          const int i = i0 + tid;
+          const int r = i / per_row, kk = (i % per_row) * 8;
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (i < total) {
+            const size_t src = a_rows != nullptr ? (size_t)a_rows[rp + r] : (size_t)(rp + r);
+            v = __ldg(reinterpret_cast<const uint4*>(a + src * K + kc + kk));
+            *reinterpret_cast<uint4*>(sX + r * xs + kk) = v;
+          }
+          float s8 = bf16lo(v.x) + bf16hi(v.x) + bf16lo(v.y) + bf16hi(v.y) + bf16lo(v.z) + bf16hi(v.z) +
+                     bf16lo(v.w) + bf16hi(v.w);
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1) s8 += __shfl_xor_sync(0xffffffffu, s8, o);
+          if ((tid & 7) == 0 && i < total) sBS[r * (kcl / QB) + kk / QB] = s8;
+        }
+        consumer_sync();
+        if (tid < R)
+          for (int b = 0; b < kn / QB; ++b) {  // w = (min + 8 scale) + (code - 8) scale
+            const float2 q = sSM[kc / QB + b];
+            min_term = fmaf(fmaf(8.0f, q.x, q.y), sBS[tid * (kcl / QB) + b], min_term);
+          }
+        for (int kb = 0; kb < kn; kb += kQ4BoxK16 * 16) {
+          if (ok) ok = wait_or_abort(full(st), phase, timeout_ns, abort_flag, status, 56);
+          ok = __all_sync(0xffffffffu, ok);
+          const int kw = kb + warp * QB;  // this warp's 64-deep k-block within the chunk
+          if (ok && kw < kn) {
+            const uint8_t* box = gring + st * kTmaBoxBytes + warp * 4 * 512 + lane * 16;
+            float blk[4][4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) blk[m][i] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 wd = *reinterpret_cast<const uint4*>(box + j * 512);
+              uint32_t b0, b1;
+              ldmatrix_x2(x_lane + (uint32_t)(kw + 16 * j) * x_step, b0, b1);
+              const uint32_t words[4] = {wd.x, wd.y, wd.z, wd.w};
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const uint32_t af[4] = {q4_pair(words[m], 0), q4_pair(words[m], 4), q4_pair(words[m], 8),
+                                        q4_pair(words[m], 12)};
+                mma_bf16_16816(blk[m], af, b0, b1);
+              }
+            }
+            const float sc = sSM[(kc + kw) / QB].x;
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) acc[m][i] = fmaf(sc, blk[m][i], acc[m][i]);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty(st));  // the box's slot goes back to the producer
+          if (++st == nst) { st = 0; phase ^= 1u; }
+        }
+      }
+      // Warp sums to shared memory ([warp][row][column]), then every (row, column) adds the warps in a
+      // fixed order and the row's block-minimum term. acc[m]: columns 16m + g (0, 1) and 16m + g + 8
+      // (2, 3), rows 2t and 2t + 1.
+      consumer_sync();  // sRed overlays the activations
+      if (tid < R) sMin[tid] = min_term;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int c = 16 * m + g;
+        sRed[(warp * kQ4Rows + 2 * t) * NS + c] = acc[m][0];
+        sRed[(warp * kQ4Rows + 2 * t + 1) * NS + c] = acc[m][1];
+        sRed[(warp * kQ4Rows + 2 * t) * NS + c + 8] = acc[m][2];
+        sRed[(warp * kQ4Rows + 2 * t + 1) * NS + c + 8] = acc[m][3];
+      }
+      consumer_sync();
+      for (int i = tid; i < R * NS; i += kThreads) {
+        const int r = i / NS, c = i % NS;
+        float v = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < kWarps; ++wi) v += sRed[(wi * kQ4Rows + r) * NS + c];
+        v += sMin[r];
+        const int grow = rp + r;
+        v = STAGE == 1 ? gelu_as(v) : row_gate[grow] * v;
+        out[(size_t)grow * N + n0 + c] = from_f32<OutT>(v);
+      }
+    }
+  }
+}
+
+size_t q4_smem_bytes(int nst, int K, int E) {
+  return 128 + (size_t)nst * kTmaBoxBytes + kBarSlotBytes + (size_t)kQ4StageElems * 2 +
+         (size_t)(K / QB) * sizeof(float2) + (size_t)(kQ4MaxChunkBlocks + kQ4Rows) * sizeof(float) + (size_t)E * 4;
+}
+static_assert(kWarps * kQ4Rows * NS * 4 <= kQ4StageElems * 2, "the warp sums fit the staging buffer");
+static_assert(kQ4StageElems / 1 - 8 >= 8192 && 8 * (1024 + 8) <= kQ4StageElems, "chunk sizes fit the buffer");
+
 constexpr size_t kSmPerSmBytes = 228 * 1024;  // shared memory per SM, of which 1 KB per resident CTA is reserved
+
+template <int STAGE, typename OutT>
+cudaError_t launch_q4(const QFfnArgs& p, EncodeTiledFn enc, cudaStream_t s) {
+  int nst = kTmaStages;
+  while (nst > 2 && 2 * (q4_smem_bytes(nst, p.K, p.E) + 1024) > kSmPerSmBytes) --nst;
+  const size_t smem = q4_smem_bytes(nst, p.K, p.E);
+  auto kern = ffn_stream_q4_kernel<STAGE, OutT>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  // codes [E][N/64][K/16][512 bytes] viewed as [E * N/64][K/16][256] 16-bit elements: 32 k-blocks of one
+  // slab per box, no swizzle; k-blocks past K/16 arrive as zeros
+  CUtensorMap tmC;
+  const cuuint64_t dims[3] = {256, (cuuint64_t)(p.K / 16), (cuuint64_t)p.E * (p.N / NS)};
+  const cuuint64_t str[2] = {512, (cuuint64_t)(p.K / 16) * 512};
+  const cuuint32_t box[3] = {256, kQ4BoxK16, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&tmC, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(p.codes), dims, str, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const int nslab = p.N / NS;
+  const long long max_units = (long long)(p.rows < p.E ? p.rows : p.E) * nslab;
+  long long grid = 2LL * device_sm_count();
+  if (grid > max_units) grid = max_units;
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, s, tmC, (const __nv_bfloat16*)p.a,
+                    p.a_rows, (const float2*)p.scale_min, p.offsets, p.row_gate, p.K, p.N, p.E, nst, (OutT*)p.out,
+                    p.status, p.timeout_ns);
+}
 
 size_t q_smem_bytes(int RMAX, int nst, int K, int E) {
   const int KC = kTmaActFloats / RMAX;
@@ -474,7 +753,7 @@ cudaError_t launch_q(const QFfnArgs& p, EncodeTiledFn enc, cudaStream_t s) {
                     p.status, p.timeout_ns);
 }
 
-template <int BITS>
+template <int BITS>  // INT8 (the INT4 codes take launch_q4)
 cudaError_t launch_q_bits(const QFfnArgs& p, EncodeTiledFn enc, cudaStream_t s) {
   if (p.max_rows_per_expert == 1)  // a single token: one row per expert
     return p.stage == 1 ? launch_q<BITS, 1, __nv_bfloat16, 1>(p, enc, s) : launch_q<BITS, 2, float, 1>(p, enc, s);
@@ -514,7 +793,9 @@ cudaError_t launch_ffn_stream_q(const QFfnArgs& p, cudaStream_t s) {
   if (p.rows == 0) return cudaSuccess;
   EncodeTiledFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
-  return p.bits == 4 ? launch_q_bits<4>(p, enc, s) : launch_q_bits<8>(p, enc, s);
+  if (p.bits == 4)
+    return p.stage == 1 ? launch_q4<1, __nv_bfloat16>(p, enc, s) : launch_q4<2, float>(p, enc, s);
+  return launch_q_bits<8>(p, enc, s);
 }
 
 }  // namespace moe

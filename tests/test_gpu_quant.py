@@ -17,17 +17,27 @@ BF16, F32 = ig.DTYPE_BF16, ig.DTYPE_F32
 
 
 def unpack_codes(raw, E, K, N, bits):
-    """Device tile format -> codes [E, K, N]: 16-byte tiles of 8 columns by 16/bits k-rows."""
-    KT = 16 // bits
-    tiles = np.ascontiguousarray(raw).reshape(E, K // KT, N // 8, 16)
+    """Device code format -> codes [E, K, N].
+
+    INT4: per expert [N/64 slabs][K/16 k-blocks][32 lanes][4 words]; lane 4g + t, word m covers
+    columns c0 = 16m + g and c1 = c0 + 8 at k-rows 2t, 2t+1, 2t+8, 2t+9 of the k-block, nibble i
+    (bits 4i..4i+3) holding (k, column) = (2t, c0), (2t, c1), (2t+8, c0), (2t+8, c1), (2t+1, c0),
+    (2t+1, c1), (2t+9, c0), (2t+9, c1) for i = 0..7.
+    INT8: 16-byte tiles of 8 columns by 2 k-rows, row-major over (k / 2, n / 8); half j is k-row j."""
     codes = np.zeros((E, K, N), np.uint8)
     if bits == 4:
-        words = tiles.view("<u4").reshape(E, K // KT, N // 8, 4)
-        for j in range(4):
-            for c in range(8):
-                codes[:, j::4, c::8] = (words[..., j] >> (4 * c)) & 0xF
+        words = np.ascontiguousarray(raw).view("<u4").reshape(E, N // 64, K // 16, 32, 4)
+        lane = np.arange(32)
+        g, t = lane // 4, lane % 4
+        slab = np.arange(N // 64)[:, None, None]
+        k16 = np.arange(K // 16)[None, :, None]
+        for m in range(4):
+            for i, (dk, dc) in enumerate([(0, 0), (0, 8), (8, 0), (8, 8), (1, 0), (1, 8), (9, 0), (9, 8)]):
+                k = k16 * 16 + (2 * t + dk)[None, None, :]
+                c = slab * 64 + (16 * m + g + dc)[None, None, :]
+                codes[:, k, c] = (words[..., m] >> (4 * i)) & 0xF
     else:
-        b = tiles.reshape(E, K // 2, N // 8, 2, 8)
+        b = np.ascontiguousarray(raw).reshape(E, K // 2, N // 8, 2, 8)
         for j in range(2):
             codes[:, j::2, :] = b[:, :, :, j, :].reshape(E, K // 2, N)
     return codes
