@@ -251,6 +251,34 @@ def test_expert_down(cfg):
     assert rel_rms_err(to_f64(y), ref) < 1e-4
 
 
+@pytest.mark.parametrize("T,F", [(1500, 512), (700, 256)])
+def test_expert_gemms_mixed_routing(T, F):
+    """The pair GEMM on a skewed batch (experts with more than 256 rows and experts with a few rows in
+    the same launch): items come from the workspace counter through the item ring, heavy and light
+    experts interleaved; h and y_perm against the oracle as in test_expert_up / test_expert_down."""
+    d, E, k = 256, 16, 2
+    c = make_case(T=T, d=d, F=F, E=E, k=k, dt=BF16, bias=_skewed(E))
+    dp, x_perm, offsets, row_gate = _ffn_inputs(c)
+    cnt = np.diff(dp["offsets"])
+    assert (cnt > 256).any() and ((cnt > 0) & (cnt <= 256)).any()  # both classes present
+    hg = Guarded((c.A, F), torch.bfloat16, fill=0)
+    ws = guarded_workspace(c)
+    for _ in range(2):  # the second launch also checks that the counter was set back to zero
+        moe.expert_up(x_perm, c.w1, offsets, T, d, F, E, k, BF16, hg.t, ws.t, path=moe.PATH_TENSOR_T)
+        assert moe.get_device_status(ws.t)[0] == moe.MOE_OK
+        assert hg.intact() and ws.intact()
+        ref = oracle.expert_rows_up(c.x64[dp["perm_token"]], dp["offsets"], c.w1_host())
+        assert_rounded_once(to_f64(hg.t), ref, BF16)
+    yg = Guarded((c.A, d), torch.float32, fill=0)
+    moe.expert_down(hg.t, c.w2, offsets, row_gate, T, d, F, E, k, BF16, yg.t, ws.t, path=moe.PATH_TENSOR_T)
+    assert moe.get_device_status(ws.t)[0] == moe.MOE_OK
+    assert yg.intact() and ws.intact()
+    yref = oracle.expert_rows_down(to_f64(hg.t), dp["offsets"], dp["row_gate"], c.w2_host())
+    assert rel_rms_err(to_f64(yg.t), yref) < 1e-4
+    hdr = ws.t[:32].view(torch.int32).cpu().numpy()
+    assert hdr[4] == 0 and hdr[5] == 0  # item counter and finished pairs back at zero
+
+
 @pytest.mark.parametrize("dt", [BF16, F32])
 def test_combine(dt):
     T, d, k = 333, 136, 3
