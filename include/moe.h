@@ -318,11 +318,13 @@ moe_status moe_selftest_wait_timeout(void* workspace, size_t ws_bytes, int timeo
  * Layout of `codes` (moe_qweight_bytes(K, N, E, bits) bytes, 16-byte aligned), per expert:
  *   INT8: 16-byte tiles of 8 consecutive columns by 2 consecutive k-rows, row-major over
  *   (k / 2, n / 8); 64-bit half j is k-row j, byte c is column c.
- *   INT4: [N/64][K/16][32][4] 32-bit words: for each 64-column slab and 16-deep k-block, lane
- *   l = 4g + t holds 4 words; word m covers columns c0 = 16m + g and c1 = c0 + 8 at k-rows
- *   2t, 2t+1, 2t+8, 2t+9 of the k-block, its nibble i (bits 4i..4i+3) holding (k, column) =
- *   (2t, c0), (2t, c1), (2t+8, c0), (2t+8, c1), (2t+1, c0), (2t+1, c1), (2t+9, c0), (2t+9, c1)
- *   for i = 0..7 (the order of an m16n8k16 A fragment, decoded two values per instruction).
+ *   INT4: [N/64][K/16][32][4] 32-bit words: for each 64-column slab and 16-deep k-block 4b + j
+ *   (step j of the 64-deep block b), lane l = 4g + t holds 4 words; word m covers columns
+ *   c0 = 16m + g and c1 = c0 + 8 at k-rows kp .. kp+3, kp = 64b + 16t + 4j, its nibble i
+ *   (bits 4i..4i+3) holding (k, column) = (kp, c0), (kp, c1), (kp+2, c0), (kp+2, c1), (kp+1, c0),
+ *   (kp+1, c1), (kp+3, c0), (kp+3, c1) for i = 0..7 (the order of an m16n8k16 A fragment, decoded
+ *   two values per instruction, with k numbered within each 64-deep block so that one lane's
+ *   activations for the block's four steps are 16 consecutive values).
  * Layout of `scale_min` (moe_qscale_bytes(K, N, E) bytes, 8-byte aligned): fp32 pairs
  *   (scale, min), [E][K/64][N/64].
  * moe_quantize_weights: w [E, K, N] (bf16 or fp32) -> codes, scale_min on the device.

@@ -79,20 +79,22 @@ quantize_kernel(const T* __restrict__ w, int K, int N, uint4* __restrict__ codes
   };
   if (BITS == 4) {
     // INT4: the fragment layout of the tensor-core streaming kernel. Per (64-column slab, 16-deep
-    // k-block) 512 bytes: lane l = 4g + t holds four words, word m covering columns 16m + g (c0) and
-    // 16m + g + 8 (c1) at k-rows 2t, 2t+1, 2t+8, 2t+9 of the k-block, nibbles (k, c):
-    //   0: (2t, c0)  1: (2t, c1)  2: (2t+8, c0)  3: (2t+8, c1)  4: (2t+1, c0)  5: (2t+1, c1)
-    //   6: (2t+9, c0)  7: (2t+9, c1),
+    // step j of a 64-deep block) 512 bytes: lane l = 4g + t holds four words, word m covering columns
+    // 16m + g (c0) and 16m + g + 8 (c1) at the block's k-rows kp .. kp+3, kp = 16t + 4j, nibbles (k, c):
+    //   0: (kp, c0)  1: (kp, c1)  2: (kp+2, c0)  3: (kp+2, c1)  4: (kp+1, c0)  5: (kp+1, c1)
+    //   6: (kp+3, c0)  7: (kp+3, c1),
     // so that (word >> 4i) & 0x000F000F puts register i of an m16n8k16 A fragment (rows = columns of
-    // w, columns = k) in place: nibble i in the low half, nibble i + 4 in the high half.
+    // w) in place, nibble i in the low half and nibble i + 4 in the high half, with the fragment's
+    // k-rows 2t, 2t+1, 2t+8, 2t+9 standing for kp .. kp+3: then lane t's B fragments for the four
+    // steps are the block's 16 consecutive activations 16t .. 16t+15.
     uint32_t* cw = reinterpret_cast<uint32_t*>(codes);
     for (int wi = tid; wi < (QB / 16) * 32 * 4; wi += 256) {
       const int m = wi & 3, lane = (wi >> 2) & 31, j = wi >> 7;
       const int g = lane >> 2, t = lane & 3;
-      const int c0 = 16 * m + g, c1 = c0 + 8, k0 = 16 * j + 2 * t;
-      const uint32_t v = code(k0, c0) | code(k0, c1) << 4 | code(k0 + 8, c0) << 8 | code(k0 + 8, c1) << 12 |
-                         code(k0 + 1, c0) << 16 | code(k0 + 1, c1) << 20 | code(k0 + 9, c0) << 24 |
-                         code(k0 + 9, c1) << 28;
+      const int c0 = 16 * m + g, c1 = c0 + 8, k0 = 16 * t + 4 * j;
+      const uint32_t v = code(k0, c0) | code(k0, c1) << 4 | code(k0 + 2, c0) << 8 | code(k0 + 2, c1) << 12 |
+                         code(k0 + 1, c0) << 16 | code(k0 + 1, c1) << 20 | code(k0 + 3, c0) << 24 |
+                         code(k0 + 3, c1) << 28;
       const size_t k16 = (size_t)bi * (QB / 16) + j;
       cw[((((size_t)e * nbj + bj) * (K / 16) + k16) * 32 + lane) * 4 + m] = v;
     }
@@ -245,6 +247,7 @@ ffn_stream_q_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16
   constexpr int kXIt = RMAX * KC / 8 / kThreads;  // 16-byte activation loads per consumer thread per chunk
   constexpr bool kPrefetch = RMAX == 2;          // the next chunk's activations in flight during the boxes
   static_assert(kXIt * kThreads * 8 == RMAX * KC && (KC / 8) % 32 == 0, "whole warps per activation row");
+  static_assert(RMAX <= kWarps, "one warp per row forms the block-minimum terms");
   extern __shared__ uint8_t smem_raw[];
   // ring [nst][128 tile rows][8 tiles] (128-byte aligned) | full [nst], empty [nst] mbarriers in
   // a 128-byte slot | sA [RMAX][KC] (the epilogue's per-warp sums reuse it) | sSM [K/64]
@@ -348,7 +351,7 @@ ffn_stream_q_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16
         for (int r = 0; r < RMAX; ++r)
 #pragma unroll
           for (int q = 0; q < 4; ++q) acc2[h][r][q] = 0ull;
-      float min_term = 0.f;  // thread r < R: row r's sum over blocks of (min_b + m scale_b) * (sum of a over b)
+      float min_term = 0.f;  // warp r < R: row r's sum over blocks of (min_b + m scale_b) * (sum of a over b)
       // With two rows a pass, the pass's first chunk of activations is loaded together with (on a
       // new unit) the slab's scale pairs, which the previous unit stopped reading before its
       // epilogue's barriers, and each later chunk while the boxes of the one before are consumed:
@@ -367,11 +370,18 @@ ffn_stream_q_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16
         else stage_rows_q<KC>(a, a_rows, K, rp, R, kc, kn, sSM, sA, sBS);
         consumer_sync();
         if (kPrefetch && kc + KC < K) load_rows_q<KC>(a, a_rows, K, rp, R, kc + KC, min(KC, K - kc - KC), xv);
-        if (tid < R)
-          for (int b = 0; b < kn / QB; ++b) {  // w = (min + centre * scale) + (c - centre) * scale
+        // w = (min + centre * scale) + (c - centre) * scale: warp r adds row r's block terms of this
+        // chunk (lanes strided over the blocks, then a fixed xor tree; every lane ends with the sum)
+        if (warp < R) {
+          float p = 0.f;
+          for (int b = lane; b < kn / QB; b += 32) {
             const float2 q = sSM[kc / QB + b];
-            min_term = fmaf(fmaf(kCentre<BITS>, q.x, q.y), sBS[tid * (KC / QB) + b], min_term);
+            p = fmaf(fmaf(kCentre<BITS>, q.x, q.y), sBS[warp * (KC / QB) + b], p);
           }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+          min_term += p;
+        }
         for (int kb = 0; kb < kn; kb += kTmaTileRows * KT) {
           if (ok) ok = wait_or_abort(full(st), phase, timeout_ns, abort_flag, status, 54);
           ok = __all_sync(0xffffffffu, ok);
@@ -418,7 +428,7 @@ ffn_stream_q_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16
           acc[r][c] = v;
         }
       consumer_sync();  // sRed overlays the activations
-      if (tid < R) sMin[tid] = min_term;
+      if (lane == 0 && warp < R) sMin[warp] = min_term;
       if (lane < LPR) {
         for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -443,24 +453,20 @@ ffn_stream_q_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16
 // The INT4 codes of a 64-column slab arrive by TMA like the tiles above (boxes of 16 KB: 32 k-blocks
 // of 16 k-rows, 512 bytes each, in the fragment layout the quantiser writes), and the dot products
 // run on mma.sync m16n8k16 (bf16 in, fp32 accumulate): A = 16 weight columns x 16 k-rows, decoded from
-// one 32-bit word per lane, B = 16 k-rows x 8 activation rows (tokens) from shared memory, so one
-// instruction does 2048 multiply-adds and a pass takes up to 8 rows at the cost of one. Decoding a
-// register pair is one shift and one LOP3 that puts two nibbles n into the low mantissa bits of bf16
-// 128.0 (128 + n, exact), and one packed bf16 subtraction of 136 that leaves the centred code n - 8
-// (exact). Each warp takes one 64-deep k-block of every box, so its products all share one
-// (scale, min) pair: they accumulate in a block accumulator that is scaled and added once per block.
-// The column-independent term (min + 8 scale) * (sum of the block's activations) is formed once per
-// row from block sums taken while staging, as in the kernel above.
+// one 32-bit word per lane, B = 16 k-rows x 8 activation rows (tokens), so one instruction does 2048
+// multiply-adds and a pass takes up to 8 rows at the cost of one. Decoding a register pair is one
+// shift and one LOP3 that puts two nibbles n into the low mantissa bits of bf16 128.0 (128 + n,
+// exact), and one packed bf16 subtraction of 136 that leaves the centred code n - 8 (exact).
+// Each warp takes one 64-deep k-block of every box. Within a block the code layout numbers k so that
+// the B fragments of lane 4g + t for all four 16-deep steps are the 16 consecutive k-rows 16t .. 16t+15
+// of activation row g: the lane loads them from global memory (two 16-byte loads, one box ahead of
+// use) and no activation is staged in shared memory. The products of a block share one (scale, min)
+// pair: they accumulate in a block accumulator that is scaled and added once per block. The
+// column-independent term (min + 8 scale) * (sum of the block's activations) takes one more MMA per
+// step, with an A fragment of ones, whose result is each row's sum over the step's k-rows.
 constexpr int kQ4Rows = 8;                     // activation rows per pass: the MMA's N
 constexpr int kQ4BoxK16 = kTmaBoxBytes / 512;  // 16-deep k-blocks per box: 32 (512 k-rows)
-constexpr int kQ4StageElems = 8256;            // staged activations (bf16): R rows x (chunk + 8) at most
-constexpr int kQ4MaxChunkBlocks = 128;         // 64-deep blocks of a chunk at most (R * chunk <= 8192)
-
-// k per staged chunk for R rows: as much of K as R rows fit (whole boxes of 512 k-rows when K does not
-// fit), so one or two rows stage all of K = 8192 at once.
-__host__ __device__ constexpr int q4_chunk(int R, int K) {
-  return (kQ4StageElems / R - 8) / 512 * 512 < K ? (kQ4StageElems / R - 8) / 512 * 512 : K;
-}
+constexpr uint32_t kBf16OnePair = 0x3F803F80u;  // bf16 1.0 in both halves
 
 __device__ __forceinline__ uint32_t q4_pair(uint32_t word, int shift) {
   uint32_t r;
@@ -475,9 +481,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void ldmatrix_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
 
 template <int STAGE, typename OutT>
 __global__ void __launch_bounds__(kTmaThreads, 2)
@@ -487,20 +490,15 @@ ffn_stream_q4_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat1
                      int nst, OutT* __restrict__ out, int* status, uint64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   // ring [nst][16 KB] (128-byte aligned) | full [nst], empty [nst] mbarriers in a 128-byte slot |
-  // sX [R][chunk + 8] bf16, kQ4StageElems at most (the epilogue's per-warp sums reuse it) | sSM [K/64]
-  // | sBS [R][chunk / 64] | sMin [kQ4Rows] | sAct [E]. The MMA reads rows R .. 7 from a zero vector.
+  // sRed [kWarps][kQ4Rows][NS] (warp sums) | sMinW [kWarps][kQ4Rows] (warp block-minimum terms) | sAct [E]
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t ring = (raw + 127u) & ~127u;
   uint8_t* gring = smem_raw + (ring - raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(gring + nst * kTmaBoxBytes);
-  __nv_bfloat16* sX = reinterpret_cast<__nv_bfloat16*>(gring + nst * kTmaBoxBytes + kBarSlotBytes);
-  float* sRed = reinterpret_cast<float*>(sX);  // [kWarps][kQ4Rows][NS]
-  float2* sSM = reinterpret_cast<float2*>(sX + kQ4StageElems);
-  float* sBS = reinterpret_cast<float*>(sSM + K / QB);
-  float* sMin = sBS + kQ4MaxChunkBlocks;
-  int* sAct = reinterpret_cast<int*>(sMin + kQ4Rows);
+  float* sRed = reinterpret_cast<float*>(gring + nst * kTmaBoxBytes + kBarSlotBytes);
+  float* sMinW = sRed + kWarps * kQ4Rows * NS;
+  int* sAct = reinterpret_cast<int*>(sMinW + kWarps * kQ4Rows);
   __shared__ int s_nact, s_abort;
-  __shared__ __align__(16) uint4 s_zero;
   volatile int* abort_flag = &s_abort;
   auto full = [&](int st) { return smem_u32(bars + st); };
   auto empty = [&](int st) { return smem_u32(bars + nst + st); };
@@ -512,7 +510,6 @@ ffn_stream_q4_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat1
     }
     fence_mbar_init();
     *abort_flag = 0;
-    s_zero = make_uint4(0u, 0u, 0u, 0u);
     tma_prefetch_desc(&tmC);
   }
   griddep_launch_dependents();
@@ -563,7 +560,8 @@ ffn_stream_q4_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat1
   // Every consumer warp runs the same trip counts, so the named barriers always match; after a
   // failed wait (recorded in the status word) the warps skip the arithmetic and run to the end.
   const int g = lane >> 2, t = lane & 3;
-  const int NB = N / QB;
+  const int NB = N / QB, KQ = K / QB;
+  const uint32_t ones[4] = {kBf16OnePair, kBf16OnePair, kBf16OnePair, kBf16OnePair};
   int st = 0;
   uint32_t phase = 0;
   bool ok = true;
@@ -571,107 +569,104 @@ ffn_stream_q4_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat1
     const int e = sAct[u / nslab];
     const int slab = u % nslab;
     const int n0 = slab * NS;
-    consumer_sync();  // the previous unit is done with sSM
-    for (int b = tid; b < K / QB; b += kThreads) sSM[b] = sm[((size_t)e * (K / QB) + b) * NB + slab];
+    const float2* sm_e = sm + (size_t)e * KQ * NB + slab;  // block b's (scale, min) at sm_e[b * NB]
     const int r_begin = offsets[e], r_end = offsets[e + 1];
     for (int rp = r_begin; rp < r_end; rp += kQ4Rows) {
       const int R = min(kQ4Rows, r_end - rp);
-      const int kcl = q4_chunk(R, K);  // k per staged chunk
-      const int xs = kcl + 8;          // staged row stride (bf16): 16 bytes mod 128, conflict-free ldmatrix
-      // ldmatrix row addresses: lanes 0-7 rows 0-7 at k, lanes 8-15 the same rows at k + 8; rows past R
-      // read the zero vector (and do not move with k)
-      const int xr = lane & 7;
-      const uint32_t x_lane = xr < R ? smem_u32(sX) + (uint32_t)((xr * xs + ((lane >> 3) & 1) * 8) * 2)
-                                     : smem_u32(&s_zero);
-      const uint32_t x_step = xr < R ? 2u : 0u;
+      // lane (g, t) feeds activation row g of the pass (column g of B); rows past R stay zero
+      const __nv_bfloat16* xrow = nullptr;
+      if (g < R) xrow = a + (size_t)(a_rows != nullptr ? a_rows[rp + g] : rp + g) * K + 16 * t;
+      // the B fragments and the (scale, min) pair of this warp's block of the box at k = kb
+      auto fetch = [&](int kb, uint4& x0, uint4& x1, float2& q) {
+        const int kw = kb + warp * QB;
+        x0 = make_uint4(0u, 0u, 0u, 0u);
+        x1 = x0;
+        q = make_float2(0.f, 0.f);
+        if (kw < K) {
+          q = sm_e[(size_t)(kw / QB) * NB];
+          if (xrow != nullptr) {
+            x0 = __ldg(reinterpret_cast<const uint4*>(xrow + kw));
+            x1 = __ldg(reinterpret_cast<const uint4*>(xrow + kw + 8));
+          }
+        }
+      };
       float acc[4][4];
 #pragma unroll
       for (int m = 0; m < 4; ++m)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
-      float min_term = 0.f;  // thread r < R: row r's sum over blocks of (min_b + 8 scale_b) * (sum of a over b)
-      for (int kc = 0; kc < K; kc += kcl) {
-        const int kn = min(kcl, K - kc);  // a multiple of 64
-        consumer_sync();  // sSM is written; the previous chunk's activations (or sums) are read
-        // stage rows rp .. rp+R-1, k in [kc, kc + kn), as bf16, and each row's per-block sums; every
-        // lane of a warp runs the same iterations (the shuffles), groups of 8 lanes share one block
-        const int per_row = kn / 8, total = R * per_row;
-        for (int i0 = 0; i0 < total; i0 += kThreads) {
-          const int i = i0 + tid;
-          const int r = i / per_row, kk = (i % per_row) * 8;
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (i < total) {
-            const size_t src = a_rows != nullptr ? (size_t)a_rows[rp + r] : (size_t)(rp + r);
-            v = __ldg(reinterpret_cast<const uint4*>(a + src * K + kc + kk));
-            *reinterpret_cast<uint4*>(sX + r * xs + kk) = v;
-          }
-          float s8 = bf16lo(v.x) + bf16hi(v.x) + bf16lo(v.y) + bf16hi(v.y) + bf16lo(v.z) + bf16hi(v.z) +
-                     bf16lo(v.w) + bf16hi(v.w);
+      float macc0 = 0.f, macc1 = 0.f;  // rows 2t and 2t + 1: sums of (min + 8 scale) * (block sum of a)
+      uint4 nx0, nx1;
+      float2 nq;
+      fetch(0, nx0, nx1, nq);
+      for (int kb = 0; kb < K; kb += kQ4BoxK16 * 16) {
+        const uint4 x0 = nx0, x1 = nx1;
+        const float2 q = nq;
+        if (kb + kQ4BoxK16 * 16 < K) fetch(kb + kQ4BoxK16 * 16, nx0, nx1, nq);  // in flight during this box
+        if (ok) ok = wait_or_abort(full(st), phase, timeout_ns, abort_flag, status, 56);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok && kb + warp * QB < K) {
+          const uint8_t* box = gring + st * kTmaBoxBytes + warp * 4 * 512 + lane * 16;
+          const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          float blk[4][4], bs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int o = 1; o < 8; o <<= 1) s8 += __shfl_xor_sync(0xffffffffu, s8, o);
-          if ((tid & 7) == 0 && i < total) sBS[r * (kcl / QB) + kk / QB] = s8;
-        }
-        consumer_sync();
-        if (tid < R)
-          for (int b = 0; b < kn / QB; ++b) {  // w = (min + 8 scale) + (code - 8) scale
-            const float2 q = sSM[kc / QB + b];
-            min_term = fmaf(fmaf(8.0f, q.x, q.y), sBS[tid * (kcl / QB) + b], min_term);
-          }
-        for (int kb = 0; kb < kn; kb += kQ4BoxK16 * 16) {
-          if (ok) ok = wait_or_abort(full(st), phase, timeout_ns, abort_flag, status, 56);
-          ok = __all_sync(0xffffffffu, ok);
-          const int kw = kb + warp * QB;  // this warp's 64-deep k-block within the chunk
-          if (ok && kw < kn) {
-            const uint8_t* box = gring + st * kTmaBoxBytes + warp * 4 * 512 + lane * 16;
-            float blk[4][4];
+          for (int m = 0; m < 4; ++m)
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+            for (int i = 0; i < 4; ++i) blk[m][i] = 0.f;
 #pragma unroll
-              for (int i = 0; i < 4; ++i) blk[m][i] = 0.f;
+          for (int j = 0; j < 4; ++j) {
+            const uint4 wd = *reinterpret_cast<const uint4*>(box + j * 512);
+            const uint32_t words[4] = {wd.x, wd.y, wd.z, wd.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint4 wd = *reinterpret_cast<const uint4*>(box + j * 512);
-              uint32_t b0, b1;
-              ldmatrix_x2(x_lane + (uint32_t)(kw + 16 * j) * x_step, b0, b1);
-              const uint32_t words[4] = {wd.x, wd.y, wd.z, wd.w};
-#pragma unroll
-              for (int m = 0; m < 4; ++m) {
-                const uint32_t af[4] = {q4_pair(words[m], 0), q4_pair(words[m], 4), q4_pair(words[m], 8),
-                                        q4_pair(words[m], 12)};
-                mma_bf16_16816(blk[m], af, b0, b1);
-              }
+            for (int m = 0; m < 4; ++m) {
+              const uint32_t af[4] = {q4_pair(words[m], 0), q4_pair(words[m], 4), q4_pair(words[m], 8),
+                                      q4_pair(words[m], 12)};
+              mma_bf16_16816(blk[m], af, xb[2 * j], xb[2 * j + 1]);
             }
-            const float sc = sSM[(kc + kw) / QB].x;
-#pragma unroll
-            for (int m = 0; m < 4; ++m)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) acc[m][i] = fmaf(sc, blk[m][i], acc[m][i]);
+            mma_bf16_16816(bs, ones, xb[2 * j], xb[2 * j + 1]);  // bs[0], bs[1]: rows 2t, 2t+1
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty(st));  // the box's slot goes back to the producer
-          if (++st == nst) { st = 0; phase ^= 1u; }
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[m][i] = fmaf(q.x, blk[m][i], acc[m][i]);
+          const float mq = fmaf(8.0f, q.x, q.y);  // w = (min + 8 scale) + (code - 8) scale
+          macc0 = fmaf(mq, bs[0], macc0);
+          macc1 = fmaf(mq, bs[1], macc1);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(st));  // the box's slot goes back to the producer
+        if (++st == nst) { st = 0; phase ^= 1u; }
       }
-      // Warp sums to shared memory ([warp][row][column]), then every (row, column) adds the warps in a
-      // fixed order and the row's block-minimum term. acc[m]: columns 16m + g (0, 1) and 16m + g + 8
-      // (2, 3), rows 2t and 2t + 1.
-      consumer_sync();  // sRed overlays the activations
-      if (tid < R) sMin[tid] = min_term;
+      // Warp sums to shared memory ([warp][row][column], and the block-minimum terms [warp][row]),
+      // then every (row, column) adds the warps in a fixed order. acc[m]: columns 16m + g (0, 1) and
+      // 16m + g + 8 (2, 3), rows 2t and 2t + 1.
+      consumer_sync();  // the previous pass's sums have been read
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const int c = 16 * m + g;
-        sRed[(warp * kQ4Rows + 2 * t) * NS + c] = acc[m][0];
-        sRed[(warp * kQ4Rows + 2 * t + 1) * NS + c] = acc[m][1];
-        sRed[(warp * kQ4Rows + 2 * t) * NS + c + 8] = acc[m][2];
-        sRed[(warp * kQ4Rows + 2 * t + 1) * NS + c + 8] = acc[m][3];
+        if (2 * t < R) {
+          sRed[(warp * kQ4Rows + 2 * t) * NS + c] = acc[m][0];
+          sRed[(warp * kQ4Rows + 2 * t) * NS + c + 8] = acc[m][2];
+        }
+        if (2 * t + 1 < R) {
+          sRed[(warp * kQ4Rows + 2 * t + 1) * NS + c] = acc[m][1];
+          sRed[(warp * kQ4Rows + 2 * t + 1) * NS + c + 8] = acc[m][3];
+        }
+      }
+      if (g == 0) {
+        if (2 * t < R) sMinW[warp * kQ4Rows + 2 * t] = macc0;
+        if (2 * t + 1 < R) sMinW[warp * kQ4Rows + 2 * t + 1] = macc1;
       }
       consumer_sync();
       for (int i = tid; i < R * NS; i += kThreads) {
         const int r = i / NS, c = i % NS;
-        float v = 0.f;
+        float v = 0.f, mt = 0.f;
 #pragma unroll
-        for (int wi = 0; wi < kWarps; ++wi) v += sRed[(wi * kQ4Rows + r) * NS + c];
-        v += sMin[r];
+        for (int wi = 0; wi < kWarps; ++wi) {
+          v += sRed[(wi * kQ4Rows + r) * NS + c];
+          mt += sMinW[wi * kQ4Rows + r];
+        }
+        v += mt;
         const int grow = rp + r;
         v = STAGE == 1 ? gelu_as(v) : row_gate[grow] * v;
         out[(size_t)grow * N + n0 + c] = from_f32<OutT>(v);
@@ -680,20 +675,18 @@ ffn_stream_q4_kernel(const __grid_constant__ CUtensorMap tmC, const __nv_bfloat1
   }
 }
 
-size_t q4_smem_bytes(int nst, int K, int E) {
-  return 128 + (size_t)nst * kTmaBoxBytes + kBarSlotBytes + (size_t)kQ4StageElems * 2 +
-         (size_t)(K / QB) * sizeof(float2) + (size_t)(kQ4MaxChunkBlocks + kQ4Rows) * sizeof(float) + (size_t)E * 4;
+size_t q4_smem_bytes(int nst, int E) {
+  return 128 + (size_t)nst * kTmaBoxBytes + kBarSlotBytes + (size_t)kWarps * kQ4Rows * (NS + 1) * sizeof(float) +
+         (size_t)E * 4;
 }
-static_assert(kWarps * kQ4Rows * NS * 4 <= kQ4StageElems * 2, "the warp sums fit the staging buffer");
-static_assert(kQ4StageElems / 1 - 8 >= 8192 && 8 * (1024 + 8) <= kQ4StageElems, "chunk sizes fit the buffer");
 
 constexpr size_t kSmPerSmBytes = 228 * 1024;  // shared memory per SM, of which 1 KB per resident CTA is reserved
 
 template <int STAGE, typename OutT>
 cudaError_t launch_q4(const QFfnArgs& p, EncodeTiledFn enc, cudaStream_t s) {
   int nst = kTmaStages;
-  while (nst > 2 && 2 * (q4_smem_bytes(nst, p.K, p.E) + 1024) > kSmPerSmBytes) --nst;
-  const size_t smem = q4_smem_bytes(nst, p.K, p.E);
+  while (nst > 2 && 2 * (q4_smem_bytes(nst, p.E) + 64 + 1024) > kSmPerSmBytes) --nst;
+  const size_t smem = q4_smem_bytes(nst, p.E);
   auto kern = ffn_stream_q4_kernel<STAGE, OutT>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;

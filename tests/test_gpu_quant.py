@@ -19,10 +19,10 @@ BF16, F32 = ig.DTYPE_BF16, ig.DTYPE_F32
 def unpack_codes(raw, E, K, N, bits):
     """Device code format -> codes [E, K, N].
 
-    INT4: per expert [N/64 slabs][K/16 k-blocks][32 lanes][4 words]; lane 4g + t, word m covers
-    columns c0 = 16m + g and c1 = c0 + 8 at k-rows 2t, 2t+1, 2t+8, 2t+9 of the k-block, nibble i
-    (bits 4i..4i+3) holding (k, column) = (2t, c0), (2t, c1), (2t+8, c0), (2t+8, c1), (2t+1, c0),
-    (2t+1, c1), (2t+9, c0), (2t+9, c1) for i = 0..7.
+    INT4: per expert [N/64 slabs][K/16 k-blocks][32 lanes][4 words]; k-block 4b + j is step j of the
+    64-deep block b; lane 4g + t, word m covers columns c0 = 16m + g and c1 = c0 + 8 at k-rows
+    kp .. kp+3 with kp = 64b + 16t + 4j, nibble i (bits 4i..4i+3) holding (k, column) = (kp, c0),
+    (kp, c1), (kp+2, c0), (kp+2, c1), (kp+1, c0), (kp+1, c1), (kp+3, c0), (kp+3, c1) for i = 0..7.
     INT8: 16-byte tiles of 8 columns by 2 k-rows, row-major over (k / 2, n / 8); half j is k-row j."""
     codes = np.zeros((E, K, N), np.uint8)
     if bits == 4:
@@ -32,8 +32,8 @@ def unpack_codes(raw, E, K, N, bits):
         slab = np.arange(N // 64)[:, None, None]
         k16 = np.arange(K // 16)[None, :, None]
         for m in range(4):
-            for i, (dk, dc) in enumerate([(0, 0), (0, 8), (8, 0), (8, 8), (1, 0), (1, 8), (9, 0), (9, 8)]):
-                k = k16 * 16 + (2 * t + dk)[None, None, :]
+            for i, (dk, dc) in enumerate([(0, 0), (0, 8), (2, 0), (2, 8), (1, 0), (1, 8), (3, 0), (3, 8)]):
+                k = (k16 // 4) * 64 + 4 * (k16 % 4) + (16 * t + dk)[None, None, :]
                 c = slab * 64 + (16 * m + g + dc)[None, None, :]
                 codes[:, k, c] = (words[..., m] >> (4 * i)) & 0xF
     else:
