@@ -48,6 +48,10 @@ constexpr int CR = 32;                            // rows per epilogue step (one
 constexpr int kStgBytes = CR * 32 * 2;            // per epilogue warp (up): 32 rows x 32 bf16 features
 constexpr uint32_t kTmemCols = 2 * BR;            // two accumulators of up to 256 columns
 constexpr int kMaxSmem = 232448;
+// Row tiles per band of a heavy expert's down-projection items. The down-projection's rows (h, 4 MB
+// per row tile at d_ff = 8192) are reread by every feature block; banding keeps a band's rows in L2
+// across them. skew_e128 down: 1968-2001 -> 1946-1947 us (bands of 4: 1951-1968).
+constexpr int kHeavyBandDown = 8;
 
 // The item ring: the leader's producer publishes each item index it takes; the MMA issuer, both
 // CTAs' epilogue warps and the peer's producer read it from there (kItemSlots deep).
@@ -178,6 +182,8 @@ struct Item {
 // in proportion to their item counts instead (item w is heavy when floor((w+1) nH / n) >
 // floor(w nH / n)), so the items in flight hold a mix of both. Within a class, items go by expert,
 // then feature block, then row tile (fastest): the pairs that run together share a weight slab.
+// With band > 0 a heavy expert's items go by band of `band` row tiles first (the down-projection,
+// whose row tiles are as large as its weight slabs).
 // Both classes share one limit, the rate at which each SM's TMA fills its shared-memory ring (about
 // 80 GB/s per SM in every mix measured), so they overlap only a little. When both are present (a
 // skewed batch) the items come from a workspace counter through an item ring, so that the items in
@@ -191,7 +197,8 @@ struct Item {
 // PH / PL: per-expert prefix sums of the row tiles of the heavy / light experts (the other class
 // counts zero tiles).
 __device__ __forceinline__ Item decode_item(int w, const int* PH, const int* PL, int E, int NB,
-                                            const int32_t* offsets, int balanced, long long nH, long long n) {
+                                            const int32_t* offsets, int balanced, int band, long long nH,
+                                            long long n) {
   long long before;  // heavy items listed before w
   bool heavy;
   if (nH == 0 || nH == n) {  // one class: the list in expert order, no division
@@ -210,7 +217,13 @@ __device__ __forceinline__ Item decode_item(int w, const int* PH, const int* PL,
   }
   const int e = lo;
   const int mt = P[e + 1] - P[e];
-  const int r = i - P[e] * NB;
+  int r = i - P[e] * NB;  // item within the expert: row tile r % mt of feature block r / mt
+  if (heavy && band > 0 && mt > band) {
+    // bands of `band` row tiles: within a band, every feature block meets each of the band's row
+    // tiles before the next band starts, so the band's rows stay in L2 across the feature blocks
+    const int b = r / (band * NB), nr = min(band, mt - b * band), j = r - b * band * NB;
+    r = (j / nr) * mt + b * band + j % nr;
+  }
   const int cnt = offsets[e + 1] - offsets[e];
   int rte = BR;
   if (balanced) {
@@ -239,7 +252,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                const __grid_constant__ CUtensorMap tmH, typename EpiOut<STAGE>::T* __restrict__ out,
                const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
-               int balanced, int heavy_rows, int a_one_box, int l2_hints, int* sched, int* status,
+               int balanced, int heavy_rows, int heavy_band, int a_one_box, int l2_hints, int* sched, int* status,
                uint64_t timeout_ns) {
   using OutT = typename EpiOut<STAGE>::T;
   constexpr int kTileABytes_ = kTileABytes<KSUB>, kTileASubBytes_ = kTileASubBytes<KSUB>;
@@ -369,7 +382,7 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
           if (++iq == kItemSlots) { iq = 0; iphase ^= 1u; }
           if (w >= total_items) break;
         }
-        const Item it = decode_item(w, PH, PL, E, NB, offsets, balanced, n_heavy, n_items);
+        const Item it = decode_item(w, PH, PL, E, NB, offsets, balanced, heavy_band, n_heavy, n_items);
         const int nt = (it.nrows + 15) & ~15;           // MMA N: rows rounded up to 16
         const int frow = it.row0 + (nt / 2) * (int)rank;  // this CTA holds rows [nt/2 * rank, +nt/2)
         const int feat = it.f0 + (BF / 2) * (int)rank;
@@ -436,7 +449,7 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             w += npairs;
           }
           if (w >= total_items) break;
-          const Item it = decode_item(w, PH, PL, E, NB, offsets, balanced, n_heavy, n_items);
+          const Item it = decode_item(w, PH, PL, E, NB, offsets, balanced, heavy_band, n_heavy, n_items);
           const uint32_t idesc = idesc_tn(BF, (it.nrows + 15) & ~15);
           if (!wait_or_abort(bar(TEMPTY + acc), acc_phase ^ 1u, timeout_ns, abort_flag, status, 42)) break;
           tc_fence_after();
@@ -486,7 +499,7 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         w += npairs;
       }
       if (w >= total_items) break;
-      const Item it = decode_item(w, PH, PL, E, NB, offsets, balanced, n_heavy, n_items);
+      const Item it = decode_item(w, PH, PL, E, NB, offsets, balanced, heavy_band, n_heavy, n_items);
       // warp-uniform: the TMEM loads below are warp-collective
       if (!__all_sync(0xffffffffu, wait_or_abort(bar(TFULL + acc), acc_phase, timeout_ns, abort_flag, status, 43)))
         break;
@@ -617,9 +630,10 @@ cudaError_t launch_tct(const FfnArgs& p, EncodeTiledFn enc, const CUtensorMap& t
   // Item counter (and the count of pairs done with it) in workspace header words 4 and 5.
   int* sched = p.status != nullptr ? p.status + 4 : nullptr;
   const int l2_hints = 1;  // skew_e128 up: DRAM reads 10.17 -> 9.16 GB per launch (8.87 GB algorithmic)
+  const int heavy_band = STAGE == 2 ? kHeavyBandDown : 0;
   return launch_pdl(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), smem, s, tmX, tmW, tmH, (OutT*)p.out,
-                    p.offsets, p.row_gate, p.K, p.N, p.E, balanced, heavy_rows, a_one_box, l2_hints, sched,
-                    p.status, p.timeout_ns);
+                    p.offsets, p.row_gate, p.K, p.N, p.E, balanced, heavy_rows, heavy_band, a_one_box, l2_hints,
+                    sched, p.status, p.timeout_ns);
 }
 
 }  // namespace
@@ -629,13 +643,17 @@ cudaError_t launch_ffn_tensor_t(const FfnArgs& p, cudaStream_t s) {
   if (p.dt != MOE_DTYPE_BF16) return cudaErrorNotSupported;
   EncodeTiledFn enc = tensor_map_encoder();
   if (enc == nullptr) return cudaErrorNotSupported;
-  // Two k-blocks per stage (64 KB, three stages) when K allows it and each weight slab serves about
-  // two or more row tiles, i.e. is mostly read from L2: fewer, larger copies per MMA (e16 up:
-  // 73.7 -> 70.6 us). When every slab streams from HBM once (prefill), six or seven 32 KB stages
-  // hide HBM latency better (1.34 vs 1.35 ms).
+  // Two k-blocks per stage (64 KB, three stages) when K allows it and the weight slabs serve
+  // several row tiles, i.e. are mostly read from L2: fewer, larger copies per MMA (e16 up:
+  // 73.7 -> 70.6 us). For the up-projection three 64 KB stages hold as many bytes in flight as its
+  // six 32 KB ones (the output staging takes the rest), and an average of one full row tile per
+  // expert suffices (skew_e128 up: 2057-2101 -> 1992-1999 us); the down-projection would give up
+  // its seventh 32 KB stage, and takes them only at two row tiles per expert (skew_e128 down with
+  // three 64 KB stages: 1953-1975 -> 2027 us). When every slab streams from HBM once (prefill),
+  // six or seven 32 KB stages hide HBM latency better (1.34 vs 1.35 ms).
   const long long active = p.rows < p.E ? p.rows : p.E;
   const long long rpe = (p.rows + active - 1) / active;
-  const bool ksub2_ok = p.K % 128 == 0 && rpe >= 2 * BR;
+  const bool ksub2_ok = p.K % 128 == 0 && rpe >= (p.stage == 1 ? BR : 2 * BR);
   CUtensorMap tmH{};  // up: h [rows][N] bf16, 32 features x CR rows per store, no swizzle
   if (p.stage == 1) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.rows};
