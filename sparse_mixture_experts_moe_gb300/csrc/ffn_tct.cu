@@ -48,6 +48,15 @@ constexpr int CR = 32;                            // rows per epilogue step (one
 constexpr int kStgBytes = CR * 32 * 2;            // per epilogue warp (up): 32 rows x 32 bf16 features
 constexpr uint32_t kTmemCols = 2 * BR;            // two accumulators of up to 256 columns
 constexpr int kMaxSmem = 232448;
+// The rows operand comes in boxes sized to the item: a CTA's half of an item of nt rows (nt / 2, a
+// multiple of 8) is copied by the smallest box of 16, 32, ..., 128 rows that covers it, one tensor
+// map per height. Fewer bytes per stage for the light experts' items (about 84 rows on skew_e128):
+// skew_e128 up 2000-2009 -> 1960 us, down 1983-2006 -> 1952 us; e16 and prefill unchanged.
+constexpr int kBoxMaps = BR / 2 / 16;
+struct BoxMaps {
+  CUtensorMap m[kBoxMaps];
+};
+__host__ __device__ constexpr int box_rows_for(int nt) { return ((nt / 2 + 15) / 16) * 16; }
 // Row tiles per band of a heavy expert's down-projection items. The down-projection's rows (h, 4 MB
 // per row tile at d_ff = 8192) are reread by every feature block; banding keeps a band's rows in L2
 // across them. skew_e128 down: 1968-2001 -> 1946-1947 us (bands of 4: 1951-1968).
@@ -140,13 +149,6 @@ __device__ __forceinline__ void tma_load_4d_pair_hint(uint32_t dst, const void* 
       "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
       "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void* tmap, int c0, int c1, int c2,
-                                                      uint32_t bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ uint64_t policy_evict_last() {
@@ -246,10 +248,11 @@ struct EpiOut<2> { using T = float; };
 
 // tmW: with a_one_box, the weights as [E][N/64][K][64] (4D: one box is this CTA's two 64-feature
 // atoms of KSUB k-blocks, a single copy); otherwise [E][K][N] (3D: one box per atom and k-block).
-// tmX: KSUB = 1, x rows as [rows][K] (2D); KSUB = 2, as [K/64][rows][64] (3D: both k-blocks at once).
+// tmXs: KSUB = 1, x rows as [rows][K] (2D); KSUB = 2, as [K/64][rows][64] (3D: both k-blocks at once,
+// the second box_rows rows after the first); map i copies 16 (i + 1) rows.
 template <int STAGE, int STAGES, int KSUB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+ffn_tct_kernel(const __grid_constant__ BoxMaps tmXs, const __grid_constant__ CUtensorMap tmW,
                const __grid_constant__ CUtensorMap tmH, typename EpiOut<STAGE>::T* __restrict__ out,
                const int32_t* __restrict__ offsets, const float* __restrict__ row_gate, int K, int N, int E,
                int balanced, int heavy_rows, int heavy_band, int a_one_box, int l2_hints, int* sched, int* status,
@@ -286,7 +289,7 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     for (int q = 0; q < kItemSlots; ++q) { mbar_init(bar(IFULL + q), 1); mbar_init(bar(IEMPTY + q), kItemReaders); }
     fence_mbar_init();
     *abort_flag = 0;
-    tma_prefetch_desc(&tmX);
+    for (int i = 0; i < kBoxMaps; ++i) tma_prefetch_desc(&tmXs.m[i]);
     tma_prefetch_desc(&tmW);
     if (STAGE == 1) tma_prefetch_desc(&tmH);
   }
@@ -386,10 +389,13 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int nt = (it.nrows + 15) & ~15;           // MMA N: rows rounded up to 16
         const int frow = it.row0 + (nt / 2) * (int)rank;  // this CTA holds rows [nt/2 * rank, +nt/2)
         const int feat = it.f0 + (BF / 2) * (int)rank;
+        const int hbox = box_rows_for(nt);
+        const CUtensorMap* tmX = &tmXs.m[hbox / 16 - 1];
+        const uint32_t stage_tx = 2u * (uint32_t)(kTileABytes_ + hbox * 128 * KSUB);  // both CTAs' bytes
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_or_abort(bar(EMPTY + stage), phase ^ 1u, timeout_ns, abort_flag, status, 41)) goto producer_out;
           const uint32_t full_leader = map_to_cta(bar(FULL + stage), 0);
-          if (leader) mbar_arrive_expect_tx(bar(FULL + stage), 2 * kStageBytes_);  // both CTAs' bytes
+          if (leader) mbar_arrive_expect_tx(bar(FULL + stage), stage_tx);
           if (a_one_box && l2_hints && mixed) {
             // a heavy expert's slab is read by every row tile of the expert: keep it in L2 ahead of
             // the light experts' slabs, which nothing reads twice
@@ -405,8 +411,8 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 tma_load_3d_pair(sA + stage * kTileABytes_ + j * kTileASubBytes_ + u * BK * 128, &tmW, feat + 64 * j,
                                  (kb * KSUB + u) * BK, it.e, full_leader);
           }
-          if (KSUB == 1) tma_load_2d_pair(sB + stage * kTileBBytes_, &tmX, kb * BK, frow, full_leader);
-          else tma_load_3d_pair(sB + stage * kTileBBytes_, &tmX, 0, frow, kb * KSUB, full_leader);
+          if (KSUB == 1) tma_load_2d_pair(sB + stage * kTileBBytes_, tmX, kb * BK, frow, full_leader);
+          else tma_load_3d_pair(sB + stage * kTileBBytes_, tmX, 0, frow, kb * KSUB, full_leader);
           filled |= 1u << stage;
           fill_phase = (fill_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -451,6 +457,7 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
           if (w >= total_items) break;
           const Item it = decode_item(w, PH, PL, E, NB, offsets, balanced, heavy_band, n_heavy, n_items);
           const uint32_t idesc = idesc_tn(BF, (it.nrows + 15) & ~15);
+          const uint32_t b_step = (uint32_t)box_rows_for((it.nrows + 15) & ~15) * 128;  // 64 k of B, KSUB = 2
           if (!wait_or_abort(bar(TEMPTY + acc), acc_phase ^ 1u, timeout_ns, abort_flag, status, 42)) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BR);
@@ -458,12 +465,12 @@ ffn_tct_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             if (!wait_or_abort(bar(FULL + stage), phase, timeout_ns, abort_flag, status, 42)) goto mma_out;
             tc_fence_after();
             // A: MN-major, two 64-feature atoms kTileASubBytes apart, 128 bytes per k; B: K-major
-            // rows, one 16 KB block per 64 k.
+            // rows, one block of the item's box rows per 64 k.
             const uint64_t a_desc = make_smem_desc_sw128(sA + stage * kTileABytes_, kTileASubBytes_, 1024);
 #pragma unroll
             for (int kk = 0; kk < KSUB * BK / 16; ++kk) {
               const uint64_t b_desc =
-                  make_smem_desc_sw128(sB + stage * kTileBBytes_ + (kk / 4) * (kTileBBytes_ / KSUB), 16, 1024);
+                  make_smem_desc_sw128(sB + stage * kTileBBytes_ + (kk / 4) * b_step, 16, 1024);
               tc_mma_f16_pair(d_tmem, a_desc + (uint64_t)((kk * 16 * 128) >> 4),
                               b_desc + (uint64_t)(((kk % 4) * 32) >> 4), idesc, (kb | kk) != 0 ? 1u : 0u);
             }
@@ -594,7 +601,8 @@ cudaError_t launch_tct(const FfnArgs& p, EncodeTiledFn enc, const CUtensorMap& t
   const long long active = p.rows < p.E ? p.rows : p.E;
   const long long rpe = (p.rows + active - 1) / active;
   const int balanced = active * ((rpe + BR - 1) / BR) * NB >= 3LL * clusters ? 0 : 1;
-  CUtensorMap tmW, tmX;
+  CUtensorMap tmW;
+  BoxMaps tmXs;
   // Weights [E][K][N], MN-major A operand. N a multiple of 64: viewed as [E][N/64][K][64] so one
   // box brings both of this CTA's 64-feature atoms (the fewer copies a stage takes, the faster the
   // SM's copy engine feeds it); otherwise one [KSUB*64 k][64 f] box per atom and k-block.
@@ -610,18 +618,23 @@ cudaError_t launch_tct(const FfnArgs& p, EncodeTiledFn enc, const CUtensorMap& t
     const cuuint32_t box[3] = {64, BK, 1};
     if (!encode_sw128(enc, &tmW, p.w, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
-  // Rows of x_perm (or h): K-major B operand, 128 rows (one CTA's half of a tile) per box: a
-  // [rows][K] view for one k-block, a [K/64][rows][64] view (K a multiple of 128) for two.
-  if (KSUB == 1) {
-    const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.rows};
-    const cuuint64_t str[1] = {(cuuint64_t)p.K * 2};
-    const cuuint32_t box[2] = {BK, BR / 2};
-    if (!encode_sw128(enc, &tmX, p.a, 2, dims, str, box)) return cudaErrorInvalidValue;
-  } else {
-    const cuuint64_t dims[3] = {64, (cuuint64_t)p.rows, (cuuint64_t)p.K / 64};
-    const cuuint64_t str[2] = {(cuuint64_t)p.K * 2, 128};
-    const cuuint32_t box[3] = {64, BR / 2, KSUB};
-    if (!encode_sw128(enc, &tmX, p.a, 3, dims, str, box)) return cudaErrorInvalidValue;
+  // Rows of x_perm (or h): K-major B operand, up to 128 rows (one CTA's half of a tile) per box: a
+  // [rows][K] view for one k-block, a [K/64][rows][64] view (K a multiple of 128) for two; one map per
+  // box height 16, 32, ..., 128. A stage copies only the rows its item has (rounded up to 16): an
+  // item of 84 rows copies 48 rows per CTA, not 128.
+  for (int i = 0; i < kBoxMaps; ++i) {
+    const cuuint32_t hrows = 16u * (cuuint32_t)(i + 1);
+    if (KSUB == 1) {
+      const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.rows};
+      const cuuint64_t str[1] = {(cuuint64_t)p.K * 2};
+      const cuuint32_t box[2] = {BK, hrows};
+      if (!encode_sw128(enc, &tmXs.m[i], p.a, 2, dims, str, box)) return cudaErrorInvalidValue;
+    } else {
+      const cuuint64_t dims[3] = {64, (cuuint64_t)p.rows, (cuuint64_t)p.K / 64};
+      const cuuint64_t str[2] = {(cuuint64_t)p.K * 2, 128};
+      const cuuint32_t box[3] = {64, hrows, KSUB};
+      if (!encode_sw128(enc, &tmXs.m[i], p.a, 3, dims, str, box)) return cudaErrorInvalidValue;
+    }
   }
   const long long max_items = ((long long)(p.rows + BR - 1) / BR + p.E) * NB;
   long long pairs = clusters < max_items ? clusters : max_items;
@@ -631,7 +644,7 @@ cudaError_t launch_tct(const FfnArgs& p, EncodeTiledFn enc, const CUtensorMap& t
   int* sched = p.status != nullptr ? p.status + 4 : nullptr;
   const int l2_hints = 1;  // skew_e128 up: DRAM reads 10.17 -> 9.16 GB per launch (8.87 GB algorithmic)
   const int heavy_band = STAGE == 2 ? kHeavyBandDown : 0;
-  return launch_pdl(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), smem, s, tmX, tmW, tmH, (OutT*)p.out,
+  return launch_pdl(kern, dim3((unsigned)(2 * pairs)), dim3(kThreads), smem, s, tmXs, tmW, tmH, (OutT*)p.out,
                     p.offsets, p.row_gate, p.K, p.N, p.E, balanced, heavy_rows, heavy_band, a_one_box, l2_hints,
                     sched, p.status, p.timeout_ns);
 }
