@@ -461,19 +461,21 @@ ffn_tct_kernel(const __grid_constant__ BoxMaps tmXs, const __grid_constant__ CUt
           if (!wait_or_abort(bar(TEMPTY + acc), acc_phase ^ 1u, timeout_ns, abort_flag, status, 42)) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BR);
+          const uint64_t a_base = make_smem_desc_sw128(sA, kTileASubBytes_, 1024);
+          const uint64_t b_base = make_smem_desc_sw128(sB, 16, 1024);
+          const uint64_t b_hi = (uint64_t)(b_step >> 4);
           for (int kb = 0; kb < KB; ++kb) {
+            // descriptors ready before the wait, so that the MMAs issue as soon as the stage lands (the
+            // address field moves by the stage's offset >> 4; skew_e128 down 1976-1988 -> 1919-1931 us)
+            const uint64_t a_desc = a_base + (uint64_t)((stage * kTileABytes_) >> 4);
+            const uint64_t b_desc = b_base + (uint64_t)((stage * kTileBBytes_) >> 4);
             if (!wait_or_abort(bar(FULL + stage), phase, timeout_ns, abort_flag, status, 42)) goto mma_out;
             tc_fence_after();
-            // A: MN-major, two 64-feature atoms kTileASubBytes apart, 128 bytes per k; B: K-major
-            // rows, one block of the item's box rows per 64 k.
-            const uint64_t a_desc = make_smem_desc_sw128(sA + stage * kTileABytes_, kTileASubBytes_, 1024);
 #pragma unroll
-            for (int kk = 0; kk < KSUB * BK / 16; ++kk) {
-              const uint64_t b_desc =
-                  make_smem_desc_sw128(sB + stage * kTileBBytes_ + (kk / 4) * b_step, 16, 1024);
+            for (int kk = 0; kk < KSUB * BK / 16; ++kk)
               tc_mma_f16_pair(d_tmem, a_desc + (uint64_t)((kk * 16 * 128) >> 4),
-                              b_desc + (uint64_t)(((kk % 4) * 32) >> 4), idesc, (kb | kk) != 0 ? 1u : 0u);
-            }
+                              b_desc + (kk / 4) * b_hi + (uint64_t)(((kk % 4) * 32) >> 4), idesc,
+                              (kb | kk) != 0 ? 1u : 0u);
             tc_commit_pair(bar(EMPTY + stage), 0x3);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }

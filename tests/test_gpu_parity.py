@@ -279,6 +279,33 @@ def test_expert_gemms_mixed_routing(T, F):
     assert hdr[4] == 0 and hdr[5] == 0  # item counter and finished pairs back at zero
 
 
+@pytest.mark.parametrize("d,F", [(256, 512), (192, 320)])
+def test_expert_gemms_given_row_counts(d, F):
+    """The pair GEMM on given per-expert row counts: heavy experts with full 256-row tiles and ragged
+    last tiles (600 = 256 + 256 + 88, 777 = 3 x 256 + 9, 300 = 256 + 44), an exact multiple (1024), a
+    light expert and an empty one, in one launch (both classes: the counter and the item ring).
+    x_perm is the case's token rows in order (k = 1); h and y_perm against the oracle."""
+    counts = np.array([600, 1024, 300, 40, 0, 777])
+    E, A = len(counts), int(counts.sum())
+    c = make_case(T=A, d=d, F=F, E=E, k=1, dt=BF16)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    offsets = torch.from_numpy(offs).to(DEV)
+    gate = np.random.default_rng(7).uniform(0.0, 1.0, A).astype(np.float32)
+    row_gate = torch.from_numpy(gate).to(DEV)
+    ws = guarded_workspace(c)
+    hg = Guarded((A, F), torch.bfloat16, fill=0)
+    moe.expert_up(c.x, c.w1, offsets, A, d, F, E, 1, BF16, hg.t, ws.t, path=moe.PATH_TENSOR_T)
+    assert moe.get_device_status(ws.t)[0] == moe.MOE_OK
+    assert hg.intact() and ws.intact()
+    assert_rounded_once(to_f64(hg.t), oracle.expert_rows_up(c.x64, offs, c.w1_host()), BF16)
+    yg = Guarded((A, d), torch.float32, fill=0)
+    moe.expert_down(hg.t, c.w2, offsets, row_gate, A, d, F, E, 1, BF16, yg.t, ws.t, path=moe.PATH_TENSOR_T)
+    assert moe.get_device_status(ws.t)[0] == moe.MOE_OK
+    assert yg.intact() and ws.intact()
+    yref = oracle.expert_rows_down(to_f64(hg.t), offs, gate, c.w2_host())
+    assert rel_rms_err(to_f64(yg.t), yref) < 1e-4
+
+
 @pytest.mark.parametrize("dt", [BF16, F32])
 def test_combine(dt):
     T, d, k = 333, 136, 3
