@@ -351,7 +351,9 @@ def dominant_roofline(w, kern_ms, touched, fpath, qbits, peaks, peak_src):
                 "traffic": stored_traffic(f"{kname}<{1 if dom == 'expert_up' else 2}>", w.name,
                                           TCT_SOURCES if kname == "ffn_tct_kernel" else TC_SOURCES),
                 "alg_flops_per_launch": alg_flops, "ms_per_launch": kern_ms[dom],
-                "peak_source": f"{peak_src} bf16_tflops (burst: the kernel runs in a short step)"}
+                "peak_source": f"{peak_src} bf16_tflops (burst: the kernel runs in a short step)",
+                # context: the measured bf16 matmul rate held for seconds at the power limit
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
     return roof
 
 
