@@ -80,6 +80,29 @@ uint64_t wait_timeout_ns() {
 
 inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// The TMA-fed kernels' tensor maps are built by the driver's cuTensorMapEncodeTiled, which needs a
+// context current on the calling host thread. The runtime makes the device's primary context current
+// on a thread only at the thread's first runtime call that needs one, so a thread whose first CUDA
+// work is one of these entry points would encode without a context, and the encode fails. Called
+// after validation and before the first launch of every entry point that may encode: when no
+// context is current, it selects the thread's current device, which makes its primary context
+// current. (cuCtxGetCurrent is a thread-local lookup; nothing else runs when a context is current.)
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+void bind_primary_context() {
+  static const CtxGetCurrentFn get = []() -> CtxGetCurrentFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  CUcontext cur = nullptr;
+  if (get != nullptr && get(&cur) == CUDA_SUCCESS && cur != nullptr) return;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) (void)cudaSetDevice(dev);
+}
+
 template <typename P>
 inline P* at(void* ws, size_t off) { return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off); }
 
@@ -120,6 +143,7 @@ moe_status run_ffn_half(moe_path path, FfnArgs& args, cudaStream_t s) {
        path == MOE_PATH_TENSOR_T) &&
       args.dt != MOE_DTYPE_BF16)
     return MOE_ERR_UNSUPPORTED;
+  bind_primary_context();
   cudaError_t e;
   switch (path) {
     case MOE_PATH_TENSOR: e = launch_ffn_tensor(args, s); break;
@@ -189,6 +213,7 @@ moe_status moe_router_topk_stats(const void* x, const void* w_r, const float* b_
   if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_INVALID_ARG;
   // header words: [0] status, [1] detail, [3] the statistics ticket
   const RouterStats st{at<float>(workspace, Layout(T, d, 8, E, k, dt).stats_part), stats, at<int>(workspace, 0) + 3};
+  bind_primary_context();
   return cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, flags, st, topk_idx, topk_gate,
                                         at<int>(workspace, 0), wait_timeout_ns(), (cudaStream_t)stream));
 }
@@ -199,6 +224,7 @@ moe_status moe_router_topk_ex(const void* x, const void* w_r, const float* b_r, 
   if (T == 0) return MOE_OK;
   if (x == nullptr || w_r == nullptr || topk_idx == nullptr || topk_gate == nullptr) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_INVALID_ARG;
+  bind_primary_context();
   return cuda_status(launch_router_topk(x, w_r, b_r, T, d, E, k, dt, flags, RouterStats{nullptr, nullptr, nullptr},
                                         topk_idx, topk_gate, nullptr, wait_timeout_ns(), (cudaStream_t)stream));
 }
@@ -340,6 +366,7 @@ moe_status expert_half_q(int stage, const void* a, const void* codes, const floa
   if (!aligned16(a) || !aligned16(codes) || !aligned8(scale_min) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   QFfnArgs p{a, codes, scale_min, offsets, row_gate, out, T * k, K, N, E, bits, stage, a_rows, T, status,
              wait_timeout_ns()};
+  bind_primary_context();
   return cuda_status(launch_ffn_stream_q(p, (cudaStream_t)stream));
 }
 }  // namespace
@@ -409,6 +436,7 @@ moe_status route_and_dispatch(const void* x, const void* w_r, const float* b_r, 
                               const Layout& L, void* workspace, size_t ws_bytes, void* stream, bool small_ok,
                               bool* rows_via_perm) {
   *rows_via_perm = false;
+  bind_primary_context();
   if (flags & MOE_CAPACITY_REROUTE) {
     // each token's R best experts, then the rerouting dispatch into the caller's idx / gate
     const int R = E < kMaxRank ? E : kMaxRank;
