@@ -117,3 +117,78 @@ def test_concurrent_layers_on_distinct_workspaces():
     # the outputs are real results, not untouched buffers
     for r in ref:
         assert float(r.float().abs().sum()) > 0 and np.isfinite(float(r.float().sum()))
+
+
+def first_call_in_fresh_thread(fn):
+    """Runs fn() as the first CUDA work of a new host thread (no context is current on it yet)."""
+    errors = []
+
+    def w():
+        try:
+            fn()
+        except Exception as e:  # reported by the caller
+            errors.append(repr(e))
+
+    t = threading.Thread(target=w)
+    t.start()
+    t.join(timeout=120)
+    assert not t.is_alive(), "the thread did not finish"
+    return errors
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("entry", ["router", "up_pair", "up_tc", "up_stream", "up_int4", "forward"])
+def test_first_cuda_work_of_a_fresh_thread(entry):
+    """Each entry point that builds tensor maps, called as a new host thread's first CUDA work (the
+    stream passed explicitly and the outputs allocated beforehand, so that nothing else binds a
+    context first), gives the same result as on the main thread."""
+    bf16 = ig.DTYPE_BF16
+    decode = entry in ("up_stream", "up_int4")
+    c = (make_case(T=4, d=512, F=512, E=16, k=2, dt=bf16) if decode
+         else make_case(T=2048, d=256, F=512, E=16, k=2, dt=bf16, bias_scale=0.6))
+    T, d, F, E, k, A = c.T, c.d, c.F, c.E, c.k, c.A
+    ws = workspace_for(c)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    counts = torch.empty(E, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(A, dtype=torch.int32, device=DEV)
+    row_of = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    row_gate = torch.empty(A, dtype=torch.float32, device=DEV)
+    x_perm = torch.empty((A, d), dtype=torch.bfloat16, device=DEV)
+    moe.router_topk(c.x, c.w_r, c.b_r, T, d, E, k, bf16, idx, gate)
+    moe.dispatch(c.x, idx, gate, T, d, E, k, bf16, counts, offsets, perm, row_of, row_gate, x_perm, ws)
+    q1 = moe.quantize(c.w1, 4) if entry == "up_int4" else None
+    path = {"up_pair": moe.PATH_TENSOR_T, "up_tc": moe.PATH_TENSOR, "up_stream": moe.PATH_STREAM}.get(entry)
+
+    def call(outs, stream):
+        if entry == "router":
+            moe.router_topk(c.x, c.w_r, c.b_r, T, d, E, k, bf16, outs[0], outs[1], stream=stream)
+        elif entry == "up_int4":
+            moe.expert_up_q(x_perm, q1[0], q1[1], offsets, T, d, F, E, k, 4, outs[0], stream=stream)
+        elif entry == "forward":
+            moe.forward(c.x, c.w_r, c.b_r, c.w1, c.w2, T, d, F, E, k, bf16, outs[0], ws, stream=stream)
+        else:
+            moe.expert_up(x_perm, c.w1, offsets, T, d, F, E, k, bf16, outs[0], ws, path=path, stream=stream)
+
+    def new_outs():
+        if entry == "router":
+            return [torch.empty((T, k), dtype=torch.int32, device=DEV),
+                    torch.empty((T, k), dtype=torch.float32, device=DEV)]
+        if entry == "forward":
+            return [torch.empty((T, d), dtype=torch.bfloat16, device=DEV)]
+        return [torch.empty((A, F), dtype=torch.bfloat16, device=DEV)]
+
+    ref = new_outs()
+    call(ref, None)
+    torch.cuda.synchronize()
+    got = new_outs()
+    stream = torch.cuda.Stream(device=DEV)
+    torch.cuda.synchronize()
+    errors = first_call_in_fresh_thread(lambda: call(got, stream))
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert moe.get_device_status(ws)[0] == moe.MOE_OK
+    for r, g in zip(ref, got):
+        assert torch.equal(r.view(torch.int16) if r.dtype == torch.bfloat16 else r,
+                           g.view(torch.int16) if g.dtype == torch.bfloat16 else g), entry
