@@ -104,10 +104,17 @@ def status_string(status: int) -> str:
 
 
 def _ptr(t) -> Optional[int]:
+    """A tensor argument's device address. The kernels dereference it on the GPU and read it as dense
+    row-major data, so a host tensor (its address would fault on the device) or a strided view (it
+    would be read as if dense) is refused here. Integers pass through as raw addresses."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError(f"moe: tensor arguments must be CUDA tensors (got one on {t.device})")
+    if not t.is_contiguous():
+        raise ValueError("moe: tensor arguments must be contiguous")
     return t.data_ptr()
 
 

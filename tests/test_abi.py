@@ -166,3 +166,13 @@ def test_reroute_arguments_rejected_without_gpu():
     assert fwd(moe.CAPACITY_REROUTE, 3, stats=FAKE) == moe.MOE_ERR_INVALID_ARG
     assert fwd(4, 3) == moe.MOE_ERR_INVALID_ARG
     assert moe.CAPACITY_REROUTE == 2 and moe.GATES_RENORMALISE == 1
+
+
+def test_binding_refuses_host_tensors_without_gpu():
+    """The binding hands the library device addresses only: a host tensor is refused before any call
+    (its address would be dereferenced on the GPU); raw integer addresses and None pass through."""
+    import torch
+    x = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        moe.router_topk(x, x, None, 4, 8, 8, 2, moe.MOE_DTYPE_BF16, x, x)
+    assert _lib._ptr(None) is None and _lib._ptr(4096) == 4096

@@ -629,3 +629,15 @@ def test_device_generator_matches_host():
     t32 = torch.empty(4099, dtype=torch.float32, device=DEV)
     ig.fill_device(t32, 7, key, 1.0, F32)
     assert np.array_equal(t32.cpu().numpy(), ig.draw(7, 4099, key, 1.0, F32))
+
+
+def test_binding_refuses_strided_views():
+    """A strided view would be read as dense data: the binding refuses it before the library is called."""
+    x = torch.zeros((64, 32), dtype=torch.bfloat16, device=DEV)
+    w_r = torch.zeros((32, 8), dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty((32, 2), dtype=torch.int32, device=DEV)
+    gate = torch.empty((32, 2), dtype=torch.float32, device=DEV)
+    with pytest.raises(ValueError, match="contiguous"):
+        moe.router_topk(x.t(), w_r, None, 32, 64, 8, 2, BF16, idx, gate)
+    with pytest.raises(ValueError, match="contiguous"):
+        moe.router_topk(x[:, :16], w_r[:16], None, 64, 16, 8, 2, BF16, idx, gate)
