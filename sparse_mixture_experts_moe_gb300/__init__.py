@@ -40,6 +40,10 @@ class MoELayer:
         self.F = int(w1.shape[2])
         if tuple(w1.shape) != (self.E, self.d, self.F) or tuple(w2.shape) != (self.E, self.F, self.d):
             raise ValueError("MoELayer: expected w1 [E, d, F] and w2 [E, F, d]")
+        if not (w_r.dtype == w1.dtype == w2.dtype):
+            raise ValueError("MoELayer: w_r, w1 and w2 must have one dtype")
+        if b_r is not None and tuple(b_r.shape) != (self.E,):
+            raise ValueError("MoELayer: expected b_r [E]")
         self.k = int(k)
         self.dt = _lib.dtype_code(w1)
         self.w_r, self.w1, self.w2 = w_r.contiguous(), w1.contiguous(), w2.contiguous()
@@ -57,6 +61,15 @@ class MoELayer:
         self._ws = None
         self._ws_T = -1
 
+    def _check_io(self, x, out):
+        """x [T, d] in the weights' dtype, and out (if given) [T, d]: any other shape would be read or
+        written as if it were one."""
+        if x.dim() != 2 or int(x.shape[1]) != self.d or x.dtype != self.w1.dtype:
+            raise ValueError(f"MoELayer: expected x [T, {self.d}] in {self.w1.dtype}, got {tuple(x.shape)} "
+                             f"in {x.dtype}")
+        if out is not None and tuple(out.shape) != tuple(x.shape):
+            raise ValueError(f"MoELayer: expected out {tuple(x.shape)}, got {tuple(out.shape)}")
+
     def workspace(self, T: int):
         import torch
         if self._ws is None or T > self._ws_T:
@@ -73,6 +86,7 @@ class MoELayer:
         """Forward pass of x [T, d]; the output is in x's dtype unless out / out_dtype say otherwise.
         router_stats: optional float32 device tensor of router_stats_len(E) for the routing statistics."""
         import torch
+        self._check_io(x, out)
         T = int(x.shape[0])
         if out is None:
             out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=x.device)
@@ -97,6 +111,7 @@ class MoELayer:
     def graph(self, x, out, topk_idx=None, topk_gate=None, counts=None, router_stats=None) -> CapturedGraph:
         """A CUDA graph of this layer on these buffers: graph.launch() reruns the layer on the current
         contents of x and writes out (one host call per step)."""
+        self._check_io(x, out)
         T = int(x.shape[0])
         cap = 0 if self.capacity_factor is None else capacity(T, self.k, self.E, self.capacity_factor)
         if cap < 0:

@@ -118,6 +118,40 @@ def _ptr(t) -> Optional[int]:
     return t.data_ptr()
 
 
+def _esize(dt) -> int:
+    """Bytes per element of the call's data type (an invalid code is left to the library to reject)."""
+    return 2 if dt == MOE_DTYPE_BF16 else 4
+
+
+def _fits(t, n, esize, name, typed=False):
+    """Refuses a tensor with fewer bytes than n elements of esize bytes, which the kernels would read or
+    write past, and, for the layer's data in the call's dtype (typed), a tensor whose elements have
+    another size. None and raw integer addresses pass (the library checks those it needs)."""
+    if t is None or isinstance(t, int):
+        return
+    if typed and t.element_size() != esize:
+        raise ValueError(f"moe: {name} has {t.element_size()}-byte elements; the call's dtype has {esize}")
+    if n > 0 and t.numel() * t.element_size() < n * esize:
+        raise ValueError(f"moe: {name} holds {t.numel() * t.element_size()} bytes; the call needs {n * esize}")
+
+
+def _routing_fits(T, E, k, topk_idx, topk_gate, counts=None, router_stats=None):
+    _fits(topk_idx, T * k, 4, "topk_idx")
+    _fits(topk_gate, T * k, 4, "topk_gate")
+    _fits(counts, E, 4, "counts")
+    _fits(router_stats, 2 * E + 2, 4, "router_stats")
+
+
+def _dispatch_fits(T, d, E, k, dt, counts, offsets, perm_token, row_of, row_gate, x_perm):
+    A = T * k
+    _fits(counts, E, 4, "counts")
+    _fits(offsets, E + 1, 4, "offsets")
+    _fits(perm_token, A, 4, "perm_token")
+    _fits(row_of, A, 4, "row_of")
+    _fits(row_gate, A, 4, "row_gate")
+    _fits(x_perm, A * d, _esize(dt), "x_perm", typed=True)
+
+
 def _stream(stream) -> Optional[int]:
     if stream is None:
         import torch
@@ -162,6 +196,10 @@ def get_device_status(ws, stream=None):
 
 def router_topk(x, w_r, b_r, T, d, E, k, dt, topk_idx, topk_gate, renormalise=False, stream=None, check=True):
     """renormalise: gates are the softmax over the k chosen logits (GATES_RENORMALISE)."""
+    _fits(x, T * d, _esize(dt), "x", typed=True)
+    _fits(w_r, d * E, _esize(dt), "w_r", typed=True)
+    _fits(b_r, E, 4, "b_r")
+    _routing_fits(T, E, k, topk_idx, topk_gate)
     rc = lib().moe_router_topk_ex(_ptr(x), _ptr(w_r), _ptr(b_r), T, d, E, k, dt,
                                   GATES_RENORMALISE if renormalise else 0, _ptr(topk_idx), _ptr(topk_gate),
                                   _stream(stream))
@@ -176,6 +214,10 @@ def router_stats_len(E) -> int:
 def router_topk_stats(x, w_r, b_r, T, d, E, k, dt, topk_idx, topk_gate, stats, ws, renormalise=False, stream=None,
                       check=True):
     """moe_router_topk_stats: the router plus the batch's routing statistics in `stats`."""
+    _fits(x, T * d, _esize(dt), "x", typed=True)
+    _fits(w_r, d * E, _esize(dt), "w_r", typed=True)
+    _fits(b_r, E, 4, "b_r")
+    _routing_fits(T, E, k, topk_idx, topk_gate, router_stats=stats)
     rc = lib().moe_router_topk_stats(_ptr(x), _ptr(w_r), _ptr(b_r), T, d, E, k, dt,
                                      GATES_RENORMALISE if renormalise else 0, _ptr(topk_idx), _ptr(topk_gate),
                                      _ptr(stats), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
@@ -200,6 +242,9 @@ def capacity(T, k, E, cf) -> int:
 def dispatch(x, topk_idx, topk_gate, T, d, E, k, dt, counts, offsets, perm_token, row_of, row_gate, x_perm, ws,
              capacity=0, stream=None, check=True):
     """capacity > 0: each expert keeps its first `capacity` assignments (moe_dispatch_ex)."""
+    _fits(x, T * d, _esize(dt), "x", typed=True)
+    _routing_fits(T, E, k, topk_idx, topk_gate)
+    _dispatch_fits(T, d, E, k, dt, counts, offsets, perm_token, row_of, row_gate, x_perm)
     rc = lib().moe_dispatch_ex(_ptr(x), _ptr(topk_idx), _ptr(topk_gate), T, d, E, k, dt, int(capacity),
                                _ptr(counts), _ptr(offsets), _ptr(perm_token), _ptr(row_of), _ptr(row_gate),
                                _ptr(x_perm), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
@@ -210,6 +255,11 @@ def dispatch_reroute(x, rank_idx, rank_gate, T, d, E, k, R, dt, capacity, final_
                      perm_token, row_of, row_gate, x_perm, ws, stream=None, check=True):
     """moe_dispatch_reroute: an assignment that meets a full expert takes the next entry of its token's
     ranking rank_idx[t, k:] with room, or is dropped (final_idx -1)."""
+    _fits(x, T * d, _esize(dt), "x", typed=True)
+    _fits(rank_idx, T * R, 4, "rank_idx")
+    _fits(rank_gate, T * R, 4, "rank_gate")
+    _routing_fits(T, E, k, final_idx, final_gate)
+    _dispatch_fits(T, d, E, k, dt, counts, offsets, perm_token, row_of, row_gate, x_perm)
     rc = lib().moe_dispatch_reroute(_ptr(x), _ptr(rank_idx), _ptr(rank_gate), T, d, E, k, R, dt, int(capacity),
                                     _ptr(final_idx), _ptr(final_gate), _ptr(counts), _ptr(offsets), _ptr(perm_token),
                                     _ptr(row_of), _ptr(row_gate), _ptr(x_perm), _ptr(ws),
@@ -224,6 +274,9 @@ def _flags(renormalise, reroute):
 def dispatch_noalloc(x, topk_idx, topk_gate, T, d, E, k, dt, counts, offsets, perm_token, row_of, row_gate,
                      x_perm, stream=None, check=True):
     """moe_dispatch without a workspace: the count tables live in the library's fixed per-GPU array."""
+    _fits(x, T * d, _esize(dt), "x", typed=True)
+    _routing_fits(T, E, k, topk_idx, topk_gate)
+    _dispatch_fits(T, d, E, k, dt, counts, offsets, perm_token, row_of, row_gate, x_perm)
     rc = lib().moe_dispatch_noalloc(_ptr(x), _ptr(topk_idx), _ptr(topk_gate), T, d, E, k, dt, _ptr(counts),
                                     _ptr(offsets), _ptr(perm_token), _ptr(row_of), _ptr(row_gate), _ptr(x_perm),
                                     _stream(stream))
@@ -231,12 +284,21 @@ def dispatch_noalloc(x, topk_idx, topk_gate, T, d, E, k, dt, counts, offsets, pe
 
 
 def expert_up(x_perm, w1, offsets, T, d, F, E, k, dt, h, ws, path=PATH_AUTO, stream=None, check=True):
+    _fits(x_perm, T * k * d, _esize(dt), "x_perm", typed=True)
+    _fits(w1, E * d * F, _esize(dt), "w1", typed=True)
+    _fits(offsets, E + 1, 4, "offsets")
+    _fits(h, T * k * F, _esize(dt), "h", typed=True)
     rc = lib().moe_expert_up_ex(_ptr(x_perm), _ptr(w1), _ptr(offsets), T, d, F, E, k, dt, path, _ptr(h), _ptr(ws),
                                 ws.numel() * ws.element_size(), _stream(stream))
     return _check(rc, "moe_expert_up") if check else rc
 
 
 def expert_down(h, w2, offsets, row_gate, T, d, F, E, k, dt, y_perm, ws, path=PATH_AUTO, stream=None, check=True):
+    _fits(h, T * k * F, _esize(dt), "h", typed=True)
+    _fits(w2, E * F * d, _esize(dt), "w2", typed=True)
+    _fits(offsets, E + 1, 4, "offsets")
+    _fits(row_gate, T * k, 4, "row_gate")
+    _fits(y_perm, T * k * d, 4, "y_perm", typed=True)
     rc = lib().moe_expert_down_ex(_ptr(h), _ptr(w2), _ptr(offsets), _ptr(row_gate), T, d, F, E, k, dt, path,
                                   _ptr(y_perm), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     return _check(rc, "moe_expert_down") if check else rc
@@ -244,14 +306,33 @@ def expert_down(h, w2, offsets, row_gate, T, d, F, E, k, dt, y_perm, ws, path=PA
 
 def grouped_ffn(x_perm, w1, w2, offsets, row_gate, T, d, F, E, k, dt, y_perm, ws, path=PATH_AUTO, stream=None,
                 check=True):
+    _fits(x_perm, T * k * d, _esize(dt), "x_perm", typed=True)
+    _fits(w1, E * d * F, _esize(dt), "w1", typed=True)
+    _fits(w2, E * F * d, _esize(dt), "w2", typed=True)
+    _fits(offsets, E + 1, 4, "offsets")
+    _fits(row_gate, T * k, 4, "row_gate")
+    _fits(y_perm, T * k * d, 4, "y_perm", typed=True)
     rc = lib().moe_grouped_ffn_ex(_ptr(x_perm), _ptr(w1), _ptr(w2), _ptr(offsets), _ptr(row_gate), T, d, F, E, k,
                                   dt, path, _ptr(y_perm), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     return _check(rc, "moe_grouped_ffn") if check else rc
 
 
 def combine(y_perm, row_of, T, d, k, dt, out, stream=None, check=True):
+    _fits(y_perm, T * k * d, 4, "y_perm", typed=True)
+    _fits(row_of, T * k, 4, "row_of")
+    _fits(out, T * d, _esize(dt), "out", typed=True)
     rc = lib().moe_combine(_ptr(y_perm), _ptr(row_of), T, d, k, dt, _ptr(out), _stream(stream))
     return _check(rc, "moe_combine") if check else rc
+
+
+def _layer_fits(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, out_dt, topk_idx, topk_gate, counts, router_stats):
+    _fits(x, T * d, _esize(dt), "x", typed=True)
+    _fits(w_r, d * E, _esize(dt), "w_r", typed=True)
+    _fits(b_r, E, 4, "b_r")
+    _fits(w1, E * d * F, _esize(dt), "w1", typed=True)
+    _fits(w2, E * F * d, _esize(dt), "w2", typed=True)
+    _fits(out, T * d, _esize(out_dt), "out", typed=True)
+    _routing_fits(T, E, k, topk_idx, topk_gate, counts, router_stats)
 
 
 def forward(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws, topk_idx=None, topk_gate=None, counts=None,
@@ -261,6 +342,7 @@ def forward(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws, topk_idx=None, topk
     reroute: CAPACITY_REROUTE (assignments past capacity go to the token's next-best expert with room);
     router_stats: None or a float32 device tensor of router_stats_len(E) (as router_topk_stats)."""
     out_dt = dt if out_dt is None else out_dt
+    _layer_fits(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, out_dt, topk_idx, topk_gate, counts, router_stats)
     rc = lib().moe_forward_ex(_ptr(x), _ptr(w_r), _ptr(b_r), _ptr(w1), _ptr(w2), T, d, F, E, k, dt, out_dt, path,
                               _flags(renormalise, reroute), int(capacity), _ptr(out),
                               _ptr(topk_idx), _ptr(topk_gate), _ptr(counts), _ptr(router_stats), _ptr(ws),
@@ -276,6 +358,7 @@ class ForwardGraph:
     def __init__(self, x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, ws, topk_idx=None, topk_gate=None, counts=None,
                  path=PATH_AUTO, out_dt=None, renormalise=False, capacity=0, router_stats=None):
         out_dt = dt if out_dt is None else out_dt
+        _layer_fits(x, w_r, b_r, w1, w2, T, d, F, E, k, dt, out, out_dt, topk_idx, topk_gate, counts, router_stats)
         self._keep = (x, w_r, b_r, w1, w2, out, ws, topk_idx, topk_gate, counts, router_stats)
         h = ctypes.c_void_p()
         self._lib = lib()
@@ -355,6 +438,8 @@ def qscale_bytes(K, N, E) -> int:
 
 def quantize_weights(w, K, N, E, dt, bits, codes, scale_min, stream=None, check=True):
     """w [E, K, N] -> codes (moe_qweight_bytes bytes) and scale_min ([E, K/64, N/64, 2] fp32)."""
+    _fits(w, E * K * N, _esize(dt), "w", typed=True)
+    _qweights_fits(codes, scale_min, K, N, E, bits, "")
     rc = lib().moe_quantize_weights(_ptr(w), K, N, E, dt, bits, _ptr(codes), _ptr(scale_min), _stream(stream))
     return _check(rc, "moe_quantize_weights") if check else rc
 
@@ -372,13 +457,27 @@ def quantize(w, bits, stream=None):
     return codes, sm
 
 
+def _qweights_fits(codes, scale_min, K, N, E, bits, which):
+    _fits(codes, qweight_bytes(K, N, E, bits), 1, which + "codes")
+    _fits(scale_min, qscale_bytes(K, N, E) // 4, 4, which + "scale_min")
+
+
 def expert_up_q(x_perm, codes, scale_min, offsets, T, d, F, E, k, bits, h, stream=None, check=True):
+    _fits(x_perm, T * k * d, 2, "x_perm", typed=True)
+    _qweights_fits(codes, scale_min, d, F, E, bits, "w1 ")
+    _fits(offsets, E + 1, 4, "offsets")
+    _fits(h, T * k * F, 2, "h", typed=True)
     rc = lib().moe_expert_up_q(_ptr(x_perm), _ptr(codes), _ptr(scale_min), _ptr(offsets), T, d, F, E, k, bits,
                                _ptr(h), _stream(stream))
     return _check(rc, "moe_expert_up_q") if check else rc
 
 
 def expert_down_q(h, codes, scale_min, offsets, row_gate, T, d, F, E, k, bits, y_perm, stream=None, check=True):
+    _fits(h, T * k * F, 2, "h", typed=True)
+    _qweights_fits(codes, scale_min, F, d, E, bits, "w2 ")
+    _fits(offsets, E + 1, 4, "offsets")
+    _fits(row_gate, T * k, 4, "row_gate")
+    _fits(y_perm, T * k * d, 4, "y_perm", typed=True)
     rc = lib().moe_expert_down_q(_ptr(h), _ptr(codes), _ptr(scale_min), _ptr(offsets), _ptr(row_gate), T, d, F, E,
                                  k, bits, _ptr(y_perm), _stream(stream))
     return _check(rc, "moe_expert_down_q") if check else rc
@@ -388,6 +487,10 @@ def forward_q(x, w_r, b_r, w1q, w2q, T, d, F, E, k, bits, out, ws, topk_idx=None
               out_dt=None, renormalise=False, capacity=0, router_stats=None, stream=None, check=True, reroute=False):
     """The layer with block-quantised expert weights; w1q / w2q are (codes, scale_min) pairs."""
     out_dt = MOE_DTYPE_BF16 if out_dt is None else out_dt
+    _layer_fits(x, w_r, b_r, None, None, T, d, F, E, k, MOE_DTYPE_BF16, out, out_dt, topk_idx, topk_gate, counts,
+                router_stats)
+    _qweights_fits(w1q[0], w1q[1], d, F, E, bits, "w1 ")
+    _qweights_fits(w2q[0], w2q[1], F, d, E, bits, "w2 ")
     rc = lib().moe_forward_q(_ptr(x), _ptr(w_r), _ptr(b_r), _ptr(w1q[0]), _ptr(w1q[1]), _ptr(w2q[0]),
                              _ptr(w2q[1]), T, d, F, E, k, bits, out_dt, _flags(renormalise, reroute),
                              int(capacity), _ptr(out), _ptr(topk_idx), _ptr(topk_gate), _ptr(counts),

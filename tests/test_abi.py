@@ -172,7 +172,25 @@ def test_binding_refuses_host_tensors_without_gpu():
     """The binding hands the library device addresses only: a host tensor is refused before any call
     (its address would be dereferenced on the GPU); raw integer addresses and None pass through."""
     import torch
-    x = torch.zeros(4, 8, dtype=torch.bfloat16)
+    x, w_r = torch.zeros(4, 8, dtype=torch.bfloat16), torch.zeros(8, 8, dtype=torch.bfloat16)
+    idx, gate = torch.zeros(4, 2, dtype=torch.int32), torch.zeros(4, 2, dtype=torch.float32)
     with pytest.raises(ValueError, match="CUDA tensors"):
-        moe.router_topk(x, x, None, 4, 8, 8, 2, moe.MOE_DTYPE_BF16, x, x)
+        moe.router_topk(x, w_r, None, 4, 8, 8, 2, moe.MOE_DTYPE_BF16, idx, gate)
     assert _lib._ptr(None) is None and _lib._ptr(4096) == 4096
+
+
+def test_binding_refuses_short_or_mistyped_tensors_without_gpu():
+    """A tensor with fewer bytes than the sizes passed would be read or written past its end, and the
+    layer's data in another element type would be misread: both are refused before any call."""
+    import torch
+    x, w_r = torch.zeros(4, 8, dtype=torch.bfloat16), torch.zeros(8, 8, dtype=torch.bfloat16)
+    idx, gate = torch.zeros(4, 2, dtype=torch.int32), torch.zeros(4, 2, dtype=torch.float32)
+    BF16 = moe.MOE_DTYPE_BF16
+    with pytest.raises(ValueError, match="the call needs"):      # T = 5 tokens, x holds 4
+        moe.router_topk(x, w_r, None, 5, 8, 8, 2, BF16, idx, gate)
+    with pytest.raises(ValueError, match="the call needs"):      # k = 3, the outputs hold k = 2
+        moe.router_topk(x, w_r, None, 4, 8, 8, 3, BF16, idx, gate)
+    with pytest.raises(ValueError, match="2-byte elements"):     # bf16 data for an fp32 call
+        moe.router_topk(x, w_r, None, 4, 8, 8, 2, moe.MOE_DTYPE_F32, idx, gate)
+    with pytest.raises(ValueError, match="the call needs"):      # out smaller than [T, d]
+        moe.combine(torch.zeros(4 * 2 * 8), idx, 4, 8, 2, BF16, torch.zeros(3, 8, dtype=torch.bfloat16))

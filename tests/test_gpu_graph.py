@@ -76,7 +76,7 @@ def test_graph_zero_tokens_and_bad_args():
     g.launch()
     torch.cuda.synchronize()
     with pytest.raises(moe.MoeError):
-        moe.ForwardGraph(c.x, c.w_r, None, c.w1, c.w2, 4, 64, 64, 4, 9, BF16, out, ws)  # k > E
+        moe.ForwardGraph(c.x, c.w_r, None, c.w1, c.w2, 0, 64, 64, 4, 9, BF16, out, ws)  # k > E: the library refuses
 
 
 @pytest.mark.parametrize("bits", [4, 8])

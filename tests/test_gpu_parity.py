@@ -634,10 +634,32 @@ def test_device_generator_matches_host():
 def test_binding_refuses_strided_views():
     """A strided view would be read as dense data: the binding refuses it before the library is called."""
     x = torch.zeros((64, 32), dtype=torch.bfloat16, device=DEV)
-    w_r = torch.zeros((32, 8), dtype=torch.bfloat16, device=DEV)
-    idx = torch.empty((32, 2), dtype=torch.int32, device=DEV)
-    gate = torch.empty((32, 2), dtype=torch.float32, device=DEV)
-    with pytest.raises(ValueError, match="contiguous"):
+    w_r = torch.zeros((64, 8), dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty((64, 2), dtype=torch.int32, device=DEV)
+    gate = torch.empty((64, 2), dtype=torch.float32, device=DEV)
+    with pytest.raises(ValueError, match="contiguous"):  # x.t(): T = 32 tokens of d = 64, transposed
         moe.router_topk(x.t(), w_r, None, 32, 64, 8, 2, BF16, idx, gate)
-    with pytest.raises(ValueError, match="contiguous"):
+    with pytest.raises(ValueError, match="contiguous"):  # the first 16 columns of each row
         moe.router_topk(x[:, :16], w_r[:16], None, 64, 16, 8, 2, BF16, idx, gate)
+
+
+def test_layer_refuses_mismatched_inputs():
+    """MoELayer takes x [T, d] in its weights' dtype and an out of x's shape; anything else is refused
+    before a kernel could read or write it as if it had that shape."""
+    w_r = torch.zeros((32, 8), dtype=torch.bfloat16, device=DEV)
+    w1 = torch.zeros((8, 32, 64), dtype=torch.bfloat16, device=DEV)
+    w2 = torch.zeros((8, 64, 32), dtype=torch.bfloat16, device=DEV)
+    layer = moe.MoELayer(w_r, w1, w2, k=2)
+    for bad in (torch.zeros((4, 16), dtype=torch.bfloat16, device=DEV),   # width is not d
+                torch.zeros((4, 32), dtype=torch.float32, device=DEV),    # not the weights' dtype
+                torch.zeros(128, dtype=torch.bfloat16, device=DEV)):      # not [T, d]
+        with pytest.raises(ValueError):
+            layer(bad)
+    x = torch.zeros((4, 32), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(ValueError):
+        layer(x, out=torch.empty((3, 32), dtype=torch.bfloat16, device=DEV))
+    with pytest.raises(ValueError):
+        moe.MoELayer(w_r.float(), w1, w2, k=2)
+    with pytest.raises(ValueError):
+        moe.MoELayer(w_r, w1, w2, k=2, b_r=torch.zeros(7, device=DEV))
+    assert layer(x).shape == (4, 32)  # the well-formed call still runs
