@@ -177,3 +177,39 @@ def test_full_size_quantised_decode(name, bits):
     ref = oracle.combine(y, dp["row_of"])
     assert rel_rms_err(to_f64(out32.t), ref) < 2e-2
     assert torch.equal(out_bf.t.view(torch.int16), out32.t.to(torch.bfloat16).view(torch.int16))
+
+
+def test_activations_past_2_31_elements():
+    """T = 65536 tokens with d_ff = 32768: h [T*k, d_ff] holds 2^32 elements, so every offset past
+    element 2^31 has to be computed in 64 bits. Routing is compared for every token, and the outputs
+    of the tokens whose rows lie furthest into h (past element 2^31) against the oracle; the outputs and
+    the workspace sit inside guard bands."""
+    T, d, F, E, k = 65536, 256, 32768, 16, 2
+    c = make_case(T=T, d=d, F=F, E=E, k=k, dt=ig.DTYPE_BF16)
+    ws = guarded_workspace(c)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    out32 = Guarded((T, d), torch.float32)
+    moe.forward(c.x, c.w_r, c.b_r, c.w1, c.w2, T, d, F, E, k, c.dt, out32.t, ws.t, topk_idx=idx,
+                out_dt=ig.DTYPE_F32)
+    st, detail = moe.get_device_status(ws.t)
+    assert st == moe.MOE_OK, (moe.status_string(st), detail)
+    assert out32.intact() and ws.intact()
+    ridx, rgate = oracle_routing(c)
+    assert np.array_equal(idx.cpu().numpy(), ridx)
+    dp_all = oracle.dispatch(ridx, E, rgate)
+    last_row = dp_all["row_of"].max(axis=1)
+    sel = np.sort(np.argsort(last_row)[-8:])  # the 8 tokens with rows furthest into h
+    assert (last_row[sel] * F >= 2 ** 31).all()
+    # the oracle on those tokens alone: their rows through both projections (h exact, and h rounded
+    # once to bf16 as the path rounds it), then the fixed-order k-way sum
+    dp = oracle.dispatch(ridx[sel], E, rgate[sel])
+    xs = c.x64[sel][dp["perm_token"]]
+    w1h, w2h = c.w1_host(), c.w2_host()
+    h = oracle.expert_rows_up(xs, dp["offsets"], w1h)
+    ref = oracle.combine(oracle.expert_rows_down(h, dp["offsets"], dp["row_gate"], w2h), dp["row_of"])
+    hb = ig.as_f64(ig.f32_to_bf16_bits(h.astype(np.float32)), ig.DTYPE_BF16)
+    emul = oracle.combine(oracle.expert_rows_down(hb, dp["offsets"], dp["row_gate"], w2h), dp["row_of"])
+    got = to_f64(out32.t)[sel]
+    assert rel_rms_err(got, emul) < EMULATION_TOL
+    rounding = rel_rms_err(emul, ref)
+    assert rel_rms_err(got, ref) < max(2e-2, 1.1 * rounding + 2e-3), (rel_rms_err(got, ref), rounding)
