@@ -313,9 +313,8 @@ def dominant_roofline(w, kern_ms, touched, fpath, qbits, peaks, peak_src):
         wbytes = K_ * N_ * qbits // 8 + (K_ // 64) * (N_ // 64) * 8
         alg_bytes = touched * wbytes + A * K_ * eb + A * N_ * (eb if dom == "expert_up" else 4)
         achieved = alg_bytes / (kern_ms[dom] / 1e3) / 1e9
-        qname = "ffn_stream_q4_kernel" if qbits == 4 else "ffn_stream_q_kernel<8>"
-        qkey = (f"ffn_stream_q4_kernel<{1 if dom == 'expert_up' else 2}>" if qbits == 4 else
-                f"ffn_stream_q_kernel<8, {1 if dom == 'expert_up' else 2}>")
+        qname = f"ffn_stream_q{qbits}_kernel"
+        qkey = f"{qname}<{1 if dom == 'expert_up' else 2}>"
         roof = {"kernel": f"{qname} ({dom})", "bound": "hbm", "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "traffic": stored_traffic(qkey, w.name, QUANT_SOURCES),

@@ -316,8 +316,12 @@ moe_status moe_selftest_wait_timeout(void* workspace, size_t ws_bytes, int timeo
  *   division, ties to even), restored as w ~ min + code * scale (|error| <= scale / 2). A block of
  *   equal values has scale 0 and codes 0. bits is 4 or 8; K and N must be multiples of 64.
  * Layout of `codes` (moe_qweight_bytes(K, N, E, bits) bytes, 16-byte aligned), per expert:
- *   INT8: 16-byte tiles of 8 consecutive columns by 2 consecutive k-rows, row-major over
- *   (k / 2, n / 8); 64-bit half j is k-row j, byte c is column c.
+ *   INT8: [N/64][K/16][2][32][16] bytes: for each 64-column slab and 16-deep k-block 2p + s (step s
+ *   of the 32-deep range p), half h of lane l = 4g + t holds column tiles m = 2h and 2h + 1, 8 bytes
+ *   each; byte q of tile m holds (k, column) = (kp, c0), (kp+1, c0), (kp, c1), (kp+1, c1), (kp+2, c0),
+ *   (kp+3, c0), (kp+2, c1), (kp+3, c1) for q = 0..7, with kp = 32p + 8t + 4s, c0 = 16m + g,
+ *   c1 = c0 + 8 (the order of an m16n8k16 fp16 A fragment, with k numbered within each 32-deep range
+ *   so that one lane's activations for the range's two steps are 8 consecutive values).
  *   INT4: [N/64][K/16][32][4] 32-bit words: for each 64-column slab and 16-deep k-block 4b + j
  *   (step j of the 64-deep block b), lane l = 4g + t holds 4 words; word m covers columns
  *   c0 = 16m + g and c1 = c0 + 8 at k-rows kp .. kp+3, kp = 64b + 16t + 4j, its nibble i

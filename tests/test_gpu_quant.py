@@ -23,7 +23,10 @@ def unpack_codes(raw, E, K, N, bits):
     64-deep block b; lane 4g + t, word m covers columns c0 = 16m + g and c1 = c0 + 8 at k-rows
     kp .. kp+3 with kp = 64b + 16t + 4j, nibble i (bits 4i..4i+3) holding (k, column) = (kp, c0),
     (kp, c1), (kp+2, c0), (kp+2, c1), (kp+1, c0), (kp+1, c1), (kp+3, c0), (kp+3, c1) for i = 0..7.
-    INT8: 16-byte tiles of 8 columns by 2 k-rows, row-major over (k / 2, n / 8); half j is k-row j."""
+    INT8: per expert [N/64 slabs][K/16 steps][2 halves][32 lanes][16 bytes]; step 2p + s is step s of
+    the 32-deep range p; half h of lane 4g + t holds column tiles m = 2h, 2h + 1, 8 bytes each: byte q of
+    tile m holds (k, column) = (kp, c0), (kp+1, c0), (kp, c1), (kp+1, c1), (kp+2, c0), (kp+3, c0),
+    (kp+2, c1), (kp+3, c1) for q = 0..7, with kp = 32p + 8t + 4s, c0 = 16m + g and c1 = c0 + 8."""
     codes = np.zeros((E, K, N), np.uint8)
     if bits == 4:
         words = np.ascontiguousarray(raw).view("<u4").reshape(E, N // 64, K // 16, 32, 4)
@@ -37,9 +40,18 @@ def unpack_codes(raw, E, K, N, bits):
                 c = slab * 64 + (16 * m + g + dc)[None, None, :]
                 codes[:, k, c] = (words[..., m] >> (4 * i)) & 0xF
     else:
-        b = np.ascontiguousarray(raw).reshape(E, K // 2, N // 8, 2, 8)
-        for j in range(2):
-            codes[:, j::2, :] = b[:, :, :, j, :].reshape(E, K // 2, N)
+        b = np.ascontiguousarray(raw).reshape(E, N // 64, K // 16, 2, 32, 16)
+        lane = np.arange(32)
+        g, t = lane // 4, lane % 4
+        slab = np.arange(N // 64)[:, None, None]
+        k16 = np.arange(K // 16)[None, :, None]
+        for h in range(2):
+            for mi in range(2):
+                m = 2 * h + mi
+                for q, (dk, dc) in enumerate([(0, 0), (1, 0), (0, 8), (1, 8), (2, 0), (3, 0), (2, 8), (3, 8)]):
+                    k = (k16 // 2) * 32 + 4 * (k16 % 2) + (8 * t + dk)[None, None, :]
+                    c = slab * 64 + (16 * m + g + dc)[None, None, :]
+                    codes[:, k, c] = b[:, :, :, h, :, 8 * mi + q]
     return codes
 
 
