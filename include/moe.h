@@ -336,6 +336,10 @@ moe_status moe_selftest_wait_timeout(void* workspace, size_t ws_bytes, int timeo
  *   y_perm fp32) reading quantised W1 [E, d, F] / W2 [E, F, d]; weight-streaming kernel for any
  *   number of rows (built for decode batches). moe_forward_q: the whole layer with them (x, w_r
  *   bf16; out_dt, flags, capacity, router_stats and the workspace as in moe_forward_ex).
+ *   Products: INT4 codes multiply bf16 activations; INT8 codes multiply the activations (x rows,
+ *   h) converted to fp16, which is exact for bf16 values of magnitude 2^-14 .. 65504. Smaller values
+ *   keep fp16's subnormal spacing (2^-24), and larger ones overflow, so INT8 layers need activations
+ *   within fp16's range. Accumulation is fp32 for both.
  *   The streaming kernel's waits on its own copies are bounded: moe_forward_q records a wait that
  *   gave up as MOE_ERR_DEVICE_TIMEOUT in its workspace; moe_expert_up_q / moe_expert_down_q take
  *   no workspace, so there the kernel ends early without a record.
