@@ -1,0 +1,92 @@
+"""Seeded random layers within the C ABI's limits, each against the fp64 oracle.
+
+160 configurations come from one fixed seed: tokens, model width d, hidden width d_ff (any
+multiples of 8), expert count, k, element type, for bf16 a kernel family (every family runs every
+valid bf16 shape), and for some an expert capacity (the assignments past it dropped) or renormalised
+gates. Each runs moe_forward with its outputs and workspace inside guard bands. Routing
+indices and counts must equal the oracle's, and the fp32 output must lie within the tolerance rule of
+the fixed parity cases: 1e-4 of the RMS for fp32 layers; 2e-2 for bf16, or a bar raised by the one
+documented rounding of h, itself at most 3e-2. The bf16 output must be the fp32 output rounded once.
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputgen as ig
+import oracle
+import sparse_mixture_experts_moe_gb300 as moe
+from moe_cases import (MAX_RAISED_TOL, Guarded, guarded_workspace, make_case, output_tolerance, rel_rms_err,
+                        to_f64, torch_dtype)
+
+BF16, F32 = ig.DTYPE_BF16, ig.DTYPE_F32
+PATHS = {moe.PATH_AUTO: "auto", moe.PATH_TENSOR: "tc", moe.PATH_STREAM: "stream", moe.PATH_SIMT: "simt",
+         moe.PATH_TENSOR_PAIR: "pair", moe.PATH_TENSOR_T: "tct"}
+
+
+def draw_cases(n=160, seed=20261203):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        dt = BF16 if rng.random() < 0.8 else F32
+        T = int(rng.choice([1, 2, 3, 7, 8, 9, 31, 64, 100, 257, 513, 700]))
+        d = 8 * int(rng.integers(1, 49))  # 8 .. 384
+        F = 8 * int(rng.integers(1, 49))
+        E = int(rng.choice([1, 2, 3, 5, 8, 16, 24, 40, 64, 100, 128, 256]))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        path = int(rng.choice(list(PATHS))) if dt == BF16 else int(rng.choice([moe.PATH_AUTO, moe.PATH_SIMT]))
+        cf = float(rng.choice([0.5, 1.0, 1.25])) if rng.random() < 0.2 else 0.0
+        renorm = bool(rng.random() < 0.2)
+        cases.append(dict(T=T, d=d, F=F, E=E, k=k, dt=dt, path=path, cf=cf, renorm=renorm))
+    return cases
+
+
+CASES = draw_cases()
+
+
+@pytest.mark.gpu
+def run(c, path, out_dt, cap, renorm):
+    """moe_forward with its outputs and workspace inside guard bands; the bands are checked."""
+    g = dict(out=Guarded((c.T, c.d), torch_dtype(out_dt)), idx=Guarded((c.T, c.k), torch.int32),
+             counts=Guarded(c.E, torch.int32))
+    ws = guarded_workspace(c)
+    moe.forward(c.x, c.w_r, c.b_r, c.w1, c.w2, c.T, c.d, c.F, c.E, c.k, c.dt, g["out"].t, ws.t,
+                topk_idx=g["idx"].t, counts=g["counts"].t, path=path, out_dt=out_dt, capacity=cap,
+                renormalise=renorm)
+    st, detail = moe.get_device_status(ws.t)
+    assert st == moe.MOE_OK, (moe.status_string(st), detail)
+    assert all(b.intact() for b in g.values()) and ws.intact()
+    return g["out"].t, g["idx"].t.cpu().numpy(), g["counts"].t.cpu().numpy()
+
+
+def case_id(c):
+    tags = ["bf16" if c["dt"] == BF16 else "f32", PATHS[c["path"]]]
+    tags += [f"cf{c['cf']}"] if c["cf"] else []
+    tags += ["renorm"] if c["renorm"] else []
+    return "T{T}_d{d}_F{F}_E{E}_k{k}_".format(**c) + "_".join(tags)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cfg", CASES, ids=case_id)
+def test_random_layer(cfg):
+    cfg = dict(cfg)
+    path, cf, renorm = cfg.pop("path"), cfg.pop("cf"), cfg.pop("renorm")
+    c = make_case(**cfg)
+    cap = moe.capacity(c.T, c.k, c.E, cf) if cf else 0
+    out, idx, counts = run(c, path, F32, cap, renorm)
+    ref = oracle.forward(c.x64, c.wr64, c.w1_host(), c.w2_host(), c.k, c.br64, renormalise=renorm,
+                         cap=cap if cap else None)
+    assert np.array_equal(idx, ref["idx"])
+    routed = oracle.dispatch(ref["idx"], c.E)["counts"]
+    assert np.array_equal(counts, np.minimum(routed, cap) if cap else routed)  # kept rows per expert
+    bar, _ = output_tolerance(c, ref, cap=cap if cap else None)
+    assert bar <= MAX_RAISED_TOL, bar
+    assert rel_rms_err(to_f64(out), ref["out"]) < bar
+    if c.dt == BF16:
+        out_bf, _, _ = run(c, path, BF16, cap, renorm)
+        assert torch.equal(out_bf.view(torch.int16), out.to(torch.bfloat16).view(torch.int16))
+
+
+def test_draw_covers_the_families():  # host only: the draw exercises every kernel family and both types
+    drawn = {(c["dt"], c["path"]) for c in CASES}
+    assert {p for dt, p in drawn if dt == BF16} == set(PATHS)
+    assert any(dt == F32 for dt, _ in drawn)
