@@ -3,7 +3,8 @@
 160 configurations come from one fixed seed: tokens, model width d, hidden width d_ff (any
 multiples of 8), expert count, k, element type, for bf16 a kernel family (every family runs every
 valid bf16 shape), and for some an expert capacity (the assignments past it dropped) or renormalised
-gates. Each runs moe_forward with its outputs and workspace inside guard bands. Routing
+gates. Each runs moe_forward with its outputs and workspace inside guard bands. Forty more layers
+run moe_forward_q on INT4 or INT8 weights against the oracle on its own quantisation of them. Routing
 indices and counts must equal the oracle's, and the fp32 output must lie within the tolerance rule of
 the fixed parity cases: 1e-4 of the RMS for fp32 layers; 2e-2 for bf16, or a bar raised by the one
 documented rounding of h, itself at most 3e-2. The bf16 output must be the fp32 output rounded once.
@@ -90,3 +91,41 @@ def test_draw_covers_the_families():  # host only: the draw exercises every kern
     drawn = {(c["dt"], c["path"]) for c in CASES}
     assert {p for dt, p in drawn if dt == BF16} == set(PATHS)
     assert any(dt == F32 for dt, _ in drawn)
+
+
+def draw_quantised_cases(n=40, seed=20261204):
+    """Layers with block-quantised expert weights: d and d_ff multiples of 64, INT4 or INT8."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        T = int(rng.choice([1, 2, 3, 8, 9, 33, 64, 130, 300]))
+        d = 64 * int(rng.integers(1, 9))  # 64 .. 512
+        F = 64 * int(rng.integers(1, 9))
+        E = int(rng.choice([1, 2, 5, 8, 16, 40, 64, 128]))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        cases.append(dict(T=T, d=d, F=F, E=E, k=k, bits=int(rng.choice([4, 8]))))
+    return cases
+
+
+Q_CASES = draw_quantised_cases()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cfg", Q_CASES, ids=lambda c: "T{T}_d{d}_F{F}_E{E}_k{k}_int{bits}".format(**c))
+def test_random_quantised_layer(cfg):
+    """moe_forward_q against the oracle run on the oracle's own quantisation of the same weights."""
+    from test_gpu_quant import q_case, q_tolerance
+    c, q1, q2, w1h, w2h = q_case(**cfg)
+    out = Guarded((c.T, c.d), torch.float32)
+    idx = Guarded((c.T, c.k), torch.int32)
+    ws = guarded_workspace(c)
+    moe.forward_q(c.x, c.w_r, c.b_r, q1, q2, c.T, c.d, c.F, c.E, c.k, cfg["bits"], out.t, ws.t, topk_idx=idx.t,
+                  out_dt=F32)
+    st, detail = moe.get_device_status(ws.t)
+    assert st == moe.MOE_OK, (moe.status_string(st), detail)
+    assert out.intact() and idx.intact() and ws.intact()
+    ref = oracle.forward(c.x64, c.wr64, w1h, w2h, c.k, c.br64)
+    assert np.array_equal(idx.t.cpu().numpy(), ref["idx"])
+    bar = q_tolerance(c, ref, w1h, w2h)
+    assert bar <= MAX_RAISED_TOL, bar
+    assert rel_rms_err(to_f64(out.t), ref["out"]) < bar
