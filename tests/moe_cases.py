@@ -219,15 +219,21 @@ STATED_TOL_BF16 = 2e-2
 MAX_RAISED_TOL = 3e-2
 
 
-def bf16_h_rounding_error(c: Case, ref: dict, cap: Optional[int] = None) -> float:
-    """Max relative-to-RMS error of the layer's output that rounding h to bf16 once (and nothing
-    else) causes on this case, computed with the oracle's step functions."""
+def oracle_h_rounded(c: Case, ref: dict, cap: Optional[int] = None) -> np.ndarray:
+    """The layer's output with h rounded once to bf16 (the bf16 path's one documented intermediate
+    rounding) and nothing else, from the oracle's step functions on ref's routing."""
     dp = oracle.dispatch(ref["idx"], c.E, ref["gate"], cap=cap)
     rows = int(dp["offsets"][-1])
     h = oracle.expert_rows_up(c.x64[dp["perm_token"][:rows]], dp["offsets"], c.w1_host())
     h_b = ig.as_f64(ig.f32_to_bf16_bits(h.astype(np.float32)), ig.DTYPE_BF16)
     y = oracle.expert_rows_down(h_b, dp["offsets"], dp["row_gate"], c.w2_host())
-    return rel_rms_err(oracle.combine(y, dp["row_of"]), ref["out"])
+    return oracle.combine(y, dp["row_of"])
+
+
+def bf16_h_rounding_error(c: Case, ref: dict, cap: Optional[int] = None) -> float:
+    """Max relative-to-RMS error of the layer's output that rounding h to bf16 once (and nothing
+    else) causes on this case, computed with the oracle's step functions."""
+    return rel_rms_err(oracle_h_rounded(c, ref, cap), ref["out"])
 
 
 def output_tolerance(c: Case, ref: dict, cap: Optional[int] = None):
