@@ -5,7 +5,8 @@ multiples of 8), expert count, k, element type, for bf16 a kernel family (every 
 valid bf16 shape), and for some an expert capacity (the assignments past it dropped) or renormalised
 gates. Each runs moe_forward with its outputs and workspace inside guard bands. Forty more layers
 run moe_forward_q on INT4 or INT8 weights against the oracle on its own quantisation of them, and
-forty run with an expert capacity that reroutes the assignments past it. Routing
+forty run with an expert capacity that reroutes the assignments past it. Forty routers are checked
+with their routing statistics, and twenty layers replayed as CUDA graphs against their direct calls. Routing
 indices and counts must equal the oracle's, and the fp32 output must lie within the tolerance rule of
 the fixed parity cases: 1e-4 of the RMS for fp32 layers; 2e-2 for bf16, or a bar raised by the one
 documented rounding of h. A random shape can raise that bar further than the fixed cases do (d_ff = 8
@@ -193,3 +194,90 @@ def test_random_reroute_layer(cfg):
     check_output(c, out.t, ref)
     gone = ~(ref["idx"] >= 0).any(axis=1)
     assert np.all(to_f64(out.t)[gone] == 0.0)
+
+
+def draw_router_cases(n=40, seed=20261206):
+    """Routers with their statistics: every router kernel (tensor-core tiles, the split-K cluster for
+    one deep tile, the CUDA-core kernel for fp32 or other E, the one-launch small batch)."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        dt = BF16 if rng.random() < 0.75 else F32
+        E = int(rng.choice([1, 3, 8, 16, 24, 64, 100, 128, 200, 256, 512, 1024]))
+        cases.append(dict(T=int(rng.choice([1, 2, 5, 8, 9, 64, 128, 129, 700, 2049])),
+                          d=8 * int(rng.integers(1, 129)), E=E, k=int(rng.integers(1, min(E, 8) + 1)), dt=dt,
+                          renorm=bool(rng.random() < 0.3), skew=bool(rng.random() < 0.5)))
+    return cases
+
+
+ROUTER_CASES = draw_router_cases()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cfg", ROUTER_CASES, ids=lambda c: "T{T}_d{d}_E{E}_k{k}_{0}{1}".format(
+    "bf16" if c["dt"] == BF16 else "f32", "_renorm" if c["renorm"] else "", **c))
+def test_random_router_with_stats(cfg):
+    """moe_router_topk_stats: indices bit for bit, gates within 1e-5, the statistics against
+    oracle.routing_stats, and a second call bit-identical (the cross-CTA sums run in a fixed order)."""
+    from test_gpu_parity import check_stats
+    cfg = dict(cfg)
+    renorm, skew = cfg.pop("renorm"), cfg.pop("skew")
+    E = cfg["E"]
+    bias = (np.log(np.arange(1, E + 1, dtype=np.float64) ** -1.2) * 0.5).astype(np.float32) if skew else None
+    c = make_case(F=8, bias=bias, **cfg)
+    ws = guarded_workspace(c)
+    idx = Guarded((c.T, c.k), torch.int32)
+    gate = Guarded((c.T, c.k), torch.float32)
+    stats = Guarded(moe.router_stats_len(E), torch.float32)
+    moe.router_topk_stats(c.x, c.w_r, c.b_r, c.T, c.d, E, c.k, c.dt, idx.t, gate.t, stats.t, ws.t,
+                          renormalise=renorm)
+    st, detail = moe.get_device_status(ws.t)
+    assert st == moe.MOE_OK, (moe.status_string(st), detail)
+    assert idx.intact() and gate.intact() and stats.intact() and ws.intact()
+    logits = oracle.router_logits(c.x64, c.wr64, c.br64)
+    ridx = oracle.topk_select(logits, c.k)
+    assert np.array_equal(idx.t.cpu().numpy(), ridx)
+    want = oracle.gates_renormalised(logits, ridx) if renorm else oracle.gates_of(oracle.softmax(logits), ridx)
+    assert np.max(np.abs(gate.t.cpu().numpy() - want)) < 1e-5
+    check_stats(stats.t, logits, ridx, c.T, E, c.k)
+    again = torch.empty_like(stats.t)
+    moe.router_topk_stats(c.x, c.w_r, c.b_r, c.T, c.d, E, c.k, c.dt, idx.t, gate.t, again, ws.t,
+                          renormalise=renorm)
+    assert torch.equal(again.view(torch.int32), stats.t.view(torch.int32))
+
+
+def draw_graph_cases(n=20, seed=20261207):
+    rng = np.random.default_rng(seed)
+    return [dict(T=int(rng.choice([1, 4, 8, 40, 300])), d=8 * int(rng.integers(1, 49)), F=8 * int(rng.integers(1, 49)),
+                 E=int(rng.choice([2, 8, 16, 64])), k=2, dt=BF16 if rng.random() < 0.8 else F32,
+                 bits=int(rng.choice([0, 0, 4, 8]))) for _ in range(n)]
+
+
+GRAPH_CASES = draw_graph_cases()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("cfg", GRAPH_CASES, ids=lambda c: "T{T}_d{d}_F{F}_E{E}_{0}_bits{bits}".format(
+    "bf16" if c["dt"] == BF16 else "f32", **c))
+def test_random_layer_graph_replay(cfg):
+    """MoELayer.graph(): a replay gives the direct call's output bit for bit, and the next replay picks
+    up new contents of the input buffer."""
+    cfg = dict(cfg)
+    bits = cfg.pop("bits")
+    if bits and (cfg["dt"] != BF16 or cfg["d"] % 64 or cfg["F"] % 64):
+        cfg.update(dt=BF16, d=64 * max(1, cfg["d"] // 64), F=64 * max(1, cfg["F"] // 64))  # quantised: bf16, blocks of 64
+    c = make_case(**cfg)
+    layer = moe.MoELayer(c.w_r, c.w1, c.w2, k=c.k, b_r=c.b_r, weight_bits=bits or None)
+    x_buf = c.x.clone()
+    out_buf = torch.empty_like(c.x)
+    g = layer.graph(x_buf, out_buf)
+    for scale in (1.0, -0.5):
+        x_new = (c.x.float() * scale).to(c.x.dtype)
+        x_buf.copy_(x_new)
+        g.launch()
+        torch.cuda.synchronize()
+        want = layer(x_new)
+        torch.cuda.synchronize()
+        assert torch.equal(out_buf.view(torch.int16 if out_buf.dtype == torch.bfloat16 else torch.int32),
+                           want.view(torch.int16 if want.dtype == torch.bfloat16 else torch.int32))
+    assert layer.device_status()[0] == moe.MOE_OK
