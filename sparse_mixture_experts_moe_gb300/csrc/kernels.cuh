@@ -93,7 +93,7 @@ cudaError_t launch_ffn_simt(const FfnArgs& a, cudaStream_t s);
 // (scale, min) per 64 x 64 block.
 struct QFfnArgs {
   const void* a;          // [rows, K] bf16
-  const void* codes;      // INT8: [E, K/2, N/8] 16-byte tiles; INT4: [E, N/64, K/16, 32, 4] words
+  const void* codes;      // INT8: [E, N/64, K/16, 2, 32, 16] bytes; INT4: [E, N/64, K/16, 32, 4] words
   const float* scale_min; // [E, K/64, N/64] (scale, min) pairs
   const int32_t* offsets; // [E+1]
   const float* row_gate;  // [rows] (stage 2)
