@@ -141,6 +141,14 @@ static_assert(2 * kTmaStages * 8 <= kBarSlotBytes, "the mbarriers fit their slot
 constexpr int kQRows = 8;                   // activation rows per pass: the MMA's N
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+// An 8-byte asynchronous copy global -> shared (n = 0: zero fill, nothing read), and an arrive on an
+// mbarrier once this thread's earlier such copies have landed (counted in the barrier's init count).
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src, int n) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 
 template <int BITS>
 struct QCodes {
@@ -151,6 +159,10 @@ struct QCodes {
   static constexpr int kBoxK = 16 * kBoxSteps;                       // k-rows per box: 512 / 256
   static constexpr float kCentre = (float)(1 << (BITS - 1));
   static constexpr uint32_t kOnePair = BITS == 4 ? 0x3F803F80u : 0x3C003C00u;  // 1.0 in both halves
+  // INT8: the producer warp copies each box's (scale, min) pairs into shared memory beside the box
+  // (an INT8 box passes in about 0.8 us, too short to hide the pairs' global load one box ahead).
+  // INT4: each consumer warp loads its pair one box ahead (measured: the copy made INT4 5% slower).
+  static constexpr bool kScalesInSmem = BITS == 8;
   static_assert(kWarps * kWarpSteps == kBoxSteps, "the warps split a box");
   static_assert(QB % kWarpK == 0, "a warp's range lies in one block");
 };
@@ -198,12 +210,14 @@ __device__ __forceinline__ void stream_q_body(const CUtensorMap* tmC, const __nv
   using C = QCodes<BITS>;
   extern __shared__ uint8_t smem_raw[];
   // ring [nst][16 KB] (128-byte aligned) | full [nst], empty [nst] mbarriers in a 128-byte slot |
-  // sRed [kWarps][kQRows][NS] (warp sums) | sMinW [kWarps][kQRows] (warp block-minimum terms) | sAct [E]
+  // sQ [kTmaStages][kWarps] (each box's (scale, min) per warp) | sRed [kWarps][kQRows][NS] (warp sums) |
+  // sMinW [kWarps][kQRows] (warp block-minimum terms) | sAct [E]
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t ring = (raw + 127u) & ~127u;
   uint8_t* gring = smem_raw + (ring - raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(gring + nst * kTmaBoxBytes);
-  float* sRed = reinterpret_cast<float*>(gring + nst * kTmaBoxBytes + kBarSlotBytes);
+  float2* sQ = reinterpret_cast<float2*>(gring + nst * kTmaBoxBytes + kBarSlotBytes);
+  float* sRed = reinterpret_cast<float*>(sQ + kTmaStages * kWarps);
   float* sMinW = sRed + kWarps * kQRows * NS;
   int* sAct = reinterpret_cast<int*>(sMinW + kWarps * kQRows);
   __shared__ int s_nact, s_abort;
@@ -213,7 +227,7 @@ __device__ __forceinline__ void stream_q_body(const CUtensorMap* tmC, const __nv
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (warp == kWarps && lane == 0) {
     for (int st = 0; st < nst; ++st) {
-      mbar_init(full(st), 1);
+      mbar_init(full(st), C::kScalesInSmem ? 1 + kWarps : 1);  // expect-tx arrive (+ the sQ copies)
       mbar_init(empty(st), kWarps);
     }
     fence_mbar_init();
@@ -239,27 +253,46 @@ __device__ __forceinline__ void stream_q_body(const CUtensorMap* tmC, const __nv
   const int K16 = K / 16;
   const int KB = (K16 + C::kBoxSteps - 1) / C::kBoxSteps;  // boxes per pass; steps past K arrive as zeros
 
+  const int NB = N / QB, KQ = K / QB;
   if (warp == kWarps) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
+    // Lane 0 waits for a free slot and copies the box (TMA). INT8: lanes 0..kWarps-1 also copy the
+    // (scale, min) pair of each consumer warp's range beside it; both land on the slot's full barrier.
+    if (C::kScalesInSmem || lane == 0) {
       int st = 0;
       uint32_t phase = 0, filled = 0, fill_phase = 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const int e = sAct[u / nslab], slab = u % nslab;
+        const float2* sm_e = sm + (size_t)e * KQ * NB + slab;  // block b's (scale, min) at sm_e[b * NB]
         const int passes = (offsets[e + 1] - offsets[e] + kQRows - 1) / kQRows;
         for (int ps = 0; ps < passes; ++ps)
           for (int kb = 0; kb < KB; ++kb) {
-            if (!wait_or_abort(empty(st), phase ^ 1u, timeout_ns, abort_flag, status, 55)) goto producer_out;
-            mbar_arrive_expect_tx(full(st), kTmaBoxBytes);
-            tma_load_3d(ring + st * kTmaBoxBytes, tmC, 0, kb * C::kBoxSteps, e * nslab + slab, full(st));
-            filled |= 1u << st;
-            fill_phase = (fill_phase & ~(1u << st)) | (phase << st);
+            bool free_slot = true;
+            if (lane == 0) free_slot = wait_or_abort(empty(st), phase ^ 1u, timeout_ns, abort_flag, status, 55);
+            if constexpr (C::kScalesInSmem) {
+              if (!__shfl_sync(0xffffffffu, free_slot, 0)) goto producer_out;
+              if (lane < kWarps) {
+                const int kw = kb * C::kBoxK + lane * C::kWarpK;  // past K: zeros
+                cp_async_8(smem_u32(sQ + st * kWarps + lane), kw < K ? sm_e + (size_t)(kw / QB) * NB : sm,
+                           kw < K ? 8 : 0);
+                cp_async_arrive_noinc(full(st));
+              }
+            } else if (!free_slot) {
+              goto producer_out;
+            }
+            if (lane == 0) {
+              mbar_arrive_expect_tx(full(st), kTmaBoxBytes);
+              tma_load_3d(ring + st * kTmaBoxBytes, tmC, 0, kb * C::kBoxSteps, e * nslab + slab, full(st));
+              filled |= 1u << st;
+              fill_phase = (fill_phase & ~(1u << st)) | (phase << st);
+            }
             if (++st == nst) { st = 0; phase ^= 1u; }
           }
       }
     producer_out:
-      for (int q = 0; q < nst; ++q)
-        if (filled & (1u << q)) mbar_wait_bounded(full(q), (fill_phase >> q) & 1u, timeout_ns);
+      if (lane == 0)
+        for (int q = 0; q < nst; ++q)
+          if (filled & (1u << q)) mbar_wait_bounded(full(q), (fill_phase >> q) & 1u, timeout_ns);
     }
     return;
   }
@@ -268,7 +301,6 @@ __device__ __forceinline__ void stream_q_body(const CUtensorMap* tmC, const __nv
   // Every consumer warp runs the same trip counts, so the named barriers always match; after a
   // failed wait (recorded in the status word) the warps skip the arithmetic and run to the end.
   const int g = lane >> 2, t = lane & 3;
-  const int NB = N / QB, KQ = K / QB;
   const uint32_t ones[4] = {C::kOnePair, C::kOnePair, C::kOnePair, C::kOnePair};
   int st = 0;
   uint32_t phase = 0;
@@ -277,7 +309,7 @@ __device__ __forceinline__ void stream_q_body(const CUtensorMap* tmC, const __nv
     const int e = sAct[u / nslab];
     const int slab = u % nslab;
     const int n0 = slab * NS;
-    const float2* sm_e = sm + (size_t)e * KQ * NB + slab;  // block b's (scale, min) at sm_e[b * NB]
+    const float2* sm_e = sm + (size_t)e * KQ * NB + slab;  // block b's (scale, min) at sm_e[b * NB] (INT4)
     const int r_begin = offsets[e], r_end = offsets[e + 1];
     for (int rp = r_begin; rp < r_end; rp += kQRows) {
       const int R = min(kQRows, r_end - rp);
@@ -285,14 +317,14 @@ __device__ __forceinline__ void stream_q_body(const CUtensorMap* tmC, const __nv
       // k-rows within a warp's range start at 16t (INT4) or 8t (INT8).
       const __nv_bfloat16* xrow = nullptr;
       if (g < R) xrow = a + (size_t)(a_rows != nullptr ? a_rows[rp + g] : rp + g) * K + (C::kWarpK / 4) * t;
-      // the B fragments and the (scale, min) pair of this warp's range of the box at k = kb
+      // the B fragments (and, INT4, the (scale, min) pair) of this warp's range of the box at k = kb
       auto fetch = [&](int kb, uint4& x0, uint4& x1, float2& q) {
         const int kw = kb + warp * C::kWarpK;
         x0 = make_uint4(0u, 0u, 0u, 0u);
         x1 = x0;
         q = make_float2(0.f, 0.f);
         if (kw < K) {
-          q = sm_e[(size_t)(kw / QB) * NB];
+          if constexpr (!C::kScalesInSmem) q = sm_e[(size_t)(kw / QB) * NB];
           if (xrow != nullptr) {
             x0 = __ldg(reinterpret_cast<const uint4*>(xrow + kw));
             if constexpr (BITS == 4) x1 = __ldg(reinterpret_cast<const uint4*>(xrow + kw + 8));
@@ -310,11 +342,13 @@ __device__ __forceinline__ void stream_q_body(const CUtensorMap* tmC, const __nv
       fetch(0, nx0, nx1, nq);
       for (int kb = 0; kb < K; kb += C::kBoxK) {
         const uint4 x0 = nx0, x1 = nx1;
-        const float2 q = nq;
+        const float2 pq = nq;
         if (kb + C::kBoxK < K) fetch(kb + C::kBoxK, nx0, nx1, nq);  // in flight during this box
         if (ok) ok = wait_or_abort(full(st), phase, timeout_ns, abort_flag, status, 56);
         ok = __all_sync(0xffffffffu, ok);
         if (ok && kb + warp * C::kWarpK < K) {
+          // this warp's block (scale, min): copied with the box (INT8) or loaded a box ahead (INT4)
+          const float2 q = C::kScalesInSmem ? sQ[st * kWarps + warp] : pq;
           const uint8_t* box = gring + st * kTmaBoxBytes + warp * C::kWarpSteps * C::kStepBytes + lane * 16;
           float blk[4][4], bs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -419,8 +453,8 @@ __global__ void __launch_bounds__(kTmaThreads, 2) ffn_stream_q8_kernel(MOE_STREA
 #undef MOE_STREAM_Q_PARAMS
 
 size_t q_smem_bytes(int nst, int E) {
-  return 128 + (size_t)nst * kTmaBoxBytes + kBarSlotBytes + (size_t)kWarps * kQRows * (NS + 1) * sizeof(float) +
-         (size_t)E * 4;
+  return 128 + (size_t)nst * kTmaBoxBytes + kBarSlotBytes + (size_t)kTmaStages * kWarps * sizeof(float2) +
+         (size_t)kWarps * kQRows * (NS + 1) * sizeof(float) + (size_t)E * 4;
 }
 
 constexpr size_t kSmPerSmBytes = 228 * 1024;  // shared memory per SM, of which 1 KB per resident CTA is reserved
