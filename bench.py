@@ -295,9 +295,20 @@ def oracle_sample(w, x, w_r, b_r, w1, w2, target_s, max_tokens=None, repeat=True
 
 # ----------------------------------------------------------------------------- our arm
 
-def dominant_roofline(w, kern_ms, touched, fpath, qbits, peaks, peak_src):
+def power_limited(clk):
+    """Whether a clock record saw the power limit: sw_power_cap active, or the median SM clock under
+    93% of its maximum."""
+    if not clk or not clk.get("samples") or clk.get("window") != "timed region":
+        return False  # no sample of the loop itself
+    sm, top = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    return "sw_power_cap" in clk.get("reasons", []) or (sm is not None and top and sm < 0.93 * top)
+
+
+def dominant_roofline(w, kern_ms, touched, fpath, qbits, peaks, peak_src, kern_clk=None):
     """Roofline of the slower expert GEMM: algorithmic bytes (weight streaming) or FLOPs (tensor-core
-    GEMMs) per launch over its measured launch time, against the measured peak."""
+    GEMMs) per launch over its measured launch time, against the measured peak. A tensor-core GEMM
+    whose timing loop ran at the power limit is measured against the bf16 matmul rate sustained at
+    that limit; one that kept its clocks, against the burst rate."""
     import sparse_mixture_experts_moe_gb300 as moe
     T, d, F, E, k, dt = w.T, w.d, w.F, w.E, w.k, w.dtype
     A = T * k
@@ -336,7 +347,14 @@ def dominant_roofline(w, kern_ms, touched, fpath, qbits, peaks, peak_src):
     else:
         alg_flops = 2.0 * A * d * F
         achieved = alg_flops / (kern_ms[dom] / 1e3) / 1e12
-        peak = peaks["bf16_tflops"]
+        clk = (kern_clk or {}).get(dom)
+        sustained = power_limited(clk)
+        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        if sustained:
+            why = (f"bf16_tflops_sustained (the launch's timing loop ran at the power limit: "
+                   f"SM median {clk.get('sm_mhz')} MHz, {', '.join(clk.get('reasons', [])) or 'no reason'})")
+        else:
+            why = "bf16_tflops (burst: the launch's timing loop kept its clocks)"
         kname = {moe.PATH_TENSOR_PAIR: "ffn_tc2_kernel", moe.PATH_TENSOR_T: "ffn_tct_kernel"}.get(run_path[dom],
                                                                                                "ffn_tc_kernel")
         # attainable: min(peak, arithmetic intensity x HBM bandwidth), the intensity over the bytes the
@@ -350,9 +368,10 @@ def dominant_roofline(w, kern_ms, touched, fpath, qbits, peaks, peak_src):
                 "traffic": stored_traffic(f"{kname}<{1 if dom == 'expert_up' else 2}>", w.name,
                                           TCT_SOURCES if kname == "ffn_tct_kernel" else TC_SOURCES),
                 "alg_flops_per_launch": alg_flops, "ms_per_launch": kern_ms[dom],
-                "peak_source": f"{peak_src} bf16_tflops (burst: the kernel runs in a short step)",
-                # context: the measured bf16 matmul rate held for seconds at the power limit
-                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
+                "peak_source": f"{peak_src} {why}",
+                "frac_of_burst": achieved / peaks["bf16_tflops"],
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "timing_loop_clocks": clk}
     return roof
 
 
@@ -488,16 +507,18 @@ def run_ours(args, w, rank, world, device):
                                                x_perm, ws)),
              ("expert_up", up_call), ("expert_down", down_call),
              ("combine", lambda: moe.combine(y_perm, row_of, T, d, k, dt, out))]
-    kern_ms = {}
+    kern_ms, kern_wall = {}, {}
     for name, fn in calls:
         fn()  # warm-up, and the inputs of the next kernel
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        tw0 = time.time()
         ev0.record(stream)
         for _ in range(reps):
             fn()
         ev1.record(stream)
         torch.cuda.synchronize()
+        kern_wall[name] = (tw0, time.time())
         kern_ms[name] = ev0.elapsed_time(ev1) / reps
     counts_h = counts.cpu().numpy()
     touched = int((counts_h > 0).sum())
@@ -562,10 +583,12 @@ def run_ours(args, w, rank, world, device):
         raise RuntimeError(f"device status after timing: {moe.status_string(st)} ({detail})")
     clocks.stop()
     clk = clocks.summary(t_wall0, t_wall1)
+    # the clocks of each GEMM's own timing loop: they choose between the burst and sustained peaks
+    kern_clk = {n: clocks.summary(*kern_wall[n]) for n in ("expert_up", "expert_down")}
 
     # --- roofline of the dominant kernel
     peaks, peak_src = load_peaks()
-    roof = dominant_roofline(w, kern_ms, touched, fpath, qbits, peaks, peak_src)
+    roof = dominant_roofline(w, kern_ms, touched, fpath, qbits, peaks, peak_src, kern_clk)
 
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,

@@ -1,5 +1,6 @@
 """bench.py's host-side bookkeeping, without a GPU: the stored ncu traffic is reported only for the
-kernel sources it was captured from, and the committed traffic table is well formed."""
+kernel sources it was captured from, the committed traffic table is well formed, and a tensor-core
+GEMM is measured against the burst or the sustained bf16 peak by the clocks of its own timing loop."""
 import json
 import os
 import sys
@@ -46,3 +47,37 @@ def test_sources_sha_depends_on_content(tmp_path):
     b.write_text("y")
     assert bench.sources_sha([str(a)]) != bench.sources_sha([str(b)])
     assert bench.sources_sha([str(a)]) == bench.sources_sha([str(a)])
+
+
+def clock_record(sm, reasons, window="timed region", samples=3):
+    return {"sm_mhz": sm, "sm_max_mhz": 2070.0, "reasons": reasons, "samples": samples, "window": window}
+
+
+def test_power_limited_reads_the_loops_own_samples():
+    assert bench.power_limited(clock_record(1695.0, ["sw_power_cap"]))
+    assert bench.power_limited(clock_record(1800.0, []))  # well below the maximum with no reason given
+    assert not bench.power_limited(clock_record(2070.0, []))
+    assert not bench.power_limited(clock_record(1990.0, []))
+    assert not bench.power_limited(clock_record(1695.0, ["sw_power_cap"], samples=0))
+    assert not bench.power_limited(clock_record(1695.0, ["sw_power_cap"], window="whole GPU phase"))
+    assert not bench.power_limited(None)
+
+
+def test_tensor_roofline_peak_follows_the_timing_loop_clocks():
+    import sparse_mixture_experts_moe_gb300 as moe
+    from inputgen import workloads
+    w = workloads.get("skew_e128")
+    peaks = {"hbm_gbs": 6784.5, "bf16_tflops": 1927.9, "bf16_tflops_sustained": 1711.9}
+    kern_ms = {"expert_up": 1.99, "expert_down": 2.03}
+    flops = 2.0 * w.T * w.k * w.d * w.F
+    capped = {n: clock_record(1695.0, ["sw_power_cap"]) for n in kern_ms}
+    free = {n: clock_record(2070.0, []) for n in kern_ms}
+    for clk, peak in ((capped, 1711.9), (free, 1927.9), (None, 1927.9)):
+        r = bench.dominant_roofline(w, kern_ms, 128, moe.PATH_TENSOR_T, 0, peaks, "measured", clk)
+        assert r["kernel"] == "ffn_tct_kernel (expert_down)" and r["bound"] == "tensor"
+        assert r["peak"] == peak
+        achieved = flops / 2.03e-3 / 1e12
+        assert abs(r["achieved"] - achieved) < 1e-9 * achieved
+        assert abs(r["frac"] - achieved / peak) < 1e-12
+        assert abs(r["frac_of_burst"] - achieved / 1927.9) < 1e-12
+        assert abs(r["frac_of_sustained"] - achieved / 1711.9) < 1e-12
