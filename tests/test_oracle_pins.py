@@ -637,6 +637,26 @@ def _mut_reroute(change):
     return fn
 
 
+def _mut_rows_down_drops_gate(h, offsets, row_gate, w2, rows=None):
+    return _ORIG_ROWS_DOWN(h, offsets, np.ones_like(np.asarray(row_gate, np.float64)), w2, rows)
+
+
+def _mut_rows_up_next_expert(x_perm, offsets, w1, rows=None):
+    # each row takes the weights of the expert after its own (an off-by-one in the row -> expert map)
+    E = len(w1)
+    shifted = {e: w1[(e + 1) % E] for e in range(E)}
+    return _ORIG_ROWS_UP(x_perm, offsets, shifted, rows)
+
+
+def _mut_dispatch_inclusive_offsets(idx, E, gate=None, cap=None):
+    res = dict(_ORIG_DISPATCH(idx, E, gate, cap))
+    counts = np.asarray(res["counts"])
+    res["offsets"] = np.concatenate([np.cumsum(counts), [int(np.sum(counts))]])
+    return res
+
+
+_ORIG_ROWS_DOWN = om.expert_rows_down
+_ORIG_ROWS_UP = om.expert_rows_up
 _ORIG_DISPATCH = om.dispatch
 _ORIG_TOPK = om.topk_select
 _ORIG_KEPT = om.kept_assignments
@@ -669,6 +689,9 @@ MUTANTS = {
     "dequant_drops_min": ("dequantize_blocks", _mut_dequant_drops_min),
     "quant_floor": ("quantize_blocks", _mut_quant_floor),
     "quant_2^bits_levels": ("quantize_blocks", _mut_quant_levels),
+    "rows_down_drops_gate": ("expert_rows_down", _mut_rows_down_drops_gate),
+    "rows_up_next_expert": ("expert_rows_up", _mut_rows_up_next_expert),
+    "dispatch_inclusive_offsets": ("dispatch", _mut_dispatch_inclusive_offsets),
 }
 
 
