@@ -489,39 +489,58 @@ def run_ours(args, w, rank, world, device):
     # the host's per-call work (argument marshalling, tensor maps) overlaps the previous launch and
     # only device time is measured; repeated calls on the same inputs give the same outputs.
     reps = max(args.steps, 10)
+    moe.router_topk(x, w_r, b_r, T, d, E, k, dt, idx, gate)
+    moe.dispatch(x, idx, gate, T, d, E, k, dt, counts, offsets, perm, row_of, row_gate, x_perm, ws)
+    counts_h = counts.cpu().numpy()
+    touched = int((counts_h > 0).sum())
+    # An expert GEMM whose touched weights fit in twice the L2 would find part of them there when
+    # repeated on the same experts. Launch i then gives the touched experts' rows, in order, to the
+    # experts i*s .. i*s + s - 1 (mod E; s = experts touched), so that neighbouring launches read
+    # weights that none near them has read. The shape of the work is unchanged.
+    w_bytes = touched * d * F * (qbits / 8 if qbits else (2 if dt == 1 else 4))
+    routings = [offsets]
+    if w_bytes < 2 * L2_BYTES and E >= 3 * touched > 0:
+        held = counts_h[counts_h > 0]
+        for i in range(1, min(reps, E // touched)):
+            c = np.zeros(E, np.int64)
+            c[(i * touched + np.arange(touched)) % E] = held
+            routings.append(torch.from_numpy(np.concatenate([[0], np.cumsum(c)]).astype(np.int32)).to(device))
+    kernel_timing = ("back-to-back launches; the expert GEMMs' rows moved to other experts at every launch "
+                     f"({len(routings)} routings) because the touched weights fit in twice the L2"
+                     if len(routings) > 1 else "back-to-back launches on the step's routing")
 
-    def up_call():
+    def up_call(i=0):
+        offs = routings[i % len(routings)]
         if qbits:
-            moe.expert_up_q(x_perm, q1[0], q1[1], offsets, T, d, F, E, k, qbits, h)
+            moe.expert_up_q(x_perm, q1[0], q1[1], offs, T, d, F, E, k, qbits, h)
         else:
-            moe.expert_up(x_perm, w1, offsets, T, d, F, E, k, dt, h, ws, path=fpath)
+            moe.expert_up(x_perm, w1, offs, T, d, F, E, k, dt, h, ws, path=fpath)
 
-    def down_call():
+    def down_call(i=0):
+        offs = routings[i % len(routings)]
         if qbits:
-            moe.expert_down_q(h, q2[0], q2[1], offsets, row_gate, T, d, F, E, k, qbits, y_perm)
+            moe.expert_down_q(h, q2[0], q2[1], offs, row_gate, T, d, F, E, k, qbits, y_perm)
         else:
-            moe.expert_down(h, w2, offsets, row_gate, T, d, F, E, k, dt, y_perm, ws, path=fpath)
+            moe.expert_down(h, w2, offs, row_gate, T, d, F, E, k, dt, y_perm, ws, path=fpath)
 
-    calls = [("router_topk", lambda: moe.router_topk(x, w_r, b_r, T, d, E, k, dt, idx, gate)),
-             ("dispatch", lambda: moe.dispatch(x, idx, gate, T, d, E, k, dt, counts, offsets, perm, row_of, row_gate,
-                                               x_perm, ws)),
+    calls = [("router_topk", lambda i=0: moe.router_topk(x, w_r, b_r, T, d, E, k, dt, idx, gate)),
+             ("dispatch", lambda i=0: moe.dispatch(x, idx, gate, T, d, E, k, dt, counts, offsets, perm, row_of,
+                                                   row_gate, x_perm, ws)),
              ("expert_up", up_call), ("expert_down", down_call),
-             ("combine", lambda: moe.combine(y_perm, row_of, T, d, k, dt, out))]
+             ("combine", lambda i=0: moe.combine(y_perm, row_of, T, d, k, dt, out))]
     kern_ms, kern_wall = {}, {}
     for name, fn in calls:
-        fn()  # warm-up, and the inputs of the next kernel
+        fn()  # warm-up, and the inputs of the next kernel (on the step's own routing)
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         tw0 = time.time()
         ev0.record(stream)
-        for _ in range(reps):
-            fn()
+        for i in range(reps):
+            fn(i)
         ev1.record(stream)
         torch.cuda.synchronize()
         kern_wall[name] = (tw0, time.time())
         kern_ms[name] = ev0.elapsed_time(ev1) / reps
-    counts_h = counts.cpu().numpy()
-    touched = int((counts_h > 0).sum())
 
     # --- e2e: public layer object, pinned host tokens in, output back to the host, every step.
     # Double-buffered as a serving loop runs it: step i's input copy (its own stream) overlaps step
@@ -605,6 +624,7 @@ def run_ours(args, w, rank, world, device):
                     "how": "each step alone after writing a 512 MB buffer on its stream, median of 20"},
         "roofline": roof,
         "kernel_ms": kern_ms,
+        "kernel_timing": kernel_timing,
         "experts_touched": touched,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": x.numel() * x.element_size(),
                 "d2h_bytes_per_step": out.numel() * out.element_size(),

@@ -17,6 +17,13 @@ int device_sm_count() {
   return sms;
 }
 
+size_t device_l2_bytes() {
+  int dev = 0, l2 = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return (size_t)126 << 20;
+  if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0) return (size_t)126 << 20;
+  return (size_t)l2;
+}
+
 namespace {
 
 constexpr int kStreamPathMaxRows = 256;

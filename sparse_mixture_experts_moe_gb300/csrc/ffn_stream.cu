@@ -69,13 +69,26 @@ constexpr int kBarSlotBytes = 128;               // the ring's mbarriers: 2 x kT
 static_assert(2 * kTmaStages * 8 <= kBarSlotBytes, "the mbarriers fit their slot");
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+// The weights' copies at L2 evict-first priority (see stream_evict_first).
+__device__ __forceinline__ uint64_t policy_evict_first_s() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_3d_first(uint32_t dst, const void* tmap, int c0, int c1, int c2,
+                                                  uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      ::"r"(dst), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(pol) : "memory");
+}
 
 template <int STAGE, typename OutT, int RMAX>
 __global__ void __launch_bounds__(kTmaThreads, 2)
 ffn_stream_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __nv_bfloat16* __restrict__ a,
                       const int32_t* __restrict__ a_rows, const int32_t* __restrict__ offsets,
                       const float* __restrict__ row_gate, int K, int N, int E, int nst, OutT* __restrict__ out,
-                      int* status, uint64_t timeout_ns) {
+                      int* status, uint64_t timeout_ns, int evict_first) {
   constexpr int KC = kTmaActFloats / RMAX;  // a multiple of kTmaRows
   extern __shared__ uint8_t smem_raw[];
   // ring [nst][kTmaRows][NS] bf16 (128-byte aligned) | full [nst], empty [nst] mbarriers in a
@@ -131,7 +144,10 @@ ffn_stream_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __nv_bfloat
           for (int kb = 0; kb < KB; ++kb) {
             if (!wait_or_abort(empty(st), phase ^ 1u, timeout_ns, abort_flag, status, 51)) goto producer_out;
             mbar_arrive_expect_tx(full(st), kTmaBoxBytes);
-            tma_load_3d(ring + st * kTmaBoxBytes, &tmW, n0, kb * kTmaRows, e, full(st));
+            if (evict_first)
+              tma_load_3d_first(ring + st * kTmaBoxBytes, &tmW, n0, kb * kTmaRows, e, full(st), policy_evict_first_s());
+            else
+              tma_load_3d(ring + st * kTmaBoxBytes, &tmW, n0, kb * kTmaRows, e, full(st));
             filled |= 1u << st;
             fill_phase = (fill_phase & ~(1u << st)) | (phase << st);
             if (++st == nst) { st = 0; phase ^= 1u; }
@@ -261,7 +277,8 @@ cudaError_t launch_tma(const FfnArgs& p, EncodeTiledFn enc, cudaStream_t s) {
   long long grid = 2LL * device_sm_count();  // persistent: the resident CTAs loop over the units
   if (grid > max_units) grid = max_units;
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, s, tmW, (const __nv_bfloat16*)p.a, p.a_rows,
-                    p.offsets, p.row_gate, p.K, p.N, p.E, nst, (OutT*)p.out, p.status, p.timeout_ns);
+                    p.offsets, p.row_gate, p.K, p.N, p.E, nst, (OutT*)p.out, p.status, p.timeout_ns,
+                    (int)stream_evict_first(p.rows, p.E, p.K, p.N, 16));
 }
 
 }  // namespace

@@ -143,5 +143,12 @@ bool encode_tmap_plain(EncodeTiledFn enc, CUtensorMap* m, CUtensorMapDataType ty
                        const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box);
 
 int device_sm_count();
+// The current device's L2 size in bytes; a streaming GEMM whose touched weights fit in twice that
+// copies them at L2 evict-first priority, so that what the step reads again stays in L2.
+size_t device_l2_bytes();
+inline bool stream_evict_first(long long rows, int E, long long K, long long N, int bits) {
+  const double touched = (double)(rows < E ? rows : E) * (double)K * (double)N * bits / 8.0;
+  return touched < 2.0 * (double)device_l2_bytes();
+}
 
 }  // namespace moe

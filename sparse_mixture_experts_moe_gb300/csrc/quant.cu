@@ -149,6 +149,19 @@ __device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src, int n)
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
+// The codes' copies at L2 evict-first priority (see stream_evict_first).
+__device__ __forceinline__ uint64_t policy_evict_first_q() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_3d_first(uint32_t dst, const void* tmap, int c0, int c1, int c2,
+                                                  uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+      ::"r"(dst), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(pol) : "memory");
+}
 
 template <int BITS>
 struct QCodes {
@@ -206,7 +219,7 @@ __device__ __forceinline__ void stream_q_body(const CUtensorMap* tmC, const __nv
                                               const int32_t* __restrict__ a_rows, const float2* __restrict__ sm,
                                               const int32_t* __restrict__ offsets, const float* __restrict__ row_gate,
                                               int K, int N, int E, int nst, OutT* __restrict__ out, int* status,
-                                              uint64_t timeout_ns) {
+                                              uint64_t timeout_ns, int evict_first) {
   using C = QCodes<BITS>;
   extern __shared__ uint8_t smem_raw[];
   // ring [nst][16 KB] (128-byte aligned) | full [nst], empty [nst] mbarriers in a 128-byte slot |
@@ -282,7 +295,11 @@ __device__ __forceinline__ void stream_q_body(const CUtensorMap* tmC, const __nv
             }
             if (lane == 0) {
               mbar_arrive_expect_tx(full(st), kTmaBoxBytes);
-              tma_load_3d(ring + st * kTmaBoxBytes, tmC, 0, kb * C::kBoxSteps, e * nslab + slab, full(st));
+              if (evict_first)
+                tma_load_3d_first(ring + st * kTmaBoxBytes, tmC, 0, kb * C::kBoxSteps, e * nslab + slab, full(st),
+                                  policy_evict_first_q());
+              else
+                tma_load_3d(ring + st * kTmaBoxBytes, tmC, 0, kb * C::kBoxSteps, e * nslab + slab, full(st));
               filled |= 1u << st;
               fill_phase = (fill_phase & ~(1u << st)) | (phase << st);
             }
@@ -441,14 +458,16 @@ __device__ __forceinline__ void stream_q_body(const CUtensorMap* tmC, const __nv
   const __grid_constant__ CUtensorMap tmC, const __nv_bfloat16* __restrict__ a,                               \
       const int32_t* __restrict__ a_rows, const float2* __restrict__ sm, const int32_t* __restrict__ offsets, \
       const float* __restrict__ row_gate, int K, int N, int E, int nst, OutT* __restrict__ out, int* status,  \
-      uint64_t timeout_ns
+      uint64_t timeout_ns, int evict_first
 template <int STAGE, typename OutT>
 __global__ void __launch_bounds__(kTmaThreads, 2) ffn_stream_q4_kernel(MOE_STREAM_Q_PARAMS) {
-  stream_q_body<4, STAGE, OutT>(&tmC, a, a_rows, sm, offsets, row_gate, K, N, E, nst, out, status, timeout_ns);
+  stream_q_body<4, STAGE, OutT>(&tmC, a, a_rows, sm, offsets, row_gate, K, N, E, nst, out, status, timeout_ns,
+                                evict_first);
 }
 template <int STAGE, typename OutT>
 __global__ void __launch_bounds__(kTmaThreads, 2) ffn_stream_q8_kernel(MOE_STREAM_Q_PARAMS) {
-  stream_q_body<8, STAGE, OutT>(&tmC, a, a_rows, sm, offsets, row_gate, K, N, E, nst, out, status, timeout_ns);
+  stream_q_body<8, STAGE, OutT>(&tmC, a, a_rows, sm, offsets, row_gate, K, N, E, nst, out, status, timeout_ns,
+                                evict_first);
 }
 #undef MOE_STREAM_Q_PARAMS
 
@@ -485,7 +504,7 @@ cudaError_t launch_q(const QFfnArgs& p, EncodeTiledFn enc, cudaStream_t s) {
   if (grid > max_units) grid = max_units;
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kTmaThreads), smem, s, tmC, (const __nv_bfloat16*)p.a,
                     p.a_rows, (const float2*)p.scale_min, p.offsets, p.row_gate, p.K, p.N, p.E, nst, (OutT*)p.out,
-                    p.status, p.timeout_ns);
+                    p.status, p.timeout_ns, (int)stream_evict_first(p.rows, p.E, p.K, p.N, BITS));
 }
 
 }  // namespace
