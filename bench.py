@@ -295,6 +295,25 @@ def oracle_sample(w, x, w_r, b_r, w1, w2, target_s, max_tokens=None, repeat=True
 
 # ----------------------------------------------------------------------------- our arm
 
+def moved_routings(counts, reps):
+    """Offsets [E+1] (int32) of routings 1, 2, ... that give the touched experts' rows, in expert order,
+    to the experts i*s .. i*s + s - 1 (mod E), s = experts touched: the same rows and work per expert
+    as the step's routing, on weights no neighbouring routing touches. Empty where E < 3 s."""
+    import numpy as np
+    counts = np.asarray(counts)
+    E = counts.shape[0]
+    held = counts[counts > 0]
+    s = held.shape[0]
+    out = []
+    if s == 0 or E < 3 * s:
+        return out
+    for i in range(1, min(reps, E // s)):
+        c = np.zeros(E, np.int64)
+        c[(i * s + np.arange(s)) % E] = held
+        out.append(np.concatenate([[0], np.cumsum(c)]).astype(np.int32))
+    return out
+
+
 def power_limited(clk):
     """Whether a clock record saw the power limit: sw_power_cap active, or the median SM clock under
     93% of its maximum."""
@@ -499,12 +518,8 @@ def run_ours(args, w, rank, world, device):
     # weights that none near them has read. The shape of the work is unchanged.
     w_bytes = touched * d * F * (qbits / 8 if qbits else (2 if dt == 1 else 4))
     routings = [offsets]
-    if w_bytes < 2 * L2_BYTES and E >= 3 * touched > 0:
-        held = counts_h[counts_h > 0]
-        for i in range(1, min(reps, E // touched)):
-            c = np.zeros(E, np.int64)
-            c[(i * touched + np.arange(touched)) % E] = held
-            routings.append(torch.from_numpy(np.concatenate([[0], np.cumsum(c)]).astype(np.int32)).to(device))
+    if w_bytes < 2 * L2_BYTES:
+        routings += [torch.from_numpy(o).to(device) for o in moved_routings(counts_h, reps)]
     kernel_timing = ("back-to-back launches; the expert GEMMs' rows moved to other experts at every launch "
                      f"({len(routings)} routings) because the touched weights fit in twice the L2"
                      if len(routings) > 1 else "back-to-back launches on the step's routing")

@@ -81,3 +81,25 @@ def test_tensor_roofline_peak_follows_the_timing_loop_clocks():
         assert abs(r["frac"] - achieved / peak) < 1e-12
         assert abs(r["frac_of_burst"] - achieved / 1927.9) < 1e-12
         assert abs(r["frac_of_sustained"] - achieved / 1711.9) < 1e-12
+
+
+def test_moved_routings_keep_the_work_on_other_experts():
+    import numpy as np
+    E = 128
+    counts = np.zeros(E, np.int64)
+    counts[[17, 90]] = 1                      # one token, top-2
+    rs = bench.moved_routings(counts, reps=200)
+    assert len(rs) == E // 2 - 1
+    prev = {17, 90}
+    for o in rs:
+        assert o.dtype == np.int32 and o.shape == (E + 1,) and o[0] == 0 and o[-1] == counts.sum()
+        c = np.diff(o)
+        assert (c >= 0).all() and sorted(c[c > 0].tolist()) == [1, 1]   # the same rows per expert
+        now = set(np.nonzero(c)[0].tolist())
+        assert not (now & prev)               # neighbouring launches read different experts
+        prev = now
+    counts = np.zeros(E, np.int64)
+    counts[[3, 4, 9]] = [5, 2, 7]             # ragged rows move with their order kept
+    o = bench.moved_routings(counts, reps=4)[0]
+    assert np.diff(o)[3:6].tolist() == [5, 2, 7]
+    assert bench.moved_routings(np.ones(8, np.int64), reps=10) == []   # every expert touched: nothing to move to
