@@ -277,10 +277,6 @@ __device__ __forceinline__ void stream_q_body(const CUtensorMap* tmC, const __nv
       for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const int e = sAct[u / nslab], slab = u % nslab;
         const float2* sm_e = sm + (size_t)e * KQ * NB + slab;  // block b's (scale, min) at sm_e[b * NB]
-        // INT8: the unit's (scale, min) column into L2 ahead of its copies (2% at one token; with
-        // lane 0 alone issuing them, INT4 lost 4%)
-        if constexpr (C::kScalesInSmem)
-          for (int b = lane; b < KQ; b += 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(sm_e + (size_t)b * NB));
         const int passes = (offsets[e + 1] - offsets[e] + kQRows - 1) / kQRows;
         for (int ps = 0; ps < passes; ++ps)
           for (int kb = 0; kb < KB; ++kb) {
