@@ -103,3 +103,25 @@ def test_moved_routings_keep_the_work_on_other_experts():
     o = bench.moved_routings(counts, reps=4)[0]
     assert np.diff(o)[3:6].tolist() == [5, 2, 7]
     assert bench.moved_routings(np.ones(8, np.int64), reps=10) == []   # every expert touched: nothing to move to
+
+
+def test_streaming_roofline_counts_the_touched_bytes():
+    """Quantised and bf16 weight streaming: bytes per launch = the touched experts' codes (or weights)
+    and block scales, plus the rows read and written, over the launch time."""
+    import sparse_mixture_experts_moe_gb300 as moe
+    from inputgen import workloads
+    w = workloads.get("decode_t1")                     # T=1, d = d_ff = 8192, E=128, top-2
+    peaks = {"hbm_gbs": 6784.5, "bf16_tflops": 1927.9, "bf16_tflops_sustained": 1711.9}
+    kern_ms = {"expert_up": 0.0206, "expert_down": 0.0205}
+    A, K, N = w.T * w.k, w.d, w.F
+    for bits in (4, 8):
+        r = bench.dominant_roofline(w, kern_ms, 2, moe.PATH_AUTO, bits, peaks, "measured")
+        assert r["bound"] == "hbm" and r["kernel"] == f"ffn_stream_q{bits}_kernel (expert_up)"
+        codes = K * N * bits // 8 + (K // 64) * (N // 64) * 8
+        want = 2 * codes + A * K * 2 + A * N * 2    # two experts; x rows in, h rows out (bf16)
+        assert r["alg_bytes_per_launch"] == want
+        assert abs(r["achieved"] - want / 0.0206e-3 / 1e9) < 1e-6 * r["achieved"]
+        assert abs(r["frac"] - r["achieved"] / 6784.5) < 1e-12
+    r = bench.dominant_roofline(w, kern_ms, 2, moe.PATH_AUTO, 0, peaks, "measured")
+    assert r["kernel"] == "ffn_stream_tma_kernel (expert_up)"
+    assert r["alg_bytes_per_launch"] == 2 * K * N * 2 + A * K * 2 + A * N * 2
